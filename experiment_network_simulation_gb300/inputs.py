@@ -1,0 +1,483 @@
+"""Seeded synthetic inputs: topologies, workload DAGs and experiment batches.
+
+This module only builds the integer tables that describe a batch of
+experiments (who is wired to whom, which DAG node waits on which, which ranks
+take part in which collective, and the per-experiment parameters).  It holds
+none of the simulation's arithmetic: no routing, no collective decomposition,
+no timing, no hashing.  Both the CUDA library and the CPU oracle consume the
+flat arrays that :meth:`Batch.pack` returns.
+
+Units follow the Multiverse page (section 5, "simulation step"): one tick is
+one packet serialisation time on the experiment's base link rate, so a
+400 Gbps link carrying 4 KiB packets has sigma = 1 tick of 81,920 ps, and a
+propagation delay is rounded half-up to whole ticks.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# DAG node kinds (Multiverse, section 3.2: Task entities are compute or comm).
+COMPUTE, INTRA, NET = 0, 1, 2
+# Collective kinds.  AR/RS/AG follow NCCL's ring (Multiverse section 5,
+# AutoCCL section 2.3); RELAY is AlpaComm's pipelined broadcast (section 3.1);
+# P2P is a pipeline-parallel send; A2A is the MoE dispatch/combine exchange.
+AR, RS, AG, RELAY, P2P, A2A = 0, 1, 2, 3, 4, 5
+KIND_NAMES = {AR: "allreduce", RS: "reducescatter", AG: "allgather",
+              RELAY: "relay", P2P: "p2p", A2A: "alltoall"}
+# Collective algorithm (AutoCCL's A parameter).
+RING, TREE = 0, 1
+
+KIB = 1024
+MIB = 1024 * 1024
+FORMAT_VERSION = 1
+
+
+def tick_ps(pkt_bytes: int, gbps: int) -> int:
+    """Serialisation time of one packet at ``gbps``, in picoseconds, rounded up."""
+    return -(-pkt_bytes * 8 * 1000 // gbps)
+
+
+def delay_ticks(prop_ps: int, tick: int) -> int:
+    """Propagation delay in whole ticks, rounded half-up."""
+    return (2 * prop_ps + tick) // (2 * tick)
+
+
+# --------------------------------------------------------------------------
+# Topology
+# --------------------------------------------------------------------------
+class Topology:
+    """Hosts (one NIC each) and switches joined by bidirectional links.
+
+    Switch ports are numbered in the order links are attached.  Each switch
+    has a tier level (edge = 1, aggregation = 2, core = 3); hosts are level 0.
+    """
+
+    def __init__(self, name: str = ""):
+        self.name = name
+        self.n_hosts = 0
+        self.sw_level: list[int] = []
+        self.sw_ports: list[list[tuple]] = []   # per switch: [(peer, sigma, delta)]
+        self.host_att: list[tuple | None] = []  # per host: (switch, port, sigma, delta)
+
+    def add_switch(self, level: int) -> int:
+        self.sw_level.append(level)
+        self.sw_ports.append([])
+        return len(self.sw_level) - 1
+
+    def add_hosts(self, n: int) -> list[int]:
+        ids = list(range(self.n_hosts, self.n_hosts + n))
+        self.n_hosts += n
+        self.host_att.extend([None] * n)
+        return ids
+
+    def attach_host(self, h: int, s: int, sigma: int = 1, delta: int = 0,
+                    sigma_down: int | None = None, delta_down: int | None = None):
+        """Link host ``h`` to a new port of switch ``s``.  ``sigma``/``delta``
+        describe the NIC uplink; the ``*_down`` values the switch-to-host link."""
+        assert self.host_att[h] is None
+        p = len(self.sw_ports[s])
+        self.sw_ports[s].append((("h", h),
+                                 sigma if sigma_down is None else sigma_down,
+                                 delta if delta_down is None else delta_down))
+        self.host_att[h] = (s, p, sigma, delta)
+
+    def link(self, a: int, b: int, sigma: int = 1, delta: int = 0):
+        pa, pb = len(self.sw_ports[a]), len(self.sw_ports[b])
+        self.sw_ports[a].append((("s", b, pb), sigma, delta))
+        self.sw_ports[b].append((("s", a, pa), sigma, delta))
+
+    @property
+    def n_switches(self) -> int:
+        return len(self.sw_level)
+
+    def arrays(self) -> dict:
+        base = np.zeros(self.n_switches + 1, dtype=np.int64)
+        for s, ports in enumerate(self.sw_ports):
+            base[s + 1] = base[s] + len(ports)
+        nq = int(base[-1])
+        peer = np.zeros(nq, np.int32)
+        sig = np.zeros(nq, np.uint32)
+        dl = np.zeros(nq, np.uint32)
+        for s, ports in enumerate(self.sw_ports):
+            for p, (pe, sg, d) in enumerate(ports):
+                q = base[s] + p
+                if pe[0] == "h":
+                    peer[q] = -(pe[1] + 1)
+                else:
+                    peer[q] = base[pe[1]] + pe[2]
+                sig[q], dl[q] = sg, d
+        hp = np.zeros(self.n_hosts, np.uint32)
+        hs = np.zeros(self.n_hosts, np.uint32)
+        hd = np.zeros(self.n_hosts, np.uint32)
+        for h, att in enumerate(self.host_att):
+            assert att is not None, f"host {h} not attached"
+            s, p, sg, d = att
+            hp[h], hs[h], hd[h] = base[s] + p, sg, d
+        return dict(sw_nports=np.diff(base).astype(np.uint32),
+                    sw_level=np.array(self.sw_level, np.uint32),
+                    port_peer=peer, port_sigma=sig, port_delta=dl,
+                    host_port=hp, host_sigma=hs, host_delta=hd)
+
+
+def single_switch(n_hosts: int, sigma: int = 1, delta: int = 0) -> Topology:
+    t = Topology(f"switch{n_hosts}")
+    s = t.add_switch(1)
+    for h in t.add_hosts(n_hosts):
+        t.attach_host(h, s, sigma, delta)
+    return t
+
+
+def leaf_spine(n_leaves: int, n_spines: int, hosts_per_leaf: int, delta: int = 0,
+               links_per_pair: int = 1, sigma: int = 1) -> Topology:
+    """Two-tier Clos: every leaf wired to every spine ``links_per_pair`` times."""
+    t = Topology(f"leafspine{n_leaves}x{n_spines}")
+    leaves = [t.add_switch(1) for _ in range(n_leaves)]
+    spines = [t.add_switch(2) for _ in range(n_spines)]
+    for l in leaves:
+        for h in t.add_hosts(hosts_per_leaf):
+            t.attach_host(h, l, sigma, delta)
+    for l in leaves:
+        for s in spines:
+            for _ in range(links_per_pair):
+                t.link(l, s, sigma, delta)
+    return t
+
+
+def fat_tree(k: int, delta: int = 0, hosts_per_edge: int | None = None,
+             uplinks_per_edge: int | None = None, sigma: int = 1) -> Topology:
+    """Three-tier k-ary fat-tree (k pods, k/2 edge + k/2 aggregation switches
+    per pod, (k/2)^2 cores).  ``hosts_per_edge``/``uplinks_per_edge`` below
+    k/2 give a partially populated or oversubscribed variant."""
+    half = k // 2
+    hpe = half if hosts_per_edge is None else hosts_per_edge
+    upe = half if uplinks_per_edge is None else uplinks_per_edge
+    t = Topology(f"fattree{k}")
+    edges, aggs = [], []
+    for _ in range(k):
+        edges.append([t.add_switch(1) for _ in range(half)])
+    for _ in range(k):
+        aggs.append([t.add_switch(2) for _ in range(half)])
+    cores = [t.add_switch(3) for _ in range(half * half)]
+    for pod in range(k):
+        for e in edges[pod]:
+            for h in t.add_hosts(hpe):
+                t.attach_host(h, e, sigma, delta)
+    for pod in range(k):
+        for e in edges[pod]:
+            for a in aggs[pod][:upe]:
+                t.link(e, a, sigma, delta)
+    for pod in range(k):
+        for j, a in enumerate(aggs[pod]):
+            for u in range(half):
+                t.link(a, cores[j * half + u], sigma, delta)
+    return t
+
+
+def rail_optimized(n_servers: int, gpus_per_server: int, servers_per_group: int,
+                   n_spines: int, delta: int = 0, links_per_pair: int = 1,
+                   sigma: int = 1) -> Topology:
+    """Rail-optimised two tier: within a group of servers, the NICs of GPU g
+    share rail leaf g; every leaf is wired to every spine.  Host numbering is
+    server-major (host = server * gpus_per_server + g)."""
+    t = Topology(f"rail{n_servers}")
+    n_groups = n_servers // servers_per_group
+    leaf = [[t.add_switch(1) for _ in range(gpus_per_server)] for _ in range(n_groups)]
+    spines = [t.add_switch(2) for _ in range(n_spines)]
+    hosts = t.add_hosts(n_servers * gpus_per_server)
+    for srv in range(n_servers):
+        for g in range(gpus_per_server):
+            t.attach_host(hosts[srv * gpus_per_server + g], leaf[srv // servers_per_group][g],
+                          sigma, delta)
+    for grp in leaf:
+        for l in grp:
+            for s in spines:
+                for _ in range(links_per_pair):
+                    t.link(l, s, sigma, delta)
+    return t
+
+
+# --------------------------------------------------------------------------
+# Workload DAG
+# --------------------------------------------------------------------------
+@dataclass
+class Coll:
+    kind: int
+    intra: bool
+    nbytes: int
+    ranks: list
+    nodes: list
+    parts: int = 0
+    alpha: int = 0
+    beta_num: int = 0
+    beta_den: int = 1
+    a2a: dict | None = None     # (src member, dst member) -> bytes
+
+
+class Workload:
+    """Per-rank task graphs in the ASTRA-sim style the Multiverse page uses
+    (section 3.1): nodes are compute tasks with an annotated duration, or a
+    rank's membership in a collective.  Edges join nodes of the same rank."""
+
+    def __init__(self, n_ranks: int, name: str = ""):
+        self.n_ranks = n_ranks
+        self.name = name
+        self.nodes: list[dict] = []
+        self.edges: list[tuple[int, int]] = []
+        self.colls: list[Coll] = []
+        self.mem = None
+
+    def compute(self, rank: int, lo_ns: int, hi_ns: int | None = None, key: int = 0) -> int:
+        """A compute task lasting ``lo_ns`` (or a duration hashed from
+        [lo_ns, hi_ns] with ``key`` and the experiment's duration seed)."""
+        self.nodes.append(dict(rank=rank, kind=COMPUTE, arg=0, lo=lo_ns,
+                               hi=lo_ns if hi_ns is None else hi_ns, key=key))
+        return len(self.nodes) - 1
+
+    def collective(self, kind: int, ranks, nbytes: int, intra: bool = False,
+                   parts: int = 0, alpha: int = 0, beta: tuple = (0, 1),
+                   a2a: dict | None = None) -> list[int]:
+        """One collective instance over ``ranks`` (member order = list order).
+        Returns the per-member node ids, in member order."""
+        ci = len(self.colls)
+        ids = []
+        for r in ranks:
+            self.nodes.append(dict(rank=r, kind=INTRA if intra else NET, arg=ci,
+                                   lo=0, hi=0, key=0))
+            ids.append(len(self.nodes) - 1)
+        self.colls.append(Coll(kind, intra, int(nbytes), list(ranks), ids, parts,
+                               alpha, beta[0], beta[1], a2a))
+        return ids
+
+    def edge(self, u: int, v: int):
+        assert self.nodes[u]["rank"] == self.nodes[v]["rank"], "edges stay within a rank"
+        self.edges.append((u, v))
+
+    def chain(self, *nodes):
+        for u, v in zip(nodes, nodes[1:]):
+            self.edge(u, v)
+
+    def set_memory_model(self, params: int, tp: int, pp: int, layers: int,
+                         micro: int, seq: int, batch: int, hidden: int, heads: int):
+        self.mem = (params, tp, pp, layers, micro, seq, batch, hidden, heads)
+
+    def arrays(self) -> dict:
+        order = sorted(range(len(self.nodes)), key=lambda i: (self.nodes[i]["rank"], i))
+        loc = np.empty(len(self.nodes), np.int64)
+        loc[order] = np.arange(len(order))
+        rank_n = np.zeros(self.n_ranks, np.uint32)
+        for n in self.nodes:
+            rank_n[n["rank"]] += 1
+        kind = np.array([self.nodes[i]["kind"] for i in order], np.uint32)
+        arg = np.array([self.nodes[i]["arg"] for i in order], np.uint32)
+        lo = np.array([self.nodes[i]["lo"] for i in order], np.uint32)
+        hi = np.array([self.nodes[i]["hi"] for i in order], np.uint32)
+        key = np.array([self.nodes[i]["key"] for i in order], np.uint32)
+        succ = [[] for _ in order]
+        npred = np.zeros(len(order), np.uint32)
+        for u, v in self.edges:
+            succ[loc[u]].append(int(loc[v]))
+            npred[loc[v]] += 1
+        nsucc = np.array([len(s) for s in succ], np.uint32)
+        succ_flat = np.array([v for s in succ for v in s], np.uint32)
+        ck = np.array([c.kind for c in self.colls], np.uint32)
+        cin = np.array([1 if c.intra else 0 for c in self.colls], np.uint32)
+        cb = np.array([c.nbytes for c in self.colls], np.uint64)
+        cn = np.array([len(c.ranks) for c in self.colls], np.uint32)
+        cp = np.array([c.parts for c in self.colls], np.uint32)
+        ca = np.array([c.alpha for c in self.colls], np.uint32)
+        cbn = np.array([c.beta_num for c in self.colls], np.uint32)
+        cbd = np.array([c.beta_den for c in self.colls], np.uint32)
+        mr = np.array([r for c in self.colls for r in c.ranks], np.uint32)
+        mn = np.array([loc[n] for c in self.colls for n in c.nodes], np.uint32)
+        # all-to-all traffic, rows (per sender, in rotation order starting at
+        # the next member) and columns (per receiver, by sender index)
+        row_n, row_d, row_b, col_n, col_s, col_b = [], [], [], [], [], []
+        for c in self.colls:
+            N = len(c.ranks)
+            m = c.a2a or {}
+            for i in range(N):
+                ents = sorted(((d, b) for (s, d), b in m.items() if s == i and d != i and b > 0),
+                              key=lambda e: (e[0] - i) % N)
+                row_n.append(len(ents))
+                row_d += [d for d, _ in ents]
+                row_b += [b for _, b in ents]
+            for j in range(N):
+                ents = sorted((s, b) for (s, d), b in m.items() if d == j and s != j and b > 0)
+                col_n.append(len(ents))
+                col_s += [s for s, _ in ents]
+                col_b += [b for _, b in ents]
+        mem = np.zeros(10, np.uint64)
+        if self.mem is not None:
+            mem[:9] = self.mem
+            mem[9] = 1
+        u32 = lambda x: np.array(x, np.uint32)
+        return dict(rank_nnodes=rank_n, node_kind=kind, node_arg=arg, node_npred=npred,
+                    node_nsucc=nsucc, node_dur_lo=lo, node_dur_hi=hi, node_dur_key=key,
+                    succ=succ_flat, coll_kind=ck, coll_intra=cin, coll_bytes=cb,
+                    coll_nmembers=cn, coll_parts=cp, coll_alpha=ca, coll_beta_num=cbn,
+                    coll_beta_den=cbd, member_rank=mr, member_node=mn,
+                    member_a2a_n=u32(row_n), a2a_dst=u32(row_d),
+                    a2a_bytes=np.array(row_b, np.uint64),
+                    member_a2a_in_n=u32(col_n), a2a_in_src=u32(col_s),
+                    a2a_in_bytes=np.array(col_b, np.uint64), mem=mem)
+
+
+# --------------------------------------------------------------------------
+# Experiments and batches
+# --------------------------------------------------------------------------
+@dataclass
+class Experiment:
+    topo: Topology
+    work: Workload
+    algo: int = RING
+    nc: int = 1
+    chunk: int = 512 * KIB
+    pkt: int = 4096
+    cap: int = 64
+    tick_ps: int = 81920
+    dur_seed: int = 0
+    ecmp_seed: int = 0
+    gpu_mem: int = 80 * 1024 ** 3
+    rec_cap: int = 0
+    label: dict = field(default_factory=dict)
+
+
+TOPO_FIELDS = ["sw_nports", "sw_level", "port_peer", "port_sigma", "port_delta",
+               "host_port", "host_sigma", "host_delta"]
+WORK_FIELDS = ["rank_nnodes", "node_kind", "node_arg", "node_npred", "node_nsucc",
+               "node_dur_lo", "node_dur_hi", "node_dur_key", "succ", "coll_kind",
+               "coll_intra", "coll_bytes", "coll_nmembers", "coll_parts", "coll_alpha",
+               "coll_beta_num", "coll_beta_den", "member_rank", "member_node",
+               "member_a2a_n", "a2a_dst", "a2a_bytes", "member_a2a_in_n", "a2a_in_src",
+               "a2a_in_bytes", "mem"]
+EXP_FIELDS = [("exp_topo", np.uint32), ("exp_work", np.uint32), ("exp_algo", np.uint32),
+              ("exp_nc", np.uint32), ("exp_chunk", np.uint64), ("exp_pkt", np.uint32),
+              ("exp_cap", np.uint32), ("exp_tick_ps", np.uint32), ("exp_dur_seed", np.uint64),
+              ("exp_ecmp_seed", np.uint64), ("exp_gpu_mem", np.uint64),
+              ("exp_rec_cap", np.uint32)]
+
+
+class Batch:
+    """A list of experiments; topologies and workloads shared by identity."""
+
+    def __init__(self, experiments: list[Experiment], name: str = ""):
+        self.experiments = experiments
+        self.name = name
+        self.topos: list[Topology] = []
+        self.works: list[Workload] = []
+        for e in experiments:
+            if not any(e.topo is t for t in self.topos):
+                self.topos.append(e.topo)
+            if not any(e.work is w for w in self.works):
+                self.works.append(e.work)
+
+    def __len__(self):
+        return len(self.experiments)
+
+    def subset(self, idx) -> "Batch":
+        return Batch([self.experiments[i] for i in idx], self.name)
+
+    def pack(self) -> dict:
+        """Flat arrays.  Indices stored inside a topology's (workload's) arrays
+        are local to that topology (workload); ``topo_*`` / ``work_*`` count
+        arrays let a reader rebuild the per-item offsets."""
+        out: dict = {"version": FORMAT_VERSION}
+        ta = [t.arrays() for t in self.topos]
+        out["topo_nhosts"] = np.array([t.n_hosts for t in self.topos], np.uint32)
+        out["topo_nsw"] = np.array([t.n_switches for t in self.topos], np.uint32)
+        out["topo_nports"] = np.array([len(a["port_peer"]) for a in ta], np.uint32)
+        for f in TOPO_FIELDS:
+            out[f] = np.concatenate([a[f] for a in ta])
+        wa = [w.arrays() for w in self.works]
+        out["work_nranks"] = np.array([w.n_ranks for w in self.works], np.uint32)
+        out["work_nnodes"] = np.array([len(a["node_kind"]) for a in wa], np.uint32)
+        out["work_nedges"] = np.array([len(a["succ"]) for a in wa], np.uint32)
+        out["work_ncolls"] = np.array([len(a["coll_kind"]) for a in wa], np.uint32)
+        out["work_nmembers"] = np.array([len(a["member_rank"]) for a in wa], np.uint32)
+        out["work_na2a"] = np.array([len(a["a2a_dst"]) for a in wa], np.uint32)
+        out["work_na2a_in"] = np.array([len(a["a2a_in_src"]) for a in wa], np.uint32)
+        for f in WORK_FIELDS:
+            out[f] = np.concatenate([a[f] for a in wa]).astype(wa[0][f].dtype)
+        for f, dt in EXP_FIELDS:
+            out[f] = np.zeros(len(self.experiments), dt)
+        for i, e in enumerate(self.experiments):
+            ti = next(j for j, t in enumerate(self.topos) if t is e.topo)
+            wi = next(j for j, w in enumerate(self.works) if w is e.work)
+            assert e.work.n_ranks <= e.topo.n_hosts
+            vals = [ti, wi, e.algo, e.nc, e.chunk, e.pkt, e.cap, e.tick_ps, e.dur_seed,
+                    e.ecmp_seed, e.gpu_mem, e.rec_cap]
+            for (f, _), v in zip(EXP_FIELDS, vals):
+                out[f][i] = v
+        return out
+
+    def node_counts(self) -> np.ndarray:
+        """Number of DAG nodes of each experiment (size of its result rows)."""
+        n = {id(w): len(w.nodes) for w in self.works}
+        return np.array([n[id(e.work)] for e in self.experiments], np.int64)
+
+
+# --------------------------------------------------------------------------
+# Workload shapes
+# --------------------------------------------------------------------------
+def single_collective(n_ranks: int, kind: int, nbytes: int, members=None,
+                      parts: int = 0) -> Workload:
+    """Every member rank runs one network collective and nothing else."""
+    w = Workload(n_ranks, f"{KIND_NAMES[kind]}{nbytes}")
+    w.collective(kind, list(range(n_ranks)) if members is None else members, nbytes,
+                 parts=parts)
+    return w
+
+
+def relay_chain(n_hosts: int, nbytes: int, parts: int) -> Workload:
+    """AlpaComm's broadcast of one slice from host 0 to hosts 1..n-1, split in
+    ``parts`` partitions that each receiver forwards once it holds them."""
+    return single_collective(n_hosts, RELAY, nbytes, parts=parts)
+
+
+def lone_message(n_ranks: int, src: int, dst: int, nbytes: int) -> Workload:
+    w = Workload(n_ranks, "p2p")
+    w.collective(P2P, [src, dst], nbytes)
+    return w
+
+
+# --------------------------------------------------------------------------
+# The five benchmark batches
+# --------------------------------------------------------------------------
+def config1() -> Batch:
+    """Ring all-reduce of 16 MiB over 8 hosts on a 2-leaf x 2-spine fabric,
+    400 Gbps, 1 us propagation, 4 KiB packets, 64-packet queues; 16
+    experiments over NC in {1,2,4,8} x chunk in {128K,512K,1M,4M}."""
+    tk = tick_ps(4096, 400)
+    topo = leaf_spine(2, 2, 4, delta=delay_ticks(1_000_000, tk))
+    work = single_collective(8, AR, 16 * MIB)
+    exps = []
+    for nc in (1, 2, 4, 8):
+        for ch in (128 * KIB, 512 * KIB, 1 * MIB, 4 * MIB):
+            exps.append(Experiment(topo, work, RING, nc, ch, 4096, 64, tk,
+                                   label=dict(nc=nc, chunk=ch)))
+    return Batch(exps, "ring-allreduce-16MiB-8hosts-leafspine")
+
+
+def config2(seed: int = 0, n_exp: int = 256) -> Batch:
+    """Pipelined broadcast over A+1 hosts on one 10 Gbps switch; (A, K) pairs
+    drawn without replacement from A in 2..16, K in 1..64, slice a uniform
+    whole number of MiB in [1, 64]."""
+    rng = np.random.default_rng(seed)
+    pairs = [(a, k) for a in range(2, 17) for k in range(1, 65)]
+    pick = rng.choice(len(pairs), size=n_exp, replace=False)
+    sizes = rng.integers(1, 65, size=n_exp)
+    tk = tick_ps(4096, 10)
+    d = delay_ticks(1_000_000, tk)
+    topos: dict = {}
+    exps = []
+    for j, p in enumerate(pick):
+        a, k = pairs[p]
+        if a not in topos:
+            topos[a] = single_switch(a + 1, 1, d)
+        work = relay_chain(a + 1, int(sizes[j]) * MIB, k)
+        exps.append(Experiment(topos[a], work, RING, 1, 0, 4096, 64, tk,
+                               label=dict(A=a, K=k, mib=int(sizes[j]))))
+    return Batch(exps, "pipelined-broadcast-10G")

@@ -1,0 +1,966 @@
+/*
+ * mv_oracle.c -- plain, slow, single-threaded CPU oracle for the lock-step
+ * packet simulation of collective traffic.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and
+ * the benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header or table with the CUDA library; both read the same flat batch
+ * arrays produced by the seeded input generators.
+ *
+ * What it follows (page = "Accelerating Design Space Exploration for LLM
+ * Training Systems with Multi-experiment Parallel Simulation", Multiverse):
+ *   - section 3.2, "system execution graph": one simulation step runs, in
+ *     order, Schedule/AnalyticalSys (DAG advance), the switch forwarding
+ *     systems, NIC send and NIC receive/ACK.  Here one step is one tick.
+ *   - section 4.2: forwarding is split into a per-ingress plan (which egress
+ *     the head packet wants) and a per-egress pull from the ingress ports.
+ *   - section 4.1: intra-server collectives take alpha + bytes/beta.
+ *   - section 3.1: the GPU memory check runs before the simulation.
+ *   - section 5: ring all-reduce / all-gather / reduce-scatter, ECMP.
+ * and from "AutoCCL" section 2.3: a message is split into NC partitions, one
+ * per channel, each cut into chunks of C bytes; from "On Optimizing the
+ * Communication of Model Parallelism" section 3.1: the pipelined broadcast
+ * in which each receiver forwards a partition once it holds it whole.
+ *
+ * Every experiment is simulated on its own, tick by tick, with one object
+ * per entity.  Within a tick the phases run over all entities in index
+ * order; cross-entity reads see the state at the start of the tick (queue
+ * snapshots, "joined before this tick"), which is what makes the result
+ * independent of the order entities are visited in.
+ *
+ * Parity pins live in tests/: the lone-message closed form, the pipelined
+ * broadcast closed form, a contention-free ring evaluated as a longest path,
+ * hand-traced tick tables, DAG critical paths, the analytic model and the
+ * memory check.  Functions without such a pin say so below.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define UNSET 0xFFFFFFFFu
+#define NLANE 64      /* send lanes per NIC (active messages streams)   */
+#define NPORT 128     /* receive counters per rank                      */
+#define NPEND 64      /* scheduled-but-not-started nodes per rank       */
+#define NACT 16       /* running collective memberships per rank        */
+
+enum { K_COMPUTE = 0, K_INTRA = 1, K_NET = 2 };
+enum { C_AR = 0, C_RS = 1, C_AG = 2, C_RELAY = 3, C_P2P = 4, C_A2A = 5 };
+enum { A_RING = 0, A_TREE = 1 };
+enum { ST_DONE = 0, ST_RUNNING = 1, ST_OOM = 2, ST_DEADLOCK = 3, ST_OVERFLOW = 4,
+       ST_ERROR = 5 };
+
+typedef struct orc_batch {
+    uint32_t version;
+    uint32_t n_topos, n_works, n_exps;
+    const uint32_t *topo_nhosts, *topo_nsw, *topo_nports;
+    const uint32_t *sw_nports, *sw_level;
+    const int32_t *port_peer;
+    const uint32_t *port_sigma, *port_delta, *host_port, *host_sigma, *host_delta;
+    const uint32_t *work_nranks, *work_nnodes, *work_nedges, *work_ncolls,
+        *work_nmembers, *work_na2a, *work_na2a_in;
+    const uint32_t *rank_nnodes, *node_kind, *node_arg, *node_npred, *node_nsucc,
+        *node_dur_lo, *node_dur_hi, *node_dur_key, *succ;
+    const uint32_t *coll_kind, *coll_intra;
+    const uint64_t *coll_bytes;
+    const uint32_t *coll_nmembers, *coll_parts, *coll_alpha, *coll_beta_num,
+        *coll_beta_den, *member_rank, *member_node, *member_a2a_n, *a2a_dst;
+    const uint64_t *a2a_bytes;
+    const uint32_t *member_a2a_in_n, *a2a_in_src;
+    const uint64_t *a2a_in_bytes;
+    const uint64_t *mem;
+    const uint32_t *exp_topo, *exp_work, *exp_algo, *exp_nc;
+    const uint64_t *exp_chunk;
+    const uint32_t *exp_pkt, *exp_cap, *exp_tick_ps;
+    const uint64_t *exp_dur_seed, *exp_ecmp_seed, *exp_gpu_mem;
+    const uint32_t *exp_rec_cap;
+} orc_batch;
+
+typedef struct orc_out {
+    uint32_t *status, *end_tick, *now;
+    uint64_t *pkts_injected, *pkt_hops, *pkts_delivered, *msgs_delivered, *digest,
+        *ticks_active;
+    uint32_t *node_start, *node_end;        /* concatenated per experiment */
+    uint32_t *rec_count;                    /* per experiment */
+    uint32_t *rec_sender, *rec_key, *rec_tick; /* concatenated, rec_cap each */
+} orc_out;
+
+/* ------------------------------------------------------------------------ */
+/* splitmix64 finaliser (S. Vigna, public domain splitmix64.c): the one
+ * counter-based hash used for ECMP, durations and the digest.              */
+static uint64_t mix64(uint64_t z)
+{
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+static uint64_t umin(uint64_t a, uint64_t b) { return a < b ? a : b; }
+static uint32_t umax32(uint32_t a, uint32_t b) { return a > b ? a : b; }
+
+/* ------------------------------------------------------------------------ */
+typedef struct pkt {
+    uint32_t ready, dst, hopsum, sender, pslot, last, key;
+} pkt;
+
+typedef struct lane {
+    int used;
+    uint32_t node, member, chan, kind;
+    uint32_t m, nmsg, pkts_left;
+    uint32_t dst_member, dst_port, dep_base, dep_mask, dep_need, key;
+    uint32_t a2a_e, a2a_start;
+} lane;
+
+typedef struct nic {
+    uint32_t busy, rr;
+    lane lanes[NLANE];
+    int port_used[NPORT];
+    uint32_t port_count[NPORT];
+    uint32_t port_node[NPORT];
+    uint32_t pend_node[NPEND], pend_start[NPEND];
+    int n_pend;
+    uint32_t act[NACT];
+    int n_act;
+} nic;
+
+typedef struct sim {
+    const orc_batch *b;
+    uint32_t e;
+    /* topology views (topology-local indices) */
+    uint32_t H, S, Q;
+    const uint32_t *sw_nports, *sw_level, *port_sigma, *port_delta, *host_port,
+        *host_sigma, *host_delta;
+    const int32_t *port_peer;
+    uint32_t *sw_base;     /* S+1 */
+    uint32_t *port_sw;     /* Q   */
+    int32_t *route;        /* S*H: down port (switch-local) or -1 */
+    uint32_t *up_base, *up_port;
+    /* workload views (workload-local indices) */
+    uint32_t R, NN;
+    uint32_t *rank_base;   /* R+1 */
+    uint32_t *node_rank;   /* NN */
+    uint32_t *succ_base;   /* NN+1 */
+    uint32_t *member_base; /* ncolls+1 */
+    uint32_t *row_base, *col_base; /* nmembers+1 */
+    uint32_t *node_member; /* NN: member index for collective nodes */
+    const uint32_t *node_kind, *node_arg, *node_npred, *node_dur_lo, *node_dur_hi,
+        *node_dur_key, *succ, *coll_kind, *coll_intra, *coll_nmembers, *coll_parts,
+        *coll_alpha, *coll_beta_num, *coll_beta_den, *member_rank, *member_node,
+        *a2a_dst, *a2a_in_src;
+    const uint64_t *coll_bytes, *a2a_bytes, *a2a_in_bytes, *mem;
+    /* experiment parameters */
+    uint32_t algo, nc, pkt, cap, tick_ps, rec_cap;
+    uint64_t chunk, dur_seed, ecmp_seed, gpu_mem;
+    /* dynamic state */
+    uint32_t nf;                    /* queues: Q switch ingress + H NIC rx */
+    uint32_t *head, *tail, *head0, *tail0;
+    pkt *slots;                     /* nf * cap */
+    uint32_t *eg_busy, *eg_rr;      /* Q */
+    nic *nics;                      /* R */
+    uint32_t *npred_left, *cand, *start, *end, *port_base, *done_max;
+    int64_t *outstanding;
+    uint32_t nodes_left;
+    int changed, status;
+    uint64_t pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
+    uint32_t *rec_sender, *rec_key, *rec_tick, rec_count;
+} sim;
+
+static void fail(sim *s, int st)
+{
+    if (s->status == ST_RUNNING) s->status = st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Routing: shortest up/down.  A switch forwards down when the destination
+ * host sits below one of its down ports (the lowest such port), otherwise up
+ * on a port chosen by the per-connection ECMP hash (Multiverse section 5).   */
+static void build_routes(sim *s)
+{
+    uint32_t S = s->S, H = s->H;
+    s->route = malloc(sizeof(int32_t) * (size_t)S * H);
+    for (size_t i = 0; i < (size_t)S * H; i++) s->route[i] = -1;
+    uint32_t maxlev = 0;
+    for (uint32_t w = 0; w < S; w++) maxlev = umax32(maxlev, s->sw_level[w]);
+    for (uint32_t lev = 1; lev <= maxlev; lev++) {
+        for (uint32_t w = 0; w < S; w++) {
+            if (s->sw_level[w] != lev) continue;
+            for (uint32_t p = 0; p < s->sw_nports[w]; p++) {
+                int32_t pe = s->port_peer[s->sw_base[w] + p];
+                if (pe < 0) {
+                    uint32_t h = (uint32_t)(-pe - 1);
+                    if (s->route[(size_t)w * H + h] < 0) s->route[(size_t)w * H + h] = (int32_t)p;
+                } else {
+                    uint32_t w2 = s->port_sw[pe];
+                    if (s->sw_level[w2] >= lev) continue;
+                    for (uint32_t h = 0; h < H; h++)
+                        if (s->route[(size_t)w2 * H + h] >= 0 && s->route[(size_t)w * H + h] < 0)
+                            s->route[(size_t)w * H + h] = (int32_t)p;
+                }
+            }
+        }
+    }
+    s->up_base = calloc(S + 1, sizeof(uint32_t));
+    s->up_port = malloc(sizeof(uint32_t) * (s->Q + 1));
+    uint32_t k = 0;
+    for (uint32_t w = 0; w < S; w++) {
+        s->up_base[w] = k;
+        for (uint32_t p = 0; p < s->sw_nports[w]; p++) {
+            int32_t pe = s->port_peer[s->sw_base[w] + p];
+            if (pe >= 0 && s->sw_level[s->port_sw[pe]] > s->sw_level[w]) s->up_port[k++] = p;
+        }
+    }
+    s->up_base[S] = k;
+}
+
+/* egress port (switch-local) for a packet at switch w */
+static int32_t route_port(sim *s, uint32_t w, const pkt *p)
+{
+    int32_t d = s->route[(size_t)w * s->H + p->dst];
+    if (d >= 0) return d;
+    uint32_t nup = s->up_base[w + 1] - s->up_base[w];
+    if (nup == 0) return -1;
+    uint64_t h = mix64((uint64_t)p->key ^ ((uint64_t)w << 40) ^ s->ecmp_seed);
+    return (int32_t)s->up_port[s->up_base[w] + (uint32_t)(h % nup)];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Collective decomposition into messages (AutoCCL section 2.3 for NC and C;
+ * the ring schedule of NCCL named on the Multiverse page, section 5).       */
+static uint32_t coll_of(sim *s, uint32_t node) { return s->node_arg[node]; }
+static uint32_t nmemb(sim *s, uint32_t c) { return s->coll_nmembers[c]; }
+static uint32_t mrank(sim *s, uint32_t c, uint32_t i) { return s->member_rank[s->member_base[c] + i]; }
+static uint32_t mnode(sim *s, uint32_t c, uint32_t i) { return s->member_node[s->member_base[c] + i]; }
+
+static int is_tree(sim *s, uint32_t c) { return s->coll_kind[c] == C_AR && s->algo == A_TREE; }
+
+static uint32_t n_chan(sim *s, uint32_t c)
+{
+    uint32_t k = s->coll_kind[c];
+    return (k == C_RELAY || k == C_P2P) ? 1 : s->nc;
+}
+/* lanes per channel / ports per channel */
+static uint32_t lanes_per_chan(sim *s, uint32_t c) { return is_tree(s, c) ? 3 : 1; }
+static uint32_t n_ports(sim *s, uint32_t c)
+{
+    uint32_t k = s->coll_kind[c];
+    if (k == C_RELAY || k == C_P2P || k == C_A2A) return 1;
+    return n_chan(s, c) * (is_tree(s, c) ? 3 : 1);
+}
+
+/* bytes of channel c's partition: the first S mod NC partitions get one more */
+static uint64_t partition(uint64_t S, uint32_t nc, uint32_t c)
+{
+    return S / nc + (c < S % nc ? 1 : 0);
+}
+
+static uint32_t ring_steps(sim *s, uint32_t c)
+{
+    uint32_t N = nmemb(s, c);
+    if (N < 2) return 0;
+    return s->coll_kind[c] == C_AR ? 2 * (N - 1) : N - 1;
+}
+
+static uint64_t ring_loops(sim *s, uint32_t c, uint64_t P)
+{
+    uint64_t stride = (uint64_t)nmemb(s, c) * s->chunk;
+    return P == 0 ? 1 : ceil_div(P, stride);
+}
+
+static uint64_t n_chunks(uint64_t bytes, uint64_t C) { return bytes == 0 ? 1 : ceil_div(bytes, C); }
+
+/* number of messages lane (chan, kind) of member i sends */
+static uint32_t lane_nmsg(sim *s, uint32_t c, uint32_t i, uint32_t chan, uint32_t kind)
+{
+    uint32_t N = nmemb(s, c);
+    uint64_t S = s->coll_bytes[c];
+    switch (s->coll_kind[c]) {
+    case C_AR: case C_RS: case C_AG:
+        if (is_tree(s, c)) {
+            uint64_t nch = n_chunks(partition(S, s->nc, chan), s->chunk);
+            if (kind == 0) return i > 0 ? (uint32_t)nch : 0;
+            if (kind == 1) return 2 * i + 1 < N ? (uint32_t)nch : 0;
+            return 2 * i + 2 < N ? (uint32_t)nch : 0;
+        }
+        return (uint32_t)(ring_loops(s, c, partition(S, s->nc, chan)) * ring_steps(s, c));
+    case C_RELAY:
+        return i + 1 < N ? s->coll_parts[c] : 0;
+    case C_P2P:
+        return i == 0 ? (uint32_t)n_chunks(S, s->chunk) : 0;
+    case C_A2A: {
+        uint64_t tot = 0;
+        for (uint32_t e = s->row_base[s->member_base[c] + i]; e < s->row_base[s->member_base[c] + i + 1]; e++)
+            tot += n_chunks(s->a2a_bytes[e], s->chunk);
+        return tot > chan ? (uint32_t)ceil_div(tot - chan, s->nc) : 0;
+    }
+    }
+    return 0;
+}
+
+/* messages expected on receive port p of member i */
+static uint32_t port_expect(sim *s, uint32_t c, uint32_t i, uint32_t p)
+{
+    uint32_t N = nmemb(s, c);
+    uint64_t S = s->coll_bytes[c];
+    switch (s->coll_kind[c]) {
+    case C_AR: case C_RS: case C_AG:
+        if (is_tree(s, c)) {
+            uint32_t chan = p / 3, q = p % 3;
+            uint64_t nch = n_chunks(partition(S, s->nc, chan), s->chunk);
+            if (q == 0) return i > 0 ? (uint32_t)nch : 0;
+            if (q == 1) return 2 * i + 1 < N ? (uint32_t)nch : 0;
+            return 2 * i + 2 < N ? (uint32_t)nch : 0;
+        }
+        return (uint32_t)(ring_loops(s, c, partition(S, s->nc, p)) * ring_steps(s, c));
+    case C_RELAY:
+        return i > 0 ? s->coll_parts[c] : 0;
+    case C_P2P:
+        return i == 1 ? (uint32_t)n_chunks(S, s->chunk) : 0;
+    case C_A2A: {
+        uint64_t tot = 0;
+        for (uint32_t e = s->col_base[s->member_base[c] + i]; e < s->col_base[s->member_base[c] + i + 1]; e++)
+            tot += n_chunks(s->a2a_in_bytes[e], s->chunk);
+        return (uint32_t)tot;
+    }
+    }
+    return 0;
+}
+
+/* Fill in message m of a lane: its bytes, destination, destination port and
+ * the receive counts it waits for.  Returns the packet count. */
+static uint32_t lane_setup(sim *s, lane *L)
+{
+    uint32_t c = coll_of(s, L->node);
+    uint32_t N = nmemb(s, c), i = L->member, m = L->m, chan = L->chan;
+    uint64_t S = s->coll_bytes[c], C = s->chunk, bytes = 0;
+    L->dep_mask = 0;
+    L->dep_need = 0;
+    L->dep_base = 0;
+    switch (s->coll_kind[c]) {
+    case C_AR: case C_RS: case C_AG: {
+        uint64_t P = partition(S, s->nc, chan);
+        if (is_tree(s, c)) {
+            uint32_t has_l = 2 * i + 1 < N, has_r = 2 * i + 2 < N;
+            bytes = P > (uint64_t)m * C ? umin(C, P - (uint64_t)m * C) : 0;
+            uint32_t child_mask = (has_l ? 2u : 0u) | (has_r ? 4u : 0u);
+            if (L->kind == 0) {               /* reduce: up to the parent */
+                uint32_t par = (i - 1) / 2;
+                L->dst_member = par;
+                L->dst_port = chan * 3 + (i == 2 * par + 1 ? 1 : 2);
+                L->dep_mask = child_mask;
+            } else {                          /* broadcast: down to a child */
+                L->dst_member = 2 * i + L->kind;
+                L->dst_port = chan * 3;
+                L->dep_mask = i == 0 ? child_mask : 1u;
+            }
+            L->dep_need = m + 1;
+            L->dep_base = chan * 3;
+        } else {
+            uint32_t steps = ring_steps(s, c);
+            uint64_t l = m / steps, k = m % steps;
+            uint64_t stride = (uint64_t)N * C;
+            uint64_t B = umin(stride, P - l * stride);
+            uint64_t bs = ceil_div(B, N);
+            uint64_t blk = ((uint64_t)i + N - (k % N)) % N;   /* (i - k) mod N */
+            bytes = B > blk * bs ? umin(bs, B - blk * bs) : 0;
+            L->dst_member = (i + 1) % N;
+            L->dst_port = chan;
+            L->dep_base = chan;
+            if (k >= 1) { L->dep_mask = 1u; L->dep_need = (uint32_t)(l * steps + k); }
+        }
+        break;
+    }
+    case C_RELAY: {
+        uint32_t K = s->coll_parts[c];
+        bytes = S / K + (m < S % K ? 1 : 0);
+        L->dst_member = i + 1;
+        L->dst_port = 0;
+        if (i >= 1) { L->dep_mask = 1u; L->dep_need = m + 1; }
+        break;
+    }
+    case C_P2P:
+        bytes = S > (uint64_t)m * C ? umin(C, S - (uint64_t)m * C) : 0;
+        L->dst_member = 1;
+        L->dst_port = 0;
+        break;
+    case C_A2A: {
+        uint32_t r0 = s->row_base[s->member_base[c] + i];
+        uint64_t g = (uint64_t)chan + (uint64_t)m * s->nc;
+        while (g >= L->a2a_start + n_chunks(s->a2a_bytes[r0 + L->a2a_e], C)) {
+            L->a2a_start += (uint32_t)n_chunks(s->a2a_bytes[r0 + L->a2a_e], C);
+            L->a2a_e++;
+        }
+        uint64_t j = g - L->a2a_start, b = s->a2a_bytes[r0 + L->a2a_e];
+        bytes = b > j * C ? umin(C, b - j * C) : 0;
+        L->dst_member = s->a2a_dst[r0 + L->a2a_e];
+        L->dst_port = 0;
+        break;
+    }
+    }
+    uint32_t drank = mrank(s, c, L->dst_member);
+    L->key = (uint32_t)(mix64((uint64_t)L->node | ((uint64_t)(chan * 4 + L->kind) << 32) |
+                              ((uint64_t)drank << 44)) & 0xFFFFFFu);
+    return (uint32_t)(bytes == 0 ? 1 : ceil_div(bytes, s->pkt));
+}
+
+/* ------------------------------------------------------------------------ */
+/* DAG advance (Schedule + AnalyticalSys, Multiverse section 3.2)           */
+static uint32_t compute_ticks(sim *s, uint32_t u)
+{
+    uint64_t lo = s->node_dur_lo[u], hi = s->node_dur_hi[u], ns = lo;
+    if (hi > lo) ns = lo + mix64(mix64((uint64_t)s->node_dur_key[u]) ^ s->dur_seed) % (hi - lo + 1);
+    return (uint32_t)ceil_div(ns * 1000, s->tick_ps);
+}
+
+/* Analytic intra-server time (Multiverse section 4.1): alpha + bytes/beta
+ * with beta given as ticks per byte beta_num/beta_den, and the bytes each
+ * GPU moves: 2(g-1)S/g for all-reduce, (g-1)S/g for all-gather and
+ * reduce-scatter, S otherwise. */
+static uint32_t intra_ticks(sim *s, uint32_t c)
+{
+    uint64_t g = nmemb(s, c), S = s->coll_bytes[c], be;
+    switch (s->coll_kind[c]) {
+    case C_AR: be = ceil_div(2 * (g - 1) * S, g); break;
+    case C_RS: case C_AG: be = ceil_div((g - 1) * S, g); break;
+    default: be = S;
+    }
+    return s->coll_alpha[c] + (uint32_t)ceil_div(be * s->coll_beta_num[c], s->coll_beta_den[c]);
+}
+
+static void pend_add(sim *s, uint32_t r, uint32_t u, uint32_t st)
+{
+    nic *n = &s->nics[r];
+    if (n->n_pend >= NPEND) { fail(s, ST_OVERFLOW); return; }
+    n->pend_node[n->n_pend] = u;
+    n->pend_start[n->n_pend] = st;
+    n->n_pend++;
+}
+
+static void complete(sim *s, uint32_t u, uint32_t c)
+{
+    uint32_t r = s->node_rank[u];
+    s->end[u] = c;
+    s->nodes_left--;
+    s->changed = 1;
+    if (c >= UNSET - 1) { fail(s, ST_OVERFLOW); return; }
+    for (uint32_t k = s->succ_base[u]; k < s->succ_base[u + 1]; k++) {
+        uint32_t v = s->succ[k];
+        s->cand[v] = umax32(s->cand[v], c + 1);
+        if (--s->npred_left[v] == 0) pend_add(s, r, v, s->cand[v]);
+    }
+}
+
+/* a rank joins a network collective: receive counters and send lanes */
+static void net_join(sim *s, uint32_t r, uint32_t u, uint32_t t)
+{
+    nic *n = &s->nics[r];
+    uint32_t c = coll_of(s, u), i = s->node_member[u];
+    uint32_t np = n_ports(s, c);
+    int base = -1;
+    for (uint32_t b = 0; b + np <= NPORT && base < 0; b++) {
+        uint32_t k = 0;
+        while (k < np && !n->port_used[b + k]) k++;
+        if (k == np) base = (int)b;
+    }
+    if (base < 0) { fail(s, ST_OVERFLOW); return; }
+    int64_t out = 0;
+    for (uint32_t p = 0; p < np; p++) {
+        n->port_used[base + p] = 1;
+        n->port_count[base + p] = 0;
+        n->port_node[base + p] = u;
+        out += port_expect(s, c, i, p);
+    }
+    s->port_base[u] = (uint32_t)base;
+    uint32_t nch = n_chan(s, c), lpc = lanes_per_chan(s, c);
+    for (uint32_t ch = 0; ch < nch; ch++) {
+        for (uint32_t k = 0; k < lpc; k++) {
+            uint32_t nm = lane_nmsg(s, c, i, ch, k);
+            if (nm == 0) continue;
+            int slot = -1;
+            for (int q = 0; q < NLANE && slot < 0; q++)
+                if (!n->lanes[q].used) slot = q;
+            if (slot < 0) { fail(s, ST_OVERFLOW); return; }
+            lane *L = &n->lanes[slot];
+            memset(L, 0, sizeof *L);
+            L->used = 1;
+            L->node = u; L->member = i; L->chan = ch; L->kind = k;
+            L->m = 0; L->nmsg = nm;
+            L->pkts_left = lane_setup(s, L);
+            out += nm;
+        }
+    }
+    s->outstanding[u] = out;
+    s->done_max[u] = t;
+    (void)t;
+}
+
+static void free_ports(sim *s, uint32_t r, uint32_t u)
+{
+    uint32_t np = n_ports(s, coll_of(s, u));
+    for (uint32_t p = 0; p < np; p++) s->nics[r].port_used[s->port_base[u] + p] = 0;
+}
+
+static void act_add(sim *s, uint32_t r, uint32_t u)
+{
+    nic *n = &s->nics[r];
+    if (n->n_act >= NACT) { fail(s, ST_OVERFLOW); return; }
+    n->act[n->n_act++] = u;
+}
+
+static int cmp_u32(const void *a, const void *b)
+{
+    uint32_t x = *(const uint32_t *)a, y = *(const uint32_t *)b;
+    return x < y ? -1 : x > y;
+}
+
+static void dag_step(sim *s, uint32_t r, uint32_t t)
+{
+    nic *n = &s->nics[r];
+    /* (a) running collectives, in node order: has this member finished? */
+    qsort(n->act, n->n_act, sizeof(uint32_t), cmp_u32);
+    uint32_t keep[NACT];
+    int nk = 0, na = n->n_act;
+    uint32_t acts[NACT];
+    memcpy(acts, n->act, sizeof(uint32_t) * na);
+    for (int a = 0; a < na; a++) {
+        uint32_t u = acts[a], c = coll_of(s, u);
+        if (s->node_kind[u] == K_INTRA) {
+            uint32_t N = nmemb(s, c), b = 0, ok = 1;
+            for (uint32_t j = 0; j < N && ok; j++) {
+                uint32_t st = s->start[mnode(s, c, j)];
+                if (st == UNSET || st >= t) ok = 0;
+                else b = umax32(b, st);
+            }
+            if (ok) complete(s, u, b + intra_ticks(s, c));
+            else keep[nk++] = u;
+        } else {
+            if (s->outstanding[u] == 0) {
+                free_ports(s, r, u);
+                complete(s, u, s->done_max[u]);
+            } else {
+                keep[nk++] = u;
+            }
+        }
+    }
+    memcpy(n->act, keep, sizeof(uint32_t) * nk);
+    n->n_act = nk;
+    /* (b) start the nodes scheduled for this tick, in node order */
+    uint32_t now_nodes[NPEND];
+    int nn = 0, w = 0;
+    for (int k = 0; k < n->n_pend; k++) {
+        if (n->pend_start[k] < t) { fail(s, ST_ERROR); return; }
+        if (n->pend_start[k] == t) now_nodes[nn++] = n->pend_node[k];
+        else { n->pend_node[w] = n->pend_node[k]; n->pend_start[w] = n->pend_start[k]; w++; }
+    }
+    n->n_pend = w;
+    qsort(now_nodes, nn, sizeof(uint32_t), cmp_u32);
+    for (int k = 0; k < nn; k++) {
+        uint32_t u = now_nodes[k];
+        s->start[u] = t;
+        s->changed = 1;
+        switch (s->node_kind[u]) {
+        case K_COMPUTE:
+            complete(s, u, t + compute_ticks(s, u));
+            break;
+        case K_INTRA:
+            act_add(s, r, u);
+            break;
+        case K_NET:
+            net_join(s, r, u, t);
+            if (s->outstanding[u] == 0) {
+                free_ports(s, r, u);
+                complete(s, u, t);
+            } else {
+                act_add(s, r, u);
+            }
+            break;
+        }
+        if (s->status != ST_RUNNING) return;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* queues: ring buffers of cap slots; head/tail are free-running counters   */
+static pkt *slot(sim *s, uint32_t f, uint32_t idx) { return &s->slots[(size_t)f * s->cap + idx % s->cap]; }
+static uint32_t q_of_host(sim *s, uint32_t h) { return s->Q + h; }
+static uint32_t downstream(sim *s, uint32_t q)
+{
+    int32_t pe = s->port_peer[q];
+    return pe >= 0 ? (uint32_t)pe : q_of_host(s, (uint32_t)(-pe - 1));
+}
+/* credit: may a sender push into queue f this tick?  Entries popped this
+ * tick free their slot from the next tick on (start-of-tick snapshot). */
+static int has_credit(sim *s, uint32_t f) { return s->tail[f] - s->head0[f] < s->cap; }
+/* the head entry, if it was present at the start of the tick and is ready */
+static pkt *ready_head(sim *s, uint32_t f, uint32_t t)
+{
+    if (s->tail0[f] == s->head[f]) return NULL;
+    pkt *p = slot(s, f, s->head[f]);
+    return p->ready <= t ? p : NULL;
+}
+
+static void push(sim *s, uint32_t f, const pkt *p)
+{
+    *slot(s, f, s->tail[f]) = *p;
+    s->tail[f]++;
+}
+
+/* Switch forwarding (Multiverse section 4.2, pull-based): plan = for each
+ * ingress port, the egress its ready head packet needs; pull = each free
+ * egress with credit downstream scans the ingress ports round-robin from its
+ * pointer and takes the first head planned for it. */
+static void forward(sim *s, uint32_t w, uint32_t t)
+{
+    uint32_t P = s->sw_nports[w], base = s->sw_base[w];
+    int32_t tgt[256];
+    for (uint32_t p = 0; p < P; p++) {
+        pkt *h = ready_head(s, base + p, t);
+        tgt[p] = -1;
+        if (h) {
+            tgt[p] = route_port(s, w, h);
+            if (tgt[p] < 0) { fail(s, ST_ERROR); return; }
+        }
+    }
+    for (uint32_t e = 0; e < P; e++) {
+        uint32_t qe = base + e;
+        if (s->eg_busy[qe] > t) continue;
+        uint32_t d = downstream(s, qe);
+        if (!has_credit(s, d)) continue;
+        for (uint32_t k = 0; k < P; k++) {
+            uint32_t i = (s->eg_rr[qe] + k) % P;
+            if (tgt[i] != (int32_t)e) continue;
+            pkt p = *slot(s, base + i, s->head[base + i]);
+            s->head[base + i]++;
+            p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
+            p.hopsum += s->port_delta[qe] + 1;
+            push(s, d, &p);
+            s->eg_busy[qe] = t + s->port_sigma[qe];
+            s->eg_rr[qe] = (i + 1) % P;
+            s->pkt_hops++;
+            s->changed = 1;
+            break;
+        }
+    }
+}
+
+/* NIC send (SendSys + NICSndSys): one packet per uplink serialisation time,
+ * round-robin over the rank's send lanes.  A lane may send when the receive
+ * counts its current message waits for are reached (NCCL's step order), and
+ * when the receiving rank joined the collective before this tick. */
+static void inject(sim *s, uint32_t r, uint32_t t)
+{
+    nic *n = &s->nics[r];
+    if (n->busy > t) return;
+    uint32_t f = s->host_port[r];
+    if (!has_credit(s, f)) return;
+    for (uint32_t k = 0; k < NLANE; k++) {
+        uint32_t q = (n->rr + k) % NLANE;
+        lane *L = &n->lanes[q];
+        if (!L->used) continue;
+        int ok = 1;
+        for (uint32_t b = 0; b < 3; b++)
+            if ((L->dep_mask >> b) & 1u)
+                if (n->port_count[s->port_base[L->node] + L->dep_base + b] < L->dep_need) ok = 0;
+        if (!ok) continue;
+        uint32_t c = coll_of(s, L->node);
+        uint32_t dnode = mnode(s, c, L->dst_member);
+        if (s->start[dnode] == UNSET || s->start[dnode] >= t) continue;
+        pkt p;
+        p.ready = t + s->host_sigma[r] + s->host_delta[r];
+        p.dst = mrank(s, c, L->dst_member);
+        p.hopsum = s->host_delta[r] + 1;
+        p.sender = L->node;
+        p.pslot = s->port_base[dnode] + L->dst_port;
+        p.last = L->pkts_left == 1;
+        p.key = L->key;
+        push(s, f, &p);
+        n->busy = t + s->host_sigma[r];
+        n->rr = (q + 1) % NLANE;
+        s->pkts_injected++;
+        s->pkt_hops++;
+        s->changed = 1;
+        if (--L->pkts_left == 0) {
+            if (++L->m == L->nmsg) L->used = 0;
+            else L->pkts_left = lane_setup(s, L);
+        }
+        return;
+    }
+}
+
+/* NIC receive (NICRcvSys + ACKSys): the ready head of the NIC's downlink
+ * queue.  The last packet of a message completes it: the receive count goes
+ * up, the receiver's membership is one message closer to done, and the
+ * sender's membership gets the message's acknowledgement, which reaches it
+ * one propagation-plus-one-tick per hop after delivery. */
+static void receive(sim *s, uint32_t r, uint32_t t)
+{
+    uint32_t f = q_of_host(s, r);
+    pkt *h = ready_head(s, f, t);
+    if (!h) return;
+    pkt p = *h;
+    s->head[f]++;
+    s->pkts_delivered++;
+    s->changed = 1;
+    if (!p.last) return;
+    nic *n = &s->nics[r];
+    n->port_count[p.pslot]++;
+    uint32_t own = n->port_node[p.pslot];
+    s->outstanding[own]--;
+    s->done_max[own] = umax32(s->done_max[own], t);
+    s->outstanding[p.sender]--;
+    s->done_max[p.sender] = umax32(s->done_max[p.sender], t + p.hopsum);
+    s->msgs_delivered++;
+    s->digest += mix64(mix64((uint64_t)p.sender | ((uint64_t)p.key << 32)) ^ (uint64_t)t);
+    if (s->rec_count < s->rec_cap) {
+        s->rec_sender[s->rec_count] = p.sender;
+        s->rec_key[s->rec_count] = p.key;
+        s->rec_tick[s->rec_count] = t;
+    }
+    s->rec_count++;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GPU memory check (Multiverse section 3.1, "GPU memory simulator").  The
+ * page gives no formula; this reads it as bf16 weights + gradients + fp32
+ * Adam state (16 bytes per parameter) split over TP x PP, plus the
+ * activations of min(m, PP) in-flight micro-batches of one pipeline stage
+ * using the per-layer activation size s*b*h*(34 + 5*a*s/h) of Korthikanti et
+ * al. 2022 (an outside source, named as such), split over TP. */
+static int memory_fits(const uint64_t *mem, uint64_t cap)
+{
+    if (mem[9] == 0) return 1;
+    uint64_t params = mem[0], tp = mem[1], pp = mem[2], layers = mem[3], m = mem[4];
+    uint64_t sq = mem[5], b = mem[6], h = mem[7], a = mem[8];
+    uint64_t weights = 16 * params / (tp * pp);
+    uint64_t per_layer = sq * b * (34 * h + 5 * a * sq);
+    uint64_t acts = layers * umin(m, pp) * per_layer / tp;
+    return weights + acts <= cap;
+}
+
+/* ------------------------------------------------------------------------ */
+static uint32_t next_event(sim *s, uint32_t t)
+{
+    uint32_t best = UNSET;
+    for (uint32_t r = 0; r < s->R; r++) {
+        nic *n = &s->nics[r];
+        for (int k = 0; k < n->n_pend; k++)
+            if (n->pend_start[k] > t && n->pend_start[k] < best) best = n->pend_start[k];
+        if (n->busy > t && n->busy < best) best = n->busy;
+    }
+    for (uint32_t f = 0; f < s->nf; f++) {
+        if (s->head[f] == s->tail[f]) continue;
+        uint32_t rd = slot(s, f, s->head[f])->ready;
+        if (rd > t && rd < best) best = rd;
+    }
+    for (uint32_t q = 0; q < s->Q; q++)
+        if (s->eg_busy[q] > t && s->eg_busy[q] < best) best = s->eg_busy[q];
+    return best;
+}
+
+static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *now_out)
+{
+    uint32_t t = 0;
+    uint64_t active = 0;
+    for (uint32_t r = 0; r < s->R; r++)
+        for (uint32_t u = s->rank_base[r]; u < s->rank_base[r + 1]; u++)
+            if (s->node_npred[u] == 0) pend_add(s, r, u, 0);
+    while (s->status == ST_RUNNING) {
+        if (s->nodes_left == 0) { s->status = ST_DONE; break; }
+        if (t >= limit) break;
+        memcpy(s->head0, s->head, sizeof(uint32_t) * s->nf);
+        memcpy(s->tail0, s->tail, sizeof(uint32_t) * s->nf);
+        s->changed = 0;
+        for (uint32_t r = 0; r < s->R && s->status == ST_RUNNING; r++) dag_step(s, r, t);
+        for (uint32_t w = 0; w < s->S && s->status == ST_RUNNING; w++) forward(s, w, t);
+        for (uint32_t r = 0; r < s->R; r++) inject(s, r, t);
+        for (uint32_t r = 0; r < s->R; r++) receive(s, r, t);
+        active++;
+        if (s->status != ST_RUNNING) break;
+        if (s->nodes_left == 0) { s->status = ST_DONE; t++; break; }
+        if (s->changed) { t++; continue; }
+        uint32_t nx = next_event(s, t);
+        if (nx == UNSET) { s->status = ST_DEADLOCK; t++; break; }
+        t = nx;
+    }
+    *ticks_active = active;
+    *now_out = t;
+}
+
+/* ------------------------------------------------------------------------ */
+static uint32_t *prefix(const uint32_t *cnt, uint32_t n)
+{
+    uint32_t *p = malloc(sizeof(uint32_t) * (n + 1));
+    p[0] = 0;
+    for (uint32_t i = 0; i < n; i++) p[i + 1] = p[i] + cnt[i];
+    return p;
+}
+
+typedef struct offs {
+    uint32_t *host, *sw, *port, *rank, *node, *edge, *coll, *memb, *a2a, *a2a_in;
+} offs;
+
+static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit,
+                   orc_out *out, uint64_t node_off, uint64_t rec_off)
+{
+    sim S_, *s = &S_;
+    memset(s, 0, sizeof *s);
+    s->b = b;
+    s->e = e;
+    uint32_t ti = b->exp_topo[e], wi = b->exp_work[e];
+    s->H = b->topo_nhosts[ti];
+    s->S = b->topo_nsw[ti];
+    s->Q = b->topo_nports[ti];
+    s->sw_nports = b->sw_nports + o->sw[ti];
+    s->sw_level = b->sw_level + o->sw[ti];
+    s->port_peer = b->port_peer + o->port[ti];
+    s->port_sigma = b->port_sigma + o->port[ti];
+    s->port_delta = b->port_delta + o->port[ti];
+    s->host_port = b->host_port + o->host[ti];
+    s->host_sigma = b->host_sigma + o->host[ti];
+    s->host_delta = b->host_delta + o->host[ti];
+    s->sw_base = prefix(s->sw_nports, s->S);
+    s->port_sw = malloc(sizeof(uint32_t) * (s->Q + 1));
+    for (uint32_t w = 0; w < s->S; w++)
+        for (uint32_t q = s->sw_base[w]; q < s->sw_base[w + 1]; q++) s->port_sw[q] = w;
+    build_routes(s);
+
+    s->R = b->work_nranks[wi];
+    s->NN = b->work_nnodes[wi];
+    uint32_t nco = b->work_ncolls[wi], nme = b->work_nmembers[wi];
+    s->node_kind = b->node_kind + o->node[wi];
+    s->node_arg = b->node_arg + o->node[wi];
+    s->node_npred = b->node_npred + o->node[wi];
+    s->node_dur_lo = b->node_dur_lo + o->node[wi];
+    s->node_dur_hi = b->node_dur_hi + o->node[wi];
+    s->node_dur_key = b->node_dur_key + o->node[wi];
+    s->succ = b->succ + o->edge[wi];
+    s->coll_kind = b->coll_kind + o->coll[wi];
+    s->coll_intra = b->coll_intra + o->coll[wi];
+    s->coll_bytes = b->coll_bytes + o->coll[wi];
+    s->coll_nmembers = b->coll_nmembers + o->coll[wi];
+    s->coll_parts = b->coll_parts + o->coll[wi];
+    s->coll_alpha = b->coll_alpha + o->coll[wi];
+    s->coll_beta_num = b->coll_beta_num + o->coll[wi];
+    s->coll_beta_den = b->coll_beta_den + o->coll[wi];
+    s->member_rank = b->member_rank + o->memb[wi];
+    s->member_node = b->member_node + o->memb[wi];
+    s->a2a_dst = b->a2a_dst + o->a2a[wi];
+    s->a2a_bytes = b->a2a_bytes + o->a2a[wi];
+    s->a2a_in_src = b->a2a_in_src + o->a2a_in[wi];
+    s->a2a_in_bytes = b->a2a_in_bytes + o->a2a_in[wi];
+    s->mem = b->mem + (size_t)10 * wi;
+    s->rank_base = prefix(b->rank_nnodes + o->rank[wi], s->R);
+    s->succ_base = prefix(b->node_nsucc + o->node[wi], s->NN);
+    s->member_base = prefix(s->coll_nmembers, nco);
+    s->row_base = prefix(b->member_a2a_n + o->memb[wi], nme);
+    s->col_base = prefix(b->member_a2a_in_n + o->memb[wi], nme);
+    s->node_rank = malloc(sizeof(uint32_t) * (s->NN + 1));
+    s->node_member = calloc(s->NN + 1, sizeof(uint32_t));
+    for (uint32_t r = 0; r < s->R; r++)
+        for (uint32_t u = s->rank_base[r]; u < s->rank_base[r + 1]; u++) s->node_rank[u] = r;
+    for (uint32_t c = 0; c < nco; c++)
+        for (uint32_t i = 0; i < s->coll_nmembers[c]; i++) s->node_member[mnode(s, c, i)] = i;
+
+    s->algo = b->exp_algo[e];
+    s->nc = b->exp_nc[e];
+    s->chunk = b->exp_chunk[e];
+    s->pkt = b->exp_pkt[e];
+    s->cap = b->exp_cap[e];
+    s->tick_ps = b->exp_tick_ps[e];
+    s->dur_seed = b->exp_dur_seed[e];
+    s->ecmp_seed = b->exp_ecmp_seed[e];
+    s->gpu_mem = b->exp_gpu_mem[e];
+    s->rec_cap = b->exp_rec_cap[e];
+
+    s->nf = s->Q + s->H;
+    s->head = calloc(s->nf, sizeof(uint32_t));
+    s->tail = calloc(s->nf, sizeof(uint32_t));
+    s->head0 = calloc(s->nf, sizeof(uint32_t));
+    s->tail0 = calloc(s->nf, sizeof(uint32_t));
+    s->slots = calloc((size_t)s->nf * s->cap, sizeof(pkt));
+    s->eg_busy = calloc(s->Q + 1, sizeof(uint32_t));
+    s->eg_rr = calloc(s->Q + 1, sizeof(uint32_t));
+    s->nics = calloc(s->R + 1, sizeof(nic));
+    s->npred_left = malloc(sizeof(uint32_t) * (s->NN + 1));
+    s->cand = calloc(s->NN + 1, sizeof(uint32_t));
+    s->start = malloc(sizeof(uint32_t) * (s->NN + 1));
+    s->end = malloc(sizeof(uint32_t) * (s->NN + 1));
+    s->port_base = calloc(s->NN + 1, sizeof(uint32_t));
+    s->done_max = calloc(s->NN + 1, sizeof(uint32_t));
+    s->outstanding = calloc(s->NN + 1, sizeof(int64_t));
+    for (uint32_t u = 0; u < s->NN; u++) {
+        s->npred_left[u] = s->node_npred[u];
+        s->start[u] = UNSET;
+        s->end[u] = UNSET;
+    }
+    s->nodes_left = s->NN;
+    s->rec_sender = out->rec_sender + rec_off;
+    s->rec_key = out->rec_key + rec_off;
+    s->rec_tick = out->rec_tick + rec_off;
+    s->status = ST_RUNNING;
+
+    uint64_t active = 0;
+    uint32_t now = 0;
+    if (!memory_fits(s->mem, s->gpu_mem)) s->status = ST_OOM;
+    else simulate(s, limit, &active, &now);
+
+    uint32_t endt = 0;
+    int any = 0;
+    for (uint32_t u = 0; u < s->NN; u++) {
+        out->node_start[node_off + u] = s->start[u];
+        out->node_end[node_off + u] = s->end[u];
+        if (s->end[u] != UNSET) { endt = umax32(endt, s->end[u]); any = 1; }
+    }
+    out->status[e] = (uint32_t)s->status;
+    out->end_tick[e] = any ? endt : UNSET;
+    out->now[e] = now;
+    out->pkts_injected[e] = s->pkts_injected;
+    out->pkt_hops[e] = s->pkt_hops;
+    out->pkts_delivered[e] = s->pkts_delivered;
+    out->msgs_delivered[e] = s->msgs_delivered;
+    out->digest[e] = s->digest;
+    out->ticks_active[e] = active;
+    out->rec_count[e] = s->rec_count;
+
+    free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
+    free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
+    free(s->col_base); free(s->node_rank); free(s->node_member);
+    free(s->head); free(s->tail); free(s->head0); free(s->tail0); free(s->slots);
+    free(s->eg_busy); free(s->eg_rr); free(s->nics); free(s->npred_left); free(s->cand);
+    free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
+    return 0;
+}
+
+/* Simulate experiments [e0, e1) of the batch (all of them when e1 == 0),
+ * each to completion or until its clock reaches `limit` ticks.  Per-node
+ * results go to node_start/node_end at the experiment's offset in the
+ * concatenation of all experiments' nodes; flow records at the experiment's
+ * offset in the concatenation of rec_cap-sized blocks. */
+int orc_run(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out)
+{
+    if (b->version != 1) return -1;
+    offs o;
+    o.host = prefix(b->topo_nhosts, b->n_topos);
+    o.sw = prefix(b->topo_nsw, b->n_topos);
+    o.port = prefix(b->topo_nports, b->n_topos);
+    uint32_t *rank = prefix(b->work_nranks, b->n_works);
+    o.rank = rank;
+    o.node = prefix(b->work_nnodes, b->n_works);
+    o.edge = prefix(b->work_nedges, b->n_works);
+    o.coll = prefix(b->work_ncolls, b->n_works);
+    o.memb = prefix(b->work_nmembers, b->n_works);
+    o.a2a = prefix(b->work_na2a, b->n_works);
+    o.a2a_in = prefix(b->work_na2a_in, b->n_works);
+    if (e1 == 0 || e1 > b->n_exps) e1 = b->n_exps;
+    uint64_t node_off = 0, rec_off = 0;
+    for (uint32_t e = 0; e < e1; e++) {
+        if (e >= e0) run_one(b, &o, e, limit, out, node_off, rec_off);
+        node_off += b->work_nnodes[b->exp_work[e]];
+        rec_off += b->exp_rec_cap[e];
+    }
+    free(o.host); free(o.sw); free(o.port); free(rank); free(o.node); free(o.edge);
+    free(o.coll); free(o.memb); free(o.a2a); free(o.a2a_in);
+    return 0;
+}
+
+/* exported for the tests that pin the hash against its published values */
+uint64_t orc_mix64(uint64_t z) { return mix64(z); }

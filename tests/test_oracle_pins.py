@@ -1,0 +1,429 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test states what fixes the expected value: a published constant, a
+closed form from the pages, a hand-traced tick table, or an independent
+evaluator (a longest-path recurrence with no queues in it).
+"""
+import os
+
+import numpy as np
+import pytest
+
+from experiment_network_simulation_gb300 import inputs as I
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def run1(topo, work, **kw):
+    kw.setdefault("tick_ps", 1000)
+    e = I.Experiment(topo, work, **kw)
+    r = O.run(I.Batch([e]).pack())
+    assert r["status"][0] == O.ST_DONE, r["status"]
+    return r
+
+
+# ---------------------------------------------------------------- hash
+def test_mix64_published_splitmix64_outputs():
+    """splitmix64 (Vigna) seeded with 0 yields 0xe220a8397b1dcdaf,
+    0x6e789e6aa1b965f4, 0x06c45d188009454f: the finaliser applied to
+    k * 0x9e3779b97f4a7c15 for k = 1, 2, 3."""
+    g = 0x9E3779B97F4A7C15
+    want = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    assert [O.mix64((k * g) % 2 ** 64) for k in (1, 2, 3)] == want
+
+
+# ---------------------------------------------------------------- lone message
+def chain_topology(n_switch_hops: int, sigmas, deltas):
+    """hosts 0 and 1 joined through a chain of switches; link j has
+    (sigmas[j], deltas[j]); link 0 is host 0's uplink, the last link is the
+    downlink to host 1.  Levels rise along the chain so up/down routing
+    follows it (the last switch reaches host 1 downward)."""
+    t = I.Topology("chain")
+    nsw = n_switch_hops
+    sws = [t.add_switch(nsw - i) for i in range(nsw)]
+    h0, h1 = t.add_hosts(2)
+    # switch levels: host 0 attaches to the top of a descending chain so that
+    # every switch reaches host 1 downward
+    t.attach_host(h0, sws[0], sigmas[0], deltas[0], sigmas[0], deltas[0])
+    for j in range(nsw - 1):
+        t.link(sws[j], sws[j + 1], sigmas[j + 1], deltas[j + 1])
+    t.attach_host(h1, sws[-1], sigmas[-1], deltas[-1], sigmas[-1], deltas[-1])
+    return t
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 40])
+@pytest.mark.parametrize("delta", [0, 1, 12])
+@pytest.mark.parametrize("topo", ["switch", "leafspine", "fattree"])
+def test_lone_message_closed_form(n, delta, topo):
+    """A lone message of n packets over L links of one tick each: the last
+    packet reaches the receiver (n-1) + L*(1+delta) ticks after the first
+    injection (serialisation of the packets behind the head plus, per hop,
+    propagation and per-packet serialisation).  The first injection is tick 1
+    (both ends join at tick 0).  The sender's acknowledgement arrives
+    L*(delta+1) ticks after delivery."""
+    if topo == "switch":
+        t, src, dst, L = I.single_switch(2, 1, delta), 0, 1, 2
+    elif topo == "leafspine":
+        t, src, dst, L = I.leaf_spine(2, 2, 2, delta), 0, 3, 4
+    else:
+        t, src, dst, L = I.fat_tree(4, delta), 0, 15, 6
+    w = I.lone_message(t.n_hosts, src, dst, n * 4096)
+    r = run1(t, w, chunk=1 << 30)
+    done = 1 + (n - 1) + L * (1 + delta)
+    ends = dict(zip(["send", "recv"], r["node_end"][[0, 1]] if src < dst else r["node_end"][[1, 0]]))
+    assert ends["recv"] == done
+    assert ends["send"] == done + L * (delta + 1)
+    assert r["pkts_injected"][0] == n and r["pkts_delivered"][0] == n
+    assert r["pkt_hops"][0] == n * L
+
+
+@pytest.mark.parametrize("n", [1, 5, 30])
+def test_heterogeneous_path_closed_form(n):
+    """Per-link serialisation differs: the bottleneck spaces the packets, so
+    delivery = first injection + (n-1)*max(sigma) + sum(sigma + delta)."""
+    sig, dl = [1, 3, 2, 1], [2, 0, 5, 1]
+    t = chain_topology(3, sig, dl)
+    w = I.lone_message(2, 0, 1, n * 4096)
+    r = run1(t, w, chunk=1 << 30)
+    assert r["node_end"][1] == 1 + (n - 1) * max(sig) + sum(s + d for s, d in zip(sig, dl))
+
+
+def test_credit_loop_needs_delta_plus_two():
+    """Line rate needs queue capacity >= delta + 2 (entries in flight count
+    against the credit).  One slot fewer must make the message slower."""
+    delta, n = 4, 30
+    t = I.single_switch(2, 1, delta)
+    w = I.lone_message(2, 0, 1, n * 4096)
+    full = run1(t, w, chunk=1 << 30, cap=delta + 2)["node_end"][1]
+    short = run1(t, w, chunk=1 << 30, cap=delta + 1)["node_end"][1]
+    assert full == 1 + (n - 1) + 2 * (1 + delta)
+    assert short > full
+
+
+# ---------------------------------------------------------------- hand trace
+def test_incast_hand_trace():
+    gold = {}
+    for line in open(os.path.join(GOLDEN, "incast_cap2_delta1.txt")):
+        if line.strip() and not line.startswith("#"):
+            k, *v = line.split()
+            gold[k] = [int(x) for x in v]
+    t = I.single_switch(3, 1, 1)
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], 3 * 4096)
+    w.collective(I.P2P, [1, 2], 3 * 4096)
+    r = run1(t, w, chunk=1 << 20, cap=2, rec_cap=8)
+    assert list(r["node_end"][:4]) == gold["node_end"]
+    assert sorted(r["rec_tick"][: r["rec_count"][0]]) == gold["delivery_ticks"]
+    assert r["pkts_injected"][0] == gold["packets"][0]
+    assert r["pkt_hops"][0] == gold["packet_hops"][0]
+
+
+# ---------------------------------------------------------------- pipelined broadcast
+@pytest.mark.parametrize("A", [1, 2, 3, 7])
+@pytest.mark.parametrize("K", [1, 2, 5, 16])
+@pytest.mark.parametrize("np_", [1, 3, 8])
+def test_pipelined_broadcast_closed_form(A, K, np_):
+    """AlpaComm section 3.1: with the slice cut in K partitions of t/K each,
+    the broadcast over A receivers takes T_bc = t/K * (K + A - 1).  In ticks
+    (t = K*n_p packets) the last receiver holds the slice at exactly
+    T_bc + A * L*(1+delta): each of the A relay hops adds its path latency
+    L*(1+delta) on top of the page's serialisation-only count (the one-tick
+    dependency and the one-tick rendezvous cancel the -1 of the last packet).
+    A=1 is a lone message; K=1 is store-and-forward."""
+    delta, L = 0, 2
+    t = I.single_switch(A + 1, 1, delta)
+    w = I.relay_chain(A + 1, K * np_ * 4096, K)
+    r = run1(t, w)
+    last = r["node_end"][A]
+    T_bc = np_ * (K + A - 1)
+    assert last == T_bc + A * L * (1 + delta)
+    if A == 1:
+        assert last == 1 + (K * np_ - 1) + L * (1 + delta)
+    assert r["pkt_hops"][0] == A * K * np_ * L
+
+
+def test_pipelined_broadcast_tends_to_t():
+    """T_bc -> t as the per-partition size grows (the page's K >> A regime
+    with hop latency negligible): ratio of simulated time to t = K*n_p."""
+    A, K = 4, 100
+    ratios = []
+    for np_ in (1, 4, 16):
+        t = I.single_switch(A + 1, 1, 0)
+        w = I.relay_chain(A + 1, K * np_ * 4096, K)
+        last = run1(t, w)["node_end"][A]
+        ratios.append(last / (K * np_))
+    assert ratios[0] > ratios[1] > ratios[2]
+    assert ratios[2] < 1 + (A - 1) / K + 0.15
+
+
+# ---------------------------------------------------------------- ring all-reduce
+def ring_longest_path(N, loops, steps, n, lat):
+    """Independent evaluator of a contention-free ring (one channel): message
+    (l,k) of member i starts after its previous message finished injecting and
+    one tick after member i received (l,k-1); it injects n packets on
+    consecutive ticks and reaches member i+1 lat[i] ticks after its last
+    packet.  Returns each member's last delivery tick."""
+    M = loops * steps
+    start = [[0] * M for _ in range(N)]
+    recv = [[0] * M for _ in range(N)]  # recv[i][m]: member i got message m from i-1
+    for m in range(M):
+        k = m % steps
+        for i in range(N):
+            s = 1 if m == 0 else start[i][m - 1] + n
+            if k >= 1:
+                s = max(s, recv[i][m - 1] + 1)
+            start[i][m] = s
+        for i in range(N):
+            recv[(i + 1) % N][m] = start[i][m] + n - 1 + lat[i]
+    return [recv[i][M - 1] for i in range(N)]
+
+
+@pytest.mark.parametrize("kind,steps_of", [(I.AR, lambda N: 2 * (N - 1)),
+                                            (I.RS, lambda N: N - 1),
+                                            (I.AG, lambda N: N - 1)])
+@pytest.mark.parametrize("N,loops,blk", [(2, 1, 3), (4, 2, 2), (8, 3, 5)])
+def test_ring_contention_free_longest_path(kind, steps_of, N, loops, blk):
+    """Ring collectives with one channel on a single switch (every ingress
+    feeds one egress): timing equals the longest path of the message DAG.
+    Sizes make every block equal (S = N * C * loops, C = blk packets)."""
+    delta = 2
+    C = blk * 4096
+    S = N * C * loops
+    t = I.single_switch(N, 1, delta)
+    w = I.single_collective(N, kind, S)
+    r = run1(t, w, nc=1, chunk=C)
+    steps = steps_of(N)
+    got = list(r["node_end"][:N])
+    lat = [2 * (1 + delta)] * N
+    recv = ring_longest_path(N, loops, steps, blk, lat)
+    # a member finishes at max(last delivery to it, ack of its own last message)
+    want = [max(recv[i], recv[(i + 1) % N] + 2 * (delta + 1)) for i in range(N)]
+    assert got == want
+    assert r["pkts_injected"][0] == N * loops * steps * blk
+
+
+def test_ring_leafspine_paths_of_two_lengths():
+    """config-1 fabric with one channel: hosts 0-3 on leaf 0, 4-7 on leaf 1;
+    only 3->4 and 7->0 cross a spine (4 links), the rest use 2 links; each
+    directed link carries one connection, so the longest path is exact."""
+    N, loops, blk, delta = 8, 2, 4, 12
+    C = blk * 4096
+    t = I.leaf_spine(2, 2, 4, delta)
+    w = I.single_collective(N, I.AR, N * C * loops)
+    r = run1(t, w, nc=1, chunk=C)
+    lat = [(4 if i in (3, 7) else 2) * (1 + delta) for i in range(N)]
+    recv = ring_longest_path(N, loops, 2 * (N - 1), blk, lat)
+    ack = [(4 if i in (3, 7) else 2) * (delta + 1) for i in range(N)]
+    want = [max(recv[i], recv[(i + 1) % N] + ack[i]) for i in range(N)]
+    assert list(r["node_end"][:N]) == want
+
+
+def test_ring_allreduce_bandwidth_term():
+    """AutoCCL's ring cost: each rank sends 2(N-1)/N * S bytes, so the
+    all-reduce cannot finish before 2(N-1)/N * S / B; with one chunk per
+    block and growing S the ratio to that bound tends to 1."""
+    N, delta = 8, 1
+    ratios = []
+    for mib in (1, 4, 16):
+        S = mib * I.MIB
+        t = I.single_switch(N, 1, delta)
+        w = I.single_collective(N, I.AR, S)
+        r = run1(t, w, nc=1, chunk=S // N)
+        bound = 2 * (N - 1) * S // N // 4096
+        assert r["pkts_injected"][0] == N * bound
+        end = int(r["node_end"][:N].max())
+        assert end >= bound
+        ratios.append(end / bound)
+    assert ratios[0] > ratios[1] > ratios[2] and ratios[2] < 1.05
+
+
+def test_ring_packet_totals_uneven_sizes():
+    """2(N-1) block sends per loop per rank cover 2(N-1)/N of every loop's
+    bytes; with partial packets rounding up, the total packet count per rank
+    is at least the byte bound and every partition is moved."""
+    N, S = 5, 3 * I.MIB + 12345
+    t = I.single_switch(N, 1, 0)
+    for nc, C in [(1, 64 * I.KIB), (3, 100000), (4, 1 << 20)]:
+        w = I.single_collective(N, I.AR, S)
+        r = run1(t, w, nc=nc, chunk=C)
+        assert r["pkts_injected"][0] >= N * -(-2 * (N - 1) * S // (N * 4096))
+        assert r["pkts_injected"][0] == r["pkts_delivered"][0]
+
+
+# ---------------------------------------------------------------- tree
+@pytest.mark.parametrize("n", [1, 6])
+def test_tree_two_members_closed_form(n):
+    """Binary tree over 2 members (root 0, leaf 1), one chunk: the leaf's
+    chunk goes up (reduce), then the root sends it down (broadcast)."""
+    delta, L = 3, 2
+    t = I.single_switch(2, 1, delta)
+    w = I.single_collective(2, I.AR, n * 4096)
+    r = run1(t, w, algo=I.TREE, nc=1, chunk=1 << 30)
+    up = 1 + (n - 1) + L * (1 + delta)
+    down = up + 1 + (n - 1) + L * (1 + delta)
+    assert r["node_end"][1] == down
+    assert r["node_end"][0] == down + L * (delta + 1)
+
+
+def test_tree_packet_totals():
+    """Each non-root member sends every chunk up once and receives it down
+    once: 2(N-1) * S / pkt packets in all."""
+    N, S = 7, 64 * 4096
+    t = I.single_switch(N, 1, 1)
+    w = I.single_collective(N, I.AR, S)
+    r = run1(t, w, algo=I.TREE, nc=2, chunk=8 * 4096)
+    assert r["pkts_injected"][0] == 2 * (N - 1) * S // 4096
+
+
+# ---------------------------------------------------------------- all-to-all
+@pytest.mark.parametrize("N,n", [(2, 5), (3, 4), (4, 2)])
+def test_alltoall_rotation_closed_form(N, n):
+    """Equal sizes, one channel, one switch: in rotation order every phase is
+    a permutation, so no link is shared; each member's last delivery is at
+    (N-1)*n + L*(1+delta) after the first injection at tick 1, minus one."""
+    delta, L = 1, 2
+    t = I.single_switch(N, 1, delta)
+    w = I.Workload(N)
+    m = {(i, j): n * 4096 for i in range(N) for j in range(N) if i != j}
+    w.collective(I.A2A, list(range(N)), 0, a2a=m)
+    r = run1(t, w, nc=1, chunk=1 << 30)
+    recv = (N - 1) * n + L * (1 + delta)
+    assert list(r["node_end"][:N]) == [recv + L * (delta + 1)] * N
+    assert r["pkts_injected"][0] == N * (N - 1) * n
+
+
+# ---------------------------------------------------------------- DAG
+def test_compute_dag_critical_path():
+    """Compute-only DAGs: the iteration ends at the longest path, each node
+    adding its duration and each edge one tick (topological DP)."""
+    rng = np.random.default_rng(7)
+    R = 3
+    w = I.Workload(R)
+    ids, dur = [], {}
+    for r in range(R):
+        nodes = []
+        for k in range(12):
+            d = int(rng.integers(0, 20))
+            u = w.compute(r, d)     # tick_ps = 1000: ns == ticks
+            dur[u] = d
+            for p in nodes:
+                if rng.random() < 0.3:
+                    w.edge(p, u)
+            nodes.append(u)
+        ids += nodes
+    t = I.single_switch(R, 1, 0)
+    r = run1(t, w)
+    fin = {}
+    preds = {u: [a for a, b in w.edges if b == u] for u in ids}
+    for u in ids:   # creation order is a topological order
+        st = max([fin[p] + 1 for p in preds[u]], default=0)
+        fin[u] = st + dur[u]
+    order = sorted(range(len(w.nodes)), key=lambda i: (w.nodes[i]["rank"], i))
+    assert [int(x) for x in r["node_end"][: len(order)]] == [fin[u] for u in order]
+    assert r["end_tick"][0] == max(fin.values())
+
+
+def test_compute_duration_units_and_hash_range():
+    """Durations in ns become ceil(ns * 1000 / tick_ps) ticks: 50,000 ns at
+    81,920 ps per tick is 610.35 -> 611 ticks.  Hashed durations stay in
+    [lo, hi] (the U[50,500] us range) and vary with the seed."""
+    w = I.Workload(1)
+    w.compute(0, 50_000)
+    t = I.single_switch(1, 1, 0)
+    assert run1(t, w, tick_ps=81920)["node_end"][0] == 611
+    w = I.Workload(1)
+    us = [w.compute(0, 50_000, 500_000, key=k) for k in range(200)]
+    w.chain(*us)   # one at a time: at most 64 nodes may wait to start per rank
+    ends = []
+    for seed in (1, 2):
+        r = run1(t, w, tick_ps=1_000_000, dur_seed=seed)   # 1 tick = 1 us
+        d = r["node_end"][: len(us)].astype(np.int64) - r["node_start"][: len(us)]
+        assert d.min() >= 50 and d.max() <= 500
+        ends.append(d)
+    assert (ends[0] != ends[1]).any()
+    assert 200 < ends[0].mean() < 350
+
+
+def test_intra_server_analytic_model():
+    """Multiverse section 4.1: an intra-server collective takes alpha +
+    bytes/beta once its last member has joined.  alpha=7 ticks, beta = 1
+    tick per 1000 bytes; all-reduce over g=4 moves 2*3/4*S bytes per GPU:
+    S=8000 -> 12000 bytes -> 12 ticks.  Members join at 3, 9, 5, 0."""
+    w = I.Workload(4)
+    pre = [w.compute(r, d) for r, d in enumerate([3, 9, 5, 0])]
+    ids = w.collective(I.AR, [0, 1, 2, 3], 8000, intra=True, alpha=7, beta=(1, 1000))
+    for p, u in zip(pre, ids):
+        w.edge(p, u)
+    t = I.single_switch(4, 1, 0)
+    r = run1(t, w)
+    order = sorted(range(len(w.nodes)), key=lambda i: (w.nodes[i]["rank"], i))
+    end = dict(zip(order, r["node_end"]))
+    # preds end at 3,9,5,0 -> joins at 4,10,6,1; last join 10 -> 10 + 7 + 12
+    assert [end[u] for u in ids] == [29] * 4
+    # reduce-scatter moves half of the all-reduce's bytes: 6000 -> 6 ticks
+    w2 = I.Workload(4)
+    ids2 = w2.collective(I.RS, [0, 1, 2, 3], 8000, intra=True, alpha=7, beta=(1, 1000))
+    r2 = run1(t, w2)
+    assert list(r2["node_end"][:4]) == [0 + 7 + 6] * 4
+
+
+# ---------------------------------------------------------------- memory check
+def test_memory_check_worked_example():
+    """GPT-3 13B, TP 8, PP 4, 10 layers per stage, 8 micro-batches, s=2048,
+    b=1, h=5120, a=40.  By hand: weights+grads+Adam 16 * 13e9 / 32 =
+    6,500,000,000 bytes; activations per layer 2048*5120*(34 + 5*40*2048/5120)
+    = 10,485,760 * 114 = 1,195,376,640 bytes, times 10 layers times min(8,4)
+    in-flight micro-batches / TP 8 = 5,976,883,200 bytes.  Total
+    12,476,883,200 bytes: fits in exactly that much memory, not one byte less."""
+    w = I.Workload(1)
+    w.compute(0, 5)
+    w.set_memory_model(13_000_000_000, 8, 4, 10, 8, 2048, 1, 5120, 40)
+    t = I.single_switch(1, 1, 0)
+    ok = I.Experiment(t, w, tick_ps=1000, gpu_mem=12_476_883_200)
+    oom = I.Experiment(t, w, tick_ps=1000, gpu_mem=12_476_883_199)
+    r = O.run(I.Batch([ok, oom]).pack())
+    assert list(r["status"]) == [O.ST_DONE, O.ST_OOM]
+    assert r["node_end"][1] == O.UNSET
+
+
+# ---------------------------------------------------------------- invariants
+def test_config1_invariants():
+    """Config 1: 7,168 packets per rank (2*7/8 * 16 MiB / 4 KiB) whatever NC
+    and chunk; 6 ring connections use 2 links and 2 use 4 links, so
+    packet-hops are 2.5 per packet."""
+    b = I.config1()
+    r = O.run(b.pack())
+    assert (r["status"] == O.ST_DONE).all()
+    assert (r["pkts_injected"] == 8 * 7168).all()
+    assert (r["pkts_delivered"] == r["pkts_injected"]).all()
+    assert (r["pkt_hops"] == 8 * 7168 * 5 // 2).all()
+    assert (r["end_tick"] >= 7168).all()
+
+
+def test_config2_invariants():
+    b = I.config2(n_exp=24)
+    r = O.run(b.pack())
+    assert (r["status"] == O.ST_DONE).all()
+    for e, ex in enumerate(b.experiments):
+        A, K, mib = ex.label["A"], ex.label["K"], ex.label["mib"]
+        S = mib * I.MIB
+        per_part = [-(-(S // K + (k < S % K)) // 4096) for k in range(K)]
+        assert r["pkts_injected"][e] == A * sum(per_part)
+        assert r["pkt_hops"][e] == 2 * r["pkts_injected"][e]
+        # at least t = the slice's serialisation, and within the pipelined bound
+        assert r["end_tick"][e] >= sum(per_part)
+
+
+def test_deadlock_is_detected():
+    """A collective whose receiver never joins (its predecessor is a member
+    of a collective that the other side never reaches) is a deadlock, not a
+    hang: two ranks each wait in a different order."""
+    w = I.Workload(2)
+    a = w.collective(I.P2P, [0, 1], 4096)
+    b = w.collective(I.P2P, [1, 0], 4096)
+    w.edge(b[1], a[0])   # rank 0: receive b before sending a
+    w.edge(a[1], b[0])   # rank 1: receive a before sending b
+    t = I.single_switch(2, 1, 0)
+    r = O.run(I.Batch([I.Experiment(t, w, tick_ps=1000, chunk=1 << 20)]).pack())
+    assert r["status"][0] == O.ST_DEADLOCK
