@@ -1,0 +1,219 @@
+/*
+ * mv.h -- C ABI of the GB300 single-process multi-experiment (SPME) packet
+ * simulator of LLM-training collective traffic.
+ *
+ * Source of the operation: "Accelerating Design Space Exploration for LLM
+ * Training Systems with Multi-experiment Parallel Simulation" (Multiverse,
+ * NSDI'25).  Section 3.1 (architecture): the user describes the workload,
+ * the collective-library parameters and the topology, lists the experiments,
+ * and the simulator runs them all in one process on one GPU.  Section 3.2
+ * fixes the per-step system order (Schedule, AnalyticalSys, SendSys,
+ * NICSndSys, ForwardSys, TransmitSys, NICRcvSys, ACKSys), section 3.3 the
+ * per-experiment columnar state, section 4.2 the pull-based forwarding and
+ * section 4.3 the single megakernel launched once per batch.  The collective
+ * parameters <algorithm, NC, C> are AutoCCL's (section 2.3); the pipelined
+ * broadcast is from "On Optimizing the Communication of Model Parallelism"
+ * (section 3.1).
+ *
+ * Three calls make the path: mv_create (upload a batch of experiments),
+ * mv_run (advance every experiment by up to N ticks in one persistent
+ * kernel launch), mv_results (per-experiment, per-node and per-message
+ * results).  All times are integer ticks; one tick is one packet
+ * serialisation time at the experiment's base link rate.
+ *
+ * Memory: the library never allocates device memory.  The caller gives
+ * mv_create a device workspace of at least mv_workspace_bytes() bytes and
+ * keeps it alive until mv_destroy.  Host arrays in mv_batch_desc are read
+ * during mv_create only.  Every call is bound to the stream given to
+ * mv_create; a context is not thread-safe.
+ *
+ * Errors: every call returns an MV_* status code (negative = error, the
+ * context is unchanged unless stated otherwise); mv_strerror names it.
+ */
+#ifndef MV_H
+#define MV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define MV_OK 0              /* every experiment finished (or stopped: OOM,
+                                deadlock, overflow)                          */
+#define MV_INCOMPLETE 1      /* the tick budget ran out; call mv_run again   */
+#define MV_EINVAL (-1)       /* malformed descriptor or argument             */
+#define MV_ENOMEM (-2)       /* workspace smaller than mv_workspace_bytes()  */
+#define MV_ECUDA (-3)        /* a CUDA call failed (launch, copy, sync)      */
+#define MV_ETIMEOUT (-4)     /* the grid barrier waited past its limit; the
+                                kernel returned, results are invalid         */
+#define MV_EOVERFLOW (-5)    /* a size or tick count exceeds 32-bit limits   */
+
+/* ---- per-experiment status (mv_results.status) ----------------------- */
+#define MV_EXP_DONE 0        /* every DAG node completed                     */
+#define MV_EXP_RUNNING 1     /* stopped by the tick budget                   */
+#define MV_EXP_OOM 2         /* failed the pre-run GPU memory check          */
+#define MV_EXP_DEADLOCK 3    /* nothing in flight, nothing scheduled, not done */
+#define MV_EXP_OVERFLOW 4    /* a per-rank table (lanes 64, receive counters
+                                128, pending nodes 64, running collectives 16)
+                                or a tick value overflowed                   */
+#define MV_EXP_ERROR 5       /* unroutable packet or inconsistent schedule   */
+
+/* node kinds, collective kinds and algorithms used in the descriptor */
+#define MV_NODE_COMPUTE 0
+#define MV_NODE_INTRA 1      /* intra-server collective: alpha + bytes/beta  */
+#define MV_NODE_NET 2        /* membership in a network collective           */
+#define MV_COLL_ALLREDUCE 0
+#define MV_COLL_REDUCESCATTER 1
+#define MV_COLL_ALLGATHER 2
+#define MV_COLL_RELAY 3      /* pipelined broadcast along the member order   */
+#define MV_COLL_P2P 4        /* member 0 sends to member 1                   */
+#define MV_COLL_ALLTOALL 5   /* explicit per-pair byte counts                */
+#define MV_ALGO_RING 0
+#define MV_ALGO_TREE 1       /* all-reduce only; other kinds use the ring    */
+
+#define MV_UNSET 0xFFFFFFFFu /* tick value of "never happened"              */
+
+/*
+ * Batch descriptor.  Flat arrays, concatenated over topologies, workloads
+ * and experiments in that order.  Indices stored inside a topology's arrays
+ * are local to that topology; inside a workload's, local to that workload.
+ * All pointers are host pointers, read only during mv_create.
+ *
+ * Topology t (n_topos of them): topo_nhosts[t] hosts (one NIC each, host h
+ * = rank h of any workload run on it), topo_nsw[t] switches, topo_nports[t]
+ * switch ports.  Per switch: sw_nports (<= 64), sw_level (1 = edge, higher
+ * = closer to the core).  Per port q (switch-major): port_peer[q] >= 0 is
+ * the peer switch port, < 0 is host -(peer+1); port_sigma/port_delta
+ * describe the link leaving the port (serialisation ticks >= 1, propagation
+ * ticks).  Per host: host_port (the switch port it is wired to) and the
+ * uplink's host_sigma/host_delta.
+ *
+ * Workload w: work_nranks[w] ranks; rank_nnodes gives each rank's node
+ * count (nodes are numbered rank-major).  Per node: node_kind, node_arg (the
+ * collective index for INTRA/NET nodes), node_npred, node_nsucc (successor
+ * lists concatenated in succ[], same rank only), node_dur_lo/hi (compute
+ * duration in ns; hi > lo draws from [lo, hi] with the experiment's
+ * duration seed and node_dur_key).  Per collective: coll_kind, coll_intra
+ * (1 = analytic), coll_bytes, coll_nmembers, coll_parts (relay partitions
+ * K), coll_alpha (ticks, >= 1 for intra), coll_beta_num/den (ticks per
+ * byte).  Per member: member_rank, member_node; all-to-all rows
+ * (member_a2a_n entries of a2a_dst/a2a_bytes, in rotation order from the
+ * next member) and columns (member_a2a_in_n entries of
+ * a2a_in_src/a2a_in_bytes).  mem: 10 uint64 per workload: params, tp, pp,
+ * layers per stage, micro-batches, seq, batch, hidden, heads, enabled.
+ *
+ * Experiment e: exp_topo, exp_work, exp_algo, exp_nc (channels, 1..1024),
+ * exp_chunk (bytes), exp_pkt (packet bytes), exp_cap (queue slots, 2..1024),
+ * exp_tick_ps, exp_dur_seed, exp_ecmp_seed, exp_gpu_mem (bytes per GPU),
+ * exp_rec_cap (per-message completion records kept, 0 = none).
+ */
+typedef struct mv_batch_desc {
+    uint32_t version;                 /* 1 */
+    uint32_t n_topos, n_works, n_exps;
+    const uint32_t *topo_nhosts, *topo_nsw, *topo_nports;
+    const uint32_t *sw_nports, *sw_level;
+    const int32_t *port_peer;
+    const uint32_t *port_sigma, *port_delta, *host_port, *host_sigma, *host_delta;
+    const uint32_t *work_nranks, *work_nnodes, *work_nedges, *work_ncolls,
+        *work_nmembers, *work_na2a, *work_na2a_in;
+    const uint32_t *rank_nnodes, *node_kind, *node_arg, *node_npred, *node_nsucc,
+        *node_dur_lo, *node_dur_hi, *node_dur_key, *succ;
+    const uint32_t *coll_kind, *coll_intra;
+    const uint64_t *coll_bytes;
+    const uint32_t *coll_nmembers, *coll_parts, *coll_alpha, *coll_beta_num,
+        *coll_beta_den, *member_rank, *member_node, *member_a2a_n, *a2a_dst;
+    const uint64_t *a2a_bytes;
+    const uint32_t *member_a2a_in_n, *a2a_in_src;
+    const uint64_t *a2a_in_bytes;
+    const uint64_t *mem;
+    const uint32_t *exp_topo, *exp_work, *exp_algo, *exp_nc;
+    const uint64_t *exp_chunk;
+    const uint32_t *exp_pkt, *exp_cap, *exp_tick_ps;
+    const uint64_t *exp_dur_seed, *exp_ecmp_seed, *exp_gpu_mem;
+    const uint32_t *exp_rec_cap;
+} mv_batch_desc;
+
+/*
+ * Results, written by mv_results into caller-owned HOST buffers (any
+ * pointer may be NULL to skip that field).  Per experiment (n_exps): status
+ * (MV_EXP_*), end_tick (latest node end, the iteration time; MV_UNSET if no
+ * node ended), now (the experiment's clock), packets injected, packet-hops
+ * (one packet placed on one link), packets delivered, messages delivered,
+ * digest (order-independent 64-bit sum over delivered messages of a hash of
+ * (sender node, connection key, delivery tick)), rec_count (records
+ * produced; only the first exp_rec_cap are kept).  Per node, concatenated
+ * over experiments in batch order (sizes from mv_result_sizes): start and
+ * end tick.  Per-message records, concatenated in blocks of exp_rec_cap:
+ * sender node, 24-bit connection key, delivery tick, in no particular order.
+ */
+typedef struct mv_results_view {
+    uint32_t *status, *end_tick, *now;
+    uint64_t *pkts_injected, *pkt_hops, *pkts_delivered, *msgs_delivered, *digest;
+    uint32_t *rec_count;
+    uint32_t *node_start, *node_end;
+    uint32_t *rec_sender, *rec_key, *rec_tick;
+} mv_results_view;
+
+typedef struct mv_ctx mv_ctx;
+
+/* Options of one mv_run call.  barrier_timeout_ns bounds every grid-barrier
+ * wait (0 = 5 s); past it the kernel sets MV_ETIMEOUT and returns.
+ * fault_skip_block/fault_skip_step (test hook, -1 = off): that block skips
+ * its arrival at that step's barrier, which must end in MV_ETIMEOUT. */
+typedef struct mv_run_opts {
+    uint64_t barrier_timeout_ns;
+    int32_t fault_skip_block;
+    int32_t fault_skip_step;
+    uint32_t grid_blocks;       /* 0 = all co-resident blocks */
+} mv_run_opts;
+
+/* Workspace bytes mv_create needs for this batch (validates the
+ * descriptor).  Returns MV_OK, MV_EINVAL or MV_EOVERFLOW. */
+int mv_workspace_bytes(const mv_batch_desc *desc, uint64_t *bytes);
+
+/* Sizes of the concatenated per-node and per-record result arrays. */
+int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_records);
+
+/* Validate the batch, lay it out in the caller's device workspace
+ * (`dev_workspace`, `ws_bytes`, 256-byte aligned), upload it on `stream`
+ * (a cudaStream_t, NULL = legacy default stream), build the routing tables,
+ * run the memory check and put every experiment at tick 0.  On success
+ * *out owns a host-side context (free with mv_destroy); the workspace stays
+ * the caller's. */
+int mv_create(const mv_batch_desc *desc, void *dev_workspace, uint64_t ws_bytes,
+              void *stream, mv_ctx **out);
+
+/* Advance every unfinished experiment by at most max_ticks ticks of its own
+ * clock, in ONE cooperative launch of the persistent megakernel, and wait
+ * for it.  State stays on the device, so run(a) then run(b) equals
+ * run(a + b).  *steps_done (may be NULL) receives the number of grid-wide
+ * steps executed.  Returns MV_OK when no experiment is still running,
+ * MV_INCOMPLETE when some hit the budget, or an error. */
+int mv_run(mv_ctx *ctx, uint32_t max_ticks, uint64_t *steps_done);
+int mv_run_ex(mv_ctx *ctx, uint32_t max_ticks, const mv_run_opts *opts,
+              uint64_t *steps_done);
+
+/* Put every experiment back to tick 0 (clear the dynamic state, rebuild the
+ * routing tables, rerun the memory check) without re-uploading the batch.
+ * Enqueued on the context's stream; does not wait. */
+int mv_reset(mv_ctx *ctx);
+
+/* Device time, in ms, of the megakernel launch of the last mv_run, taken
+ * with CUDA events recorded on the context's stream around that launch. */
+int mv_last_run_ms(mv_ctx *ctx, float *ms);
+
+/* Copy the results to the caller's host buffers (blocking on the stream). */
+int mv_results(mv_ctx *ctx, const mv_results_view *out);
+
+/* Free the host context.  The workspace is not touched. */
+int mv_destroy(mv_ctx *ctx);
+
+const char *mv_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MV_H */

@@ -1,0 +1,89 @@
+"""The C-ABI library loads, exports every entry point its header declares,
+and validates descriptors on the host (no GPU needed for any of this)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from experiment_network_simulation_gb300 import inputs as I
+from experiment_network_simulation_gb300 import mv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "mv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mv_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    lib = mv.library()
+    names = header_functions()
+    assert "mv_create" in names and "mv_run" in names and "mv_results" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_bytes_and_result_sizes():
+    b = I.config1()
+    p = b.pack()
+    n = mv.workspace_bytes(p)
+    assert n > 0 and n % 256 == 0
+    d, _ = mv.make_desc(p)
+    nn, nr = C.c_uint64(), C.c_uint64()
+    assert mv.library().mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)) == mv.MV_OK
+    assert nn.value == 16 * 8 and nr.value == 0
+
+
+def _bad(p, **changes):
+    q = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in p.items()}
+    for k, f in changes.items():
+        f(q[k]) if callable(f) else q.__setitem__(k, f)
+    d, _ = mv.make_desc(q)
+    n = C.c_uint64()
+    return mv.library().mv_workspace_bytes(C.byref(d), C.byref(n))
+
+
+def test_descriptor_validation():
+    p = I.config1().pack()
+    assert _bad(p) == mv.MV_OK
+    assert _bad(p, version=2) == mv.MV_EINVAL
+
+    def asym(a): a[0] = a[1]       # peer of a port no longer points back
+    assert _bad(p, port_peer=asym) == mv.MV_EINVAL
+
+    def zero_sigma(a): a[3] = 0
+    assert _bad(p, port_sigma=zero_sigma) == mv.MV_EINVAL
+
+    def nc0(a): a[0] = 0
+    assert _bad(p, exp_nc=nc0) == mv.MV_EINVAL
+
+    def cap1(a): a[0] = 1
+    assert _bad(p, exp_cap=cap1) == mv.MV_EINVAL
+
+    def topo_oob(a): a[0] = 7
+    assert _bad(p, exp_topo=topo_oob) == mv.MV_EINVAL
+
+    def huge(a): a[0] = 1 << 41
+    assert _bad(p, coll_bytes=huge) == mv.MV_EOVERFLOW
+
+    def pred(a): a[0] += 1         # predecessor count no longer matches the edges
+    assert _bad(p, node_npred=pred) == mv.MV_EINVAL
+
+
+def test_too_many_switch_ports_rejected():
+    t = I.single_switch(65, 1, 0)
+    w = I.lone_message(2, 0, 1, 4096)
+    p = I.Batch([I.Experiment(t, w, chunk=1 << 20)]).pack()
+    d, _ = mv.make_desc(p)
+    n = C.c_uint64()
+    assert mv.library().mv_workspace_bytes(C.byref(d), C.byref(n)) == mv.MV_EINVAL
+
+
+def test_strerror_names_codes():
+    lib = mv.library()
+    for code in (0, 1, -1, -2, -3, -4, -5):
+        assert lib.mv_strerror(code)
