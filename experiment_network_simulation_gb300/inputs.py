@@ -481,3 +481,221 @@ def config2(seed: int = 0, n_exp: int = 256) -> Batch:
         exps.append(Experiment(topos[a], work, RING, 1, 0, 4096, 64, tk,
                                label=dict(A=a, K=k, mib=int(sizes[j]))))
     return Batch(exps, "pipelined-broadcast-10G")
+
+
+# --------------------------------------------------------------------------
+# GPT-style 1F1B training iteration (config 3 / config 5 workload)
+# --------------------------------------------------------------------------
+def gpt_1f1b(n_servers: int, gpus: int, pp: int, layers: int, micro: int, seq: int,
+             hidden: int, heads: int, params: int, tick: int, batch: int = 1,
+             dur_ns=(50_000, 500_000), tp_alpha_ns: int = 10_000,
+             tp_bytes_per_tick: int = 36_864) -> Workload:
+    """One training iteration, per GPU, TP = gpus (one server), PP = pp
+    consecutive blocks of servers, DP = the servers of a stage, rail-aligned.
+
+    Per layer and micro-batch, forward and backward are each compute, TP
+    all-reduce, compute, TP all-reduce (the TP all-reduces are intra-server,
+    analytic).  Stages pass s*b*h*2/TP bytes per GPU to the neighbouring
+    stage's same GPU (pipeline p2p).  A receive sits in the GPU's chain; a
+    send branches off it (posted asynchronously, as the 1F1B steady state
+    posts its send and receive together), so the next op does not wait for
+    the send to be delivered.  Each layer's data-parallel gradient
+    all-reduce (12h^2/TP parameters, 2 bytes each) starts after that layer's
+    last backward, chained in backward order on a second stream so that it
+    overlaps the rest of the backward pass.  Micro-batches follow 1F1B: stage
+    i runs min(pp-i-1, m) warm-up forwards, then alternates, then drains.
+    Compute durations are drawn from dur_ns per (stage, micro-batch, layer,
+    direction, part), the same for every GPU of a stage."""
+    assert n_servers % pp == 0 and layers % pp == 0
+    dp = n_servers // pp
+    lps = layers // pp
+    R = n_servers * gpus
+    w = Workload(R, f"gpt-{n_servers}x{gpus}-pp{pp}-dp{dp}")
+    act_tp = seq * batch * hidden * 2                # TP all-reduce of the activations
+    act_pp = act_tp // gpus                          # pipeline p2p per GPU
+    dp_bytes = 12 * hidden * hidden // gpus * 2      # gradient all-reduce per layer per GPU
+    alpha = max(1, -(-tp_alpha_ns * 1000 // tick))
+
+    def rank(srv, g):
+        return srv * gpus + g
+
+    # pipeline p2p instances: (kind, boundary, micro, dp index, gpu) -> (send, recv)
+    p2p = {}
+    for b in range(pp - 1):
+        for j in range(micro):
+            for d in range(dp):
+                for g in range(gpus):
+                    lo, hi = rank(b * dp + d, g), rank((b + 1) * dp + d, g)
+                    p2p[("act", b, j, d, g)] = tuple(w.collective(P2P, [lo, hi], act_pp))
+                    p2p[("grad", b, j, d, g)] = tuple(w.collective(P2P, [hi, lo], act_pp))
+    # data-parallel all-reduces: (stage, layer, gpu) -> member nodes by dp index
+    dpar = {}
+    for st in range(pp):
+        for l in range(lps):
+            for g in range(gpus):
+                dpar[(st, l, g)] = w.collective(AR, [rank(st * dp + d, g) for d in range(dp)],
+                                                dp_bytes)
+    for st in range(pp):
+        wu = min(pp - st - 1, micro)
+        prog = [("F", j) for j in range(wu)]
+        for j in range(micro - wu):
+            prog += [("F", wu + j), ("B", j)]
+        prog += [("B", j) for j in range(micro - wu, micro)]
+        for d in range(dp):
+            srv = st * dp + d
+            chains = [[] for _ in range(gpus)]
+            sends = [[] for _ in range(gpus)]        # (chain position, send node)
+            layer_end = [[None] * lps for _ in range(gpus)]
+
+            def tp_step(fb, j, l, part):
+                key = (((st * micro + j) * lps + l) * 2 + (fb == "B")) * 2 + part
+                for g in range(gpus):
+                    chains[g].append(w.compute(rank(srv, g), dur_ns[0], dur_ns[1], key=key))
+                ids = w.collective(AR, [rank(srv, g) for g in range(gpus)], act_tp, intra=True,
+                                   alpha=alpha, beta=(1, tp_bytes_per_tick))
+                for g in range(gpus):
+                    chains[g].append(ids[g])
+
+            for fb, j in prog:
+                if fb == "F":
+                    if st > 0:
+                        for g in range(gpus):
+                            chains[g].append(p2p[("act", st - 1, j, d, g)][1])
+                    for l in range(lps):
+                        tp_step("F", j, l, 0)
+                        tp_step("F", j, l, 1)
+                    if st < pp - 1:
+                        for g in range(gpus):
+                            sends[g].append((chains[g][-1], p2p[("act", st, j, d, g)][0]))
+                else:
+                    if st < pp - 1:
+                        for g in range(gpus):
+                            chains[g].append(p2p[("grad", st, j, d, g)][1])
+                    for l in reversed(range(lps)):
+                        tp_step("B", j, l, 0)
+                        tp_step("B", j, l, 1)
+                        if j == micro - 1:
+                            for g in range(gpus):
+                                layer_end[g][l] = chains[g][-1]
+                    if st > 0:
+                        for g in range(gpus):
+                            sends[g].append((chains[g][-1], p2p[("grad", st - 1, j, d, g)][0]))
+            for g in range(gpus):
+                w.chain(*chains[g])
+                for after, node in sends[g]:
+                    w.edge(after, node)
+                prev = None
+                for l in reversed(range(lps)):        # gradient all-reduces, backward order
+                    node = dpar[(st, l, g)][d]
+                    w.edge(layer_end[g][l], node)
+                    if prev is not None:
+                        w.edge(prev, node)
+                    prev = node
+    w.set_memory_model(params, gpus, pp, lps, micro, seq, batch, hidden, heads)
+    return w
+
+
+def config3(n_exp: int | None = None) -> Batch:
+    """GPT-3 13B shape (40 layers, h 5120, 40 heads, s 2048, 8 micro-batches)
+    on 128 servers x 8 GPUs: TP 8 (analytic), PP 4, DP 32, k=16 fat-tree at
+    400 Gbps; 500 experiments over algorithm x NC x chunk x duration seed."""
+    tk = tick_ps(4096, 400)
+    topo = fat_tree(16, delta=delay_ticks(1_000_000, tk), hosts_per_edge=8)
+    work = gpt_1f1b(128, 8, 4, 40, 8, 2048, 5120, 40, 13_000_000_000, tk)
+    exps = []
+    for algo in (RING, TREE):
+        for nc in (1, 2, 4, 8, 16):
+            for ch in (64 * KIB, 128 * KIB, 256 * KIB, 512 * KIB, 1 * MIB):
+                for seed in range(5):
+                    exps.append(Experiment(topo, work, algo, nc, ch, 4096, 64, tk, dur_seed=seed,
+                                           label=dict(algo=algo, nc=nc, chunk=ch, seed=seed)))
+    if n_exp is not None:
+        exps = exps[:n_exp]
+    return Batch(exps, "gpt13b-1f1b-128x8-fattree16")
+
+
+def gpt_small(algo: int = RING, nc: int = 2, chunk: int = 64 * KIB, seeds=(0, 1),
+              layers: int = 4, micro: int = 3) -> Batch:
+    """The config-3 DAG shape at test size: 8 servers x 2 GPUs on a k=4
+    fat-tree, PP 2, DP 4, small activations."""
+    tk = tick_ps(4096, 400)
+    topo = fat_tree(4, delta=3, hosts_per_edge=2)
+    work = gpt_1f1b(8, 2, 2, layers, micro, 256, 512, 8, 50_000_000, tk,
+                    dur_ns=(2_000, 20_000), tp_alpha_ns=2_000)
+    exps = [Experiment(topo, work, algo, nc, chunk, 4096, 64, tk, dur_seed=s) for s in seeds]
+    return Batch(exps, "gpt-small")
+
+
+# --------------------------------------------------------------------------
+# MoE dispatch / combine (config 4)
+# --------------------------------------------------------------------------
+def moe_traffic(seed: int, n_ranks: int = 512, tokens: int = 128, experts: int = 256,
+                topk: int = 8, hidden: int = 7168, zipf: float = 1.2):
+    """Per-(source, destination) dispatch bytes.  Expert e lives on rank 2e;
+    expert popularity p_e ~ (pi(e)+1)^-zipf with pi a seeded permutation;
+    each token picks topk distinct experts by Gumbel-top-k on log p."""
+    rng = np.random.default_rng(seed)
+    pi = rng.permutation(experts)
+    logp = -zipf * np.log(pi + 1.0)
+    g = rng.gumbel(size=(n_ranks, tokens, experts))
+    pick = np.argpartition(-(logp[None, None, :] + g), topk, axis=2)[:, :, :topk]
+    counts = np.zeros((n_ranks, experts), np.int64)
+    for r in range(n_ranks):
+        np.add.at(counts[r], pick[r].ravel(), 1)
+    per_token = hidden * 2
+    byte = np.zeros((n_ranks, n_ranks), np.int64)
+    stride = max(1, n_ranks // experts)
+    byte[:, np.arange(experts) * stride] = counts * per_token
+    return byte
+
+
+def moe_workload(byte: np.ndarray, gpus: int, alpha: int, beta=(1, 36_864)) -> Workload:
+    """Dispatch then combine.  Same GPU: no traffic; same server: one analytic
+    intra-server exchange per server (the largest per-GPU share); else network
+    all-to-all.  A rank's combine (reverse sizes) starts once its dispatch
+    parts are done (the combine-receive barrier of the MoE kernels)."""
+    R = byte.shape[0]
+    w = Workload(R, "moe")
+    srv = np.arange(R) // gpus
+    same = srv[:, None] == srv[None, :]
+    net = np.where(same, 0, byte)
+    intra = np.where(same & ~np.eye(R, dtype=bool), byte, 0)
+    stages = []
+    for M_net, M_in in ((net, intra), (net.T, intra.T)):
+        m = {(i, j): int(M_net[i, j]) for i, j in zip(*np.nonzero(M_net))}
+        ids_net = w.collective(A2A, list(range(R)), 0, a2a=m)
+        ids_in = [None] * R
+        for s in range(R // gpus):
+            members = list(range(s * gpus, (s + 1) * gpus))
+            b = int(M_in[members].sum(axis=1).max())
+            ids = w.collective(A2A, members, b, intra=True, alpha=alpha, beta=beta)
+            for r, u in zip(members, ids):
+                ids_in[r] = u
+        stages.append((ids_net, ids_in))
+    for r in range(R):
+        for a in (stages[0][0][r], stages[0][1][r]):
+            for b in (stages[1][0][r], stages[1][1][r]):
+                w.edge(a, b)
+    return w
+
+
+def config4(n_seeds: int = 256, n_exp: int | None = None) -> Batch:
+    """MoE dispatch/combine, 64 servers x 8 GPUs, 128 tokens per rank, hidden
+    7168 bf16, top-8 of 256 experts, Zipf(1.2); four 512-NIC fabrics x
+    n_seeds router seeds; NC 4, chunk 512 KiB."""
+    tk = tick_ps(4096, 400)
+    dl = delay_ticks(1_000_000, tk)
+    topos = [leaf_spine(16, 32, 32, dl),                      # 2-tier 1:1
+             leaf_spine(16, 16, 32, dl),                      # 2-tier 2:1
+             fat_tree(16, dl, hosts_per_edge=4),              # 3-tier, half populated
+             rail_optimized(64, 8, 32, 32, dl)]               # rail-optimised 2-tier
+    alpha = max(1, -(-10_000 * 1000 // tk))
+    exps = []
+    for seed in range(n_seeds):
+        work = moe_workload(moe_traffic(seed), 8, alpha)
+        for ti, t in enumerate(topos):
+            exps.append(Experiment(t, work, RING, 4, 512 * KIB, 4096, 64, tk, dur_seed=seed,
+                                   label=dict(topo=ti, seed=seed)))
+            if n_exp is not None and len(exps) >= n_exp:
+                return Batch(exps, "moe-dispatch-combine-512")
+    return Batch(exps, "moe-dispatch-combine-512")
