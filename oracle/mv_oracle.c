@@ -119,6 +119,7 @@ typedef struct nic {
     uint32_t port_node[NPORT];
     uint32_t pend_node[NPEND], pend_start[NPEND];
     int n_pend;
+    int n_lanes;          /* lanes in use (skip the scan when none)        */
     uint32_t act[NACT];
     int n_act;
 } nic;
@@ -156,6 +157,7 @@ typedef struct sim {
     uint32_t *head, *tail, *head0, *tail0;
     pkt *slots;                     /* nf * cap */
     uint32_t *eg_busy, *eg_rr;      /* Q */
+    uint32_t *sw_queued;            /* S: packets in the switch's ingress queues */
     nic *nics;                      /* R */
     uint32_t *npred_left, *cand, *start, *end, *port_base, *done_max;
     int64_t *outstanding;
@@ -485,6 +487,7 @@ static void net_join(sim *s, uint32_t r, uint32_t u, uint32_t t)
             L->node = u; L->member = i; L->chan = ch; L->kind = k;
             L->m = 0; L->nmsg = nm;
             L->pkts_left = lane_setup(s, L);
+            n->n_lanes++;
             out += nm;
         }
     }
@@ -503,7 +506,9 @@ static void act_add(sim *s, uint32_t r, uint32_t u)
 {
     nic *n = &s->nics[r];
     if (n->n_act >= NACT) { fail(s, ST_OVERFLOW); return; }
-    n->act[n->n_act++] = u;
+    int j = n->n_act++;                   /* insert in node order */
+    while (j > 0 && n->act[j - 1] > u) { n->act[j] = n->act[j - 1]; j--; }
+    n->act[j] = u;
 }
 
 static int cmp_u32(const void *a, const void *b)
@@ -515,14 +520,17 @@ static int cmp_u32(const void *a, const void *b)
 static void dag_step(sim *s, uint32_t r, uint32_t t)
 {
     nic *n = &s->nics[r];
-    /* (a) running collectives, in node order: has this member finished? */
-    qsort(n->act, n->n_act, sizeof(uint32_t), cmp_u32);
-    uint32_t keep[NACT];
+    if (n->n_act == 0) {                  /* nothing running: anything due now? */
+        int due = 0;
+        for (int k = 0; k < n->n_pend && !due; k++) due = n->pend_start[k] <= t;
+        if (!due) return;
+    }
+    /* (a) running collectives, in node order (the list is kept sorted):
+     * has this member finished? */
     int nk = 0, na = n->n_act;
-    uint32_t acts[NACT];
-    memcpy(acts, n->act, sizeof(uint32_t) * na);
     for (int a = 0; a < na; a++) {
-        uint32_t u = acts[a], c = coll_of(s, u);
+        uint32_t u = n->act[a], c = coll_of(s, u);
+        int fin = 0;
         if (s->node_kind[u] == K_INTRA) {
             uint32_t N = nmemb(s, c), b = 0, ok = 1;
             for (uint32_t j = 0; j < N && ok; j++) {
@@ -530,18 +538,14 @@ static void dag_step(sim *s, uint32_t r, uint32_t t)
                 if (st == UNSET || st >= t) ok = 0;
                 else b = umax32(b, st);
             }
-            if (ok) complete(s, u, b + intra_ticks(s, c));
-            else keep[nk++] = u;
-        } else {
-            if (s->outstanding[u] == 0) {
-                free_ports(s, r, u);
-                complete(s, u, s->done_max[u]);
-            } else {
-                keep[nk++] = u;
-            }
+            if (ok) { complete(s, u, b + intra_ticks(s, c)); fin = 1; }
+        } else if (s->outstanding[u] == 0) {
+            free_ports(s, r, u);
+            complete(s, u, s->done_max[u]);
+            fin = 1;
         }
+        if (!fin) n->act[nk++] = u;
     }
-    memcpy(n->act, keep, sizeof(uint32_t) * nk);
     n->n_act = nk;
     /* (b) start the nodes scheduled for this tick, in node order */
     uint32_t now_nodes[NPEND];
@@ -602,6 +606,7 @@ static void push(sim *s, uint32_t f, const pkt *p)
 {
     *slot(s, f, s->tail[f]) = *p;
     s->tail[f]++;
+    if (f < s->Q) s->sw_queued[s->port_sw[f]]++;
 }
 
 /* Switch forwarding (Multiverse section 4.2, pull-based): plan = for each
@@ -610,19 +615,23 @@ static void push(sim *s, uint32_t f, const pkt *p)
  * pointer and takes the first head planned for it. */
 static void forward(sim *s, uint32_t w, uint32_t t)
 {
+    if (s->sw_queued[w] == 0) return;     /* nothing queued: nothing to plan */
     uint32_t P = s->sw_nports[w], base = s->sw_base[w];
     int32_t tgt[256];
+    uint32_t wanted[256];                 /* how many heads want each egress */
+    memset(wanted, 0, sizeof(uint32_t) * P);
     for (uint32_t p = 0; p < P; p++) {
         pkt *h = ready_head(s, base + p, t);
         tgt[p] = -1;
         if (h) {
             tgt[p] = route_port(s, w, h);
             if (tgt[p] < 0) { fail(s, ST_ERROR); return; }
+            wanted[tgt[p]]++;
         }
     }
     for (uint32_t e = 0; e < P; e++) {
         uint32_t qe = base + e;
-        if (s->eg_busy[qe] > t) continue;
+        if (wanted[e] == 0 || s->eg_busy[qe] > t) continue;
         uint32_t d = downstream(s, qe);
         if (!has_credit(s, d)) continue;
         for (uint32_t k = 0; k < P; k++) {
@@ -630,6 +639,7 @@ static void forward(sim *s, uint32_t w, uint32_t t)
             if (tgt[i] != (int32_t)e) continue;
             pkt p = *slot(s, base + i, s->head[base + i]);
             s->head[base + i]++;
+            s->sw_queued[w]--;
             p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
             p.hopsum += s->port_delta[qe] + 1;
             push(s, d, &p);
@@ -649,7 +659,7 @@ static void forward(sim *s, uint32_t w, uint32_t t)
 static void inject(sim *s, uint32_t r, uint32_t t)
 {
     nic *n = &s->nics[r];
-    if (n->busy > t) return;
+    if (n->n_lanes == 0 || n->busy > t) return;
     uint32_t f = s->host_port[r];
     if (!has_credit(s, f)) return;
     for (uint32_t k = 0; k < NLANE; k++) {
@@ -679,7 +689,7 @@ static void inject(sim *s, uint32_t r, uint32_t t)
         s->pkt_hops++;
         s->changed = 1;
         if (--L->pkts_left == 0) {
-            if (++L->m == L->nmsg) L->used = 0;
+            if (++L->m == L->nmsg) { L->used = 0; n->n_lanes--; }
             else L->pkts_left = lane_setup(s, L);
         }
         return;
@@ -879,6 +889,7 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     s->slots = calloc((size_t)s->nf * s->cap, sizeof(pkt));
     s->eg_busy = calloc(s->Q + 1, sizeof(uint32_t));
     s->eg_rr = calloc(s->Q + 1, sizeof(uint32_t));
+    s->sw_queued = calloc(s->S + 1, sizeof(uint32_t));
     s->nics = calloc(s->R + 1, sizeof(nic));
     s->npred_left = malloc(sizeof(uint32_t) * (s->NN + 1));
     s->cand = calloc(s->NN + 1, sizeof(uint32_t));
@@ -925,7 +936,7 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
     free(s->col_base); free(s->node_rank); free(s->node_member);
     free(s->head); free(s->tail); free(s->head0); free(s->tail0); free(s->slots);
-    free(s->eg_busy); free(s->eg_rr); free(s->nics); free(s->npred_left); free(s->cand);
+    free(s->eg_busy); free(s->eg_rr); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
     free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
     return 0;
 }

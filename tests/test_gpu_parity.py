@@ -177,3 +177,13 @@ def test_barrier_timeout_is_reported_not_hung():
     sim.close()
     got, want = mv.simulate(p), O.run(p)
     assert_same(got, want)
+
+
+@pytest.mark.parametrize("algo", [I.RING, I.TREE])
+def test_gpt_small_bit_exact(algo):
+    """The config-3 DAG shape (1F1B, analytic TP all-reduces, pipeline p2p,
+    chained DP all-reduces) at test size, three duration seeds."""
+    p = I.gpt_small(algo=algo, seeds=(0, 1, 2)).pack()
+    got, want = mv.simulate(p), O.run(p)
+    assert_same(got, want)
+    assert (got["status"] == mv.EXP_DONE).all()
