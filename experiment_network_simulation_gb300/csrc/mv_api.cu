@@ -4,6 +4,7 @@
 // here allocates device memory.
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -715,3 +716,48 @@ int mv_destroy(mv_ctx *c)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free one-shot entry point: same create/run/results/destroy path,
+// with the workspace in this file-scope device array instead of caller memory.
+static __device__ __align__(256) unsigned char g_static_scratch[MV_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kStaticMaxDevices] = {};
+}  // namespace
+
+extern "C" int mv_simulate_static(const mv_batch_desc *desc, uint32_t max_ticks, void *stream,
+                                  const mv_results_view *out, uint64_t *steps_done)
+{
+    if (!desc || !out) return MV_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return MV_ECUDA;
+    void *scratch = nullptr;
+    {
+        // once per device, with that device current: host code cannot use
+        // the array's name as an address, it needs the device address
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_ptr[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MV_ECUDA;
+            g_static_ptr[dev] = p;
+        }
+        scratch = g_static_ptr[dev];
+    }
+    uint64_t need = 0;
+    int rc = mv_workspace_bytes(desc, &need);
+    if (rc != MV_OK) return rc;
+    if (need > MV_STATIC_SCRATCH_BYTES) return MV_ENOMEM;
+    mv_ctx *c = nullptr;
+    rc = mv_create(desc, scratch, MV_STATIC_SCRATCH_BYTES, stream, &c);
+    if (rc != MV_OK) return rc;
+    int run = mv_run(c, max_ticks, steps_done);
+    if (run >= 0) {
+        int r2 = mv_results(c, out);
+        if (r2 != MV_OK) run = r2;
+    }
+    mv_destroy(c);
+    return run;
+}

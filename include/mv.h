@@ -211,6 +211,39 @@ int mv_results(mv_ctx *ctx, const mv_results_view *out);
 /* Free the host context.  The workspace is not touched. */
 int mv_destroy(mv_ctx *ctx);
 
+/*
+ * Allocation-free one-shot simulation.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- for
+ * example code running inside a framework whose caching allocator already
+ * holds the free device memory, a plugin host whose policy forbids new
+ * device allocations, or a latency-critical loop where cudaMalloc's implicit
+ * device synchronisation is not acceptable.
+ *
+ * It does what mv_create + mv_run + mv_results + mv_destroy do, but its
+ * workspace is a file-scope device array of MV_STATIC_SCRATCH_BYTES (32 MiB)
+ * inside the library instead of caller memory.  The caller still passes the
+ * batch (host arrays, as for mv_create) and the host result buffers (as for
+ * mv_results); `stream` is a cudaStream_t (NULL = legacy default stream),
+ * `max_ticks` and `steps_done` are as for mv_run.  It calls no cudaMalloc,
+ * cudaFree or other device-allocating routine.
+ *
+ * The array belongs to the current device's context: the first call on a
+ * device looks up its device address (cudaGetSymbolAddress) and caches it,
+ * so make that first call before any stream capture.  Once the library's
+ * module is loaded on a device, the 32 MiB stay reserved there until the
+ * process exits.  Every call reuses the same array (each call clears and
+ * re-uploads what it needs), so calls whose GPU work overlaps -- two host
+ * threads, or two streams of the same device -- race and must be serialised
+ * by the caller.
+ *
+ * Returns MV_OK / MV_INCOMPLETE as mv_run does, MV_ENOMEM when the batch
+ * needs more than MV_STATIC_SCRATCH_BYTES of workspace (see
+ * mv_workspace_bytes), or the error of the failing step.
+ */
+#define MV_STATIC_SCRATCH_BYTES (32ull << 20)
+int mv_simulate_static(const mv_batch_desc *desc, uint32_t max_ticks, void *stream,
+                       const mv_results_view *out, uint64_t *steps_done);
+
 const char *mv_strerror(int code);
 
 #ifdef __cplusplus
