@@ -298,17 +298,22 @@ class Workload:
         for c in self.colls:
             N = len(c.ranks)
             m = c.a2a or {}
-            for i in range(N):
-                ents = sorted(((d, b) for (s, d), b in m.items() if s == i and d != i and b > 0),
-                              key=lambda e: (e[0] - i) % N)
-                row_n.append(len(ents))
-                row_d += [d for d, _ in ents]
-                row_b += [b for _, b in ents]
-            for j in range(N):
-                ents = sorted((s, b) for (s, d), b in m.items() if d == j and s != j and b > 0)
-                col_n.append(len(ents))
-                col_s += [s for s, _ in ents]
-                col_b += [b for _, b in ents]
+            if m:
+                src = np.array([k[0] for k in m], np.int64)
+                dst = np.array([k[1] for k in m], np.int64)
+                byt = np.array(list(m.values()), np.int64)
+                keep = (src != dst) & (byt > 0)
+                src, dst, byt = src[keep], dst[keep], byt[keep]
+            else:
+                src = dst = byt = np.zeros(0, np.int64)
+            o = np.lexsort(((dst - src) % N, src))
+            row_n += np.bincount(src, minlength=N).tolist()
+            row_d += dst[o].tolist()
+            row_b += byt[o].tolist()
+            o = np.lexsort((src, dst))
+            col_n += np.bincount(dst, minlength=N).tolist()
+            col_s += src[o].tolist()
+            col_b += byt[o].tolist()
         mem = np.zeros(10, np.uint64)
         if self.mem is not None:
             mem[:9] = self.mem
@@ -699,3 +704,77 @@ def config4(n_seeds: int = 256, n_exp: int | None = None) -> Batch:
             if n_exp is not None and len(exps) >= n_exp:
                 return Batch(exps, "moe-dispatch-combine-512")
     return Batch(exps, "moe-dispatch-combine-512")
+
+
+# --------------------------------------------------------------------------
+# Topology search (config 5)
+# --------------------------------------------------------------------------
+def clos3(radix: int, oversub: int, n_hosts: int, rail: bool, gpus: int = 8,
+          delta: int = 0, sigma: int = 1) -> Topology:
+    """Three-tier Clos of radix-port switches.  Edge: u = radix // (oversub+1)
+    up ports (one per aggregation switch of its pod) and d = u * oversub host
+    ports.  A pod has radix/2 edges and u aggregation switches; aggregation
+    switch j has radix/2 up ports to core group j (cores j*radix/2 ...), each
+    core one link per pod.  Plain: consecutive hosts fill an edge; rail-
+    optimised: within a pod, the NIC of GPU g sits on one of the pod's edges
+    of rail g (server-major host numbering)."""
+    half = radix // 2
+    u = radix // (oversub + 1)
+    d = u * oversub
+    per_pod = half * d
+    pods = -(-n_hosts // per_pod)
+    assert pods <= radix, "fabric does not reach the host count"
+    if rail:
+        assert half % gpus == 0
+    t = Topology(f"clos3-r{radix}-o{oversub}-{'rail' if rail else 'plain'}")
+    edges = [[t.add_switch(1) for _ in range(half)] for _ in range(pods)]
+    aggs = [[t.add_switch(2) for _ in range(u)] for _ in range(pods)]
+    cores = [t.add_switch(3) for _ in range(u * half)]
+    hosts = t.add_hosts(n_hosts)
+    for h in hosts:
+        pod, i = divmod(h, per_pod)
+        if rail:
+            srv, g = divmod(i, gpus)               # server within the pod, GPU
+            per_rail = half // gpus                # edges per rail in a pod
+            e = g * per_rail + srv // d
+        else:
+            e = i // d
+        t.attach_host(h, edges[pod][e], sigma, delta)
+    for pod in range(pods):
+        for e in edges[pod]:
+            for a in aggs[pod]:
+                t.link(e, a, sigma, delta)
+        for j, a in enumerate(aggs[pod]):
+            for c in range(half):
+                t.link(a, cores[j * half + c], sigma, delta)
+    return t
+
+
+def config5_topologies(n_hosts: int = 8192, delta: int = 12) -> list:
+    """Feasible members of {2,3 tiers} x {32,48,64 ports} x {1..4:1} x
+    {rail-optimised, plain} for n_hosts NICs.  A 2-tier Clos of <=64-port
+    switches reaches at most 64 leaves x 64 ports, so none of the 2-tier
+    members reaches 8,192 NICs: all feasible members are 3-tier."""
+    out = []
+    for radix in (32, 48, 64):
+        for o in (1, 2, 3, 4):
+            for rail in (False, True):
+                out.append(clos3(radix, o, n_hosts, rail, delta=delta))
+    return out
+
+
+def config5(n_exp: int = 10_000, topo_idx=None, wave: tuple | None = None) -> Batch:
+    """Topology search: config-3's GPT-13B DAG at DP=128 (TP 8, PP 4: 512
+    servers, hosts 0..4095) on 1,024-server (8,192-NIC) fabrics, ring, NC 8,
+    chunk 256 KiB; experiments cycle over the 24 fabrics, then duration seeds.
+    ``wave=(start, stop)`` selects a slice of the experiment list."""
+    tk = tick_ps(4096, 400)
+    topos = config5_topologies(8192, delay_ticks(1_000_000, tk))
+    if topo_idx is not None:
+        topos = [topos[i] for i in topo_idx]
+    work = gpt_1f1b(512, 8, 4, 40, 8, 2048, 5120, 40, 13_000_000_000, tk)
+    idx = range(n_exp) if wave is None else range(wave[0], min(wave[1], n_exp))
+    exps = [Experiment(topos[i % len(topos)], work, RING, 8, 256 * KIB, 4096, 64, tk,
+                       dur_seed=i // len(topos), label=dict(topo=i % len(topos)))
+            for i in idx]
+    return Batch(exps, "topology-search-1024srv")
