@@ -35,7 +35,7 @@ struct Layout {
     std::vector<WorkRec> work;
     std::vector<ExpRec> exp;
     std::vector<u32> sw_pstart, port_sw, rank_first, succ_start, node_member, coll_mstart,
-        memb_row, memb_col, item_exp, item_loc;
+        memb_row, memb_col, item_exp, item_loc, node_rank;
     // regions
     Region r_topo, r_work, r_exp, r_sw_nports, r_sw_level, r_sw_pstart, r_port_sw, r_port_peer,
         r_port_sigma, r_port_delta, r_host_port, r_host_sigma, r_host_delta, r_rank_first,
@@ -44,11 +44,11 @@ struct Layout {
         r_coll_intra, r_coll_nmembers, r_coll_parts, r_coll_alpha, r_coll_beta_num,
         r_coll_beta_den, r_coll_mstart, r_coll_bytes, r_member_rank, r_member_node,
         r_member_a2a_n, r_memb_row, r_a2a_dst, r_member_a2a_in_n, r_memb_col, r_a2a_in_src,
-        r_a2a_bytes, r_a2a_in_bytes, r_mem, r_item_exp, r_item_loc;
+        r_a2a_bytes, r_a2a_in_bytes, r_mem, r_item_exp, r_item_loc, r_node_rank;
     u64 static_bytes = 0;
     Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_pend, r_act,
-        r_lanes, r_ports, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
-        r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_glob;
+        r_lanes, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
+        r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_glob, r_wake;
     u64 total = 0;
 
     u64 cur = 0;
@@ -88,6 +88,7 @@ int plan(const mv_batch_desc *d, Layout &L)
         R.sw_off = (u32)L.nsw;
         R.port_off = (u32)L.nports;
         R.route_off = L.route_bytes;
+        R.rdv = kUnset;
         L.nhosts += R.nh;
         L.nsw += R.nsw;
         L.nports += R.nq;
@@ -113,7 +114,8 @@ int plan(const mv_batch_desc *d, Layout &L)
         for (u32 p = 0; p < R.nq; p++) {
             i32 pe = d->port_peer[R.port_off + p];
             u32 sg = d->port_sigma[R.port_off + p], dl = d->port_delta[R.port_off + p];
-            if (sg == 0 || sg > 65535 || dl > 4095) return MV_EINVAL;
+            if (sg == 0 || sg > 65535 || dl + 1 > kPopLog) return MV_EINVAL;
+            R.rdv = std::min(R.rdv, dl + 1);
             if (pe >= 0) {
                 if ((u32)pe >= R.nq || d->port_peer[R.port_off + pe] != (i32)p) return MV_EINVAL;
             } else {
@@ -125,7 +127,8 @@ int plan(const mv_batch_desc *d, Layout &L)
             u32 hp = d->host_port[R.host_off + h];
             u32 sg = d->host_sigma[R.host_off + h], dl = d->host_delta[R.host_off + h];
             if (hp >= R.nq || d->port_peer[R.port_off + hp] != -(i32)(h + 1)) return MV_EINVAL;
-            if (sg == 0 || sg > 65535 || dl > 4095) return MV_EINVAL;
+            if (sg == 0 || sg > 65535 || dl + 1 > kPopLog) return MV_EINVAL;
+            R.rdv = std::min(R.rdv, dl + 1);
         }
     }
     // ---- workloads
@@ -157,6 +160,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.rank_first.resize(L.nranks);
     L.succ_start.resize(L.nnodes);
     L.node_member.assign(L.nnodes, kUnset);
+    L.node_rank.resize(L.nnodes);
     L.coll_mstart.resize(L.ncolls);
     L.memb_row.resize(L.nmemb);
     L.memb_col.resize(L.nmemb);
@@ -168,7 +172,10 @@ int plan(const mv_batch_desc *d, Layout &L)
         for (u32 r = 0; r < R.nr; r++) {
             L.rank_first[R.rank_off + r] = n;
             u32 c = d->rank_nnodes[R.rank_off + r];
-            for (u32 k = 0; k < c; k++) node_rank[n + k] = r;
+            for (u32 k = 0; k < c; k++) {
+                node_rank[n + k] = r;
+                L.node_rank[R.node_off + n + k] = r;
+            }
             n += c;
         }
         if (n != R.nn) return MV_EINVAL;
@@ -283,6 +290,8 @@ int plan(const mv_batch_desc *d, Layout &L)
         L.max_nodes = std::max(L.max_nodes, W.nn);
         L.max_queues = std::max(L.max_queues, X.nq);
         L.max_ranks = std::max(L.max_ranks, W.nr);
+        X.item_off = (u32)L.item_exp.size();
+        X.n_items = T.nsw + (W.nr + 31) / 32;
         for (u32 s = 0; s < T.nsw; s++) {
             L.item_exp.push_back(e);
             L.item_loc.push_back(s);
@@ -344,6 +353,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_mem = L.take(80 * L.W);
     L.r_item_exp = L.take(4 * L.items);
     L.r_item_loc = L.take(4 * L.items);
+    L.r_node_rank = L.take(4 * L.nnodes);
     L.static_bytes = L.cur;
     L.r_route = L.take(L.route_bytes);
     L.r_up_n = L.take(L.nsw);
@@ -357,6 +367,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_act = L.take(4ull * kNAct * L.rk_total);
     L.r_lanes = L.take(sizeof(Lane) * kNLane * L.rk_total);
     L.r_ports = L.take(8ull * kNPort * L.rk_total);
+    L.r_poplog = L.take(4ull * kPopLog * L.q_total);
     L.r_nd_pred = L.take(4 * L.nd_total);
     L.r_nd_cand = L.take(4 * L.nd_total);
     L.r_nd_start = L.take(4 * L.nd_total);
@@ -369,6 +380,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_rec_key = L.take(4 * L.rec_total);
     L.r_rec_tick = L.take(4 * L.rec_total);
     L.r_glob = L.take(sizeof(Glob));
+    L.r_wake = L.take(4 * L.items);
     L.total = L.cur;
     return MV_OK;
 }
@@ -440,6 +452,7 @@ Params make_params(void *ws, const Layout &L)
     P.act = at<u32>(ws, L.r_act);
     P.lanes = at<Lane>(ws, L.r_lanes);
     P.ports = at<uint2>(ws, L.r_ports);
+    P.poplog = at<u32>(ws, L.r_poplog);
     P.nd_pred = at<u32>(ws, L.r_nd_pred);
     P.nd_cand = at<u32>(ws, L.r_nd_cand);
     P.nd_start = at<u32>(ws, L.r_nd_start);
@@ -453,6 +466,8 @@ Params make_params(void *ws, const Layout &L)
     P.rec_tick = at<u32>(ws, L.r_rec_tick);
     P.item_exp = at<u32>(ws, L.r_item_exp);
     P.item_loc = at<u32>(ws, L.r_item_loc);
+    P.node_rank = at<u32>(ws, L.r_node_rank);
+    P.wake = at<u32>(ws, L.r_wake);
     P.n_items = (u32)L.items;
     P.n_exps = L.E;
     P.n_topos = L.T;
@@ -594,6 +609,7 @@ int mv_create(const mv_batch_desc *d, void *ws, uint64_t ws_bytes, void *stream,
     put(img, L.r_mem, d->mem, 80 * L.W);
     put(img, L.r_item_exp, L.item_exp.data(), 4 * L.items);
     put(img, L.r_item_loc, L.item_loc.data(), 4 * L.items);
+    put(img, L.r_node_rank, L.node_rank.data(), 4 * L.nnodes);
     cudaError_t e = cudaMemcpyAsync(ws, img.data(), L.static_bytes, cudaMemcpyHostToDevice,
                                     c->stream);
     if (e == cudaSuccess) e = setup_dynamic(c);

@@ -22,6 +22,7 @@ constexpr u32 kNPend = 64;    // nodes scheduled to start, per rank
 constexpr u32 kNAct = 16;     // running collective memberships, per rank
 constexpr u32 kMaxPorts = 64; // ports per switch (one warp, two ports a lane)
 constexpr u32 kTickLimit = 0xFFF00000u;
+constexpr u32 kPopLog = 64;    // pops remembered per queue (credit delay <= 64)
 
 enum : u32 { NODE_COMPUTE = 0, NODE_INTRA = 1, NODE_NET = 2 };
 enum : u32 { COLL_AR = 0, COLL_RS = 1, COLL_AG = 2, COLL_RELAY = 3, COLL_P2P = 4, COLL_A2A = 5 };
@@ -31,7 +32,8 @@ enum : u32 { EXP_DONE = 0, EXP_RUNNING = 1, EXP_OOM = 2, EXP_DEADLOCK = 3, EXP_O
 
 struct TopoRec {
     u32 nh, nsw, nq, maxlev;        // hosts, switches, switch ports, top level
-    u32 host_off, sw_off, port_off, pad;
+    u32 host_off, sw_off, port_off;
+    u32 rdv;                        // 1 + smallest link delta: how late a join reaches peers
     u64 route_off;                  // route table: nsw * nh bytes
 };
 
@@ -50,6 +52,8 @@ struct ExpRec {
     u64 nd_off;     // first node
     u64 rec_off;    // first message record
     u32 nq, nsw, nr, nn;
+    u32 item_off;   // first work item (switches, then groups of 32 ranks)
+    u32 n_items, pad0, pad1;
 };
 
 // One send lane: a stream of messages one rank sends for one channel of one
@@ -70,9 +74,12 @@ struct RankCtl {
 
 struct ExpCtl {
     u32 status, now, limit, nodes_left;
-    u32 clk[3], chg[3], nxt[3], rec_count;
+    u32 clk[3];              // tick processed at step k (slot k % 3)
+    u32 nxt[3];              // min over pending wake ticks reported at step k
+    u32 rec_count;
     u32 stop_step;           // first step in which it finished or failed
     u32 end_max1;            // 1 + latest node end tick (0: none yet)
+    u32 pad;
     u64 pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
 };
 
@@ -101,6 +108,7 @@ struct Params {
     const u64 *a2a_bytes, *a2a_in_bytes, *mem;
     // dynamic state
     u64 *q_push, *q_pop;     // per queue: (tick << 32) | counter of the last push / pop
+    u32 *poplog;             // per queue: tick of each of the last 64 pops (by head % 64)
     uint4 *slots;            // packet descriptors
     uint2 *eg;               // per switch port: (busy_until, round-robin pointer)
     RankCtl *rk;
@@ -113,6 +121,8 @@ struct Params {
     ExpCtl *ctl;
     u32 *rec_sender, *rec_key, *rec_tick;
     const u32 *item_exp, *item_loc;
+    u32 *wake;               // per work item: earliest tick it may have work
+    const u32 *node_rank;    // per node: its rank (workload-local)
     u32 n_items, n_exps, n_topos, pad;
     Glob *glob;
     // run options

@@ -69,6 +69,24 @@ __device__ __forceinline__ void set_status(ExpCtl *c, u32 st, u32 k)
     atomicMin(&c->stop_step, k);
 }
 
+// Credit of queue qi for a sender at tick t: the queue holds `tail` pushes
+// and `H` pops as of the start of the tick; the credit of a pop at tick x
+// reaches the sender at x + D (D = delta + 1 of the link).  At most D - 1
+// pops can still be on their way, so the pop log is only read when the
+// queue is within D - 1 of full.
+__device__ __forceinline__ bool credit_ok(const Params &P, u64 qi, u32 tail, u32 H, u32 D, u32 t,
+                                          u32 cap)
+{
+    if (tail - H + D - 1 < cap) return true;
+    u32 back = 0;
+    const u32 *log = P.poplog + qi * kPopLog;
+    while (back < H && back + 1 < D) {
+        if (__ldcg(&log[(H - 1 - back) % kPopLog]) + D <= t) break;
+        back++;
+    }
+    return tail - (H - back) < cap;
+}
+
 // ---------------------------------------------------------------- set-up
 // Shortest up/down routing: a switch sends a packet down the lowest port
 // under which its destination host sits, else up (ECMP over its up ports).
@@ -154,6 +172,8 @@ __global__ void k_init(Params P)
         P.q_push[X.q_off + q] = (u64)kUnset << 32;
         P.q_pop[X.q_off + q] = (u64)kUnset << 32;
     }
+    // work items: switches wake on their first packet, rank groups at tick 0
+    for (u32 it = i; it < X.n_items; it += stride) P.wake[X.item_off + it] = it < X.nsw ? kUnset : 0;
     bool fits = memory_fits(P.mem + 10 * (u64)X.work, X.gpu_mem);
     // roots (no predecessor) are scheduled at tick 0, in node order
     for (u32 r = i; r < X.nr; r += stride) {
@@ -192,7 +212,6 @@ __global__ void k_run_reset(Params P, u32 max_ticks)
         c->limit = lim > kTickLimit ? kTickLimit : (u32)lim;
         for (int k = 0; k < 3; k++) {
             c->clk[k] = kUnset;
-            c->chg[k] = 0;
             c->nxt[k] = kUnset;
         }
     }
@@ -253,59 +272,75 @@ __device__ bool grid_barrier(const Params &P, u32 step)
 
 // ---------------------------------------------------------------- clocks
 // Tick that experiment e processes at step k, or kUnset if it does not run.
-// Computed identically by every warp touching e: from the clock, change flag
-// and next-event slots of step k-1 (three rotating slots, so that the slots
-// of step k-1 are stable while step k runs and step k+1's are cleared).
+// Every lane that touches e computes it the same way, from the slots of step
+// k-1 only: the clock and the minimum over every pending wake tick reported
+// during step k-1 (three rotating slots: step k-1's are stable while step k
+// runs, and step k+1's are cleared during step k).
 __device__ __forceinline__ u32 exp_tick(const Params &P, u32 e, u32 k)
 {
     ExpCtl *c = &P.ctl[e];
-    if (ld_rlx32(&c->stop_step) < k) return kUnset;   // finished or failed earlier
+    u32 stop = ld_rlx32(&c->stop_step), lim = ld_rlx32(&c->limit);
+    if (stop < k) return kUnset;                  // finished or failed earlier
     u32 t;
     if (k == 0) {
-        if (ld_rlx32(&c->status) != EXP_RUNNING || ld_rlx32(&c->nodes_left) == 0) return kUnset;
+        u32 st = ld_rlx32(&c->status), left = ld_rlx32(&c->nodes_left);
         t = ld_rlx32(&c->now);
+        if (st != EXP_RUNNING || left == 0) return kUnset;
     } else {
         u32 p = (k - 1) % 3;
         u32 tp = ld_rlx32(&c->clk[p]);
-        if (tp == kUnset) return kUnset;
-        t = ld_rlx32(&c->chg[p]) ? tp + 1 : ld_rlx32(&c->nxt[p]);
-        if (t == kUnset) return kUnset;
+        t = ld_rlx32(&c->nxt[p]);
+        if (tp == kUnset || t == kUnset) return kUnset;
     }
-    if (t >= ld_rlx32(&c->limit)) return kUnset;
-    return t;
+    return t >= lim ? kUnset : t;
 }
 
-// Control of one experiment at step k: publish its tick, clear the slots of
-// step k+1, and settle its final state when it stops running.
-__device__ void exp_control(const Params &P, u32 e, u32 k)
+// Control of one experiment at step k (run by the lane holding its first
+// work item): publish its tick, clear the slot of step k+1, count it as
+// running, and settle its final state when it stops.
+__device__ void exp_control(const Params &P, u32 e, u32 k, u32 t)
 {
     ExpCtl *c = &P.ctl[e];
-    u32 t = exp_tick(P, e, k);
     st_rlx32(&c->clk[k % 3], t);
-    st_rlx32(&c->chg[(k + 1) % 3], 0);
     st_rlx32(&c->nxt[(k + 1) % 3], kUnset);
     if (t != kUnset) {
         atomicAdd(&P.glob->run_cnt[k % 3], 1);
         return;
     }
+    // a stopped experiment's clock is one past its latest node end (0: none)
     if (k == 0) {
-        if (ld_rlx32(&c->status) == EXP_RUNNING && ld_rlx32(&c->nodes_left) == 0)
+        if (ld_rlx32(&c->status) == EXP_RUNNING && ld_rlx32(&c->nodes_left) == 0) {
             st_rlx32(&c->status, EXP_DONE);
+            st_rlx32(&c->now, ld_rlx32(&c->end_max1));
+        }
         return;                                   // else stopped before: now unchanged
     }
     u32 p = (k - 1) % 3, tp = ld_rlx32(&c->clk[p]);
     if (tp == kUnset) return;                     // settled at an earlier step
+    u32 nx = ld_rlx32(&c->nxt[p]);
     if (ld_rlx32(&c->status) != EXP_RUNNING) {    // failed during the last tick
-        st_rlx32(&c->now, tp);
+        st_rlx32(&c->now, ld_rlx32(&c->end_max1));
     } else if (ld_rlx32(&c->nodes_left) == 0) {
         st_rlx32(&c->status, EXP_DONE);
-        st_rlx32(&c->now, tp + 1);
-    } else if (!ld_rlx32(&c->chg[p]) && ld_rlx32(&c->nxt[p]) == kUnset) {
+        st_rlx32(&c->now, ld_rlx32(&c->end_max1));
+    } else if (nx == kUnset) {                    // nothing pending anywhere
         st_rlx32(&c->status, EXP_DEADLOCK);
-        st_rlx32(&c->now, tp + 1);
+        st_rlx32(&c->now, ld_rlx32(&c->end_max1));
     } else {                                      // stopped by the tick budget
-        st_rlx32(&c->now, ld_rlx32(&c->chg[p]) ? tp + 1 : ld_rlx32(&c->nxt[p]));
+        st_rlx32(&c->now, nx);
     }
+}
+
+// Work items and their wake ticks.  An item is processed at tick t when its
+// wake <= t.  Whoever creates work for another item lowers that item's wake
+// (a push, a collective join, a message delivery) and the experiment's next
+// tick; a processed item sets its own next wake from its own state.
+__device__ __forceinline__ u32 sw_item(const ExpRec &X, u32 s) { return X.item_off + s; }
+__device__ __forceinline__ u32 rank_item(const ExpRec &X, u32 r) { return X.item_off + X.nsw + r / 32; }
+__device__ __forceinline__ void poke(const Params &P, u32 item, u32 e, u32 k, u32 at)
+{
+    atomicMin(&P.wake[item], at);
+    atomicMin(&P.ctl[e].nxt[k % 3], at);
 }
 
 // ---------------------------------------------------------------- switches
@@ -338,7 +373,13 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
     const u32 lane = threadIdx.x & 31;
     const u32 gs = T.sw_off + s;
     const u32 np = P.sw_nports[gs], p0 = P.sw_pstart[gs];
-    u32 nxt = kUnset;
+    const u32 it = sw_item(X, s);
+    u32 old = 0;
+    if (lane == 0) old = atomicExch(&P.wake[it], kUnset);   // consume pending wakes
+    old = __shfl_sync(0xffffffffu, old, 0);
+    u32 nxt = kUnset;                   // own next wake
+    u32 pk_min = kUnset;                // earliest tick poked into a downstream item
+    bool ready_any = false;
     bool bad = false;
     sm->mask[lane] = 0;
     sm->mask[lane + 32] = 0;
@@ -355,6 +396,7 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
         if (head == tail) continue;
         uint4 pk = __ldcg(&P.slots[X.slot_off + (u64)(p0 + p) * X.cap + head % X.cap]);
         if (pk.x > t) { nxt = min(nxt, pk.x); continue; }
+        ready_any = true;
         u32 tg = route_port(P, T, X, gs, s, pk);
         if (tg >= np) { bad = true; continue; }
         sm->pkt[p] = pk;
@@ -371,14 +413,15 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
         if (!M) continue;
         u32 qe = p0 + eg;
         uint2 st = __ldcg(&P.eg[X.eg_off + qe]);
-        if (st.x > t) { nxt = min(nxt, st.x); continue; }
+        if (st.x > t) continue;             // busy: its heads wake the switch at t+1
         i32 pe = P.port_peer[T.port_off + qe];
         u32 dq = pe >= 0 ? (u32)pe : T.nq + (u32)(-pe - 1);
         u64 dqi = X.q_off + dq;
         u64 dpop = ld_rlx64(&P.q_pop[dqi]);
         u32 dhead = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
         u32 dtail = (u32)__ldcg(&P.q_push[dqi]);
-        if (dtail - dhead >= X.cap) continue;
+        u32 dl_e = P.port_delta[T.port_off + qe];
+        if (!credit_ok(P, dqi, dtail, dhead, dl_e + 1, t, X.cap)) continue;
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
         uint4 pk = sm->pkt[i];
@@ -388,6 +431,10 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
         __stcg(&P.slots[X.slot_off + (u64)dq * X.cap + dtail % X.cap], pk);
         st_rlx64(&P.q_push[dqi], ((u64)t << 32) | (u32)(dtail + 1));
         __stcg(&P.eg[X.eg_off + qe], make_uint2(t + sg, (i + 1) % np));
+        // the queue's owner: the peer switch, or the rank group of the host
+        if (pe >= 0) atomicMin(&P.wake[sw_item(X, P.port_sw[T.port_off + pe])], pk.x);
+        else if ((u32)(-pe - 1) < X.nr) atomicMin(&P.wake[rank_item(X, (u32)(-pe - 1))], pk.x);
+        pk_min = min(pk_min, pk.x);
         popped |= 1ull << i;
         hops++;
     }
@@ -397,19 +444,24 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
 #pragma unroll
     for (u32 j = 0; j < 2; j++) {
         u32 p = lane + 32 * j;
-        if (p < np && ((all >> p) & 1ull))
-            st_rlx64(&P.q_pop[X.q_off + p0 + p], ((u64)t << 32) | (u32)(sm->head[p] + 1));
+        if (p < np && ((all >> p) & 1ull)) {
+            u64 qi = X.q_off + p0 + p;
+            __stcg(&P.poplog[qi * kPopLog + sm->head[p] % kPopLog], t);
+            st_rlx64(&P.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
+        }
     }
     hops = __reduce_add_sync(0xffffffffu, hops);
     nxt = __reduce_min_sync(0xffffffffu, nxt);
+    pk_min = __reduce_min_sync(0xffffffffu, pk_min);
     bool anybad = __any_sync(0xffffffffu, bad);
+    if (__any_sync(0xffffffffu, ready_any)) nxt = t + 1;   // heads left or blocked
     if (lane == 0) {
         ExpCtl *c = &P.ctl[e];
-        if (all) {
-            st_rlx32(&c->chg[k % 3], 1);
-            atomicAdd((unsigned long long *)&c->pkt_hops, (unsigned long long)hops);
-        }
-        if (nxt != kUnset) atomicMin(&c->nxt[k % 3], nxt);
+        u32 w = min(nxt, old > t ? old : kUnset);
+        if (w != kUnset) atomicMin(&P.wake[it], w);
+        u32 m = min(w, pk_min);
+        if (m != kUnset) atomicMin(&c->nxt[k % 3], m);
+        if (all) atomicAdd((unsigned long long *)&c->pkt_hops, (unsigned long long)hops);
         if (anybad) set_status(c, EXP_ERROR, k);
     }
     __syncwarp();
@@ -460,11 +512,12 @@ struct RankView {
     const TopoRec *T;
     const WorkRec *W;
     ExpCtl *c;
-    u32 r, t;
+    u32 r, t, e, k;
     u64 rk;             // X.rk_off + r
     RankCtl C;
     bool changed, fail_over, fail_err;
-    u32 nxt;
+    u32 nxt;            // this rank's own next wake
+    u32 pk_min;         // earliest wake poked into other items
     u32 n_inj, n_del, n_msg, n_done, end_max1;
     u64 dig;
 };
@@ -666,6 +719,25 @@ __device__ u32 intra_ticks(const RankView &v, u32 c)
     return P.coll_alpha[cc] + (u32)cdiv(be * P.coll_beta_num[cc], P.coll_beta_den[cc]);
 }
 
+__device__ __forceinline__ void rank_poke(RankView &v, u32 item, u32 at)
+{
+    atomicMin(&v.P->wake[item], at);
+    v.pk_min = min(v.pk_min, at);
+}
+
+// A member joined collective c at this tick: members waiting on its start
+// look again when the join reaches them (intra-server barrier: next tick;
+// network rendezvous: 1 + min(delta) ticks later).
+__device__ void poke_members(RankView &v, u32 c, u32 at)
+{
+    u32 N = nmemb(v, c), last = kUnset;
+    for (u32 m = 0; m < N; m++) {
+        u32 g = rank_item(*v.X, mrank(v, c, m));
+        if (g != last) rank_poke(v, g, at);
+        last = g;
+    }
+}
+
 __device__ void pend_add(RankView &v, u32 u, u32 st)
 {
     if (v.C.npend >= kNPend) { v.fail_over = true; return; }
@@ -812,9 +884,11 @@ __device__ void dag_step(RankView &v)
         } else if (kind == NODE_INTRA) {
             st_rlx32(&P.nd_start[g], t);
             act_add(v, u);
+            poke_members(v, coll_of(v, u), t + 1);
         } else {
             if (!net_join(v, u)) return;
             st_rlx32(&P.nd_start[g], t);
+            poke_members(v, coll_of(v, u), t + v.T->rdv);
             if (__ldcg(&P.nd_out[g]) == 0) {
                 free_ports(v, u);
                 complete_node(v, u, t);
@@ -843,7 +917,10 @@ __device__ void inject(RankView &v)
     u64 pw = ld_rlx64(&P.q_pop[qi]);
     u32 head = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
     u32 tail = (u32)__ldcg(&P.q_push[qi]);
-    if (tail - head >= v.X->cap) return;
+    if (!credit_ok(P, qi, tail, head, P.host_delta[T.host_off + v.r] + 1, t, v.X->cap)) {
+        v.nxt = min(v.nxt, t + 1);
+        return;
+    }
     u64 M = v.C.lane_mask;
     u64 hi = v.C.rr < 64 ? (M & (~0ull << v.C.rr)) : 0ull;
     u64 lo = M & ~hi;
@@ -863,7 +940,11 @@ __device__ void inject(RankView &v)
             u32 c = coll_of(v, L.node);
             u64 dg = v.X->nd_off + mnode(v, c, L.dst_member);
             u32 dst_start = ld_rlx32(&P.nd_start[dg]);
-            if (dst_start == kUnset || dst_start >= t) continue;
+            // the destination's join reaches this rank 1 + min(delta) ticks
+            // later; when that time is known, it is this rank's own wake (a
+            // poke alone could be shadowed by an earlier pending wake)
+            if (dst_start == kUnset) continue;
+            if (dst_start + T.rdv > t) { v.nxt = min(v.nxt, dst_start + T.rdv); continue; }
             u32 dpb = ld_rlx32(&P.nd_pbase[dg]);
             u32 hs = P.host_sigma[T.host_off + v.r], hd = P.host_delta[T.host_off + v.r];
             uint4 pk;
@@ -877,11 +958,13 @@ __device__ void inject(RankView &v)
             v.C.rr = (l + 1) % kNLane;
             v.n_inj++;
             v.changed = true;
+            rank_poke(v, sw_item(*v.X, P.port_sw[T.port_off + qp]), pk.x);
             if (--L.pkts_left == 0) {
                 if (++L.m == L.nmsg) v.C.lane_mask &= ~(1ull << l);
                 else L.pkts_left = lane_setup(v, L);
             }
             store_lane(&lanes[l], L);
+            if (v.C.lane_mask) v.nxt = min(v.nxt, v.C.busy > t + 1 ? v.C.busy : t + 1);
             return;
         }
     }
@@ -902,10 +985,14 @@ __device__ void receive(RankView &v)
     if (head == tail) return;
     uint4 pk = __ldcg(&P.slots[v.X->slot_off + (u64)ql * v.X->cap + head % v.X->cap]);
     if (pk.x > t) { v.nxt = min(v.nxt, pk.x); return; }
+    __stcg(&P.poplog[qi * kPopLog + head % kPopLog], t);
     st_rlx64(&P.q_pop[qi], ((u64)t << 32) | (u32)(head + 1));
     v.n_del++;
     v.changed = true;
+    if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     if (!pk_last(pk)) return;
+    v.nxt = min(v.nxt, t + 1);                         // DAG looks at its counts next tick
+    rank_poke(v, rank_item(*v.X, P.node_rank[v.W->node_off + pk.z]), t + 1);   // the ACK
     u32 ps = pk_slot(pk);
     uint2 port = __ldcg(&P.ports[v.rk * kNPort + ps]);
     port.x++;
@@ -937,9 +1024,14 @@ __device__ __noinline__ void rank_tick(const Params &P, const ExpRec &X, u32 e, 
     const WorkRec W = P.work[X.work];
     RankView v;
     v.P = &P; v.X = &X; v.T = &T; v.W = &W; v.c = &P.ctl[e];
-    v.r = r; v.t = t; v.rk = X.rk_off + r;
+    v.r = r; v.t = t; v.e = e; v.k = k; v.rk = X.rk_off + r;
     v.changed = v.fail_over = v.fail_err = false;
     v.nxt = kUnset;
+    v.pk_min = kUnset;
+    const u32 it = rank_item(X, r - (r % 32));
+    u32 old = 0;
+    if ((threadIdx.x & 31) == 0) old = atomicExch(&P.wake[it], kUnset);
+    old = __shfl_sync(0xffffffffu, old, 0);
     v.n_inj = v.n_del = v.n_msg = v.n_done = v.end_max1 = 0;
     v.dig = 0;
     const bool active = r < X.nr;
@@ -953,8 +1045,8 @@ __device__ __noinline__ void rank_tick(const Params &P, const ExpRec &X, u32 e, 
         store_ctl(&P.rk[v.rk], v.C);
     }
     const u32 full = 0xffffffffu;
-    bool ch = __any_sync(full, v.changed);
     u32 nxt = __reduce_min_sync(full, v.nxt);
+    u32 pkm = __reduce_min_sync(full, v.pk_min);
     u32 inj = __reduce_add_sync(full, v.n_inj);
     u32 del = __reduce_add_sync(full, v.n_del);
     u32 msg = __reduce_add_sync(full, v.n_msg);
@@ -966,8 +1058,10 @@ __device__ __noinline__ void rank_tick(const Params &P, const ExpRec &X, u32 e, 
     for (int o = 16; o > 0; o >>= 1) dig += __shfl_xor_sync(full, dig, o);
     if ((threadIdx.x & 31) == 0) {
         ExpCtl *c = v.c;
-        if (ch) st_rlx32(&c->chg[k % 3], 1);
-        if (nxt != kUnset) atomicMin(&c->nxt[k % 3], nxt);
+        u32 w = min(nxt, old > t ? old : kUnset);
+        if (w != kUnset) atomicMin(&P.wake[it], w);
+        u32 m = min(w, pkm);
+        if (m != kUnset) atomicMin(&c->nxt[k % 3], m);
         if (inj) {
             atomicAdd((unsigned long long *)&c->pkts_injected, (unsigned long long)inj);
             atomicAdd((unsigned long long *)&c->pkt_hops, (unsigned long long)inj);
@@ -985,31 +1079,53 @@ __device__ __noinline__ void rank_tick(const Params &P, const ExpRec &X, u32 e, 
 }
 
 // ---------------------------------------------------------------- megakernel
-constexpr int kBlock = 256;
+constexpr int kBlock = 512;
 constexpr int kWarps = kBlock / 32;
 
+// Each warp owns a contiguous chunk of work items (an experiment's items are
+// contiguous: its switches, then its rank groups).  Per step it reads the
+// wake ticks of 32 items at once, ballots the ones due, reports the pending
+// wakes of the others (one atomic per experiment per warp), and processes the
+// due ones one after the other with the whole warp.
 __global__ void __launch_bounds__(kBlock, 1) k_megakernel(Params P)
 {
     __shared__ SwSmem smem[kWarps];
+    const u32 full = 0xffffffffu;
     const u32 warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const u32 gwarp = blockIdx.x * kWarps + warp;
     const u32 nwarps = gridDim.x * kWarps;
-    const u32 gthread = blockIdx.x * blockDim.x + threadIdx.x;
-    const u32 nthreads = gridDim.x * blockDim.x;
+    const u32 per = (P.n_items + nwarps - 1) / nwarps;
+    const u32 i0 = min(gwarp * per, P.n_items), i1 = min(i0 + per, P.n_items);
+    const bool leader_thread = blockIdx.x == 0 && threadIdx.x == 0;
     for (u32 k = 0;; k++) {
-        if (gthread == 0) P.glob->run_cnt[(k + 1) % 3] = 0;   // last read after barrier k-2
-        for (u32 e = gthread; e < P.n_exps; e += nthreads) exp_control(P, e, k);
-        for (u32 it = gwarp; it < P.n_items; it += nwarps) {
-            u32 e = P.item_exp[it], loc = P.item_loc[it];
-            u32 t = exp_tick(P, e, k);
-            if (t == kUnset) continue;
-            const ExpRec X = P.exp[e];
-            if (loc < X.nsw) switch_tick(P, X, e, loc, t, k, &smem[warp]);
-            else rank_tick(P, X, e, (loc - X.nsw) * 32 + lane, t, k);
+        if (leader_thread) P.glob->run_cnt[(k + 1) % 3] = 0;   // last read after barrier k-2
+        for (u32 base = i0; base < i1; base += 32) {
+            const u32 it = base + lane;
+            const bool valid = it < i1;
+            const u32 e = valid ? P.item_exp[it] : kUnset;
+            const u32 loc = valid ? P.item_loc[it] : 0;
+            const u32 t = valid ? exp_tick(P, e, k) : kUnset;
+            if (valid && loc == 0) exp_control(P, e, k, t);
+            const u32 w = t != kUnset ? ld_rlx32(&P.wake[it]) : kUnset;
+            const bool due = t != kUnset && w <= t;
+            const u32 peers = __match_any_sync(full, e);
+            const u32 rep = __reduce_min_sync(peers, due ? kUnset : w);
+            if (e != kUnset && rep != kUnset && lane == (u32)__ffs(peers) - 1)
+                atomicMin(&P.ctl[e].nxt[k % 3], rep);
+            u32 M = __ballot_sync(full, due);
+            while (M) {
+                const u32 j = (u32)__ffs(M) - 1;
+                M &= M - 1;
+                const u32 ej = __shfl_sync(full, e, j), lj = __shfl_sync(full, loc, j),
+                          tj = __shfl_sync(full, t, j);
+                const ExpRec X = P.exp[ej];
+                if (lj < X.nsw) switch_tick(P, X, ej, lj, tj, k, &smem[warp]);
+                else rank_tick(P, X, ej, (lj - X.nsw) * 32 + lane, tj, k);
+            }
         }
         if (!grid_barrier(P, k)) break;
         if (ld_rlx32(&P.glob->run_cnt[k % 3]) == 0) {
-            if (gthread == 0) P.glob->steps = k + 1;
+            if (leader_thread) P.glob->steps = k + 1;
             break;
         }
     }

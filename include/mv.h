@@ -140,7 +140,9 @@ typedef struct mv_batch_desc {
  * Results, written by mv_results into caller-owned HOST buffers (any
  * pointer may be NULL to skip that field).  Per experiment (n_exps): status
  * (MV_EXP_*), end_tick (latest node end, the iteration time; MV_UNSET if no
- * node ended), now (the experiment's clock), packets injected, packet-hops
+ * node ended), now (the experiment's clock: where a budget-stopped one
+ * resumes; one past end_tick for one that stopped for good, 0 if no node
+ * ended), packets injected, packet-hops
  * (one packet placed on one link), packets delivered, messages delivered,
  * digest (order-independent 64-bit sum over delivered messages of a hash of
  * (sender node, connection key, delivery tick)), rec_count (records

@@ -24,9 +24,12 @@
  *
  * Every experiment is simulated on its own, tick by tick, with one object
  * per entity.  Within a tick the phases run over all entities in index
- * order; cross-entity reads see the state at the start of the tick (queue
- * snapshots, "joined before this tick"), which is what makes the result
- * independent of the order entities are visited in.
+ * order.  Information that crosses entities is never from the current tick:
+ * queue entries become visible at their ready tick, credit for a popped
+ * entry travels back over its link (delta + 1 ticks), a rank's join reaches
+ * its peers after one minimum link latency, and acknowledgements carry their
+ * own arrival tick.  That makes the result independent of the order entities
+ * are visited in.
  *
  * Parity pins live in tests/: the lone-message closed form, the pipelined
  * broadcast closed form, a contention-free ring evaluated as a longest path,
@@ -120,6 +123,7 @@ typedef struct nic {
     uint32_t pend_node[NPEND], pend_start[NPEND];
     int n_pend;
     int n_lanes;          /* lanes in use (skip the scan when none)        */
+    uint64_t used_mask;   /* bit q set when lane slot q is in use           */
     uint32_t act[NACT];
     int n_act;
 } nic;
@@ -154,7 +158,10 @@ typedef struct sim {
     uint64_t chunk, dur_seed, ecmp_seed, gpu_mem;
     /* dynamic state */
     uint32_t nf;                    /* queues: Q switch ingress + H NIC rx */
-    uint32_t *head, *tail, *head0, *tail0;
+    uint32_t *head, *tail, *tail0;
+    uint32_t *poplog;               /* nf * 64: tick of each of the last 64 pops */
+    uint32_t *credit_delay;         /* nf: delta + 1 of the link feeding the queue */
+    uint32_t rdv_delay;             /* 1 + smallest link delta of the topology */
     pkt *slots;                     /* nf * cap */
     uint32_t *eg_busy, *eg_rr;      /* Q */
     uint32_t *sw_queued;            /* S: packets in the switch's ingress queues */
@@ -488,6 +495,7 @@ static void net_join(sim *s, uint32_t r, uint32_t u, uint32_t t)
             L->m = 0; L->nmsg = nm;
             L->pkts_left = lane_setup(s, L);
             n->n_lanes++;
+            n->used_mask |= 1ULL << slot;
             out += nm;
         }
     }
@@ -593,7 +601,28 @@ static uint32_t downstream(sim *s, uint32_t q)
 }
 /* credit: may a sender push into queue f this tick?  Entries popped this
  * tick free their slot from the next tick on (start-of-tick snapshot). */
-static int has_credit(sim *s, uint32_t f) { return s->tail[f] - s->head0[f] < s->cap; }
+/* Credit (lossless, PFC-like): a sender may push into queue f at tick t only
+ * if the queue holds fewer than cap entries as far as the sender knows.  An
+ * entry counts from its push until its pop's credit gets back to the sender,
+ * which travels back over the link: pop tick + delta + 1 (the queue's
+ * credit_delay).  Pops are at most one per tick, so only the last
+ * credit_delay - 1 pops can still be on their way. */
+static int has_credit(sim *s, uint32_t f, uint32_t t)
+{
+    uint32_t h = s->head[f], back = 0, d = s->credit_delay[f];
+    while (back < h && back < 64) {
+        uint32_t pt = s->poplog[(size_t)f * 64 + (h - 1 - back) % 64];
+        if (pt + d <= t) break;          /* this pop's credit has arrived */
+        back++;
+    }
+    return s->tail[f] - (h - back) < s->cap;
+}
+
+static void pop(sim *s, uint32_t f, uint32_t t)
+{
+    s->poplog[(size_t)f * 64 + s->head[f] % 64] = t;
+    s->head[f]++;
+}
 /* the head entry, if it was present at the start of the tick and is ready */
 static pkt *ready_head(sim *s, uint32_t f, uint32_t t)
 {
@@ -633,12 +662,12 @@ static void forward(sim *s, uint32_t w, uint32_t t)
         uint32_t qe = base + e;
         if (wanted[e] == 0 || s->eg_busy[qe] > t) continue;
         uint32_t d = downstream(s, qe);
-        if (!has_credit(s, d)) continue;
+        if (!has_credit(s, d, t)) continue;
         for (uint32_t k = 0; k < P; k++) {
             uint32_t i = (s->eg_rr[qe] + k) % P;
             if (tgt[i] != (int32_t)e) continue;
             pkt p = *slot(s, base + i, s->head[base + i]);
-            s->head[base + i]++;
+            pop(s, base + i, t);
             s->sw_queued[w]--;
             p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
             p.hopsum += s->port_delta[qe] + 1;
@@ -661,38 +690,45 @@ static void inject(sim *s, uint32_t r, uint32_t t)
     nic *n = &s->nics[r];
     if (n->n_lanes == 0 || n->busy > t) return;
     uint32_t f = s->host_port[r];
-    if (!has_credit(s, f)) return;
-    for (uint32_t k = 0; k < NLANE; k++) {
-        uint32_t q = (n->rr + k) % NLANE;
-        lane *L = &n->lanes[q];
-        if (!L->used) continue;
-        int ok = 1;
-        for (uint32_t b = 0; b < 3; b++)
-            if ((L->dep_mask >> b) & 1u)
-                if (n->port_count[s->port_base[L->node] + L->dep_base + b] < L->dep_need) ok = 0;
-        if (!ok) continue;
-        uint32_t c = coll_of(s, L->node);
-        uint32_t dnode = mnode(s, c, L->dst_member);
-        if (s->start[dnode] == UNSET || s->start[dnode] >= t) continue;
-        pkt p;
-        p.ready = t + s->host_sigma[r] + s->host_delta[r];
-        p.dst = mrank(s, c, L->dst_member);
-        p.hopsum = s->host_delta[r] + 1;
-        p.sender = L->node;
-        p.pslot = s->port_base[dnode] + L->dst_port;
-        p.last = L->pkts_left == 1;
-        p.key = L->key;
-        push(s, f, &p);
-        n->busy = t + s->host_sigma[r];
-        n->rr = (q + 1) % NLANE;
-        s->pkts_injected++;
-        s->pkt_hops++;
-        s->changed = 1;
-        if (--L->pkts_left == 0) {
-            if (++L->m == L->nmsg) { L->used = 0; n->n_lanes--; }
-            else L->pkts_left = lane_setup(s, L);
+    if (!has_credit(s, f, t)) return;
+    /* occupied slots in round-robin order from the pointer: those at or
+     * after it, then those before it */
+    for (int pass = 0; pass < 2; pass++) {
+        uint64_t m = pass == 0 ? (n->used_mask & (~0ULL << n->rr)) : (n->used_mask & ((1ULL << n->rr) - 1));
+        while (m) {
+            uint32_t q = (uint32_t)__builtin_ctzll(m);
+            m &= m - 1;
+            lane *L = &n->lanes[q];
+            int ok = 1;
+            for (uint32_t b = 0; b < 3; b++)
+                if ((L->dep_mask >> b) & 1u)
+                    if (n->port_count[s->port_base[L->node] + L->dep_base + b] < L->dep_need) ok = 0;
+            if (!ok) continue;
+            uint32_t c = coll_of(s, L->node);
+            uint32_t dnode = mnode(s, c, L->dst_member);
+            /* rendezvous: the destination's join reaches this rank one
+             * link latency (1 + smallest delta) after it happened */
+            if (s->start[dnode] == UNSET || s->start[dnode] + s->rdv_delay > t) continue;
+            pkt p;
+            p.ready = t + s->host_sigma[r] + s->host_delta[r];
+            p.dst = mrank(s, c, L->dst_member);
+            p.hopsum = s->host_delta[r] + 1;
+            p.sender = L->node;
+            p.pslot = s->port_base[dnode] + L->dst_port;
+            p.last = L->pkts_left == 1;
+            p.key = L->key;
+            push(s, f, &p);
+            n->busy = t + s->host_sigma[r];
+            n->rr = (q + 1) % NLANE;
+            s->pkts_injected++;
+            s->pkt_hops++;
+            s->changed = 1;
+            if (--L->pkts_left == 0) {
+                if (++L->m == L->nmsg) { L->used = 0; n->n_lanes--; n->used_mask &= ~(1ULL << q); }
+                else L->pkts_left = lane_setup(s, L);
+            }
+            return;
         }
-        return;
     }
 }
 
@@ -707,7 +743,7 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     pkt *h = ready_head(s, f, t);
     if (!h) return;
     pkt p = *h;
-    s->head[f]++;
+    pop(s, f, t);
     s->pkts_delivered++;
     s->changed = 1;
     if (!p.last) return;
@@ -763,6 +799,26 @@ static uint32_t next_event(sim *s, uint32_t t)
     }
     for (uint32_t q = 0; q < s->Q; q++)
         if (s->eg_busy[q] > t && s->eg_busy[q] < best) best = s->eg_busy[q];
+    /* credit still travelling back to a sender */
+    for (uint32_t f = 0; f < s->nf; f++) {
+        uint32_t h = s->head[f];
+        for (uint32_t back = 0; back < h && back < 64; back++) {
+            uint32_t at = s->poplog[(size_t)f * 64 + (h - 1 - back) % 64] + s->credit_delay[f];
+            if (at <= t) break;
+            if (at < best) best = at;
+        }
+    }
+    /* a destination's join still on its way to a sending rank */
+    for (uint32_t r = 0; r < s->R; r++) {
+        nic *n = &s->nics[r];
+        for (int q = 0; q < NLANE; q++) {
+            if (!n->lanes[q].used) continue;
+            uint32_t c = coll_of(s, n->lanes[q].node);
+            uint32_t st = s->start[mnode(s, c, n->lanes[q].dst_member)];
+            if (st != UNSET && st + s->rdv_delay > t && st + s->rdv_delay < best)
+                best = st + s->rdv_delay;
+        }
+    }
     return best;
 }
 
@@ -776,7 +832,6 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
     while (s->status == ST_RUNNING) {
         if (s->nodes_left == 0) { s->status = ST_DONE; break; }
         if (t >= limit) break;
-        memcpy(s->head0, s->head, sizeof(uint32_t) * s->nf);
         memcpy(s->tail0, s->tail, sizeof(uint32_t) * s->nf);
         s->changed = 0;
         for (uint32_t r = 0; r < s->R && s->status == ST_RUNNING; r++) dag_step(s, r, t);
@@ -884,8 +939,21 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     s->nf = s->Q + s->H;
     s->head = calloc(s->nf, sizeof(uint32_t));
     s->tail = calloc(s->nf, sizeof(uint32_t));
-    s->head0 = calloc(s->nf, sizeof(uint32_t));
     s->tail0 = calloc(s->nf, sizeof(uint32_t));
+    s->poplog = calloc((size_t)s->nf * 64, sizeof(uint32_t));
+    s->credit_delay = calloc(s->nf, sizeof(uint32_t));
+    s->rdv_delay = UNSET;
+    for (uint32_t q = 0; q < s->Q; q++) {            /* switch ingress q: fed by its peer */
+        int32_t pe = s->port_peer[q];
+        uint32_t dl = pe >= 0 ? s->port_delta[pe] : s->host_delta[-pe - 1];
+        s->credit_delay[q] = dl + 1;
+        if (dl + 1 < s->rdv_delay) s->rdv_delay = dl + 1;
+    }
+    for (uint32_t h = 0; h < s->H; h++) {            /* NIC receive queue: fed by its switch port */
+        uint32_t dl = s->port_delta[s->host_port[h]];
+        s->credit_delay[s->Q + h] = dl + 1;
+        if (dl + 1 < s->rdv_delay) s->rdv_delay = dl + 1;
+    }
     s->slots = calloc((size_t)s->nf * s->cap, sizeof(pkt));
     s->eg_busy = calloc(s->Q + 1, sizeof(uint32_t));
     s->eg_rr = calloc(s->Q + 1, sizeof(uint32_t));
@@ -923,7 +991,9 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     }
     out->status[e] = (uint32_t)s->status;
     out->end_tick[e] = any ? endt : UNSET;
-    out->now[e] = now;
+    /* the clock: where a stopped-by-budget experiment resumes; for one that
+     * stopped for good, one past its latest node end (0 if none ended) */
+    out->now[e] = s->status == ST_RUNNING ? now : (any ? endt + 1 : 0);
     out->pkts_injected[e] = s->pkts_injected;
     out->pkt_hops[e] = s->pkt_hops;
     out->pkts_delivered[e] = s->pkts_delivered;
@@ -935,7 +1005,8 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
     free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
     free(s->col_base); free(s->node_rank); free(s->node_member);
-    free(s->head); free(s->tail); free(s->head0); free(s->tail0); free(s->slots);
+    free(s->head); free(s->tail); free(s->tail0); free(s->slots);
+    free(s->poplog); free(s->credit_delay);
     free(s->eg_busy); free(s->eg_rr); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
     free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
     return 0;

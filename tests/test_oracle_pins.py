@@ -59,9 +59,10 @@ def test_lone_message_closed_form(n, delta, topo):
     """A lone message of n packets over L links of one tick each: the last
     packet reaches the receiver (n-1) + L*(1+delta) ticks after the first
     injection (serialisation of the packets behind the head plus, per hop,
-    propagation and per-packet serialisation).  The first injection is tick 1
-    (both ends join at tick 0).  The sender's acknowledgement arrives
-    L*(delta+1) ticks after delivery."""
+    propagation and per-packet serialisation).  Both ends join at tick 0 and
+    the join reaches the sender 1 + delta ticks later, so the first injection
+    is at tick 1 + delta.  The sender's acknowledgement arrives L*(delta+1)
+    ticks after delivery."""
     if topo == "switch":
         t, src, dst, L = I.single_switch(2, 1, delta), 0, 1, 2
     elif topo == "leafspine":
@@ -70,7 +71,7 @@ def test_lone_message_closed_form(n, delta, topo):
         t, src, dst, L = I.fat_tree(4, delta), 0, 15, 6
     w = I.lone_message(t.n_hosts, src, dst, n * 4096)
     r = run1(t, w, chunk=1 << 30)
-    done = 1 + (n - 1) + L * (1 + delta)
+    done = (1 + delta) + (n - 1) + L * (1 + delta)
     ends = dict(zip(["send", "recv"], r["node_end"][[0, 1]] if src < dst else r["node_end"][[1, 0]]))
     assert ends["recv"] == done
     assert ends["send"] == done + L * (delta + 1)
@@ -89,15 +90,17 @@ def test_heterogeneous_path_closed_form(n):
     assert r["node_end"][1] == 1 + (n - 1) * max(sig) + sum(s + d for s, d in zip(sig, dl))
 
 
-def test_credit_loop_needs_delta_plus_two():
-    """Line rate needs queue capacity >= delta + 2 (entries in flight count
-    against the credit).  One slot fewer must make the message slower."""
+def test_credit_loop_needs_two_delta_plus_two():
+    """A slot is held from the push until the pop's credit is back: sigma +
+    delta to reach the head, delta + 1 for the credit to return.  Line rate
+    therefore needs queue capacity >= 2*delta + 2; one slot fewer must make
+    the message slower."""
     delta, n = 4, 30
     t = I.single_switch(2, 1, delta)
     w = I.lone_message(2, 0, 1, n * 4096)
-    full = run1(t, w, chunk=1 << 30, cap=delta + 2)["node_end"][1]
-    short = run1(t, w, chunk=1 << 30, cap=delta + 1)["node_end"][1]
-    assert full == 1 + (n - 1) + 2 * (1 + delta)
+    full = run1(t, w, chunk=1 << 30, cap=2 * delta + 2)["node_end"][1]
+    short = run1(t, w, chunk=1 << 30, cap=2 * delta + 1)["node_end"][1]
+    assert full == (1 + delta) + (n - 1) + 2 * (1 + delta)
     assert short > full
 
 
@@ -158,10 +161,11 @@ def test_pipelined_broadcast_tends_to_t():
 
 
 # ---------------------------------------------------------------- ring all-reduce
-def ring_longest_path(N, loops, steps, n, lat):
+def ring_longest_path(N, loops, steps, n, lat, first=1):
     """Independent evaluator of a contention-free ring (one channel): message
     (l,k) of member i starts after its previous message finished injecting and
-    one tick after member i received (l,k-1); it injects n packets on
+    one tick after member i received (l,k-1); the first message starts at
+    `first` (when the joins have reached the senders); it injects n packets on
     consecutive ticks and reaches member i+1 lat[i] ticks after its last
     packet.  Returns each member's last delivery tick."""
     M = loops * steps
@@ -170,7 +174,7 @@ def ring_longest_path(N, loops, steps, n, lat):
     for m in range(M):
         k = m % steps
         for i in range(N):
-            s = 1 if m == 0 else start[i][m - 1] + n
+            s = first if m == 0 else start[i][m - 1] + n
             if k >= 1:
                 s = max(s, recv[i][m - 1] + 1)
             start[i][m] = s
@@ -196,7 +200,7 @@ def test_ring_contention_free_longest_path(kind, steps_of, N, loops, blk):
     steps = steps_of(N)
     got = list(r["node_end"][:N])
     lat = [2 * (1 + delta)] * N
-    recv = ring_longest_path(N, loops, steps, blk, lat)
+    recv = ring_longest_path(N, loops, steps, blk, lat, first=1 + delta)
     # a member finishes at max(last delivery to it, ack of its own last message)
     want = [max(recv[i], recv[(i + 1) % N] + 2 * (delta + 1)) for i in range(N)]
     assert got == want
@@ -213,7 +217,7 @@ def test_ring_leafspine_paths_of_two_lengths():
     w = I.single_collective(N, I.AR, N * C * loops)
     r = run1(t, w, nc=1, chunk=C)
     lat = [(4 if i in (3, 7) else 2) * (1 + delta) for i in range(N)]
-    recv = ring_longest_path(N, loops, 2 * (N - 1), blk, lat)
+    recv = ring_longest_path(N, loops, 2 * (N - 1), blk, lat, first=1 + delta)
     ack = [(4 if i in (3, 7) else 2) * (delta + 1) for i in range(N)]
     want = [max(recv[i], recv[(i + 1) % N] + ack[i]) for i in range(N)]
     assert list(r["node_end"][:N]) == want
@@ -260,7 +264,7 @@ def test_tree_two_members_closed_form(n):
     t = I.single_switch(2, 1, delta)
     w = I.single_collective(2, I.AR, n * 4096)
     r = run1(t, w, algo=I.TREE, nc=1, chunk=1 << 30)
-    up = 1 + (n - 1) + L * (1 + delta)
+    up = (1 + delta) + (n - 1) + L * (1 + delta)
     down = up + 1 + (n - 1) + L * (1 + delta)
     assert r["node_end"][1] == down
     assert r["node_end"][0] == down + L * (delta + 1)
@@ -280,15 +284,15 @@ def test_tree_packet_totals():
 @pytest.mark.parametrize("N,n", [(2, 5), (3, 4), (4, 2)])
 def test_alltoall_rotation_closed_form(N, n):
     """Equal sizes, one channel, one switch: in rotation order every phase is
-    a permutation, so no link is shared; each member's last delivery is at
-    (N-1)*n + L*(1+delta) after the first injection at tick 1, minus one."""
+    a permutation, so no link is shared; each member's last delivery is
+    (N-1)*n - 1 + L*(1+delta) ticks after the first injection at tick 1+delta."""
     delta, L = 1, 2
     t = I.single_switch(N, 1, delta)
     w = I.Workload(N)
     m = {(i, j): n * 4096 for i in range(N) for j in range(N) if i != j}
     w.collective(I.A2A, list(range(N)), 0, a2a=m)
     r = run1(t, w, nc=1, chunk=1 << 30)
-    recv = (N - 1) * n + L * (1 + delta)
+    recv = (1 + delta) + (N - 1) * n - 1 + L * (1 + delta)
     assert list(r["node_end"][:N]) == [recv + L * (delta + 1)] * N
     assert r["pkts_injected"][0] == N * (N - 1) * n
 
