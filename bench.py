@@ -191,7 +191,7 @@ def run_gpu(args, rank: int, world: int):
     stream = torch.cuda.Stream(dev)
     sim = mv.Simulator(packed, device=str(dev), stream=stream)
     n_levels = int(packed["sw_level"].max())
-    launches_per_step = n_levels + 5                  # routes per level, up lists, 2 init, reset, megakernel
+    launches_per_step = n_levels + 4                  # routes per level, up lists, 2 init, megakernel
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def step():

@@ -4,7 +4,10 @@
 // here allocates device memory.
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <numeric>
+#include <tuple>
 #include <new>
 #include <vector>
 
@@ -19,6 +22,10 @@ struct Region {
     u64 off = 0, bytes = 0;
 };
 
+// Largest shared-memory image of one experiment's dynamic state; larger
+// experiments keep their state in global memory (wake table still staged).
+constexpr u64 kStageMax = 112 * 1024;
+
 // Byte layout of the workspace: a static part uploaded from the host, then
 // a dynamic part cleared and filled by the set-up kernels.
 struct Layout {
@@ -26,8 +33,10 @@ struct Layout {
     u32 T = 0, W = 0, E = 0;
     u64 nsw = 0, nports = 0, nhosts = 0, nranks = 0, nnodes = 0, nedges = 0, ncolls = 0,
         nmemb = 0, na2a = 0, na2a_in = 0;
-    u64 route_bytes = 0, q_total = 0, slot_total = 0, eg_total = 0, rk_total = 0,
+    u64 route_bytes = 0, q_total = 0, slot_total = 0, plog_total = 0, eg_total = 0,
+        rk_total = 0, pend_total = 0, act_total = 0, lane_total = 0, portc_total = 0,
         nd_total = 0, rec_total = 0, items = 0;
+    u32 warps = 1, image = 16;      // megakernel block size and shared image budget
     u32 max_level = 0, max_nodes = 0, max_queues = 0, max_ranks = 0;
     u64 max_pairs = 0;
     // host copies of the derived tables
@@ -35,7 +44,7 @@ struct Layout {
     std::vector<WorkRec> work;
     std::vector<ExpRec> exp;
     std::vector<u32> sw_pstart, port_sw, rank_first, succ_start, node_member, coll_mstart,
-        memb_row, memb_col, item_exp, item_loc, node_rank;
+        memb_row, memb_col, node_rank, order;
     // regions
     Region r_topo, r_work, r_exp, r_sw_nports, r_sw_level, r_sw_pstart, r_port_sw, r_port_peer,
         r_port_sigma, r_port_delta, r_host_port, r_host_sigma, r_host_delta, r_rank_first,
@@ -44,7 +53,7 @@ struct Layout {
         r_coll_intra, r_coll_nmembers, r_coll_parts, r_coll_alpha, r_coll_beta_num,
         r_coll_beta_den, r_coll_mstart, r_coll_bytes, r_member_rank, r_member_node,
         r_member_a2a_n, r_memb_row, r_a2a_dst, r_member_a2a_in_n, r_memb_col, r_a2a_in_src,
-        r_a2a_bytes, r_a2a_in_bytes, r_mem, r_item_exp, r_item_loc, r_node_rank;
+        r_a2a_bytes, r_a2a_in_bytes, r_mem, r_order, r_node_rank;
     u64 static_bytes = 0;
     Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_pend, r_act,
         r_lanes, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
@@ -61,13 +70,6 @@ struct Layout {
         return r;
     }
 };
-
-u64 sum32(const u32 *a, u64 n)
-{
-    u64 s = 0;
-    for (u64 i = 0; i < n; i++) s += a[i];
-    return s;
-}
 
 // Validate the descriptor and compute the layout.  Returns an MV_* code.
 int plan(const mv_batch_desc *d, Layout &L)
@@ -130,6 +132,12 @@ int plan(const mv_batch_desc *d, Layout &L)
             if (sg == 0 || sg > 65535 || dl + 1 > kPopLog) return MV_EINVAL;
             R.rdv = std::min(R.rdv, dl + 1);
         }
+        // pop log: only the last (delta + 1) - 1 pops of a queue are ever read
+        u32 dmax = 1;
+        for (u32 p = 0; p < R.nq; p++) dmax = std::max(dmax, d->port_delta[R.port_off + p] + 1);
+        for (u32 h = 0; h < R.nh; h++) dmax = std::max(dmax, d->host_delta[R.host_off + h] + 1);
+        R.plog = 1;
+        while (R.plog < dmax) R.plog *= 2;
     }
     // ---- workloads
     L.work.resize(L.W);
@@ -243,7 +251,56 @@ int plan(const mv_batch_desc *d, Layout &L)
         if (mm[9] && (mm[1] == 0 || mm[2] == 0)) return MV_EINVAL;
     }
     // ---- experiments
+    // Per-rank table strides: the fixed limit, or less when no rank of the
+    // workload can ever need that many (each NET node adds at most its
+    // channels x lanes-per-channel send lanes and that many receive
+    // counters; first-fit placement never reaches past their sum), so that
+    // results and overflow statuses are those of the fixed-size tables.
+    struct Caps { u32 lane, port, pend, act; };
+    std::map<std::tuple<u32, u32, u32>, Caps> caps_cache;
+    auto caps_of = [&](u32 w, u32 nc, u32 algo) -> Caps {
+        auto key = std::make_tuple(w, nc, algo);
+        auto it = caps_cache.find(key);
+        if (it != caps_cache.end()) return it->second;
+        const WorkRec &R = L.work[w];
+        Caps c = {1, 1, 1, 1};
+        u32 n = 0;
+        for (u32 r = 0; r < R.nr; r++) {
+            u64 lanes = 0, ports = 0, acts = 0;
+            u32 cnt = d->rank_nnodes[R.rank_off + r];
+            for (u32 u = n; u < n + cnt; u++) {
+                u32 k = d->node_kind[R.node_off + u];
+                if (k == NODE_COMPUTE) continue;
+                acts++;
+                if (k != NODE_NET) continue;
+                u32 kind = d->coll_kind[R.coll_off + d->node_arg[R.node_off + u]];
+                bool one = kind == COLL_RELAY || kind == COLL_P2P;
+                u64 per = (one ? 1ull : nc) * ((kind == COLL_AR && algo == ALGO_TREE) ? 3ull : 1ull);
+                lanes += per;
+                ports += (one || kind == COLL_A2A) ? 1ull : per;
+            }
+            c.lane = std::max<u32>(c.lane, (u32)std::min<u64>(lanes, kNLane));
+            c.port = std::max<u32>(c.port, (u32)std::min<u64>(ports, kNPort));
+            c.pend = std::max<u32>(c.pend, std::min<u32>(cnt, kNPend));
+            c.act = std::max<u32>(c.act, (u32)std::min<u64>(acts, kNAct));
+            n += cnt;
+        }
+        caps_cache[key] = c;
+        return c;
+    };
+    // processing order: largest first (bytes moved over the network), so
+    // the persistent blocks finish close together
+    std::vector<u64> work_cost(L.W, 0);
+    for (u32 w = 0; w < L.W; w++) {
+        const WorkRec &R = L.work[w];
+        for (u32 u = 0; u < R.nn; u++)
+            if (d->node_kind[R.node_off + u] == NODE_NET)
+                work_cost[w] += d->coll_bytes[R.coll_off + d->node_arg[R.node_off + u]] / 4096 + 1;
+    }
     L.exp.resize(L.E);
+    u64 items = 0;
+    u32 max_items = 1;
+    u64 full_max = 0, wake_max = 16;
     for (u32 e = 0; e < L.E; e++) {
         ExpRec &X = L.exp[e];
         std::memset(&X, 0, sizeof X);
@@ -271,39 +328,59 @@ int plan(const mv_batch_desc *d, Layout &L)
                 if (!d->coll_intra[W.coll_off + c] && d->coll_kind[W.coll_off + c] != COLL_RELAY)
                     return MV_EINVAL;
         }
+        Caps cp = caps_of(X.work, X.nc, X.algo);
+        X.lane_cap = cp.lane;
+        X.port_cap = cp.port;
+        X.pend_cap = cp.pend;
+        X.act_cap = cp.act;
         X.nq = T.nq + T.nh;
         X.nsw = T.nsw;
         X.nr = W.nr;
         X.nn = W.nn;
         X.q_off = L.q_total;
         X.slot_off = L.slot_total;
+        X.plog_off = L.plog_total;
         X.eg_off = L.eg_total;
         X.rk_off = L.rk_total;
+        X.pend_off = L.pend_total;
+        X.act_off = L.act_total;
+        X.lane_off = L.lane_total;
+        X.portc_off = L.portc_total;
         X.nd_off = L.nd_total;
         X.rec_off = L.rec_total;
         L.q_total += X.nq;
         L.slot_total += (u64)X.nq * X.cap;
+        L.plog_total += (u64)X.nq * T.plog;
         L.eg_total += T.nq;
         L.rk_total += W.nr;
+        L.pend_total += (u64)W.nr * X.pend_cap;
+        L.act_total += (u64)W.nr * X.act_cap;
+        L.lane_total += (u64)W.nr * X.lane_cap;
+        L.portc_total += (u64)W.nr * X.port_cap;
         L.nd_total += W.nn;
         L.rec_total += X.rec_cap;
         L.max_nodes = std::max(L.max_nodes, W.nn);
         L.max_queues = std::max(L.max_queues, X.nq);
         L.max_ranks = std::max(L.max_ranks, W.nr);
-        X.item_off = (u32)L.item_exp.size();
+        X.item_off = (u32)items;
         X.n_items = T.nsw + (W.nr + 31) / 32;
-        for (u32 s = 0; s < T.nsw; s++) {
-            L.item_exp.push_back(e);
-            L.item_loc.push_back(s);
-        }
-        for (u32 g = 0; g < (W.nr + 31) / 32; g++) {
-            L.item_exp.push_back(e);
-            L.item_loc.push_back(T.nsw + g);
-        }
-        if (L.nd_total > 0xFFFFFFFFull * 4 || L.item_exp.size() > 0xFFFFFFFFull)
-            return MV_EOVERFLOW;
+        items += X.n_items;
+        max_items = std::max(max_items, X.n_items);
+        u64 off[IM_N];
+        u64 img = image_layout(X, T.plog, T.nq, off);
+        X.stage_bytes = img <= kStageMax ? (u32)img : 0;
+        if (X.stage_bytes) full_max = std::max(full_max, img);
+        wake_max = std::max(wake_max, im_round(12ull * X.n_items));
+        if (L.nd_total > 0xFFFFFFFFull * 4 || items > 0xFFFFFFFFull) return MV_EOVERFLOW;
     }
-    L.items = L.item_exp.size();
+    L.items = items;
+    L.warps = std::min<u32>(kMaxWarps, max_items);
+    L.image = (u32)std::min<u64>(std::max(full_max, wake_max), kStageMax);
+    L.order.resize(L.E);
+    std::iota(L.order.begin(), L.order.end(), 0u);
+    std::stable_sort(L.order.begin(), L.order.end(), [&](u32 a, u32 b) {
+        return work_cost[L.exp[a].work] > work_cost[L.exp[b].work];
+    });
     // ---- regions
     L.cur = 0;
     L.r_topo = L.take(sizeof(TopoRec) * L.T);
@@ -351,8 +428,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_a2a_bytes = L.take(8 * L.na2a);
     L.r_a2a_in_bytes = L.take(8 * L.na2a_in);
     L.r_mem = L.take(80 * L.W);
-    L.r_item_exp = L.take(4 * L.items);
-    L.r_item_loc = L.take(4 * L.items);
+    L.r_order = L.take(4ull * std::max<u32>(L.E, 1));
     L.r_node_rank = L.take(4 * L.nnodes);
     L.static_bytes = L.cur;
     L.r_route = L.take(L.route_bytes);
@@ -363,11 +439,11 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_slots = L.take(16 * L.slot_total);
     L.r_eg = L.take(8 * L.eg_total);
     L.r_rk = L.take(sizeof(RankCtl) * L.rk_total);
-    L.r_pend = L.take(8ull * kNPend * L.rk_total);
-    L.r_act = L.take(4ull * kNAct * L.rk_total);
-    L.r_lanes = L.take(sizeof(Lane) * kNLane * L.rk_total);
-    L.r_ports = L.take(8ull * kNPort * L.rk_total);
-    L.r_poplog = L.take(4ull * kPopLog * L.q_total);
+    L.r_pend = L.take(8ull * L.pend_total);
+    L.r_act = L.take(4ull * L.act_total);
+    L.r_lanes = L.take(sizeof(Lane) * L.lane_total);
+    L.r_ports = L.take(8ull * L.portc_total);
+    L.r_poplog = L.take(4ull * L.plog_total);
     L.r_nd_pred = L.take(4 * L.nd_total);
     L.r_nd_cand = L.take(4 * L.nd_total);
     L.r_nd_start = L.take(4 * L.nd_total);
@@ -380,7 +456,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_rec_key = L.take(4 * L.rec_total);
     L.r_rec_tick = L.take(4 * L.rec_total);
     L.r_glob = L.take(sizeof(Glob));
-    L.r_wake = L.take(4 * L.items);
+    L.r_wake = L.take(12 * L.items);
     L.total = L.cur;
     return MV_OK;
 }
@@ -464,17 +540,15 @@ Params make_params(void *ws, const Layout &L)
     P.rec_sender = at<u32>(ws, L.r_rec_sender);
     P.rec_key = at<u32>(ws, L.r_rec_key);
     P.rec_tick = at<u32>(ws, L.r_rec_tick);
-    P.item_exp = at<u32>(ws, L.r_item_exp);
-    P.item_loc = at<u32>(ws, L.r_item_loc);
+    P.order = at<u32>(ws, L.r_order);
     P.node_rank = at<u32>(ws, L.r_node_rank);
     P.wake = at<u32>(ws, L.r_wake);
-    P.n_items = (u32)L.items;
     P.n_exps = L.E;
     P.n_topos = L.T;
     P.glob = at<Glob>(ws, L.r_glob);
-    P.barrier_timeout_ns = 5000000000ull;
-    P.fault_block = -1;
-    P.fault_step = -1;
+    P.watchdog_ns = 0;
+    P.stage_limit = L.image;
+    P.stage_mode = 0;
     return P;
 }
 
@@ -490,7 +564,6 @@ struct mv_ctx {
     Params P;
     void *ws;
     cudaStream_t stream;
-    u32 blocks;
     std::vector<ExpCtl> host_ctl;
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     bool timed = false;
@@ -522,7 +595,7 @@ const char *mv_strerror(int code)
     case MV_EINVAL: return "invalid batch descriptor or argument";
     case MV_ENOMEM: return "workspace smaller than mv_workspace_bytes()";
     case MV_ECUDA: return "CUDA call failed";
-    case MV_ETIMEOUT: return "grid barrier timed out; kernel returned, results invalid";
+    case MV_ETIMEOUT: return "run stopped by its watchdog; state kept at a tick boundary";
     case MV_EOVERFLOW: return "size or tick count beyond 32-bit limits";
     default: return "unknown status";
     }
@@ -607,8 +680,7 @@ int mv_create(const mv_batch_desc *d, void *ws, uint64_t ws_bytes, void *stream,
     put(img, L.r_a2a_bytes, d->a2a_bytes, 8 * L.na2a);
     put(img, L.r_a2a_in_bytes, d->a2a_in_bytes, 8 * L.na2a_in);
     put(img, L.r_mem, d->mem, 80 * L.W);
-    put(img, L.r_item_exp, L.item_exp.data(), 4 * L.items);
-    put(img, L.r_item_loc, L.item_loc.data(), 4 * L.items);
+    put(img, L.r_order, L.order.data(), 4ull * L.E);
     put(img, L.r_node_rank, L.node_rank.data(), 4 * L.nnodes);
     cudaError_t e = cudaMemcpyAsync(ws, img.data(), L.static_bytes, cudaMemcpyHostToDevice,
                                     c->stream);
@@ -616,15 +688,12 @@ int mv_create(const mv_batch_desc *d, void *ws, uint64_t ws_bytes, void *stream,
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);   // img is freed on return
     if (e == cudaSuccess) e = cudaEventCreate(&c->ev0);
     if (e == cudaSuccess) e = cudaEventCreate(&c->ev1);
-    int bpsm = 0, nsm = 0;
-    if (e == cudaSuccess) e = megakernel_occupancy(&bpsm, &nsm);
-    if (e != cudaSuccess || bpsm == 0) {
+    if (e != cudaSuccess) {
         if (c->ev0) cudaEventDestroy(c->ev0);
         if (c->ev1) cudaEventDestroy(c->ev1);
         delete c;
         return MV_ECUDA;
     }
-    c->blocks = (u32)(bpsm * nsm);
     c->host_ctl.resize(std::max<u32>(L.E, 1));
     *out = c;
     return MV_OK;
@@ -635,16 +704,24 @@ int mv_run_ex(mv_ctx *c, uint32_t max_ticks, const mv_run_opts *o, uint64_t *ste
     if (!c) return MV_EINVAL;
     if (c->L.E == 0) return MV_OK;
     Params P = c->P;
-    u32 blocks = c->blocks;
+    P.max_ticks = max_ticks;
+    u32 warps = c->L.warps, grid = 0;
     if (o) {
-        if (o->barrier_timeout_ns) P.barrier_timeout_ns = o->barrier_timeout_ns;
-        P.fault_block = o->fault_skip_block;
-        P.fault_step = o->fault_skip_step;
-        if (o->grid_blocks) blocks = std::min(o->grid_blocks, c->blocks);
+        if (o->stage > 2) return MV_EINVAL;
+        P.watchdog_ns = o->watchdog_ns;
+        P.stage_mode = o->stage;
+        if (o->block_warps) warps = std::min<u32>(o->block_warps, kMaxWarps);
+        grid = o->grid_blocks;
     }
-    cudaError_t e = launch_run_reset(P, max_ticks, c->stream);
+    const u32 smem = megakernel_smem(warps, c->L.image);
+    int bpsm = 0, nsm = 0;
+    cudaError_t e = megakernel_prepare(warps, smem, &bpsm, &nsm);
+    if (e != cudaSuccess || bpsm == 0) return MV_ECUDA;
+    u32 blocks = std::min<u32>(c->L.E, (u32)(bpsm * nsm));
+    if (grid) blocks = std::min(blocks, grid);
+    e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev0, c->stream);
-    if (e == cudaSuccess) e = launch_megakernel(P, blocks, c->stream);
+    if (e == cudaSuccess) e = launch_megakernel(P, blocks, warps, smem, c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev1, c->stream);
     c->timed = e == cudaSuccess;
     Glob g;

@@ -22,7 +22,8 @@ constexpr u32 kNPend = 64;    // nodes scheduled to start, per rank
 constexpr u32 kNAct = 16;     // running collective memberships, per rank
 constexpr u32 kMaxPorts = 64; // ports per switch (one warp, two ports a lane)
 constexpr u32 kTickLimit = 0xFFF00000u;
-constexpr u32 kPopLog = 64;    // pops remembered per queue (credit delay <= 64)
+constexpr u32 kPopLog = 64;   // credit delay (delta + 1) of a link is at most this
+constexpr u32 kMaxWarps = 16; // warps of the block that steps one experiment
 
 enum : u32 { NODE_COMPUTE = 0, NODE_INTRA = 1, NODE_NET = 2 };
 enum : u32 { COLL_AR = 0, COLL_RS = 1, COLL_AG = 2, COLL_RELAY = 3, COLL_P2P = 4, COLL_A2A = 5 };
@@ -35,6 +36,8 @@ struct TopoRec {
     u32 host_off, sw_off, port_off;
     u32 rdv;                        // 1 + smallest link delta: how late a join reaches peers
     u64 route_off;                  // route table: nsw * nh bytes
+    u32 plog;                       // pop-log entries per queue: power of two >= largest delta + 1
+    u32 pad;
 };
 
 struct WorkRec {
@@ -42,18 +45,21 @@ struct WorkRec {
     u32 rank_off, node_off, edge_off, coll_off, memb_off, a2a_off, a2a_in_off, pad;
 };
 
+// One experiment: parameters, and where its slice of each dynamic array
+// starts (element offsets).  Per-rank tables have per-experiment strides
+// (lane_cap, port_cap, pend_cap, act_cap): the smaller of the fixed limit
+// and what the experiment's DAG can ever need, so small experiments fit in
+// shared memory while the limits (and the overflow status) are unchanged.
 struct ExpRec {
     u32 topo, work, algo, nc, pkt, cap, tick_ps, rec_cap;
     u64 chunk, dur_seed, ecmp_seed, gpu_mem;
-    u64 q_off;      // first queue (switch ingress queues, then NIC receive queues)
-    u64 slot_off;   // first packet slot (queue-major, cap slots per queue)
-    u64 eg_off;     // first egress record (one per switch port)
-    u64 rk_off;     // first rank
-    u64 nd_off;     // first node
-    u64 rec_off;    // first message record
-    u32 nq, nsw, nr, nn;
-    u32 item_off;   // first work item (switches, then groups of 32 ranks)
-    u32 n_items, pad0, pad1;
+    u64 q_off, slot_off, plog_off, eg_off, rk_off, pend_off, act_off, lane_off, portc_off,
+        nd_off, rec_off;
+    u32 nq, nsw, nr, nn;            // queues (switch ingress, then NIC receive), switches, ranks, nodes
+    u32 item_off, n_items;          // work items: switches, then groups of 32 ranks
+    u32 lane_cap, port_cap, pend_cap, act_cap;
+    u32 stage_bytes;                // bytes of the whole dynamic state as one shared-memory image
+    u32 pad;
 };
 
 // One send lane: a stream of messages one rank sends for one channel of one
@@ -72,21 +78,18 @@ struct RankCtl {
     u64 pad;
 };
 
+// Per-experiment control, kept across runs (resume) and read by mv_results.
 struct ExpCtl {
-    u32 status, now, limit, nodes_left;
-    u32 clk[3];              // tick processed at step k (slot k % 3)
-    u32 nxt[3];              // min over pending wake ticks reported at step k
-    u32 rec_count;
-    u32 stop_step;           // first step in which it finished or failed
-    u32 end_max1;            // 1 + latest node end tick (0: none yet)
-    u32 pad;
+    u32 status, now, nodes_left, end_max1;   // end_max1 = 1 + latest node end (0: none yet)
+    u32 rec_count, pad0, pad1, pad2;
     u64 pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
 };
 
 struct Glob {
-    u32 bar_count, bar_gen, error, run_cnt[3];
-    u64 steps;
-    u32 err_step, err_block;
+    u32 next;       // next slot of the processing order to hand out
+    u32 error;      // set by the watchdog: blocks stop at their next tick boundary
+    u32 err_exp, pad;
+    u64 steps;      // most ticks one experiment processed in the last run
 };
 
 struct Params {
@@ -106,28 +109,31 @@ struct Params {
     const u32 *member_rank, *member_node, *member_a2a_n, *memb_row, *a2a_dst,
         *member_a2a_in_n, *memb_col, *a2a_in_src;
     const u64 *a2a_bytes, *a2a_in_bytes, *mem;
+    const u32 *node_rank;    // per node: its rank (workload-local)
+    const u32 *order;        // experiments in the order blocks take them (largest first)
     // dynamic state
     u64 *q_push, *q_pop;     // per queue: (tick << 32) | counter of the last push / pop
-    u32 *poplog;             // per queue: tick of each of the last 64 pops (by head % 64)
+    u32 *poplog;             // per queue: tick of each of the last plog pops (by head % plog)
     uint4 *slots;            // packet descriptors
     uint2 *eg;               // per switch port: (busy_until, round-robin pointer)
     RankCtl *rk;
-    uint2 *pend;             // per rank: kNPend (node, start tick)
-    u32 *act;                // per rank: kNAct running nodes, ascending
-    Lane *lanes;             // per rank: kNLane
-    uint2 *ports;            // per rank: kNPort (messages received, owner node)
+    uint2 *pend;             // per rank: pend_cap (node, start tick)
+    u32 *act;                // per rank: act_cap running nodes, ascending
+    Lane *lanes;             // per rank: lane_cap
+    uint2 *ports;            // per rank: port_cap (messages received, owner node)
     u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
     i32 *nd_out;
     ExpCtl *ctl;
     u32 *rec_sender, *rec_key, *rec_tick;
-    const u32 *item_exp, *item_loc;
-    u32 *wake;               // per work item: earliest tick it may have work
-    const u32 *node_rank;    // per node: its rank (workload-local)
-    u32 n_items, n_exps, n_topos, pad;
+    u32 *wake;               // per experiment: own wake tick of each item, then two poke words each
+    u32 n_exps, n_topos;
     Glob *glob;
     // run options
-    u64 barrier_timeout_ns;
-    i32 fault_block, fault_step;
+    u64 watchdog_ns;         // 0 = none
+    u32 max_ticks;           // tick budget of this run, per experiment clock
+    u32 stage_limit;         // bytes of shared memory for an experiment's image
+    u32 stage_mode;          // 0 = whole image when it fits, 1 = wake table only, 2 = none
+    u32 pad;
 };
 
 // Packet descriptor (16 bytes):
@@ -139,13 +145,52 @@ __host__ __device__ inline u32 pk_key(uint4 p) { return p.w & 0xFFFFFFu; }
 __host__ __device__ inline u32 pk_last(uint4 p) { return (p.w >> 24) & 1u; }
 __host__ __device__ inline u32 pk_slot(uint4 p) { return p.w >> 25; }
 
+// Shared-memory image of one experiment's dynamic state: byte offsets of
+// each array (16-byte aligned), in this order.  The wake table comes first,
+// so an image cut after it holds the wake table alone.
+enum : int { IM_WAKE, IM_QPUSH, IM_QPOP, IM_EG, IM_RK, IM_PRED, IM_CAND, IM_START, IM_END,
+             IM_PBASE, IM_DONE, IM_OUT, IM_ACT, IM_PEND, IM_PORTS, IM_POPLOG, IM_LANES,
+             IM_SLOTS, IM_N };
+
+__host__ __device__ inline u64 im_round(u64 b) { return (b + 15) & ~15ull; }
+
+__host__ __device__ inline void image_bytes(const ExpRec &X, u32 plog, u32 n_eg, u64 *sz)
+{
+    sz[IM_WAKE] = 12ull * X.n_items;          // own wake + two poke words per item
+    sz[IM_QPUSH] = 8ull * X.nq;
+    sz[IM_QPOP] = 8ull * X.nq;
+    sz[IM_EG] = 8ull * n_eg;
+    sz[IM_RK] = sizeof(RankCtl) * (u64)X.nr;
+    for (int k = IM_PRED; k <= IM_OUT; k++) sz[k] = 4ull * X.nn;
+    sz[IM_ACT] = 4ull * X.nr * X.act_cap;
+    sz[IM_PEND] = 8ull * X.nr * X.pend_cap;
+    sz[IM_PORTS] = 8ull * X.nr * X.port_cap;
+    sz[IM_POPLOG] = 4ull * X.nq * plog;
+    sz[IM_LANES] = sizeof(Lane) * (u64)X.nr * X.lane_cap;
+    sz[IM_SLOTS] = 16ull * X.nq * X.cap;
+}
+
+// offsets into the image; returns the total
+__host__ __device__ inline u64 image_layout(const ExpRec &X, u32 plog, u32 n_eg, u64 *off)
+{
+    u64 sz[IM_N];
+    image_bytes(X, plog, n_eg, sz);
+    u64 o = 0;
+    for (int k = 0; k < IM_N; k++) {
+        off[k] = o;
+        o += im_round(sz[k]);
+    }
+    return o;
+}
+
 // launch wrappers (mv_kernel.cu)
 cudaError_t launch_routes(const Params &p, u64 n_pairs_max, u32 level, cudaStream_t st);
 cudaError_t launch_up_lists(const Params &p, u32 n_sw_total, cudaStream_t st);
 cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_ranks,
                         cudaStream_t st);
-cudaError_t launch_run_reset(const Params &p, u32 max_ticks, cudaStream_t st);
-cudaError_t launch_megakernel(const Params &p, u32 blocks, cudaStream_t st);
-cudaError_t megakernel_occupancy(int *blocks_per_sm, int *n_sm);
+cudaError_t megakernel_prepare(u32 warps, u32 smem_bytes, int *blocks_per_sm, int *n_sm);
+u32 megakernel_smem(u32 warps, u32 image_bytes);
+cudaError_t launch_megakernel(const Params &p, u32 blocks, u32 warps, u32 smem_bytes,
+                              cudaStream_t st);
 
 }  // namespace mv

@@ -2,23 +2,31 @@
 // simulator, plus its set-up kernels.
 //
 // One launch advances every experiment of the batch (Multiverse section 4.3:
-// all systems fused in one kernel, launched once per batch).  A grid-wide
-// step processes one tick of every live experiment; each experiment keeps its
-// own clock and skips ticks in which nothing can change.  Work items are
-//   - one warp per (experiment, switch): plan + pull forwarding (section 4.2)
-//     for up to 64 ports, staged in shared memory;
-//   - one warp per (experiment, 32 ranks): DAG advance with the analytic
-//     intra-server model (sections 3.2, 4.1), NIC injection, NIC receive and
-//     acknowledgements.
-// A single grid barrier separates steps.  Reads of state another entity may
-// change in the same step see start-of-tick values: queue counters carry the
+// all systems fused in one kernel, launched once per batch).  Experiments
+// are independent (section 5: nothing crosses experiments), so each one is
+// stepped by one thread block: blocks of the persistent grid take
+// experiments from a shared counter, largest first, and step them tick by
+// tick with a block barrier as the per-tick synchronisation.  While a block
+// holds an experiment, its dynamic state lives in shared memory when it fits
+// (and in global memory otherwise); only the wake table always does.
+//
+// Inside a block, work items are
+//   - one warp per switch: plan + pull forwarding (section 4.2) for up to 64
+//     ports, the per-egress plan bitmaps staged in shared memory;
+//   - one warp per 32 ranks: DAG advance with the analytic intra-server model
+//     (sections 3.2, 4.1), NIC injection, NIC receive and acknowledgements.
+// Warps own disjoint item ranges, read their 32 wake ticks at once and ballot
+// the items due at the current tick.  Reads of state another entity may
+// change in the same tick see start-of-tick values: queue counters carry the
 // tick of their last change (at most one push and one pop per queue and
 // tick), start ticks are read as "joined before this tick", and completion
 // counters are monotone with timestamped results.  That makes the parallel
-// step equal to the serial phase order.
+// tick equal to the serial phase order, with a single barrier per tick.
 #include "mv_device.cuh"
 
 namespace mv {
+
+constexpr u32 kFull = 0xffffffffu;
 
 // ---------------------------------------------------------------- helpers
 // splitmix64 finaliser (S. Vigna, splitmix64.c, public domain).
@@ -30,30 +38,18 @@ __device__ __forceinline__ u64 mix64(u64 z)
 }
 __device__ __forceinline__ u64 cdiv(u64 a, u64 b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ u64 ld_rlx64(const u64 *p)
-{
-    u64 v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_rlx64(u64 *p, u64 v)
-{
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ u32 ld_rlx32(const u32 *p)
-{
-    u32 v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_rlx32(u32 *p, u32 v)
-{
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
+// State shared between warps of the block may sit in shared or in global
+// memory, so these accessors use generic addresses.  Volatile accesses keep
+// the compiler from caching or splitting a word another warp may change in
+// the same tick.
+__device__ __forceinline__ u64 ld_vol64(const u64 *p) { return *reinterpret_cast<const volatile u64 *>(p); }
+__device__ __forceinline__ void st_vol64(u64 *p, u64 v) { *reinterpret_cast<volatile u64 *>(p) = v; }
+__device__ __forceinline__ u32 ld_vol32(const u32 *p) { return *reinterpret_cast<const volatile u32 *>(p); }
+__device__ __forceinline__ void st_vol32(u32 *p, u32 v) { *reinterpret_cast<volatile u32 *>(p) = v; }
 __device__ __forceinline__ i32 ld_acq32(const i32 *p)
 {
     i32 v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.cta.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ u64 globaltimer()
@@ -61,30 +57,6 @@ __device__ __forceinline__ u64 globaltimer()
     u64 t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-__device__ __forceinline__ void set_status(ExpCtl *c, u32 st, u32 k)
-{
-    atomicCAS(&c->status, (u32)EXP_RUNNING, st);
-    atomicMin(&c->stop_step, k);
-}
-
-// Credit of queue qi for a sender at tick t: the queue holds `tail` pushes
-// and `H` pops as of the start of the tick; the credit of a pop at tick x
-// reaches the sender at x + D (D = delta + 1 of the link).  At most D - 1
-// pops can still be on their way, so the pop log is only read when the
-// queue is within D - 1 of full.
-__device__ __forceinline__ bool credit_ok(const Params &P, u64 qi, u32 tail, u32 H, u32 D, u32 t,
-                                          u32 cap)
-{
-    if (tail - H + D - 1 < cap) return true;
-    u32 back = 0;
-    const u32 *log = P.poplog + qi * kPopLog;
-    while (back < H && back + 1 < D) {
-        if (__ldcg(&log[(H - 1 - back) % kPopLog]) + D <= t) break;
-        back++;
-    }
-    return tail - (H - back) < cap;
 }
 
 // ---------------------------------------------------------------- set-up
@@ -118,7 +90,7 @@ __global__ void k_routes(Params P, u32 level)
     }
 }
 
-__global__ void k_up_lists(Params P, u32 n_sw_total)
+__global__ void k_up_lists(Params P)
 {
     for (u32 t = 0; t < P.n_topos; t++) {
         const TopoRec T = P.topo[t];
@@ -132,7 +104,6 @@ __global__ void k_up_lists(Params P, u32 n_sw_total)
             P.up_n[gs] = (u8)k;
         }
     }
-    (void)n_sw_total;
 }
 
 // GPU memory check before the run (Multiverse section 3.1).  The page gives
@@ -161,19 +132,21 @@ __global__ void k_init(Params P)
     for (u32 u = i; u < X.nn; u += stride) {
         u64 g = X.nd_off + u;
         P.nd_pred[g] = P.node_npred[W.node_off + u];
-        P.nd_cand[g] = 0;
         P.nd_start[g] = kUnset;
         P.nd_end[g] = kUnset;
-        P.nd_pbase[g] = 0;
-        P.nd_done[g] = 0;
-        P.nd_out[g] = 0;
     }
     for (u32 q = i; q < X.nq; q += stride) {
         P.q_push[X.q_off + q] = (u64)kUnset << 32;
         P.q_pop[X.q_off + q] = (u64)kUnset << 32;
     }
-    // work items: switches wake on their first packet, rank groups at tick 0
-    for (u32 it = i; it < X.n_items; it += stride) P.wake[X.item_off + it] = it < X.nsw ? kUnset : 0;
+    // work items: switches wake on their first packet, rank groups at tick 0;
+    // no pokes pending
+    u32 *wk = P.wake + 3ull * X.item_off;
+    for (u32 it = i; it < X.n_items; it += stride) {
+        wk[it] = it < X.nsw ? kUnset : 0;
+        wk[X.n_items + it] = kUnset;
+        wk[2 * X.n_items + it] = kUnset;
+    }
     bool fits = memory_fits(P.mem + 10 * (u64)X.work, X.gpu_mem);
     // roots (no predecessor) are scheduled at tick 0, in node order
     for (u32 r = i; r < X.nr; r += stride) {
@@ -182,8 +155,8 @@ __global__ void k_init(Params P)
         bool over = false;
         for (u32 u = first; u < first + cnt && fits; u++) {
             if (P.node_npred[W.node_off + u] != 0) continue;
-            if (c.npend == kNPend) { over = true; break; }
-            P.pend[(X.rk_off + r) * kNPend + c.npend++] = make_uint2(u, 0);
+            if (c.npend == X.pend_cap) { over = true; break; }
+            P.pend[X.pend_off + (u64)r * X.pend_cap + c.npend++] = make_uint2(u, 0);
         }
         P.rk[X.rk_off + r] = c;
         if (over) atomicCAS(&P.ctl[e].status, (u32)EXP_RUNNING, (u32)EXP_OVERFLOW);
@@ -198,185 +171,96 @@ __global__ void k_init_ctl(Params P)
         c.status = memory_fits(P.mem + 10 * (u64)X.work, X.gpu_mem) ? EXP_RUNNING : EXP_OOM;
         c.now = 0;
         c.nodes_left = X.nn;
-        c.stop_step = kUnset;
         P.ctl[e] = c;
     }
 }
 
-__global__ void k_run_reset(Params P, u32 max_ticks)
-{
-    for (u32 e = blockIdx.x * blockDim.x + threadIdx.x; e < P.n_exps; e += gridDim.x * blockDim.x) {
-        ExpCtl *c = &P.ctl[e];
-        c->stop_step = kUnset;
-        u64 lim = (u64)c->now + max_ticks;
-        c->limit = lim > kTickLimit ? kTickLimit : (u32)lim;
-        for (int k = 0; k < 3; k++) {
-            c->clk[k] = kUnset;
-            c->nxt[k] = kUnset;
-        }
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        Glob *g = P.glob;
-        g->bar_count = 0;
-        g->error = 0;
-        g->run_cnt[0] = g->run_cnt[1] = g->run_cnt[2] = 0;
-        g->steps = 0;
-        g->err_step = g->err_block = kUnset;
-    }
-}
+// ---------------------------------------------------------------- block state
+// The experiment a block holds: its records, and generic pointers to its
+// slice of every dynamic array (shared memory when staged, global if not).
+struct XV {
+    ExpRec X;
+    TopoRec T;
+    WorkRec W;
+    u32 e, staged, plog, pad;
+    u64 *q_push, *q_pop;
+    u32 *poplog;
+    uint4 *slots;
+    uint2 *eg;
+    RankCtl *rk;
+    uint2 *pend;
+    u32 *act;
+    Lane *lanes;
+    uint2 *ports;
+    u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
+    i32 *nd_out;
+    u32 *wake;
+};
 
-// ---------------------------------------------------------------- grid barrier
-// Sense-counting barrier over all blocks of the cooperative launch.  Every
-// wait is bounded by the run's timeout; past it the block records the error
-// and leaves, and every block exits at its next barrier.
-__device__ bool grid_barrier(const Params &P, u32 step)
-{
-    Glob *g = P.glob;
-    __shared__ u32 ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        ok = 1;
-        bool skip = (i32)blockIdx.x == P.fault_block && (i32)step == P.fault_step;
-        u32 gen = ld_rlx32(&g->bar_gen);
-        __threadfence();
-        if (!skip) {
-            u32 arrived = atomicAdd(&g->bar_count, 1);
-            if (arrived == gridDim.x - 1) {
-                g->bar_count = 0;
-                __threadfence();
-                atomicAdd(&g->bar_gen, 1);
-            }
-        }
-        if (ld_rlx32(&g->bar_gen) == gen) {
-            u64 t0 = globaltimer();
-            u32 it = 0;
-            while (ld_rlx32(&g->bar_gen) == gen) {
-                if (ld_rlx32(&g->error)) { ok = 0; break; }
-                if ((++it & 255) == 0 && globaltimer() - t0 > P.barrier_timeout_ns) {
-                    if (atomicCAS(&g->error, 0u, 1u) == 0) {
-                        g->err_step = step;
-                        g->err_block = blockIdx.x;
-                    }
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        if (ld_rlx32(&g->error)) ok = 0;
-        __threadfence();
-    }
-    __syncthreads();
-    return ok != 0;
-}
+// Per-experiment counters while a block holds it; only read after the last
+// tick.  Decisions taken every tick use the per-warp reports instead, which
+// are double-buffered so that one barrier per tick suffices.
+struct Team {
+    u32 end_max1, rec_count, now0, status0, left0, pad[3];
+    unsigned long long pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
+    uint4 rep[2][kMaxWarps];    // per warp: (next wake, nodes completed, failure key, abort)
+};
 
-// ---------------------------------------------------------------- clocks
-// Tick that experiment e processes at step k, or kUnset if it does not run.
-// Every lane that touches e computes it the same way, from the slots of step
-// k-1 only: the clock and the minimum over every pending wake tick reported
-// during step k-1 (three rotating slots: step k-1's are stable while step k
-// runs, and step k+1's are cleared during step k).
-__device__ __forceinline__ u32 exp_tick(const Params &P, u32 e, u32 k)
-{
-    ExpCtl *c = &P.ctl[e];
-    u32 stop = ld_rlx32(&c->stop_step), lim = ld_rlx32(&c->limit);
-    if (stop < k) return kUnset;                  // finished or failed earlier
-    u32 t;
-    if (k == 0) {
-        u32 st = ld_rlx32(&c->status), left = ld_rlx32(&c->nodes_left);
-        t = ld_rlx32(&c->now);
-        if (st != EXP_RUNNING || left == 0) return kUnset;
-    } else {
-        u32 p = (k - 1) % 3;
-        u32 tp = ld_rlx32(&c->clk[p]);
-        t = ld_rlx32(&c->nxt[p]);
-        if (tp == kUnset || t == kUnset) return kUnset;
-    }
-    return t >= lim ? kUnset : t;
-}
+// Failure keys: the lowest key of a tick wins, so rank failures (in rank
+// order, as the serial phase order visits them) come before switch errors.
+__device__ __forceinline__ u32 fail_key_rank(u32 r, u32 code) { return (r << 3) | code; }
+constexpr u32 kFailSwitch = 0xF0000000u | EXP_ERROR;
 
-// Control of one experiment at step k (run by the lane holding its first
-// work item): publish its tick, clear the slot of step k+1, count it as
-// running, and settle its final state when it stops.
-__device__ void exp_control(const Params &P, u32 e, u32 k, u32 t)
-{
-    ExpCtl *c = &P.ctl[e];
-    st_rlx32(&c->clk[k % 3], t);
-    st_rlx32(&c->nxt[(k + 1) % 3], kUnset);
-    if (t != kUnset) {
-        atomicAdd(&P.glob->run_cnt[k % 3], 1);
-        return;
-    }
-    // a stopped experiment's clock is one past its latest node end (0: none)
-    if (k == 0) {
-        if (ld_rlx32(&c->status) == EXP_RUNNING && ld_rlx32(&c->nodes_left) == 0) {
-            st_rlx32(&c->status, EXP_DONE);
-            st_rlx32(&c->now, ld_rlx32(&c->end_max1));
-        }
-        return;                                   // else stopped before: now unchanged
-    }
-    u32 p = (k - 1) % 3, tp = ld_rlx32(&c->clk[p]);
-    if (tp == kUnset) return;                     // settled at an earlier step
-    u32 nx = ld_rlx32(&c->nxt[p]);
-    if (ld_rlx32(&c->status) != EXP_RUNNING) {    // failed during the last tick
-        st_rlx32(&c->now, ld_rlx32(&c->end_max1));
-    } else if (ld_rlx32(&c->nodes_left) == 0) {
-        st_rlx32(&c->status, EXP_DONE);
-        st_rlx32(&c->now, ld_rlx32(&c->end_max1));
-    } else if (nx == kUnset) {                    // nothing pending anywhere
-        st_rlx32(&c->status, EXP_DEADLOCK);
-        st_rlx32(&c->now, ld_rlx32(&c->end_max1));
-    } else {                                      // stopped by the tick budget
-        st_rlx32(&c->now, nx);
-    }
-}
-
-// Work items and their wake ticks.  An item is processed at tick t when its
-// wake <= t.  Whoever creates work for another item lowers that item's wake
-// (a push, a collective join, a message delivery) and the experiment's next
-// tick; a processed item sets its own next wake from its own state.
-__device__ __forceinline__ u32 sw_item(const ExpRec &X, u32 s) { return X.item_off + s; }
-__device__ __forceinline__ u32 rank_item(const ExpRec &X, u32 r) { return X.item_off + X.nsw + r / 32; }
-__device__ __forceinline__ void poke(const Params &P, u32 item, u32 e, u32 k, u32 at)
-{
-    atomicMin(&P.wake[item], at);
-    atomicMin(&P.ctl[e].nxt[k % 3], at);
-}
-
-// ---------------------------------------------------------------- switches
 struct SwSmem {
     uint4 pkt[kMaxPorts];
     unsigned long long mask[kMaxPorts];
     u32 head[kMaxPorts];
-    u32 pad[2];
 };
 
-__device__ __forceinline__ u32 route_port(const Params &P, const TopoRec &T, const ExpRec &X,
-                                          u32 gs, u32 s, uint4 pk)
+// ---------------------------------------------------------------- credit
+// Credit of queue qi for a sender at tick t: the queue holds `tail` pushes
+// and `H` pops as of the start of the tick; the credit of a pop at tick x
+// reaches the sender at x + D (D = delta + 1 of the link).  At most D - 1
+// pops can still be on their way, so the pop log is only read when the
+// queue is within D - 1 of full.
+__device__ __forceinline__ bool credit_ok(const XV &V, u32 qi, u32 tail, u32 H, u32 D, u32 t)
 {
-    u8 r = P.route[T.route_off + (u64)s * T.nh + pk_dst(pk)];
+    const u32 cap = V.X.cap;
+    if (tail - H + D - 1 < cap) return true;
+    const u32 pm = V.plog - 1;
+    const u32 *log = V.poplog + (u64)qi * V.plog;
+    u32 back = 0;
+    while (back < H && back + 1 < D) {
+        if (ld_vol32(&log[(H - 1 - back) & pm]) + D <= t) break;
+        back++;
+    }
+    return tail - (H - back) < cap;
+}
+
+// ---------------------------------------------------------------- switches
+__device__ __forceinline__ u32 route_port(const Params &P, const XV &V, u32 gs, u32 s, uint4 pk)
+{
+    u8 r = P.route[V.T.route_off + (u64)s * V.T.nh + pk_dst(pk)];
     if (r != 0xFF) return r;
     u32 nup = P.up_n[gs];
     if (nup == 0) return 0xFFu;
-    u64 h = mix64((u64)pk_key(pk) ^ ((u64)s << 40) ^ X.ecmp_seed);
-    return P.up_list[T.port_off + P.sw_pstart[gs] + (u32)(h % nup)];
+    u64 h = mix64((u64)pk_key(pk) ^ ((u64)s << 40) ^ V.X.ecmp_seed);
+    return P.up_list[V.T.port_off + P.sw_pstart[gs] + (u32)(h % nup)];
 }
 
-// Forwarding at one switch for one tick (Multiverse section 4.2): each lane
+// Forwarding at switch s for one tick (Multiverse section 4.2): each lane
 // plans its ingress ports (the egress their ready head packet needs), then
 // each lane pulls for its egress ports: free link, credit downstream, first
-// planned ingress at or after the round-robin pointer.
-__device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 t, u32 k,
-                            SwSmem *sm)
+// planned ingress at or after the round-robin pointer.  Returns the earliest
+// tick this warp knows of at which something may happen (its own next wake
+// and the wakes it gave other items); *fail gets a failure key.
+__device__ u32 switch_tick(const Params &P, const XV &V, Team &TC, u32 s, u32 t, u32 old,
+                           u32 *poke, SwSmem *sm, u32 *fail)
 {
-    const TopoRec T = P.topo[X.topo];
     const u32 lane = threadIdx.x & 31;
-    const u32 gs = T.sw_off + s;
+    const u32 gs = V.T.sw_off + s;
     const u32 np = P.sw_nports[gs], p0 = P.sw_pstart[gs];
-    const u32 it = sw_item(X, s);
-    u32 old = 0;
-    if (lane == 0) old = atomicExch(&P.wake[it], kUnset);   // consume pending wakes
-    old = __shfl_sync(0xffffffffu, old, 0);
+    const u32 cap = V.X.cap, pm = V.plog - 1;
     u32 nxt = kUnset;                   // own next wake
     u32 pk_min = kUnset;                // earliest tick poked into a downstream item
     bool ready_any = false;
@@ -388,16 +272,16 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
     for (u32 j = 0; j < 2; j++) {
         u32 p = lane + 32 * j;
         if (p >= np) continue;
-        u64 qi = X.q_off + p0 + p;
-        u64 pw = ld_rlx64(&P.q_push[qi]);
+        u32 qi = p0 + p;
+        u64 pw = ld_vol64(&V.q_push[qi]);
         u32 tail = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-        u32 head = (u32)__ldcg(&P.q_pop[qi]);
+        u32 head = (u32)V.q_pop[qi];
         sm->head[p] = head;
         if (head == tail) continue;
-        uint4 pk = __ldcg(&P.slots[X.slot_off + (u64)(p0 + p) * X.cap + head % X.cap]);
+        uint4 pk = V.slots[(u64)qi * cap + head % cap];
         if (pk.x > t) { nxt = min(nxt, pk.x); continue; }
         ready_any = true;
-        u32 tg = route_port(P, T, X, gs, s, pk);
+        u32 tg = route_port(P, V, gs, s, pk);
         if (tg >= np) { bad = true; continue; }
         sm->pkt[p] = pk;
         atomicOr(&sm->mask[tg], 1ull << p);
@@ -412,68 +296,63 @@ __device__ void switch_tick(const Params &P, const ExpRec &X, u32 e, u32 s, u32 
         unsigned long long M = sm->mask[eg];
         if (!M) continue;
         u32 qe = p0 + eg;
-        uint2 st = __ldcg(&P.eg[X.eg_off + qe]);
+        uint2 st = V.eg[qe];
         if (st.x > t) continue;             // busy: its heads wake the switch at t+1
-        i32 pe = P.port_peer[T.port_off + qe];
-        u32 dq = pe >= 0 ? (u32)pe : T.nq + (u32)(-pe - 1);
-        u64 dqi = X.q_off + dq;
-        u64 dpop = ld_rlx64(&P.q_pop[dqi]);
+        i32 pe = P.port_peer[V.T.port_off + qe];
+        u32 dq = pe >= 0 ? (u32)pe : V.T.nq + (u32)(-pe - 1);
+        u64 dpop = ld_vol64(&V.q_pop[dq]);
         u32 dhead = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
-        u32 dtail = (u32)__ldcg(&P.q_push[dqi]);
-        u32 dl_e = P.port_delta[T.port_off + qe];
-        if (!credit_ok(P, dqi, dtail, dhead, dl_e + 1, t, X.cap)) continue;
+        u32 dtail = (u32)V.q_push[dq];
+        u32 dl = P.port_delta[V.T.port_off + qe];
+        if (!credit_ok(V, dq, dtail, dhead, dl + 1, t)) continue;
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
         uint4 pk = sm->pkt[i];
-        u32 sg = P.port_sigma[T.port_off + qe], dl = P.port_delta[T.port_off + qe];
+        u32 sg = P.port_sigma[V.T.port_off + qe];
         pk.x = t + sg + dl;
         pk.y += (dl + 1) << 16;
-        __stcg(&P.slots[X.slot_off + (u64)dq * X.cap + dtail % X.cap], pk);
-        st_rlx64(&P.q_push[dqi], ((u64)t << 32) | (u32)(dtail + 1));
-        __stcg(&P.eg[X.eg_off + qe], make_uint2(t + sg, (i + 1) % np));
+        V.slots[(u64)dq * cap + dtail % cap] = pk;
+        st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
+        V.eg[qe] = make_uint2(t + sg, (i + 1) % np);
         // the queue's owner: the peer switch, or the rank group of the host
-        if (pe >= 0) atomicMin(&P.wake[sw_item(X, P.port_sw[T.port_off + pe])], pk.x);
-        else if ((u32)(-pe - 1) < X.nr) atomicMin(&P.wake[rank_item(X, (u32)(-pe - 1))], pk.x);
+        if (pe >= 0) atomicMin(&poke[P.port_sw[V.T.port_off + pe]], pk.x);
+        else if ((u32)(-pe - 1) < V.X.nr) atomicMin(&poke[V.X.nsw + (u32)(-pe - 1) / 32], pk.x);
         pk_min = min(pk_min, pk.x);
         popped |= 1ull << i;
         hops++;
     }
-    u32 lo = __reduce_or_sync(0xffffffffu, (u32)popped);
-    u32 hi32 = __reduce_or_sync(0xffffffffu, (u32)(popped >> 32));
+    u32 lo = __reduce_or_sync(kFull, (u32)popped);
+    u32 hi32 = __reduce_or_sync(kFull, (u32)(popped >> 32));
     unsigned long long all = ((unsigned long long)hi32 << 32) | lo;
 #pragma unroll
     for (u32 j = 0; j < 2; j++) {
         u32 p = lane + 32 * j;
         if (p < np && ((all >> p) & 1ull)) {
-            u64 qi = X.q_off + p0 + p;
-            __stcg(&P.poplog[qi * kPopLog + sm->head[p] % kPopLog], t);
-            st_rlx64(&P.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
+            u32 qi = p0 + p;
+            st_vol32(&V.poplog[(u64)qi * V.plog + (sm->head[p] & pm)], t);
+            st_vol64(&V.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
         }
     }
-    hops = __reduce_add_sync(0xffffffffu, hops);
-    nxt = __reduce_min_sync(0xffffffffu, nxt);
-    pk_min = __reduce_min_sync(0xffffffffu, pk_min);
-    bool anybad = __any_sync(0xffffffffu, bad);
-    if (__any_sync(0xffffffffu, ready_any)) nxt = t + 1;   // heads left or blocked
+    hops = __reduce_add_sync(kFull, hops);
+    nxt = __reduce_min_sync(kFull, nxt);
+    pk_min = __reduce_min_sync(kFull, pk_min);
+    bool anybad = __any_sync(kFull, bad);
+    if (__any_sync(kFull, ready_any)) nxt = t + 1;   // heads left or blocked
+    u32 w = min(nxt, old > t ? old : kUnset);
     if (lane == 0) {
-        ExpCtl *c = &P.ctl[e];
-        u32 w = min(nxt, old > t ? old : kUnset);
-        if (w != kUnset) atomicMin(&P.wake[it], w);
-        u32 m = min(w, pk_min);
-        if (m != kUnset) atomicMin(&c->nxt[k % 3], m);
-        if (all) atomicAdd((unsigned long long *)&c->pkt_hops, (unsigned long long)hops);
-        if (anybad) set_status(c, EXP_ERROR, k);
+        V.wake[s] = w;
+        if (all) atomicAdd(&TC.pkt_hops, (unsigned long long)hops);
     }
+    if (anybad) *fail = min(*fail, kFailSwitch);
     __syncwarp();
+    return min(w, pk_min);
 }
 
 // ---------------------------------------------------------------- ranks
-// Rank state goes through L2 (.cg): the item of a rank always lands on the
-// same warp, but state written by set-up kernels must not come from L1.
 __device__ __forceinline__ RankCtl load_ctl(const RankCtl *p)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
-    uint4 a = __ldcg(q), b = __ldcg(q + 1), c = __ldcg(q + 2);
+    uint4 a = q[0], b = q[1], c = q[2];
     RankCtl r;
     r.busy = a.x; r.rr = a.y; r.npend = a.z; r.nact = a.w;
     r.lane_mask = ((u64)b.y << 32) | b.x;
@@ -485,35 +364,33 @@ __device__ __forceinline__ RankCtl load_ctl(const RankCtl *p)
 __device__ __forceinline__ void store_ctl(RankCtl *p, const RankCtl &r)
 {
     uint4 *q = reinterpret_cast<uint4 *>(p);
-    __stcg(q, make_uint4(r.busy, r.rr, r.npend, r.nact));
-    __stcg(q + 1, make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_mask[0],
-                             (u32)(r.port_mask[0] >> 32)));
-    __stcg(q + 2, make_uint4((u32)r.port_mask[1], (u32)(r.port_mask[1] >> 32), 0, 0));
+    q[0] = make_uint4(r.busy, r.rr, r.npend, r.nact);
+    q[1] = make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_mask[0],
+                      (u32)(r.port_mask[0] >> 32));
+    q[2] = make_uint4((u32)r.port_mask[1], (u32)(r.port_mask[1] >> 32), 0, 0);
 }
 __device__ __forceinline__ Lane load_lane(const Lane *p)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
     Lane L;
     uint4 *d = reinterpret_cast<uint4 *>(&L);
-    d[0] = __ldcg(q); d[1] = __ldcg(q + 1); d[2] = __ldcg(q + 2); d[3] = __ldcg(q + 3);
+    d[0] = q[0]; d[1] = q[1]; d[2] = q[2]; d[3] = q[3];
     return L;
 }
 __device__ __forceinline__ void store_lane(Lane *p, const Lane &L)
 {
     uint4 *q = reinterpret_cast<uint4 *>(p);
     const uint4 *s = reinterpret_cast<const uint4 *>(&L);
-    __stcg(q, s[0]); __stcg(q + 1, s[1]); __stcg(q + 2, s[2]); __stcg(q + 3, s[3]);
+    q[0] = s[0]; q[1] = s[1]; q[2] = s[2]; q[3] = s[3];
 }
 
 // Per-rank view used while processing one tick.
 struct RankView {
     const Params *P;
-    const ExpRec *X;
-    const TopoRec *T;
-    const WorkRec *W;
-    ExpCtl *c;
-    u32 r, t, e, k;
-    u64 rk;             // X.rk_off + r
+    const XV *V;
+    Team *TC;
+    u32 *poke;          // this step's poke words of the experiment's items
+    u32 r, t;
     RankCtl C;
     bool changed, fail_over, fail_err;
     u32 nxt;            // this rank's own next wake
@@ -522,24 +399,26 @@ struct RankView {
     u64 dig;
 };
 
-__device__ __forceinline__ u32 coll_of(const RankView &v, u32 u) { return v.P->node_arg[v.W->node_off + u]; }
-__device__ __forceinline__ u32 nmemb(const RankView &v, u32 c) { return v.P->coll_nmembers[v.W->coll_off + c]; }
-__device__ __forceinline__ u32 ckind(const RankView &v, u32 c) { return v.P->coll_kind[v.W->coll_off + c]; }
-__device__ __forceinline__ u64 cbytes(const RankView &v, u32 c) { return v.P->coll_bytes[v.W->coll_off + c]; }
+__device__ __forceinline__ const WorkRec &W_(const RankView &v) { return v.V->W; }
+__device__ __forceinline__ const ExpRec &X_(const RankView &v) { return v.V->X; }
+__device__ __forceinline__ u32 coll_of(const RankView &v, u32 u) { return v.P->node_arg[W_(v).node_off + u]; }
+__device__ __forceinline__ u32 nmemb(const RankView &v, u32 c) { return v.P->coll_nmembers[W_(v).coll_off + c]; }
+__device__ __forceinline__ u32 ckind(const RankView &v, u32 c) { return v.P->coll_kind[W_(v).coll_off + c]; }
+__device__ __forceinline__ u64 cbytes(const RankView &v, u32 c) { return v.P->coll_bytes[W_(v).coll_off + c]; }
 __device__ __forceinline__ u32 mabs(const RankView &v, u32 c, u32 i)
 {
-    return v.W->memb_off + v.P->coll_mstart[v.W->coll_off + c] + i;
+    return W_(v).memb_off + v.P->coll_mstart[W_(v).coll_off + c] + i;
 }
 __device__ __forceinline__ u32 mrank(const RankView &v, u32 c, u32 i) { return v.P->member_rank[mabs(v, c, i)]; }
 __device__ __forceinline__ u32 mnode(const RankView &v, u32 c, u32 i) { return v.P->member_node[mabs(v, c, i)]; }
 __device__ __forceinline__ bool tree_of(const RankView &v, u32 c)
 {
-    return ckind(v, c) == COLL_AR && v.X->algo == ALGO_TREE;
+    return ckind(v, c) == COLL_AR && X_(v).algo == ALGO_TREE;
 }
 __device__ __forceinline__ u32 nchan(const RankView &v, u32 c)
 {
     u32 k = ckind(v, c);
-    return (k == COLL_RELAY || k == COLL_P2P) ? 1u : v.X->nc;
+    return (k == COLL_RELAY || k == COLL_P2P) ? 1u : X_(v).nc;
 }
 __device__ __forceinline__ u32 nports_of(const RankView &v, u32 c)
 {
@@ -558,14 +437,14 @@ __device__ __forceinline__ u32 ring_steps(const RankView &v, u32 c)
 }
 __device__ __forceinline__ u64 ring_loops(const RankView &v, u32 c, u64 Pc)
 {
-    return Pc == 0 ? 1 : cdiv(Pc, (u64)nmemb(v, c) * v.X->chunk);
+    return Pc == 0 ? 1 : cdiv(Pc, (u64)nmemb(v, c) * X_(v).chunk);
 }
 __device__ u64 a2a_row_chunks(const RankView &v, u32 c, u32 i)
 {
     u32 m = mabs(v, c, i);
-    u32 b = v.W->a2a_off + v.P->memb_row[m], n = v.P->member_a2a_n[m];
+    u32 b = W_(v).a2a_off + v.P->memb_row[m], n = v.P->member_a2a_n[m];
     u64 tot = 0;
-    for (u32 j = 0; j < n; j++) tot += nchunks(v.P->a2a_bytes[b + j], v.X->chunk);
+    for (u32 j = 0; j < n; j++) tot += nchunks(v.P->a2a_bytes[b + j], X_(v).chunk);
     return tot;
 }
 
@@ -576,18 +455,18 @@ __device__ u32 lane_count(const RankView &v, u32 c, u32 i, u32 ch, u32 kind)
     switch (ckind(v, c)) {
     case COLL_AR: case COLL_RS: case COLL_AG:
         if (tree_of(v, c)) {
-            u64 n = nchunks(part_bytes(S, v.X->nc, ch), v.X->chunk);
+            u64 n = nchunks(part_bytes(S, X_(v).nc, ch), X_(v).chunk);
             if (kind == 0) return i > 0 ? (u32)n : 0;
             return 2 * i + kind < N ? (u32)n : 0;
         }
-        return (u32)(ring_loops(v, c, part_bytes(S, v.X->nc, ch)) * ring_steps(v, c));
+        return (u32)(ring_loops(v, c, part_bytes(S, X_(v).nc, ch)) * ring_steps(v, c));
     case COLL_RELAY:
-        return i + 1 < N ? v.P->coll_parts[v.W->coll_off + c] : 0;
+        return i + 1 < N ? v.P->coll_parts[W_(v).coll_off + c] : 0;
     case COLL_P2P:
-        return i == 0 ? (u32)nchunks(S, v.X->chunk) : 0;
+        return i == 0 ? (u32)nchunks(S, X_(v).chunk) : 0;
     case COLL_A2A: {
         u64 tot = a2a_row_chunks(v, c, i);
-        return tot > ch ? (u32)cdiv(tot - ch, v.X->nc) : 0;
+        return tot > ch ? (u32)cdiv(tot - ch, X_(v).nc) : 0;
     }
     }
     return 0;
@@ -601,20 +480,20 @@ __device__ u32 port_count_expect(const RankView &v, u32 c, u32 i, u32 p)
     case COLL_AR: case COLL_RS: case COLL_AG:
         if (tree_of(v, c)) {
             u32 ch = p / 3, q = p % 3;
-            u64 n = nchunks(part_bytes(S, v.X->nc, ch), v.X->chunk);
+            u64 n = nchunks(part_bytes(S, X_(v).nc, ch), X_(v).chunk);
             if (q == 0) return i > 0 ? (u32)n : 0;
             return 2 * i + q < N ? (u32)n : 0;
         }
-        return (u32)(ring_loops(v, c, part_bytes(S, v.X->nc, p)) * ring_steps(v, c));
+        return (u32)(ring_loops(v, c, part_bytes(S, X_(v).nc, p)) * ring_steps(v, c));
     case COLL_RELAY:
-        return i > 0 ? v.P->coll_parts[v.W->coll_off + c] : 0;
+        return i > 0 ? v.P->coll_parts[W_(v).coll_off + c] : 0;
     case COLL_P2P:
-        return i == 1 ? (u32)nchunks(S, v.X->chunk) : 0;
+        return i == 1 ? (u32)nchunks(S, X_(v).chunk) : 0;
     case COLL_A2A: {
         u32 m = mabs(v, c, i);
-        u32 b = v.W->a2a_in_off + v.P->memb_col[m], n = v.P->member_a2a_in_n[m];
+        u32 b = W_(v).a2a_in_off + v.P->memb_col[m], n = v.P->member_a2a_in_n[m];
         u64 tot = 0;
-        for (u32 j = 0; j < n; j++) tot += nchunks(v.P->a2a_in_bytes[b + j], v.X->chunk);
+        for (u32 j = 0; j < n; j++) tot += nchunks(v.P->a2a_in_bytes[b + j], X_(v).chunk);
         return (u32)tot;
     }
     }
@@ -626,13 +505,13 @@ __device__ u32 port_count_expect(const RankView &v, u32 c, u32 i, u32 p)
 __device__ u32 lane_setup(const RankView &v, Lane &L)
 {
     u32 c = coll_of(v, L.node), N = nmemb(v, c), i = L.member, m = L.m, ch = L.chan;
-    u64 S = cbytes(v, c), C = v.X->chunk, bytes = 0;
+    u64 S = cbytes(v, c), C = X_(v).chunk, bytes = 0;
     L.dep_mask = 0;
     L.dep_need = 0;
     L.dep_base = 0;
     switch (ckind(v, c)) {
     case COLL_AR: case COLL_RS: case COLL_AG: {
-        u64 Pc = part_bytes(S, v.X->nc, ch);
+        u64 Pc = part_bytes(S, X_(v).nc, ch);
         if (tree_of(v, c)) {
             bytes = Pc > (u64)m * C ? min(C, Pc - (u64)m * C) : 0;
             u32 kids = (2 * i + 1 < N ? 2u : 0u) | (2 * i + 2 < N ? 4u : 0u);
@@ -663,7 +542,7 @@ __device__ u32 lane_setup(const RankView &v, Lane &L)
         break;
     }
     case COLL_RELAY: {                                // pipelined broadcast hop
-        u32 K = v.P->coll_parts[v.W->coll_off + c];
+        u32 K = v.P->coll_parts[W_(v).coll_off + c];
         bytes = S / K + (m < S % K ? 1 : 0);
         L.dst_member = i + 1;
         L.dst_port = 0;
@@ -677,8 +556,8 @@ __device__ u32 lane_setup(const RankView &v, Lane &L)
         break;
     case COLL_A2A: {
         u32 mm = mabs(v, c, i);
-        u32 r0 = v.W->a2a_off + v.P->memb_row[mm];
-        u64 g = (u64)ch + (u64)m * v.X->nc;
+        u32 r0 = W_(v).a2a_off + v.P->memb_row[mm];
+        u64 g = (u64)ch + (u64)m * X_(v).nc;
         while (g >= L.a2a_start + nchunks(v.P->a2a_bytes[r0 + L.a2a_e], C)) {
             L.a2a_start += (u32)nchunks(v.P->a2a_bytes[r0 + L.a2a_e], C);
             L.a2a_e++;
@@ -693,23 +572,23 @@ __device__ u32 lane_setup(const RankView &v, Lane &L)
     u32 drank = mrank(v, c, L.dst_member);
     L.key = (u32)(mix64((u64)L.node | ((u64)(ch * 4 + L.kind) << 32) | ((u64)drank << 44)) &
                   0xFFFFFFu);
-    return (u32)(bytes == 0 ? 1 : cdiv(bytes, v.X->pkt));
+    return (u32)(bytes == 0 ? 1 : cdiv(bytes, X_(v).pkt));
 }
 
 __device__ u32 compute_ticks(const RankView &v, u32 u)
 {
     const Params &P = *v.P;
-    u64 lo = P.node_dur_lo[v.W->node_off + u], hi = P.node_dur_hi[v.W->node_off + u], ns = lo;
-    if (hi > lo)
-        ns = lo + mix64(mix64((u64)P.node_dur_key[v.W->node_off + u]) ^ v.X->dur_seed) % (hi - lo + 1);
-    return (u32)cdiv(ns * 1000, v.X->tick_ps);
+    const u32 g = W_(v).node_off + u;
+    u64 lo = P.node_dur_lo[g], hi = P.node_dur_hi[g], ns = lo;
+    if (hi > lo) ns = lo + mix64(mix64((u64)P.node_dur_key[g]) ^ X_(v).dur_seed) % (hi - lo + 1);
+    return (u32)cdiv(ns * 1000, X_(v).tick_ps);
 }
 
 // alpha + bytes/beta (Multiverse section 4.1), beta as ticks per byte
 __device__ u32 intra_ticks(const RankView &v, u32 c)
 {
     const Params &P = *v.P;
-    u32 cc = v.W->coll_off + c;
+    u32 cc = W_(v).coll_off + c;
     u64 g = nmemb(v, c), S = cbytes(v, c), be;
     switch (ckind(v, c)) {
     case COLL_AR: be = cdiv(2 * (g - 1) * S, g); break;
@@ -719,9 +598,11 @@ __device__ u32 intra_ticks(const RankView &v, u32 c)
     return P.coll_alpha[cc] + (u32)cdiv(be * P.coll_beta_num[cc], P.coll_beta_den[cc]);
 }
 
+__device__ __forceinline__ u32 rank_item(const XV &V, u32 r) { return V.X.nsw + r / 32; }
+
 __device__ __forceinline__ void rank_poke(RankView &v, u32 item, u32 at)
 {
-    atomicMin(&v.P->wake[item], at);
+    atomicMin(&v.poke[item], at);
     v.pk_min = min(v.pk_min, at);
 }
 
@@ -732,7 +613,7 @@ __device__ void poke_members(RankView &v, u32 c, u32 at)
 {
     u32 N = nmemb(v, c), last = kUnset;
     for (u32 m = 0; m < N; m++) {
-        u32 g = rank_item(*v.X, mrank(v, c, m));
+        u32 g = rank_item(*v.V, mrank(v, c, m));
         if (g != last) rank_poke(v, g, at);
         last = g;
     }
@@ -740,34 +621,33 @@ __device__ void poke_members(RankView &v, u32 c, u32 at)
 
 __device__ void pend_add(RankView &v, u32 u, u32 st)
 {
-    if (v.C.npend >= kNPend) { v.fail_over = true; return; }
-    v.P->pend[v.rk * kNPend + v.C.npend++] = make_uint2(u, st);
+    if (v.C.npend >= X_(v).pend_cap) { v.fail_over = true; return; }
+    v.V->pend[(u64)v.r * X_(v).pend_cap + v.C.npend++] = make_uint2(u, st);
 }
 
 __device__ void complete_node(RankView &v, u32 u, u32 c)
 {
     const Params &P = *v.P;
-    u64 g = v.X->nd_off + u;
-    __stcg(&P.nd_end[g], c);
+    const XV &V = *v.V;
+    V.nd_end[u] = c;
     v.n_done++;
     v.end_max1 = max(v.end_max1, c + 1);
     v.changed = true;
     if (c >= kTickLimit) { v.fail_over = true; return; }
-    u32 s0 = P.succ_start[v.W->node_off + u], ns = P.node_nsucc[v.W->node_off + u];
+    u32 s0 = P.succ_start[W_(v).node_off + u], ns = P.node_nsucc[W_(v).node_off + u];
     for (u32 j = 0; j < ns; j++) {
-        u32 w = P.succ[v.W->edge_off + s0 + j];
-        u64 gw = v.X->nd_off + w;
-        u32 cd = max(__ldcg(&P.nd_cand[gw]), c + 1);
-        __stcg(&P.nd_cand[gw], cd);
-        u32 left = __ldcg(&P.nd_pred[gw]) - 1;
-        __stcg(&P.nd_pred[gw], left);
+        u32 w = P.succ[W_(v).edge_off + s0 + j];
+        u32 cd = max(V.nd_cand[w], c + 1);
+        V.nd_cand[w] = cd;
+        u32 left = V.nd_pred[w] - 1;
+        V.nd_pred[w] = left;
         if (left == 0) pend_add(v, w, cd);
     }
 }
 
 __device__ void free_ports(RankView &v, u32 u)
 {
-    u32 np = nports_of(v, coll_of(v, u)), b = __ldcg(&v.P->nd_pbase[v.X->nd_off + u]);
+    u32 np = nports_of(v, coll_of(v, u)), b = v.V->nd_pbase[u];
     for (u32 p = b; p < b + np; p++) v.C.port_mask[p >> 6] &= ~(1ull << (p & 63));
 }
 
@@ -775,53 +655,57 @@ __device__ void free_ports(RankView &v, u32 u)
 __device__ bool net_join(RankView &v, u32 u)
 {
     const Params &P = *v.P;
-    u32 c = coll_of(v, u), i = P.node_member[v.W->node_off + u];
+    const XV &V = *v.V;
+    const ExpRec &X = V.X;
+    u32 c = coll_of(v, u), i = P.node_member[W_(v).node_off + u];
     u32 np = nports_of(v, c);
     i32 base = -1;
-    for (u32 b = 0; b + np <= kNPort && base < 0; b++) {
+    for (u32 b = 0; b + np <= X.port_cap && base < 0; b++) {
         u32 k = 0;
         while (k < np && !((v.C.port_mask[(b + k) >> 6] >> ((b + k) & 63)) & 1ull)) k++;
         if (k == np) base = (i32)b;
     }
     if (base < 0) { v.fail_over = true; return false; }
     i32 out = 0;
+    uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     for (u32 p = 0; p < np; p++) {
         u32 s = (u32)base + p;
         v.C.port_mask[s >> 6] |= 1ull << (s & 63);
-        P.ports[v.rk * kNPort + s] = make_uint2(0, u);
+        ports[s] = make_uint2(0, u);
         out += (i32)port_count_expect(v, c, i, p);
     }
     u32 nch = nchan(v, c), lpc = tree_of(v, c) ? 3u : 1u;
+    const u64 lane_ok = X.lane_cap >= 64 ? ~0ull : ((1ull << X.lane_cap) - 1);
+    Lane *lanes = V.lanes + (u64)v.r * X.lane_cap;
     for (u32 ch = 0; ch < nch; ch++) {
         for (u32 kd = 0; kd < lpc; kd++) {
             u32 nm = lane_count(v, c, i, ch, kd);
             if (nm == 0) continue;
-            u64 freem = ~v.C.lane_mask;
+            u64 freem = ~v.C.lane_mask & lane_ok;
             if (!freem) { v.fail_over = true; return false; }
             u32 slot = (u32)__ffsll((long long)freem) - 1;
             Lane L = {};
             L.node = u; L.member = i; L.chan = ch; L.kind = kd;
             L.m = 0; L.nmsg = nm;
             L.pkts_left = lane_setup(v, L);
-            store_lane(&P.lanes[v.rk * kNLane + slot], L);
+            store_lane(&lanes[slot], L);
             v.C.lane_mask |= 1ull << slot;
             out += (i32)nm;
         }
     }
-    u64 g = v.X->nd_off + u;
-    __stcg(&P.nd_pbase[g], (u32)base);
-    __stcg(&P.nd_done[g], v.t);
-    __stcg(&P.nd_out[g], out);
+    st_vol32(&V.nd_pbase[u], (u32)base);
+    st_vol32(&V.nd_done[u], v.t);
+    *reinterpret_cast<volatile i32 *>(&V.nd_out[u]) = out;
     return true;
 }
 
 __device__ void act_add(RankView &v, u32 u)
 {
-    if (v.C.nact >= kNAct) { v.fail_over = true; return; }
-    u32 *a = v.P->act + v.rk * kNAct;
+    if (v.C.nact >= X_(v).act_cap) { v.fail_over = true; return; }
+    u32 *a = v.V->act + (u64)v.r * X_(v).act_cap;
     u32 j = v.C.nact;                       // keep ascending node order
-    while (j > 0 && __ldcg(&a[j - 1]) > u) { __stcg(&a[j], __ldcg(&a[j - 1])); j--; }
-    __stcg(&a[j], u);
+    while (j > 0 && a[j - 1] > u) { a[j] = a[j - 1]; j--; }
+    a[j] = u;
     v.C.nact++;
 }
 
@@ -830,42 +714,42 @@ __device__ void act_add(RankView &v, u32 u)
 __device__ void dag_step(RankView &v)
 {
     const Params &P = *v.P;
+    const XV &V = *v.V;
     const u32 t = v.t;
-    u32 *a = P.act + v.rk * kNAct;
+    u32 *a = V.act + (u64)v.r * V.X.act_cap;
     u32 w = 0;
     for (u32 j = 0; j < v.C.nact; j++) {
-        u32 u = __ldcg(&a[j]), c = coll_of(v, u);
+        u32 u = a[j], c = coll_of(v, u);
         bool fin = false;
-        if (P.node_kind[v.W->node_off + u] == NODE_INTRA) {
+        if (P.node_kind[W_(v).node_off + u] == NODE_INTRA) {
             u32 N = nmemb(v, c), b = 0;
             bool ok = true;
             for (u32 m = 0; m < N && ok; m++) {
-                u32 st = ld_rlx32(&P.nd_start[v.X->nd_off + mnode(v, c, m)]);
+                u32 st = ld_vol32(&V.nd_start[mnode(v, c, m)]);
                 if (st == kUnset || st >= t) ok = false;
                 else b = max(b, st);
             }
             if (ok) { complete_node(v, u, b + intra_ticks(v, c)); fin = true; }
         } else {
-            u64 g = v.X->nd_off + u;
-            if (ld_acq32(&P.nd_out[g]) == 0) {
-                u32 done = ld_rlx32(&P.nd_done[g]);
+            if (ld_acq32(&V.nd_out[u]) == 0) {
+                u32 done = ld_vol32(&V.nd_done[u]);
                 free_ports(v, u);
                 complete_node(v, u, done);
                 fin = true;
             }
         }
-        if (!fin) __stcg(&a[w++], u);
+        if (!fin) a[w++] = u;
     }
     v.C.nact = w;
     // start scheduled nodes: take those due now out of the pending list
-    uint2 *pd = P.pend + v.rk * kNPend;
+    uint2 *pd = V.pend + (u64)v.r * V.X.pend_cap;
     u32 due[kNPend];
     u32 nd = 0, keep = 0;
     for (u32 j = 0; j < v.C.npend; j++) {
-        uint2 x = __ldcg(&pd[j]);
+        uint2 x = pd[j];
         if (x.y < t) { v.fail_err = true; continue; }
         if (x.y == t) due[nd++] = x.x;
-        else { __stcg(&pd[keep++], x); v.nxt = min(v.nxt, x.y); }
+        else { pd[keep++] = x; v.nxt = min(v.nxt, x.y); }
     }
     v.C.npend = keep;
     for (u32 j = 1; j < nd; j++) {           // insertion sort, node order
@@ -875,21 +759,20 @@ __device__ void dag_step(RankView &v)
     }
     for (u32 j = 0; j < nd; j++) {
         u32 u = due[j];
-        u64 g = v.X->nd_off + u;
         v.changed = true;
-        u32 kind = P.node_kind[v.W->node_off + u];
+        u32 kind = P.node_kind[W_(v).node_off + u];
         if (kind == NODE_COMPUTE) {
-            __stcg(&P.nd_start[g], t);
+            st_vol32(&V.nd_start[u], t);
             complete_node(v, u, t + compute_ticks(v, u));
         } else if (kind == NODE_INTRA) {
-            st_rlx32(&P.nd_start[g], t);
+            st_vol32(&V.nd_start[u], t);
             act_add(v, u);
             poke_members(v, coll_of(v, u), t + 1);
         } else {
             if (!net_join(v, u)) return;
-            st_rlx32(&P.nd_start[g], t);
-            poke_members(v, coll_of(v, u), t + v.T->rdv);
-            if (__ldcg(&P.nd_out[g]) == 0) {
+            st_vol32(&V.nd_start[u], t);
+            poke_members(v, coll_of(v, u), t + V.T.rdv);
+            if (ld_acq32(&V.nd_out[u]) == 0) {
                 free_ports(v, u);
                 complete_node(v, u, t);
             } else {
@@ -899,7 +782,7 @@ __device__ void dag_step(RankView &v)
         if (v.fail_over || v.fail_err) return;
     }
     // nodes scheduled by completions above may start later; note the earliest
-    for (u32 j = 0; j < v.C.npend; j++) v.nxt = min(v.nxt, __ldcg(&pd[j]).y);
+    for (u32 j = 0; j < v.C.npend; j++) v.nxt = min(v.nxt, pd[j].y);
 }
 
 // SendSys + NICSndSys: one packet per uplink serialisation time, round-robin
@@ -908,57 +791,59 @@ __device__ void dag_step(RankView &v)
 __device__ void inject(RankView &v)
 {
     const Params &P = *v.P;
+    const XV &V = *v.V;
+    const ExpRec &X = V.X;
+    const TopoRec &T = V.T;
     const u32 t = v.t;
     if (!v.C.lane_mask) return;
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
-    const TopoRec &T = *v.T;
     u32 qp = P.host_port[T.host_off + v.r];
-    u64 qi = v.X->q_off + qp;
-    u64 pw = ld_rlx64(&P.q_pop[qi]);
+    u64 pw = ld_vol64(&V.q_pop[qp]);
     u32 head = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-    u32 tail = (u32)__ldcg(&P.q_push[qi]);
-    if (!credit_ok(P, qi, tail, head, P.host_delta[T.host_off + v.r] + 1, t, v.X->cap)) {
+    u32 tail = (u32)V.q_push[qp];
+    if (!credit_ok(V, qp, tail, head, P.host_delta[T.host_off + v.r] + 1, t)) {
         v.nxt = min(v.nxt, t + 1);
         return;
     }
     u64 M = v.C.lane_mask;
     u64 hi = v.C.rr < 64 ? (M & (~0ull << v.C.rr)) : 0ull;
     u64 lo = M & ~hi;
-    Lane *lanes = P.lanes + v.rk * kNLane;
+    Lane *lanes = V.lanes + (u64)v.r * X.lane_cap;
+    const uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     for (int pass = 0; pass < 2; pass++) {
         u64 m = pass == 0 ? hi : lo;
         while (m) {
             u32 l = (u32)__ffsll((long long)m) - 1;
             m &= m - 1;
             Lane L = load_lane(&lanes[l]);
-            u32 pb = __ldcg(&P.nd_pbase[v.X->nd_off + L.node]);
+            u32 pb = V.nd_pbase[L.node];
             bool ok = true;
             for (u32 b = 0; b < 3 && ok; b++)
                 if ((L.dep_mask >> b) & 1u)
-                    if (__ldcg(&P.ports[v.rk * kNPort + pb + L.dep_base + b]).x < L.dep_need) ok = false;
+                    if (ports[pb + L.dep_base + b].x < L.dep_need) ok = false;
             if (!ok) continue;
             u32 c = coll_of(v, L.node);
-            u64 dg = v.X->nd_off + mnode(v, c, L.dst_member);
-            u32 dst_start = ld_rlx32(&P.nd_start[dg]);
+            u32 dn = mnode(v, c, L.dst_member);
+            u32 dst_start = ld_vol32(&V.nd_start[dn]);
             // the destination's join reaches this rank 1 + min(delta) ticks
             // later; when that time is known, it is this rank's own wake (a
             // poke alone could be shadowed by an earlier pending wake)
             if (dst_start == kUnset) continue;
             if (dst_start + T.rdv > t) { v.nxt = min(v.nxt, dst_start + T.rdv); continue; }
-            u32 dpb = ld_rlx32(&P.nd_pbase[dg]);
+            u32 dpb = ld_vol32(&V.nd_pbase[dn]);
             u32 hs = P.host_sigma[T.host_off + v.r], hd = P.host_delta[T.host_off + v.r];
             uint4 pk;
             pk.x = t + hs + hd;
             pk.y = mrank(v, c, L.dst_member) | ((hd + 1) << 16);
             pk.z = L.node;
             pk.w = L.key | ((L.pkts_left == 1 ? 1u : 0u) << 24) | ((dpb + L.dst_port) << 25);
-            __stcg(&P.slots[v.X->slot_off + (u64)qp * v.X->cap + tail % v.X->cap], pk);
-            st_rlx64(&P.q_push[qi], ((u64)t << 32) | (u32)(tail + 1));
+            V.slots[(u64)qp * X.cap + tail % X.cap] = pk;
+            st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
             v.C.busy = t + hs;
             v.C.rr = (l + 1) % kNLane;
             v.n_inj++;
             v.changed = true;
-            rank_poke(v, sw_item(*v.X, P.port_sw[T.port_off + qp]), pk.x);
+            rank_poke(v, P.port_sw[T.port_off + qp], pk.x);
             if (--L.pkts_left == 0) {
                 if (++L.m == L.nmsg) v.C.lane_mask &= ~(1ull << l);
                 else L.pkts_left = lane_setup(v, L);
@@ -976,158 +861,327 @@ __device__ void inject(RankView &v)
 __device__ void receive(RankView &v)
 {
     const Params &P = *v.P;
+    const XV &V = *v.V;
+    const ExpRec &X = V.X;
     const u32 t = v.t;
-    u32 ql = v.T->nq + v.r;
-    u64 qi = v.X->q_off + ql;
-    u64 pw = ld_rlx64(&P.q_push[qi]);
+    u32 ql = V.T.nq + v.r;
+    u64 pw = ld_vol64(&V.q_push[ql]);
     u32 tail = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-    u32 head = (u32)__ldcg(&P.q_pop[qi]);
+    u32 head = (u32)V.q_pop[ql];
     if (head == tail) return;
-    uint4 pk = __ldcg(&P.slots[v.X->slot_off + (u64)ql * v.X->cap + head % v.X->cap]);
+    uint4 pk = V.slots[(u64)ql * X.cap + head % X.cap];
     if (pk.x > t) { v.nxt = min(v.nxt, pk.x); return; }
-    __stcg(&P.poplog[qi * kPopLog + head % kPopLog], t);
-    st_rlx64(&P.q_pop[qi], ((u64)t << 32) | (u32)(head + 1));
+    st_vol32(&V.poplog[(u64)ql * V.plog + (head & (V.plog - 1))], t);
+    st_vol64(&V.q_pop[ql], ((u64)t << 32) | (u32)(head + 1));
     v.n_del++;
     v.changed = true;
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     if (!pk_last(pk)) return;
     v.nxt = min(v.nxt, t + 1);                         // DAG looks at its counts next tick
-    rank_poke(v, rank_item(*v.X, P.node_rank[v.W->node_off + pk.z]), t + 1);   // the ACK
+    rank_poke(v, rank_item(V, P.node_rank[W_(v).node_off + pk.z]), t + 1);   // the ACK
+    uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     u32 ps = pk_slot(pk);
-    uint2 port = __ldcg(&P.ports[v.rk * kNPort + ps]);
+    uint2 port = ports[ps];
     port.x++;
-    __stcg(&P.ports[v.rk * kNPort + ps], port);
-    u64 own = v.X->nd_off + port.y, snd = v.X->nd_off + pk.z;
-    atomicMax(&P.nd_done[own], t);
-    __threadfence();
-    atomicSub(&P.nd_out[own], 1);
-    atomicMax(&P.nd_done[snd], t + pk_hops(pk));
-    __threadfence();
-    atomicSub(&P.nd_out[snd], 1);
+    ports[ps] = port;
+    u32 own = port.y, snd = pk.z;
+    atomicMax(&V.nd_done[own], t);
+    __threadfence_block();
+    atomicSub(&V.nd_out[own], 1);
+    atomicMax(&V.nd_done[snd], t + pk_hops(pk));
+    __threadfence_block();
+    atomicSub(&V.nd_out[snd], 1);
     v.n_msg++;
     v.dig += mix64(mix64((u64)pk.z | ((u64)pk_key(pk) << 32)) ^ (u64)t);
-    if (v.X->rec_cap) {
-        u32 idx = atomicAdd(&v.c->rec_count, 1);
-        if (idx < v.X->rec_cap) {
-            P.rec_sender[v.X->rec_off + idx] = pk.z;
-            P.rec_key[v.X->rec_off + idx] = pk_key(pk);
-            P.rec_tick[v.X->rec_off + idx] = t;
-        }
-    } else {
-        atomicAdd(&v.c->rec_count, 1);
+    u32 idx = atomicAdd(&v.TC->rec_count, 1u);
+    if (idx < X.rec_cap) {
+        P.rec_sender[X.rec_off + idx] = pk.z;
+        P.rec_key[X.rec_off + idx] = pk_key(pk);
+        P.rec_tick[X.rec_off + idx] = t;
     }
 }
 
-__device__ __noinline__ void rank_tick(const Params &P, const ExpRec &X, u32 e, u32 r, u32 t, u32 k)
+// Ranks g*32 .. g*32+31 for one tick, one lane each.  Returns the warp's
+// earliest known next event; *done / *fail receive nodes completed and the
+// failure key.
+__device__ __noinline__ u32 rank_tick(const Params &P, const XV &V, Team &TC, u32 g, u32 t,
+                                      u32 old, u32 *poke, u32 *done_out, u32 *fail)
 {
-    const TopoRec T = P.topo[X.topo];
-    const WorkRec W = P.work[X.work];
+    const u32 lane = threadIdx.x & 31;
+    const u32 it = V.X.nsw + g;
     RankView v;
-    v.P = &P; v.X = &X; v.T = &T; v.W = &W; v.c = &P.ctl[e];
-    v.r = r; v.t = t; v.e = e; v.k = k; v.rk = X.rk_off + r;
+    v.P = &P; v.V = &V; v.TC = &TC; v.poke = poke;
+    v.r = g * 32 + lane; v.t = t;
     v.changed = v.fail_over = v.fail_err = false;
     v.nxt = kUnset;
     v.pk_min = kUnset;
-    const u32 it = rank_item(X, r - (r % 32));
-    u32 old = 0;
-    if ((threadIdx.x & 31) == 0) old = atomicExch(&P.wake[it], kUnset);
-    old = __shfl_sync(0xffffffffu, old, 0);
     v.n_inj = v.n_del = v.n_msg = v.n_done = v.end_max1 = 0;
     v.dig = 0;
-    const bool active = r < X.nr;
-    if (active) {
-        v.C = load_ctl(&P.rk[v.rk]);
+    if (v.r < V.X.nr) {
+        v.C = load_ctl(&V.rk[v.r]);
         dag_step(v);
         if (!v.fail_over && !v.fail_err) {
             inject(v);
             receive(v);
         }
-        store_ctl(&P.rk[v.rk], v.C);
+        store_ctl(&V.rk[v.r], v.C);
     }
-    const u32 full = 0xffffffffu;
-    u32 nxt = __reduce_min_sync(full, v.nxt);
-    u32 pkm = __reduce_min_sync(full, v.pk_min);
-    u32 inj = __reduce_add_sync(full, v.n_inj);
-    u32 del = __reduce_add_sync(full, v.n_del);
-    u32 msg = __reduce_add_sync(full, v.n_msg);
-    u32 done = __reduce_add_sync(full, v.n_done);
-    u32 emax = __reduce_max_sync(full, v.end_max1);
-    bool over = __any_sync(full, v.fail_over), err = __any_sync(full, v.fail_err);
+    u32 nxt = __reduce_min_sync(kFull, v.nxt);
+    u32 pkm = __reduce_min_sync(kFull, v.pk_min);
+    u32 inj = __reduce_add_sync(kFull, v.n_inj);
+    u32 del = __reduce_add_sync(kFull, v.n_del);
+    u32 msg = __reduce_add_sync(kFull, v.n_msg);
+    u32 done = __reduce_add_sync(kFull, v.n_done);
+    u32 emax = __reduce_max_sync(kFull, v.end_max1);
+    u32 fk = v.fail_over ? fail_key_rank(v.r, EXP_OVERFLOW)
+           : v.fail_err ? fail_key_rank(v.r, EXP_ERROR) : kUnset;
+    fk = __reduce_min_sync(kFull, fk);
     // 64-bit digest sum across the warp
     u64 dig = v.dig;
-    for (int o = 16; o > 0; o >>= 1) dig += __shfl_xor_sync(full, dig, o);
-    if ((threadIdx.x & 31) == 0) {
-        ExpCtl *c = v.c;
-        u32 w = min(nxt, old > t ? old : kUnset);
-        if (w != kUnset) atomicMin(&P.wake[it], w);
-        u32 m = min(w, pkm);
-        if (m != kUnset) atomicMin(&c->nxt[k % 3], m);
+    for (int o = 16; o > 0; o >>= 1) dig += __shfl_xor_sync(kFull, dig, o);
+    u32 w = min(nxt, old > t ? old : kUnset);
+    if (lane == 0) {
+        V.wake[it] = w;
         if (inj) {
-            atomicAdd((unsigned long long *)&c->pkts_injected, (unsigned long long)inj);
-            atomicAdd((unsigned long long *)&c->pkt_hops, (unsigned long long)inj);
+            atomicAdd(&TC.pkts_injected, (unsigned long long)inj);
+            atomicAdd(&TC.pkt_hops, (unsigned long long)inj);
         }
-        if (del) atomicAdd((unsigned long long *)&c->pkts_delivered, (unsigned long long)del);
+        if (del) atomicAdd(&TC.pkts_delivered, (unsigned long long)del);
         if (msg) {
-            atomicAdd((unsigned long long *)&c->msgs_delivered, (unsigned long long)msg);
-            atomicAdd((unsigned long long *)&c->digest, (unsigned long long)dig);
+            atomicAdd(&TC.msgs_delivered, (unsigned long long)msg);
+            atomicAdd(&TC.digest, (unsigned long long)dig);
         }
-        if (emax) atomicMax(&c->end_max1, emax);
-        if (done && atomicSub(&c->nodes_left, done) == done) atomicMin(&c->stop_step, k);
-        if (over) set_status(c, EXP_OVERFLOW, k);
-        if (err) set_status(c, EXP_ERROR, k);
+        if (emax) atomicMax(&TC.end_max1, emax);
     }
+    *done_out += done;
+    *fail = min(*fail, fk);
+    return min(w, pkm);
 }
 
 // ---------------------------------------------------------------- megakernel
-constexpr int kBlock = 512;
-constexpr int kWarps = kBlock / 32;
-
-// Each warp owns a contiguous chunk of work items (an experiment's items are
-// contiguous: its switches, then its rank groups).  Per step it reads the
-// wake ticks of 32 items at once, ballots the ones due, reports the pending
-// wakes of the others (one atomic per experiment per warp), and processes the
-// due ones one after the other with the whole warp.
-__global__ void __launch_bounds__(kBlock, 1) k_megakernel(Params P)
+// Copy n bytes (a multiple of 4) between an experiment's global slice and
+// its shared-memory image, all threads of the block.
+__device__ __forceinline__ void block_copy(void *dst, const void *src, u64 n)
 {
-    __shared__ SwSmem smem[kWarps];
-    const u32 full = 0xffffffffu;
-    const u32 warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const u32 gwarp = blockIdx.x * kWarps + warp;
-    const u32 nwarps = gridDim.x * kWarps;
-    const u32 per = (P.n_items + nwarps - 1) / nwarps;
-    const u32 i0 = min(gwarp * per, P.n_items), i1 = min(i0 + per, P.n_items);
-    const bool leader_thread = blockIdx.x == 0 && threadIdx.x == 0;
-    for (u32 k = 0;; k++) {
-        if (leader_thread) P.glob->run_cnt[(k + 1) % 3] = 0;   // last read after barrier k-2
+    u32 *d = reinterpret_cast<u32 *>(dst);
+    const u32 *s = reinterpret_cast<const u32 *>(src);
+    for (u64 i = threadIdx.x; i < n / 4; i += blockDim.x) d[i] = s[i];
+}
+
+// Global slice of array k of experiment X (k in the image order).
+__device__ void *global_slice(const Params &P, const ExpRec &X, int k)
+{
+    switch (k) {
+    case IM_WAKE: return P.wake + 3ull * X.item_off;
+    case IM_QPUSH: return P.q_push + X.q_off;
+    case IM_QPOP: return P.q_pop + X.q_off;
+    case IM_EG: return P.eg + X.eg_off;
+    case IM_RK: return P.rk + X.rk_off;
+    case IM_PRED: return P.nd_pred + X.nd_off;
+    case IM_CAND: return P.nd_cand + X.nd_off;
+    case IM_START: return P.nd_start + X.nd_off;
+    case IM_END: return P.nd_end + X.nd_off;
+    case IM_PBASE: return P.nd_pbase + X.nd_off;
+    case IM_DONE: return P.nd_done + X.nd_off;
+    case IM_OUT: return P.nd_out + X.nd_off;
+    case IM_ACT: return P.act + X.act_off;
+    case IM_PEND: return P.pend + X.pend_off;
+    case IM_PORTS: return P.ports + X.portc_off;
+    case IM_POPLOG: return P.poplog + X.plog_off;
+    case IM_LANES: return P.lanes + X.lane_off;
+    default: return P.slots + X.slot_off;
+    }
+}
+
+__device__ void set_slice(XV &V, int k, void *p)
+{
+    switch (k) {
+    case IM_WAKE: V.wake = (u32 *)p; break;
+    case IM_QPUSH: V.q_push = (u64 *)p; break;
+    case IM_QPOP: V.q_pop = (u64 *)p; break;
+    case IM_EG: V.eg = (uint2 *)p; break;
+    case IM_RK: V.rk = (RankCtl *)p; break;
+    case IM_PRED: V.nd_pred = (u32 *)p; break;
+    case IM_CAND: V.nd_cand = (u32 *)p; break;
+    case IM_START: V.nd_start = (u32 *)p; break;
+    case IM_END: V.nd_end = (u32 *)p; break;
+    case IM_PBASE: V.nd_pbase = (u32 *)p; break;
+    case IM_DONE: V.nd_done = (u32 *)p; break;
+    case IM_OUT: V.nd_out = (i32 *)p; break;
+    case IM_ACT: V.act = (u32 *)p; break;
+    case IM_PEND: V.pend = (uint2 *)p; break;
+    case IM_PORTS: V.ports = (uint2 *)p; break;
+    case IM_POPLOG: V.poplog = (u32 *)p; break;
+    case IM_LANES: V.lanes = (Lane *)p; break;
+    default: V.slots = (uint4 *)p; break;
+    }
+}
+
+__shared__ XV s_V;
+__shared__ Team s_TC;
+__shared__ u64 s_off[IM_N];
+__shared__ u64 s_sz[IM_N];
+__shared__ u32 s_slot;
+
+// Step experiment e from its clock until it finishes, stops, or reaches the
+// run's tick budget; `img` is this block's shared-memory image space.
+__device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSmem *sm,
+                               u64 t_start)
+{
+    XV &V = s_V;
+    Team &TC = s_TC;
+    const u32 warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nW = blockDim.x >> 5;
+    if (threadIdx.x == 0) {
+        V.X = P.exp[e];
+        V.T = P.topo[V.X.topo];
+        V.W = P.work[V.X.work];
+        V.e = e;
+        V.plog = V.T.plog;
+        const ExpCtl c = P.ctl[e];
+        TC.end_max1 = c.end_max1;
+        TC.rec_count = c.rec_count;
+        TC.now0 = c.now;
+        TC.status0 = c.status;
+        TC.left0 = c.nodes_left;
+        TC.pkts_injected = c.pkts_injected;
+        TC.pkt_hops = c.pkt_hops;
+        TC.pkts_delivered = c.pkts_delivered;
+        TC.msgs_delivered = c.msgs_delivered;
+        TC.digest = c.digest;
+        image_layout(V.X, V.plog, V.T.nq, s_off);
+        image_bytes(V.X, V.plog, V.T.nq, s_sz);
+        // what goes to shared memory: the whole image, the wake table, or nothing
+        u32 n_staged = 0;
+        if (P.stage_mode == 0 && V.X.stage_bytes && V.X.stage_bytes <= P.stage_limit) n_staged = IM_N;
+        else if (P.stage_mode <= 1 && im_round(s_sz[IM_WAKE]) <= P.stage_limit) n_staged = 1;
+        V.staged = n_staged;
+        for (int k = 0; k < IM_N; k++)
+            set_slice(V, k, k < (int)n_staged ? (void *)(img + s_off[k]) : global_slice(P, V.X, k));
+    }
+    __syncthreads();
+    const u32 n_staged = V.staged;
+    for (int k = 0; k < (int)n_staged; k++) block_copy(img + s_off[k], global_slice(P, V.X, k), s_sz[k]);
+    __syncthreads();
+
+    u32 t = TC.now0, status = TC.status0, left = TC.left0, now = TC.now0;
+    const u64 lim64 = (u64)t + P.max_ticks;
+    const u32 limit = lim64 > kTickLimit ? kTickLimit : (u32)lim64;
+    u32 k = 0;
+    if (status == EXP_RUNNING && left == 0) {
+        status = EXP_DONE;
+        now = TC.end_max1;
+    }
+    const u32 nI = V.X.n_items, nsw = V.X.nsw;
+    const u32 per = (nI + nW - 1) / nW;
+    const u32 i0 = min(warp * per, nI), i1 = min(i0 + per, nI);
+    // Wake table: own[nI] (written by the item's warp only) and two poke
+    // words per item.  Pokes made during step k go to word k & 1; the owner
+    // folds them into own at the start of step k + 1, after the barrier, so
+    // no poke is lost whatever order warps run in.  Pokes left by an earlier
+    // run are folded before the first step.
+    u32 *own = V.wake, *pk0 = V.wake + nI, *pk1 = V.wake + 2 * nI;
+    for (u32 it = i0 + lane; it < i1; it += 32) {
+        u32 o = own[it], a = ld_vol32(&pk0[it]), b = ld_vol32(&pk1[it]);
+        own[it] = min(o, min(a, b));
+        pk0[it] = kUnset;
+        pk1[it] = kUnset;
+    }
+    __syncthreads();
+    while (status == EXP_RUNNING) {
+        if (t >= limit) { now = t; break; }
+        u32 rep = kUnset, done = 0, fail = kUnset;
+        u32 *poke = (k & 1) ? pk1 : pk0, *prev = (k & 1) ? pk0 : pk1;
         for (u32 base = i0; base < i1; base += 32) {
             const u32 it = base + lane;
-            const bool valid = it < i1;
-            const u32 e = valid ? P.item_exp[it] : kUnset;
-            const u32 loc = valid ? P.item_loc[it] : 0;
-            const u32 t = valid ? exp_tick(P, e, k) : kUnset;
-            if (valid && loc == 0) exp_control(P, e, k, t);
-            const u32 w = t != kUnset ? ld_rlx32(&P.wake[it]) : kUnset;
-            const bool due = t != kUnset && w <= t;
-            const u32 peers = __match_any_sync(full, e);
-            const u32 rep = __reduce_min_sync(peers, due ? kUnset : w);
-            if (e != kUnset && rep != kUnset && lane == (u32)__ffs(peers) - 1)
-                atomicMin(&P.ctl[e].nxt[k % 3], rep);
-            u32 M = __ballot_sync(full, due);
+            u32 w = kUnset;
+            if (it < i1) {
+                w = own[it];
+                const u32 q = ld_vol32(&prev[it]);
+                if (q != kUnset) {
+                    prev[it] = kUnset;
+                    w = min(w, q);
+                    own[it] = w;
+                }
+            }
+            const bool due = w <= t;
+            rep = min(rep, due ? kUnset : w);
+            u32 M = __ballot_sync(kFull, due);
             while (M) {
                 const u32 j = (u32)__ffs(M) - 1;
                 M &= M - 1;
-                const u32 ej = __shfl_sync(full, e, j), lj = __shfl_sync(full, loc, j),
-                          tj = __shfl_sync(full, t, j);
-                const ExpRec X = P.exp[ej];
-                if (lj < X.nsw) switch_tick(P, X, ej, lj, tj, k, &smem[warp]);
-                else rank_tick(P, X, ej, (lj - X.nsw) * 32 + lane, tj, k);
+                const u32 item = base + j;
+                const u32 old = __shfl_sync(kFull, w, j);
+                u32 r = item < nsw ? switch_tick(P, V, TC, item, t, old, poke, sm, &fail)
+                                   : rank_tick(P, V, TC, item - nsw, t, old, poke, &done, &fail);
+                rep = min(rep, r);
             }
         }
-        if (!grid_barrier(P, k)) break;
-        if (ld_rlx32(&P.glob->run_cnt[k % 3]) == 0) {
-            if (leader_thread) P.glob->steps = k + 1;
-            break;
+        rep = __reduce_min_sync(kFull, rep);
+        if (lane == 0) {
+            u32 ab = 0;
+            if (warp == 0 && (k & 255) == 255) {
+                if (ld_vol32(&P.glob->error)) ab = 1;
+                else if (P.watchdog_ns && globaltimer() - t_start > P.watchdog_ns) {
+                    atomicExch(&P.glob->error, 1u);
+                    ab = 1;
+                }
+            }
+            TC.rep[k & 1][warp] = make_uint4(rep, done, fail, ab);
         }
+        __syncthreads();
+        u32 nx = kUnset, dn = 0, fk = kUnset, ab = 0;
+        for (u32 q = 0; q < nW; q++) {
+            uint4 r = TC.rep[k & 1][q];
+            nx = min(nx, r.x);
+            dn += r.y;
+            fk = min(fk, r.z);
+            ab |= r.w;
+        }
+        left -= dn;
+        k++;
+        if (fk != kUnset) { status = fk & 7u; now = TC.end_max1; break; }
+        if (left == 0) { status = EXP_DONE; now = TC.end_max1; break; }
+        if (nx == kUnset) { status = EXP_DEADLOCK; now = TC.end_max1; break; }
+        t = nx;
+        if (ab) { now = t; break; }
+    }
+    __syncthreads();
+    for (int k2 = 0; k2 < (int)n_staged; k2++) block_copy(global_slice(P, V.X, k2), img + s_off[k2], s_sz[k2]);
+    if (threadIdx.x == 0) {
+        ExpCtl c;
+        c.status = status;
+        c.now = now;
+        c.nodes_left = left;
+        c.end_max1 = TC.end_max1;
+        c.rec_count = TC.rec_count;
+        c.pad0 = c.pad1 = c.pad2 = 0;
+        c.pkts_injected = TC.pkts_injected;
+        c.pkt_hops = TC.pkt_hops;
+        c.pkts_delivered = TC.pkts_delivered;
+        c.msgs_delivered = TC.msgs_delivered;
+        c.digest = TC.digest;
+        P.ctl[e] = c;
+        atomicMax((unsigned long long *)&P.glob->steps, (unsigned long long)k);
+    }
+    __syncthreads();
+}
+
+// Persistent grid: each block takes the next experiment of the processing
+// order until none is left (or the watchdog fired).
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_megakernel(Params P)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    const u32 nW = blockDim.x >> 5, warp = threadIdx.x >> 5;
+    SwSmem *sw = reinterpret_cast<SwSmem *>(dsm);
+    unsigned char *img = dsm + nW * sizeof(SwSmem);
+    const u64 t_start = globaltimer();
+    for (;;) {
+        if (threadIdx.x == 0) s_slot = ld_vol32(&P.glob->error) ? kUnset : atomicAdd(&P.glob->next, 1u);
+        __syncthreads();
+        const u32 slot = s_slot;
+        __syncthreads();
+        if (slot >= P.n_exps) break;
+        run_experiment(P, P.order[slot], img, sw + warp, t_start);
     }
 }
 
@@ -1144,7 +1198,7 @@ cudaError_t launch_routes(const Params &p, u64 n_pairs_max, u32 level, cudaStrea
 cudaError_t launch_up_lists(const Params &p, u32 n_sw_total, cudaStream_t st)
 {
     u32 blocks = (n_sw_total + 255) / 256;
-    k_up_lists<<<blocks ? (blocks > 1024 ? 1024 : blocks) : 1, 256, 0, st>>>(p, n_sw_total);
+    k_up_lists<<<blocks ? (blocks > 1024 ? 1024 : blocks) : 1, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1162,29 +1216,27 @@ cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_
     return cudaGetLastError();
 }
 
-cudaError_t launch_run_reset(const Params &p, u32 max_ticks, cudaStream_t st)
-{
-    u32 blocks = (p.n_exps + 255) / 256;
-    k_run_reset<<<blocks ? blocks : 1, 256, 0, st>>>(p, max_ticks);
-    return cudaGetLastError();
-}
+u32 megakernel_smem(u32 warps, u32 image_bytes) { return warps * (u32)sizeof(SwSmem) + image_bytes; }
 
-cudaError_t megakernel_occupancy(int *blocks_per_sm, int *n_sm)
+cudaError_t megakernel_prepare(u32 warps, u32 smem_bytes, int *blocks_per_sm, int *n_sm)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_megakernel, kBlock, 0);
+    e = cudaFuncSetAttribute(k_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_megakernel,
+                                                         (int)(warps * 32), smem_bytes);
 }
 
-cudaError_t launch_megakernel(const Params &p, u32 blocks, cudaStream_t st)
+cudaError_t launch_megakernel(const Params &p, u32 blocks, u32 warps, u32 smem_bytes,
+                              cudaStream_t st)
 {
-    Params q = p;
-    void *args[] = {&q};
-    return cudaLaunchCooperativeKernel((void *)k_megakernel, dim3(blocks), dim3(kBlock), args, 0,
-                                       st);
+    k_megakernel<<<blocks, warps * 32, smem_bytes, st>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace mv

@@ -59,8 +59,10 @@ class ResultsView(C.Structure):
 
 
 class RunOpts(C.Structure):
-    _fields_ = [("barrier_timeout_ns", C.c_uint64), ("fault_skip_block", C.c_int32),
-                ("fault_skip_step", C.c_int32), ("grid_blocks", C.c_uint32)]
+    _fields_ = [("watchdog_ns", C.c_uint64), ("grid_blocks", C.c_uint32),
+                ("stage", C.c_uint32), ("block_warps", C.c_uint32), ("pad", C.c_uint32)]
+
+STAGE_AUTO, STAGE_WAKE, STAGE_NONE = 0, 1, 2
 
 
 _lib = None
@@ -171,10 +173,10 @@ class Simulator:
         rc_per = packed["exp_rec_cap"].astype(np.int64)
         self.rec_offset = np.concatenate([[0], np.cumsum(rc_per)])
 
-    def run(self, max_ticks: int = UNSET - 1, barrier_timeout_ns: int = 0,
-            fault_skip_block: int = -1, fault_skip_step: int = -1, grid_blocks: int = 0) -> int:
+    def run(self, max_ticks: int = UNSET - 1, watchdog_ns: int = 0, grid_blocks: int = 0,
+            stage: int = STAGE_AUTO, block_warps: int = 0) -> int:
         steps = C.c_uint64(0)
-        opts = RunOpts(barrier_timeout_ns, fault_skip_block, fault_skip_step, grid_blocks)
+        opts = RunOpts(watchdog_ns, grid_blocks, stage, block_warps, 0)
         with self.torch.cuda.device(self.device):
             rc = self.lib.mv_run_ex(self.ctx, int(max_ticks), C.byref(opts), C.byref(steps))
         self.steps = int(steps.value)
@@ -229,10 +231,11 @@ class Simulator:
             pass
 
 
-def simulate(packed: dict, max_ticks: int = UNSET - 1, **kw) -> dict:
+def simulate(packed: dict, max_ticks: int = UNSET - 1, run_opts: dict | None = None,
+             **kw) -> dict:
     """Create, run to completion (or the budget) and return the results."""
     sim = Simulator(packed, **kw)
-    sim.run(max_ticks)
+    sim.run(max_ticks, **(run_opts or {}))
     out = sim.results()
     out["steps"] = sim.steps
     sim.close()

@@ -47,8 +47,8 @@ extern "C" {
 #define MV_EINVAL (-1)       /* malformed descriptor or argument             */
 #define MV_ENOMEM (-2)       /* workspace smaller than mv_workspace_bytes()  */
 #define MV_ECUDA (-3)        /* a CUDA call failed (launch, copy, sync)      */
-#define MV_ETIMEOUT (-4)     /* the grid barrier waited past its limit; the
-                                kernel returned, results are invalid         */
+#define MV_ETIMEOUT (-4)     /* the run's watchdog fired: every experiment
+                                stopped at a tick boundary (resumable)       */
 #define MV_EOVERFLOW (-5)    /* a size or tick count exceeds 32-bit limits   */
 
 /* ---- per-experiment status (mv_results.status) ----------------------- */
@@ -161,15 +161,26 @@ typedef struct mv_results_view {
 
 typedef struct mv_ctx mv_ctx;
 
-/* Options of one mv_run call.  barrier_timeout_ns bounds every grid-barrier
- * wait (0 = 5 s); past it the kernel sets MV_ETIMEOUT and returns.
- * fault_skip_block/fault_skip_step (test hook, -1 = off): that block skips
- * its arrival at that step's barrier, which must end in MV_ETIMEOUT. */
+/* Options of one mv_run call.
+ * watchdog_ns: 0 = none.  Otherwise, once the launch has run that long
+ *   (device global timer), every block stops its experiment at the next
+ *   tick boundary it checks (every 256 ticks), takes no further experiment,
+ *   and mv_run_ex returns MV_ETIMEOUT.  The state stays consistent: a later
+ *   mv_run continues where each experiment stopped.  The kernel holds no
+ *   lock and waits on no other block, so it cannot hang; the watchdog bounds
+ *   the run time of a call.
+ * grid_blocks: 0 = every block that fits on the device at once.
+ * stage: 0 = an experiment's dynamic state is staged in shared memory when
+ *   it fits, 1 = only its wake table is, 2 = nothing is (results are the
+ *   same in every mode; the modes exist to test and measure that).
+ * block_warps: warps of the block stepping one experiment (0 = automatic,
+ *   at most 16). */
 typedef struct mv_run_opts {
-    uint64_t barrier_timeout_ns;
-    int32_t fault_skip_block;
-    int32_t fault_skip_step;
-    uint32_t grid_blocks;       /* 0 = all co-resident blocks */
+    uint64_t watchdog_ns;
+    uint32_t grid_blocks;
+    uint32_t stage;
+    uint32_t block_warps;
+    uint32_t pad;
 } mv_run_opts;
 
 /* Workspace bytes mv_create needs for this batch (validates the
@@ -189,11 +200,14 @@ int mv_create(const mv_batch_desc *desc, void *dev_workspace, uint64_t ws_bytes,
               void *stream, mv_ctx **out);
 
 /* Advance every unfinished experiment by at most max_ticks ticks of its own
- * clock, in ONE cooperative launch of the persistent megakernel, and wait
- * for it.  State stays on the device, so run(a) then run(b) equals
- * run(a + b).  *steps_done (may be NULL) receives the number of grid-wide
- * steps executed.  Returns MV_OK when no experiment is still running,
- * MV_INCOMPLETE when some hit the budget, or an error. */
+ * clock, in ONE launch of the persistent megakernel, and wait for it.  Each
+ * experiment is stepped by one thread block (its entities spread over the
+ * block's warps, one block barrier per tick); blocks take experiments
+ * largest first.  State stays on the device, so run(a) then run(b) equals
+ * run(a + b).  *steps_done (may be NULL) receives the largest number of
+ * ticks one experiment processed in this call.  Returns MV_OK when no
+ * experiment is still running, MV_INCOMPLETE when some hit the budget, or
+ * an error. */
 int mv_run(mv_ctx *ctx, uint32_t max_ticks, uint64_t *steps_done);
 int mv_run_ex(mv_ctx *ctx, uint32_t max_ticks, const mv_run_opts *opts,
               uint64_t *steps_done);

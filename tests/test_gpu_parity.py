@@ -166,17 +166,32 @@ def test_repeatable():
     assert_same(a, b)
 
 
-def test_barrier_timeout_is_reported_not_hung():
-    """One block skips its barrier arrival: the others give up after the
-    bounded wait, the call returns MV_ETIMEOUT, and the device stays usable."""
+def test_watchdog_stops_at_a_tick_boundary_and_resumes():
+    """The run watchdog fires: every block stops its experiment at a tick
+    boundary, the call returns MV_ETIMEOUT (no hang, no fault), and a later
+    run continues from the saved state to the oracle's exact results."""
     p = I.config1().pack()
     sim = mv.Simulator(p)
     with pytest.raises(mv.MVError) as ei:
-        sim.run(barrier_timeout_ns=200_000_000, fault_skip_block=0, fault_skip_step=3)
+        sim.run(watchdog_ns=1)
     assert ei.value.code == mv.MV_ETIMEOUT
+    mid = sim.results()
+    assert (mid["status"] == mv.EXP_RUNNING).any()
+    assert sim.run() == mv.MV_OK
+    got = sim.results()
     sim.close()
-    got, want = mv.simulate(p), O.run(p)
-    assert_same(got, want)
+    assert_same(got, O.run(p))
+
+
+@pytest.mark.parametrize("stage", [mv.STAGE_WAKE, mv.STAGE_NONE])
+def test_global_memory_path_bit_exact(stage):
+    """The same batches with the dynamic state kept in global memory (wake
+    table in shared memory, or nothing staged) and other block shapes."""
+    for p in (pin_batch().pack(), I.config1().pack()):
+        want = O.run(p)
+        for warps in (0, 1, 3):
+            got = mv.simulate(p, run_opts=dict(stage=stage, block_warps=warps))
+            assert_same(got, want)
 
 
 @pytest.mark.parametrize("algo", [I.RING, I.TREE])

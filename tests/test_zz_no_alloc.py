@@ -65,9 +65,13 @@ def test_static_matches_regular_two_calls_in_a_row():
 
 
 def test_static_rejects_batches_beyond_its_scratch():
-    a, b = I.config2(seed=0), I.config2(seed=1)
-    big = I.Batch(a.experiments + b.experiments).pack()
-    assert mv.workspace_bytes(big) > 32 << 20
+    exps, seed = [], 0
+    while True:                          # enough broadcast experiments to exceed 32 MiB
+        exps += I.config2(seed=seed).experiments
+        seed += 1
+        big = I.Batch(exps).pack()
+        if mv.workspace_bytes(big) > 32 << 20:
+            break
     rc, _ = simulate_static(big)
     assert rc == mv.MV_ENOMEM
     rc, got = simulate_static(I.config1().pack())     # still usable afterwards
