@@ -45,6 +45,8 @@ struct Layout {
     std::vector<ExpRec> exp;
     std::vector<u32> sw_pstart, port_sw, rank_first, succ_start, node_member, coll_mstart,
         memb_row, memb_col, node_rank, order;
+    std::vector<uint2> sw_rec;
+    std::vector<uint4> port_rec, host_rec;
     // regions
     Region r_topo, r_work, r_exp, r_sw_nports, r_sw_level, r_sw_pstart, r_port_sw, r_port_peer,
         r_port_sigma, r_port_delta, r_host_port, r_host_sigma, r_host_delta, r_rank_first,
@@ -53,7 +55,8 @@ struct Layout {
         r_coll_intra, r_coll_nmembers, r_coll_parts, r_coll_alpha, r_coll_beta_num,
         r_coll_beta_den, r_coll_mstart, r_coll_bytes, r_member_rank, r_member_node,
         r_member_a2a_n, r_memb_row, r_a2a_dst, r_member_a2a_in_n, r_memb_col, r_a2a_in_src,
-        r_a2a_bytes, r_a2a_in_bytes, r_mem, r_order, r_node_rank;
+        r_a2a_bytes, r_a2a_in_bytes, r_mem, r_order, r_node_rank, r_sw_rec, r_port_rec,
+        r_host_rec;
     u64 static_bytes = 0;
     Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_pend, r_act,
         r_lanes, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
@@ -100,6 +103,9 @@ int plan(const mv_batch_desc *d, Layout &L)
     }
     L.sw_pstart.resize(L.nsw);
     L.port_sw.resize(L.nports);
+    L.sw_rec.resize(L.nsw);
+    L.port_rec.resize(L.nports);
+    L.host_rec.resize(L.nhosts);
     for (u32 t = 0; t < L.T; t++) {
         TopoRec &R = L.topo[t];
         u32 q = 0;
@@ -131,6 +137,22 @@ int plan(const mv_batch_desc *d, Layout &L)
             if (hp >= R.nq || d->port_peer[R.port_off + hp] != -(i32)(h + 1)) return MV_EINVAL;
             if (sg == 0 || sg > 65535 || dl + 1 > kPopLog) return MV_EINVAL;
             R.rdv = std::min(R.rdv, dl + 1);
+        }
+        // packed records the forwarding and injection steps read per packet
+        for (u32 s = 0; s < R.nsw; s++)
+            L.sw_rec[R.sw_off + s] = make_uint2(L.sw_pstart[R.sw_off + s], d->sw_nports[R.sw_off + s]);
+        for (u32 p = 0; p < R.nq; p++) {
+            i32 pe = d->port_peer[R.port_off + p];
+            u32 dq = pe >= 0 ? (u32)pe : R.nq + (u32)(-(pe + 1));
+            u32 owner = pe >= 0 ? L.port_sw[R.port_off + pe] : (0x80000000u | (u32)(-(pe + 1)));
+            L.port_rec[R.port_off + p] = make_uint4(dq, d->port_sigma[R.port_off + p],
+                                                    d->port_delta[R.port_off + p], owner);
+        }
+        for (u32 h = 0; h < R.nh; h++) {
+            u32 hp = d->host_port[R.host_off + h];
+            L.host_rec[R.host_off + h] = make_uint4(hp, d->host_sigma[R.host_off + h],
+                                                    d->host_delta[R.host_off + h],
+                                                    L.port_sw[R.port_off + hp]);
         }
         // pop log: only the last (delta + 1) - 1 pops of a queue are ever read
         u32 dmax = 1;
@@ -367,7 +389,7 @@ int plan(const mv_batch_desc *d, Layout &L)
         items += X.n_items;
         max_items = std::max(max_items, X.n_items);
         u64 off[IM_N];
-        u64 img = image_layout(X, T.plog, T.nq, off);
+        u64 img = image_layout(X, T, off);
         X.stage_bytes = img <= kStageMax ? (u32)img : 0;
         if (X.stage_bytes) full_max = std::max(full_max, img);
         wake_max = std::max(wake_max, im_round(12ull * X.n_items));
@@ -429,6 +451,9 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_a2a_in_bytes = L.take(8 * L.na2a_in);
     L.r_mem = L.take(80 * L.W);
     L.r_order = L.take(4ull * std::max<u32>(L.E, 1));
+    L.r_sw_rec = L.take(8 * L.nsw);
+    L.r_port_rec = L.take(16 * L.nports);
+    L.r_host_rec = L.take(16 * L.nhosts);
     L.r_node_rank = L.take(4 * L.nnodes);
     L.static_bytes = L.cur;
     L.r_route = L.take(L.route_bytes);
@@ -541,6 +566,9 @@ Params make_params(void *ws, const Layout &L)
     P.rec_key = at<u32>(ws, L.r_rec_key);
     P.rec_tick = at<u32>(ws, L.r_rec_tick);
     P.order = at<u32>(ws, L.r_order);
+    P.sw_rec = at<uint2>(ws, L.r_sw_rec);
+    P.port_rec = at<uint4>(ws, L.r_port_rec);
+    P.host_rec = at<uint4>(ws, L.r_host_rec);
     P.node_rank = at<u32>(ws, L.r_node_rank);
     P.wake = at<u32>(ws, L.r_wake);
     P.n_exps = L.E;
@@ -681,6 +709,9 @@ int mv_create(const mv_batch_desc *d, void *ws, uint64_t ws_bytes, void *stream,
     put(img, L.r_a2a_in_bytes, d->a2a_in_bytes, 8 * L.na2a_in);
     put(img, L.r_mem, d->mem, 80 * L.W);
     put(img, L.r_order, L.order.data(), 4ull * L.E);
+    put(img, L.r_sw_rec, L.sw_rec.data(), 8 * L.nsw);
+    put(img, L.r_port_rec, L.port_rec.data(), 16 * L.nports);
+    put(img, L.r_host_rec, L.host_rec.data(), 16 * L.nhosts);
     put(img, L.r_node_rank, L.node_rank.data(), 4 * L.nnodes);
     cudaError_t e = cudaMemcpyAsync(ws, img.data(), L.static_bytes, cudaMemcpyHostToDevice,
                                     c->stream);

@@ -23,7 +23,7 @@ constexpr u32 kNAct = 16;     // running collective memberships, per rank
 constexpr u32 kMaxPorts = 64; // ports per switch (one warp, two ports a lane)
 constexpr u32 kTickLimit = 0xFFF00000u;
 constexpr u32 kPopLog = 64;   // credit delay (delta + 1) of a link is at most this
-constexpr u32 kMaxWarps = 16; // warps of the block that steps one experiment
+constexpr u32 kMaxWarps = 8;  // warps of the block that steps one experiment
 
 enum : u32 { NODE_COMPUTE = 0, NODE_INTRA = 1, NODE_NET = 2 };
 enum : u32 { COLL_AR = 0, COLL_RS = 1, COLL_AG = 2, COLL_RELAY = 3, COLL_P2P = 4, COLL_A2A = 5 };
@@ -63,19 +63,24 @@ struct ExpRec {
 };
 
 // One send lane: a stream of messages one rank sends for one channel of one
-// collective membership (a queue pair in RDMA terms).
+// collective membership (a queue pair in RDMA terms).  The last row caches
+// what every packet of the current message needs: destination node and
+// rank, the destination's receive slot once its join has been seen, and the
+// sender's own receive-counter base.
 struct Lane {
     u32 node, member, chan, kind;
     u32 m, nmsg, pkts_left, dst_member;
     u32 dst_port, dep_base, dep_mask, dep_need;
-    u32 key, a2a_e, a2a_start, pad;
+    u32 key, a2a_e, a2a_start, dnode;
+    u32 drank, dslot, ok_dst, pbase;
 };
 
 struct RankCtl {
     u32 busy, rr, npend, nact;
     u64 lane_mask;
     u64 port_mask[2];
-    u64 pad;
+    u32 blocked;    // every send lane waits for a receive count (no scan needed)
+    u32 pad;
 };
 
 // Per-experiment control, kept across runs (resume) and read by mv_results.
@@ -110,6 +115,10 @@ struct Params {
         *member_a2a_in_n, *memb_col, *a2a_in_src;
     const u64 *a2a_bytes, *a2a_in_bytes, *mem;
     const u32 *node_rank;    // per node: its rank (workload-local)
+    const uint2 *sw_rec;     // per switch: (first port, ports)
+    const uint4 *port_rec;   // per switch port: (downstream queue, sigma, delta, owner of that
+                             //   queue: peer switch, or 0x80000000 | host)
+    const uint4 *host_rec;   // per host: (uplink queue, sigma, delta, switch of that queue)
     const u32 *order;        // experiments in the order blocks take them (largest first)
     // dynamic state
     u64 *q_push, *q_pop;     // per queue: (tick << 32) | counter of the last push / pop
@@ -145,17 +154,21 @@ __host__ __device__ inline u32 pk_key(uint4 p) { return p.w & 0xFFFFFFu; }
 __host__ __device__ inline u32 pk_last(uint4 p) { return (p.w >> 24) & 1u; }
 __host__ __device__ inline u32 pk_slot(uint4 p) { return p.w >> 25; }
 
-// Shared-memory image of one experiment's dynamic state: byte offsets of
-// each array (16-byte aligned), in this order.  The wake table comes first,
-// so an image cut after it holds the wake table alone.
+// Shared-memory image of one experiment: byte offsets of each array
+// (16-byte aligned), in this order.  The wake table comes first, so an
+// image cut after it holds the wake table alone.  The dynamic state
+// (IM_WAKE .. IM_SLOTS) is copied in and back out; the topology records and
+// routing tables after it are only copied in.
 enum : int { IM_WAKE, IM_QPUSH, IM_QPOP, IM_EG, IM_RK, IM_PRED, IM_CAND, IM_START, IM_END,
              IM_PBASE, IM_DONE, IM_OUT, IM_ACT, IM_PEND, IM_PORTS, IM_POPLOG, IM_LANES,
-             IM_SLOTS, IM_N };
+             IM_SLOTS, IM_NDYN, IM_SWREC = IM_NDYN, IM_PORTREC, IM_HOSTREC, IM_ROUTE, IM_UPN,
+             IM_UPLIST, IM_N };
 
 __host__ __device__ inline u64 im_round(u64 b) { return (b + 15) & ~15ull; }
 
-__host__ __device__ inline void image_bytes(const ExpRec &X, u32 plog, u32 n_eg, u64 *sz)
+__host__ __device__ inline void image_bytes(const ExpRec &X, const TopoRec &T, u64 *sz)
 {
+    const u32 plog = T.plog, n_eg = T.nq;
     sz[IM_WAKE] = 12ull * X.n_items;          // own wake + two poke words per item
     sz[IM_QPUSH] = 8ull * X.nq;
     sz[IM_QPOP] = 8ull * X.nq;
@@ -168,13 +181,19 @@ __host__ __device__ inline void image_bytes(const ExpRec &X, u32 plog, u32 n_eg,
     sz[IM_POPLOG] = 4ull * X.nq * plog;
     sz[IM_LANES] = sizeof(Lane) * (u64)X.nr * X.lane_cap;
     sz[IM_SLOTS] = 16ull * X.nq * X.cap;
+    sz[IM_SWREC] = 8ull * T.nsw;
+    sz[IM_PORTREC] = 16ull * T.nq;
+    sz[IM_HOSTREC] = 16ull * T.nh;
+    sz[IM_ROUTE] = (u64)T.nsw * T.nh;
+    sz[IM_UPN] = T.nsw;
+    sz[IM_UPLIST] = T.nq;
 }
 
 // offsets into the image; returns the total
-__host__ __device__ inline u64 image_layout(const ExpRec &X, u32 plog, u32 n_eg, u64 *off)
+__host__ __device__ inline u64 image_layout(const ExpRec &X, const TopoRec &T, u64 *off)
 {
     u64 sz[IM_N];
-    image_bytes(X, plog, n_eg, sz);
+    image_bytes(X, T, sz);
     u64 o = 0;
     for (int k = 0; k < IM_N; k++) {
         off[k] = o;

@@ -46,12 +46,6 @@ __device__ __forceinline__ u64 ld_vol64(const u64 *p) { return *reinterpret_cast
 __device__ __forceinline__ void st_vol64(u64 *p, u64 v) { *reinterpret_cast<volatile u64 *>(p) = v; }
 __device__ __forceinline__ u32 ld_vol32(const u32 *p) { return *reinterpret_cast<const volatile u32 *>(p); }
 __device__ __forceinline__ void st_vol32(u32 *p, u32 v) { *reinterpret_cast<volatile u32 *>(p) = v; }
-__device__ __forceinline__ i32 ld_acq32(const i32 *p)
-{
-    i32 v;
-    asm volatile("ld.acquire.cta.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ u64 globaltimer()
 {
     u64 t;
@@ -195,7 +189,60 @@ struct XV {
     u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
     i32 *nd_out;
     u32 *wake;
+    const uint2 *sw_rec;
+    const uint4 *port_rec, *host_rec;
+    const u8 *route, *up_n, *up_list;
 };
+
+// The fields the per-tick code reads, copied from the block's view into
+// registers at the start of each switch or rank-group step: stores through
+// the state pointers (shared or global) cannot alias registers, so the
+// compiler loads each field once.
+struct HV {
+    struct {
+        u32 algo, nc, pkt, cap, tick_ps, rec_cap, nr, nsw, lane_cap, port_cap, pend_cap, act_cap;
+        u64 chunk, dur_seed, ecmp_seed, rec_off;
+    } X;
+    struct { u32 nh, nq, rdv; } T;
+    struct { u32 node_off, edge_off, coll_off, memb_off, a2a_off, a2a_in_off; } W;
+    u32 plog;
+    u64 *q_push, *q_pop;
+    u32 *poplog;
+    uint4 *slots;
+    uint2 *eg;
+    RankCtl *rk;
+    uint2 *pend;
+    u32 *act;
+    Lane *lanes;
+    uint2 *ports;
+    u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
+    i32 *nd_out;
+    u32 *wake;
+    const uint2 *sw_rec;
+    const uint4 *port_rec, *host_rec;
+    const u8 *route, *up_n, *up_list;
+};
+
+__device__ __forceinline__ HV make_hv(const XV &S)
+{
+    HV V;
+    V.X.algo = S.X.algo; V.X.nc = S.X.nc; V.X.pkt = S.X.pkt; V.X.cap = S.X.cap;
+    V.X.tick_ps = S.X.tick_ps; V.X.rec_cap = S.X.rec_cap; V.X.nr = S.X.nr; V.X.nsw = S.X.nsw;
+    V.X.lane_cap = S.X.lane_cap; V.X.port_cap = S.X.port_cap; V.X.pend_cap = S.X.pend_cap;
+    V.X.act_cap = S.X.act_cap; V.X.chunk = S.X.chunk; V.X.dur_seed = S.X.dur_seed;
+    V.X.ecmp_seed = S.X.ecmp_seed; V.X.rec_off = S.X.rec_off;
+    V.T.nh = S.T.nh; V.T.nq = S.T.nq; V.T.rdv = S.T.rdv;
+    V.W.node_off = S.W.node_off; V.W.edge_off = S.W.edge_off; V.W.coll_off = S.W.coll_off;
+    V.W.memb_off = S.W.memb_off; V.W.a2a_off = S.W.a2a_off; V.W.a2a_in_off = S.W.a2a_in_off;
+    V.plog = S.plog;
+    V.q_push = S.q_push; V.q_pop = S.q_pop; V.poplog = S.poplog; V.slots = S.slots; V.eg = S.eg;
+    V.rk = S.rk; V.pend = S.pend; V.act = S.act; V.lanes = S.lanes; V.ports = S.ports;
+    V.nd_pred = S.nd_pred; V.nd_cand = S.nd_cand; V.nd_start = S.nd_start; V.nd_end = S.nd_end;
+    V.nd_pbase = S.nd_pbase; V.nd_done = S.nd_done; V.nd_out = S.nd_out; V.wake = S.wake;
+    V.sw_rec = S.sw_rec; V.port_rec = S.port_rec; V.host_rec = S.host_rec; V.route = S.route;
+    V.up_n = S.up_n; V.up_list = S.up_list;
+    return V;
+}
 
 // Per-experiment counters while a block holds it; only read after the last
 // tick.  Decisions taken every tick use the per-warp reports instead, which
@@ -204,6 +251,13 @@ struct Team {
     u32 end_max1, rec_count, now0, status0, left0, pad[3];
     unsigned long long pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
     uint4 rep[2][kMaxWarps];    // per warp: (next wake, nodes completed, failure key, abort)
+};
+
+// Per-warp counters, kept in registers for the whole run of an experiment
+// and added to the block's totals once at the end.
+struct Acc {
+    unsigned long long inj, hops, del, msg, dig;
+    u32 emax;
 };
 
 // Failure keys: the lowest key of a tick wins, so rank failures (in rank
@@ -223,7 +277,7 @@ struct SwSmem {
 // reaches the sender at x + D (D = delta + 1 of the link).  At most D - 1
 // pops can still be on their way, so the pop log is only read when the
 // queue is within D - 1 of full.
-__device__ __forceinline__ bool credit_ok(const XV &V, u32 qi, u32 tail, u32 H, u32 D, u32 t)
+__device__ __forceinline__ bool credit_ok(const HV &V, u32 qi, u32 tail, u32 H, u32 D, u32 t)
 {
     const u32 cap = V.X.cap;
     if (tail - H + D - 1 < cap) return true;
@@ -238,28 +292,32 @@ __device__ __forceinline__ bool credit_ok(const XV &V, u32 qi, u32 tail, u32 H, 
 }
 
 // ---------------------------------------------------------------- switches
-__device__ __forceinline__ u32 route_port(const Params &P, const XV &V, u32 gs, u32 s, uint4 pk)
+__device__ __forceinline__ u32 route_port(const HV &V, u32 s, u32 p0, uint4 pk)
 {
-    u8 r = P.route[V.T.route_off + (u64)s * V.T.nh + pk_dst(pk)];
+    u8 r = V.route[(u64)s * V.T.nh + pk_dst(pk)];
     if (r != 0xFF) return r;
-    u32 nup = P.up_n[gs];
+    u32 nup = V.up_n[s];
     if (nup == 0) return 0xFFu;
     u64 h = mix64((u64)pk_key(pk) ^ ((u64)s << 40) ^ V.X.ecmp_seed);
-    return P.up_list[V.T.port_off + P.sw_pstart[gs] + (u32)(h % nup)];
+    return V.up_list[p0 + (u32)(h % nup)];
 }
 
 // Forwarding at switch s for one tick (Multiverse section 4.2): each lane
 // plans its ingress ports (the egress their ready head packet needs), then
 // each lane pulls for its egress ports: free link, credit downstream, first
-// planned ingress at or after the round-robin pointer.  Returns the earliest
-// tick this warp knows of at which something may happen (its own next wake
-// and the wakes it gave other items); *fail gets a failure key.
-__device__ u32 switch_tick(const Params &P, const XV &V, Team &TC, u32 s, u32 t, u32 old,
-                           u32 *poke, SwSmem *sm, u32 *fail)
+// planned ingress at or after the round-robin pointer.  `old` is the
+// switch's pending wake; pokes for other items go to `poke`.  Returns the
+// earliest tick this warp knows of at which something may happen (its own
+// next wake and the wakes it gave other items); *fail gets a failure key.
+__device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t, u32 old,
+                                           u32 *poke, SwSmem *sm, u32 *fail)
 {
+    // a register copy of the view: stores through the state pointers cannot
+    // alias it, so its fields are loaded once per tick
+    const HV V = make_hv(Vs);
     const u32 lane = threadIdx.x & 31;
-    const u32 gs = V.T.sw_off + s;
-    const u32 np = P.sw_nports[gs], p0 = P.sw_pstart[gs];
+    const uint2 sr = V.sw_rec[s];
+    const u32 p0 = sr.x, np = sr.y;
     const u32 cap = V.X.cap, pm = V.plog - 1;
     u32 nxt = kUnset;                   // own next wake
     u32 pk_min = kUnset;                // earliest tick poked into a downstream item
@@ -281,7 +339,7 @@ __device__ u32 switch_tick(const Params &P, const XV &V, Team &TC, u32 s, u32 t,
         uint4 pk = V.slots[(u64)qi * cap + head % cap];
         if (pk.x > t) { nxt = min(nxt, pk.x); continue; }
         ready_any = true;
-        u32 tg = route_port(P, V, gs, s, pk);
+        u32 tg = route_port(V, s, p0, pk);
         if (tg >= np) { bad = true; continue; }
         sm->pkt[p] = pk;
         atomicOr(&sm->mask[tg], 1ull << p);
@@ -298,25 +356,23 @@ __device__ u32 switch_tick(const Params &P, const XV &V, Team &TC, u32 s, u32 t,
         u32 qe = p0 + eg;
         uint2 st = V.eg[qe];
         if (st.x > t) continue;             // busy: its heads wake the switch at t+1
-        i32 pe = P.port_peer[V.T.port_off + qe];
-        u32 dq = pe >= 0 ? (u32)pe : V.T.nq + (u32)(-pe - 1);
+        const uint4 pr = V.port_rec[qe];    // downstream queue, sigma, delta, its owner
+        const u32 dq = pr.x, sg = pr.y, dl = pr.z;
         u64 dpop = ld_vol64(&V.q_pop[dq]);
         u32 dhead = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
         u32 dtail = (u32)V.q_push[dq];
-        u32 dl = P.port_delta[V.T.port_off + qe];
         if (!credit_ok(V, dq, dtail, dhead, dl + 1, t)) continue;
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
         uint4 pk = sm->pkt[i];
-        u32 sg = P.port_sigma[V.T.port_off + qe];
         pk.x = t + sg + dl;
         pk.y += (dl + 1) << 16;
         V.slots[(u64)dq * cap + dtail % cap] = pk;
         st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
         V.eg[qe] = make_uint2(t + sg, (i + 1) % np);
         // the queue's owner: the peer switch, or the rank group of the host
-        if (pe >= 0) atomicMin(&poke[P.port_sw[V.T.port_off + pe]], pk.x);
-        else if ((u32)(-pe - 1) < V.X.nr) atomicMin(&poke[V.X.nsw + (u32)(-pe - 1) / 32], pk.x);
+        if (!(pr.w & 0x80000000u)) atomicMin(&poke[pr.w], pk.x);
+        else if ((pr.w & 0x7FFFFFFFu) < V.X.nr) atomicMin(&poke[V.X.nsw + (pr.w & 0x7FFFFFFFu) / 32], pk.x);
         pk_min = min(pk_min, pk.x);
         popped |= 1ull << i;
         hops++;
@@ -333,17 +389,13 @@ __device__ u32 switch_tick(const Params &P, const XV &V, Team &TC, u32 s, u32 t,
             st_vol64(&V.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
         }
     }
-    hops = __reduce_add_sync(kFull, hops);
-    nxt = __reduce_min_sync(kFull, nxt);
+    if (all) hops = __reduce_add_sync(kFull, hops);
+    nxt = __reduce_min_sync(kFull, ready_any ? t + 1 : nxt);   // heads left or blocked: next tick
     pk_min = __reduce_min_sync(kFull, pk_min);
-    bool anybad = __any_sync(kFull, bad);
-    if (__any_sync(kFull, ready_any)) nxt = t + 1;   // heads left or blocked
+    if (__any_sync(kFull, bad)) *fail = min(*fail, kFailSwitch);
     u32 w = min(nxt, old > t ? old : kUnset);
-    if (lane == 0) {
-        V.wake[s] = w;
-        if (all) atomicAdd(&TC.pkt_hops, (unsigned long long)hops);
-    }
-    if (anybad) *fail = min(*fail, kFailSwitch);
+    if (lane == 0) V.wake[s] = w;
+    if (all) acc.hops += hops;
     __syncwarp();
     return min(w, pk_min);
 }
@@ -358,6 +410,7 @@ __device__ __forceinline__ RankCtl load_ctl(const RankCtl *p)
     r.lane_mask = ((u64)b.y << 32) | b.x;
     r.port_mask[0] = ((u64)b.w << 32) | b.z;
     r.port_mask[1] = ((u64)c.y << 32) | c.x;
+    r.blocked = c.z;
     r.pad = 0;
     return r;
 }
@@ -367,27 +420,28 @@ __device__ __forceinline__ void store_ctl(RankCtl *p, const RankCtl &r)
     q[0] = make_uint4(r.busy, r.rr, r.npend, r.nact);
     q[1] = make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_mask[0],
                       (u32)(r.port_mask[0] >> 32));
-    q[2] = make_uint4((u32)r.port_mask[1], (u32)(r.port_mask[1] >> 32), 0, 0);
+    q[2] = make_uint4((u32)r.port_mask[1], (u32)(r.port_mask[1] >> 32), r.blocked, 0);
 }
+static_assert(sizeof(Lane) == 80, "Lane is five 16-byte words");
 __device__ __forceinline__ Lane load_lane(const Lane *p)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
     Lane L;
     uint4 *d = reinterpret_cast<uint4 *>(&L);
-    d[0] = q[0]; d[1] = q[1]; d[2] = q[2]; d[3] = q[3];
+    d[0] = q[0]; d[1] = q[1]; d[2] = q[2]; d[3] = q[3]; d[4] = q[4];
     return L;
 }
 __device__ __forceinline__ void store_lane(Lane *p, const Lane &L)
 {
     uint4 *q = reinterpret_cast<uint4 *>(p);
     const uint4 *s = reinterpret_cast<const uint4 *>(&L);
-    q[0] = s[0]; q[1] = s[1]; q[2] = s[2]; q[3] = s[3];
+    q[0] = s[0]; q[1] = s[1]; q[2] = s[2]; q[3] = s[3]; q[4] = s[4];
 }
 
 // Per-rank view used while processing one tick.
 struct RankView {
     const Params *P;
-    const XV *V;
+    HV V;
     Team *TC;
     u32 *poke;          // this step's poke words of the experiment's items
     u32 r, t;
@@ -399,8 +453,8 @@ struct RankView {
     u64 dig;
 };
 
-__device__ __forceinline__ const WorkRec &W_(const RankView &v) { return v.V->W; }
-__device__ __forceinline__ const ExpRec &X_(const RankView &v) { return v.V->X; }
+__device__ __forceinline__ const auto &W_(const RankView &v) { return v.V.W; }
+__device__ __forceinline__ const auto &X_(const RankView &v) { return v.V.X; }
 __device__ __forceinline__ u32 coll_of(const RankView &v, u32 u) { return v.P->node_arg[W_(v).node_off + u]; }
 __device__ __forceinline__ u32 nmemb(const RankView &v, u32 c) { return v.P->coll_nmembers[W_(v).coll_off + c]; }
 __device__ __forceinline__ u32 ckind(const RankView &v, u32 c) { return v.P->coll_kind[W_(v).coll_off + c]; }
@@ -439,7 +493,7 @@ __device__ __forceinline__ u64 ring_loops(const RankView &v, u32 c, u64 Pc)
 {
     return Pc == 0 ? 1 : cdiv(Pc, (u64)nmemb(v, c) * X_(v).chunk);
 }
-__device__ u64 a2a_row_chunks(const RankView &v, u32 c, u32 i)
+__device__ __forceinline__ u64 a2a_row_chunks(const RankView &v, u32 c, u32 i)
 {
     u32 m = mabs(v, c, i);
     u32 b = W_(v).a2a_off + v.P->memb_row[m], n = v.P->member_a2a_n[m];
@@ -448,7 +502,7 @@ __device__ u64 a2a_row_chunks(const RankView &v, u32 c, u32 i)
     return tot;
 }
 
-__device__ u32 lane_count(const RankView &v, u32 c, u32 i, u32 ch, u32 kind)
+__device__ __forceinline__ u32 lane_count(const RankView &v, u32 c, u32 i, u32 ch, u32 kind)
 {
     u32 N = nmemb(v, c);
     u64 S = cbytes(v, c);
@@ -472,7 +526,7 @@ __device__ u32 lane_count(const RankView &v, u32 c, u32 i, u32 ch, u32 kind)
     return 0;
 }
 
-__device__ u32 port_count_expect(const RankView &v, u32 c, u32 i, u32 p)
+__device__ __forceinline__ u32 port_count_expect(const RankView &v, u32 c, u32 i, u32 p)
 {
     u32 N = nmemb(v, c);
     u64 S = cbytes(v, c);
@@ -502,7 +556,7 @@ __device__ u32 port_count_expect(const RankView &v, u32 c, u32 i, u32 p)
 
 // Message L.m of a lane: bytes, destination member and port, and the own
 // receive counts it waits for.  Returns its packet count.
-__device__ u32 lane_setup(const RankView &v, Lane &L)
+__device__ __forceinline__ u32 lane_setup(const RankView &v, Lane &L)
 {
     u32 c = coll_of(v, L.node), N = nmemb(v, c), i = L.member, m = L.m, ch = L.chan;
     u64 S = cbytes(v, c), C = X_(v).chunk, bytes = 0;
@@ -569,13 +623,18 @@ __device__ u32 lane_setup(const RankView &v, Lane &L)
         break;
     }
     }
-    u32 drank = mrank(v, c, L.dst_member);
+    const u32 drank = mrank(v, c, L.dst_member), dnode = mnode(v, c, L.dst_member);
     L.key = (u32)(mix64((u64)L.node | ((u64)(ch * 4 + L.kind) << 32) | ((u64)drank << 44)) &
                   0xFFFFFFu);
+    if (dnode != L.dnode) {          // a new destination: its join is yet to be seen
+        L.dnode = dnode;
+        L.drank = drank;
+        L.ok_dst = 0;
+    }
     return (u32)(bytes == 0 ? 1 : cdiv(bytes, X_(v).pkt));
 }
 
-__device__ u32 compute_ticks(const RankView &v, u32 u)
+__device__ __forceinline__ u32 compute_ticks(const RankView &v, u32 u)
 {
     const Params &P = *v.P;
     const u32 g = W_(v).node_off + u;
@@ -585,7 +644,7 @@ __device__ u32 compute_ticks(const RankView &v, u32 u)
 }
 
 // alpha + bytes/beta (Multiverse section 4.1), beta as ticks per byte
-__device__ u32 intra_ticks(const RankView &v, u32 c)
+__device__ __forceinline__ u32 intra_ticks(const RankView &v, u32 c)
 {
     const Params &P = *v.P;
     u32 cc = W_(v).coll_off + c;
@@ -598,7 +657,7 @@ __device__ u32 intra_ticks(const RankView &v, u32 c)
     return P.coll_alpha[cc] + (u32)cdiv(be * P.coll_beta_num[cc], P.coll_beta_den[cc]);
 }
 
-__device__ __forceinline__ u32 rank_item(const XV &V, u32 r) { return V.X.nsw + r / 32; }
+__device__ __forceinline__ u32 rank_item(const HV &V, u32 r) { return V.X.nsw + r / 32; }
 
 __device__ __forceinline__ void rank_poke(RankView &v, u32 item, u32 at)
 {
@@ -609,26 +668,36 @@ __device__ __forceinline__ void rank_poke(RankView &v, u32 item, u32 at)
 // A member joined collective c at this tick: members waiting on its start
 // look again when the join reaches them (intra-server barrier: next tick;
 // network rendezvous: 1 + min(delta) ticks later).
-__device__ void poke_members(RankView &v, u32 c, u32 at)
+__device__ __forceinline__ void poke_members(RankView &v, u32 c, u32 at)
 {
     u32 N = nmemb(v, c), last = kUnset;
     for (u32 m = 0; m < N; m++) {
-        u32 g = rank_item(*v.V, mrank(v, c, m));
+        u32 g = rank_item(v.V, mrank(v, c, m));
         if (g != last) rank_poke(v, g, at);
         last = g;
     }
 }
 
-__device__ void pend_add(RankView &v, u32 u, u32 st)
+// The pending list is kept sorted by (start tick, node): the nodes due at a
+// tick are its prefix, already in node order.
+__device__ __forceinline__ void pend_add(RankView &v, u32 u, u32 st)
 {
     if (v.C.npend >= X_(v).pend_cap) { v.fail_over = true; return; }
-    v.V->pend[(u64)v.r * X_(v).pend_cap + v.C.npend++] = make_uint2(u, st);
+    uint2 *pd = v.V.pend + (u64)v.r * X_(v).pend_cap;
+    u32 j = v.C.npend++;
+    while (j > 0) {
+        const uint2 x = pd[j - 1];
+        if (x.y < st || (x.y == st && x.x < u)) break;
+        pd[j] = x;
+        j--;
+    }
+    pd[j] = make_uint2(u, st);
 }
 
-__device__ void complete_node(RankView &v, u32 u, u32 c)
+__device__ __forceinline__ void complete_node(RankView &v, u32 u, u32 c)
 {
     const Params &P = *v.P;
-    const XV &V = *v.V;
+    const HV &V = v.V;
     V.nd_end[u] = c;
     v.n_done++;
     v.end_max1 = max(v.end_max1, c + 1);
@@ -645,18 +714,18 @@ __device__ void complete_node(RankView &v, u32 u, u32 c)
     }
 }
 
-__device__ void free_ports(RankView &v, u32 u)
+__device__ __forceinline__ void free_ports(RankView &v, u32 u)
 {
-    u32 np = nports_of(v, coll_of(v, u)), b = v.V->nd_pbase[u];
+    u32 np = nports_of(v, coll_of(v, u)), b = v.V.nd_pbase[u];
     for (u32 p = b; p < b + np; p++) v.C.port_mask[p >> 6] &= ~(1ull << (p & 63));
 }
 
 // A rank joins a network collective: receive counters, then send lanes.
-__device__ bool net_join(RankView &v, u32 u)
+__device__ __forceinline__ bool net_join(RankView &v, u32 u)
 {
     const Params &P = *v.P;
-    const XV &V = *v.V;
-    const ExpRec &X = V.X;
+    const HV &V = v.V;
+    const auto &X = V.X;
     u32 c = coll_of(v, u), i = P.node_member[W_(v).node_off + u];
     u32 np = nports_of(v, c);
     i32 base = -1;
@@ -687,9 +756,12 @@ __device__ bool net_join(RankView &v, u32 u)
             Lane L = {};
             L.node = u; L.member = i; L.chan = ch; L.kind = kd;
             L.m = 0; L.nmsg = nm;
+            L.dnode = kUnset;
+            L.pbase = (u32)base;
             L.pkts_left = lane_setup(v, L);
             store_lane(&lanes[slot], L);
             v.C.lane_mask |= 1ull << slot;
+            v.C.blocked = 0;
             out += (i32)nm;
         }
     }
@@ -699,30 +771,38 @@ __device__ bool net_join(RankView &v, u32 u)
     return true;
 }
 
-__device__ void act_add(RankView &v, u32 u)
+// Running memberships in ascending node order; bit 31 marks an intra-server
+// (analytic) one.
+constexpr u32 kActIntra = 0x80000000u;
+__device__ __forceinline__ void act_add(RankView &v, u32 u, u32 flag)
 {
     if (v.C.nact >= X_(v).act_cap) { v.fail_over = true; return; }
-    u32 *a = v.V->act + (u64)v.r * X_(v).act_cap;
-    u32 j = v.C.nact;                       // keep ascending node order
-    while (j > 0 && a[j - 1] > u) { a[j] = a[j - 1]; j--; }
-    a[j] = u;
+    u32 *a = v.V.act + (u64)v.r * X_(v).act_cap;
+    u32 j = v.C.nact;
+    while (j > 0 && (a[j - 1] & ~kActIntra) > u) { a[j] = a[j - 1]; j--; }
+    a[j] = u | flag;
     v.C.nact++;
 }
 
 // Schedule + AnalyticalSys: finish running memberships, then start the nodes
 // scheduled for this tick (both in node order).
-__device__ void dag_step(RankView &v)
+__device__ __forceinline__ void dag_step(RankView &v)
 {
-    const Params &P = *v.P;
-    const XV &V = *v.V;
+    const HV &V = v.V;
     const u32 t = v.t;
+    uint2 *pd = V.pend + (u64)v.r * V.X.pend_cap;
+    if (v.C.nact == 0 && (v.C.npend == 0 || pd[0].y > t)) {      // nothing running or due
+        if (v.C.npend) v.nxt = min(v.nxt, pd[0].y);
+        return;
+    }
     u32 *a = V.act + (u64)v.r * V.X.act_cap;
     u32 w = 0;
     for (u32 j = 0; j < v.C.nact; j++) {
-        u32 u = a[j], c = coll_of(v, u);
+        const u32 e = a[j], u = e & ~kActIntra;
         bool fin = false;
-        if (P.node_kind[W_(v).node_off + u] == NODE_INTRA) {
-            u32 N = nmemb(v, c), b = 0;
+        if (e & kActIntra) {
+            const u32 c = coll_of(v, u), N = nmemb(v, c);
+            u32 b = 0;
             bool ok = true;
             for (u32 m = 0; m < N && ok; m++) {
                 u32 st = ld_vol32(&V.nd_start[mnode(v, c, m)]);
@@ -730,78 +810,70 @@ __device__ void dag_step(RankView &v)
                 else b = max(b, st);
             }
             if (ok) { complete_node(v, u, b + intra_ticks(v, c)); fin = true; }
-        } else {
-            if (ld_acq32(&V.nd_out[u]) == 0) {
-                u32 done = ld_vol32(&V.nd_done[u]);
-                free_ports(v, u);
-                complete_node(v, u, done);
-                fin = true;
-            }
+        } else if (ld_vol32((const u32 *)&V.nd_out[u]) == 0) {
+            __threadfence_block();         // the count reached 0: read the latest event after it
+            u32 done = ld_vol32(&V.nd_done[u]);
+            free_ports(v, u);
+            complete_node(v, u, done);
+            fin = true;
         }
-        if (!fin) a[w++] = u;
+        if (!fin) a[w++] = e;
     }
     v.C.nact = w;
-    // start scheduled nodes: take those due now out of the pending list
-    uint2 *pd = V.pend + (u64)v.r * V.X.pend_cap;
-    u32 due[kNPend];
-    u32 nd = 0, keep = 0;
-    for (u32 j = 0; j < v.C.npend; j++) {
-        uint2 x = pd[j];
-        if (x.y < t) { v.fail_err = true; continue; }
-        if (x.y == t) due[nd++] = x.x;
-        else { pd[keep++] = x; v.nxt = min(v.nxt, x.y); }
-    }
-    v.C.npend = keep;
-    for (u32 j = 1; j < nd; j++) {           // insertion sort, node order
-        u32 x = due[j], q = j;
-        while (q > 0 && due[q - 1] > x) { due[q] = due[q - 1]; q--; }
-        due[q] = x;
-    }
-    for (u32 j = 0; j < nd; j++) {
-        u32 u = due[j];
+    // start the nodes due now: the prefix of the sorted pending list (a
+    // start tick already past is an inconsistent schedule)
+    u32 lo = 0;
+    while (lo < v.C.npend && pd[lo].y < t) lo++;
+    if (lo) { v.fail_err = true; return; }
+    u32 hi = lo;
+    while (hi < v.C.npend && pd[hi].y == t) hi++;
+    for (u32 j = lo; j < hi && !v.fail_over; j++) {
+        const u32 u = pd[j].x;
         v.changed = true;
-        u32 kind = P.node_kind[W_(v).node_off + u];
+        const u32 kind = v.P->node_kind[W_(v).node_off + u];
         if (kind == NODE_COMPUTE) {
             st_vol32(&V.nd_start[u], t);
-            complete_node(v, u, t + compute_ticks(v, u));
+            complete_node(v, u, t + compute_ticks(v, u));   // successors start later: after hi
         } else if (kind == NODE_INTRA) {
             st_vol32(&V.nd_start[u], t);
-            act_add(v, u);
+            act_add(v, u, kActIntra);
             poke_members(v, coll_of(v, u), t + 1);
         } else {
-            if (!net_join(v, u)) return;
+            if (!net_join(v, u)) break;
             st_vol32(&V.nd_start[u], t);
             poke_members(v, coll_of(v, u), t + V.T.rdv);
-            if (ld_acq32(&V.nd_out[u]) == 0) {
+            if (ld_vol32((const u32 *)&V.nd_out[u]) == 0) {
                 free_ports(v, u);
                 complete_node(v, u, t);
             } else {
-                act_add(v, u);
+                act_add(v, u, 0);
             }
         }
-        if (v.fail_over || v.fail_err) return;
     }
-    // nodes scheduled by completions above may start later; note the earliest
-    for (u32 j = 0; j < v.C.npend; j++) v.nxt = min(v.nxt, pd[j].y);
+    if (v.fail_over || v.fail_err) return;
+    // drop the started prefix; nodes scheduled above start later
+    const u32 n = v.C.npend;
+    for (u32 j = hi; j < n; j++) pd[j - hi] = pd[j];
+    v.C.npend = n - hi;
+    if (v.C.npend) v.nxt = min(v.nxt, pd[0].y);
 }
 
 // SendSys + NICSndSys: one packet per uplink serialisation time, round-robin
 // over the send lanes from the pointer; a lane is eligible once its receive
 // dependencies are met and its destination joined before this tick.
-__device__ void inject(RankView &v)
+__device__ __forceinline__ void inject(RankView &v)
 {
-    const Params &P = *v.P;
-    const XV &V = *v.V;
-    const ExpRec &X = V.X;
-    const TopoRec &T = V.T;
+    const HV &V = v.V;
+    const auto &X = V.X;
     const u32 t = v.t;
-    if (!v.C.lane_mask) return;
+    if (!v.C.lane_mask || v.C.blocked) return;
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
-    u32 qp = P.host_port[T.host_off + v.r];
+    const uint4 hr = V.host_rec[v.r];       // uplink queue, sigma, delta, its switch
+    const u32 qp = hr.x, hs = hr.y, hd = hr.z;
     u64 pw = ld_vol64(&V.q_pop[qp]);
     u32 head = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
     u32 tail = (u32)V.q_push[qp];
-    if (!credit_ok(V, qp, tail, head, P.host_delta[T.host_off + v.r] + 1, t)) {
+    if (!credit_ok(V, qp, tail, head, hd + 1, t)) {
         v.nxt = min(v.nxt, t + 1);
         return;
     }
@@ -810,40 +882,44 @@ __device__ void inject(RankView &v)
     u64 lo = M & ~hi;
     Lane *lanes = V.lanes + (u64)v.r * X.lane_cap;
     const uint2 *ports = V.ports + (u64)v.r * X.port_cap;
+    bool timed = false;                 // some lane waits for a destination's join
     for (int pass = 0; pass < 2; pass++) {
         u64 m = pass == 0 ? hi : lo;
         while (m) {
             u32 l = (u32)__ffsll((long long)m) - 1;
             m &= m - 1;
             Lane L = load_lane(&lanes[l]);
-            u32 pb = V.nd_pbase[L.node];
             bool ok = true;
             for (u32 b = 0; b < 3 && ok; b++)
                 if ((L.dep_mask >> b) & 1u)
-                    if (ports[pb + L.dep_base + b].x < L.dep_need) ok = false;
+                    if (ports[L.pbase + L.dep_base + b].x < L.dep_need) ok = false;
             if (!ok) continue;
-            u32 c = coll_of(v, L.node);
-            u32 dn = mnode(v, c, L.dst_member);
-            u32 dst_start = ld_vol32(&V.nd_start[dn]);
-            // the destination's join reaches this rank 1 + min(delta) ticks
-            // later; when that time is known, it is this rank's own wake (a
-            // poke alone could be shadowed by an earlier pending wake)
-            if (dst_start == kUnset) continue;
-            if (dst_start + T.rdv > t) { v.nxt = min(v.nxt, dst_start + T.rdv); continue; }
-            u32 dpb = ld_vol32(&V.nd_pbase[dn]);
-            u32 hs = P.host_sigma[T.host_off + v.r], hd = P.host_delta[T.host_off + v.r];
+            if (!L.ok_dst) {
+                // the destination's join reaches this rank 1 + min(delta) ticks
+                // later; when that time is known, it is this rank's own wake (a
+                // poke alone could be shadowed by an earlier pending wake)
+                const u32 dst_start = ld_vol32(&V.nd_start[L.dnode]);
+                if (dst_start == kUnset) { timed = true; continue; }
+                if (dst_start + V.T.rdv > t) {
+                    v.nxt = min(v.nxt, dst_start + V.T.rdv);
+                    timed = true;
+                    continue;
+                }
+                L.dslot = ld_vol32(&V.nd_pbase[L.dnode]) + L.dst_port;
+                L.ok_dst = 1;
+            }
             uint4 pk;
             pk.x = t + hs + hd;
-            pk.y = mrank(v, c, L.dst_member) | ((hd + 1) << 16);
+            pk.y = L.drank | ((hd + 1) << 16);
             pk.z = L.node;
-            pk.w = L.key | ((L.pkts_left == 1 ? 1u : 0u) << 24) | ((dpb + L.dst_port) << 25);
+            pk.w = L.key | ((L.pkts_left == 1 ? 1u : 0u) << 24) | (L.dslot << 25);
             V.slots[(u64)qp * X.cap + tail % X.cap] = pk;
             st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
             v.C.busy = t + hs;
             v.C.rr = (l + 1) % kNLane;
             v.n_inj++;
             v.changed = true;
-            rank_poke(v, P.port_sw[T.port_off + qp], pk.x);
+            rank_poke(v, hr.w, pk.x);
             if (--L.pkts_left == 0) {
                 if (++L.m == L.nmsg) v.C.lane_mask &= ~(1ull << l);
                 else L.pkts_left = lane_setup(v, L);
@@ -853,16 +929,19 @@ __device__ void inject(RankView &v)
             return;
         }
     }
+    // every lane waits for receive counts: nothing changes that but a
+    // message completing at this rank (receive) or a new lane (join)
+    if (!timed) v.C.blocked = 1;
 }
 
 // NICRcvSys + ACKSys: take the ready head of the downlink queue; the last
 // packet of a message completes it at this rank and acknowledges it to the
 // sender, sum over hops of (delta + 1) ticks later.
-__device__ void receive(RankView &v)
+__device__ __forceinline__ void receive(RankView &v)
 {
     const Params &P = *v.P;
-    const XV &V = *v.V;
-    const ExpRec &X = V.X;
+    const HV &V = v.V;
+    const auto &X = V.X;
     const u32 t = v.t;
     u32 ql = V.T.nq + v.r;
     u64 pw = ld_vol64(&V.q_push[ql]);
@@ -884,6 +963,7 @@ __device__ void receive(RankView &v)
     uint2 port = ports[ps];
     port.x++;
     ports[ps] = port;
+    v.C.blocked = 0;
     u32 own = port.y, snd = pk.z;
     atomicMax(&V.nd_done[own], t);
     __threadfence_block();
@@ -901,16 +981,18 @@ __device__ void receive(RankView &v)
     }
 }
 
-// Ranks g*32 .. g*32+31 for one tick, one lane each.  Returns the warp's
+// Ranks g*32 .. g*32+31 for one tick, one lane each.  `old` is the group's
+// pending wake; pokes for other items go to `poke`.  Returns the warp's
 // earliest known next event; *done / *fail receive nodes completed and the
 // failure key.
-__device__ __noinline__ u32 rank_tick(const Params &P, const XV &V, Team &TC, u32 g, u32 t,
-                                      u32 old, u32 *poke, u32 *done_out, u32 *fail)
+__device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC, Acc &acc, u32 g,
+                                         u32 t, u32 old, u32 *poke, u32 *done_out, u32 *fail)
 {
     const u32 lane = threadIdx.x & 31;
-    const u32 it = V.X.nsw + g;
     RankView v;
-    v.P = &P; v.V = &V; v.TC = &TC; v.poke = poke;
+    v.P = &P; v.V = make_hv(Vs); v.TC = &TC; v.poke = poke;    // register copy (see switch_tick)
+    const HV &V = v.V;
+    const u32 it = V.X.nsw + g;
     v.r = g * 32 + lane; v.t = t;
     v.changed = v.fail_over = v.fail_err = false;
     v.nxt = kUnset;
@@ -926,50 +1008,56 @@ __device__ __noinline__ u32 rank_tick(const Params &P, const XV &V, Team &TC, u3
         }
         store_ctl(&V.rk[v.r], v.C);
     }
-    u32 nxt = __reduce_min_sync(kFull, v.nxt);
-    u32 pkm = __reduce_min_sync(kFull, v.pk_min);
-    u32 inj = __reduce_add_sync(kFull, v.n_inj);
-    u32 del = __reduce_add_sync(kFull, v.n_del);
-    u32 msg = __reduce_add_sync(kFull, v.n_msg);
-    u32 done = __reduce_add_sync(kFull, v.n_done);
-    u32 emax = __reduce_max_sync(kFull, v.end_max1);
-    u32 fk = v.fail_over ? fail_key_rank(v.r, EXP_OVERFLOW)
-           : v.fail_err ? fail_key_rank(v.r, EXP_ERROR) : kUnset;
-    fk = __reduce_min_sync(kFull, fk);
-    // 64-bit digest sum across the warp
-    u64 dig = v.dig;
-    for (int o = 16; o > 0; o >>= 1) dig += __shfl_xor_sync(kFull, dig, o);
-    u32 w = min(nxt, old > t ? old : kUnset);
-    if (lane == 0) {
-        V.wake[it] = w;
-        if (inj) {
-            atomicAdd(&TC.pkts_injected, (unsigned long long)inj);
-            atomicAdd(&TC.pkt_hops, (unsigned long long)inj);
-        }
-        if (del) atomicAdd(&TC.pkts_delivered, (unsigned long long)del);
-        if (msg) {
-            atomicAdd(&TC.msgs_delivered, (unsigned long long)msg);
-            atomicAdd(&TC.digest, (unsigned long long)dig);
-        }
-        if (emax) atomicMax(&TC.end_max1, emax);
+    // one packed sum for the per-lane 0/1 counts (each at most 32 a warp)
+    const u32 cnt = __reduce_add_sync(kFull, v.n_inj | (v.n_del << 8) | (v.n_msg << 16));
+    const u32 inj = cnt & 0xFF, del = (cnt >> 8) & 0xFF, msg = cnt >> 16;
+    const u32 nxt = __reduce_min_sync(kFull, v.nxt);
+    const u32 pkm = __reduce_min_sync(kFull, v.pk_min);
+    u32 done = 0, emax = 0;
+    if (__any_sync(kFull, v.n_done != 0)) {
+        done = __reduce_add_sync(kFull, v.n_done);
+        emax = __reduce_max_sync(kFull, v.end_max1);
     }
+    if (__any_sync(kFull, v.fail_over || v.fail_err)) {
+        u32 fk = v.fail_over ? fail_key_rank(v.r, EXP_OVERFLOW)
+               : v.fail_err ? fail_key_rank(v.r, EXP_ERROR) : kUnset;
+        *fail = min(*fail, __reduce_min_sync(kFull, fk));
+    }
+    u64 dig = 0;
+    if (msg) {                              // 64-bit digest sum across the warp
+        dig = v.dig;
+        for (int o = 16; o > 0; o >>= 1) dig += __shfl_xor_sync(kFull, dig, o);
+    }
+    u32 w = min(nxt, old > t ? old : kUnset);
+    if (lane == 0) V.wake[it] = w;
+    acc.inj += inj;
+    acc.hops += inj;
+    acc.del += del;
+    acc.msg += msg;
+    acc.dig += dig;
+    acc.emax = max(acc.emax, emax);
     *done_out += done;
-    *fail = min(*fail, fk);
     return min(w, pkm);
 }
 
 // ---------------------------------------------------------------- megakernel
-// Copy n bytes (a multiple of 4) between an experiment's global slice and
-// its shared-memory image, all threads of the block.
+// Copy n bytes between an experiment's global slice and its shared-memory
+// image, all threads of the block (word copies when both sides allow).
 __device__ __forceinline__ void block_copy(void *dst, const void *src, u64 n)
 {
-    u32 *d = reinterpret_cast<u32 *>(dst);
-    const u32 *s = reinterpret_cast<const u32 *>(src);
-    for (u64 i = threadIdx.x; i < n / 4; i += blockDim.x) d[i] = s[i];
+    if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | n) & 3) == 0) {
+        u32 *d = reinterpret_cast<u32 *>(dst);
+        const u32 *s = reinterpret_cast<const u32 *>(src);
+        for (u64 i = threadIdx.x; i < n / 4; i += blockDim.x) d[i] = s[i];
+    } else {
+        u8 *d = reinterpret_cast<u8 *>(dst);
+        const u8 *s = reinterpret_cast<const u8 *>(src);
+        for (u64 i = threadIdx.x; i < n; i += blockDim.x) d[i] = s[i];
+    }
 }
 
 // Global slice of array k of experiment X (k in the image order).
-__device__ void *global_slice(const Params &P, const ExpRec &X, int k)
+__device__ const void *global_slice(const Params &P, const ExpRec &X, const TopoRec &T, int k)
 {
     switch (k) {
     case IM_WAKE: return P.wake + 3ull * X.item_off;
@@ -989,12 +1077,19 @@ __device__ void *global_slice(const Params &P, const ExpRec &X, int k)
     case IM_PORTS: return P.ports + X.portc_off;
     case IM_POPLOG: return P.poplog + X.plog_off;
     case IM_LANES: return P.lanes + X.lane_off;
-    default: return P.slots + X.slot_off;
+    case IM_SLOTS: return P.slots + X.slot_off;
+    case IM_SWREC: return P.sw_rec + T.sw_off;
+    case IM_PORTREC: return P.port_rec + T.port_off;
+    case IM_HOSTREC: return P.host_rec + T.host_off;
+    case IM_ROUTE: return P.route + T.route_off;
+    case IM_UPN: return P.up_n + T.sw_off;
+    default: return P.up_list + T.port_off;
     }
 }
 
-__device__ void set_slice(XV &V, int k, void *p)
+__device__ void set_slice(XV &V, int k, const void *c)
 {
+    void *p = const_cast<void *>(c);
     switch (k) {
     case IM_WAKE: V.wake = (u32 *)p; break;
     case IM_QPUSH: V.q_push = (u64 *)p; break;
@@ -1013,7 +1108,13 @@ __device__ void set_slice(XV &V, int k, void *p)
     case IM_PORTS: V.ports = (uint2 *)p; break;
     case IM_POPLOG: V.poplog = (u32 *)p; break;
     case IM_LANES: V.lanes = (Lane *)p; break;
-    default: V.slots = (uint4 *)p; break;
+    case IM_SLOTS: V.slots = (uint4 *)p; break;
+    case IM_SWREC: V.sw_rec = (const uint2 *)p; break;
+    case IM_PORTREC: V.port_rec = (const uint4 *)p; break;
+    case IM_HOSTREC: V.host_rec = (const uint4 *)p; break;
+    case IM_ROUTE: V.route = (const u8 *)p; break;
+    case IM_UPN: V.up_n = (const u8 *)p; break;
+    default: V.up_list = (const u8 *)p; break;
     }
 }
 
@@ -1048,19 +1149,20 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         TC.pkts_delivered = c.pkts_delivered;
         TC.msgs_delivered = c.msgs_delivered;
         TC.digest = c.digest;
-        image_layout(V.X, V.plog, V.T.nq, s_off);
-        image_bytes(V.X, V.plog, V.T.nq, s_sz);
+        image_layout(V.X, V.T, s_off);
+        image_bytes(V.X, V.T, s_sz);
         // what goes to shared memory: the whole image, the wake table, or nothing
         u32 n_staged = 0;
         if (P.stage_mode == 0 && V.X.stage_bytes && V.X.stage_bytes <= P.stage_limit) n_staged = IM_N;
         else if (P.stage_mode <= 1 && im_round(s_sz[IM_WAKE]) <= P.stage_limit) n_staged = 1;
         V.staged = n_staged;
         for (int k = 0; k < IM_N; k++)
-            set_slice(V, k, k < (int)n_staged ? (void *)(img + s_off[k]) : global_slice(P, V.X, k));
+            set_slice(V, k, k < (int)n_staged ? (const void *)(img + s_off[k])
+                                              : global_slice(P, V.X, V.T, k));
     }
     __syncthreads();
     const u32 n_staged = V.staged;
-    for (int k = 0; k < (int)n_staged; k++) block_copy(img + s_off[k], global_slice(P, V.X, k), s_sz[k]);
+    for (int k = 0; k < (int)n_staged; k++) block_copy(img + s_off[k], global_slice(P, V.X, V.T, k), s_sz[k]);
     __syncthreads();
 
     u32 t = TC.now0, status = TC.status0, left = TC.left0, now = TC.now0;
@@ -1087,6 +1189,8 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         pk1[it] = kUnset;
     }
     __syncthreads();
+    Acc acc = {0, 0, 0, 0, 0, 0};
+    bool now_end = false;              // the clock becomes 1 + the latest node end
     while (status == EXP_RUNNING) {
         if (t >= limit) { now = t; break; }
         u32 rep = kUnset, done = 0, fail = kUnset;
@@ -1111,8 +1215,8 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                 M &= M - 1;
                 const u32 item = base + j;
                 const u32 old = __shfl_sync(kFull, w, j);
-                u32 r = item < nsw ? switch_tick(P, V, TC, item, t, old, poke, sm, &fail)
-                                   : rank_tick(P, V, TC, item - nsw, t, old, poke, &done, &fail);
+                u32 r = item < nsw ? switch_tick(V, acc, item, t, old, poke, sm, &fail)
+                                   : rank_tick(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail);
                 rep = min(rep, r);
             }
         }
@@ -1139,14 +1243,24 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         }
         left -= dn;
         k++;
-        if (fk != kUnset) { status = fk & 7u; now = TC.end_max1; break; }
-        if (left == 0) { status = EXP_DONE; now = TC.end_max1; break; }
-        if (nx == kUnset) { status = EXP_DEADLOCK; now = TC.end_max1; break; }
+        if (fk != kUnset) { status = fk & 7u; now_end = true; break; }
+        if (left == 0) { status = EXP_DONE; now_end = true; break; }
+        if (nx == kUnset) { status = EXP_DEADLOCK; now_end = true; break; }
         t = nx;
         if (ab) { now = t; break; }
     }
+    if (lane == 0) {
+        atomicAdd(&TC.pkts_injected, acc.inj);
+        atomicAdd(&TC.pkt_hops, acc.hops);
+        atomicAdd(&TC.pkts_delivered, acc.del);
+        atomicAdd(&TC.msgs_delivered, acc.msg);
+        atomicAdd(&TC.digest, acc.dig);
+    }
+    if (lane == 0 && acc.emax) atomicMax(&TC.end_max1, acc.emax);
     __syncthreads();
-    for (int k2 = 0; k2 < (int)n_staged; k2++) block_copy(global_slice(P, V.X, k2), img + s_off[k2], s_sz[k2]);
+    if (now_end) now = TC.end_max1;
+    for (int k2 = 0; k2 < (int)n_staged && k2 < IM_NDYN; k2++)
+        block_copy(const_cast<void *>(global_slice(P, V.X, V.T, k2)), img + s_off[k2], s_sz[k2]);
     if (threadIdx.x == 0) {
         ExpCtl c;
         c.status = status;
