@@ -323,6 +323,31 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
     u32 pk_min = kUnset;                // earliest tick poked into a downstream item
     bool ready_any = false;
     bool bad = false;
+    // Issue the independent loads together: per port (a lane has ports lane
+    // and lane + 32) its ingress queue words, its egress state and record,
+    // then the downstream queue words of each free egress.
+    u32 tail_[2] = {0, 0}, head_[2] = {0, 0}, dhead_[2] = {0, 0}, dtail_[2] = {0, 0};
+    uint2 st_[2] = {make_uint2(kUnset, 0), make_uint2(kUnset, 0)};
+    uint4 pr_[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        const u32 p = lane + 32 * j;
+        if (p >= np) continue;
+        const u32 qi = p0 + p;
+        const u64 pw = ld_vol64(&V.q_push[qi]);
+        tail_[j] = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
+        head_[j] = (u32)V.q_pop[qi];
+        st_[j] = V.eg[qi];
+        pr_[j] = V.port_rec[qi];
+    }
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        if (lane + 32 * j >= np || st_[j].x > t) continue;
+        const u32 dq = pr_[j].x;
+        const u64 dpop = ld_vol64(&V.q_pop[dq]);
+        dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
+        dtail_[j] = (u32)V.q_push[dq];
+    }
     sm->mask[lane] = 0;
     sm->mask[lane + 32] = 0;
     __syncwarp();
@@ -330,12 +355,9 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
     for (u32 j = 0; j < 2; j++) {
         u32 p = lane + 32 * j;
         if (p >= np) continue;
-        u32 qi = p0 + p;
-        u64 pw = ld_vol64(&V.q_push[qi]);
-        u32 tail = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-        u32 head = (u32)V.q_pop[qi];
+        const u32 qi = p0 + p, head = head_[j];
         sm->head[p] = head;
-        if (head == tail) continue;
+        if (head == tail_[j]) continue;
         uint4 pk = V.slots[(u64)qi * cap + head % cap];
         if (pk.x > t) { nxt = min(nxt, pk.x); continue; }
         ready_any = true;
@@ -353,15 +375,11 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         if (eg >= np) continue;
         unsigned long long M = sm->mask[eg];
         if (!M) continue;
-        u32 qe = p0 + eg;
-        uint2 st = V.eg[qe];
+        const uint2 st = st_[j];
         if (st.x > t) continue;             // busy: its heads wake the switch at t+1
-        const uint4 pr = V.port_rec[qe];    // downstream queue, sigma, delta, its owner
-        const u32 dq = pr.x, sg = pr.y, dl = pr.z;
-        u64 dpop = ld_vol64(&V.q_pop[dq]);
-        u32 dhead = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
-        u32 dtail = (u32)V.q_push[dq];
-        if (!credit_ok(V, dq, dtail, dhead, dl + 1, t)) continue;
+        const uint4 pr = pr_[j];            // downstream queue, sigma, delta, its owner
+        const u32 dq = pr.x, sg = pr.y, dl = pr.z, dtail = dtail_[j];
+        if (!credit_ok(V, dq, dtail, dhead_[j], dl + 1, t)) continue;
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
         uint4 pk = sm->pkt[i];
@@ -369,7 +387,7 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         pk.y += (dl + 1) << 16;
         V.slots[(u64)dq * cap + dtail % cap] = pk;
         st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
-        V.eg[qe] = make_uint2(t + sg, (i + 1) % np);
+        V.eg[p0 + eg] = make_uint2(t + sg, i + 1 == np ? 0u : i + 1);
         // the queue's owner: the peer switch, or the rank group of the host
         if (!(pr.w & 0x80000000u)) atomicMin(&poke[pr.w], pk.x);
         else if ((pr.w & 0x7FFFFFFFu) < V.X.nr) atomicMin(&poke[V.X.nsw + (pr.w & 0x7FFFFFFFu) / 32], pk.x);
@@ -861,18 +879,17 @@ __device__ __forceinline__ void dag_step(RankView &v)
 // SendSys + NICSndSys: one packet per uplink serialisation time, round-robin
 // over the send lanes from the pointer; a lane is eligible once its receive
 // dependencies are met and its destination joined before this tick.
-__device__ __forceinline__ void inject(RankView &v)
+// hr: the host's uplink record (queue, sigma, delta, switch); pw / tail:
+// that queue's pop word and push count, loaded at the start of the tick.
+__device__ __forceinline__ void inject(RankView &v, uint4 hr, u64 pw, u32 tail)
 {
     const HV &V = v.V;
     const auto &X = V.X;
     const u32 t = v.t;
     if (!v.C.lane_mask || v.C.blocked) return;
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
-    const uint4 hr = V.host_rec[v.r];       // uplink queue, sigma, delta, its switch
     const u32 qp = hr.x, hs = hr.y, hd = hr.z;
-    u64 pw = ld_vol64(&V.q_pop[qp]);
     u32 head = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-    u32 tail = (u32)V.q_push[qp];
     if (!credit_ok(V, qp, tail, head, hd + 1, t)) {
         v.nxt = min(v.nxt, t + 1);
         return;
@@ -937,18 +954,15 @@ __device__ __forceinline__ void inject(RankView &v)
 // NICRcvSys + ACKSys: take the ready head of the downlink queue; the last
 // packet of a message completes it at this rank and acknowledges it to the
 // sender, sum over hops of (delta + 1) ticks later.
-__device__ __forceinline__ void receive(RankView &v)
+// ql / head / tail: the downlink queue and its start-of-tick counters; pk:
+// its head packet (loaded at the start of the tick when the queue held one).
+__device__ __forceinline__ void receive(RankView &v, u32 ql, u32 head, u32 tail, uint4 pk)
 {
     const Params &P = *v.P;
     const HV &V = v.V;
     const auto &X = V.X;
     const u32 t = v.t;
-    u32 ql = V.T.nq + v.r;
-    u64 pw = ld_vol64(&V.q_push[ql]);
-    u32 tail = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-    u32 head = (u32)V.q_pop[ql];
     if (head == tail) return;
-    uint4 pk = V.slots[(u64)ql * X.cap + head % X.cap];
     if (pk.x > t) { v.nxt = min(v.nxt, pk.x); return; }
     st_vol32(&V.poplog[(u64)ql * V.plog + (head & (V.plog - 1))], t);
     st_vol64(&V.q_pop[ql], ((u64)t << 32) | (u32)(head + 1));
@@ -1000,11 +1014,23 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
     v.n_inj = v.n_del = v.n_msg = v.n_done = v.end_max1 = 0;
     v.dig = 0;
     if (v.r < V.X.nr) {
+        // issue the independent loads together: control word, uplink record,
+        // downlink queue words; then the uplink queue words and the downlink
+        // head packet
         v.C = load_ctl(&V.rk[v.r]);
+        const uint4 hr = V.host_rec[v.r];
+        const u32 ql = V.T.nq + v.r;
+        const u64 rx_push = ld_vol64(&V.q_push[ql]);
+        const u32 rx_head = (u32)V.q_pop[ql];
+        const u32 rx_tail = (u32)rx_push - ((u32)(rx_push >> 32) == t ? 1u : 0u);
+        const u64 up_pop = ld_vol64(&V.q_pop[hr.x]);
+        const u32 up_tail = (u32)V.q_push[hr.x];
+        uint4 rx_pk = make_uint4(kUnset, 0, 0, 0);
+        if (rx_head != rx_tail) rx_pk = V.slots[(u64)ql * V.X.cap + rx_head % V.X.cap];
         dag_step(v);
         if (!v.fail_over && !v.fail_err) {
-            inject(v);
-            receive(v);
+            inject(v, hr, up_pop, up_tail);
+            receive(v, ql, rx_head, rx_tail, rx_pk);
         }
         store_ctl(&V.rk[v.r], v.C);
     }
@@ -1174,15 +1200,17 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         now = TC.end_max1;
     }
     const u32 nI = V.X.n_items, nsw = V.X.nsw;
-    const u32 per = (nI + nW - 1) / nW;
-    const u32 i0 = min(warp * per, nI), i1 = min(i0 + per, nI);
+    // items are dealt to warps round-robin (item warp + j * nW), so switches
+    // and rank groups spread over all warps
+    const u32 cnt = warp < nI ? (nI - warp + nW - 1) / nW : 0;
     // Wake table: own[nI] (written by the item's warp only) and two poke
     // words per item.  Pokes made during step k go to word k & 1; the owner
     // folds them into own at the start of step k + 1, after the barrier, so
     // no poke is lost whatever order warps run in.  Pokes left by an earlier
     // run are folded before the first step.
     u32 *own = V.wake, *pk0 = V.wake + nI, *pk1 = V.wake + 2 * nI;
-    for (u32 it = i0 + lane; it < i1; it += 32) {
+    for (u32 j = lane; j < cnt; j += 32) {
+        const u32 it = warp + j * nW;
         u32 o = own[it], a = ld_vol32(&pk0[it]), b = ld_vol32(&pk1[it]);
         own[it] = min(o, min(a, b));
         pk0[it] = kUnset;
@@ -1195,10 +1223,10 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         if (t >= limit) { now = t; break; }
         u32 rep = kUnset, done = 0, fail = kUnset;
         u32 *poke = (k & 1) ? pk1 : pk0, *prev = (k & 1) ? pk0 : pk1;
-        for (u32 base = i0; base < i1; base += 32) {
-            const u32 it = base + lane;
+        for (u32 base = 0; base < cnt; base += 32) {
+            const u32 it = warp + (base + lane) * nW;
             u32 w = kUnset;
-            if (it < i1) {
+            if (base + lane < cnt) {
                 w = own[it];
                 const u32 q = ld_vol32(&prev[it]);
                 if (q != kUnset) {
@@ -1213,7 +1241,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
             while (M) {
                 const u32 j = (u32)__ffs(M) - 1;
                 M &= M - 1;
-                const u32 item = base + j;
+                const u32 item = warp + (base + j) * nW;
                 const u32 old = __shfl_sync(kFull, w, j);
                 u32 r = item < nsw ? switch_tick(V, acc, item, t, old, poke, sm, &fail)
                                    : rank_tick(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail);

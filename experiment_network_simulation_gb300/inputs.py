@@ -603,7 +603,8 @@ def gpt_1f1b(n_servers: int, gpus: int, pp: int, layers: int, micro: int, seq: i
 def config3(n_exp: int | None = None) -> Batch:
     """GPT-3 13B shape (40 layers, h 5120, 40 heads, s 2048, 8 micro-batches)
     on 128 servers x 8 GPUs: TP 8 (analytic), PP 4, DP 32, k=16 fat-tree at
-    400 Gbps; 500 experiments over algorithm x NC x chunk x duration seed."""
+    400 Gbps; 500 experiments = algorithm {ring, tree} x NC {1,2,4,8,16} x
+    chunk {64K..1M} x duration seeds 0..9."""
     tk = tick_ps(4096, 400)
     topo = fat_tree(16, delta=delay_ticks(1_000_000, tk), hosts_per_edge=8)
     work = gpt_1f1b(128, 8, 4, 40, 8, 2048, 5120, 40, 13_000_000_000, tk)
@@ -611,7 +612,7 @@ def config3(n_exp: int | None = None) -> Batch:
     for algo in (RING, TREE):
         for nc in (1, 2, 4, 8, 16):
             for ch in (64 * KIB, 128 * KIB, 256 * KIB, 512 * KIB, 1 * MIB):
-                for seed in range(5):
+                for seed in range(10):
                     exps.append(Experiment(topo, work, algo, nc, ch, 4096, 64, tk, dur_seed=seed,
                                            label=dict(algo=algo, nc=nc, chunk=ch, seed=seed)))
     if n_exp is not None:
