@@ -37,6 +37,7 @@ struct Layout {
         rk_total = 0, pend_total = 0, act_total = 0, lane_total = 0, portc_total = 0,
         nd_total = 0, rec_total = 0, items = 0;
     u32 warps = 1, image = 16;      // megakernel block size and shared image budget
+    u32 variant = 1;                // 1: every experiment staged whole; 2: some are not
     u32 max_level = 0, max_nodes = 0, max_queues = 0, max_ranks = 0;
     u64 max_pairs = 0;
     // host copies of the derived tables
@@ -397,6 +398,9 @@ int plan(const mv_batch_desc *d, Layout &L)
     }
     L.items = items;
     L.warps = std::min<u32>(kMaxWarps, max_items);
+    L.variant = 1;
+    for (u32 e = 0; e < L.E; e++)
+        if (!L.exp[e].stage_bytes) L.variant = 2;
     L.image = (u32)std::min<u64>(std::max(full_max, wake_max), kStageMax);
     L.order.resize(L.E);
     std::iota(L.order.begin(), L.order.end(), 0u);
@@ -736,23 +740,24 @@ int mv_run_ex(mv_ctx *c, uint32_t max_ticks, const mv_run_opts *o, uint64_t *ste
     if (c->L.E == 0) return MV_OK;
     Params P = c->P;
     P.max_ticks = max_ticks;
-    u32 warps = c->L.warps, grid = 0;
+    u32 warps = c->L.warps, grid = 0, variant = c->L.variant;
     if (o) {
-        if (o->stage > 2) return MV_EINVAL;
+        if (o->stage > 2 || o->variant > 2) return MV_EINVAL;
         P.watchdog_ns = o->watchdog_ns;
         P.stage_mode = o->stage;
         if (o->block_warps) warps = std::min<u32>(o->block_warps, kMaxWarps);
+        if (o->variant) variant = o->variant;
         grid = o->grid_blocks;
     }
     const u32 smem = megakernel_smem(warps, c->L.image);
     int bpsm = 0, nsm = 0;
-    cudaError_t e = megakernel_prepare(warps, smem, &bpsm, &nsm);
+    cudaError_t e = megakernel_prepare(variant, warps, smem, &bpsm, &nsm);
     if (e != cudaSuccess || bpsm == 0) return MV_ECUDA;
     u32 blocks = std::min<u32>(c->L.E, (u32)(bpsm * nsm));
     if (grid) blocks = std::min(blocks, grid);
     e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev0, c->stream);
-    if (e == cudaSuccess) e = launch_megakernel(P, blocks, warps, smem, c->stream);
+    if (e == cudaSuccess) e = launch_megakernel(variant, P, blocks, warps, smem, c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev1, c->stream);
     c->timed = e == cudaSuccess;
     Glob g;

@@ -207,9 +207,11 @@ cudaError_t launch_routes(const Params &p, u64 n_pairs_max, u32 level, cudaStrea
 cudaError_t launch_up_lists(const Params &p, u32 n_sw_total, cudaStream_t st);
 cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_ranks,
                         cudaStream_t st);
-cudaError_t megakernel_prepare(u32 warps, u32 smem_bytes, int *blocks_per_sm, int *n_sm);
+// variant 1: latency (one block an SM); 2: occupancy (two blocks an SM)
+cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,
+                               int *n_sm);
 u32 megakernel_smem(u32 warps, u32 image_bytes);
-cudaError_t launch_megakernel(const Params &p, u32 blocks, u32 warps, u32 smem_bytes,
-                              cudaStream_t st);
+cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
+                              u32 smem_bytes, cudaStream_t st);
 
 }  // namespace mv

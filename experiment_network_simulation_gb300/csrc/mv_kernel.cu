@@ -1309,8 +1309,13 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
 }
 
 // Persistent grid: each block takes the next experiment of the processing
-// order until none is left (or the watchdog fired).
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_megakernel(Params P)
+// order until none is left (or the watchdog fired).  MINB = 1 lets a block
+// use up to 255 registers a thread (lowest latency per tick, for
+// experiments stepped from shared memory); MINB = 2 caps registers so two
+// blocks share an SM (more experiments in flight, for experiments whose
+// state stays in global memory and whose ticks wait on memory).
+template <int MINB>
+__global__ void __launch_bounds__(kMaxWarps * 32, MINB) k_megakernel(Params P)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
     const u32 nW = blockDim.x >> 5, warp = threadIdx.x >> 5;
@@ -1360,24 +1365,31 @@ cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_
 
 u32 megakernel_smem(u32 warps, u32 image_bytes) { return warps * (u32)sizeof(SwSmem) + image_bytes; }
 
-cudaError_t megakernel_prepare(u32 warps, u32 smem_bytes, int *blocks_per_sm, int *n_sm)
+static const void *megakernel_fn(u32 variant)
+{
+    return variant == 2 ? (const void *)k_megakernel<2> : (const void *)k_megakernel<1>;
+}
+
+cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,
+                               int *n_sm)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes);
+    const void *fn = megakernel_fn(variant);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_megakernel,
-                                                         (int)(warps * 32), smem_bytes);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, (int)(warps * 32),
+                                                         smem_bytes);
 }
 
-cudaError_t launch_megakernel(const Params &p, u32 blocks, u32 warps, u32 smem_bytes,
-                              cudaStream_t st)
+cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
+                              u32 smem_bytes, cudaStream_t st)
 {
-    k_megakernel<<<blocks, warps * 32, smem_bytes, st>>>(p);
+    if (variant == 2) k_megakernel<2><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    else k_megakernel<1><<<blocks, warps * 32, smem_bytes, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -60,7 +60,7 @@ class ResultsView(C.Structure):
 
 class RunOpts(C.Structure):
     _fields_ = [("watchdog_ns", C.c_uint64), ("grid_blocks", C.c_uint32),
-                ("stage", C.c_uint32), ("block_warps", C.c_uint32), ("pad", C.c_uint32)]
+                ("stage", C.c_uint32), ("block_warps", C.c_uint32), ("variant", C.c_uint32)]
 
 STAGE_AUTO, STAGE_WAKE, STAGE_NONE = 0, 1, 2
 
@@ -174,9 +174,9 @@ class Simulator:
         self.rec_offset = np.concatenate([[0], np.cumsum(rc_per)])
 
     def run(self, max_ticks: int = UNSET - 1, watchdog_ns: int = 0, grid_blocks: int = 0,
-            stage: int = STAGE_AUTO, block_warps: int = 0) -> int:
+            stage: int = STAGE_AUTO, block_warps: int = 0, variant: int = 0) -> int:
         steps = C.c_uint64(0)
-        opts = RunOpts(watchdog_ns, grid_blocks, stage, block_warps, 0)
+        opts = RunOpts(watchdog_ns, grid_blocks, stage, block_warps, variant)
         with self.torch.cuda.device(self.device):
             rc = self.lib.mv_run_ex(self.ctx, int(max_ticks), C.byref(opts), C.byref(steps))
         self.steps = int(steps.value)

@@ -174,13 +174,17 @@ typedef struct mv_ctx mv_ctx;
  *   it fits, 1 = only its wake table is, 2 = nothing is (results are the
  *   same in every mode; the modes exist to test and measure that).
  * block_warps: warps of the block stepping one experiment (0 = automatic,
- *   at most 16). */
+ *   at most 8).
+ * variant: 0 = automatic, 1 = one block an SM with the most registers (for
+ *   batches whose experiments all fit in shared memory), 2 = two blocks an
+ *   SM (more experiments in flight, for larger ones).  Results are the same
+ *   in every variant. */
 typedef struct mv_run_opts {
     uint64_t watchdog_ns;
     uint32_t grid_blocks;
     uint32_t stage;
     uint32_t block_warps;
-    uint32_t pad;
+    uint32_t variant;
 } mv_run_opts;
 
 /* Workspace bytes mv_create needs for this batch (validates the
