@@ -40,47 +40,63 @@ UNIT = "packet-hops/s"
 # downstream queue and reads it back out (32 B); each packet also costs a
 # sender flow-state read-modify-write (16 B) and a receiver update (8 B).
 BYTES_PER_HOP, BYTES_PER_PKT = 32, 24
+# DRAM bytes (read + write) of one megakernel launch from an ncu capture of
+# the same workload (see profiles/); None until captured for this kernel.
+TRAFFIC = {}
 
 WORKLOADS = {
-    "config1": (I.config1, "ring all-reduce 16 MiB, 8 hosts, 2x2 leaf-spine, 400G, 16 experiments"),
-    "config2": (I.config2, "pipelined broadcast 1-64 MiB over A in 2..16 hosts, K in 1..64, 10G, 256 experiments"),
+    "config1": (lambda seed: I.config1(),
+                "ring all-reduce 16 MiB, 8 hosts, 2x2 leaf-spine, 400G, 16 experiments"),
+    "config2": (lambda seed: I.config2(seed=seed),
+                "pipelined broadcast 1-64 MiB over A in 2..16 hosts, K in 1..64, 10G, 256 experiments"),
+    "config3": (lambda seed: I.config3(),
+                "GPT-13B 1F1B iteration, 128 servers x 8 GPUs, TP8 PP4 DP32, k=16 fat-tree, 400G, "
+                "500 experiments"),
+    "config4": (lambda seed: I.config4(),
+                "MoE dispatch/combine, 512 ranks, top-8 of 256, 4 fabrics x 256 router seeds, "
+                "1,024 experiments"),
+    "config5": (lambda seed: I.config5(n_exp=24),
+                "topology search, GPT-13B at DP128 on 1,024-server 3-tier fabrics (24 of them)"),
 }
 DEFAULT = "config2"
 
 
-def make_batch(name: str, seed: int = 0):
-    fn = WORKLOADS[name][0]
-    return fn(seed=seed) if name == "config2" else fn()
+def make_batch(name: str, seed: int = 0, exps: int = 0):
+    b = WORKLOADS[name][0](seed)
+    return b.subset(range(min(exps, len(b)))) if exps else b
 
 
 # ----------------------------------------------------------------- oracle pool
 _W = {}
 
 
-def _worker_init(name: str, seed: int):
+def _worker_init(name: str, seed: int, exps: int, limit: int):
     sys.path.insert(0, ROOT)
     from oracle import oracle
 
     oracle.build()
-    _W["packed"] = make_batch(name, seed).pack()
+    _W["packed"] = make_batch(name, seed, exps).pack()
     _W["oracle"] = oracle
+    _W["limit"] = limit
 
 
 def _worker_run(e: int):
-    r = _W["oracle"].run(_W["packed"], e, e + 1)
+    r = _W["oracle"].run(_W["packed"], e, e + 1, _W["limit"])
     return int(r["pkt_hops"][e])
 
 
-def oracle_sample(name: str, seed: int, budget_s: float, cores: int):
+def oracle_sample(name: str, seed: int, budget_s: float, cores: int, exps: int = 0,
+                  limit: int = 0xFFFFFFFE):
     """Time the oracle over a seeded sample of experiments, all host cores in
-    parallel (one experiment per task), until about budget_s of wall clock."""
+    parallel (one experiment per task, each to completion or to `limit`
+    ticks), until about budget_s of wall clock."""
     from oracle import oracle
 
     oracle.build()
-    n_exp = len(make_batch(name, seed))
+    n_exp = len(make_batch(name, seed, exps))
     order = np.random.default_rng(1234).permutation(n_exp)
     ctx = mp.get_context("spawn")
-    with ctx.Pool(cores, initializer=_worker_init, initargs=(name, seed)) as pool:
+    with ctx.Pool(cores, initializer=_worker_init, initargs=(name, seed, exps, limit)) as pool:
         pool.map(_worker_run, [int(order[0])] * cores)          # warm the workers
         hops, done, t0 = 0, 0, time.perf_counter()
         while done < n_exp and time.perf_counter() - t0 < budget_s:
@@ -157,11 +173,12 @@ def run_reference(args, rank: int, world: int):
     cores = os.cpu_count() or 1
     name = args.workload
     per_step = max(1.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
+    lim = args.start_tick + args.max_ticks if (args.start_tick or args.max_ticks) else 0xFFFFFFFE
     for _ in range(args.warmup):
-        oracle_sample(name, 0, min(per_step, 5.0), cores)
+        oracle_sample(name, 0, min(per_step, 5.0), cores, args.exps, lim)
     hops, secs, n_done = 0, 0.0, 0
     for _ in range(args.steps):
-        h, dt, done, n_exp = oracle_sample(name, 0, per_step, cores)
+        h, dt, done, n_exp = oracle_sample(name, 0, per_step, cores, args.exps, lim)
         hops += h
         secs += dt
         n_done += done
@@ -186,50 +203,79 @@ def run_gpu(args, rank: int, world: int):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    batch = make_batch(args.workload, seed=rank)      # each rank: its own shard of experiments
+    batch = make_batch(args.workload, seed=rank, exps=args.exps)   # each rank: its own shard
     packed = batch.pack()
     stream = torch.cuda.Stream(dev)
     sim = mv.Simulator(packed, device=str(dev), stream=stream)
     n_levels = int(packed["sw_level"].max())
     launches_per_step = n_levels + 4                  # routes per level, up lists, 2 init, megakernel
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    window = args.start_tick > 0 or args.max_ticks > 0
+    budget = args.max_ticks if args.max_ticks > 0 else mv.UNSET - 1
 
-    def step():
-        sim.reset()
-        rc = sim.run()
-        assert rc == mv.MV_OK, rc
+    snap = {}
+
+    def prefix():
+        """Untimed: back to tick 0 and, for a window, on to its start tick.
+        The simulator's whole state is its workspace, so the window's start
+        state is computed once and then restored by a device copy."""
+        if args.start_tick:
+            if not snap:
+                sim.reset()
+                rc = sim.run(max_ticks=args.start_tick)
+                assert rc in (mv.MV_OK, mv.MV_INCOMPLETE), rc
+                c = sim.counters()
+                snap["ws"] = sim.ws.clone()
+                snap["h"] = (int(c["pkt_hops"].sum()), int(c["pkts_injected"].sum()))
+            with torch.cuda.stream(stream):
+                sim.ws.copy_(snap["ws"])
+        with torch.cuda.stream(stream):
+            flush.zero_()                             # L2 flush between steps
+        return snap.get("h", (0, 0))
+
+    def timed():
+        """The timed region: reset (unless a window) + one megakernel run."""
+        if not args.start_tick:
+            sim.reset()
+        rc = sim.run(max_ticks=budget)
+        assert rc in ((mv.MV_OK, mv.MV_INCOMPLETE) if window else (mv.MV_OK,)), rc
 
     for _ in range(args.warmup):
-        step()
-    res = sim.results()
-    assert (res["status"] == mv.EXP_DONE).all(), "warm-up did not finish every experiment"
-    hops_step = int(res["pkt_hops"].sum())
-    pkts_step = int(res["pkts_injected"].sum())
+        prefix()
+        timed()
+    res = sim.counters()
+    if not window:
+        assert (res["status"] == mv.EXP_DONE).all(), "warm-up did not finish every experiment"
 
     clocks = Clocks(dev.index if dev.index is not None else 0)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
-    total_ms, kernel_ms, steps_grid = 0.0, [], []
+    total_ms, kernel_ms, steps_grid, hops_l, pkts_l = 0.0, [], [], [], []
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.steps):
+        h0, p0 = prefix()
         with torch.cuda.stream(stream):
-            flush.zero_()
             ev0.record(stream)
-        step()
+        timed()
         ev1.record(stream)
         ev1.synchronize()
         total_ms += ev0.elapsed_time(ev1)
         kernel_ms.append(sim.last_run_ms())
         steps_grid.append(sim.steps)
+        c = sim.counters()
+        hops_l.append(int(c["pkt_hops"].sum()) - h0)
+        pkts_l.append(int(c["pkts_injected"].sum()) - p0)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    res = sim.results()
-    assert (res["status"] == mv.EXP_DONE).all()
-    assert int(res["pkt_hops"].sum()) == hops_step, "a step simulated different work"
+    res = sim.counters()
+    if not window:
+        assert (res["status"] == mv.EXP_DONE).all()
+    assert len(set(hops_l)) == 1, "a step simulated different work"
+    hops_step, pkts_step = hops_l[0], pkts_l[0]
 
     ms_step = total_ms / args.steps
     t = torch.tensor([ms_step, float(hops_step), float(len(batch))], dtype=torch.float64)
@@ -244,22 +290,25 @@ def run_gpu(args, rank: int, world: int):
         ms_max, hops_all, exps_all = ms_step, float(hops_step), float(len(batch))
     value = hops_all / (ms_max / 1000.0)
 
-    # e2e through the public API from host buffers
-    h2d = sum(int(np.asarray(v).nbytes) for k, v in packed.items() if k != "version")
-    e2e_s = []
-    d2h = 0
-    for i in range(max(1, args.e2e_steps)):
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        s2 = mv.Simulator(packed, device=str(dev), stream=stream)
-        s2.run()
-        r2 = s2.results()
-        s2.close()
-        e2e_s.append(time.perf_counter() - t0)
-        d2h = sum(int(v.nbytes) for k, v in r2.items() if isinstance(v, np.ndarray)
-                  and k not in ("node_offset", "rec_offset"))
-        del s2
-    e2e_val = hops_step / statistics.mean(e2e_s)
+    # e2e through the public API from host buffers: create (upload), run,
+    # results (download); whole runs only
+    e2e = None
+    if not window and args.e2e_steps > 0:
+        h2d = sum(int(np.asarray(v).nbytes) for k, v in packed.items() if k != "version")
+        e2e_s, d2h = [], 0
+        for _ in range(args.e2e_steps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            s2 = mv.Simulator(packed, device=str(dev), stream=stream)
+            s2.run()
+            r2 = s2.results()
+            s2.close()
+            e2e_s.append(time.perf_counter() - t0)
+            d2h = sum(int(v.nbytes) for k, v in r2.items() if isinstance(v, np.ndarray)
+                      and k not in ("node_offset", "rec_offset"))
+            del s2
+        e2e = {"value": hops_step / statistics.mean(e2e_s), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks = load_peaks()
     km = statistics.mean(kernel_ms)
@@ -267,7 +316,7 @@ def run_gpu(args, rank: int, world: int):
     achieved = alg_bytes / (km / 1000.0) / 1e9
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": None,
+            "frac": achieved / peak, "traffic": TRAFFIC.get(args.workload) if not window else None,
             "peak_source": "measured" if peaks else "fallback",
             "kernel": "k_megakernel", "kernel_ms": km,
             "alg_bytes_per_launch": alg_bytes}
@@ -275,26 +324,32 @@ def run_gpu(args, rank: int, world: int):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        h, dt, done, n_exp = oracle_sample(args.workload, 0, args.cpu_budget_s, cores)
+        lim = args.start_tick + args.max_ticks if window else 0xFFFFFFFE
+        h, dt, done, n_exp = oracle_sample(args.workload, 0, args.cpu_budget_s, cores,
+                                           args.exps, lim)
+        what = f"first {lim} ticks of " if window else ""
         cpu = {"value": h / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{done} of {n_exp} experiments (seeded permutation), "
+               "sample": f"{what}{done} of {n_exp} experiments (seeded permutation), "
                          f"{dt:.1f} s wall, one experiment per process"}
 
     if rank == 0:
+        cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload][1],
+               "experiments": int(exps_all), "packet_hops_per_step": int(hops_all),
+               "l2": "flushed between steps (512 MiB write)",
+               "grid_steps_per_run": int(statistics.mean(steps_grid))}
+        if window:
+            cfg["window"] = {"start_tick": args.start_tick, "max_ticks": args.max_ticks,
+                             "note": "each step times ticks [start, start + max) of every "
+                                     "experiment's clock; the prefix runs untimed"}
         out = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "u32", "data": "synthetic",
-            "config": {"workload": args.workload, "desc": WORKLOADS[args.workload][1],
-                       "experiments": int(exps_all), "packet_hops_per_step": int(hops_all),
-                       "l2": "flushed between steps (512 MiB write)",
-                       "grid_steps_per_run": int(statistics.mean(steps_grid))},
-            "experiments_per_hour": exps_all / (ms_max / 1000.0) * 3600.0,
+            "dtype": "u32", "data": "synthetic", "config": cfg,
+            "experiments_per_hour": None if window else exps_all / (ms_max / 1000.0) * 3600.0,
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "e2e": e2e,
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }
@@ -312,6 +367,11 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--exps", type=int, default=0, help="first N experiments of the batch")
+    ap.add_argument("--start-tick", type=int, default=0,
+                    help="run every experiment to this tick before the timed region")
+    ap.add_argument("--max-ticks", type=int, default=0,
+                    help="timed run budget in ticks of each experiment's clock (0 = to the end)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -78,7 +78,7 @@ struct Lane {
 struct RankCtl {
     u32 busy, rr, npend, nact;
     u64 lane_mask;
-    u64 port_mask[2];
+    u64 port_lo, port_hi;   // receive counters in use: bits 0..63, 64..127
     u32 blocked;    // every send lane waits for a receive count (no scan needed)
     u32 pad;
 };

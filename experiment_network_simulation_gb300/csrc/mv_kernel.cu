@@ -310,7 +310,7 @@ __device__ __forceinline__ u32 route_port(const HV &V, u32 s, u32 p0, uint4 pk)
 // earliest tick this warp knows of at which something may happen (its own
 // next wake and the wakes it gave other items); *fail gets a failure key.
 __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t, u32 old,
-                                           u32 *poke, SwSmem *sm, u32 *fail)
+                                           u32 *poke, SwSmem *sm, u32 *fail, bool staged)
 {
     // a register copy of the view: stores through the state pointers cannot
     // alias it, so its fields are loaded once per tick
@@ -340,13 +340,17 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         st_[j] = V.eg[qi];
         pr_[j] = V.port_rec[qi];
     }
+    // in shared memory these are cheap, so every free egress gets them now;
+    // in global memory only egresses that a packet wants load them (below)
+    if (staged) {
 #pragma unroll
-    for (u32 j = 0; j < 2; j++) {
-        if (lane + 32 * j >= np || st_[j].x > t) continue;
-        const u32 dq = pr_[j].x;
-        const u64 dpop = ld_vol64(&V.q_pop[dq]);
-        dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
-        dtail_[j] = (u32)V.q_push[dq];
+        for (u32 j = 0; j < 2; j++) {
+            if (lane + 32 * j >= np || st_[j].x > t) continue;
+            const u32 dq = pr_[j].x;
+            const u64 dpop = ld_vol64(&V.q_pop[dq]);
+            dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
+            dtail_[j] = (u32)V.q_push[dq];
+        }
     }
     sm->mask[lane] = 0;
     sm->mask[lane + 32] = 0;
@@ -378,7 +382,13 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         const uint2 st = st_[j];
         if (st.x > t) continue;             // busy: its heads wake the switch at t+1
         const uint4 pr = pr_[j];            // downstream queue, sigma, delta, its owner
-        const u32 dq = pr.x, sg = pr.y, dl = pr.z, dtail = dtail_[j];
+        const u32 dq = pr.x, sg = pr.y, dl = pr.z;
+        if (!staged) {
+            const u64 dpop = ld_vol64(&V.q_pop[dq]);
+            dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
+            dtail_[j] = (u32)V.q_push[dq];
+        }
+        const u32 dtail = dtail_[j];
         if (!credit_ok(V, dq, dtail, dhead_[j], dl + 1, t)) continue;
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
@@ -426,8 +436,8 @@ __device__ __forceinline__ RankCtl load_ctl(const RankCtl *p)
     RankCtl r;
     r.busy = a.x; r.rr = a.y; r.npend = a.z; r.nact = a.w;
     r.lane_mask = ((u64)b.y << 32) | b.x;
-    r.port_mask[0] = ((u64)b.w << 32) | b.z;
-    r.port_mask[1] = ((u64)c.y << 32) | c.x;
+    r.port_lo = ((u64)b.w << 32) | b.z;
+    r.port_hi = ((u64)c.y << 32) | c.x;
     r.blocked = c.z;
     r.pad = 0;
     return r;
@@ -436,24 +446,46 @@ __device__ __forceinline__ void store_ctl(RankCtl *p, const RankCtl &r)
 {
     uint4 *q = reinterpret_cast<uint4 *>(p);
     q[0] = make_uint4(r.busy, r.rr, r.npend, r.nact);
-    q[1] = make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_mask[0],
-                      (u32)(r.port_mask[0] >> 32));
-    q[2] = make_uint4((u32)r.port_mask[1], (u32)(r.port_mask[1] >> 32), r.blocked, 0);
+    q[1] = make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_lo,
+                      (u32)(r.port_lo >> 32));
+    q[2] = make_uint4((u32)r.port_hi, (u32)(r.port_hi >> 32), r.blocked, 0);
 }
 static_assert(sizeof(Lane) == 80, "Lane is five 16-byte words");
+// Field by field through 16-byte words: the local Lane never has its
+// address taken, so it stays in registers.
 __device__ __forceinline__ Lane load_lane(const Lane *p)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
+    const uint4 a = q[0], b = q[1], c = q[2], d = q[3], e = q[4];
     Lane L;
-    uint4 *d = reinterpret_cast<uint4 *>(&L);
-    d[0] = q[0]; d[1] = q[1]; d[2] = q[2]; d[3] = q[3]; d[4] = q[4];
+    L.node = a.x; L.member = a.y; L.chan = a.z; L.kind = a.w;
+    L.m = b.x; L.nmsg = b.y; L.pkts_left = b.z; L.dst_member = b.w;
+    L.dst_port = c.x; L.dep_base = c.y; L.dep_mask = c.z; L.dep_need = c.w;
+    L.key = d.x; L.a2a_e = d.y; L.a2a_start = d.z; L.dnode = d.w;
+    L.drank = e.x; L.dslot = e.y; L.ok_dst = e.z; L.pbase = e.w;
     return L;
 }
 __device__ __forceinline__ void store_lane(Lane *p, const Lane &L)
 {
     uint4 *q = reinterpret_cast<uint4 *>(p);
-    const uint4 *s = reinterpret_cast<const uint4 *>(&L);
-    q[0] = s[0]; q[1] = s[1]; q[2] = s[2]; q[3] = s[3]; q[4] = s[4];
+    q[0] = make_uint4(L.node, L.member, L.chan, L.kind);
+    q[1] = make_uint4(L.m, L.nmsg, L.pkts_left, L.dst_member);
+    q[2] = make_uint4(L.dst_port, L.dep_base, L.dep_mask, L.dep_need);
+    q[3] = make_uint4(L.key, L.a2a_e, L.a2a_start, L.dnode);
+    q[4] = make_uint4(L.drank, L.dslot, L.ok_dst, L.pbase);
+}
+
+// Receive-counter occupancy bits, by value (no indexed array, so the rank's
+// control word stays in registers).
+__device__ __forceinline__ bool port_used(const RankCtl &C, u32 p)
+{
+    return ((p < 64 ? C.port_lo >> p : C.port_hi >> (p - 64)) & 1ull) != 0;
+}
+__device__ __forceinline__ void port_set(RankCtl &C, u32 p, bool on)
+{
+    const u64 bit = 1ull << (p & 63);
+    if (p < 64) C.port_lo = on ? (C.port_lo | bit) : (C.port_lo & ~bit);
+    else C.port_hi = on ? (C.port_hi | bit) : (C.port_hi & ~bit);
 }
 
 // Per-rank view used while processing one tick.
@@ -735,7 +767,7 @@ __device__ __forceinline__ void complete_node(RankView &v, u32 u, u32 c)
 __device__ __forceinline__ void free_ports(RankView &v, u32 u)
 {
     u32 np = nports_of(v, coll_of(v, u)), b = v.V.nd_pbase[u];
-    for (u32 p = b; p < b + np; p++) v.C.port_mask[p >> 6] &= ~(1ull << (p & 63));
+    for (u32 p = b; p < b + np; p++) port_set(v.C, p, false);
 }
 
 // A rank joins a network collective: receive counters, then send lanes.
@@ -749,7 +781,7 @@ __device__ __forceinline__ bool net_join(RankView &v, u32 u)
     i32 base = -1;
     for (u32 b = 0; b + np <= X.port_cap && base < 0; b++) {
         u32 k = 0;
-        while (k < np && !((v.C.port_mask[(b + k) >> 6] >> ((b + k) & 63)) & 1ull)) k++;
+        while (k < np && !port_used(v.C, b + k)) k++;
         if (k == np) base = (i32)b;
     }
     if (base < 0) { v.fail_over = true; return false; }
@@ -757,7 +789,7 @@ __device__ __forceinline__ bool net_join(RankView &v, u32 u)
     uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     for (u32 p = 0; p < np; p++) {
         u32 s = (u32)base + p;
-        v.C.port_mask[s >> 6] |= 1ull << (s & 63);
+        port_set(v.C, s, true);
         ports[s] = make_uint2(0, u);
         out += (i32)port_count_expect(v, c, i, p);
     }
@@ -1200,6 +1232,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         now = TC.end_max1;
     }
     const u32 nI = V.X.n_items, nsw = V.X.nsw;
+    const bool full = n_staged == IM_N;        // the whole state is in shared memory
     // items are dealt to warps round-robin (item warp + j * nW), so switches
     // and rank groups spread over all warps
     const u32 cnt = warp < nI ? (nI - warp + nW - 1) / nW : 0;
@@ -1243,7 +1276,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                 M &= M - 1;
                 const u32 item = warp + (base + j) * nW;
                 const u32 old = __shfl_sync(kFull, w, j);
-                u32 r = item < nsw ? switch_tick(V, acc, item, t, old, poke, sm, &fail)
+                u32 r = item < nsw ? switch_tick(V, acc, item, t, old, poke, sm, &fail, full)
                                    : rank_tick(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail);
                 rep = min(rep, r);
             }

@@ -198,6 +198,23 @@ class Simulator:
             raise MVError(rc, "mv_last_run_ms")
         return float(ms.value)
 
+    def counters(self) -> dict:
+        """Per-experiment status, clock and counters only (no per-node rows)."""
+        E = self.n_exps
+        r = {"status": np.zeros(E, np.uint32), "end_tick": np.zeros(E, np.uint32),
+             "now": np.zeros(E, np.uint32)}
+        for k in ("pkts_injected", "pkt_hops", "pkts_delivered", "msgs_delivered"):
+            r[k] = np.zeros(E, np.uint64)
+        v = ResultsView()
+        for n, t in _RES:
+            if n in r:
+                setattr(v, n, r[n].ctypes.data_as(_CT[t]))
+        with self.torch.cuda.device(self.device):
+            rc = self.lib.mv_results(self.ctx, C.byref(v))
+        if rc != MV_OK:
+            raise MVError(rc, "mv_results")
+        return r
+
     def results(self) -> dict:
         E = self.n_exps
         r = {"status": np.zeros(E, np.uint32), "end_tick": np.zeros(E, np.uint32),
