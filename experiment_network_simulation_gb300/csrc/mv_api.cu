@@ -59,7 +59,7 @@ struct Layout {
         r_a2a_bytes, r_a2a_in_bytes, r_mem, r_order, r_node_rank, r_sw_rec, r_port_rec,
         r_host_rec;
     u64 static_bytes = 0;
-    Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_pend, r_act,
+    Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_rdirty, r_pend, r_act,
         r_lanes, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
         r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_glob, r_wake;
     u64 total = 0;
@@ -468,6 +468,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_slots = L.take(16 * L.slot_total);
     L.r_eg = L.take(8 * L.eg_total);
     L.r_rk = L.take(sizeof(RankCtl) * L.rk_total);
+    L.r_rdirty = L.take(4 * L.rk_total);
     L.r_pend = L.take(8ull * L.pend_total);
     L.r_act = L.take(4ull * L.act_total);
     L.r_lanes = L.take(sizeof(Lane) * L.lane_total);
@@ -553,6 +554,7 @@ Params make_params(void *ws, const Layout &L)
     P.slots = at<uint4>(ws, L.r_slots);
     P.eg = at<uint2>(ws, L.r_eg);
     P.rk = at<RankCtl>(ws, L.r_rk);
+    P.rdirty = at<u32>(ws, L.r_rdirty);
     P.pend = at<uint2>(ws, L.r_pend);
     P.act = at<u32>(ws, L.r_act);
     P.lanes = at<Lane>(ws, L.r_lanes);

@@ -80,7 +80,7 @@ struct RankCtl {
     u64 lane_mask;
     u64 port_lo, port_hi;   // receive counters in use: bits 0..63, 64..127
     u32 blocked;    // every send lane waits for a receive count (no scan needed)
-    u32 pad;
+    u32 nintra;     // running intra-server memberships (checked every tick)
 };
 
 // Per-experiment control, kept across runs (resume) and read by mv_results.
@@ -126,6 +126,7 @@ struct Params {
     uint4 *slots;            // packet descriptors
     uint2 *eg;               // per switch port: (busy_until, round-robin pointer)
     RankCtl *rk;
+    u32 *rdirty;             // per rank: a message of one of its running nodes completed
     uint2 *pend;             // per rank: pend_cap (node, start tick)
     u32 *act;                // per rank: act_cap running nodes, ascending
     Lane *lanes;             // per rank: lane_cap
@@ -159,7 +160,7 @@ __host__ __device__ inline u32 pk_slot(uint4 p) { return p.w >> 25; }
 // image cut after it holds the wake table alone.  The dynamic state
 // (IM_WAKE .. IM_SLOTS) is copied in and back out; the topology records and
 // routing tables after it are only copied in.
-enum : int { IM_WAKE, IM_QPUSH, IM_QPOP, IM_EG, IM_RK, IM_PRED, IM_CAND, IM_START, IM_END,
+enum : int { IM_WAKE, IM_QPUSH, IM_QPOP, IM_EG, IM_RK, IM_RDIRTY, IM_PRED, IM_CAND, IM_START, IM_END,
              IM_PBASE, IM_DONE, IM_OUT, IM_ACT, IM_PEND, IM_PORTS, IM_POPLOG, IM_LANES,
              IM_SLOTS, IM_NDYN, IM_SWREC = IM_NDYN, IM_PORTREC, IM_HOSTREC, IM_ROUTE, IM_UPN,
              IM_UPLIST, IM_N };
@@ -174,6 +175,7 @@ __host__ __device__ inline void image_bytes(const ExpRec &X, const TopoRec &T, u
     sz[IM_QPOP] = 8ull * X.nq;
     sz[IM_EG] = 8ull * n_eg;
     sz[IM_RK] = sizeof(RankCtl) * (u64)X.nr;
+    sz[IM_RDIRTY] = 4ull * X.nr;
     for (int k = IM_PRED; k <= IM_OUT; k++) sz[k] = 4ull * X.nn;
     sz[IM_ACT] = 4ull * X.nr * X.act_cap;
     sz[IM_PEND] = 8ull * X.nr * X.pend_cap;

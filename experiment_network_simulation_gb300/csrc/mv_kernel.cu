@@ -182,6 +182,7 @@ struct XV {
     uint4 *slots;
     uint2 *eg;
     RankCtl *rk;
+    u32 *rdirty;
     uint2 *pend;
     u32 *act;
     Lane *lanes;
@@ -211,6 +212,7 @@ struct HV {
     uint4 *slots;
     uint2 *eg;
     RankCtl *rk;
+    u32 *rdirty;
     uint2 *pend;
     u32 *act;
     Lane *lanes;
@@ -236,7 +238,7 @@ __device__ __forceinline__ HV make_hv(const XV &S)
     V.W.memb_off = S.W.memb_off; V.W.a2a_off = S.W.a2a_off; V.W.a2a_in_off = S.W.a2a_in_off;
     V.plog = S.plog;
     V.q_push = S.q_push; V.q_pop = S.q_pop; V.poplog = S.poplog; V.slots = S.slots; V.eg = S.eg;
-    V.rk = S.rk; V.pend = S.pend; V.act = S.act; V.lanes = S.lanes; V.ports = S.ports;
+    V.rk = S.rk; V.rdirty = S.rdirty; V.pend = S.pend; V.act = S.act; V.lanes = S.lanes; V.ports = S.ports;
     V.nd_pred = S.nd_pred; V.nd_cand = S.nd_cand; V.nd_start = S.nd_start; V.nd_end = S.nd_end;
     V.nd_pbase = S.nd_pbase; V.nd_done = S.nd_done; V.nd_out = S.nd_out; V.wake = S.wake;
     V.sw_rec = S.sw_rec; V.port_rec = S.port_rec; V.host_rec = S.host_rec; V.route = S.route;
@@ -417,13 +419,12 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
             st_vol64(&V.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
         }
     }
-    if (all) hops = __reduce_add_sync(kFull, hops);
+    acc.hops += hops;                   // per lane; summed over the warp once per experiment
     nxt = __reduce_min_sync(kFull, ready_any ? t + 1 : nxt);   // heads left or blocked: next tick
     pk_min = __reduce_min_sync(kFull, pk_min);
     if (__any_sync(kFull, bad)) *fail = min(*fail, kFailSwitch);
     u32 w = min(nxt, old > t ? old : kUnset);
     if (lane == 0) V.wake[s] = w;
-    if (all) acc.hops += hops;
     __syncwarp();
     return min(w, pk_min);
 }
@@ -439,7 +440,7 @@ __device__ __forceinline__ RankCtl load_ctl(const RankCtl *p)
     r.port_lo = ((u64)b.w << 32) | b.z;
     r.port_hi = ((u64)c.y << 32) | c.x;
     r.blocked = c.z;
-    r.pad = 0;
+    r.nintra = c.w;
     return r;
 }
 __device__ __forceinline__ void store_ctl(RankCtl *p, const RankCtl &r)
@@ -448,7 +449,7 @@ __device__ __forceinline__ void store_ctl(RankCtl *p, const RankCtl &r)
     q[0] = make_uint4(r.busy, r.rr, r.npend, r.nact);
     q[1] = make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_lo,
                       (u32)(r.port_lo >> 32));
-    q[2] = make_uint4((u32)r.port_hi, (u32)(r.port_hi >> 32), r.blocked, 0);
+    q[2] = make_uint4((u32)r.port_hi, (u32)(r.port_hi >> 32), r.blocked, r.nintra);
 }
 static_assert(sizeof(Lane) == 80, "Lane is five 16-byte words");
 // Field by field through 16-byte words: the local Lane never has its
@@ -832,6 +833,7 @@ __device__ __forceinline__ void act_add(RankView &v, u32 u, u32 flag)
     while (j > 0 && (a[j - 1] & ~kActIntra) > u) { a[j] = a[j - 1]; j--; }
     a[j] = u | flag;
     v.C.nact++;
+    if (flag) v.C.nintra++;
 }
 
 // Schedule + AnalyticalSys: finish running memberships, then start the nodes
@@ -845,9 +847,15 @@ __device__ __forceinline__ void dag_step(RankView &v)
         if (v.C.npend) v.nxt = min(v.nxt, pd[0].y);
         return;
     }
+    // Running memberships: an intra-server one can finish whenever its last
+    // member has started, so those are checked every tick; a network one
+    // only when a message of this rank's completed (receive sets rdirty).
     u32 *a = V.act + (u64)v.r * V.X.act_cap;
     u32 w = 0;
-    for (u32 j = 0; j < v.C.nact; j++) {
+    const bool dirty = ld_vol32(&V.rdirty[v.r]) != 0;
+    if (dirty) atomicExch(&V.rdirty[v.r], 0u);
+    const u32 nscan = (dirty || v.C.nintra) ? v.C.nact : 0;
+    for (u32 j = 0; j < nscan; j++) {
         const u32 e = a[j], u = e & ~kActIntra;
         bool fin = false;
         if (e & kActIntra) {
@@ -859,7 +867,7 @@ __device__ __forceinline__ void dag_step(RankView &v)
                 if (st == kUnset || st >= t) ok = false;
                 else b = max(b, st);
             }
-            if (ok) { complete_node(v, u, b + intra_ticks(v, c)); fin = true; }
+            if (ok) { complete_node(v, u, b + intra_ticks(v, c)); fin = true; v.C.nintra--; }
         } else if (ld_vol32((const u32 *)&V.nd_out[u]) == 0) {
             __threadfence_block();         // the count reached 0: read the latest event after it
             u32 done = ld_vol32(&V.nd_done[u]);
@@ -867,9 +875,9 @@ __device__ __forceinline__ void dag_step(RankView &v)
             complete_node(v, u, done);
             fin = true;
         }
-        if (!fin) a[w++] = e;
+        if (!fin) { if (w != j) a[w] = e; w++; }
     }
-    v.C.nact = w;
+    if (nscan) v.C.nact = w;
     // start the nodes due now: the prefix of the sorted pending list (a
     // start tick already past is an inconsistent schedule)
     u32 lo = 0;
@@ -1003,7 +1011,7 @@ __device__ __forceinline__ void receive(RankView &v, u32 ql, u32 head, u32 tail,
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     if (!pk_last(pk)) return;
     v.nxt = min(v.nxt, t + 1);                         // DAG looks at its counts next tick
-    rank_poke(v, rank_item(V, P.node_rank[W_(v).node_off + pk.z]), t + 1);   // the ACK
+    rank_poke(v, rank_item(V, P.node_rank[W_(v).node_off + pk.z]), t + 1);   // the ACK (see below)
     uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     u32 ps = pk_slot(pk);
     uint2 port = ports[ps];
@@ -1011,12 +1019,16 @@ __device__ __forceinline__ void receive(RankView &v, u32 ql, u32 head, u32 tail,
     ports[ps] = port;
     v.C.blocked = 0;
     u32 own = port.y, snd = pk.z;
+    const u32 srank = P.node_rank[W_(v).node_off + snd];
     atomicMax(&V.nd_done[own], t);
     __threadfence_block();
     atomicSub(&V.nd_out[own], 1);
     atomicMax(&V.nd_done[snd], t + pk_hops(pk));
     __threadfence_block();
     atomicSub(&V.nd_out[snd], 1);
+    __threadfence_block();                 // counts before the flags that announce them
+    atomicOr(&V.rdirty[v.r], 1u);
+    atomicOr(&V.rdirty[srank], 1u);
     v.n_msg++;
     v.dig += mix64(mix64((u64)pk.z | ((u64)pk_key(pk) << 32)) ^ (u64)t);
     u32 idx = atomicAdd(&v.TC->rec_count, 1u);
@@ -1066,34 +1078,24 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
         }
         store_ctl(&V.rk[v.r], v.C);
     }
-    // one packed sum for the per-lane 0/1 counts (each at most 32 a warp)
-    const u32 cnt = __reduce_add_sync(kFull, v.n_inj | (v.n_del << 8) | (v.n_msg << 16));
-    const u32 inj = cnt & 0xFF, del = (cnt >> 8) & 0xFF, msg = cnt >> 16;
     const u32 nxt = __reduce_min_sync(kFull, v.nxt);
     const u32 pkm = __reduce_min_sync(kFull, v.pk_min);
-    u32 done = 0, emax = 0;
-    if (__any_sync(kFull, v.n_done != 0)) {
-        done = __reduce_add_sync(kFull, v.n_done);
-        emax = __reduce_max_sync(kFull, v.end_max1);
-    }
+    u32 done = 0;
+    if (__any_sync(kFull, v.n_done != 0)) done = __reduce_add_sync(kFull, v.n_done);
     if (__any_sync(kFull, v.fail_over || v.fail_err)) {
         u32 fk = v.fail_over ? fail_key_rank(v.r, EXP_OVERFLOW)
                : v.fail_err ? fail_key_rank(v.r, EXP_ERROR) : kUnset;
         *fail = min(*fail, __reduce_min_sync(kFull, fk));
     }
-    u64 dig = 0;
-    if (msg) {                              // 64-bit digest sum across the warp
-        dig = v.dig;
-        for (int o = 16; o > 0; o >>= 1) dig += __shfl_xor_sync(kFull, dig, o);
-    }
     u32 w = min(nxt, old > t ? old : kUnset);
     if (lane == 0) V.wake[it] = w;
-    acc.inj += inj;
-    acc.hops += inj;
-    acc.del += del;
-    acc.msg += msg;
-    acc.dig += dig;
-    acc.emax = max(acc.emax, emax);
+    // counters per lane; summed over the warp once per experiment
+    acc.inj += v.n_inj;
+    acc.hops += v.n_inj;
+    acc.del += v.n_del;
+    acc.msg += v.n_msg;
+    acc.dig += v.dig;
+    acc.emax = max(acc.emax, v.end_max1);
     *done_out += done;
     return min(w, pkm);
 }
@@ -1123,6 +1125,7 @@ __device__ const void *global_slice(const Params &P, const ExpRec &X, const Topo
     case IM_QPOP: return P.q_pop + X.q_off;
     case IM_EG: return P.eg + X.eg_off;
     case IM_RK: return P.rk + X.rk_off;
+    case IM_RDIRTY: return P.rdirty + X.rk_off;
     case IM_PRED: return P.nd_pred + X.nd_off;
     case IM_CAND: return P.nd_cand + X.nd_off;
     case IM_START: return P.nd_start + X.nd_off;
@@ -1154,6 +1157,7 @@ __device__ void set_slice(XV &V, int k, const void *c)
     case IM_QPOP: V.q_pop = (u64 *)p; break;
     case IM_EG: V.eg = (uint2 *)p; break;
     case IM_RK: V.rk = (RankCtl *)p; break;
+    case IM_RDIRTY: V.rdirty = (u32 *)p; break;
     case IM_PRED: V.nd_pred = (u32 *)p; break;
     case IM_CAND: V.nd_cand = (u32 *)p; break;
     case IM_START: V.nd_start = (u32 *)p; break;
@@ -1309,6 +1313,14 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         if (nx == kUnset) { status = EXP_DEADLOCK; now_end = true; break; }
         t = nx;
         if (ab) { now = t; break; }
+    }
+    for (int o = 16; o > 0; o >>= 1) {           // warp totals of the per-lane counters
+        acc.inj += __shfl_xor_sync(kFull, acc.inj, o);
+        acc.hops += __shfl_xor_sync(kFull, acc.hops, o);
+        acc.del += __shfl_xor_sync(kFull, acc.del, o);
+        acc.msg += __shfl_xor_sync(kFull, acc.msg, o);
+        acc.dig += __shfl_xor_sync(kFull, acc.dig, o);
+        acc.emax = max(acc.emax, __shfl_xor_sync(kFull, acc.emax, o));
     }
     if (lane == 0) {
         atomicAdd(&TC.pkts_injected, acc.inj);
