@@ -246,6 +246,19 @@ __device__ __forceinline__ HV make_hv(const XV &S)
     return V;
 }
 
+// How a step sees its experiment: a register copy (HV: fewest reloads, for
+// the latency build) or the block's shared view itself (const XV &: fewest
+// registers, for the occupancy build, whose state reads wait on HBM anyway).
+template <class VT> struct ViewOf;
+template <> struct ViewOf<HV> {
+    __device__ __forceinline__ static HV get(const XV &s) { return make_hv(s); }
+};
+template <> struct ViewOf<const XV &> {
+    __device__ __forceinline__ static const XV &get(const XV &s) { return s; }
+};
+template <int MINB> struct ViewFor { typedef HV T; };
+template <> struct ViewFor<2> { typedef const XV &T; };
+
 // Per-experiment counters while a block holds it; only read after the last
 // tick.  Decisions taken every tick use the per-warp reports instead, which
 // are double-buffered so that one barrier per tick suffices.
@@ -279,7 +292,8 @@ struct SwSmem {
 // reaches the sender at x + D (D = delta + 1 of the link).  At most D - 1
 // pops can still be on their way, so the pop log is only read when the
 // queue is within D - 1 of full.
-__device__ __forceinline__ bool credit_ok(const HV &V, u32 qi, u32 tail, u32 H, u32 D, u32 t)
+template <class VW>
+__device__ __forceinline__ bool credit_ok(const VW &V, u32 qi, u32 tail, u32 H, u32 D, u32 t)
 {
     const u32 cap = V.X.cap;
     if (tail - H + D - 1 < cap) return true;
@@ -294,7 +308,8 @@ __device__ __forceinline__ bool credit_ok(const HV &V, u32 qi, u32 tail, u32 H, 
 }
 
 // ---------------------------------------------------------------- switches
-__device__ __forceinline__ u32 route_port(const HV &V, u32 s, u32 p0, uint4 pk)
+template <class VW>
+__device__ __forceinline__ u32 route_port(const VW &V, u32 s, u32 p0, uint4 pk)
 {
     u8 r = V.route[(u64)s * V.T.nh + pk_dst(pk)];
     if (r != 0xFF) return r;
@@ -311,12 +326,13 @@ __device__ __forceinline__ u32 route_port(const HV &V, u32 s, u32 p0, uint4 pk)
 // switch's pending wake; pokes for other items go to `poke`.  Returns the
 // earliest tick this warp knows of at which something may happen (its own
 // next wake and the wakes it gave other items); *fail gets a failure key.
+template <class VT>
 __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t, u32 old,
                                            u32 *poke, SwSmem *sm, u32 *fail, bool staged)
 {
-    // a register copy of the view: stores through the state pointers cannot
-    // alias it, so its fields are loaded once per tick
-    const HV V = make_hv(Vs);
+    // the view (see ViewOf): as a register copy, stores through the state
+    // pointers cannot alias it, so its fields are loaded once per tick
+    VT V = ViewOf<VT>::get(Vs);
     const u32 lane = threadIdx.x & 31;
     const uint2 sr = V.sw_rec[s];
     const u32 p0 = sr.x, np = sr.y;
@@ -490,9 +506,10 @@ __device__ __forceinline__ void port_set(RankCtl &C, u32 p, bool on)
 }
 
 // Per-rank view used while processing one tick.
-struct RankView {
+template <class VT>
+struct RankViewT {
     const Params *P;
-    HV V;
+    VT V;            // the view: a register copy (HV) or the block's shared view (const XV &)
     Team *TC;
     u32 *poke;          // this step's poke words of the experiment's items
     u32 r, t;
@@ -502,30 +519,43 @@ struct RankView {
     u32 pk_min;         // earliest wake poked into other items
     u32 n_inj, n_del, n_msg, n_done, end_max1;
     u64 dig;
+    __device__ __forceinline__ RankViewT(const Params *p, VT vv) : P(p), V(vv) {}
 };
 
-__device__ __forceinline__ const auto &W_(const RankView &v) { return v.V.W; }
-__device__ __forceinline__ const auto &X_(const RankView &v) { return v.V.X; }
-__device__ __forceinline__ u32 coll_of(const RankView &v, u32 u) { return v.P->node_arg[W_(v).node_off + u]; }
-__device__ __forceinline__ u32 nmemb(const RankView &v, u32 c) { return v.P->coll_nmembers[W_(v).coll_off + c]; }
-__device__ __forceinline__ u32 ckind(const RankView &v, u32 c) { return v.P->coll_kind[W_(v).coll_off + c]; }
-__device__ __forceinline__ u64 cbytes(const RankView &v, u32 c) { return v.P->coll_bytes[W_(v).coll_off + c]; }
-__device__ __forceinline__ u32 mabs(const RankView &v, u32 c, u32 i)
+template <class RV>
+__device__ __forceinline__ const auto &W_(const RV &v) { return v.V.W; }
+template <class RV>
+__device__ __forceinline__ const auto &X_(const RV &v) { return v.V.X; }
+template <class RV>
+__device__ __forceinline__ u32 coll_of(const RV &v, u32 u) { return v.P->node_arg[W_(v).node_off + u]; }
+template <class RV>
+__device__ __forceinline__ u32 nmemb(const RV &v, u32 c) { return v.P->coll_nmembers[W_(v).coll_off + c]; }
+template <class RV>
+__device__ __forceinline__ u32 ckind(const RV &v, u32 c) { return v.P->coll_kind[W_(v).coll_off + c]; }
+template <class RV>
+__device__ __forceinline__ u64 cbytes(const RV &v, u32 c) { return v.P->coll_bytes[W_(v).coll_off + c]; }
+template <class RV>
+__device__ __forceinline__ u32 mabs(const RV &v, u32 c, u32 i)
 {
     return W_(v).memb_off + v.P->coll_mstart[W_(v).coll_off + c] + i;
 }
-__device__ __forceinline__ u32 mrank(const RankView &v, u32 c, u32 i) { return v.P->member_rank[mabs(v, c, i)]; }
-__device__ __forceinline__ u32 mnode(const RankView &v, u32 c, u32 i) { return v.P->member_node[mabs(v, c, i)]; }
-__device__ __forceinline__ bool tree_of(const RankView &v, u32 c)
+template <class RV>
+__device__ __forceinline__ u32 mrank(const RV &v, u32 c, u32 i) { return v.P->member_rank[mabs(v, c, i)]; }
+template <class RV>
+__device__ __forceinline__ u32 mnode(const RV &v, u32 c, u32 i) { return v.P->member_node[mabs(v, c, i)]; }
+template <class RV>
+__device__ __forceinline__ bool tree_of(const RV &v, u32 c)
 {
     return ckind(v, c) == COLL_AR && X_(v).algo == ALGO_TREE;
 }
-__device__ __forceinline__ u32 nchan(const RankView &v, u32 c)
+template <class RV>
+__device__ __forceinline__ u32 nchan(const RV &v, u32 c)
 {
     u32 k = ckind(v, c);
     return (k == COLL_RELAY || k == COLL_P2P) ? 1u : X_(v).nc;
 }
-__device__ __forceinline__ u32 nports_of(const RankView &v, u32 c)
+template <class RV>
+__device__ __forceinline__ u32 nports_of(const RV &v, u32 c)
 {
     u32 k = ckind(v, c);
     if (k == COLL_RELAY || k == COLL_P2P || k == COLL_A2A) return 1;
@@ -534,17 +564,20 @@ __device__ __forceinline__ u32 nports_of(const RankView &v, u32 c)
 // channel c's share of S bytes (AutoCCL section 2.3: NC partitions)
 __device__ __forceinline__ u64 part_bytes(u64 S, u32 nc, u32 c) { return S / nc + (c < S % nc ? 1 : 0); }
 __device__ __forceinline__ u64 nchunks(u64 b, u64 C) { return b == 0 ? 1 : cdiv(b, C); }
-__device__ __forceinline__ u32 ring_steps(const RankView &v, u32 c)
+template <class RV>
+__device__ __forceinline__ u32 ring_steps(const RV &v, u32 c)
 {
     u32 N = nmemb(v, c);
     if (N < 2) return 0;
     return ckind(v, c) == COLL_AR ? 2 * (N - 1) : N - 1;
 }
-__device__ __forceinline__ u64 ring_loops(const RankView &v, u32 c, u64 Pc)
+template <class RV>
+__device__ __forceinline__ u64 ring_loops(const RV &v, u32 c, u64 Pc)
 {
     return Pc == 0 ? 1 : cdiv(Pc, (u64)nmemb(v, c) * X_(v).chunk);
 }
-__device__ __forceinline__ u64 a2a_row_chunks(const RankView &v, u32 c, u32 i)
+template <class RV>
+__device__ __forceinline__ u64 a2a_row_chunks(const RV &v, u32 c, u32 i)
 {
     u32 m = mabs(v, c, i);
     u32 b = W_(v).a2a_off + v.P->memb_row[m], n = v.P->member_a2a_n[m];
@@ -553,7 +586,8 @@ __device__ __forceinline__ u64 a2a_row_chunks(const RankView &v, u32 c, u32 i)
     return tot;
 }
 
-__device__ __forceinline__ u32 lane_count(const RankView &v, u32 c, u32 i, u32 ch, u32 kind)
+template <class RV>
+__device__ __forceinline__ u32 lane_count(const RV &v, u32 c, u32 i, u32 ch, u32 kind)
 {
     u32 N = nmemb(v, c);
     u64 S = cbytes(v, c);
@@ -577,7 +611,8 @@ __device__ __forceinline__ u32 lane_count(const RankView &v, u32 c, u32 i, u32 c
     return 0;
 }
 
-__device__ __forceinline__ u32 port_count_expect(const RankView &v, u32 c, u32 i, u32 p)
+template <class RV>
+__device__ __forceinline__ u32 port_count_expect(const RV &v, u32 c, u32 i, u32 p)
 {
     u32 N = nmemb(v, c);
     u64 S = cbytes(v, c);
@@ -607,7 +642,8 @@ __device__ __forceinline__ u32 port_count_expect(const RankView &v, u32 c, u32 i
 
 // Message L.m of a lane: bytes, destination member and port, and the own
 // receive counts it waits for.  Returns its packet count.
-__device__ __forceinline__ u32 lane_setup(const RankView &v, Lane &L)
+template <class RV>
+__device__ __forceinline__ u32 lane_setup(const RV &v, Lane &L)
 {
     u32 c = coll_of(v, L.node), N = nmemb(v, c), i = L.member, m = L.m, ch = L.chan;
     u64 S = cbytes(v, c), C = X_(v).chunk, bytes = 0;
@@ -685,7 +721,8 @@ __device__ __forceinline__ u32 lane_setup(const RankView &v, Lane &L)
     return (u32)(bytes == 0 ? 1 : cdiv(bytes, X_(v).pkt));
 }
 
-__device__ __forceinline__ u32 compute_ticks(const RankView &v, u32 u)
+template <class RV>
+__device__ __forceinline__ u32 compute_ticks(const RV &v, u32 u)
 {
     const Params &P = *v.P;
     const u32 g = W_(v).node_off + u;
@@ -695,7 +732,8 @@ __device__ __forceinline__ u32 compute_ticks(const RankView &v, u32 u)
 }
 
 // alpha + bytes/beta (Multiverse section 4.1), beta as ticks per byte
-__device__ __forceinline__ u32 intra_ticks(const RankView &v, u32 c)
+template <class RV>
+__device__ __forceinline__ u32 intra_ticks(const RV &v, u32 c)
 {
     const Params &P = *v.P;
     u32 cc = W_(v).coll_off + c;
@@ -708,9 +746,11 @@ __device__ __forceinline__ u32 intra_ticks(const RankView &v, u32 c)
     return P.coll_alpha[cc] + (u32)cdiv(be * P.coll_beta_num[cc], P.coll_beta_den[cc]);
 }
 
-__device__ __forceinline__ u32 rank_item(const HV &V, u32 r) { return V.X.nsw + r / 32; }
+template <class VW>
+__device__ __forceinline__ u32 rank_item(const VW &V, u32 r) { return V.X.nsw + r / 32; }
 
-__device__ __forceinline__ void rank_poke(RankView &v, u32 item, u32 at)
+template <class RV>
+__device__ __forceinline__ void rank_poke(RV &v, u32 item, u32 at)
 {
     atomicMin(&v.poke[item], at);
     v.pk_min = min(v.pk_min, at);
@@ -719,7 +759,8 @@ __device__ __forceinline__ void rank_poke(RankView &v, u32 item, u32 at)
 // A member joined collective c at this tick: members waiting on its start
 // look again when the join reaches them (intra-server barrier: next tick;
 // network rendezvous: 1 + min(delta) ticks later).
-__device__ __forceinline__ void poke_members(RankView &v, u32 c, u32 at)
+template <class RV>
+__device__ __forceinline__ void poke_members(RV &v, u32 c, u32 at)
 {
     u32 N = nmemb(v, c), last = kUnset;
     for (u32 m = 0; m < N; m++) {
@@ -731,7 +772,8 @@ __device__ __forceinline__ void poke_members(RankView &v, u32 c, u32 at)
 
 // The pending list is kept sorted by (start tick, node): the nodes due at a
 // tick are its prefix, already in node order.
-__device__ __forceinline__ void pend_add(RankView &v, u32 u, u32 st)
+template <class RV>
+__device__ __forceinline__ void pend_add(RV &v, u32 u, u32 st)
 {
     if (v.C.npend >= X_(v).pend_cap) { v.fail_over = true; return; }
     uint2 *pd = v.V.pend + (u64)v.r * X_(v).pend_cap;
@@ -745,10 +787,11 @@ __device__ __forceinline__ void pend_add(RankView &v, u32 u, u32 st)
     pd[j] = make_uint2(u, st);
 }
 
-__device__ __forceinline__ void complete_node(RankView &v, u32 u, u32 c)
+template <class RV>
+__device__ __forceinline__ void complete_node(RV &v, u32 u, u32 c)
 {
     const Params &P = *v.P;
-    const HV &V = v.V;
+    const auto &V = v.V;
     V.nd_end[u] = c;
     v.n_done++;
     v.end_max1 = max(v.end_max1, c + 1);
@@ -765,17 +808,19 @@ __device__ __forceinline__ void complete_node(RankView &v, u32 u, u32 c)
     }
 }
 
-__device__ __forceinline__ void free_ports(RankView &v, u32 u)
+template <class RV>
+__device__ __forceinline__ void free_ports(RV &v, u32 u)
 {
     u32 np = nports_of(v, coll_of(v, u)), b = v.V.nd_pbase[u];
     for (u32 p = b; p < b + np; p++) port_set(v.C, p, false);
 }
 
 // A rank joins a network collective: receive counters, then send lanes.
-__device__ __forceinline__ bool net_join(RankView &v, u32 u)
+template <class RV>
+__device__ __forceinline__ bool net_join(RV &v, u32 u)
 {
     const Params &P = *v.P;
-    const HV &V = v.V;
+    const auto &V = v.V;
     const auto &X = V.X;
     u32 c = coll_of(v, u), i = P.node_member[W_(v).node_off + u];
     u32 np = nports_of(v, c);
@@ -825,7 +870,8 @@ __device__ __forceinline__ bool net_join(RankView &v, u32 u)
 // Running memberships in ascending node order; bit 31 marks an intra-server
 // (analytic) one.
 constexpr u32 kActIntra = 0x80000000u;
-__device__ __forceinline__ void act_add(RankView &v, u32 u, u32 flag)
+template <class RV>
+__device__ __forceinline__ void act_add(RV &v, u32 u, u32 flag)
 {
     if (v.C.nact >= X_(v).act_cap) { v.fail_over = true; return; }
     u32 *a = v.V.act + (u64)v.r * X_(v).act_cap;
@@ -838,9 +884,10 @@ __device__ __forceinline__ void act_add(RankView &v, u32 u, u32 flag)
 
 // Schedule + AnalyticalSys: finish running memberships, then start the nodes
 // scheduled for this tick (both in node order).
-__device__ __forceinline__ void dag_step(RankView &v)
+template <class RV>
+__device__ __forceinline__ void dag_step(RV &v)
 {
-    const HV &V = v.V;
+    const auto &V = v.V;
     const u32 t = v.t;
     uint2 *pd = V.pend + (u64)v.r * V.X.pend_cap;
     if (v.C.nact == 0 && (v.C.npend == 0 || pd[0].y > t)) {      // nothing running or due
@@ -921,9 +968,10 @@ __device__ __forceinline__ void dag_step(RankView &v)
 // dependencies are met and its destination joined before this tick.
 // hr: the host's uplink record (queue, sigma, delta, switch); pw / tail:
 // that queue's pop word and push count, loaded at the start of the tick.
-__device__ __forceinline__ void inject(RankView &v, uint4 hr, u64 pw, u32 tail)
+template <class RV>
+__device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
 {
-    const HV &V = v.V;
+    const auto &V = v.V;
     const auto &X = V.X;
     const u32 t = v.t;
     if (!v.C.lane_mask || v.C.blocked) return;
@@ -996,10 +1044,11 @@ __device__ __forceinline__ void inject(RankView &v, uint4 hr, u64 pw, u32 tail)
 // sender, sum over hops of (delta + 1) ticks later.
 // ql / head / tail: the downlink queue and its start-of-tick counters; pk:
 // its head packet (loaded at the start of the tick when the queue held one).
-__device__ __forceinline__ void receive(RankView &v, u32 ql, u32 head, u32 tail, uint4 pk)
+template <class RV>
+__device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4 pk)
 {
     const Params &P = *v.P;
-    const HV &V = v.V;
+    const auto &V = v.V;
     const auto &X = V.X;
     const u32 t = v.t;
     if (head == tail) return;
@@ -1043,13 +1092,15 @@ __device__ __forceinline__ void receive(RankView &v, u32 ql, u32 head, u32 tail,
 // pending wake; pokes for other items go to `poke`.  Returns the warp's
 // earliest known next event; *done / *fail receive nodes completed and the
 // failure key.
+template <class VT>
 __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC, Acc &acc, u32 g,
                                          u32 t, u32 old, u32 *poke, u32 *done_out, u32 *fail)
 {
     const u32 lane = threadIdx.x & 31;
-    RankView v;
-    v.P = &P; v.V = make_hv(Vs); v.TC = &TC; v.poke = poke;    // register copy (see switch_tick)
-    const HV &V = v.V;
+    RankViewT<VT> v(&P, ViewOf<VT>::get(Vs));     // the view (see ViewOf)
+    v.TC = &TC;
+    v.poke = poke;
+    const auto &V = v.V;
     const u32 it = V.X.nsw + g;
     v.r = g * 32 + lane; v.t = t;
     v.changed = v.fail_over = v.fail_err = false;
@@ -1188,6 +1239,7 @@ __shared__ u32 s_slot;
 
 // Step experiment e from its clock until it finishes, stops, or reaches the
 // run's tick budget; `img` is this block's shared-memory image space.
+template <class VT>
 __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSmem *sm,
                                u64 t_start)
 {
@@ -1280,8 +1332,8 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                 M &= M - 1;
                 const u32 item = warp + (base + j) * nW;
                 const u32 old = __shfl_sync(kFull, w, j);
-                u32 r = item < nsw ? switch_tick(V, acc, item, t, old, poke, sm, &fail, full)
-                                   : rank_tick(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail);
+                u32 r = item < nsw ? switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, full)
+                                   : rank_tick<VT>(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail);
                 rep = min(rep, r);
             }
         }
@@ -1373,7 +1425,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, MINB) k_megakernel(Params P)
         const u32 slot = s_slot;
         __syncthreads();
         if (slot >= P.n_exps) break;
-        run_experiment(P, P.order[slot], img, sw + warp, t_start);
+        run_experiment<typename ViewFor<MINB>::T>(P, P.order[slot], img, sw + warp, t_start);
     }
 }
 
