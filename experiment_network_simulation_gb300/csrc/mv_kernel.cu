@@ -256,6 +256,8 @@ template <> struct ViewOf<HV> {
 template <> struct ViewOf<const XV &> {
     __device__ __forceinline__ static const XV &get(const XV &s) { return s; }
 };
+template <class VT> struct kOnePerPass { static constexpr bool value = false; };
+template <> struct kOnePerPass<HV> { static constexpr bool value = true; };
 template <int MINB> struct ViewFor { typedef HV T; };
 template <> struct ViewFor<2> { typedef const XV &T; };
 
@@ -280,10 +282,16 @@ struct Acc {
 __device__ __forceinline__ u32 fail_key_rank(u32 r, u32 code) { return (r << 3) | code; }
 constexpr u32 kFailSwitch = 0xF0000000u | EXP_ERROR;
 
+// Per-warp scratch of one forwarding pass.  A pass handles a pack of up to
+// kPack switches laid side by side over the 64 port positions (a lane has
+// positions lane and lane + 32): switch k of the pack owns positions
+// [base[k], base[k] + np[k]).
+constexpr u32 kPack = 4;
 struct SwSmem {
     uint4 pkt[kMaxPorts];
     unsigned long long mask[kMaxPorts];
     u32 head[kMaxPorts];
+    u32 sw[kPack], base[kPack], np[kPack], p0[kPack], old[kPack], nxt[kPack];
 };
 
 // ---------------------------------------------------------------- credit
@@ -319,7 +327,149 @@ __device__ __forceinline__ u32 route_port(const VW &V, u32 s, u32 p0, uint4 pk)
     return V.up_list[p0 + (u32)(h % nup)];
 }
 
-// Forwarding at switch s for one tick (Multiverse section 4.2): each lane
+// Forwarding for one tick (Multiverse section 4.2) at the n switches of a
+// pack (sm->sw/base/np/p0/old): each lane plans its ingress positions (the
+// egress their ready head packet needs), then each lane pulls for its egress
+// positions: free link, credit downstream, first planned ingress at or after
+// the round-robin pointer.  Switches of a pack share nothing but the pass,
+// so their steps are independent.  Pokes for other items go to `poke`.
+// Returns the earliest tick this warp knows of at which something may happen
+// (the switches' own next wakes and the wakes they gave other items); *fail
+// gets a failure key.
+template <class VT>
+__device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t, u32 *poke,
+                                           SwSmem *sm, u32 *fail, bool staged)
+{
+    // the view (see ViewOf): as a register copy, stores through the state
+    // pointers cannot alias it, so its fields are loaded once per tick
+    VT V = ViewOf<VT>::get(Vs);
+    const u32 lane = threadIdx.x & 31;
+    const u32 cap = V.X.cap, pm = V.plog - 1;
+    // segment bounds (warp-uniform): position p belongs to switch k when
+    // base[k] <= p < base[k] + np[k]
+    const u32 b1 = n > 1 ? sm->base[1] : 64u, b2 = n > 2 ? sm->base[2] : 64u,
+              b3 = n > 3 ? sm->base[3] : 64u;
+    const u32 end = sm->base[n - 1] + sm->np[n - 1];
+    u32 seg_[2], lp_[2], np_[2], q_[2];
+    u32 pk_min = kUnset;                // earliest tick poked into a downstream item
+    bool bad = false;
+    u32 tail_[2] = {0, 0}, head_[2] = {0, 0}, dhead_[2] = {0, 0}, dtail_[2] = {0, 0};
+    uint2 st_[2] = {make_uint2(kUnset, 0), make_uint2(kUnset, 0)};
+    uint4 pr_[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    // Issue the independent loads together: per position its ingress queue
+    // words, its egress state and record.
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        const u32 p = lane + 32 * j;
+        const u32 k = (p >= b1) + (p >= b2) + (p >= b3);
+        seg_[j] = k;
+        lp_[j] = p - sm->base[k];
+        np_[j] = sm->np[k];
+        q_[j] = sm->p0[k] + lp_[j];
+        if (p >= end || lp_[j] >= np_[j]) { seg_[j] = kUnset; continue; }
+        const u32 qi = q_[j];
+        const u64 pw = ld_vol64(&V.q_push[qi]);
+        tail_[j] = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
+        head_[j] = (u32)V.q_pop[qi];
+        st_[j] = V.eg[qi];
+        pr_[j] = V.port_rec[qi];
+    }
+    // in shared memory these are cheap, so every free egress gets them now;
+    // in global memory only egresses that a packet wants load them (below)
+    if (staged) {
+#pragma unroll
+        for (u32 j = 0; j < 2; j++) {
+            if (seg_[j] == kUnset || st_[j].x > t) continue;
+            const u32 dq = pr_[j].x;
+            const u64 dpop = ld_vol64(&V.q_pop[dq]);
+            dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
+            dtail_[j] = (u32)V.q_push[dq];
+        }
+    }
+    sm->mask[lane] = 0;
+    sm->mask[lane + 32] = 0;
+    if (lane < kPack) sm->nxt[lane] = kUnset;
+    __syncwarp();
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        const u32 p = lane + 32 * j, k = seg_[j];
+        if (k == kUnset) continue;
+        const u32 head = head_[j];
+        sm->head[p] = head;
+        if (head == tail_[j]) continue;
+        const uint4 pk = V.slots[(u64)q_[j] * cap + head % cap];
+        if (pk.x > t) { atomicMin(&sm->nxt[k], pk.x); continue; }
+        atomicMin(&sm->nxt[k], t + 1);  // a ready head: left or blocked, look again next tick
+        const u32 tg = route_port(V, sm->sw[k], sm->p0[k], pk);
+        if (tg >= np_[j]) { bad = true; continue; }
+        sm->pkt[p] = pk;
+        atomicOr(&sm->mask[sm->base[k] + tg], 1ull << p);
+    }
+    __syncwarp();
+    unsigned long long popped = 0;
+    u32 hops = 0;
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        const u32 p = lane + 32 * j, k = seg_[j];
+        if (k == kUnset) continue;
+        const unsigned long long M = sm->mask[p];
+        if (!M) continue;
+        const uint2 st = st_[j];
+        if (st.x > t) continue;             // busy: its heads wake the switch at t+1
+        const uint4 pr = pr_[j];            // downstream queue, sigma, delta, its owner
+        const u32 dq = pr.x, sg = pr.y, dl = pr.z;
+        if (!staged) {
+            const u64 dpop = ld_vol64(&V.q_pop[dq]);
+            dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
+            dtail_[j] = (u32)V.q_push[dq];
+        }
+        const u32 dtail = dtail_[j];
+        if (!credit_ok(V, dq, dtail, dhead_[j], dl + 1, t)) continue;
+        const u32 base = sm->base[k], np = np_[j];
+        const unsigned long long hi = M & (~0ull << (base + st.y));   // round robin from rr
+        const u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;      // a position
+        uint4 pk = sm->pkt[i];
+        pk.x = t + sg + dl;
+        pk.y += (dl + 1) << 16;
+        V.slots[(u64)dq * cap + dtail % cap] = pk;
+        st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
+        V.eg[q_[j]] = make_uint2(t + sg, i - base + 1 == np ? 0u : i - base + 1);
+        // the queue's owner: the peer switch, or the rank group of the host
+        if (!(pr.w & 0x80000000u)) atomicMin(&poke[pr.w], pk.x);
+        else if ((pr.w & 0x7FFFFFFFu) < V.X.nr) atomicMin(&poke[V.X.nsw + (pr.w & 0x7FFFFFFFu) / 32], pk.x);
+        pk_min = min(pk_min, pk.x);
+        popped |= 1ull << i;
+        hops++;
+    }
+    u32 lo = __reduce_or_sync(kFull, (u32)popped);
+    u32 hi32 = __reduce_or_sync(kFull, (u32)(popped >> 32));
+    unsigned long long all = ((unsigned long long)hi32 << 32) | lo;
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        const u32 p = lane + 32 * j;
+        if (seg_[j] != kUnset && ((all >> p) & 1ull)) {
+            const u32 qi = q_[j];
+            st_vol32(&V.poplog[(u64)qi * V.plog + (sm->head[p] & pm)], t);
+            st_vol64(&V.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
+        }
+    }
+    acc.hops += hops;                   // per lane; summed over the warp once per experiment
+    if (__any_sync(kFull, bad)) *fail = min(*fail, kFailSwitch);
+    __syncwarp();                       // sm->nxt complete
+    u32 w = kUnset;
+    if (lane < n) {                     // each switch's own next wake
+        const u32 old = sm->old[lane];
+        w = min(sm->nxt[lane], old > t ? old : kUnset);
+        V.wake[sm->sw[lane]] = w;
+    }
+    const u32 r = __reduce_min_sync(kFull, min(w, pk_min));
+    __syncwarp();
+    return r;
+}
+
+// One switch for one tick (the latency build's form of switch_pack, with
+// register reductions instead of the pack table).  Forwarding at switch s
+// for one tick (Multiverse section 4.2): each lane
 // plans its ingress ports (the egress their ready head packet needs), then
 // each lane pulls for its egress ports: free link, credit downstream, first
 // planned ingress at or after the round-robin pointer.  `old` is the
@@ -1326,15 +1476,53 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
             }
             const bool due = w <= t;
             rep = min(rep, due ? kUnset : w);
-            u32 M = __ballot_sync(kFull, due);
-            while (M) {
-                const u32 j = (u32)__ffs(M) - 1;
-                M &= M - 1;
+            // due switches: the latency build steps them one a pass; the
+            // occupancy build packs up to kPack switches and 64 ports a pass
+            const bool dsw = due && it < nsw;
+            if (kOnePerPass<VT>::value) {
+                u32 Ms1 = __ballot_sync(kFull, dsw);
+                while (Ms1) {
+                    const u32 j = (u32)__ffs(Ms1) - 1;
+                    Ms1 &= Ms1 - 1;
+                    const u32 item = warp + (base + j) * nW;
+                    const u32 old = __shfl_sync(kFull, w, j);
+                    rep = min(rep, switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, full));
+                }
+            }
+            uint2 sr = make_uint2(0, 0);
+            if (dsw && !kOnePerPass<VT>::value) sr = V.sw_rec[it];
+            u32 Ms = kOnePerPass<VT>::value ? 0u : __ballot_sync(kFull, dsw);
+            u32 n = 0, used = 0;
+            while (Ms) {
+                const u32 j = (u32)__ffs(Ms) - 1;
+                Ms &= Ms - 1;
+                const u32 np = __shfl_sync(kFull, sr.y, j), p0 = __shfl_sync(kFull, sr.x, j);
+                const u32 old = __shfl_sync(kFull, w, j);
+                if (n == kPack || used + np > kMaxPorts) {
+                    rep = min(rep, switch_pack<VT>(V, acc, n, t, poke, sm, &fail, full));
+                    n = 0;
+                    used = 0;
+                }
+                if (lane == 0) {
+                    sm->sw[n] = warp + (base + j) * nW;
+                    sm->base[n] = used;
+                    sm->np[n] = np;
+                    sm->p0[n] = p0;
+                    sm->old[n] = old;
+                }
+                __syncwarp();
+                n++;
+                used += np;
+            }
+            if (n) rep = min(rep, switch_pack<VT>(V, acc, n, t, poke, sm, &fail, full));
+            // due rank groups, one a pass
+            u32 Mr = __ballot_sync(kFull, due && it >= nsw);
+            while (Mr) {
+                const u32 j = (u32)__ffs(Mr) - 1;
+                Mr &= Mr - 1;
                 const u32 item = warp + (base + j) * nW;
                 const u32 old = __shfl_sync(kFull, w, j);
-                u32 r = item < nsw ? switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, full)
-                                   : rank_tick<VT>(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail);
-                rep = min(rep, r);
+                rep = min(rep, rank_tick<VT>(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail));
             }
         }
         rep = __reduce_min_sync(kFull, rep);
