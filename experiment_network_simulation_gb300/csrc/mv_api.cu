@@ -25,6 +25,9 @@ struct Region {
 // Largest shared-memory image of one experiment's dynamic state; larger
 // experiments keep their state in global memory (wake table still staged).
 constexpr u64 kStageMax = 112 * 1024;
+// Shared-memory image budget when some experiment does not fit whole: what
+// is left for one of two blocks an SM after the per-warp scratch.
+constexpr u32 kPartialImage = 88 * 1024;
 
 // Byte layout of the workspace: a static part uploaded from the host, then
 // a dynamic part cleared and filled by the set-up kernels.
@@ -402,6 +405,11 @@ int plan(const mv_batch_desc *d, Layout &L)
     for (u32 e = 0; e < L.E; e++)
         if (!L.exp[e].stage_bytes) L.variant = 2;
     L.image = (u32)std::min<u64>(std::max(full_max, wake_max), kStageMax);
+    // experiments that do not fit whole stage their hottest arrays in what
+    // two blocks an SM leave of shared memory
+    bool partial = false;
+    for (u32 e = 0; e < L.E; e++) partial |= L.exp[e].stage_bytes == 0;
+    if (partial) L.image = kPartialImage;
     L.order.resize(L.E);
     std::iota(L.order.begin(), L.order.end(), 0u);
     std::stable_sort(L.order.begin(), L.order.end(), [&](u32 a, u32 b) {

@@ -1381,6 +1381,13 @@ __device__ void set_slice(XV &V, int k, const void *c)
     }
 }
 
+// Arrays staged for an experiment that does not fit whole, most useful
+// first: the per-item wake table, per-switch records, per-rank dirty words,
+// the queue words, per-host records, egress state, the up lists.
+__constant__ int kStagePrio[] = {IM_WAKE, IM_SWREC, IM_UPN, IM_RDIRTY, IM_QPUSH, IM_QPOP,
+                                 IM_HOSTREC, IM_EG, IM_UPLIST, IM_RK, IM_PORTREC, IM_ACT};
+constexpr int kNStagePrio = 12;
+
 __shared__ XV s_V;
 __shared__ Team s_TC;
 __shared__ u64 s_off[IM_N];
@@ -1413,20 +1420,34 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         TC.pkts_delivered = c.pkts_delivered;
         TC.msgs_delivered = c.msgs_delivered;
         TC.digest = c.digest;
-        image_layout(V.X, V.T, s_off);
         image_bytes(V.X, V.T, s_sz);
-        // what goes to shared memory: the whole image, the wake table, or nothing
-        u32 n_staged = 0;
-        if (P.stage_mode == 0 && V.X.stage_bytes && V.X.stage_bytes <= P.stage_limit) n_staged = IM_N;
-        else if (P.stage_mode <= 1 && im_round(s_sz[IM_WAKE]) <= P.stage_limit) n_staged = 1;
-        V.staged = n_staged;
+        // What goes to shared memory: the whole image when it fits; else the
+        // arrays of kStagePrio in that order while the budget lasts (mode 0),
+        // the wake table alone (mode 1), or nothing (mode 2).
+        u32 mask = 0;
+        if (P.stage_mode == 0 && V.X.stage_bytes && V.X.stage_bytes <= P.stage_limit) {
+            image_layout(V.X, V.T, s_off);
+            mask = (1u << IM_N) - 1;
+        } else if (P.stage_mode <= 1) {
+            u64 used = 0;
+            for (int i = 0; i < kNStagePrio && (P.stage_mode == 0 || i == 0); i++) {
+                const int k = kStagePrio[i];
+                const u64 b = im_round(s_sz[k]);
+                if (used + b > P.stage_limit) continue;
+                s_off[k] = used;
+                used += b;
+                mask |= 1u << k;
+            }
+        }
+        V.staged = mask;
         for (int k = 0; k < IM_N; k++)
-            set_slice(V, k, k < (int)n_staged ? (const void *)(img + s_off[k])
+            set_slice(V, k, ((mask >> k) & 1) ? (const void *)(img + s_off[k])
                                               : global_slice(P, V.X, V.T, k));
     }
     __syncthreads();
-    const u32 n_staged = V.staged;
-    for (int k = 0; k < (int)n_staged; k++) block_copy(img + s_off[k], global_slice(P, V.X, V.T, k), s_sz[k]);
+    const u32 smask = V.staged;
+    for (int k = 0; k < IM_N; k++)
+        if ((smask >> k) & 1) block_copy(img + s_off[k], global_slice(P, V.X, V.T, k), s_sz[k]);
     __syncthreads();
 
     u32 t = TC.now0, status = TC.status0, left = TC.left0, now = TC.now0;
@@ -1438,7 +1459,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         now = TC.end_max1;
     }
     const u32 nI = V.X.n_items, nsw = V.X.nsw;
-    const bool full = n_staged == IM_N;        // the whole state is in shared memory
+    const bool full = smask == (1u << IM_N) - 1;   // the whole state is in shared memory
     // items are dealt to warps round-robin (item warp + j * nW), so switches
     // and rank groups spread over all warps
     const u32 cnt = warp < nI ? (nI - warp + nW - 1) / nW : 0;
@@ -1572,8 +1593,9 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
     if (lane == 0 && acc.emax) atomicMax(&TC.end_max1, acc.emax);
     __syncthreads();
     if (now_end) now = TC.end_max1;
-    for (int k2 = 0; k2 < (int)n_staged && k2 < IM_NDYN; k2++)
-        block_copy(const_cast<void *>(global_slice(P, V.X, V.T, k2)), img + s_off[k2], s_sz[k2]);
+    for (int k2 = 0; k2 < IM_NDYN; k2++)            // dynamic arrays back to global memory
+        if ((smask >> k2) & 1)
+            block_copy(const_cast<void *>(global_slice(P, V.X, V.T, k2)), img + s_off[k2], s_sz[k2]);
     if (threadIdx.x == 0) {
         ExpCtl c;
         c.status = status;
