@@ -37,6 +37,12 @@ __device__ __forceinline__ u64 mix64(u64 z)
     return z ^ (z >> 31);
 }
 __device__ __forceinline__ u64 cdiv(u64 a, u64 b) { return (a + b - 1) / b; }
+// ring-buffer slot of counter x in a queue of cap slots (a mask when cap is
+// a power of two, as in every configured batch)
+__device__ __forceinline__ u32 slot_ix(u32 x, u32 cap)
+{
+    return (cap & (cap - 1)) == 0 ? (x & (cap - 1)) : x % cap;
+}
 
 // State shared between warps of the block may sit in shared or in global
 // memory, so these accessors use generic addresses.  Volatile accesses keep
@@ -397,7 +403,7 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         const u32 head = head_[j];
         sm->head[p] = head;
         if (head == tail_[j]) continue;
-        const uint4 pk = V.slots[(u64)q_[j] * cap + head % cap];
+        const uint4 pk = V.slots[(u64)q_[j] * cap + slot_ix(head, cap)];
         if (pk.x > t) { atomicMin(&sm->nxt[k], pk.x); continue; }
         atomicMin(&sm->nxt[k], t + 1);  // a ready head: left or blocked, look again next tick
         const u32 tg = route_port(V, sm->sw[k], sm->p0[k], pk);
@@ -406,7 +412,6 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         atomicOr(&sm->mask[sm->base[k] + tg], 1ull << p);
     }
     __syncwarp();
-    unsigned long long popped = 0;
     u32 hops = 0;
 #pragma unroll
     for (u32 j = 0; j < 2; j++) {
@@ -431,27 +436,18 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         uint4 pk = sm->pkt[i];
         pk.x = t + sg + dl;
         pk.y += (dl + 1) << 16;
-        V.slots[(u64)dq * cap + dtail % cap] = pk;
+        V.slots[(u64)dq * cap + slot_ix(dtail, cap)] = pk;
         st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
         V.eg[q_[j]] = make_uint2(t + sg, i - base + 1 == np ? 0u : i - base + 1);
+        // pop the ingress this egress took (an ingress head wants one egress)
+        const u32 qin = sm->p0[k] + (i - base), hd = sm->head[i];
+        st_vol32(&V.poplog[(u64)qin * V.plog + (hd & pm)], t);
+        st_vol64(&V.q_pop[qin], ((u64)t << 32) | (u32)(hd + 1));
         // the queue's owner: the peer switch, or the rank group of the host
         if (!(pr.w & 0x80000000u)) atomicMin(&poke[pr.w], pk.x);
         else if ((pr.w & 0x7FFFFFFFu) < V.X.nr) atomicMin(&poke[V.X.nsw + (pr.w & 0x7FFFFFFFu) / 32], pk.x);
         pk_min = min(pk_min, pk.x);
-        popped |= 1ull << i;
         hops++;
-    }
-    u32 lo = __reduce_or_sync(kFull, (u32)popped);
-    u32 hi32 = __reduce_or_sync(kFull, (u32)(popped >> 32));
-    unsigned long long all = ((unsigned long long)hi32 << 32) | lo;
-#pragma unroll
-    for (u32 j = 0; j < 2; j++) {
-        const u32 p = lane + 32 * j;
-        if (seg_[j] != kUnset && ((all >> p) & 1ull)) {
-            const u32 qi = q_[j];
-            st_vol32(&V.poplog[(u64)qi * V.plog + (sm->head[p] & pm)], t);
-            st_vol64(&V.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
-        }
     }
     acc.hops += hops;                   // per lane; summed over the warp once per experiment
     if (__any_sync(kFull, bad)) *fail = min(*fail, kFailSwitch);
@@ -530,7 +526,7 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         const u32 qi = p0 + p, head = head_[j];
         sm->head[p] = head;
         if (head == tail_[j]) continue;
-        uint4 pk = V.slots[(u64)qi * cap + head % cap];
+        uint4 pk = V.slots[(u64)qi * cap + slot_ix(head, cap)];
         if (pk.x > t) { nxt = min(nxt, pk.x); continue; }
         ready_any = true;
         u32 tg = route_port(V, s, p0, pk);
@@ -539,7 +535,6 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         atomicOr(&sm->mask[tg], 1ull << p);
     }
     __syncwarp();
-    unsigned long long popped = 0;
     u32 hops = 0;
 #pragma unroll
     for (u32 j = 0; j < 2; j++) {
@@ -563,27 +558,18 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         uint4 pk = sm->pkt[i];
         pk.x = t + sg + dl;
         pk.y += (dl + 1) << 16;
-        V.slots[(u64)dq * cap + dtail % cap] = pk;
+        V.slots[(u64)dq * cap + slot_ix(dtail, cap)] = pk;
         st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
         V.eg[p0 + eg] = make_uint2(t + sg, i + 1 == np ? 0u : i + 1);
+        // pop the ingress this egress took (an ingress head wants one egress)
+        const u32 hd = sm->head[i];
+        st_vol32(&V.poplog[(u64)(p0 + i) * V.plog + (hd & pm)], t);
+        st_vol64(&V.q_pop[p0 + i], ((u64)t << 32) | (u32)(hd + 1));
         // the queue's owner: the peer switch, or the rank group of the host
         if (!(pr.w & 0x80000000u)) atomicMin(&poke[pr.w], pk.x);
         else if ((pr.w & 0x7FFFFFFFu) < V.X.nr) atomicMin(&poke[V.X.nsw + (pr.w & 0x7FFFFFFFu) / 32], pk.x);
         pk_min = min(pk_min, pk.x);
-        popped |= 1ull << i;
         hops++;
-    }
-    u32 lo = __reduce_or_sync(kFull, (u32)popped);
-    u32 hi32 = __reduce_or_sync(kFull, (u32)(popped >> 32));
-    unsigned long long all = ((unsigned long long)hi32 << 32) | lo;
-#pragma unroll
-    for (u32 j = 0; j < 2; j++) {
-        u32 p = lane + 32 * j;
-        if (p < np && ((all >> p) & 1ull)) {
-            u32 qi = p0 + p;
-            st_vol32(&V.poplog[(u64)qi * V.plog + (sm->head[p] & pm)], t);
-            st_vol64(&V.q_pop[qi], ((u64)t << 32) | (u32)(sm->head[p] + 1));
-        }
     }
     acc.hops += hops;                   // per lane; summed over the warp once per experiment
     nxt = __reduce_min_sync(kFull, ready_any ? t + 1 : nxt);   // heads left or blocked: next tick
@@ -1168,7 +1154,7 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
             pk.y = L.drank | ((hd + 1) << 16);
             pk.z = L.node;
             pk.w = L.key | ((L.pkts_left == 1 ? 1u : 0u) << 24) | (L.dslot << 25);
-            V.slots[(u64)qp * X.cap + tail % X.cap] = pk;
+            V.slots[(u64)qp * X.cap + slot_ix(tail, X.cap)] = pk;
             st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
             v.C.busy = t + hs;
             v.C.rr = (l + 1) % kNLane;
@@ -1271,7 +1257,7 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
         const u64 up_pop = ld_vol64(&V.q_pop[hr.x]);
         const u32 up_tail = (u32)V.q_push[hr.x];
         uint4 rx_pk = make_uint4(kUnset, 0, 0, 0);
-        if (rx_head != rx_tail) rx_pk = V.slots[(u64)ql * V.X.cap + rx_head % V.X.cap];
+        if (rx_head != rx_tail) rx_pk = V.slots[(u64)ql * V.X.cap + slot_ix(rx_head, V.X.cap)];
         dag_step(v);
         if (!v.fail_over && !v.fail_err) {
             inject(v, hr, up_pop, up_tail);
