@@ -40,9 +40,9 @@ UNIT = "packet-hops/s"
 # downstream queue and reads it back out (32 B); each packet also costs a
 # sender flow-state read-modify-write (16 B) and a receiver update (8 B).
 BYTES_PER_HOP, BYTES_PER_PKT = 32, 24
-# DRAM bytes (read + write) of one megakernel launch from an ncu capture of
-# the same workload (see profiles/); None until captured for this kernel.
-TRAFFIC = {}
+# DRAM bytes (read + write) of one megakernel launch of the whole-run
+# workload, from an ncu capture of the current kernel (see profiles/).
+TRAFFIC = {"config2": 6718976}
 
 WORKLOADS = {
     "config1": (lambda seed: I.config1(),
