@@ -28,6 +28,8 @@ constexpr u64 kStageMax = 112 * 1024;
 // Shared-memory image budget when some experiment does not fit whole: what
 // is left for one of two blocks an SM after the per-warp scratch.
 constexpr u32 kPartialImage = 88 * 1024;
+// ... and for the build with one 16-warp block an SM
+constexpr u32 kPartialImage3 = 192 * 1024;
 
 // Byte layout of the workspace: a static part uploaded from the host, then
 // a dynamic part cleared and filled by the set-up kernels.
@@ -400,16 +402,32 @@ int plan(const mv_batch_desc *d, Layout &L)
         if (L.nd_total > 0xFFFFFFFFull * 4 || items > 0xFFFFFFFFull) return MV_EOVERFLOW;
     }
     L.items = items;
-    L.warps = std::min<u32>(kMaxWarps, max_items);
+    L.warps = std::min<u32>(8, max_items);
+    // Build: 1 when every experiment fits in shared memory whole; else 2
+    // (two 8-warp blocks an SM) when the hottest arrays of the largest
+    // experiment fit its budget, 3 (one 16-warp block an SM, twice the
+    // shared memory a block) when they do not.
     L.variant = 1;
-    for (u32 e = 0; e < L.E; e++)
-        if (!L.exp[e].stage_bytes) L.variant = 2;
+    u64 hot_max = 0;
+    for (u32 e = 0; e < L.E; e++) {
+        const ExpRec &X = L.exp[e];
+        if (X.stage_bytes) continue;
+        L.variant = 2;
+        u64 sz[IM_N];
+        image_bytes(X, L.topo[X.topo], sz);
+        u64 hot = 0;
+        for (int k : {IM_WAKE, IM_SWREC, IM_UPN, IM_RDIRTY, IM_QPUSH, IM_QPOP, IM_HOSTREC, IM_EG,
+                      IM_UPLIST})
+            hot += im_round(sz[k]);
+        hot_max = std::max(hot_max, hot);
+    }
+    if (L.variant == 2 && hot_max > kPartialImage) L.variant = 3;
     L.image = (u32)std::min<u64>(std::max(full_max, wake_max), kStageMax);
     // experiments that do not fit whole stage their hottest arrays in what
     // two blocks an SM leave of shared memory
     bool partial = false;
     for (u32 e = 0; e < L.E; e++) partial |= L.exp[e].stage_bytes == 0;
-    if (partial) L.image = kPartialImage;
+    if (partial) L.image = kPartialImage;      // build 2's budget; build 3 widens it
     L.order.resize(L.E);
     std::iota(L.order.begin(), L.order.end(), 0u);
     std::stable_sort(L.order.begin(), L.order.end(), [&](u32 a, u32 b) {
@@ -752,14 +770,22 @@ int mv_run_ex(mv_ctx *c, uint32_t max_ticks, const mv_run_opts *o, uint64_t *ste
     P.max_ticks = max_ticks;
     u32 warps = c->L.warps, grid = 0, variant = c->L.variant;
     if (o) {
-        if (o->stage > 2 || o->variant > 2) return MV_EINVAL;
+        if (o->stage > 2 || o->variant > 3) return MV_EINVAL;
         P.watchdog_ns = o->watchdog_ns;
         P.stage_mode = o->stage;
-        if (o->block_warps) warps = std::min<u32>(o->block_warps, kMaxWarps);
         if (o->variant) variant = o->variant;
+        if (o->block_warps) warps = o->block_warps;
         grid = o->grid_blocks;
     }
-    const u32 smem = megakernel_smem(warps, c->L.image);
+    if (variant == 3 && !(o && o->block_warps)) warps = kMaxWarps;
+    warps = std::min<u32>(warps, variant == 3 ? kMaxWarps : 8);
+    // shared image budget: the batch's own (whole images) for the latency
+    // build, else what the build's blocks an SM leave
+    u32 image = c->L.image;
+    if (variant == 2 && c->L.variant == 2) image = kPartialImage;
+    if (variant == 3) image = std::max<u32>(c->L.image, kPartialImage3);
+    P.stage_limit = image;
+    const u32 smem = megakernel_smem(warps, image);
     int bpsm = 0, nsm = 0;
     cudaError_t e = megakernel_prepare(variant, warps, smem, &bpsm, &nsm);
     if (e != cudaSuccess || bpsm == 0) return MV_ECUDA;

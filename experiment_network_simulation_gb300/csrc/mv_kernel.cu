@@ -121,10 +121,9 @@ __device__ bool memory_fits(const u64 *m, u64 cap)
     return weights + acts <= cap;
 }
 
-// blockIdx.y = experiment; x covers that experiment's entities
-__global__ void k_init(Params P)
+// Tick-0 state of experiment e; the block's x threads cover its entities.
+__device__ void init_experiment(const Params &P, u32 e)
 {
-    u32 e = blockIdx.y;
     const ExpRec X = P.exp[e];
     const WorkRec W = P.work[X.work];
     u32 i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -161,6 +160,12 @@ __global__ void k_init(Params P)
         P.rk[X.rk_off + r] = c;
         if (over) atomicCAS(&P.ctl[e].status, (u32)EXP_RUNNING, (u32)EXP_OVERFLOW);
     }
+}
+
+// blockIdx.y strides over experiments
+__global__ void k_init(Params P)
+{
+    for (u32 e = blockIdx.y; e < P.n_exps; e += gridDim.y) init_experiment(P, e);
 }
 
 __global__ void k_init_ctl(Params P)
@@ -264,8 +269,8 @@ template <> struct ViewOf<const XV &> {
 };
 template <class VT> struct kOnePerPass { static constexpr bool value = false; };
 template <> struct kOnePerPass<HV> { static constexpr bool value = true; };
-template <int MINB> struct ViewFor { typedef HV T; };
-template <> struct ViewFor<2> { typedef const XV &T; };
+template <int VAR> struct ViewFor { typedef const XV &T; };
+template <> struct ViewFor<1> { typedef HV T; };
 
 // Per-experiment counters while a block holds it; only read after the last
 // tick.  Decisions taken every tick use the per-warp reports instead, which
@@ -1602,13 +1607,13 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
 }
 
 // Persistent grid: each block takes the next experiment of the processing
-// order until none is left (or the watchdog fired).  MINB = 1 lets a block
+// order until none is left (or the watchdog fired).  Builds (VAR): 1 lets a block
 // use up to 255 registers a thread (lowest latency per tick, for
 // experiments stepped from shared memory); MINB = 2 caps registers so two
 // blocks share an SM (more experiments in flight, for experiments whose
 // state stays in global memory and whose ticks wait on memory).
-template <int MINB>
-__global__ void __launch_bounds__(kMaxWarps * 32, MINB) k_megakernel(Params P)
+template <int VAR>
+__global__ void __launch_bounds__(VAR == 3 ? 512 : 256, VAR == 2 ? 2 : 1) k_megakernel(Params P)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
     const u32 nW = blockDim.x >> 5, warp = threadIdx.x >> 5;
@@ -1621,7 +1626,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, MINB) k_megakernel(Params P)
         const u32 slot = s_slot;
         __syncthreads();
         if (slot >= P.n_exps) break;
-        run_experiment<typename ViewFor<MINB>::T>(P, P.order[slot], img, sw + warp, t_start);
+        run_experiment<typename ViewFor<VAR>::T>(P, P.order[slot], img, sw + warp, t_start);
     }
 }
 
@@ -1651,7 +1656,7 @@ cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_
     if (bx > 64) bx = 64;
     if (bx == 0) bx = 1;
     k_init_ctl<<<(p.n_exps + 255) / 256, 256, 0, st>>>(p);
-    dim3 grid(bx, p.n_exps);
+    dim3 grid(bx, p.n_exps < 65535 ? p.n_exps : 65535);
     k_init<<<grid, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
@@ -1660,7 +1665,8 @@ u32 megakernel_smem(u32 warps, u32 image_bytes) { return warps * (u32)sizeof(SwS
 
 static const void *megakernel_fn(u32 variant)
 {
-    return variant == 2 ? (const void *)k_megakernel<2> : (const void *)k_megakernel<1>;
+    return variant == 3 ? (const void *)k_megakernel<3>
+         : variant == 2 ? (const void *)k_megakernel<2> : (const void *)k_megakernel<1>;
 }
 
 cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,
@@ -1681,7 +1687,8 @@ cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *bloc
 cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
                               u32 smem_bytes, cudaStream_t st)
 {
-    if (variant == 2) k_megakernel<2><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    if (variant == 3) k_megakernel<3><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    else if (variant == 2) k_megakernel<2><<<blocks, warps * 32, smem_bytes, st>>>(p);
     else k_megakernel<1><<<blocks, warps * 32, smem_bytes, st>>>(p);
     return cudaGetLastError();
 }
