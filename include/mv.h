@@ -173,12 +173,14 @@ typedef struct mv_ctx mv_ctx;
  * stage: 0 = an experiment's dynamic state is staged in shared memory when
  *   it fits, 1 = only its wake table is, 2 = nothing is (results are the
  *   same in every mode; the modes exist to test and measure that).
- * block_warps: warps of the block stepping one experiment (0 = automatic,
- *   at most 8).
- * variant: 0 = automatic, 1 = one block an SM with the most registers (for
- *   batches whose experiments all fit in shared memory), 2 = two blocks an
- *   SM (more experiments in flight, for larger ones).  Results are the same
- *   in every variant. */
+ * block_warps: warps of the block stepping one experiment (0 = automatic;
+ *   at most 8, or 16 for variant 3).
+ * variant: the kernel build.  0 = automatic; 1 = one block an SM with the
+ *   most registers (for batches whose experiments all fit in shared memory);
+ *   2 = two 8-warp blocks an SM (more experiments in flight); 3 = one
+ *   16-warp block an SM with twice the shared memory for staging (for
+ *   experiments whose hottest arrays do not fit variant 2's share).  Results
+ *   are the same in every variant. */
 typedef struct mv_run_opts {
     uint64_t watchdog_ns;
     uint32_t grid_blocks;
