@@ -632,6 +632,40 @@ def gpt_small(algo: int = RING, nc: int = 2, chunk: int = 64 * KIB, seeds=(0, 1)
     return Batch(exps, "gpt-small")
 
 
+def table_limits() -> Batch:
+    """Experiments at and one past each per-rank table limit (send lanes 64,
+    receive counters 128, pending nodes 64, running collectives 16): the
+    first of each pair must finish, the second must stop with the overflow
+    status."""
+    tk = 1000
+    exps = []
+    for nc in (64, 65):                       # ring all-reduce lanes: NC a rank
+        w = single_collective(2, AR, nc * 4096)
+        exps.append(Experiment(single_switch(2, 1, 0), w, RING, nc, 4096, tick_ps=tk,
+                               label=dict(table="lanes", n=nc)))
+    for nc in (42, 43):                       # tree receive counters: 3 NC a rank
+        w = single_collective(2, AR, nc * 4096)
+        exps.append(Experiment(single_switch(2, 1, 0), w, TREE, nc, 4096, tick_ps=tk,
+                               label=dict(table="ports", n=3 * nc)))
+    for n in (64, 65):                        # pending nodes: n roots on one rank
+        w = Workload(1, "roots")
+        for i in range(n):
+            w.compute(0, 1000 * (1 + i % 3))
+        exps.append(Experiment(single_switch(1, 1, 0), w, tick_ps=tk,
+                               label=dict(table="pend", n=n)))
+    for n in (16, 17):                        # running memberships: n intra collectives
+        w = Workload(2, "intra")
+        slow = w.compute(1, 50_000)           # rank 1 joins late: rank 0 keeps n running
+        prev = slow
+        for _ in range(n):
+            ids = w.collective(AR, [0, 1], 4096, intra=True, alpha=3, beta=(1, 1000))
+            w.edge(prev, ids[1])
+            prev = ids[1]
+        exps.append(Experiment(single_switch(2, 1, 0), w, tick_ps=tk,
+                               label=dict(table="act", n=n)))
+    return Batch(exps, "table-limits")
+
+
 # --------------------------------------------------------------------------
 # MoE dispatch / combine (config 4)
 # --------------------------------------------------------------------------

@@ -45,6 +45,7 @@
 #define NPORT 128     /* receive counters per rank                      */
 #define NPEND 64      /* scheduled-but-not-started nodes per rank       */
 #define NACT 16       /* running collective memberships per rank        */
+#define TICK_LIMIT 0xFFF00000u   /* largest tick value a run reaches        */
 
 enum { K_COMPUTE = 0, K_INTRA = 1, K_NET = 2 };
 enum { C_AR = 0, C_RS = 1, C_AG = 2, C_RELAY = 3, C_P2P = 4, C_A2A = 5 };
@@ -126,6 +127,7 @@ typedef struct nic {
     uint64_t used_mask;   /* bit q set when lane slot q is in use           */
     uint32_t act[NACT];
     int n_act;
+    int tick_fail;        /* one of its tables overflowed during this tick  */
 } nic;
 
 typedef struct sim {
@@ -170,13 +172,20 @@ typedef struct sim {
     int64_t *outstanding;
     uint32_t nodes_left;
     int changed, status;
+    int cur_rank;                   /* rank whose DAG step is running, or -1 */
     uint64_t pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
     uint32_t *rec_sender, *rec_key, *rec_tick, rec_count;
 } sim;
 
+/* A failure stops the experiment at the end of the current tick.  Within
+ * that tick every other entity still completes its step (Multiverse section
+ * 3.2: a system processes all of its entities in one invocation), while the
+ * rank that failed does nothing more.  The first failure in the phase order
+ * (ranks in index order, then switches) names the status. */
 static void fail(sim *s, int st)
 {
     if (s->status == ST_RUNNING) s->status = st;
+    if (s->cur_rank >= 0) s->nics[s->cur_rank].tick_fail = 1;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -450,7 +459,7 @@ static void complete(sim *s, uint32_t u, uint32_t c)
     s->end[u] = c;
     s->nodes_left--;
     s->changed = 1;
-    if (c >= UNSET - 1) { fail(s, ST_OVERFLOW); return; }
+    if (c >= TICK_LIMIT) { fail(s, ST_OVERFLOW); return; }
     for (uint32_t k = s->succ_base[u]; k < s->succ_base[u + 1]; k++) {
         uint32_t v = s->succ[k];
         s->cand[v] = umax32(s->cand[v], c + 1);
@@ -566,18 +575,22 @@ static void dag_step(sim *s, uint32_t r, uint32_t t)
     n->n_pend = w;
     qsort(now_nodes, nn, sizeof(uint32_t), cmp_u32);
     for (int k = 0; k < nn; k++) {
+        if (n->tick_fail) return;         /* this rank failed: it starts nothing more */
         uint32_t u = now_nodes[k];
-        s->start[u] = t;
         s->changed = 1;
         switch (s->node_kind[u]) {
         case K_COMPUTE:
+            s->start[u] = t;
             complete(s, u, t + compute_ticks(s, u));
             break;
         case K_INTRA:
+            s->start[u] = t;
             act_add(s, r, u);
             break;
         case K_NET:
             net_join(s, r, u, t);
+            if (n->tick_fail) return;     /* a join that does not fit never starts */
+            s->start[u] = t;
             if (s->outstanding[u] == 0) {
                 free_ports(s, r, u);
                 complete(s, u, t);
@@ -586,7 +599,6 @@ static void dag_step(sim *s, uint32_t r, uint32_t t)
             }
             break;
         }
-        if (s->status != ST_RUNNING) return;
     }
 }
 
@@ -654,7 +666,7 @@ static void forward(sim *s, uint32_t w, uint32_t t)
         tgt[p] = -1;
         if (h) {
             tgt[p] = route_port(s, w, h);
-            if (tgt[p] < 0) { fail(s, ST_ERROR); return; }
+            if (tgt[p] < 0) { fail(s, ST_ERROR); continue; }   /* that head stays */
             wanted[tgt[p]]++;
         }
     }
@@ -826,6 +838,8 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
 {
     uint32_t t = 0;
     uint64_t active = 0;
+    if (limit > TICK_LIMIT) limit = TICK_LIMIT;
+    s->cur_rank = -1;
     for (uint32_t r = 0; r < s->R; r++)
         for (uint32_t u = s->rank_base[r]; u < s->rank_base[r + 1]; u++)
             if (s->node_npred[u] == 0) pend_add(s, r, u, 0);
@@ -834,10 +848,16 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
         if (t >= limit) break;
         memcpy(s->tail0, s->tail, sizeof(uint32_t) * s->nf);
         s->changed = 0;
-        for (uint32_t r = 0; r < s->R && s->status == ST_RUNNING; r++) dag_step(s, r, t);
-        for (uint32_t w = 0; w < s->S && s->status == ST_RUNNING; w++) forward(s, w, t);
-        for (uint32_t r = 0; r < s->R; r++) inject(s, r, t);
-        for (uint32_t r = 0; r < s->R; r++) receive(s, r, t);
+        for (uint32_t r = 0; r < s->R; r++) {
+            s->cur_rank = (int)r;
+            dag_step(s, r, t);
+        }
+        s->cur_rank = -1;
+        for (uint32_t w = 0; w < s->S; w++) forward(s, w, t);
+        for (uint32_t r = 0; r < s->R; r++)
+            if (!s->nics[r].tick_fail) inject(s, r, t);
+        for (uint32_t r = 0; r < s->R; r++)
+            if (!s->nics[r].tick_fail) receive(s, r, t);
         active++;
         if (s->status != ST_RUNNING) break;
         if (s->nodes_left == 0) { s->status = ST_DONE; t++; break; }

@@ -198,6 +198,16 @@ def test_every_build_and_staging_bit_exact(stage, variant):
             assert_same(got, want)
 
 
+@pytest.mark.parametrize("variant", [1, 2])
+def test_table_limits_match_oracle(variant):
+    """At and one past each per-rank table limit, in both register builds
+    (their per-rank table strides are sized from the DAG, so this pins that
+    the overflow status appears exactly where the fixed-size tables put it)."""
+    p = I.table_limits().pack()
+    got = mv.simulate(p, run_opts=dict(variant=variant))
+    assert_same(got, O.run(p))
+
+
 @pytest.mark.parametrize("algo", [I.RING, I.TREE])
 def test_gpt_small_bit_exact(algo):
     """The config-3 DAG shape (1F1B, analytic TP all-reduces, pipeline p2p,

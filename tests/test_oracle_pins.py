@@ -431,3 +431,14 @@ def test_deadlock_is_detected():
     t = I.single_switch(2, 1, 0)
     r = O.run(I.Batch([I.Experiment(t, w, tick_ps=1000, chunk=1 << 20)]).pack())
     assert r["status"][0] == O.ST_DEADLOCK
+
+
+def test_table_limits_overflow_exactly_one_past_the_limit():
+    """Each per-rank table (send lanes 64, receive counters 128, pending
+    nodes 64, running collectives 16) holds its limit and fails one past it
+    with the overflow status (the limits the C ABI documents)."""
+    b = I.table_limits()
+    r = O.run(b.pack())
+    for e, x in enumerate(b.experiments):
+        over = x.label["n"] in (65, 129, 17)
+        assert r["status"][e] == (O.ST_OVERFLOW if over else O.ST_DONE), x.label
