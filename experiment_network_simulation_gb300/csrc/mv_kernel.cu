@@ -37,6 +37,22 @@ __device__ __forceinline__ u64 mix64(u64 z)
     return z ^ (z >> 31);
 }
 __device__ __forceinline__ u64 cdiv(u64 a, u64 b) { return (a + b - 1) / b; }
+// h mod n for 1 <= n <= 255 by Barrett reduction: with m = floor((2^64 - 1) / n),
+// the estimate hi64(h * m) of floor(h / n) is low by at most two, so two
+// conditional subtractions finish the remainder exactly.  m comes from a
+// table the compiler fills; a 64-bit division per packet would cost far more.
+struct BarrettTab {
+    u64 m[256];
+    constexpr BarrettTab() : m() { for (u32 n = 1; n < 256; n++) m[n] = ~0ull / n; }
+};
+__constant__ BarrettTab kBarrett = BarrettTab();
+__device__ __forceinline__ u32 mod_small(u64 h, u32 n)
+{
+    u64 r = h - __umul64hi(h, kBarrett.m[n]) * n;
+    if (r >= n) r -= n;
+    if (r >= n) r -= n;
+    return (u32)r;
+}
 // ring-buffer slot of counter x in a queue of cap slots (a mask when cap is
 // a power of two, as in every configured batch)
 __device__ __forceinline__ u32 slot_ix(u32 x, u32 cap)
@@ -335,7 +351,7 @@ __device__ __forceinline__ u32 route_port(const VW &V, u32 s, u32 p0, uint4 pk)
     u32 nup = V.up_n[s];
     if (nup == 0) return 0xFFu;
     u64 h = mix64((u64)pk_key(pk) ^ ((u64)s << 40) ^ V.X.ecmp_seed);
-    return V.up_list[p0 + (u32)(h % nup)];
+    return V.up_list[p0 + mod_small(h, nup)];
 }
 
 // Forwarding for one tick (Multiverse section 4.2) at the n switches of a
@@ -385,8 +401,9 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         st_[j] = V.eg[qi];
         pr_[j] = V.port_rec[qi];
     }
-    // in shared memory these are cheap, so every free egress gets them now;
-    // in global memory only egresses that a packet wants load them (below)
+    // with the queue words in shared memory these are cheap, so every free
+    // egress gets them now; in global memory only egresses that a packet
+    // wants load them (below)
     if (staged) {
 #pragma unroll
         for (u32 j = 0; j < 2; j++) {
@@ -509,8 +526,9 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         st_[j] = V.eg[qi];
         pr_[j] = V.port_rec[qi];
     }
-    // in shared memory these are cheap, so every free egress gets them now;
-    // in global memory only egresses that a packet wants load them (below)
+    // with the queue words in shared memory these are cheap, so every free
+    // egress gets them now; in global memory only egresses that a packet
+    // wants load them (below)
     if (staged) {
 #pragma unroll
         for (u32 j = 0; j < 2; j++) {
@@ -1450,7 +1468,9 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         now = TC.end_max1;
     }
     const u32 nI = V.X.n_items, nsw = V.X.nsw;
-    const bool full = smask == (1u << IM_N) - 1;   // the whole state is in shared memory
+    // queue words in shared memory: a pass reads every free egress's
+    // downstream queue words up front instead of after the plan
+    const bool qstaged = ((smask >> IM_QPUSH) & (smask >> IM_QPOP) & 1u) != 0;
     // items are dealt to warps round-robin (item warp + j * nW), so switches
     // and rank groups spread over all warps
     const u32 cnt = warp < nI ? (nI - warp + nW - 1) / nW : 0;
@@ -1498,7 +1518,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                     Ms1 &= Ms1 - 1;
                     const u32 item = warp + (base + j) * nW;
                     const u32 old = __shfl_sync(kFull, w, j);
-                    rep = min(rep, switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, full));
+                    rep = min(rep, switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, qstaged));
                 }
             }
             uint2 sr = make_uint2(0, 0);
@@ -1511,7 +1531,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                 const u32 np = __shfl_sync(kFull, sr.y, j), p0 = __shfl_sync(kFull, sr.x, j);
                 const u32 old = __shfl_sync(kFull, w, j);
                 if (n == kPack || used + np > kMaxPorts) {
-                    rep = min(rep, switch_pack<VT>(V, acc, n, t, poke, sm, &fail, full));
+                    rep = min(rep, switch_pack<VT>(V, acc, n, t, poke, sm, &fail, qstaged));
                     n = 0;
                     used = 0;
                 }
@@ -1526,7 +1546,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                 n++;
                 used += np;
             }
-            if (n) rep = min(rep, switch_pack<VT>(V, acc, n, t, poke, sm, &fail, full));
+            if (n) rep = min(rep, switch_pack<VT>(V, acc, n, t, poke, sm, &fail, qstaged));
             // due rank groups, one a pass
             u32 Mr = __ballot_sync(kFull, due && it >= nsw);
             while (Mr) {
