@@ -75,12 +75,14 @@ struct Lane {
     u32 drank, dslot, ok_dst, pbase;
 };
 
+// Per-rank control word as stored (48 bytes).
 struct RankCtl {
     u32 busy, rr, npend, nact;
     u64 lane_mask;
     u64 port_lo, port_hi;   // receive counters in use: bits 0..63, 64..127
-    u32 blocked;    // every send lane waits for a receive count (no scan needed)
-    u32 nintra;     // running intra-server memberships (checked every tick)
+    u32 flags;      // bit 0: every send lane waits for a receive count (no scan
+                    // needed); bits 1..: running intra-server memberships
+    u32 pfirst;     // start tick of the first pending node (kUnset: none)
 };
 
 // Per-experiment control, kept across runs (resume) and read by mv_results.

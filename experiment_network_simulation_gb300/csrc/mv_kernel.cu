@@ -173,6 +173,7 @@ __device__ void init_experiment(const Params &P, u32 e)
             if (c.npend == X.pend_cap) { over = true; break; }
             P.pend[X.pend_off + (u64)r * X.pend_cap + c.npend++] = make_uint2(u, 0);
         }
+        c.pfirst = c.npend ? 0u : kUnset;
         P.rk[X.rk_off + r] = c;
         if (over) atomicCAS(&P.ctl[e].status, (u32)EXP_RUNNING, (u32)EXP_OVERFLOW);
     }
@@ -383,8 +384,12 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
     u32 tail_[2] = {0, 0}, head_[2] = {0, 0}, dhead_[2] = {0, 0}, dtail_[2] = {0, 0};
     uint2 st_[2] = {make_uint2(kUnset, 0), make_uint2(kUnset, 0)};
     uint4 pr_[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    uint4 pk_[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     // Issue the independent loads together: per position its ingress queue
-    // words, its egress state and record.
+    // words, its egress state and record, and (once the queue words are in)
+    // the ingress head packet, so that the head packet and the port record
+    // are in flight at the same time.  The head slot cannot change during
+    // the tick: its upstream may only push into a slot freed before it.
 #pragma unroll
     for (u32 j = 0; j < 2; j++) {
         const u32 p = lane + 32 * j;
@@ -400,6 +405,7 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         head_[j] = (u32)V.q_pop[qi];
         st_[j] = V.eg[qi];
         pr_[j] = V.port_rec[qi];
+        if (head_[j] != tail_[j]) pk_[j] = V.slots[(u64)qi * cap + slot_ix(head_[j], cap)];
     }
     // with the queue words in shared memory these are cheap, so every free
     // egress gets them now; in global memory only egresses that a packet
@@ -425,7 +431,7 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         const u32 head = head_[j];
         sm->head[p] = head;
         if (head == tail_[j]) continue;
-        const uint4 pk = V.slots[(u64)q_[j] * cap + slot_ix(head, cap)];
+        const uint4 pk = pk_[j];
         if (pk.x > t) { atomicMin(&sm->nxt[k], pk.x); continue; }
         atomicMin(&sm->nxt[k], t + 1);  // a ready head: left or blocked, look again next tick
         const u32 tg = route_port(V, sm->sw[k], sm->p0[k], pk);
@@ -605,26 +611,39 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
 }
 
 // ---------------------------------------------------------------- ranks
-__device__ __forceinline__ RankCtl load_ctl(const RankCtl *p)
+// A rank's control word while its lane works on it.
+struct RankReg {
+    u32 busy, rr, npend, nact;
+    u64 lane_mask;
+    u64 port_lo, port_hi;   // receive counters in use: bits 0..63, 64..127
+    u32 blocked;    // every send lane waits for a receive count (no scan needed)
+    u32 nintra;     // running intra-server memberships (checked every tick)
+    u32 pfirst;     // start tick of the first pending node (kUnset: none), so
+                    // that a tick with nothing due reads no pending list
+};
+static_assert(sizeof(RankCtl) == 48, "RankCtl is three 16-byte words");
+__device__ __forceinline__ RankReg load_ctl(const RankCtl *p)
 {
     const uint4 *q = reinterpret_cast<const uint4 *>(p);
     uint4 a = q[0], b = q[1], c = q[2];
-    RankCtl r;
+    RankReg r;
     r.busy = a.x; r.rr = a.y; r.npend = a.z; r.nact = a.w;
     r.lane_mask = ((u64)b.y << 32) | b.x;
     r.port_lo = ((u64)b.w << 32) | b.z;
     r.port_hi = ((u64)c.y << 32) | c.x;
-    r.blocked = c.z;
-    r.nintra = c.w;
+    r.blocked = c.z & 1u;
+    r.nintra = c.z >> 1;
+    r.pfirst = c.w;
     return r;
 }
-__device__ __forceinline__ void store_ctl(RankCtl *p, const RankCtl &r)
+__device__ __forceinline__ void store_ctl(RankCtl *p, const RankReg &r)
 {
     uint4 *q = reinterpret_cast<uint4 *>(p);
     q[0] = make_uint4(r.busy, r.rr, r.npend, r.nact);
     q[1] = make_uint4((u32)r.lane_mask, (u32)(r.lane_mask >> 32), (u32)r.port_lo,
                       (u32)(r.port_lo >> 32));
-    q[2] = make_uint4((u32)r.port_hi, (u32)(r.port_hi >> 32), r.blocked, r.nintra);
+    q[2] = make_uint4((u32)r.port_hi, (u32)(r.port_hi >> 32), r.blocked | (r.nintra << 1),
+                      r.pfirst);
 }
 static_assert(sizeof(Lane) == 80, "Lane is five 16-byte words");
 // Field by field through 16-byte words: the local Lane never has its
@@ -653,11 +672,11 @@ __device__ __forceinline__ void store_lane(Lane *p, const Lane &L)
 
 // Receive-counter occupancy bits, by value (no indexed array, so the rank's
 // control word stays in registers).
-__device__ __forceinline__ bool port_used(const RankCtl &C, u32 p)
+__device__ __forceinline__ bool port_used(const RankReg &C, u32 p)
 {
     return ((p < 64 ? C.port_lo >> p : C.port_hi >> (p - 64)) & 1ull) != 0;
 }
-__device__ __forceinline__ void port_set(RankCtl &C, u32 p, bool on)
+__device__ __forceinline__ void port_set(RankReg &C, u32 p, bool on)
 {
     const u64 bit = 1ull << (p & 63);
     if (p < 64) C.port_lo = on ? (C.port_lo | bit) : (C.port_lo & ~bit);
@@ -672,7 +691,7 @@ struct RankViewT {
     Team *TC;
     u32 *poke;          // this step's poke words of the experiment's items
     u32 r, t;
-    RankCtl C;
+    RankReg C;
     bool changed, fail_over, fail_err;
     u32 nxt;            // this rank's own next wake
     u32 pk_min;         // earliest wake poked into other items
@@ -944,6 +963,7 @@ __device__ __forceinline__ void pend_add(RV &v, u32 u, u32 st)
         j--;
     }
     pd[j] = make_uint2(u, st);
+    if (j == 0) v.C.pfirst = st;
 }
 
 template <class RV>
@@ -1049,8 +1069,8 @@ __device__ __forceinline__ void dag_step(RV &v)
     const auto &V = v.V;
     const u32 t = v.t;
     uint2 *pd = V.pend + (u64)v.r * V.X.pend_cap;
-    if (v.C.nact == 0 && (v.C.npend == 0 || pd[0].y > t)) {      // nothing running or due
-        if (v.C.npend) v.nxt = min(v.nxt, pd[0].y);
+    if (v.C.nact == 0 && v.C.pfirst > t) {      // nothing running or due
+        v.nxt = min(v.nxt, v.C.pfirst);
         return;
     }
     // Running memberships: an intra-server one can finish whenever its last
@@ -1086,12 +1106,11 @@ __device__ __forceinline__ void dag_step(RV &v)
     if (nscan) v.C.nact = w;
     // start the nodes due now: the prefix of the sorted pending list (a
     // start tick already past is an inconsistent schedule)
-    u32 lo = 0;
-    while (lo < v.C.npend && pd[lo].y < t) lo++;
-    if (lo) { v.fail_err = true; return; }
-    u32 hi = lo;
-    while (hi < v.C.npend && pd[hi].y == t) hi++;
-    for (u32 j = lo; j < hi && !v.fail_over; j++) {
+    if (v.C.pfirst < t) { v.fail_err = true; return; }
+    u32 hi = 0;
+    if (v.C.pfirst == t)
+        while (hi < v.C.npend && pd[hi].y == t) hi++;
+    for (u32 j = 0; j < hi && !v.fail_over; j++) {
         const u32 u = pd[j].x;
         v.changed = true;
         const u32 kind = v.P->node_kind[W_(v).node_off + u];
@@ -1116,10 +1135,18 @@ __device__ __forceinline__ void dag_step(RV &v)
     }
     if (v.fail_over || v.fail_err) return;
     // drop the started prefix; nodes scheduled above start later
-    const u32 n = v.C.npend;
-    for (u32 j = hi; j < n; j++) pd[j - hi] = pd[j];
-    v.C.npend = n - hi;
-    if (v.C.npend) v.nxt = min(v.nxt, pd[0].y);
+    if (hi) {
+        const u32 n = v.C.npend;
+        u32 first = kUnset;
+        for (u32 j = hi; j < n; j++) {
+            const uint2 x = pd[j];
+            if (j == hi) first = x.y;
+            pd[j - hi] = x;
+        }
+        v.C.npend = n - hi;
+        v.C.pfirst = first;
+    }
+    v.nxt = min(v.nxt, v.C.pfirst);
 }
 
 // SendSys + NICSndSys: one packet per uplink serialisation time, round-robin
@@ -1158,6 +1185,10 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
                 if ((L.dep_mask >> b) & 1u)
                     if (ports[L.pbase + L.dep_base + b].x < L.dep_need) ok = false;
             if (!ok) continue;
+            // receive counts only grow while the lane's message is current, so
+            // a met dependency stays met: later packets of the message skip it
+            // (the next message sets its own)
+            L.dep_mask = 0;
             if (!L.ok_dst) {
                 // the destination's join reaches this rank 1 + min(delta) ticks
                 // later; when that time is known, it is this rank's own wake (a
