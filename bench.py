@@ -42,7 +42,7 @@ UNIT = "packet-hops/s"
 BYTES_PER_HOP, BYTES_PER_PKT = 32, 24
 # DRAM bytes (read + write) of one megakernel launch of the whole-run
 # workload, from an ncu capture of the current kernel (see profiles/).
-TRAFFIC = {"config2": 6317056}
+TRAFFIC = {"config2": 6724608}
 
 WORKLOADS = {
     "config1": (lambda seed: I.config1(),

@@ -239,7 +239,7 @@ int plan(const mv_batch_desc *d, Layout &L)
         for (u32 c = 0; c < R.ncoll; c++) {
             u32 g = R.coll_off + c, N = d->coll_nmembers[g], kind = d->coll_kind[g];
             L.coll_mstart[g] = m;
-            if (N == 0 || kind > COLL_A2A) return MV_EINVAL;
+            if (N == 0 || N > 0xFFFF || kind > COLL_A2A) return MV_EINVAL;   // 16-bit member index
             if (d->coll_bytes[g] >= (1ull << 40)) return MV_EOVERFLOW;
             bool intra = d->coll_intra[g] != 0;
             if (intra && (d->coll_alpha[g] == 0 || d->coll_beta_den[g] == 0 ||

@@ -62,17 +62,21 @@ struct ExpRec {
     u32 pad;
 };
 
-// One send lane: a stream of messages one rank sends for one channel of one
-// collective membership (a queue pair in RDMA terms).  The last row caches
-// what every packet of the current message needs: destination node and
-// rank, the destination's receive slot once its join has been seen, and the
-// sender's own receive-counter base.
+// One send lane as stored: a stream of messages one rank sends for one
+// channel of one collective membership (a queue pair in RDMA terms), five
+// 16-byte words.  Besides the message counters it caches what every packet
+// or message of the lane needs without another table read: the collective,
+// its member count, kind and first member entry; destination node and rank;
+// the destination's receive slot once its join has been seen; the sender's
+// own receive-counter base.  Field packing (mv_kernel.cu, load_lane):
+//   w0: node, member | chan << 16 | kind << 24, collective, members
+//   w1: message, messages, packets left, destination member
+//   w2: dst_port | dep_base << 8 | dep_mask << 16 | ok_dst << 19 | coll kind << 20,
+//       dep_need, first member entry, connection key
+//   w3: a2a entry, a2a first chunk, destination node, destination rank
+//   w4: destination slot, receive-counter base, 0, 0
 struct Lane {
-    u32 node, member, chan, kind;
-    u32 m, nmsg, pkts_left, dst_member;
-    u32 dst_port, dep_base, dep_mask, dep_need;
-    u32 key, a2a_e, a2a_start, dnode;
-    u32 drank, dslot, ok_dst, pbase;
+    uint4 w[5];
 };
 
 // Per-rank control word as stored (48 bytes).

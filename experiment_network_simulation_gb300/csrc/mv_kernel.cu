@@ -37,6 +37,16 @@ __device__ __forceinline__ u64 mix64(u64 z)
     return z ^ (z >> 31);
 }
 __device__ __forceinline__ u64 cdiv(u64 a, u64 b) { return (a + b - 1) / b; }
+// a / b and a mod b for a 32-bit divisor, in 32-bit arithmetic whenever the
+// dividend fits (the usual case: message and chunk sizes), else in 64-bit
+__device__ __forceinline__ u64 udiv(u64 a, u32 b)
+{
+    return (a >> 32) == 0 ? (u64)((u32)a / b) : a / b;
+}
+__device__ __forceinline__ u64 umod(u64 a, u32 b)
+{
+    return (a >> 32) == 0 ? (u64)((u32)a % b) : a % b;
+}
 // h mod n for 1 <= n <= 255 by Barrett reduction: with m = floor((2^64 - 1) / n),
 // the estimate hi64(h * m) of floor(h / n) is low by at most two, so two
 // conditional subtractions finish the remainder exactly.  m comes from a
@@ -645,29 +655,43 @@ __device__ __forceinline__ void store_ctl(RankCtl *p, const RankReg &r)
     q[2] = make_uint4((u32)r.port_hi, (u32)(r.port_hi >> 32), r.blocked | (r.nintra << 1),
                       r.pfirst);
 }
+// A send lane while its rank's lane works on it (the stored form, Lane,
+// packs the small fields).
+struct LaneReg {
+    u32 node, member, chan, kind;       // membership node, member index, channel, tree role
+    u32 coll, nmemb, ckind, mbase;      // its collective, members, kind, first member entry
+    u32 m, nmsg, pkts_left, dst_member;
+    u32 dst_port, dep_base, dep_mask, dep_need;
+    u32 key, a2a_e, a2a_start, dnode;
+    u32 drank, dslot, ok_dst, pbase;
+};
 static_assert(sizeof(Lane) == 80, "Lane is five 16-byte words");
-// Field by field through 16-byte words: the local Lane never has its
-// address taken, so it stays in registers.
-__device__ __forceinline__ Lane load_lane(const Lane *p)
+static_assert(kNPort <= 256 && kNLane <= 256, "ports and channels fit the packed lane fields");
+// Word by word: the local LaneReg never has its address taken, so it stays
+// in registers.
+__device__ __forceinline__ LaneReg load_lane(const Lane *p)
 {
-    const uint4 *q = reinterpret_cast<const uint4 *>(p);
-    const uint4 a = q[0], b = q[1], c = q[2], d = q[3], e = q[4];
-    Lane L;
-    L.node = a.x; L.member = a.y; L.chan = a.z; L.kind = a.w;
+    const uint4 a = p->w[0], b = p->w[1], c = p->w[2], d = p->w[3], e = p->w[4];
+    LaneReg L;
+    L.node = a.x; L.member = a.y & 0xFFFFu; L.chan = (a.y >> 16) & 0xFFu; L.kind = a.y >> 24;
+    L.coll = a.z; L.nmemb = a.w;
     L.m = b.x; L.nmsg = b.y; L.pkts_left = b.z; L.dst_member = b.w;
-    L.dst_port = c.x; L.dep_base = c.y; L.dep_mask = c.z; L.dep_need = c.w;
-    L.key = d.x; L.a2a_e = d.y; L.a2a_start = d.z; L.dnode = d.w;
-    L.drank = e.x; L.dslot = e.y; L.ok_dst = e.z; L.pbase = e.w;
+    L.dst_port = c.x & 0xFFu; L.dep_base = (c.x >> 8) & 0xFFu; L.dep_mask = (c.x >> 16) & 7u;
+    L.ok_dst = (c.x >> 19) & 1u; L.ckind = c.x >> 20;
+    L.dep_need = c.y; L.mbase = c.z; L.key = c.w;
+    L.a2a_e = d.x; L.a2a_start = d.y; L.dnode = d.z; L.drank = d.w;
+    L.dslot = e.x; L.pbase = e.y;
     return L;
 }
-__device__ __forceinline__ void store_lane(Lane *p, const Lane &L)
+__device__ __forceinline__ void store_lane(Lane *p, const LaneReg &L)
 {
-    uint4 *q = reinterpret_cast<uint4 *>(p);
-    q[0] = make_uint4(L.node, L.member, L.chan, L.kind);
-    q[1] = make_uint4(L.m, L.nmsg, L.pkts_left, L.dst_member);
-    q[2] = make_uint4(L.dst_port, L.dep_base, L.dep_mask, L.dep_need);
-    q[3] = make_uint4(L.key, L.a2a_e, L.a2a_start, L.dnode);
-    q[4] = make_uint4(L.drank, L.dslot, L.ok_dst, L.pbase);
+    p->w[0] = make_uint4(L.node, L.member | (L.chan << 16) | (L.kind << 24), L.coll, L.nmemb);
+    p->w[1] = make_uint4(L.m, L.nmsg, L.pkts_left, L.dst_member);
+    p->w[2] = make_uint4(L.dst_port | (L.dep_base << 8) | (L.dep_mask << 16) | (L.ok_dst << 19) |
+                             (L.ckind << 20),
+                         L.dep_need, L.mbase, L.key);
+    p->w[3] = make_uint4(L.a2a_e, L.a2a_start, L.dnode, L.drank);
+    p->w[4] = make_uint4(L.dslot, L.pbase, 0u, 0u);
 }
 
 // Receive-counter occupancy bits, by value (no indexed array, so the rank's
@@ -819,19 +843,24 @@ __device__ __forceinline__ u32 port_count_expect(const RV &v, u32 c, u32 i, u32 
 }
 
 // Message L.m of a lane: bytes, destination member and port, and the own
-// receive counts it waits for.  Returns its packet count.
+// receive counts it waits for.  Returns its packet count.  The collective's
+// member count, kind and first member entry come from the lane itself, so
+// the only table reads are the collective's size and the destination's
+// member entry, issued together.
 template <class RV>
-__device__ __forceinline__ u32 lane_setup(const RV &v, Lane &L)
+__device__ __forceinline__ u32 lane_setup(const RV &v, LaneReg &L)
 {
-    u32 c = coll_of(v, L.node), N = nmemb(v, c), i = L.member, m = L.m, ch = L.chan;
-    u64 S = cbytes(v, c), C = X_(v).chunk, bytes = 0;
+    const Params &P = *v.P;
+    const u32 c = L.coll, N = L.nmemb, i = L.member, m = L.m, ch = L.chan, nc = X_(v).nc;
+    const u64 S = cbytes(v, c), C = X_(v).chunk;
+    u64 bytes = 0;
     L.dep_mask = 0;
     L.dep_need = 0;
     L.dep_base = 0;
-    switch (ckind(v, c)) {
+    switch (L.ckind) {
     case COLL_AR: case COLL_RS: case COLL_AG: {
-        u64 Pc = part_bytes(S, X_(v).nc, ch);
-        if (tree_of(v, c)) {
+        const u64 Pc = udiv(S, nc) + (ch < umod(S, nc) ? 1 : 0);    // channel ch's partition
+        if (L.ckind == COLL_AR && X_(v).algo == ALGO_TREE) {
             bytes = Pc > (u64)m * C ? min(C, Pc - (u64)m * C) : 0;
             u32 kids = (2 * i + 1 < N ? 2u : 0u) | (2 * i + 2 < N ? 4u : 0u);
             if (L.kind == 0) {                        // reduce toward the root
@@ -847,22 +876,24 @@ __device__ __forceinline__ u32 lane_setup(const RV &v, Lane &L)
             L.dep_need = m + 1;
             L.dep_base = ch * 3;
         } else {                                      // NCCL ring step order
-            u32 steps = ring_steps(v, c);
-            u64 l = m / steps, kk = m % steps, stride = (u64)N * C;
-            u64 B = min(stride, Pc - l * stride);
-            u64 bs = cdiv(B, N);
-            u64 blk = ((u64)i + N - (kk % N)) % N;
-            bytes = B > blk * bs ? min(bs, B - blk * bs) : 0;
+            // a ring lane exists only for N >= 2, so steps >= 1
+            const u32 steps = L.ckind == COLL_AR ? 2 * (N - 1) : N - 1;
+            const u32 l = m / steps, kk = m - l * steps;
+            const u64 stride = (u64)N * C;
+            const u64 B = min(stride, Pc - (u64)l * stride);
+            const u64 bs = udiv(B + N - 1, N);
+            const u32 blk = (i + N - kk % N) % N;
+            bytes = B > (u64)blk * bs ? min(bs, B - (u64)blk * bs) : 0;
             L.dst_member = (i + 1) % N;
             L.dst_port = ch;
             L.dep_base = ch;
-            if (kk >= 1) { L.dep_mask = 1u; L.dep_need = (u32)(l * steps + kk); }
+            if (kk >= 1) { L.dep_mask = 1u; L.dep_need = l * steps + kk; }
         }
         break;
     }
     case COLL_RELAY: {                                // pipelined broadcast hop
-        u32 K = v.P->coll_parts[W_(v).coll_off + c];
-        bytes = S / K + (m < S % K ? 1 : 0);
+        u32 K = P.coll_parts[W_(v).coll_off + c];
+        bytes = udiv(S, K) + (m < umod(S, K) ? 1 : 0);
         L.dst_member = i + 1;
         L.dst_port = 0;
         if (i >= 1) { L.dep_mask = 1u; L.dep_need = m + 1; }
@@ -874,21 +905,21 @@ __device__ __forceinline__ u32 lane_setup(const RV &v, Lane &L)
         L.dst_port = 0;
         break;
     case COLL_A2A: {
-        u32 mm = mabs(v, c, i);
-        u32 r0 = W_(v).a2a_off + v.P->memb_row[mm];
-        u64 g = (u64)ch + (u64)m * X_(v).nc;
-        while (g >= L.a2a_start + nchunks(v.P->a2a_bytes[r0 + L.a2a_e], C)) {
-            L.a2a_start += (u32)nchunks(v.P->a2a_bytes[r0 + L.a2a_e], C);
+        u32 mm = L.mbase + i;
+        u32 r0 = W_(v).a2a_off + P.memb_row[mm];
+        u64 g = (u64)ch + (u64)m * nc;
+        while (g >= L.a2a_start + nchunks(P.a2a_bytes[r0 + L.a2a_e], C)) {
+            L.a2a_start += (u32)nchunks(P.a2a_bytes[r0 + L.a2a_e], C);
             L.a2a_e++;
         }
-        u64 j = g - L.a2a_start, b = v.P->a2a_bytes[r0 + L.a2a_e];
+        u64 j = g - L.a2a_start, b = P.a2a_bytes[r0 + L.a2a_e];
         bytes = b > j * C ? min(C, b - j * C) : 0;
-        L.dst_member = v.P->a2a_dst[r0 + L.a2a_e];
+        L.dst_member = P.a2a_dst[r0 + L.a2a_e];
         L.dst_port = 0;
         break;
     }
     }
-    const u32 drank = mrank(v, c, L.dst_member), dnode = mnode(v, c, L.dst_member);
+    const u32 drank = P.member_rank[L.mbase + L.dst_member], dnode = P.member_node[L.mbase + L.dst_member];
     L.key = (u32)(mix64((u64)L.node | ((u64)(ch * 4 + L.kind) << 32) | ((u64)drank << 44)) &
                   0xFFFFFFu);
     if (dnode != L.dnode) {          // a new destination: its join is yet to be seen
@@ -896,7 +927,8 @@ __device__ __forceinline__ u32 lane_setup(const RV &v, Lane &L)
         L.drank = drank;
         L.ok_dst = 0;
     }
-    return (u32)(bytes == 0 ? 1 : cdiv(bytes, X_(v).pkt));
+    const u32 pkt = X_(v).pkt;
+    return (u32)(bytes == 0 ? 1 : udiv(bytes + pkt - 1, pkt));
 }
 
 template <class RV>
@@ -1028,8 +1060,10 @@ __device__ __forceinline__ bool net_join(RV &v, u32 u)
             u64 freem = ~v.C.lane_mask & lane_ok;
             if (!freem) { v.fail_over = true; return false; }
             u32 slot = (u32)__ffsll((long long)freem) - 1;
-            Lane L = {};
+            LaneReg L = {};
             L.node = u; L.member = i; L.chan = ch; L.kind = kd;
+            L.coll = c; L.nmemb = nmemb(v, c); L.ckind = ckind(v, c);
+            L.mbase = W_(v).memb_off + P.coll_mstart[W_(v).coll_off + c];
             L.m = 0; L.nmsg = nm;
             L.dnode = kUnset;
             L.pbase = (u32)base;
@@ -1179,7 +1213,7 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
         while (m) {
             u32 l = (u32)__ffsll((long long)m) - 1;
             m &= m - 1;
-            Lane L = load_lane(&lanes[l]);
+            LaneReg L = load_lane(&lanes[l]);
             bool ok = true;
             for (u32 b = 0; b < 3 && ok; b++)
                 if ((L.dep_mask >> b) & 1u)

@@ -97,7 +97,7 @@ extern "C" {
  * lists concatenated in succ[], same rank only), node_dur_lo/hi (compute
  * duration in ns; hi > lo draws from [lo, hi] with the experiment's
  * duration seed and node_dur_key).  Per collective: coll_kind, coll_intra
- * (1 = analytic), coll_bytes, coll_nmembers, coll_parts (relay partitions
+ * (1 = analytic), coll_bytes, coll_nmembers (1..65535), coll_parts (relay partitions
  * K), coll_alpha (ticks, >= 1 for intra), coll_beta_num/den (ticks per
  * byte).  Per member: member_rank, member_node; all-to-all rows
  * (member_a2a_n entries of a2a_dst/a2a_bytes, in rotation order from the
