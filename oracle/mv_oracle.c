@@ -86,6 +86,7 @@ typedef struct orc_out {
     uint32_t *node_start, *node_end;        /* concatenated per experiment */
     uint32_t *rec_count;                    /* per experiment */
     uint32_t *rec_sender, *rec_key, *rec_tick; /* concatenated, rec_cap each */
+    uint64_t *violations;                   /* per experiment: broken invariants */
 } orc_out;
 
 /* ------------------------------------------------------------------------ */
@@ -175,6 +176,12 @@ typedef struct sim {
     int cur_rank;                   /* rank whose DAG step is running, or -1 */
     uint64_t pkts_injected, pkt_hops, pkts_delivered, msgs_delivered, digest;
     uint32_t *rec_sender, *rec_key, *rec_tick, rec_count;
+    /* invariant checks, independent of the state that enforces them: a
+     * queue never holds more than cap packets; the one link feeding a queue
+     * carries at most one packet per its serialisation time; a packet is
+     * delivered at the host it was addressed to */
+    uint32_t *last_push;            /* nf: tick of the last push into the queue */
+    uint64_t violations;
 } sim;
 
 /* A failure stops the experiment at the end of the current tick.  Within
@@ -643,8 +650,12 @@ static pkt *ready_head(sim *s, uint32_t f, uint32_t t)
     return p->ready <= t ? p : NULL;
 }
 
-static void push(sim *s, uint32_t f, const pkt *p)
+/* push a packet sent at tick t over a link of serialisation time sigma */
+static void push(sim *s, uint32_t f, const pkt *p, uint32_t t, uint32_t sigma)
 {
+    if (s->tail[f] - s->head[f] >= s->cap) s->violations++;
+    if (s->last_push[f] != UNSET && t < s->last_push[f] + sigma) s->violations++;
+    s->last_push[f] = t;
     *slot(s, f, s->tail[f]) = *p;
     s->tail[f]++;
     if (f < s->Q) s->sw_queued[s->port_sw[f]]++;
@@ -683,7 +694,7 @@ static void forward(sim *s, uint32_t w, uint32_t t)
             s->sw_queued[w]--;
             p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
             p.hopsum += s->port_delta[qe] + 1;
-            push(s, d, &p);
+            push(s, d, &p, t, s->port_sigma[qe]);
             s->eg_busy[qe] = t + s->port_sigma[qe];
             s->eg_rr[qe] = (i + 1) % P;
             s->pkt_hops++;
@@ -729,7 +740,7 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             p.pslot = s->port_base[dnode] + L->dst_port;
             p.last = L->pkts_left == 1;
             p.key = L->key;
-            push(s, f, &p);
+            push(s, f, &p, t, s->host_sigma[r]);
             n->busy = t + s->host_sigma[r];
             n->rr = (q + 1) % NLANE;
             s->pkts_injected++;
@@ -755,6 +766,7 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     pkt *h = ready_head(s, f, t);
     if (!h) return;
     pkt p = *h;
+    if (p.dst != r) s->violations++;
     pop(s, f, t);
     s->pkts_delivered++;
     s->changed = 1;
@@ -975,6 +987,8 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
         if (dl + 1 < s->rdv_delay) s->rdv_delay = dl + 1;
     }
     s->slots = calloc((size_t)s->nf * s->cap, sizeof(pkt));
+    s->last_push = malloc(sizeof(uint32_t) * s->nf);
+    for (uint32_t f = 0; f < s->nf; f++) s->last_push[f] = UNSET;
     s->eg_busy = calloc(s->Q + 1, sizeof(uint32_t));
     s->eg_rr = calloc(s->Q + 1, sizeof(uint32_t));
     s->sw_queued = calloc(s->S + 1, sizeof(uint32_t));
@@ -1021,12 +1035,13 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     out->digest[e] = s->digest;
     out->ticks_active[e] = active;
     out->rec_count[e] = s->rec_count;
+    out->violations[e] = s->violations;
 
     free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
     free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
     free(s->col_base); free(s->node_rank); free(s->node_member);
     free(s->head); free(s->tail); free(s->tail0); free(s->slots);
-    free(s->poplog); free(s->credit_delay);
+    free(s->poplog); free(s->credit_delay); free(s->last_push);
     free(s->eg_busy); free(s->eg_rr); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
     free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
     return 0;

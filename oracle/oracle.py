@@ -56,7 +56,8 @@ class _Batch(C.Structure):
 _OUT = [("status", "u4"), ("end_tick", "u4"), ("now", "u4"), ("pkts_injected", "u8"),
         ("pkt_hops", "u8"), ("pkts_delivered", "u8"), ("msgs_delivered", "u8"),
         ("digest", "u8"), ("ticks_active", "u8"), ("node_start", "u4"), ("node_end", "u4"),
-        ("rec_count", "u4"), ("rec_sender", "u4"), ("rec_key", "u4"), ("rec_tick", "u4")]
+        ("rec_count", "u4"), ("rec_sender", "u4"), ("rec_key", "u4"), ("rec_tick", "u4"),
+        ("violations", "u8")]
 
 
 class _Out(C.Structure):
@@ -64,7 +65,7 @@ class _Out(C.Structure):
 
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}
 
 
 def build(force: bool = False) -> str:
@@ -77,27 +78,32 @@ def build(force: bool = False) -> str:
     return LIB
 
 
-def _load():
-    global _lib
+def _load(path: str | None = None):
+    """The oracle library (built on first use), or another build of the same
+    source at `path` (the tests' planted-mistake copies)."""
     with _lock:
-        if _lib is None:
-            lib = C.CDLL(build())
+        key = path or LIB
+        if key not in _libs:
+            lib = C.CDLL(path or build())
             lib.orc_run.argtypes = [C.POINTER(_Batch), C.c_uint32, C.c_uint32, C.c_uint32,
                                     C.POINTER(_Out)]
             lib.orc_run.restype = C.c_int
             lib.orc_mix64.argtypes = [C.c_uint64]
             lib.orc_mix64.restype = C.c_uint64
-            _lib = lib
-    return _lib
+            _libs[key] = lib
+    return _libs[key]
 
 
 def mix64(z: int) -> int:
     return int(_load().orc_mix64(C.c_uint64(z & (2 ** 64 - 1))))
 
 
-def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1) -> dict:
-    """Run experiments [e0, e1) of a packed batch (all when e1 == 0)."""
-    lib = _load()
+def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
+        lib_path: str | None = None) -> dict:
+    """Run experiments [e0, e1) of a packed batch (all when e1 == 0).
+    `violations` counts broken invariants (queue over capacity, a link faster
+    than its serialisation time, a packet delivered to the wrong host)."""
+    lib = _load(lib_path)
     keep = {}
     b = _Batch()
     b.version = packed["version"]
@@ -116,7 +122,7 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1) -> dict:
     res = {"status": np.full(E, UNSET, np.uint32), "end_tick": np.zeros(E, np.uint32),
            "now": np.zeros(E, np.uint32)}
     for k in ("pkts_injected", "pkt_hops", "pkts_delivered", "msgs_delivered", "digest",
-              "ticks_active"):
+              "ticks_active", "violations"):
         res[k] = np.zeros(E, np.uint64)
     res["node_start"] = np.full(max(1, int(nn.sum())), UNSET, np.uint32)
     res["node_end"] = np.full(max(1, int(nn.sum())), UNSET, np.uint32)

@@ -442,3 +442,52 @@ def test_table_limits_overflow_exactly_one_past_the_limit():
     for e, x in enumerate(b.experiments):
         over = x.label["n"] in (65, 129, 17)
         assert r["status"][e] == (O.ST_OVERFLOW if over else O.ST_DONE), x.label
+
+
+# ---------------------------------------------------------------- invariants
+def _incast(n_pkts: int, sigma: int = 1):
+    """Hosts 0 and 1 each send n_pkts packets to host 2 through one switch
+    with 2-slot queues: the egress to host 2 is the bottleneck, so both
+    ingress queues run full and the credit rule is what holds them."""
+    t = I.single_switch(3, sigma, 1)
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], n_pkts * 4096)
+    w.collective(I.P2P, [1, 2], n_pkts * 4096)
+    return I.Batch([I.Experiment(t, w, tick_ps=1000, chunk=1 << 20, cap=2)]).pack()
+
+
+def _planted(tmp_path, name: str, old: str, new: str) -> str:
+    """A copy of the oracle with one planted mistake, built with gcc."""
+    src = open(O.SRC).read()
+    assert src.count(old) == 1, old
+    c = tmp_path / f"{name}.c"
+    c.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib{name}.so"
+    import subprocess
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-shared", "-fPIC", "-o", str(lib), str(c)])
+    return str(lib)
+
+
+def test_invariants_hold():
+    """Lossless credit (no queue beyond cap), one packet per serialisation
+    time on every link, and delivery at the addressed host, over ring, tree,
+    relay, point-to-point and incast traffic."""
+    for packed in (I.config1().pack(), I.config2(n_exp=8).pack(), _incast(20), _incast(9, 3),
+                   I.gpt_small(algo=I.TREE, seeds=(0,)).pack()):
+        r = O.run(packed)
+        assert (r["violations"] == 0).all()
+        assert (r["status"] == O.ST_DONE).all()
+
+
+def test_invariant_checks_catch_planted_mistakes(tmp_path):
+    """Each check fails on an oracle with the matching mistake planted: credit
+    always granted (queues overflow), the egress busy time not kept (a link
+    outruns its serialisation time), routing by the wrong destination."""
+    no_credit = _planted(tmp_path, "no_credit", "return s->tail[f] - (h - back) < s->cap;",
+                         "return 1;")
+    assert O.run(_incast(20), lib_path=no_credit)["violations"][0] > 0
+    no_busy = _planted(tmp_path, "no_busy", "s->eg_busy[qe] = t + s->port_sigma[qe];", "")
+    assert O.run(_incast(9, 3), lib_path=no_busy)["violations"][0] > 0
+    bad_route = _planted(tmp_path, "bad_route", "s->route[(size_t)w * s->H + p->dst]",
+                         "s->route[(size_t)w * s->H + (p->dst ^ 1u)]")
+    assert O.run(_incast(3), lib_path=bad_route)["violations"][0] > 0
