@@ -373,10 +373,10 @@ __device__ __forceinline__ u32 route_port(const VW &V, u32 s, u32 p0, uint4 pk)
 // so their steps are independent.  Pokes for other items go to `poke`.
 // Returns the earliest tick this warp knows of at which something may happen
 // (the switches' own next wakes and the wakes they gave other items); *fail
-// gets a failure key.
+// gets a failure key.  `qstaged`: the queue words are in shared memory.
 template <class VT>
 __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t, u32 *poke,
-                                           SwSmem *sm, u32 *fail, bool staged)
+                                           SwSmem *sm, u32 *fail, bool qstaged)
 {
     // the view (see ViewOf): as a register copy, stores through the state
     // pointers cannot alias it, so its fields are loaded once per tick
@@ -420,7 +420,7 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
     // with the queue words in shared memory these are cheap, so every free
     // egress gets them now; in global memory only egresses that a packet
     // wants load them (below)
-    if (staged) {
+    if (qstaged) {
 #pragma unroll
         for (u32 j = 0; j < 2; j++) {
             if (seg_[j] == kUnset || st_[j].x > t) continue;
@@ -461,7 +461,7 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
         if (st.x > t) continue;             // busy: its heads wake the switch at t+1
         const uint4 pr = pr_[j];            // downstream queue, sigma, delta, its owner
         const u32 dq = pr.x, sg = pr.y, dl = pr.z;
-        if (!staged) {
+        if (!qstaged) {
             const u64 dpop = ld_vol64(&V.q_pop[dq]);
             dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
             dtail_[j] = (u32)V.q_push[dq];
@@ -510,9 +510,10 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
 // switch's pending wake; pokes for other items go to `poke`.  Returns the
 // earliest tick this warp knows of at which something may happen (its own
 // next wake and the wakes it gave other items); *fail gets a failure key.
+// `qstaged`: the queue words are in shared memory.
 template <class VT>
 __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t, u32 old,
-                                           u32 *poke, SwSmem *sm, u32 *fail, bool staged)
+                                           u32 *poke, SwSmem *sm, u32 *fail, bool qstaged)
 {
     // the view (see ViewOf): as a register copy, stores through the state
     // pointers cannot alias it, so its fields are loaded once per tick
@@ -545,7 +546,7 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
     // with the queue words in shared memory these are cheap, so every free
     // egress gets them now; in global memory only egresses that a packet
     // wants load them (below)
-    if (staged) {
+    if (qstaged) {
 #pragma unroll
         for (u32 j = 0; j < 2; j++) {
             if (lane + 32 * j >= np || st_[j].x > t) continue;
@@ -585,7 +586,7 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         if (st.x > t) continue;             // busy: its heads wake the switch at t+1
         const uint4 pr = pr_[j];            // downstream queue, sigma, delta, its owner
         const u32 dq = pr.x, sg = pr.y, dl = pr.z;
-        if (!staged) {
+        if (!qstaged) {
             const u64 dpop = ld_vol64(&V.q_pop[dq]);
             dhead_[j] = (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u);
             dtail_[j] = (u32)V.q_push[dq];
