@@ -1,0 +1,45 @@
+"""bench.py's JSON-line contract, on the CPU: the reference arm (the oracle on
+the host cores) prints exactly one line with the agreed keys, and the GPU arm
+fails loudly on a machine without a GPU instead of falling back."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args):
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_json_line():
+    p = _bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    assert r["impl"] == "reference"
+    assert r["metric"] == "simulated packet-hops/s over experiment batch"
+    assert r["unit"] == "packet-hops/s" and r["higher_is_better"] is True
+    assert r["value"] > 0 and r["ms_per_step"] > 0
+    assert (r["n_gpus"], r["steps"], r["warmup"]) == (1, 1, 3)
+    assert r["scaling"] == "weak" and r["vs_baseline"] is None and r["data"] == "synthetic"
+    assert r["config"]["workload"] == "config2"
+    cb = r["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == r["value"]
+    assert cb["sample"]
+    e2e = r["e2e"]
+    assert e2e["value"] == r["value"] and e2e["unit"] == r["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
+def test_gpu_arm_fails_loudly_without_a_gpu():
+    p = _bench("--steps", "1", "--warmup", "3")
+    assert p.returncode != 0
+    assert not p.stdout.strip()
