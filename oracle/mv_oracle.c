@@ -89,6 +89,18 @@ typedef struct orc_out {
     uint64_t *violations;                   /* per experiment: broken invariants */
 } orc_out;
 
+/* Optional event trace of one run (parity bisection): what happened at which
+ * tick, in the order the serial phases meet it.
+ *   EV_START   a = node, b = rank          EV_END     a = node, b = end tick
+ *   EV_INJECT  a = rank, b = connection key
+ *   EV_HOP     a = egress port, b = ingress queue it pulled from (switch hop)
+ *   EV_DELIVER a = rank, b = sender node   EV_MESSAGE a = rank, b = sender node
+ *                                            (the message's last packet) */
+typedef struct orc_event {
+    uint32_t tick, kind, a, b;
+} orc_event;
+enum { EV_START = 1, EV_END = 2, EV_INJECT = 3, EV_HOP = 4, EV_DELIVER = 5, EV_MESSAGE = 6 };
+
 /* ------------------------------------------------------------------------ */
 /* splitmix64 finaliser (S. Vigna, public domain splitmix64.c): the one
  * counter-based hash used for ECMP, durations and the digest.              */
@@ -182,7 +194,25 @@ typedef struct sim {
      * delivered at the host it was addressed to */
     uint32_t *last_push;            /* nf: tick of the last push into the queue */
     uint64_t violations;
+    /* event trace (none when trace is NULL): events beyond trace_cap are
+     * counted, not kept */
+    orc_event *trace;
+    uint64_t trace_cap, trace_n;
+    uint32_t now;                   /* the tick being simulated */
 } sim;
+
+static void ev(sim *s, uint32_t kind, uint32_t a, uint32_t b)
+{
+    if (!s->trace) return;
+    if (s->trace_n < s->trace_cap) {
+        orc_event *x = &s->trace[s->trace_n];
+        x->tick = s->now;
+        x->kind = kind;
+        x->a = a;
+        x->b = b;
+    }
+    s->trace_n++;
+}
 
 /* A failure stops the experiment at the end of the current tick.  Within
  * that tick every other entity still completes its step (Multiverse section
@@ -462,6 +492,7 @@ static void pend_add(sim *s, uint32_t r, uint32_t u, uint32_t st)
 
 static void complete(sim *s, uint32_t u, uint32_t c)
 {
+    ev(s, EV_END, u, c);
     uint32_t r = s->node_rank[u];
     s->end[u] = c;
     s->nodes_left--;
@@ -588,16 +619,19 @@ static void dag_step(sim *s, uint32_t r, uint32_t t)
         switch (s->node_kind[u]) {
         case K_COMPUTE:
             s->start[u] = t;
+            ev(s, EV_START, u, r);
             complete(s, u, t + compute_ticks(s, u));
             break;
         case K_INTRA:
             s->start[u] = t;
+            ev(s, EV_START, u, r);
             act_add(s, r, u);
             break;
         case K_NET:
             net_join(s, r, u, t);
             if (n->tick_fail) return;     /* a join that does not fit never starts */
             s->start[u] = t;
+            ev(s, EV_START, u, r);
             if (s->outstanding[u] == 0) {
                 free_ports(s, r, u);
                 complete(s, u, t);
@@ -695,6 +729,7 @@ static void forward(sim *s, uint32_t w, uint32_t t)
             p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
             p.hopsum += s->port_delta[qe] + 1;
             push(s, d, &p, t, s->port_sigma[qe]);
+            ev(s, EV_HOP, qe, base + i);
             s->eg_busy[qe] = t + s->port_sigma[qe];
             s->eg_rr[qe] = (i + 1) % P;
             s->pkt_hops++;
@@ -741,6 +776,7 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             p.last = L->pkts_left == 1;
             p.key = L->key;
             push(s, f, &p, t, s->host_sigma[r]);
+            ev(s, EV_INJECT, r, p.key);
             n->busy = t + s->host_sigma[r];
             n->rr = (q + 1) % NLANE;
             s->pkts_injected++;
@@ -770,7 +806,9 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     pop(s, f, t);
     s->pkts_delivered++;
     s->changed = 1;
+    ev(s, EV_DELIVER, r, p.sender);
     if (!p.last) return;
+    ev(s, EV_MESSAGE, r, p.sender);
     nic *n = &s->nics[r];
     n->port_count[p.pslot]++;
     uint32_t own = n->port_node[p.pslot];
@@ -858,6 +896,7 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
     while (s->status == ST_RUNNING) {
         if (s->nodes_left == 0) { s->status = ST_DONE; break; }
         if (t >= limit) break;
+        s->now = t;
         memcpy(s->tail0, s->tail, sizeof(uint32_t) * s->nf);
         s->changed = 0;
         for (uint32_t r = 0; r < s->R; r++) {
@@ -896,12 +935,15 @@ typedef struct offs {
 } offs;
 
 static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit,
-                   orc_out *out, uint64_t node_off, uint64_t rec_off)
+                   orc_out *out, uint64_t node_off, uint64_t rec_off, orc_event *trace,
+                   uint64_t trace_cap, uint64_t *trace_n)
 {
     sim S_, *s = &S_;
     memset(s, 0, sizeof *s);
     s->b = b;
     s->e = e;
+    s->trace = trace;
+    s->trace_cap = trace_cap;
     uint32_t ti = b->exp_topo[e], wi = b->exp_work[e];
     s->H = b->topo_nhosts[ti];
     s->S = b->topo_nsw[ti];
@@ -1036,6 +1078,7 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     out->ticks_active[e] = active;
     out->rec_count[e] = s->rec_count;
     out->violations[e] = s->violations;
+    if (trace_n) *trace_n = s->trace_n;
 
     free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
     free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
@@ -1052,7 +1095,8 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
  * results go to node_start/node_end at the experiment's offset in the
  * concatenation of all experiments' nodes; flow records at the experiment's
  * offset in the concatenation of rec_cap-sized blocks. */
-int orc_run(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out)
+int orc_run_traced(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out,
+                   orc_event *trace, uint64_t trace_cap, uint64_t *trace_n)
 {
     if (b->version != 1) return -1;
     offs o;
@@ -1070,13 +1114,20 @@ int orc_run(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_ou
     if (e1 == 0 || e1 > b->n_exps) e1 = b->n_exps;
     uint64_t node_off = 0, rec_off = 0;
     for (uint32_t e = 0; e < e1; e++) {
-        if (e >= e0) run_one(b, &o, e, limit, out, node_off, rec_off);
+        if (e >= e0) run_one(b, &o, e, limit, out, node_off, rec_off, trace, trace_cap, trace_n);
         node_off += b->work_nnodes[b->exp_work[e]];
         rec_off += b->exp_rec_cap[e];
     }
     free(o.host); free(o.sw); free(o.port); free(rank); free(o.node); free(o.edge);
     free(o.coll); free(o.memb); free(o.a2a); free(o.a2a_in);
     return 0;
+}
+
+/* Without a trace.  With one (orc_run_traced), give e1 = e0 + 1: the events
+ * of one experiment; *trace_n gets how many happened. */
+int orc_run(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out)
+{
+    return orc_run_traced(b, e0, e1, limit, out, NULL, 0, NULL);
 }
 
 /* exported for the tests that pin the hash against its published values */

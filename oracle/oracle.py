@@ -46,6 +46,9 @@ _ARR = [("topo_nhosts", "u4"), ("topo_nsw", "u4"), ("topo_nports", "u4"),
         ("exp_dur_seed", "u8"), ("exp_ecmp_seed", "u8"), ("exp_gpu_mem", "u8"),
         ("exp_rec_cap", "u4")]
 _CT = {"u4": _P32, "u8": _P64, "i4": _PI32}
+# event trace records (struct orc_event): kinds and their (a, b) fields
+EV_START, EV_END, EV_INJECT, EV_HOP, EV_DELIVER, EV_MESSAGE = range(1, 7)
+EVENT = np.dtype([("tick", np.uint32), ("kind", np.uint32), ("a", np.uint32), ("b", np.uint32)])
 _NP = {"u4": np.uint32, "u8": np.uint64, "i4": np.int32}
 
 
@@ -88,6 +91,10 @@ def _load(path: str | None = None):
             lib.orc_run.argtypes = [C.POINTER(_Batch), C.c_uint32, C.c_uint32, C.c_uint32,
                                     C.POINTER(_Out)]
             lib.orc_run.restype = C.c_int
+            lib.orc_run_traced.argtypes = [C.POINTER(_Batch), C.c_uint32, C.c_uint32,
+                                           C.c_uint32, C.POINTER(_Out), C.c_void_p,
+                                           C.c_uint64, _P64]
+            lib.orc_run_traced.restype = C.c_int
             lib.orc_mix64.argtypes = [C.c_uint64]
             lib.orc_mix64.restype = C.c_uint64
             _libs[key] = lib
@@ -99,10 +106,12 @@ def mix64(z: int) -> int:
 
 
 def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
-        lib_path: str | None = None) -> dict:
+        lib_path: str | None = None, trace_cap: int = 0) -> dict:
     """Run experiments [e0, e1) of a packed batch (all when e1 == 0).
     `violations` counts broken invariants (queue over capacity, a link faster
-    than its serialisation time, a packet delivered to the wrong host)."""
+    than its serialisation time, a packet delivered to the wrong host).
+    With trace_cap > 0 (one experiment: e1 = e0 + 1), `trace` holds its first
+    trace_cap events (EVENT records) and `trace_total` how many happened."""
     lib = _load(lib_path)
     keep = {}
     b = _Batch()
@@ -132,9 +141,59 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
     o = _Out()
     for n, t in _OUT:
         setattr(o, n, res[n].ctypes.data_as(_CT[t]))
-    rcode = lib.orc_run(C.byref(b), e0, e1, limit, C.byref(o))
+    if trace_cap:
+        if e1 != e0 + 1:
+            raise ValueError("a trace covers one experiment: e1 must be e0 + 1")
+        ev = np.zeros(trace_cap, EVENT)
+        n = C.c_uint64(0)
+        rcode = lib.orc_run_traced(C.byref(b), e0, e1, limit, C.byref(o),
+                                   ev.ctypes.data_as(C.c_void_p), trace_cap, C.byref(n))
+        res["trace"] = ev[: min(trace_cap, n.value)]
+        res["trace_total"] = n.value
+    else:
+        rcode = lib.orc_run(C.byref(b), e0, e1, limit, C.byref(o))
     if rcode != 0:
         raise RuntimeError(f"oracle rejected the batch ({rcode})")
     res["node_offset"] = np.concatenate([[0], np.cumsum(nn)])
     res["rec_offset"] = np.concatenate([[0], np.cumsum(rc)])
     return res
+
+
+def first_divergence(packed: dict, other: dict, e: int, limit: int = UNSET - 1) -> dict | None:
+    """Where experiment e of `other` (results of the same packed batch from
+    another implementation, in the layout mv.Simulator.results() returns)
+    first departs from the oracle: the earliest tick at which a node start,
+    a node end or a message completion differs, with what each side has
+    there.  None when the node and message results agree.  The oracle's event
+    trace around that tick (run(..., trace_cap=...)) then shows what led to
+    it."""
+    r = run(packed, e, e + 1, limit)
+    a0, a1 = int(r["node_offset"][e]), int(r["node_offset"][e + 1])
+    b0 = int(other["node_offset"][e])
+    found = []
+    for k in ("node_start", "node_end"):
+        mine = r[k][a0:a1].astype(np.int64)
+        theirs = other[k][b0:b0 + (a1 - a0)].astype(np.int64)
+        bad = np.nonzero(mine != theirs)[0]
+        if bad.size:
+            # the earlier of the two values is where the runs have parted
+            at = np.minimum(mine[bad], theirs[bad])
+            j = int(np.argmin(at))
+            found.append({"tick": int(at[j]), "what": k, "node": int(bad[j]),
+                          "oracle": int(mine[bad[j]]), "other": int(theirs[bad[j]])})
+    n_mine, n_theirs = int(r["rec_count"][e]), int(other["rec_count"][e])
+    c0, c1 = int(r["rec_offset"][e]), int(other["rec_offset"][e])
+    k = min(n_mine, n_theirs, int(r["rec_offset"][e + 1]) - c0)
+    if k:
+        keys = ("rec_tick", "rec_sender", "rec_key")
+        mine = np.stack([r[x][c0:c0 + k] for x in keys], 1)
+        theirs = np.stack([other[x][c1:c1 + k] for x in keys], 1)
+        mine = mine[np.lexsort(mine.T[::-1])]
+        theirs = theirs[np.lexsort(theirs.T[::-1])]
+        bad = np.nonzero((mine != theirs).any(1))[0]
+        if bad.size:
+            j = int(bad[0])
+            found.append({"tick": int(min(mine[j, 0], theirs[j, 0])), "what": "message",
+                          "oracle": [int(x) for x in mine[j]],
+                          "other": [int(x) for x in theirs[j]]})
+    return min(found, key=lambda f: f["tick"]) if found else None

@@ -105,12 +105,17 @@ def test_credit_loop_needs_two_delta_plus_two():
 
 
 # ---------------------------------------------------------------- hand trace
-def test_incast_hand_trace():
+def _incast_gold():
     gold = {}
     for line in open(os.path.join(GOLDEN, "incast_cap2_delta1.txt")):
         if line.strip() and not line.startswith("#"):
             k, *v = line.split()
             gold[k] = [int(x) for x in v]
+    return gold
+
+
+def test_incast_hand_trace():
+    gold = _incast_gold()
     t = I.single_switch(3, 1, 1)
     w = I.Workload(3)
     w.collective(I.P2P, [0, 2], 3 * 4096)
@@ -120,6 +125,53 @@ def test_incast_hand_trace():
     assert sorted(r["rec_tick"][: r["rec_count"][0]]) == gold["delivery_ticks"]
     assert r["pkts_injected"][0] == gold["packets"][0]
     assert r["pkt_hops"][0] == gold["packet_hops"][0]
+
+
+def test_incast_event_trace_matches_hand_trace():
+    """The oracle's event trace reproduces the hand-traced table tick by tick:
+    every injection, switch hop and delivery of A's and B's packets."""
+    gold = _incast_gold()
+    t = I.single_switch(3, 1, 1)
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], 3 * 4096)
+    w.collective(I.P2P, [1, 2], 3 * 4096)
+    p = I.Batch([I.Experiment(t, w, tick_ps=1000, chunk=1 << 20, cap=2)]).pack()
+    r = O.run(p, 0, 1, trace_cap=1000)
+    ev = r["trace"]
+    assert r["trace_total"] == len(ev)
+    sender_node = {"A": 0, "B": 1}          # node order: A's send, B's send, C's receives
+    for who, h in (("A", 0), ("B", 1)):
+        inj = ev[(ev["kind"] == O.EV_INJECT) & (ev["a"] == h)]["tick"]
+        hop = ev[(ev["kind"] == O.EV_HOP) & (ev["b"] == h)]["tick"]        # ingress queue = port h
+        dlv = ev[(ev["kind"] == O.EV_DELIVER) & (ev["b"] == sender_node[who])]["tick"]
+        assert list(inj) == gold[f"inject_ticks_{who}"]
+        assert list(hop) == gold[f"hop_ticks_{who}"]
+        assert list(dlv) == gold[f"deliver_ticks_{who}"]
+    assert (np.diff(ev["tick"].astype(np.int64)) >= 0).all()
+    ends = ev[ev["kind"] == O.EV_END]
+    assert sorted(zip(ends["a"], ends["b"])) == list(enumerate(gold["node_end"]))
+
+
+def test_first_divergence_finds_the_earliest_difference():
+    b = I.config1()
+    p = b.pack()
+    mine = O.run(p)
+    assert O.first_divergence(p, mine, 3) is None
+    other = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in mine.items()}
+    e, n0 = 3, int(mine["node_offset"][3])
+    other["node_end"][n0 + 5] += 7
+    d = O.first_divergence(p, other, e)
+    assert d["what"] == "node_end" and d["node"] == 5
+    assert d["tick"] == int(mine["node_end"][n0 + 5])
+    other = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in mine.items()}
+    import dataclasses
+    p2 = I.Batch([dataclasses.replace(b.experiments[0], rec_cap=64)]).pack()
+    mine2 = O.run(p2)
+    other2 = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in mine2.items()}
+    j = int(np.argsort(mine2["rec_tick"][:64])[10])
+    other2["rec_tick"][j] += 1
+    d = O.first_divergence(p2, other2, 0)
+    assert d["what"] == "message" and d["tick"] <= int(mine2["rec_tick"][j])
 
 
 # ---------------------------------------------------------------- pipelined broadcast
