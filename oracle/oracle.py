@@ -83,7 +83,9 @@ def build(force: bool = False) -> str:
 
 def _load(path: str | None = None):
     """The oracle library (built on first use), or another build of the same
-    source at `path` (the tests' planted-mistake copies)."""
+    source at `path` or named by MV_ORACLE_LIB (the tests' planted-mistake
+    copies)."""
+    path = path or os.environ.get("MV_ORACLE_LIB") or None
     with _lock:
         key = path or LIB
         if key not in _libs:

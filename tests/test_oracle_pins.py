@@ -543,3 +543,156 @@ def test_invariant_checks_catch_planted_mistakes(tmp_path):
     bad_route = _planted(tmp_path, "bad_route", "s->route[(size_t)w * s->H + p->dst]",
                          "s->route[(size_t)w * s->H + (p->dst ^ 1u)]")
     assert O.run(_incast(3), lib_path=bad_route)["violations"][0] > 0
+
+
+# ---------------------------------------------------------------- schedule details, by trace
+def _per_message(ev, sender):
+    """Packets of each message from node `sender`, in delivery order."""
+    out, n = [], 0
+    for x in ev:
+        if x["kind"] == O.EV_DELIVER and x["b"] == sender:
+            n += 1
+        elif x["kind"] == O.EV_MESSAGE and x["b"] == sender:
+            out.append(n)
+            n = 0
+    return out
+
+
+def _traced(topo, work, **kw):
+    kw.setdefault("tick_ps", 1000)
+    r = O.run(I.Batch([I.Experiment(topo, work, **kw)]).pack(), 0, 1, trace_cap=100_000)
+    assert r["status"][0] == O.ST_DONE and r["trace_total"] == len(r["trace"])
+    return r["trace"]
+
+
+def test_ring_step_sends_block_i_minus_k():
+    """R12/R13: at step k member i sends block (i - k) mod N.  Reduce-scatter
+    of 12,289 B over 3 ranks, one loop: blocks of ceil(12289/3) = 4,097 B, the
+    last 4,095 B, so 2, 2 and 1 packets.  Member 0 sends blocks 0 then 2 (2, 1
+    packets), member 1 blocks 1 then 0 (2, 2), member 2 blocks 2 then 1 (1, 2)."""
+    w = I.Workload(3)
+    ids = w.collective(I.RS, [0, 1, 2], 12289)
+    ev = _traced(I.single_switch(3, 1, 0), w, nc=1, chunk=1 << 20)
+    assert [_per_message(ev, ids[i]) for i in range(3)] == [[2, 1], [2, 2], [1, 2]]
+
+
+def test_nic_round_robin_and_partition_extra_byte():
+    """R7 and R12: a NIC serves its send lanes round-robin from its pointer,
+    and the first S mod NC partitions carry one byte more.  Reduce-scatter of
+    16,385 B over 2 ranks with NC = 2: channel 0's partition is 8,193 B, so
+    member 0's block on channel 0 is 4,097 B (2 packets) and on channel 1
+    4,096 B (1 packet).  Member 0 injects on channel 0, channel 1, channel 0."""
+    w = I.Workload(2)
+    w.collective(I.RS, [0, 1], 16385)
+    ev = _traced(I.single_switch(2, 1, 0), w, nc=2, chunk=1 << 20)
+    keys = ev[(ev["kind"] == O.EV_INJECT) & (ev["a"] == 0)]["b"]
+    assert len(keys) == 3 and keys[0] == keys[2] and keys[0] != keys[1]
+
+
+def test_alltoall_chunks_stripe_over_lanes():
+    """R25: all-to-all chunk j goes on lane j mod NC, destinations in rotation
+    order from the next rank.  Rank 0 sends two chunks to rank 1 and one each
+    to ranks 2 and 3 (a packet a chunk), NC = 2: lane 0 carries chunks 0 and 2
+    (to ranks 1 and 2), lane 1 chunks 1 and 3 (to ranks 1 and 3), so the
+    NIC's round robin delivers to ranks 1, 1, 2, 3."""
+    w = I.Workload(4)
+    ids = w.collective(I.A2A, [0, 1, 2, 3], 0, a2a={(0, 1): 8192, (0, 2): 4096, (0, 3): 4096})
+    ev = _traced(I.single_switch(4, 1, 0), w, nc=2, chunk=4096)
+    recv = ev[(ev["kind"] == O.EV_DELIVER) & (ev["b"] == ids[0])]["a"]
+    assert list(recv) == [1, 1, 2, 3]
+
+
+def test_duration_range_includes_both_ends():
+    """R18: U[lo, hi] includes hi.  With hi = lo + 1 ns and 1 tick = 1 ns, 64
+    hashed compute nodes take both 1,000 and 1,001 ticks."""
+    w = I.Workload(1)
+    us = [w.compute(0, 1000, 1001, key=k) for k in range(64)]
+    w.chain(*us)
+    r = run1(I.single_switch(1, 1, 0), w, tick_ps=1000)
+    d = r["node_end"][:64].astype(np.int64) - r["node_start"][:64]
+    assert set(d.tolist()) == {1000, 1001}
+
+
+def test_ecmp_one_path_per_connection_spread_over_up_ports():
+    """R10: the up port is a hash of the connection, so all packets of a
+    connection take one path (in order), and connections spread over the up
+    ports.  Eight 3-packet messages from leaf 0's hosts to leaf 1's over four
+    spines: each ingress port of leaf 0 forwards up on exactly one port, and
+    more than one up port is used."""
+    t = I.leaf_spine(2, 4, 8)
+    w = I.Workload(16)
+    for i in range(8):
+        w.collective(I.P2P, [i, 8 + i], 3 * 4096)
+    ev = _traced(t, w, chunk=1 << 20)
+    hops = ev[ev["kind"] == O.EV_HOP]
+    up = {}
+    for x in hops:
+        if x["b"] < 8:                     # leaf 0's host-facing ingress queues 0..7
+            up.setdefault(int(x["b"]), set()).add(int(x["a"]))
+    assert sorted(up) == list(range(8))
+    assert all(len(v) == 1 for v in up.values())
+    assert all(min(v) >= 8 for v in up.values())           # ports 8..11 face the spines
+    assert len(set().union(*up.values())) > 1
+
+
+def test_same_tick_starts_go_in_node_order():
+    """R7/R15: nodes of a rank due at one tick start in node order, so the
+    lower node's send lane takes the lower lane slot and the NIC's round robin
+    (pointer 0) serves it first.  Rank 0's two root sends, to rank 1 (the
+    lower node) and to rank 2: the first delivery is at rank 1."""
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 1], 2 * 4096)
+    w.collective(I.P2P, [0, 2], 2 * 4096)
+    ev = _traced(I.single_switch(3, 1, 0), w, chunk=1 << 20)
+    recv = ev[ev["kind"] == O.EV_DELIVER]["a"]          # rank 0 is the only sender
+    assert list(recv) == [1, 2, 1, 2]
+
+
+def test_relay_partitions_first_get_the_extra_byte():
+    """R19 with R12's rule: the slice's first S mod K partitions carry one
+    byte more.  S = 3*4096 + 1 in K = 3 partitions over one hop: the first
+    partition is 4,097 B (2 packets), the others 4,096 B (1 packet)."""
+    w = I.relay_chain(2, 3 * 4096 + 1, 3)
+    ev = _traced(I.single_switch(2, 1, 0), w)
+    sender = int(ev[ev["kind"] == O.EV_DELIVER]["b"][0])
+    assert _per_message(ev, sender) == [2, 1, 1]
+
+
+def test_zero_byte_message_is_one_packet():
+    """R2: a message of no bytes still costs one packet (a synchronisation
+    message): a 0-byte point-to-point send behaves as the 1-packet lone
+    message, (n-1) + L(1+delta) = 2(1+delta) ticks from its first injection."""
+    delta = 3
+    r = run1(I.single_switch(2, 1, delta), I.lone_message(2, 0, 1, 0), chunk=1 << 20)
+    assert r["pkts_injected"][0] == 1 and r["msgs_delivered"][0] == 1
+    first = 1 + delta                       # the join reaches the sender 1 + delta later
+    assert r["node_end"][1] == first + 2 * (1 + delta)
+
+
+def test_point_to_point_splits_into_chunks():
+    """R25: a point-to-point send is a train of messages of at most C bytes:
+    S = 5*4096 + 100 with C = 8192 is 3 messages (8192, 8192, 4196 B) of
+    2 + 2 + 2 = 6 packets."""
+    r = run1(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 5 * 4096 + 100), chunk=8192)
+    assert r["msgs_delivered"][0] == 3 and r["pkts_injected"][0] == 6
+
+
+def test_digest_depends_on_completion_ticks():
+    """The per-experiment digest covers every message's completion tick: the
+    same messages on links one tick slower give another digest."""
+    d = [run1(I.single_switch(3, 1, delta), I.lone_message(3, 0, 2, 3 * 4096),
+              chunk=4096)["digest"][0] for delta in (0, 1)]
+    assert d[0] != d[1]
+
+
+def test_down_route_takes_the_lowest_port():
+    """R10: a switch sends a packet down the lowest port under which its
+    destination sits.  Leaf-spine with two parallel links per leaf-spine
+    pair: the spine reaches leaf 1 on its ports 2 and 3 and uses port 2."""
+    t = I.leaf_spine(2, 1, 1, links_per_pair=2)
+    ev = _traced(t, I.lone_message(2, 0, 1, 4 * 4096), chunk=1 << 20)
+    nports = t.arrays()["sw_nports"]
+    spine_base = int(nports[0] + nports[1])        # switches: leaf 0, leaf 1, spine
+    at_spine = {int(x["a"]) - spine_base for x in ev[ev["kind"] == O.EV_HOP]
+                if spine_base <= x["a"] < spine_base + nports[2]}
+    assert at_spine == {2}
