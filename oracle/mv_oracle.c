@@ -100,6 +100,7 @@ typedef struct orc_event {
     uint32_t tick, kind, a, b;
 } orc_event;
 enum { EV_START = 1, EV_END = 2, EV_INJECT = 3, EV_HOP = 4, EV_DELIVER = 5, EV_MESSAGE = 6 };
+#define ORC_NO_SKIP 1u
 
 /* ------------------------------------------------------------------------ */
 /* splitmix64 finaliser (S. Vigna, public domain splitmix64.c): the one
@@ -199,6 +200,7 @@ typedef struct sim {
     orc_event *trace;
     uint64_t trace_cap, trace_n;
     uint32_t now;                   /* the tick being simulated */
+    int no_skip;                    /* step every tick instead of jumping to the next event */
 } sim;
 
 static void ev(sim *s, uint32_t kind, uint32_t a, uint32_t b)
@@ -915,7 +917,7 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
         if (s->changed) { t++; continue; }
         uint32_t nx = next_event(s, t);
         if (nx == UNSET) { s->status = ST_DEADLOCK; t++; break; }
-        t = nx;
+        t = s->no_skip ? t + 1 : nx;
     }
     *ticks_active = active;
     *now_out = t;
@@ -936,7 +938,7 @@ typedef struct offs {
 
 static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit,
                    orc_out *out, uint64_t node_off, uint64_t rec_off, orc_event *trace,
-                   uint64_t trace_cap, uint64_t *trace_n)
+                   uint64_t trace_cap, uint64_t *trace_n, uint32_t flags)
 {
     sim S_, *s = &S_;
     memset(s, 0, sizeof *s);
@@ -944,6 +946,7 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     s->e = e;
     s->trace = trace;
     s->trace_cap = trace_cap;
+    s->no_skip = (flags & ORC_NO_SKIP) != 0;
     uint32_t ti = b->exp_topo[e], wi = b->exp_work[e];
     s->H = b->topo_nhosts[ti];
     s->S = b->topo_nsw[ti];
@@ -1095,8 +1098,8 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
  * results go to node_start/node_end at the experiment's offset in the
  * concatenation of all experiments' nodes; flow records at the experiment's
  * offset in the concatenation of rec_cap-sized blocks. */
-int orc_run_traced(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out,
-                   orc_event *trace, uint64_t trace_cap, uint64_t *trace_n)
+int orc_run_ex(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out,
+               orc_event *trace, uint64_t trace_cap, uint64_t *trace_n, uint32_t flags)
 {
     if (b->version != 1) return -1;
     offs o;
@@ -1114,7 +1117,8 @@ int orc_run_traced(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit,
     if (e1 == 0 || e1 > b->n_exps) e1 = b->n_exps;
     uint64_t node_off = 0, rec_off = 0;
     for (uint32_t e = 0; e < e1; e++) {
-        if (e >= e0) run_one(b, &o, e, limit, out, node_off, rec_off, trace, trace_cap, trace_n);
+        if (e >= e0)
+            run_one(b, &o, e, limit, out, node_off, rec_off, trace, trace_cap, trace_n, flags);
         node_off += b->work_nnodes[b->exp_work[e]];
         rec_off += b->exp_rec_cap[e];
     }
@@ -1123,11 +1127,13 @@ int orc_run_traced(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit,
     return 0;
 }
 
-/* Without a trace.  With one (orc_run_traced), give e1 = e0 + 1: the events
- * of one experiment; *trace_n gets how many happened. */
+/* Without a trace and with idle ticks skipped.  orc_run_ex: with a trace,
+ * give e1 = e0 + 1 (the events of one experiment; *trace_n gets how many
+ * happened); flags ORC_NO_SKIP steps every tick one by one (the brute-force
+ * check that skipping idle ticks changes no result). */
 int orc_run(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out)
 {
-    return orc_run_traced(b, e0, e1, limit, out, NULL, 0, NULL);
+    return orc_run_ex(b, e0, e1, limit, out, NULL, 0, NULL, 0);
 }
 
 /* exported for the tests that pin the hash against its published values */

@@ -93,10 +93,10 @@ def _load(path: str | None = None):
             lib.orc_run.argtypes = [C.POINTER(_Batch), C.c_uint32, C.c_uint32, C.c_uint32,
                                     C.POINTER(_Out)]
             lib.orc_run.restype = C.c_int
-            lib.orc_run_traced.argtypes = [C.POINTER(_Batch), C.c_uint32, C.c_uint32,
-                                           C.c_uint32, C.POINTER(_Out), C.c_void_p,
-                                           C.c_uint64, _P64]
-            lib.orc_run_traced.restype = C.c_int
+            lib.orc_run_ex.argtypes = [C.POINTER(_Batch), C.c_uint32, C.c_uint32,
+                                       C.c_uint32, C.POINTER(_Out), C.c_void_p,
+                                       C.c_uint64, _P64, C.c_uint32]
+            lib.orc_run_ex.restype = C.c_int
             lib.orc_mix64.argtypes = [C.c_uint64]
             lib.orc_mix64.restype = C.c_uint64
             _libs[key] = lib
@@ -108,12 +108,14 @@ def mix64(z: int) -> int:
 
 
 def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
-        lib_path: str | None = None, trace_cap: int = 0) -> dict:
+        lib_path: str | None = None, trace_cap: int = 0, no_skip: bool = False) -> dict:
     """Run experiments [e0, e1) of a packed batch (all when e1 == 0).
     `violations` counts broken invariants (queue over capacity, a link faster
     than its serialisation time, a packet delivered to the wrong host).
     With trace_cap > 0 (one experiment: e1 = e0 + 1), `trace` holds its first
-    trace_cap events (EVENT records) and `trace_total` how many happened."""
+    trace_cap events (EVENT records) and `trace_total` how many happened.
+    no_skip steps every tick instead of jumping over idle ones (same results
+    but `ticks_active`, by the skipping rule; a brute-force check of it)."""
     lib = _load(lib_path)
     keep = {}
     b = _Batch()
@@ -143,15 +145,17 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
     o = _Out()
     for n, t in _OUT:
         setattr(o, n, res[n].ctypes.data_as(_CT[t]))
-    if trace_cap:
-        if e1 != e0 + 1:
+    if trace_cap or no_skip:
+        if trace_cap and e1 != e0 + 1:
             raise ValueError("a trace covers one experiment: e1 must be e0 + 1")
-        ev = np.zeros(trace_cap, EVENT)
+        ev = np.zeros(max(1, trace_cap), EVENT)
         n = C.c_uint64(0)
-        rcode = lib.orc_run_traced(C.byref(b), e0, e1, limit, C.byref(o),
-                                   ev.ctypes.data_as(C.c_void_p), trace_cap, C.byref(n))
-        res["trace"] = ev[: min(trace_cap, n.value)]
-        res["trace_total"] = n.value
+        rcode = lib.orc_run_ex(C.byref(b), e0, e1, limit, C.byref(o),
+                               ev.ctypes.data_as(C.c_void_p) if trace_cap else None,
+                               trace_cap, C.byref(n), 1 if no_skip else 0)
+        if trace_cap:
+            res["trace"] = ev[: min(trace_cap, n.value)]
+            res["trace_total"] = n.value
     else:
         rcode = lib.orc_run(C.byref(b), e0, e1, limit, C.byref(o))
     if rcode != 0:

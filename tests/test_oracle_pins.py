@@ -80,10 +80,12 @@ def test_lone_message_closed_form(n, delta, topo):
 
 
 @pytest.mark.parametrize("n", [1, 5, 30])
-def test_heterogeneous_path_closed_form(n):
+@pytest.mark.parametrize("sig", [[1, 3, 2, 1], [3, 1, 2, 1]])
+def test_heterogeneous_path_closed_form(n, sig):
     """Per-link serialisation differs: the bottleneck spaces the packets, so
-    delivery = first injection + (n-1)*max(sigma) + sum(sigma + delta)."""
-    sig, dl = [1, 3, 2, 1], [2, 0, 5, 1]
+    delivery = first injection + (n-1)*max(sigma) + sum(sigma + delta).  The
+    bottleneck is a switch link, or the sender's own uplink."""
+    dl = [2, 0, 5, 1]
     t = chain_topology(3, sig, dl)
     w = I.lone_message(2, 0, 1, n * 4096)
     r = run1(t, w, chunk=1 << 30)
@@ -696,3 +698,89 @@ def test_down_route_takes_the_lowest_port():
     at_spine = {int(x["a"]) - spine_base for x in ev[ev["kind"] == O.EV_HOP]
                 if spine_base <= x["a"] < spine_base + nports[2]}
     assert at_spine == {2}
+
+
+
+def test_skipping_idle_ticks_changes_nothing():
+    """R26: jumping the clock over ticks in which nothing can change gives the
+    same results as stepping every tick one by one (brute force), over
+    bottlenecked senders, credit stalls, incast, relays, rings and trees, and
+    200 seeded small paths and incasts of random link times and capacities."""
+    ex = []
+    for sig in ([1, 3, 2, 1], [3, 1, 2, 1]):
+        ex.append(I.Experiment(chain_topology(3, sig, [2, 0, 5, 1]),
+                               I.lone_message(2, 0, 1, 9 * 4096), chunk=1 << 30, tick_ps=1000))
+    for cap in (2, 5, 10):                         # credit loop 2*4+2 = 10
+        ex.append(I.Experiment(I.single_switch(2, 1, 4), I.lone_message(2, 0, 1, 30 * 4096),
+                               chunk=1 << 30, cap=cap, tick_ps=1000))
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], 7 * 4096)
+    w.collective(I.P2P, [1, 2], 5 * 4096)
+    ex.append(I.Experiment(I.single_switch(3, 2, 3), w, chunk=8192, cap=3, tick_ps=1000))
+    ex.append(I.Experiment(I.single_switch(5, 1, 2), I.relay_chain(5, 9 * 4096, 3), tick_ps=1000))
+    for algo in (I.RING, I.TREE):
+        ex.append(I.Experiment(I.leaf_spine(2, 2, 3, 3),
+                               I.single_collective(6, I.AR, 48 * 4096 + 5), algo=algo, nc=2,
+                               chunk=16384, cap=8))
+    rng = np.random.default_rng(11)              # seeded small paths and incasts
+    for _ in range(150):
+        nsw = int(rng.integers(1, 4))
+        sig, dl = rng.integers(1, 5, nsw + 1).tolist(), rng.integers(0, 5, nsw + 1).tolist()
+        ex.append(I.Experiment(chain_topology(nsw, sig, dl),
+                               I.lone_message(2, 0, 1, int(rng.integers(1, 13)) * 4096),
+                               chunk=int(rng.choice([4096, 8192, 1 << 30])),
+                               cap=int(rng.integers(2, 7)), tick_ps=1000))
+    for _ in range(50):
+        w = I.Workload(3)
+        w.collective(I.P2P, [0, 2], int(rng.integers(1, 9)) * 4096)
+        w.collective(I.P2P, [1, 2], int(rng.integers(1, 9)) * 4096)
+        ex.append(I.Experiment(I.single_switch(3, int(rng.integers(1, 4)), int(rng.integers(0, 4))),
+                               w, chunk=int(rng.choice([4096, 1 << 20])),
+                               cap=int(rng.integers(2, 6)), tick_ps=1000))
+    p = I.Batch(ex).pack()
+    a, b = O.run(p), O.run(p, no_skip=True)
+    for k in ("status", "end_tick", "now", "pkts_injected", "pkt_hops", "pkts_delivered",
+              "msgs_delivered", "digest", "node_start", "node_end", "violations"):
+        assert (a[k] == b[k]).all(), k
+    assert (a["status"] == O.ST_DONE).all()
+    assert (a["ticks_active"] < b["ticks_active"]).any()      # skipping did skip
+
+
+def test_tree_waits_for_both_children():
+    """R14: a tree member sends chunk j on (up, or down from the root) only
+    after chunk j arrived from every child.  Three members on one switch,
+    sigma 1, delta 0, one 1-packet chunk: both leaves send at tick 1 (the
+    joins of tick 0 reach them one tick later); their packets are ready at
+    the switch at 2, which forwards the left child's first (round robin
+    from port 0) and the right child's at 3; the root receives them at 3
+    and 4, and its first broadcast goes at 5 (a receipt counts from the next
+    tick)."""
+    ev = _traced(I.single_switch(3, 1, 0), I.single_collective(3, I.AR, 4096),
+                 algo=I.TREE, nc=1, chunk=4096)
+    inj = ev[ev["kind"] == O.EV_INJECT]
+    assert sorted(int(x["tick"]) for x in inj if x["a"] != 0) == [1, 1]
+    dl = ev[(ev["kind"] == O.EV_DELIVER) & (ev["a"] == 0)]["tick"]
+    assert list(dl) == [3, 4]
+    assert int(inj[inj["a"] == 0]["tick"].min()) == 5
+
+
+def test_failure_tick_completes_for_every_other_rank():
+    """R31: the tick in which one rank's table overflows still completes for
+    the other ranks.  Rank 2 finishes a 2-tick compute node at tick 2, and 17
+    intra-server collectives (one more than the 16 running collectives a rank
+    may hold) become due at tick 3, so its table overflows at tick 3.  In the
+    same tick rank 1 receives the one packet of rank 0's lone message
+    (injected at 1, at the switch at 2, at rank 1 at 3): that delivery and
+    its message still count."""
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 1], 4096)
+    c = w.compute(2, 2)
+    for _ in range(17):
+        u = w.collective(I.AR, [2], 1000, intra=True, alpha=5, beta=(1, 1))[0]
+        w.edge(c, u)
+    r = O.run(I.Batch([I.Experiment(I.single_switch(3, 1, 0), w, chunk=1 << 20,
+                                    tick_ps=1000, rec_cap=4)]).pack())
+    assert r["status"][0] == O.ST_OVERFLOW
+    assert r["node_end"][2] == 2                 # rank 2's compute node (rank-major order)
+    assert r["pkts_delivered"][0] == 1 and r["msgs_delivered"][0] == 1
+    assert list(r["rec_tick"][: r["rec_count"][0]]) == [3]
