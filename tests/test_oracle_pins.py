@@ -784,3 +784,97 @@ def test_failure_tick_completes_for_every_other_rank():
     assert r["node_end"][2] == 2                 # rank 2's compute node (rank-major order)
     assert r["pkts_delivered"][0] == 1 and r["msgs_delivered"][0] == 1
     assert list(r["rec_tick"][: r["rec_count"][0]]) == [3]
+
+
+def test_intra_server_time_rounds_up():
+    """R17: bytes/beta rounds up to whole ticks.  All-reduce over g = 4 of
+    S = 8,001 B moves ceil(2*3*8001/4) = 12,002 B per GPU: at 1 tick per
+    1,000 B that is 13 ticks (12.002 rounded up), after alpha = 7."""
+    w = I.Workload(4)
+    w.collective(I.AR, [0, 1, 2, 3], 8001, intra=True, alpha=7, beta=(1, 1000))
+    r = run1(I.single_switch(4, 1, 0), w)
+    assert list(r["node_end"][:4]) == [7 + 13] * 4
+
+
+def test_tick_limit_is_exclusive():
+    """R27: ticks stop at 0xFFF00000: a node that would end there overflows,
+    one that ends a tick earlier completes (1 tick = 1 ns)."""
+    limit = 0xFFF00000
+    st = []
+    for d in (limit - 1, limit):
+        w = I.Workload(1)
+        w.compute(0, d)
+        st.append(O.run(I.Batch([I.Experiment(I.single_switch(1, 1, 0), w,
+                                               tick_ps=1000)]).pack())["status"][0])
+    assert st == [O.ST_DONE, O.ST_OVERFLOW]
+
+
+def test_receive_counters_are_freed():
+    """A membership's receive counters return to the rank when it completes:
+    130 one-after-another point-to-point receives at rank 1 (more than its
+    128 counters) complete."""
+    w = I.Workload(2)
+    prev = None
+    for _ in range(130):
+        a, b = w.collective(I.P2P, [0, 1], 4096)
+        if prev is not None:
+            w.edge(prev[0], a)
+            w.edge(prev[1], b)
+        prev = (a, b)
+    r = run1(I.single_switch(2, 1, 0), w, chunk=1 << 20)
+    assert r["msgs_delivered"][0] == 130
+
+
+def test_routes_use_no_same_level_link():
+    """R10: routes go up then down; a link between two switches of one level
+    is neither, so no packet crosses it.  Two leaves under one spine, wired
+    to each other too: eight connections each way between leaf 0's hosts
+    and leaf 1's all pass the spine."""
+    t = I.Topology("leaves-linked")
+    l0, l1, sp = t.add_switch(1), t.add_switch(1), t.add_switch(2)
+    hs = t.add_hosts(16)
+    for h in hs[:8]:
+        t.attach_host(h, l0)
+    for h in hs[8:]:
+        t.attach_host(h, l1)
+    t.link(l0, sp)
+    t.link(l1, sp)
+    t.link(l0, l1)                         # leaf 0's port 9, leaf 1's port 9
+    w = I.Workload(16)
+    for i in range(8):
+        w.collective(I.P2P, [i, 8 + i], 2 * 4096)
+        w.collective(I.P2P, [8 + i, i], 2 * 4096)
+    ev = _traced(t, w, chunk=1 << 20)
+    hops = ev[ev["kind"] == O.EV_HOP]
+    assert not np.isin(hops["a"], [9, 10 + 9]).any()       # the leaf-leaf ports (global index)
+    assert (hops["a"] == 8).sum() == 8 * 2                  # leaf 0 sends everything up
+    assert (hops["a"] == 10 + 8).sum() == 8 * 2             # and so does leaf 1
+
+
+def test_ecmp_depends_on_seed_and_switch():
+    """R10: the up port hashes the connection with the experiment's ECMP seed
+    and the switch.  Another seed moves some connections to other up ports.
+    In a k=4 fat-tree the edge and the aggregation switches both have their
+    up ports at local ports 2 and 3, so a hash blind to the switch would
+    take the same local port at both; over eight one-packet connections
+    across pods, some take different ones."""
+    t = I.fat_tree(4)
+    base = np.concatenate([[0], np.cumsum(t.arrays()["sw_nports"])])
+    local = lambda q: int(q - base[np.searchsorted(base, q, "right") - 1])
+    firsts = []
+    for src, dst in [(0, 15), (1, 14), (2, 13), (3, 12), (4, 11), (5, 10), (6, 9), (7, 8)]:
+        w = I.lone_message(16, src, dst, 4096)
+        ev = _traced(t, w, chunk=1 << 20)
+        hops = ev[ev["kind"] == O.EV_HOP]["a"]
+        assert len(hops) == 5                       # edge, aggregation, core, aggregation, edge
+        firsts.append((local(hops[0]), local(hops[1])))
+    assert all(a in (2, 3) and b in (2, 3) for a, b in firsts)
+    assert any(a != b for a, b in firsts)
+    paths = []
+    for sd in (0, 1):
+        w = I.Workload(16)
+        for src, dst in [(0, 15), (1, 14), (2, 13), (3, 12), (4, 11), (5, 10), (6, 9), (7, 8)]:
+            w.collective(I.P2P, [src, dst], 4096)
+        ev = _traced(t, w, chunk=1 << 20, ecmp_seed=sd)
+        paths.append(sorted((int(x["b"]), int(x["a"])) for x in ev[ev["kind"] == O.EV_HOP]))
+    assert paths[0] != paths[1]
