@@ -1,0 +1,120 @@
+"""The seeded input generators build the workloads the configurations name:
+unit conversions, fabric sizes, experiment sweeps and DAG shapes, each
+checked against the numbers stated for it (figures derived by hand from the
+configuration text and the readings of the pages)."""
+import collections
+
+import numpy as np
+
+from experiment_network_simulation_gb300 import inputs as I
+
+
+def test_tick_and_delay_units():
+    """R1: one tick is a 4 KiB packet's serialisation: 81,920 ps at 400 Gbps,
+    3,276,800 ps at 10 Gbps; 1 us of propagation rounds half-up to 12 ticks
+    and to 0 ticks."""
+    assert I.tick_ps(4096, 400) == 81_920
+    assert I.tick_ps(4096, 10) == 3_276_800
+    assert I.delay_ticks(1_000_000, 81_920) == 12
+    assert I.delay_ticks(1_000_000, 3_276_800) == 0
+
+
+def test_config1_sweep_and_fabric():
+    """16 MiB ring all-reduce over 8 hosts, 2 leaves x 2 spines, 16
+    experiments = NC {1,2,4,8} x chunk {128K,512K,1M,4M}."""
+    b = I.config1()
+    assert len(b) == 16
+    assert {(e.nc, e.chunk) for e in b.experiments} == {
+        (nc, c) for nc in (1, 2, 4, 8) for c in (128 << 10, 512 << 10, 1 << 20, 4 << 20)}
+    t = b.experiments[0].topo
+    a = t.arrays()
+    assert t.n_hosts == 8 and collections.Counter(a["sw_level"].tolist()) == {1: 2, 2: 2}
+    assert set(a["port_delta"].tolist()) == {12} and set(a["host_delta"].tolist()) == {12}
+    w = b.experiments[0].work
+    assert [(c.kind, c.nbytes, c.ranks) for c in w.colls] == [(I.AR, 16 << 20, list(range(8)))]
+    assert {(e.pkt, e.cap, e.tick_ps, e.algo) for e in b.experiments} == {(4096, 64, 81_920, I.RING)}
+
+
+def test_config2_sweep():
+    """256 distinct (A, K) pairs, A in 2..16, K in 1..64, a whole number of
+    MiB in [1, 64], A+1 hosts on one 10 Gbps switch with no propagation
+    delay in ticks."""
+    b = I.config2()
+    assert len(b) == 256
+    ak = [(e.label["A"], e.label["K"]) for e in b.experiments]
+    assert len(set(ak)) == 256
+    assert all(2 <= A <= 16 and 1 <= K <= 64 for A, K in ak)
+    assert all(1 <= e.label["mib"] <= 64 for e in b.experiments)
+    for e in b.experiments:
+        assert e.topo.n_hosts == e.label["A"] + 1 and e.tick_ps == 3_276_800
+        c = e.work.colls[0]
+        assert (c.kind, c.nbytes, c.parts) == (I.RELAY, e.label["mib"] << 20, e.label["K"])
+        assert set(e.topo.arrays()["port_delta"].tolist()) == {0}
+
+
+def test_config3_dag_shape_and_sweep():
+    """R23 and R29: GPT-13B on 128 servers x 8 GPUs (TP 8, PP 4, DP 32), 40
+    layers (10 a stage), 8 micro-batches.  Per collective kind:
+    - DP all-reduce of 12*h^2/TP*2 B = 78,643,200 B over 32 ranks, one per
+      layer and (stage, TP rank): 10 * 32 = 320;
+    - TP all-reduce (intra-server) of s*b*h*2 B = 20,971,520 B over 8 GPUs,
+      four per layer and micro-batch: 4 * 10 * 8 * 128 groups = 40,960;
+    - pipeline point-to-point of s*b*h*2/TP B = 2,621,440 B: 8 micro-batches
+      x 3 boundaries x 2 directions x 256 (TP, DP) pairs = 12,288.
+    Nodes: per GPU 4 computes + 4 TP joins per layer and micro-batch (640),
+    10 DP joins and 16 (end stages) or 32 (middle stages) pipeline nodes:
+    1,024 GPUs average 674, 690,176 in all.  Fabric: k=16 fat-tree, 128 edge,
+    128 aggregation, 64 core switches, 1,024 NICs.  500 experiments =
+    {ring, tree} x NC {1,2,4,8,16} x chunk {64K..1M} x duration seeds 0..9."""
+    b = I.config3()
+    w = b.experiments[0].work
+    got = collections.Counter((c.kind, c.intra, c.nbytes, len(c.ranks)) for c in w.colls)
+    assert got == {(I.AR, False, 78_643_200, 32): 320, (I.AR, True, 20_971_520, 8): 40_960,
+                   (I.P2P, False, 2_621_440, 2): 12_288}
+    assert len(w.nodes) == 690_176
+    t = b.experiments[0].topo
+    assert t.n_hosts == 1024
+    assert collections.Counter(t.arrays()["sw_level"].tolist()) == {1: 128, 2: 128, 3: 64}
+    assert len(b) == 500
+    assert collections.Counter((e.algo, e.nc, e.chunk, e.dur_seed) for e in b.experiments) == {
+        (a, nc, c << 10, s): 1 for a in (I.RING, I.TREE) for nc in (1, 2, 4, 8, 16)
+        for c in (64, 128, 256, 512, 1024) for s in range(10)}
+
+
+def test_config4_router_traffic():
+    """R22: 512 ranks, 128 tokens each, top-8 distinct experts of 256 (expert
+    e on rank 2e), 7,168 x 2 B a token copy.  Every rank sends 128 * 8 copies,
+    only even ranks receive, an expert gets a token at most once, and the
+    Zipf(1.2) popularity makes the busiest expert far busier than the
+    median."""
+    byte = I.moe_traffic(0)
+    assert byte.shape == (512, 512)
+    assert (byte.sum(axis=1) == 128 * 8 * 14_336).all()
+    assert not byte[:, 1::2].any()
+    assert (byte[:, ::2] <= 128 * 14_336).all()
+    load = byte[:, ::2].sum(axis=0)
+    assert load.max() > 4 * np.median(load)
+    assert not (I.moe_traffic(1) == byte).all()
+    b = I.config4(n_seeds=2)
+    assert len(b) == 8 and len({id(e.topo) for e in b.experiments}) == 4
+    assert all(e.topo.n_hosts == 512 and (e.nc, e.chunk) == (4, 512 << 10) for e in b.experiments)
+
+
+def test_config5_fabrics():
+    """R21: 24 three-tier fabrics of {32, 48, 64}-port switches x
+    oversubscription {1..4}:1 x {plain, rail-optimised}, each with 8,192
+    NICs, no switch beyond its radix; ring, NC 8, chunk 256 KiB; the DAG is
+    config 3's at DP 128 on the first 512 servers."""
+    topos = I.config5_topologies()
+    assert len(topos) == 24
+    for t in topos:
+        a = t.arrays()
+        assert t.n_hosts == 8192
+        assert set(a["sw_level"].tolist()) == {1, 2, 3}
+        assert a["sw_nports"].max() <= 64
+    b = I.config5(n_exp=48, wave=(0, 2))
+    w = b.experiments[0].work
+    dp = [c for c in w.colls if c.kind == I.AR and not c.intra]
+    assert {len(c.ranks) for c in dp} == {128}
+    assert max(max(c.ranks) for c in w.colls) == 4095
+    assert {(e.algo, e.nc, e.chunk) for e in b.experiments} == {(I.RING, 8, 256 << 10)}
