@@ -87,3 +87,21 @@ def test_strerror_names_codes():
     lib = mv.library()
     for code in (0, 1, -1, -2, -3, -4, -5):
         assert lib.mv_strerror(code)
+
+
+def test_binding_fails_loudly_without_a_gpu():
+    """No CPU fallback: without a CUDA device the simulator refuses to start."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("checks the behaviour without a GPU")
+    with pytest.raises(RuntimeError, match="CUDA"):
+        mv.Simulator(I.config1().pack())
+
+
+def test_binding_raises_library_errors():
+    p = I.config1().pack()
+    p = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in p.items()}
+    p["exp_nc"][0] = 0
+    with pytest.raises(mv.MVError) as e:
+        mv.workspace_bytes(p)
+    assert e.value.code == mv.MV_EINVAL and str(mv.MV_EINVAL) in str(e.value)
