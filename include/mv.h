@@ -170,9 +170,12 @@ typedef struct mv_ctx mv_ctx;
  *   lock and waits on no other block, so it cannot hang; the watchdog bounds
  *   the run time of a call.
  * grid_blocks: 0 = every block that fits on the device at once.
- * stage: 0 = an experiment's dynamic state is staged in shared memory when
- *   it fits, 1 = only its wake table is, 2 = nothing is (results are the
- *   same in every mode; the modes exist to test and measure that).
+ * stage: 0 = an experiment's whole state is staged in shared memory when it
+ *   fits, else its hottest arrays in priority order up to the build's share
+ *   (wake table, switch and host records, dirty words, queue words, egress
+ *   state, up lists, rank control words, port records, running lists);
+ *   1 = only its wake table is; 2 = nothing is (results are the same in
+ *   every mode; the modes exist to test and measure that).
  * block_warps: warps of the block stepping one experiment (0 = automatic;
  *   at most 8, or 16 for variant 3).
  * variant: the kernel build.  0 = automatic; 1 = one block an SM with the
