@@ -61,13 +61,16 @@ class Topology:
         self.sw_level: list[int] = []
         self.sw_ports: list[list[tuple]] = []   # per switch: [(peer, sigma, delta)]
         self.host_att: list[tuple | None] = []  # per host: (switch, port, sigma, delta)
+        self._edits, self._arrays = 0, None     # arrays() is cached until the next edit
 
     def add_switch(self, level: int) -> int:
+        self._edits += 1
         self.sw_level.append(level)
         self.sw_ports.append([])
         return len(self.sw_level) - 1
 
     def add_hosts(self, n: int) -> list[int]:
+        self._edits += 1
         ids = list(range(self.n_hosts, self.n_hosts + n))
         self.n_hosts += n
         self.host_att.extend([None] * n)
@@ -78,6 +81,7 @@ class Topology:
         """Link host ``h`` to a new port of switch ``s``.  ``sigma``/``delta``
         describe the NIC uplink; the ``*_down`` values the switch-to-host link."""
         assert self.host_att[h] is None
+        self._edits += 1
         p = len(self.sw_ports[s])
         self.sw_ports[s].append((("h", h),
                                  sigma if sigma_down is None else sigma_down,
@@ -85,6 +89,7 @@ class Topology:
         self.host_att[h] = (s, p, sigma, delta)
 
     def link(self, a: int, b: int, sigma: int = 1, delta: int = 0):
+        self._edits += 1
         pa, pb = len(self.sw_ports[a]), len(self.sw_ports[b])
         self.sw_ports[a].append((("s", b, pb), sigma, delta))
         self.sw_ports[b].append((("s", a, pa), sigma, delta))
@@ -94,6 +99,15 @@ class Topology:
         return len(self.sw_level)
 
     def arrays(self) -> dict:
+        """Flat per-port and per-host tables (cached until the next edit; the
+        caller must not modify them)."""
+        if self._arrays is not None and self._arrays[0] == self._edits:
+            return self._arrays[1]
+        a = self._build_arrays()
+        self._arrays = (self._edits, a)
+        return a
+
+    def _build_arrays(self) -> dict:
         base = np.zeros(self.n_switches + 1, dtype=np.int64)
         for s, ports in enumerate(self.sw_ports):
             base[s + 1] = base[s] + len(ports)
@@ -228,10 +242,12 @@ class Workload:
         self.edges: list[tuple[int, int]] = []
         self.colls: list[Coll] = []
         self.mem = None
+        self._edits, self._arrays = 0, None     # arrays() is cached until the next edit
 
     def compute(self, rank: int, lo_ns: int, hi_ns: int | None = None, key: int = 0) -> int:
         """A compute task lasting ``lo_ns`` (or a duration hashed from
         [lo_ns, hi_ns] with ``key`` and the experiment's duration seed)."""
+        self._edits += 1
         self.nodes.append(dict(rank=rank, kind=COMPUTE, arg=0, lo=lo_ns,
                                hi=lo_ns if hi_ns is None else hi_ns, key=key))
         return len(self.nodes) - 1
@@ -241,6 +257,7 @@ class Workload:
                    a2a: dict | None = None) -> list[int]:
         """One collective instance over ``ranks`` (member order = list order).
         Returns the per-member node ids, in member order."""
+        self._edits += 1
         ci = len(self.colls)
         ids = []
         for r in ranks:
@@ -253,6 +270,7 @@ class Workload:
 
     def edge(self, u: int, v: int):
         assert self.nodes[u]["rank"] == self.nodes[v]["rank"], "edges stay within a rank"
+        self._edits += 1
         self.edges.append((u, v))
 
     def chain(self, *nodes):
@@ -261,9 +279,19 @@ class Workload:
 
     def set_memory_model(self, params: int, tp: int, pp: int, layers: int,
                          micro: int, seq: int, batch: int, hidden: int, heads: int):
+        self._edits += 1
         self.mem = (params, tp, pp, layers, micro, seq, batch, hidden, heads)
 
     def arrays(self) -> dict:
+        """Flat DAG, collective and all-to-all tables (cached until the next
+        edit; the caller must not modify them)."""
+        if self._arrays is not None and self._arrays[0] == self._edits:
+            return self._arrays[1]
+        a = self._build_arrays()
+        self._arrays = (self._edits, a)
+        return a
+
+    def _build_arrays(self) -> dict:
         order = sorted(range(len(self.nodes)), key=lambda i: (self.nodes[i]["rank"], i))
         loc = np.empty(len(self.nodes), np.int64)
         loc[order] = np.arange(len(order))
