@@ -31,10 +31,18 @@
  * own arrival tick.  That makes the result independent of the order entities
  * are visited in.
  *
- * Parity pins live in tests/: the lone-message closed form, the pipelined
- * broadcast closed form, a contention-free ring evaluated as a longest path,
- * hand-traced tick tables, DAG critical paths, the analytic model and the
- * memory check.  Functions without such a pin say so below.
+ * Parity pins live in tests/: the lone-message and heterogeneous-path closed
+ * forms, the pipelined broadcast closed form, a contention-free ring
+ * evaluated as a longest path, hand-traced tick tables (matched event by
+ * event through the trace below), schedule details derived by hand (ring
+ * blocks, lane round robin, partitions, all-to-all striping, tree
+ * children), DAG critical paths, the analytic model, the memory check, the
+ * table and tick limits, idle-tick skipping against stepping every tick,
+ * and the run-time invariant counts; a mutation test plants plausible
+ * mistakes here and requires those pins to fail.  Parity unpinned: which
+ * up port the ECMP hash gives a particular connection (route_port) is this
+ * build's convention; the pins fix only its properties (one path per
+ * connection, spread over the up ports, dependence on seed and switch).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -269,7 +277,8 @@ static void build_routes(sim *s)
     s->up_base[S] = k;
 }
 
-/* egress port (switch-local) for a packet at switch w */
+/* egress port (switch-local) for a packet at switch w.  Parity unpinned for
+ * the exact up port the hash picks (a convention); see the header. */
 static int32_t route_port(sim *s, uint32_t w, const pkt *p)
 {
     int32_t d = s->route[(size_t)w * s->H + p->dst];
