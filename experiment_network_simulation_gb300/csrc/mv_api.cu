@@ -117,7 +117,8 @@ int plan(const mv_batch_desc *d, Layout &L)
         u32 q = 0;
         for (u32 s = 0; s < R.nsw; s++) {
             u32 np = d->sw_nports[R.sw_off + s], lev = d->sw_level[R.sw_off + s];
-            if (np == 0 || np > kMaxPorts || lev == 0 || lev > 250) return MV_EINVAL;
+            if (np == 0 || np > kMaxPorts || lev == 0 || lev > 250 || np > R.nq - q)
+                return MV_EINVAL;
             L.max_level = std::max(L.max_level, lev);
             R.maxlev = std::max(R.maxlev, lev);
             L.sw_pstart[R.sw_off + s] = q;
@@ -208,6 +209,7 @@ int plan(const mv_batch_desc *d, Layout &L)
         for (u32 r = 0; r < R.nr; r++) {
             L.rank_first[R.rank_off + r] = n;
             u32 c = d->rank_nnodes[R.rank_off + r];
+            if (c > R.nn - n) return MV_EINVAL;         // more nodes than the workload declares
             for (u32 k = 0; k < c; k++) {
                 node_rank[n + k] = r;
                 L.node_rank[R.node_off + n + k] = r;
@@ -247,6 +249,7 @@ int plan(const mv_batch_desc *d, Layout &L)
                 return MV_EINVAL;
             if (!intra && kind == COLL_RELAY && d->coll_parts[g] == 0) return MV_EINVAL;
             if (!intra && kind == COLL_P2P && N != 2) return MV_EINVAL;
+            if (N > R.nmemb - m) return MV_EINVAL;          // more members than declared
             for (u32 i = 0; i < N; i++) {
                 u32 gm = R.memb_off + m + i;
                 u32 rr = d->member_rank[gm], u = d->member_node[gm];
@@ -258,6 +261,9 @@ int plan(const mv_batch_desc *d, Layout &L)
                 L.node_member[R.node_off + u] = i;
                 L.memb_row[gm] = ra;
                 L.memb_col[gm] = ca;
+                if (d->member_a2a_n[gm] > d->work_na2a[w] - ra ||
+                    d->member_a2a_in_n[gm] > d->work_na2a_in[w] - ca)
+                    return MV_EINVAL;                       // more entries than declared
                 for (u32 j = 0; j < d->member_a2a_n[gm]; j++) {
                     u32 dst = d->a2a_dst[R.a2a_off + ra + j];
                     if (dst >= N || dst == i || d->a2a_bytes[R.a2a_off + ra + j] >= (1ull << 40))

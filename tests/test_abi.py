@@ -105,3 +105,51 @@ def test_binding_raises_library_errors():
     with pytest.raises(mv.MVError) as e:
         mv.workspace_bytes(p)
     assert e.value.code == mv.MV_EINVAL and str(mv.MV_EINVAL) in str(e.value)
+
+
+_FUZZ = r'''
+import sys, ctypes as C
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from experiment_network_simulation_gb300 import inputs as I, mv
+rng = np.random.default_rng(int(sys.argv[2]))
+bases = [I.config1().pack(), I.gpt_small(seeds=(0,)).pack(),
+         I.Batch([I.Experiment(I.fat_tree(4), I.single_collective(16, I.A2A, 0), nc=2)]).pack(),
+         I.config2(n_exp=4).pack()]
+fixed = {k for k in bases[0] if k.startswith("topo_n") or k.startswith("work_n") or k == "version"}
+lib, codes = mv.library(), set()
+for it in range(int(sys.argv[3])):
+    p = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in bases[it % len(bases)].items()}
+    keys = [k for k, v in p.items() if isinstance(v, np.ndarray) and v.size > 0 and k not in fixed]
+    for _ in range(int(rng.integers(1, 4))):
+        a = p[keys[int(rng.integers(len(keys)))]]
+        i = int(rng.integers(a.size))
+        if a.dtype == np.int32:
+            a[i] = rng.integers(-70000, 70000)
+        else:
+            top = int(np.iinfo(a.dtype).max)
+            vals = [0, 1, int(a.flat[i]) + 1, max(int(a.flat[i]) - 1, 0),
+                    int(rng.integers(0, 1 << 20)), top]
+            a.flat[i] = vals[int(rng.integers(len(vals)))] % (top + 1)
+    d, keep = mv.make_desc(p)
+    n, nn, nr = C.c_uint64(), C.c_uint64(), C.c_uint64()
+    codes.add(lib.mv_workspace_bytes(C.byref(d), C.byref(n)))
+    codes.add(lib.mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)))
+print(sorted(codes))
+'''
+
+
+def test_descriptor_fuzz_never_crashes():
+    """Validation survives corrupted descriptors: with every declared count
+    left as is (so each array has its declared length), random values in the
+    other arrays -- counts per rank, per node, per collective and per member
+    included -- give a status code, never a crash.  (A count larger than
+    the workload declared once overran a host table here.)  The run is a
+    child process, so a crash fails the test instead of ending the suite."""
+    import subprocess
+    import sys
+    p = subprocess.run([sys.executable, "-c", _FUZZ, ROOT, "7", "1500"], capture_output=True,
+                       text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    codes = eval(p.stdout.strip().splitlines()[-1])
+    assert set(codes) <= {mv.MV_OK, mv.MV_EINVAL, mv.MV_EOVERFLOW} and mv.MV_EINVAL in codes
