@@ -542,8 +542,9 @@ def test_invariant_checks_catch_planted_mistakes(tmp_path):
     assert O.run(_incast(20), lib_path=no_credit)["violations"][0] > 0
     no_busy = _planted(tmp_path, "no_busy", "s->eg_busy[qe] = t + s->port_sigma[qe];", "")
     assert O.run(_incast(9, 3), lib_path=no_busy)["violations"][0] > 0
+    # (the planted copies run in this process, so each mistake stays in bounds)
     bad_route = _planted(tmp_path, "bad_route", "s->route[(size_t)w * s->H + p->dst]",
-                         "s->route[(size_t)w * s->H + (p->dst ^ 1u)]")
+                         "s->route[(size_t)w * s->H + (p->dst + 1) % s->H]")
     assert O.run(_incast(3), lib_path=bad_route)["violations"][0] > 0
 
 
