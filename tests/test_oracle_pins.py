@@ -879,3 +879,46 @@ def test_ecmp_depends_on_seed_and_switch():
         ev = _traced(t, w, chunk=1 << 20, ecmp_seed=sd)
         paths.append(sorted((int(x["b"]), int(x["a"])) for x in ev[ev["kind"] == O.EV_HOP]))
     assert paths[0] != paths[1]
+
+
+def test_random_scenarios_keep_invariants():
+    """Seeded random collectives on random small fabrics: every run ends
+    DONE, delivers every packet it injected, breaks no run-time invariant
+    (queue within cap, links within their rate, delivery at the addressed
+    host) and gives the same results stepped tick by tick (R26)."""
+    rng = np.random.default_rng(2024)
+    ex = []
+    for _ in range(200):
+        fab = int(rng.integers(3))
+        delta, sigma = int(rng.integers(0, 4)), int(rng.integers(1, 3))
+        if fab == 0:
+            t = I.single_switch(6, sigma, delta)
+        elif fab == 1:
+            t = I.leaf_spine(2, 2, 3, delta, sigma=sigma)
+        else:
+            t = I.fat_tree(4, delta, sigma=sigma)
+        H = t.n_hosts
+        kind = int(rng.choice([I.AR, I.RS, I.AG, I.RELAY, I.P2P, I.A2A]))
+        n = 2 if kind == I.P2P else int(rng.integers(2, min(H, 6) + 1))
+        ranks = [int(x) for x in rng.choice(H, n, replace=False)]
+        w = I.Workload(H)
+        nbytes = int(rng.choice([0, 1, 4095, 4096, 4097, int(rng.integers(1, 40)) * 4096 + int(rng.integers(0, 4096))]))
+        if kind == I.A2A:
+            m = {(i, j): int(rng.integers(0, 5)) * 4096 + int(rng.integers(0, 100))
+                 for i in range(n) for j in range(n) if i != j}
+            w.collective(I.A2A, ranks, 0, a2a=m)
+        elif kind == I.RELAY:
+            w.collective(I.RELAY, ranks, nbytes, parts=int(rng.integers(1, 6)))
+        else:
+            w.collective(kind, ranks, nbytes)
+        ex.append(I.Experiment(t, w, algo=int(rng.integers(2)), nc=int(rng.integers(1, 5)),
+                               chunk=int(rng.choice([4096, 8192, 3 * 4096 + 7, 1 << 20])),
+                               cap=int(rng.integers(2, 17)), tick_ps=1000,
+                               ecmp_seed=int(rng.integers(1 << 30))))
+    p = I.Batch(ex).pack()
+    a, b = O.run(p), O.run(p, no_skip=True)
+    assert (a["status"] == O.ST_DONE).all()
+    assert (a["violations"] == 0).all()
+    assert (a["pkts_injected"] == a["pkts_delivered"]).all()
+    for k in ("end_tick", "pkts_injected", "pkt_hops", "msgs_delivered", "digest", "node_end"):
+        assert (a[k] == b[k]).all(), k
