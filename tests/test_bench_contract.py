@@ -43,3 +43,22 @@ def test_gpu_arm_fails_loudly_without_a_gpu():
     p = _bench("--steps", "1", "--warmup", "3")
     assert p.returncode != 0
     assert not p.stdout.strip()
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched the way multi-GPU runs are (torchrun, 2 ranks, rendezvous on
+    127.0.0.1), the reference arm runs on rank 0 alone and prints one line."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    p = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    assert r["impl"] == "reference" and r["n_gpus"] == 2 and r["value"] > 0
