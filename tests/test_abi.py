@@ -153,3 +153,24 @@ def test_descriptor_fuzz_never_crashes():
     assert p.returncode == 0, p.stderr[-2000:]
     codes = eval(p.stdout.strip().splitlines()[-1])
     assert set(codes) <= {mv.MV_OK, mv.MV_EINVAL, mv.MV_EOVERFLOW} and mv.MV_EINVAL in codes
+
+
+def test_size_limits_and_empty_batches():
+    """Hosts are 16-bit in a packet descriptor and member indices 16-bit in a
+    send lane: 65,536 hosts or members are refused.  A batch of no
+    experiments is valid and has no results."""
+    p = I.config1().pack()
+    q = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in p.items()}
+    q["topo_nhosts"][0] = 65536
+    d, _ = mv.make_desc(q)
+    n = C.c_uint64()
+    assert mv.library().mv_workspace_bytes(C.byref(d), C.byref(n)) == mv.MV_EINVAL
+    q = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in p.items()}
+    q["coll_nmembers"][0] = 65536
+    assert _bad(q) == mv.MV_EINVAL
+    e = {k: (v[:0] if k.startswith("exp_") else v) for k, v in p.items()}
+    assert mv.workspace_bytes(e) > 0
+    d, _ = mv.make_desc(e)
+    nn, nr = C.c_uint64(), C.c_uint64()
+    assert mv.library().mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)) == mv.MV_OK
+    assert nn.value == 0 and nr.value == 0
