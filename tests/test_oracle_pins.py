@@ -922,3 +922,27 @@ def test_random_scenarios_keep_invariants():
     assert (a["pkts_injected"] == a["pkts_delivered"]).all()
     for k in ("end_tick", "pkts_injected", "pkt_hops", "msgs_delivered", "digest", "node_end"):
         assert (a[k] == b[k]).all(), k
+
+
+def test_ingress_queue_is_fifo_with_head_of_line_blocking():
+    """R3: an ingress port is one FIFO; its packets leave in arrival order,
+    so a packet for a free egress waits behind a head whose egress is busy
+    (head-of-line blocking).  Rank 0 alternates packets to ranks 1 and 3
+    (lanes in node order, R7) while ranks 2 and 4 also send to rank 1: port
+    1 serves ingress 0 a third of the time but rank 0 offers it half its
+    packets, so ingress 0 backs up.  Its packets still leave in exactly the
+    order rank 0 injected them, and packets for the idle port 3 wait
+    behind them (leave later than the tick after they arrived)."""
+    w = I.Workload(5)
+    w.collective(I.P2P, [0, 1], 8 * 4096)
+    w.collective(I.P2P, [0, 3], 8 * 4096)
+    w.collective(I.P2P, [2, 1], 8 * 4096)
+    w.collective(I.P2P, [4, 1], 8 * 4096)
+    ev = _traced(I.single_switch(5, 1, 0), w, chunk=1 << 20, cap=4)
+    inj = ev[(ev["kind"] == O.EV_INJECT) & (ev["a"] == 0)]
+    dst_of = {int(inj["b"][0]): 1, int(inj["b"][1]): 3}      # lane 0 -> rank 1, lane 1 -> rank 3
+    want = [dst_of[int(k)] for k in inj["b"]]
+    hops = ev[(ev["kind"] == O.EV_HOP) & (ev["b"] == 0)]
+    assert [int(x) for x in hops["a"]] == want                 # egress port p faces host p
+    ready = inj["tick"] + 1                                    # sigma 1, delta 0: at the switch next tick
+    assert any(int(h["tick"]) > int(r) for h, r, d in zip(hops, ready, want) if d == 3)
