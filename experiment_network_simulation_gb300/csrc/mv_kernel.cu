@@ -7,16 +7,20 @@
 // stepped by one thread block: blocks of the persistent grid take
 // experiments from a shared counter, largest first, and step them tick by
 // tick with a block barrier as the per-tick synchronisation.  While a block
-// holds an experiment, its dynamic state lives in shared memory when it fits
-// (and in global memory otherwise); only the wake table always does.
+// holds an experiment, its whole state lives in shared memory when it fits;
+// otherwise the hottest arrays that fit the build's budget do (wake table
+// first) and the rest stays in global memory.
 //
 // Inside a block, work items are
-//   - one warp per switch: plan + pull forwarding (section 4.2) for up to 64
-//     ports, the per-egress plan bitmaps staged in shared memory;
-//   - one warp per 32 ranks: DAG advance with the analytic intra-server model
-//     (sections 3.2, 4.1), NIC injection, NIC receive and acknowledgements.
-// Warps own disjoint item ranges, read their 32 wake ticks at once and ballot
-// the items due at the current tick.  Reads of state another entity may
+//   - switches: plan + pull forwarding (section 4.2), two ports a lane, the
+//     per-egress plan bitmaps in shared memory; the latency build forwards
+//     one switch a warp pass, the others pack up to four (64 ports);
+//   - groups of 32 ranks, a lane each: DAG advance with the analytic
+//     intra-server model (sections 3.2, 4.1), NIC injection, NIC receive and
+//     acknowledgements.
+// Items are dealt to warps round-robin; a warp reads 32 of its wake ticks at
+// once and ballots the items due at the current tick.  Three builds differ
+// only in registers, warps and shared memory a block (k_megakernel<1..3>).  Reads of state another entity may
 // change in the same tick see start-of-tick values: queue counters carry the
 // tick of their last change (at most one push and one pop per queue and
 // tick), start ticks are read as "joined before this tick", and completion
