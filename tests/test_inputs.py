@@ -118,3 +118,33 @@ def test_config5_fabrics():
     assert {len(c.ranks) for c in dp} == {128}
     assert max(max(c.ranks) for c in w.colls) == 4095
     assert {(e.algo, e.nc, e.chunk) for e in b.experiments} == {(I.RING, 8, 256 << 10)}
+
+
+def test_moe_workload_shape():
+    """R22: dispatch then combine.  Same GPU: no traffic; same server: one
+    analytic exchange per server whose size is the largest per-GPU share;
+    other servers: one network all-to-all.  Combine uses the transposed
+    sizes, and each rank's combine waits for both of its dispatch parts."""
+    R, gpus = 16, 8
+    rng = np.random.default_rng(5)
+    byte = rng.integers(0, 4, (R, R)) * 14_336
+    w = I.moe_workload(byte, gpus, alpha=3)
+    net = [c for c in w.colls if c.kind == I.A2A and not c.intra]
+    intra = [c for c in w.colls if c.kind == I.A2A and c.intra]
+    assert len(net) == 2 and len(intra) == 2 * (R // gpus)
+    srv = np.arange(R) // gpus
+    for c, M in zip(net, (byte, byte.T)):
+        want = {(i, j): int(M[i, j]) for i in range(R) for j in range(R)
+                if srv[i] != srv[j] and M[i, j]}
+        assert {k: v for k, v in c.a2a.items() if v} == want
+    for c, M in zip(intra, [byte] * (R // gpus) + [byte.T] * (R // gpus)):
+        members = c.ranks
+        share = np.where(np.eye(gpus, dtype=bool), 0, M[np.ix_(members, members)]).sum(axis=1)
+        assert c.nbytes == int(share.max())
+    preds = collections.defaultdict(set)
+    for u, v in w.edges:
+        preds[v].add(u)
+    for r in range(R):
+        disp = {net[0].nodes[r]} | {n for c in intra[: R // gpus] for n, rr in zip(c.nodes, c.ranks) if rr == r}
+        comb = [net[1].nodes[r]] + [n for c in intra[R // gpus:] for n, rr in zip(c.nodes, c.ranks) if rr == r]
+        assert all(preds[v] == disp for v in comb)
