@@ -148,3 +148,56 @@ def test_moe_workload_shape():
         disp = {net[0].nodes[r]} | {n for c in intra[: R // gpus] for n, rr in zip(c.nodes, c.ranks) if rr == r}
         comb = [net[1].nodes[r]] + [n for c in intra[R // gpus:] for n, rr in zip(c.nodes, c.ranks) if rr == r]
         assert all(preds[v] == disp for v in comb)
+
+
+def test_gpt_1f1b_schedule_and_branches():
+    """R23: each GPU's chain runs 1F1B -- stage i does min(PP - i - 1, m)
+    warm-up forwards, then alternates one forward and one backward, then
+    drains the backwards; a pipeline receive sits in the chain, a send
+    branches off it; each layer's DP all-reduce follows that layer's last
+    backward and the previous layer's all-reduce.  PP 3, 4 micro-batches,
+    one layer a stage, 2 GPUs a server (TP 2), DP 1."""
+    pp, micro = 3, 4
+    w = I.gpt_1f1b(3, 2, pp, 3, micro, 16, 8, 2, 1000, 1000)
+    nk = [n["kind"] for n in w.nodes]
+    succ = collections.defaultdict(list)
+    for u, v in w.edges:
+        succ[u].append(v)
+    indeg = collections.Counter(v for _, v in w.edges)
+    coll_of = {n: (c, i) for c in w.colls for i, n in enumerate(c.nodes)}
+    for st in range(pp):
+        r = st * 2                                   # GPU 0 of the stage's one server
+        root = [u for u, n in enumerate(w.nodes) if n["rank"] == r and indeg[u] == 0]
+        assert len(root) == 1
+        seq, u = [], root[0]
+        while True:
+            if nk[u] == I.COMPUTE:
+                key = w.nodes[u]["key"]
+                part, isb, j = key & 1, (key >> 1) & 1, key >> 2   # one layer a stage
+                assert (j // micro) == st
+                if part == 0:
+                    seq.append(("B" if isb else "F", j % micro))
+            nxt = []
+            for v in succ[u]:
+                c, i = coll_of.get(v, (None, None))
+                if c is not None and c.kind == I.P2P and i == 0:
+                    continue                          # a send: a branch off the chain
+                if c is not None and c.kind == I.AR and not c.intra:
+                    continue                          # the DP all-reduce: a branch
+                nxt.append(v)
+            assert len(nxt) <= 1
+            if not nxt:
+                break
+            u = nxt[0]
+        wu = min(pp - st - 1, micro)
+        want = [("F", j) for j in range(wu)]
+        for j in range(micro - wu):
+            want += [("F", wu + j), ("B", j)]
+        want += [("B", j) for j in range(micro - wu, micro)]
+        assert seq == want, (st, seq)
+    dp = [c for c in w.colls if c.kind == I.AR and not c.intra]
+    assert len(dp) == pp * 2                          # per stage and GPU, one layer each
+    for c in dp:
+        (u,) = c.nodes                                # DP 1: one member
+        preds = [a for a, b in w.edges if b == u]
+        assert len(preds) == 1 and nk[preds[0]] == I.INTRA   # after the last backward's TP step
