@@ -1,7 +1,7 @@
 """The seeded input generators build the workloads the configurations name:
 unit conversions, fabric sizes, experiment sweeps and DAG shapes, each
 checked against the numbers stated for it (figures derived by hand from the
-configuration text and the readings of the pages)."""
+configuration text and the pages)."""
 import collections
 
 import numpy as np
@@ -10,7 +10,7 @@ from experiment_network_simulation_gb300 import inputs as I
 
 
 def test_tick_and_delay_units():
-    """R1: one tick is a 4 KiB packet's serialisation: 81,920 ps at 400 Gbps,
+    """One tick is a 4 KiB packet's serialisation: 81,920 ps at 400 Gbps,
     3,276,800 ps at 10 Gbps; 1 us of propagation rounds half-up to 12 ticks
     and to 0 ticks."""
     assert I.tick_ps(4096, 400) == 81_920
@@ -53,7 +53,7 @@ def test_config2_sweep():
 
 
 def test_config3_dag_shape_and_sweep():
-    """R23 and R29: GPT-13B on 128 servers x 8 GPUs (TP 8, PP 4, DP 32), 40
+    """GPT-13B on 128 servers x 8 GPUs (TP 8, PP 4, DP 32), 40
     layers (10 a stage), 8 micro-batches.  Per collective kind:
     - DP all-reduce of 12*h^2/TP*2 B = 78,643,200 B over 32 ranks, one per
       layer and (stage, TP rank): 10 * 32 = 320;
@@ -82,7 +82,7 @@ def test_config3_dag_shape_and_sweep():
 
 
 def test_config4_router_traffic():
-    """R22: 512 ranks, 128 tokens each, top-8 distinct experts of 256 (expert
+    """512 ranks, 128 tokens each, top-8 distinct experts of 256 (expert
     e on rank 2e), 7,168 x 2 B a token copy.  Every rank sends 128 * 8 copies,
     only even ranks receive, an expert gets a token at most once, and the
     Zipf(1.2) popularity makes the busiest expert far busier than the
@@ -101,7 +101,7 @@ def test_config4_router_traffic():
 
 
 def test_config5_fabrics():
-    """R21: 24 three-tier fabrics of {32, 48, 64}-port switches x
+    """24 three-tier fabrics of {32, 48, 64}-port switches x
     oversubscription {1..4}:1 x {plain, rail-optimised}, each with 8,192
     NICs, no switch beyond its radix; ring, NC 8, chunk 256 KiB; the DAG is
     config 3's at DP 128 on the first 512 servers."""
@@ -121,7 +121,7 @@ def test_config5_fabrics():
 
 
 def test_moe_workload_shape():
-    """R22: dispatch then combine.  Same GPU: no traffic; same server: one
+    """Dispatch then combine.  Same GPU: no traffic; same server: one
     analytic exchange per server whose size is the largest per-GPU share;
     other servers: one network all-to-all.  Combine uses the transposed
     sizes, and each rank's combine waits for both of its dispatch parts."""
@@ -151,7 +151,7 @@ def test_moe_workload_shape():
 
 
 def test_gpt_1f1b_schedule_and_branches():
-    """R23: each GPU's chain runs 1F1B -- stage i does min(PP - i - 1, m)
+    """Each GPU's chain runs 1F1B -- stage i does min(PP - i - 1, m)
     warm-up forwards, then alternates one forward and one backward, then
     drains the backwards; a pipeline receive sits in the chain, a send
     branches off it; each layer's DP all-reduce follows that layer's last

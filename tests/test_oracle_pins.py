@@ -569,7 +569,8 @@ def _traced(topo, work, **kw):
 
 
 def test_ring_step_sends_block_i_minus_k():
-    """R12/R13: at step k member i sends block (i - k) mod N.  Reduce-scatter
+    """Ring schedule (the NCCL ring named in Multiverse section 5, cut per
+    AutoCCL section 2.3): at step k member i sends block (i - k) mod N.  Reduce-scatter
     of 12,289 B over 3 ranks, one loop: blocks of ceil(12289/3) = 4,097 B, the
     last 4,095 B, so 2, 2 and 1 packets.  Member 0 sends blocks 0 then 2 (2, 1
     packets), member 1 blocks 1 then 0 (2, 2), member 2 blocks 2 then 1 (1, 2)."""
@@ -580,8 +581,9 @@ def test_ring_step_sends_block_i_minus_k():
 
 
 def test_nic_round_robin_and_partition_extra_byte():
-    """R7 and R12: a NIC serves its send lanes round-robin from its pointer,
-    and the first S mod NC partitions carry one byte more.  Reduce-scatter of
+    """A NIC serves its send lanes round-robin from its pointer (Multiverse
+    section 3.2, NIC send), and of AutoCCL's NC partitions (section 2.3) the
+    first S mod NC carry one byte more.  Reduce-scatter of
     16,385 B over 2 ranks with NC = 2: channel 0's partition is 8,193 B, so
     member 0's block on channel 0 is 4,097 B (2 packets) and on channel 1
     4,096 B (1 packet).  Member 0 injects on channel 0, channel 1, channel 0."""
@@ -593,7 +595,7 @@ def test_nic_round_robin_and_partition_extra_byte():
 
 
 def test_alltoall_chunks_stripe_over_lanes():
-    """R25: all-to-all chunk j goes on lane j mod NC, destinations in rotation
+    """All-to-all chunk j goes on lane j mod NC, destinations in rotation
     order from the next rank.  Rank 0 sends two chunks to rank 1 and one each
     to ranks 2 and 3 (a packet a chunk), NC = 2: lane 0 carries chunks 0 and 2
     (to ranks 1 and 2), lane 1 chunks 1 and 3 (to ranks 1 and 3), so the
@@ -606,7 +608,8 @@ def test_alltoall_chunks_stripe_over_lanes():
 
 
 def test_duration_range_includes_both_ends():
-    """R18: U[lo, hi] includes hi.  With hi = lo + 1 ns and 1 tick = 1 ns, 64
+    """Compute durations drawn from U[lo, hi] include hi.  With hi = lo + 1 ns
+    and 1 tick = 1 ns, 64
     hashed compute nodes take both 1,000 and 1,001 ticks."""
     w = I.Workload(1)
     us = [w.compute(0, 1000, 1001, key=k) for k in range(64)]
@@ -617,7 +620,8 @@ def test_duration_range_includes_both_ends():
 
 
 def test_ecmp_one_path_per_connection_spread_over_up_ports():
-    """R10: the up port is a hash of the connection, so all packets of a
+    """ECMP (Multiverse section 5): the up port is a hash of the connection,
+    so all packets of a
     connection take one path (in order), and connections spread over the up
     ports.  Eight 3-packet messages from leaf 0's hosts to leaf 1's over four
     spines: each ingress port of leaf 0 forwards up on exactly one port, and
@@ -639,7 +643,7 @@ def test_ecmp_one_path_per_connection_spread_over_up_ports():
 
 
 def test_same_tick_starts_go_in_node_order():
-    """R7/R15: nodes of a rank due at one tick start in node order, so the
+    """Nodes of a rank due at one tick start in node order, so the
     lower node's send lane takes the lower lane slot and the NIC's round robin
     (pointer 0) serves it first.  Rank 0's two root sends, to rank 1 (the
     lower node) and to rank 2: the first delivery is at rank 1."""
@@ -652,7 +656,9 @@ def test_same_tick_starts_go_in_node_order():
 
 
 def test_relay_partitions_first_get_the_extra_byte():
-    """R19 with R12's rule: the slice's first S mod K partitions carry one
+    """The pipelined broadcast (On Optimizing the Communication of Model
+    Parallelism, section 3.1) cuts its slice like NC partitions: the first
+    S mod K partitions carry one
     byte more.  S = 3*4096 + 1 in K = 3 partitions over one hop: the first
     partition is 4,097 B (2 packets), the others 4,096 B (1 packet)."""
     w = I.relay_chain(2, 3 * 4096 + 1, 3)
@@ -662,7 +668,7 @@ def test_relay_partitions_first_get_the_extra_byte():
 
 
 def test_zero_byte_message_is_one_packet():
-    """R2: a message of no bytes still costs one packet (a synchronisation
+    """A message of no bytes still costs one packet (a synchronisation
     message): a 0-byte point-to-point send behaves as the 1-packet lone
     message, (n-1) + L(1+delta) = 2(1+delta) ticks from its first injection."""
     delta = 3
@@ -673,7 +679,7 @@ def test_zero_byte_message_is_one_packet():
 
 
 def test_point_to_point_splits_into_chunks():
-    """R25: a point-to-point send is a train of messages of at most C bytes:
+    """A point-to-point send is a train of messages of at most C bytes:
     S = 5*4096 + 100 with C = 8192 is 3 messages (8192, 8192, 4196 B) of
     2 + 2 + 2 = 6 packets."""
     r = run1(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 5 * 4096 + 100), chunk=8192)
@@ -689,7 +695,7 @@ def test_digest_depends_on_completion_ticks():
 
 
 def test_down_route_takes_the_lowest_port():
-    """R10: a switch sends a packet down the lowest port under which its
+    """A switch sends a packet down the lowest port under which its
     destination sits.  Leaf-spine with two parallel links per leaf-spine
     pair: the spine reaches leaf 1 on its ports 2 and 3 and uses port 2."""
     t = I.leaf_spine(2, 1, 1, links_per_pair=2)
@@ -703,7 +709,7 @@ def test_down_route_takes_the_lowest_port():
 
 
 def test_skipping_idle_ticks_changes_nothing():
-    """R26: jumping the clock over ticks in which nothing can change gives the
+    """Jumping the clock over ticks in which nothing can change gives the
     same results as stepping every tick one by one (brute force), over
     bottlenecked senders, credit stalls, incast, relays, rings and trees, and
     200 seeded small paths and incasts of random link times and capacities."""
@@ -748,7 +754,7 @@ def test_skipping_idle_ticks_changes_nothing():
 
 
 def test_tree_waits_for_both_children():
-    """R14: a tree member sends chunk j on (up, or down from the root) only
+    """A tree member sends chunk j on (up, or down from the root) only
     after chunk j arrived from every child.  Three members on one switch,
     sigma 1, delta 0, one 1-packet chunk: both leaves send at tick 1 (the
     joins of tick 0 reach them one tick later); their packets are ready at
@@ -766,7 +772,7 @@ def test_tree_waits_for_both_children():
 
 
 def test_failure_tick_completes_for_every_other_rank():
-    """R31: the tick in which one rank's table overflows still completes for
+    """The tick in which one rank's table overflows still completes for
     the other ranks.  Rank 2 finishes a 2-tick compute node at tick 2, and 17
     intra-server collectives (one more than the 16 running collectives a rank
     may hold) become due at tick 3, so its table overflows at tick 3.  In the
@@ -788,7 +794,8 @@ def test_failure_tick_completes_for_every_other_rank():
 
 
 def test_intra_server_time_rounds_up():
-    """R17: bytes/beta rounds up to whole ticks.  All-reduce over g = 4 of
+    """The analytic model (Multiverse section 4.1) rounds bytes/beta up to
+    whole ticks.  All-reduce over g = 4 of
     S = 8,001 B moves ceil(2*3*8001/4) = 12,002 B per GPU: at 1 tick per
     1,000 B that is 13 ticks (12.002 rounded up), after alpha = 7."""
     w = I.Workload(4)
@@ -798,7 +805,7 @@ def test_intra_server_time_rounds_up():
 
 
 def test_tick_limit_is_exclusive():
-    """R27: ticks stop at 0xFFF00000: a node that would end there overflows,
+    """Ticks stop at 0xFFF00000: a node that would end there overflows,
     one that ends a tick earlier completes (1 tick = 1 ns)."""
     limit = 0xFFF00000
     st = []
@@ -827,7 +834,7 @@ def test_receive_counters_are_freed():
 
 
 def test_routes_use_no_same_level_link():
-    """R10: routes go up then down; a link between two switches of one level
+    """Routes go up then down; a link between two switches of one level
     is neither, so no packet crosses it.  Two leaves under one spine, wired
     to each other too: eight connections each way between leaf 0's hosts
     and leaf 1's all pass the spine."""
@@ -853,7 +860,7 @@ def test_routes_use_no_same_level_link():
 
 
 def test_ecmp_depends_on_seed_and_switch():
-    """R10: the up port hashes the connection with the experiment's ECMP seed
+    """The up port hashes the connection with the experiment's ECMP seed
     and the switch.  Another seed moves some connections to other up ports.
     In a k=4 fat-tree the edge and the aggregation switches both have their
     up ports at local ports 2 and 3, so a hash blind to the switch would
@@ -885,7 +892,7 @@ def test_random_scenarios_keep_invariants():
     """Seeded random collectives on random small fabrics: every run ends
     DONE, delivers every packet it injected, breaks no run-time invariant
     (queue within cap, links within their rate, delivery at the addressed
-    host) and gives the same results stepped tick by tick (R26)."""
+    host) and gives the same results stepped tick by tick."""
     rng = np.random.default_rng(2024)
     ex = []
     for _ in range(200):
@@ -925,10 +932,11 @@ def test_random_scenarios_keep_invariants():
 
 
 def test_ingress_queue_is_fifo_with_head_of_line_blocking():
-    """R3: an ingress port is one FIFO; its packets leave in arrival order,
+    """An ingress port is one FIFO (the per-ingress to-do list of Multiverse
+    section 4.2); its packets leave in arrival order,
     so a packet for a free egress waits behind a head whose egress is busy
     (head-of-line blocking).  Rank 0 alternates packets to ranks 1 and 3
-    (lanes in node order, R7) while ranks 2 and 4 also send to rank 1: port
+    (lanes in node order) while ranks 2 and 4 also send to rank 1: port
     1 serves ingress 0 a third of the time but rank 0 offers it half its
     packets, so ingress 0 backs up.  Its packets still leave in exactly the
     order rank 0 injected them, and packets for the idle port 3 wait
