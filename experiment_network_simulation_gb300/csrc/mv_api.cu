@@ -129,7 +129,7 @@ int plan(const mv_batch_desc *d, Layout &L)
         for (u32 p = 0; p < R.nq; p++) {
             i32 pe = d->port_peer[R.port_off + p];
             u32 sg = d->port_sigma[R.port_off + p], dl = d->port_delta[R.port_off + p];
-            if (sg == 0 || sg > 65535 || dl + 1 > kPopLog) return MV_EINVAL;
+            if (sg == 0 || sg > 65535 || dl >= kPopLog) return MV_EINVAL;
             R.rdv = std::min(R.rdv, dl + 1);
             if (pe >= 0) {
                 if ((u32)pe >= R.nq || d->port_peer[R.port_off + pe] != (i32)p) return MV_EINVAL;
@@ -142,7 +142,7 @@ int plan(const mv_batch_desc *d, Layout &L)
             u32 hp = d->host_port[R.host_off + h];
             u32 sg = d->host_sigma[R.host_off + h], dl = d->host_delta[R.host_off + h];
             if (hp >= R.nq || d->port_peer[R.port_off + hp] != -(i32)(h + 1)) return MV_EINVAL;
-            if (sg == 0 || sg > 65535 || dl + 1 > kPopLog) return MV_EINVAL;
+            if (sg == 0 || sg > 65535 || dl >= kPopLog) return MV_EINVAL;
             R.rdv = std::min(R.rdv, dl + 1);
         }
         // packed records the forwarding and injection steps read per packet

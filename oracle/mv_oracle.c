@@ -95,6 +95,10 @@ typedef struct orc_out {
     uint32_t *rec_count;                    /* per experiment */
     uint32_t *rec_sender, *rec_key, *rec_tick; /* concatenated, rec_cap each */
     uint64_t *violations;                   /* per experiment: broken invariants */
+    /* per collective instance, concatenated per experiment (the workload's
+     * collectives in order): earliest member start and latest member end;
+     * UNSET while some member has not ended (optional: may be NULL) */
+    uint32_t *coll_start, *coll_end;
 } orc_out;
 
 /* Optional event trace of one run (parity bisection): what happened at which
@@ -945,8 +949,123 @@ typedef struct offs {
     uint32_t *host, *sw, *port, *rank, *node, *edge, *coll, *memb, *a2a, *a2a_in;
 } offs;
 
+/* The inputs this simulator takes, checked before any run (-2 when a batch
+ * breaks one): the limits the library's header documents, so that both
+ * sides refuse the same batches.  Switches have 1..64 ports; a link's
+ * serialisation time is 1..65535 ticks and its delay + 1 at most 64 ticks
+ * (the pop log keeps 64 entries); hosts number 1..65535; a collective has
+ * 1..65535 members and fewer than 2^40 bytes; every DAG edge joins nodes of
+ * one rank and the predecessor counts match the edges; every membership
+ * names a node of its own kind and rank; an experiment has 1..1024
+ * channels, 2..1024 queue slots and a chunk size whenever a network
+ * collective other than the relay needs one. */
+static int validate(const orc_batch *b, const offs *o)
+{
+    if (b->version != 1 || b->n_topos == 0 || b->n_works == 0) return -2;
+    for (uint32_t t = 0; t < b->n_topos; t++) {
+        uint32_t nh = b->topo_nhosts[t], ns = b->topo_nsw[t], nq = b->topo_nports[t];
+        const uint32_t *np = b->sw_nports + o->sw[t], *lev = b->sw_level + o->sw[t];
+        const int32_t *peer = b->port_peer + o->port[t];
+        const uint32_t *hp = b->host_port + o->host[t];
+        if (nh == 0 || nh > 65535 || ns == 0) return -2;
+        uint64_t q = 0;
+        for (uint32_t w = 0; w < ns; w++) {
+            if (np[w] == 0 || np[w] > 64 || lev[w] == 0 || lev[w] > 250) return -2;
+            q += np[w];
+        }
+        if (q != nq) return -2;
+        for (uint32_t p = 0; p < nq; p++) {
+            uint32_t sg = b->port_sigma[o->port[t] + p], dl = b->port_delta[o->port[t] + p];
+            if (sg == 0 || sg > 65535 || dl > 63) return -2;
+            if (peer[p] >= 0) {
+                if ((uint32_t)peer[p] >= nq || peer[peer[p]] != (int32_t)p) return -2;
+            } else {
+                uint32_t h = (uint32_t)(-(peer[p] + 1));
+                if (h >= nh || hp[h] != p) return -2;
+            }
+        }
+        for (uint32_t h = 0; h < nh; h++) {
+            uint32_t sg = b->host_sigma[o->host[t] + h], dl = b->host_delta[o->host[t] + h];
+            if (hp[h] >= nq || peer[hp[h]] != -(int32_t)(h + 1)) return -2;
+            if (sg == 0 || sg > 65535 || dl > 63) return -2;
+        }
+    }
+    for (uint32_t w = 0; w < b->n_works; w++) {
+        uint32_t nr = b->work_nranks[w], nn = b->work_nnodes[w], nco = b->work_ncolls[w];
+        const uint32_t *cnt = b->rank_nnodes + o->rank[w];
+        const uint32_t *kind = b->node_kind + o->node[w], *arg = b->node_arg + o->node[w];
+        const uint32_t *nsucc = b->node_nsucc + o->node[w], *succ = b->succ + o->edge[w];
+        uint64_t tot = 0, edges = 0;
+        for (uint32_t r = 0; r < nr; r++) tot += cnt[r];
+        if (tot != nn) return -2;
+        for (uint32_t u = 0; u < nn; u++) edges += nsucc[u];
+        if (edges != b->work_nedges[w]) return -2;
+        uint32_t *rank_of = malloc(sizeof(uint32_t) * (nn + 1));
+        uint32_t *indeg = calloc(nn + 1, sizeof(uint32_t));
+        uint32_t *seen = calloc(nn + 1, sizeof(uint32_t));
+        int bad = 0;
+        for (uint32_t r = 0, u = 0; r < nr; r++)
+            for (uint32_t k = 0; k < cnt[r]; k++) rank_of[u++] = r;
+        for (uint32_t u = 0, j = 0; u < nn && !bad; u++) {
+            if (kind[u] > K_NET) bad = 1;
+            else if (kind[u] != K_COMPUTE && arg[u] >= nco) bad = 1;
+            if (b->node_dur_hi[o->node[w] + u] < b->node_dur_lo[o->node[w] + u]) bad = 1;
+            for (uint32_t k = 0; k < nsucc[u] && !bad; k++, j++) {
+                if (succ[j] >= nn || rank_of[succ[j]] != rank_of[u]) bad = 1;
+                else indeg[succ[j]]++;
+            }
+        }
+        for (uint32_t u = 0; u < nn && !bad; u++)
+            if (indeg[u] != b->node_npred[o->node[w] + u]) bad = 1;
+        uint32_t m = o->memb[w], ra = o->a2a[w], ca = o->a2a_in[w];
+        for (uint32_t c = 0; c < nco && !bad; c++) {
+            uint32_t g = o->coll[w] + c, N = b->coll_nmembers[g], k = b->coll_kind[g];
+            int intra = b->coll_intra[g] != 0;
+            if (N == 0 || N > 65535 || k > C_A2A || b->coll_bytes[g] >= (1ull << 40)) { bad = 1; break; }
+            if (intra && (b->coll_alpha[g] == 0 || b->coll_beta_den[g] == 0 ||
+                          b->coll_beta_num[g] > (1u << 20))) { bad = 1; break; }
+            if (!intra && k == C_RELAY && b->coll_parts[g] == 0) { bad = 1; break; }
+            if (!intra && k == C_P2P && N != 2) { bad = 1; break; }
+            if (m + N > o->memb[w + 1]) { bad = 1; break; }
+            for (uint32_t i = 0; i < N && !bad; i++, m++) {
+                uint32_t rr = b->member_rank[m], u = b->member_node[m];
+                if (rr >= nr || u >= nn || rank_of[u] != rr || seen[u]) { bad = 1; break; }
+                if (kind[u] != (intra ? K_INTRA : K_NET) || arg[u] != c) { bad = 1; break; }
+                seen[u] = 1;
+                uint32_t na = b->member_a2a_n[m], ni = b->member_a2a_in_n[m];
+                if (ra + na > o->a2a[w + 1] || ca + ni > o->a2a_in[w + 1]) { bad = 1; break; }
+                for (uint32_t j = 0; j < na; j++, ra++)
+                    if (b->a2a_dst[ra] >= N || b->a2a_dst[ra] == i ||
+                        b->a2a_bytes[ra] >= (1ull << 40)) bad = 1;
+                for (uint32_t j = 0; j < ni; j++, ca++)
+                    if (b->a2a_in_src[ca] >= N) bad = 1;
+            }
+        }
+        if (!bad && (m != o->memb[w + 1] || ra != o->a2a[w + 1] || ca != o->a2a_in[w + 1])) bad = 1;
+        for (uint32_t u = 0; u < nn && !bad; u++)
+            if (kind[u] != K_COMPUTE && !seen[u]) bad = 1;
+        const uint64_t *mm = b->mem + (size_t)10 * w;
+        if (mm[9] && (mm[1] == 0 || mm[2] == 0)) bad = 1;
+        free(rank_of); free(indeg); free(seen);
+        if (bad) return -2;
+    }
+    for (uint32_t e = 0; e < b->n_exps; e++) {
+        uint32_t ti = b->exp_topo[e], wi = b->exp_work[e];
+        if (ti >= b->n_topos || wi >= b->n_works) return -2;
+        if (b->work_nranks[wi] > b->topo_nhosts[ti] || b->exp_algo[e] > A_TREE ||
+            b->exp_nc[e] == 0 || b->exp_nc[e] > 1024 || b->exp_pkt[e] == 0 ||
+            b->exp_cap[e] < 2 || b->exp_cap[e] > 1024 || b->exp_tick_ps[e] == 0)
+            return -2;
+        if (b->exp_chunk[e] == 0)
+            for (uint32_t c = o->coll[wi]; c < o->coll[wi + 1]; c++)
+                if (!b->coll_intra[c] && b->coll_kind[c] != C_RELAY) return -2;
+    }
+    return 0;
+}
+
 static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit,
-                   orc_out *out, uint64_t node_off, uint64_t rec_off, orc_event *trace,
+                   orc_out *out, uint64_t node_off, uint64_t rec_off, uint64_t coll_off,
+                   orc_event *trace,
                    uint64_t trace_cap, uint64_t *trace_n, uint32_t flags)
 {
     sim S_, *s = &S_;
@@ -1090,6 +1209,24 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
     out->ticks_active[e] = active;
     out->rec_count[e] = s->rec_count;
     out->violations[e] = s->violations;
+    /* Per-collective time (Multiverse section 3.1: the network simulator
+     * tells the system simulator when each flow completes; a collective is
+     * done when its last member is): from its first member's start to its
+     * last member's end. */
+    if (out->coll_start && out->coll_end) {
+        for (uint32_t c = 0; c < nco; c++) {
+            uint32_t lo = UNSET, hi = 0;
+            int all_ended = 1;
+            for (uint32_t i = 0; i < s->coll_nmembers[c]; i++) {
+                uint32_t u = mnode(s, c, i);
+                if (s->start[u] < lo) lo = s->start[u];
+                if (s->end[u] == UNSET) all_ended = 0;
+                else if (s->end[u] > hi) hi = s->end[u];
+            }
+            out->coll_start[coll_off + c] = lo;
+            out->coll_end[coll_off + c] = all_ended ? hi : UNSET;
+        }
+    }
     if (trace_n) *trace_n = s->trace_n;
 
     free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
@@ -1110,7 +1247,6 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
 int orc_run_ex(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_out *out,
                orc_event *trace, uint64_t trace_cap, uint64_t *trace_n, uint32_t flags)
 {
-    if (b->version != 1) return -1;
     offs o;
     o.host = prefix(b->topo_nhosts, b->n_topos);
     o.sw = prefix(b->topo_nsw, b->n_topos);
@@ -1124,16 +1260,19 @@ int orc_run_ex(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc
     o.a2a = prefix(b->work_na2a, b->n_works);
     o.a2a_in = prefix(b->work_na2a_in, b->n_works);
     if (e1 == 0 || e1 > b->n_exps) e1 = b->n_exps;
-    uint64_t node_off = 0, rec_off = 0;
-    for (uint32_t e = 0; e < e1; e++) {
+    int bad = validate(b, &o);
+    uint64_t node_off = 0, rec_off = 0, coll_off = 0;
+    for (uint32_t e = 0; e < e1 && !bad; e++) {
         if (e >= e0)
-            run_one(b, &o, e, limit, out, node_off, rec_off, trace, trace_cap, trace_n, flags);
+            run_one(b, &o, e, limit, out, node_off, rec_off, coll_off, trace, trace_cap,
+                    trace_n, flags);
         node_off += b->work_nnodes[b->exp_work[e]];
         rec_off += b->exp_rec_cap[e];
+        coll_off += b->work_ncolls[b->exp_work[e]];
     }
     free(o.host); free(o.sw); free(o.port); free(rank); free(o.node); free(o.edge);
     free(o.coll); free(o.memb); free(o.a2a); free(o.a2a_in);
-    return 0;
+    return bad;
 }
 
 /* Without a trace and with idle ticks skipped.  orc_run_ex: with a trace,

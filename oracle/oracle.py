@@ -60,7 +60,7 @@ _OUT = [("status", "u4"), ("end_tick", "u4"), ("now", "u4"), ("pkts_injected", "
         ("pkt_hops", "u8"), ("pkts_delivered", "u8"), ("msgs_delivered", "u8"),
         ("digest", "u8"), ("ticks_active", "u8"), ("node_start", "u4"), ("node_end", "u4"),
         ("rec_count", "u4"), ("rec_sender", "u4"), ("rec_key", "u4"), ("rec_tick", "u4"),
-        ("violations", "u8")]
+        ("violations", "u8"), ("coll_start", "u4"), ("coll_end", "u4")]
 
 
 class _Out(C.Structure):
@@ -110,6 +110,9 @@ def mix64(z: int) -> int:
 def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
         lib_path: str | None = None, trace_cap: int = 0, no_skip: bool = False) -> dict:
     """Run experiments [e0, e1) of a packed batch (all when e1 == 0).
+    Per collective instance, `coll_start` / `coll_end` hold its first
+    member's start and its last member's end (UNSET while a member has not
+    ended), concatenated per experiment at `coll_offset`.
     `violations` counts broken invariants (queue over capacity, a link faster
     than its serialisation time, a packet delivered to the wrong host).
     With trace_cap > 0 (one experiment: e1 = e0 + 1), `trace` holds its first
@@ -130,7 +133,10 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
         keep[n] = a
         setattr(b, n, a.ctypes.data_as(_CT[t]))
     E = b.n_exps
-    nn = packed["work_nnodes"][packed["exp_work"]].astype(np.int64)
+    # result sizes; an out-of-range workload index is refused by the oracle
+    # itself before it writes anything, so clip it here only to size arrays
+    wk = np.minimum(np.asarray(packed["exp_work"], np.int64), max(0, b.n_works - 1))
+    nn = packed["work_nnodes"][wk].astype(np.int64)
     rc = packed["exp_rec_cap"].astype(np.int64)
     res = {"status": np.full(E, UNSET, np.uint32), "end_tick": np.zeros(E, np.uint32),
            "now": np.zeros(E, np.uint32)}
@@ -142,6 +148,9 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
     res["rec_count"] = np.zeros(E, np.uint32)
     for k in ("rec_sender", "rec_key", "rec_tick"):
         res[k] = np.zeros(max(1, int(rc.sum())), np.uint32)
+    nco = packed["work_ncolls"][wk].astype(np.int64)
+    for k in ("coll_start", "coll_end"):
+        res[k] = np.full(max(1, int(nco.sum())), UNSET, np.uint32)
     o = _Out()
     for n, t in _OUT:
         setattr(o, n, res[n].ctypes.data_as(_CT[t]))
@@ -162,6 +171,7 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
         raise RuntimeError(f"oracle rejected the batch ({rcode})")
     res["node_offset"] = np.concatenate([[0], np.cumsum(nn)])
     res["rec_offset"] = np.concatenate([[0], np.cumsum(rc)])
+    res["coll_offset"] = np.concatenate([[0], np.cumsum(nco)])
     return res
 
 

@@ -83,6 +83,58 @@ def test_too_many_switch_ports_rejected():
     assert mv.library().mv_workspace_bytes(C.byref(d), C.byref(n)) == mv.MV_EINVAL
 
 
+def _both(p):
+    """(library accepts, oracle accepts) for one packed batch."""
+    from oracle import oracle as O
+    d, _ = mv.make_desc(p)
+    n = C.c_uint64()
+    lib_ok = mv.library().mv_workspace_bytes(C.byref(d), C.byref(n)) == mv.MV_OK
+    try:
+        O.run(p, limit=1)
+        orc_ok = True
+    except RuntimeError:
+        orc_ok = False
+    return lib_ok, orc_ok
+
+
+def test_library_and_oracle_refuse_the_same_batches():
+    """The CUDA library and the CPU oracle take the same inputs: both refuse a
+    switch of 65 ports, a link delay of 64 ticks (delay + 1 beyond the
+    64-entry pop log), a serialisation time of 65,536 ticks, 1,025 queue
+    slots or channels, and the other malformed descriptors below; both
+    accept the largest legal values (64 ports, delay 63)."""
+    def one(topo, **kw):
+        w = I.lone_message(2, 0, 1, 4096)
+        kw.setdefault("chunk", 1 << 20)
+        return I.Batch([I.Experiment(topo, w, tick_ps=1000, **kw)]).pack()
+
+    assert _both(one(I.single_switch(64, 1, 63))) == (True, True)
+    assert _both(one(I.single_switch(65, 1, 0))) == (False, False)
+    assert _both(one(I.single_switch(4, 1, 64))) == (False, False)
+    assert _both(one(I.single_switch(4, 65536, 0))) == (False, False)
+    assert _both(one(I.single_switch(4, 65535, 0))) == (True, True)
+    assert _both(one(I.single_switch(4, 1, 0), cap=1025)) == (False, False)
+    assert _both(one(I.single_switch(4, 1, 0), nc=1025)) == (False, False)
+    assert _both(one(I.single_switch(4, 1, 0), chunk=0)) == (False, False)
+    p = I.config1().pack()
+
+    def changed(**changes):
+        q = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in p.items()}
+        for k, f in changes.items():
+            f(q[k]) if callable(f) else q.__setitem__(k, f)
+        return q
+
+    def asym(a): a[0] = a[1]
+    def zero(a): a[0] = 0
+    def big(a): a[0] = 1 << 41
+    def inc(a): a[0] += 1
+    def lev(a): a[0] = 251
+    for q in (changed(version=2), changed(port_peer=asym), changed(port_sigma=zero),
+              changed(exp_nc=zero), changed(coll_bytes=big), changed(node_npred=inc),
+              changed(sw_level=lev), changed(host_delta=lambda a: a.__setitem__(0, 64))):
+        assert _both(q) == (False, False)
+
+
 def test_strerror_names_codes():
     lib = mv.library()
     for code in (0, 1, -1, -2, -3, -4, -5):
@@ -117,7 +169,10 @@ bases = [I.config1().pack(), I.gpt_small(seeds=(0,)).pack(),
          I.Batch([I.Experiment(I.fat_tree(4), I.single_collective(16, I.A2A, 0), nc=2)]).pack(),
          I.config2(n_exp=4).pack()]
 fixed = {k for k in bases[0] if k.startswith("topo_n") or k.startswith("work_n") or k == "version"}
-lib, codes = mv.library(), set()
+lib, codes, differ = mv.library(), set(), []
+check_oracle = sys.argv[4] == "1"
+if check_oracle:
+    from oracle import oracle as O
 for it in range(int(sys.argv[3])):
     p = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in bases[it % len(bases)].items()}
     keys = [k for k, v in p.items() if isinstance(v, np.ndarray) and v.size > 0 and k not in fixed]
@@ -133,9 +188,19 @@ for it in range(int(sys.argv[3])):
             a.flat[i] = vals[int(rng.integers(len(vals)))] % (top + 1)
     d, keep = mv.make_desc(p)
     n, nn, nr = C.c_uint64(), C.c_uint64(), C.c_uint64()
-    codes.add(lib.mv_workspace_bytes(C.byref(d), C.byref(n)))
+    c1 = lib.mv_workspace_bytes(C.byref(d), C.byref(n))
+    codes.add(c1)
     codes.add(lib.mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)))
+    if check_oracle:
+        try:
+            O.run(p, limit=1)
+            ok = True
+        except RuntimeError:
+            ok = False
+        if ok != (c1 == mv.MV_OK):
+            differ.append(it)
 print(sorted(codes))
+print(differ)
 '''
 
 
@@ -148,11 +213,22 @@ def test_descriptor_fuzz_never_crashes():
     child process, so a crash fails the test instead of ending the suite."""
     import subprocess
     import sys
-    p = subprocess.run([sys.executable, "-c", _FUZZ, ROOT, "7", "1500"], capture_output=True,
-                       text=True, timeout=600)
+    p = subprocess.run([sys.executable, "-c", _FUZZ, ROOT, "7", "1500", "0"],
+                       capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-2000:]
-    codes = eval(p.stdout.strip().splitlines()[-1])
+    codes = eval(p.stdout.strip().splitlines()[-2])
     assert set(codes) <= {mv.MV_OK, mv.MV_EINVAL, mv.MV_EOVERFLOW} and mv.MV_EINVAL in codes
+
+
+def test_descriptor_fuzz_library_and_oracle_agree():
+    """On corrupted descriptors the oracle refuses exactly the batches the
+    library refuses (each accepted one runs one tick in the oracle)."""
+    import subprocess
+    import sys
+    p = subprocess.run([sys.executable, "-c", _FUZZ, ROOT, "11", "2000", "1"],
+                       capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    assert eval(p.stdout.strip().splitlines()[-1]) == []
 
 
 def test_size_limits_and_empty_batches():

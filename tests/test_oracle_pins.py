@@ -771,6 +771,100 @@ def test_tree_waits_for_both_children():
     assert int(inj[inj["a"] == 0]["tick"].min()) == 5
 
 
+def test_tree_depth_two_hand_trace():
+    """A tree deep enough to have an internal member: 4 members on one
+    switch (root 0; children 1 and 2; member 1's child 3), sigma 1, delta 0,
+    one channel, two 1-packet chunks.  Traced by hand: a packet injected at
+    t is at the switch at t+1 and delivered at t+2; a receipt counts from the
+    next tick; acknowledgements take 2 ticks.  Leaves 2 and 3 send chunks 0,
+    1 up at 1, 2 (delivered 3, 4).  Internal member 1 sends chunk j up only
+    after it holds chunk j from child 3: at 4 and 5 (delivered at the root at
+    6, 7).  The root broadcasts chunk 0 at 7 (to 1) and 8 (to 2), once both
+    children's chunk 0 arrived, then chunk 1 at 9 and 10, round-robin over
+    its two down lanes.  Member 1 forwards chunk j down only after the
+    root's chunk j arrived: delivered at 9 and 11, so sent at 10 and 12
+    (delivered at 3 at 12, 14).  Ends: root 14 (last acknowledgement of its
+    chunk 1 to member 2), member 1 16 (acknowledgement of its last send to
+    3), member 2 12, member 3 14."""
+    w = I.single_collective(4, I.AR, 2 * 4096)
+    e = I.Experiment(I.single_switch(4, 1, 0), w, algo=I.TREE, nc=1, chunk=4096,
+                     tick_ps=1000, rec_cap=64)
+    r = O.run(I.Batch([e]).pack(), 0, 1, trace_cap=10_000)
+    assert r["status"][0] == O.ST_DONE
+    assert list(r["node_end"][:4]) == [14, 16, 12, 14]
+    ev = r["trace"]
+    inj = ev[ev["kind"] == O.EV_INJECT]
+    ticks = {m: [int(x["tick"]) for x in inj if x["a"] == m] for m in range(4)}
+    assert ticks == {0: [7, 8, 9, 10], 1: [4, 5, 10, 12], 2: [1, 2], 3: [1, 2]}
+    msg = ev[ev["kind"] == O.EV_MESSAGE]
+    got = sorted((int(x["tick"]), int(x["a"]), int(x["b"])) for x in msg)
+    # (delivery tick, receiving rank, sending node); node = rank here
+    assert got == [(3, 0, 2), (3, 1, 3), (4, 0, 2), (4, 1, 3), (6, 0, 1), (7, 0, 1),
+                   (9, 1, 0), (10, 2, 0), (11, 1, 0), (12, 2, 0), (12, 3, 1), (14, 3, 1)]
+
+
+def _conn_key(node, chan, kind, drank):
+    """The 24-bit connection identifier a packet carries (R10/R11 layout)."""
+    return O.mix64(node | ((chan * 4 + kind) << 32) | (drank << 44)) & 0xFFFFFF
+
+
+@pytest.mark.parametrize("topo", ["switch", "switch_delta", "leafspine"])
+def test_tree_seven_members_data_dependencies(topo):
+    """A reduction cannot send what it has not received: in a 7-member tree
+    (depth 2; members 1 and 2 internal), with 2 channels of 2 one-packet
+    chunks each, every member sends chunk j of channel c up only after
+    chunk j of channel c arrived from each of its children, the root sends
+    it down only after both children's arrived, and an internal member
+    forwards it down only after the root's (its parent's) arrived.  Every
+    member receives each chunk once from each child and once from its
+    parent, in chunk order on each connection."""
+    N, nc, chunks = 7, 2, 2
+    t = {"switch": I.single_switch(N, 1, 0), "switch_delta": I.single_switch(N, 1, 3),
+         "leafspine": I.leaf_spine(2, 2, 4, 2)}[topo]
+    w = I.single_collective(N, I.AR, nc * chunks * 4096)
+    e = I.Experiment(t, w, algo=I.TREE, nc=nc, chunk=4096, tick_ps=1000, rec_cap=1024)
+    r = O.run(I.Batch([e]).pack(), 0, 1, trace_cap=100_000)
+    assert r["status"][0] == O.ST_DONE and r["trace_total"] == len(r["trace"])
+    ev = r["trace"]
+    inj = ev[ev["kind"] == O.EV_INJECT]
+    n = int(r["rec_count"][0])
+    rec = sorted(zip(r["rec_key"][:n].tolist(), r["rec_sender"][:n].tolist(),
+                     r["rec_tick"][:n].tolist()), key=lambda x: x[2])
+    assert n == 2 * (N - 1) * nc * chunks
+
+    def sends(node, key):          # injection tick of each chunk, in order
+        return [int(x["tick"]) for x in inj if x["a"] == node and x["b"] == key]
+
+    def delivered(node, key):      # delivery tick of each chunk, in order
+        return [tk for k, s, tk in rec if k == key and s == node]
+
+    kids = {i: [c for c in (2 * i + 1, 2 * i + 2) if c < N] for i in range(N)}
+    for ch in range(nc):
+        up_in = {i: [delivered(c, _conn_key(c, ch, 0, i)) for c in kids[i]] for i in range(N)}
+        for i in range(N):
+            for d in up_in[i]:
+                assert len(d) == chunks
+        for i in range(1, N):
+            par = (i - 1) // 2
+            up = sends(i, _conn_key(i, ch, 0, par))
+            assert len(up) == chunks
+            for j in range(chunks):
+                for d in up_in[i]:
+                    assert up[j] > d[j], (topo, ch, i, j)
+            down_in = delivered(par, _conn_key(par, ch, 1 + (i - 2 * par - 1), i))
+            assert len(down_in) == chunks
+            for k, c in enumerate(kids[i]):
+                down = sends(i, _conn_key(i, ch, 1 + k, c))
+                assert len(down) == chunks
+                for j in range(chunks):
+                    assert down[j] > down_in[j], (topo, ch, i, j)
+        for k, c in enumerate(kids[0]):
+            down = sends(0, _conn_key(0, ch, 1 + k, c))
+            for j in range(chunks):
+                for d in up_in[0]:
+                    assert down[j] > d[j], (topo, ch, j)
+
+
 def test_failure_tick_completes_for_every_other_rank():
     """The tick in which one rank's table overflows still completes for
     the other ranks.  Rank 2 finishes a 2-tick compute node at tick 2, and 17
