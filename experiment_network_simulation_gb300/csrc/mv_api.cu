@@ -40,10 +40,10 @@ struct Layout {
         nmemb = 0, na2a = 0, na2a_in = 0;
     u64 route_bytes = 0, q_total = 0, slot_total = 0, plog_total = 0, eg_total = 0,
         rk_total = 0, pend_total = 0, act_total = 0, lane_total = 0, portc_total = 0,
-        nd_total = 0, rec_total = 0, items = 0;
+        nd_total = 0, rec_total = 0, coll_total = 0, items = 0;
     u32 warps = 1, image = 16;      // megakernel block size and shared image budget
     u32 variant = 1;                // 1: every experiment staged whole; 2: some are not
-    u32 max_level = 0, max_nodes = 0, max_queues = 0, max_ranks = 0;
+    u32 max_level = 0, max_nodes = 0, max_queues = 0, max_ranks = 0, max_colls = 0;
     u64 max_pairs = 0;
     // host copies of the derived tables
     std::vector<TopoRec> topo;
@@ -66,7 +66,8 @@ struct Layout {
     u64 static_bytes = 0;
     Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_rdirty, r_pend, r_act,
         r_lanes, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
-        r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_glob, r_wake;
+        r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_coll_start, r_coll_end, r_glob,
+        r_wake;
     u64 total = 0;
 
     u64 cur = 0;
@@ -382,6 +383,7 @@ int plan(const mv_batch_desc *d, Layout &L)
         X.portc_off = L.portc_total;
         X.nd_off = L.nd_total;
         X.rec_off = L.rec_total;
+        X.coll_res_off = L.coll_total;
         L.q_total += X.nq;
         L.slot_total += (u64)X.nq * X.cap;
         L.plog_total += (u64)X.nq * T.plog;
@@ -393,6 +395,8 @@ int plan(const mv_batch_desc *d, Layout &L)
         L.portc_total += (u64)W.nr * X.port_cap;
         L.nd_total += W.nn;
         L.rec_total += X.rec_cap;
+        L.coll_total += W.ncoll;
+        L.max_colls = std::max(L.max_colls, W.ncoll);
         L.max_nodes = std::max(L.max_nodes, W.nn);
         L.max_queues = std::max(L.max_queues, X.nq);
         L.max_ranks = std::max(L.max_ranks, W.nr);
@@ -517,6 +521,8 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_rec_sender = L.take(4 * L.rec_total);
     L.r_rec_key = L.take(4 * L.rec_total);
     L.r_rec_tick = L.take(4 * L.rec_total);
+    L.r_coll_start = L.take(4 * L.coll_total);
+    L.r_coll_end = L.take(4 * L.coll_total);
     L.r_glob = L.take(sizeof(Glob));
     L.r_wake = L.take(12 * L.items);
     L.total = L.cur;
@@ -603,6 +609,8 @@ Params make_params(void *ws, const Layout &L)
     P.rec_sender = at<u32>(ws, L.r_rec_sender);
     P.rec_key = at<u32>(ws, L.r_rec_key);
     P.rec_tick = at<u32>(ws, L.r_rec_tick);
+    P.coll_start = at<u32>(ws, L.r_coll_start);
+    P.coll_end = at<u32>(ws, L.r_coll_end);
     P.order = at<u32>(ws, L.r_order);
     P.sw_rec = at<uint2>(ws, L.r_sw_rec);
     P.port_rec = at<uint4>(ws, L.r_port_rec);
@@ -676,13 +684,15 @@ int mv_workspace_bytes(const mv_batch_desc *desc, uint64_t *bytes)
     return rc;
 }
 
-int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_records)
+int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_records,
+                    uint64_t *n_colls)
 {
     Layout L;
     int rc = plan(desc, L);
     if (rc != MV_OK) return rc;
     if (n_nodes) *n_nodes = L.nd_total;
     if (n_records) *n_records = L.rec_total;
+    if (n_colls) *n_colls = L.coll_total;
     return MV_OK;
 }
 
@@ -845,6 +855,16 @@ int mv_results(mv_ctx *c, const mv_results_view *o)
     if (e == cudaSuccess && o->rec_tick && L.rec_total)
         e = cudaMemcpyAsync(o->rec_tick, c->P.rec_tick, 4 * L.rec_total, cudaMemcpyDeviceToHost,
                             c->stream);
+    // per-collective times: reduced on the device from the per-node ticks
+    if (e == cudaSuccess && (o->coll_start || o->coll_end) && L.coll_total) {
+        e = launch_coll_times(c->P, L.max_colls, c->stream);
+        if (e == cudaSuccess && o->coll_start)
+            e = cudaMemcpyAsync(o->coll_start, c->P.coll_start, 4 * L.coll_total,
+                                cudaMemcpyDeviceToHost, c->stream);
+        if (e == cudaSuccess && o->coll_end)
+            e = cudaMemcpyAsync(o->coll_end, c->P.coll_end, 4 * L.coll_total,
+                                cudaMemcpyDeviceToHost, c->stream);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) return MV_ECUDA;
     for (u32 i = 0; i < L.E; i++) {
@@ -892,11 +912,47 @@ int mv_destroy(mv_ctx *c)
 // Allocation-free one-shot entry point: same create/run/results/destroy path,
 // with the workspace in this file-scope device array instead of caller memory.
 static __device__ __align__(256) unsigned char g_static_scratch[MV_STATIC_SCRATCH_BYTES];
+// Set-up token of the array's device copy: device data starts at zero when
+// the module is (re)loaded on a device, so a token that no longer reads back
+// means the cached address belongs to an earlier load (for example before a
+// cudaDeviceReset) and the set-up runs again.
+static __device__ unsigned long long g_static_token;
 
 namespace {
 constexpr int kStaticMaxDevices = 64;
 std::mutex g_static_mu;
 void *g_static_ptr[kStaticMaxDevices] = {};
+unsigned long long g_static_tok[kStaticMaxDevices] = {};
+unsigned long long g_static_next = 0;
+
+// The array's device address for the current device: looked up (with that
+// device current) by the first call on the device, and again whenever the
+// module's device data was re-initialised since.  Host code cannot use the
+// array's name as an address: it needs the device address.
+int static_scratch(int dev, cudaStream_t st, void **out)
+{
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    unsigned long long tok = 0;
+    if (g_static_ptr[dev]) {
+        if (cudaMemcpyFromSymbolAsync(&tok, g_static_token, sizeof tok, 0,
+                                      cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return MV_ECUDA;
+    }
+    if (!g_static_ptr[dev] || tok != g_static_tok[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MV_ECUDA;
+        const unsigned long long t = ++g_static_next;
+        if (cudaMemcpyToSymbolAsync(g_static_token, &t, sizeof t, 0, cudaMemcpyHostToDevice,
+                                    st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return MV_ECUDA;
+        g_static_ptr[dev] = p;
+        g_static_tok[dev] = t;
+    }
+    *out = g_static_ptr[dev];
+    return MV_OK;
+}
 }  // namespace
 
 extern "C" int mv_simulate_static(const mv_batch_desc *desc, uint32_t max_ticks, void *stream,
@@ -905,22 +961,13 @@ extern "C" int mv_simulate_static(const mv_batch_desc *desc, uint32_t max_ticks,
     if (!desc || !out) return MV_EINVAL;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return MV_ECUDA;
-    void *scratch = nullptr;
-    {
-        // once per device, with that device current: host code cannot use
-        // the array's name as an address, it needs the device address
-        std::lock_guard<std::mutex> lock(g_static_mu);
-        if (!g_static_ptr[dev]) {
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MV_ECUDA;
-            g_static_ptr[dev] = p;
-        }
-        scratch = g_static_ptr[dev];
-    }
     uint64_t need = 0;
     int rc = mv_workspace_bytes(desc, &need);
     if (rc != MV_OK) return rc;
     if (need > MV_STATIC_SCRATCH_BYTES) return MV_ENOMEM;
+    void *scratch = nullptr;
+    rc = static_scratch(dev, static_cast<cudaStream_t>(stream), &scratch);
+    if (rc != MV_OK) return rc;
     mv_ctx *c = nullptr;
     rc = mv_create(desc, scratch, MV_STATIC_SCRATCH_BYTES, stream, &c);
     if (rc != MV_OK) return rc;

@@ -54,7 +54,7 @@ struct ExpRec {
     u32 topo, work, algo, nc, pkt, cap, tick_ps, rec_cap;
     u64 chunk, dur_seed, ecmp_seed, gpu_mem;
     u64 q_off, slot_off, plog_off, eg_off, rk_off, pend_off, act_off, lane_off, portc_off,
-        nd_off, rec_off;
+        nd_off, rec_off, coll_res_off;
     u32 nq, nsw, nr, nn;            // queues (switch ingress, then NIC receive), switches, ranks, nodes
     u32 item_off, n_items;          // work items: switches, then groups of 32 ranks
     u32 lane_cap, port_cap, pend_cap, act_cap;
@@ -141,6 +141,7 @@ struct Params {
     i32 *nd_out;
     ExpCtl *ctl;
     u32 *rec_sender, *rec_key, *rec_tick;
+    u32 *coll_start, *coll_end;  // per experiment and collective: first member start, last end
     u32 *wake;               // per experiment: own wake tick of each item, then two poke words each
     u32 n_exps, n_topos;
     Glob *glob;
@@ -215,6 +216,7 @@ cudaError_t launch_routes(const Params &p, u64 n_pairs_max, u32 level, cudaStrea
 cudaError_t launch_up_lists(const Params &p, u32 n_sw_total, cudaStream_t st);
 cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_ranks,
                         cudaStream_t st);
+cudaError_t launch_coll_times(const Params &p, u32 max_colls, cudaStream_t st);
 // variant 1: latency (one block of <= 8 warps an SM, register view); 2: occupancy (two
 // blocks of 8 warps an SM); 3: one block of 16 warps an SM (more shared memory a block)
 cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,

@@ -211,6 +211,31 @@ __global__ void k_init_ctl(Params P)
     }
 }
 
+// Per-collective times from the per-node ticks (Multiverse section 3.1: the
+// system simulator learns of each flow's completion; a collective is done
+// when its last member is): first member start, last member end, or kUnset
+// while some member has not ended.  blockIdx.y strides over experiments,
+// x threads over the workload's collectives.
+__global__ void k_coll_times(Params P)
+{
+    for (u32 e = blockIdx.y; e < P.n_exps; e += gridDim.y) {
+        const ExpRec &X = P.exp[e];
+        const WorkRec W = P.work[X.work];
+        for (u32 c = blockIdx.x * blockDim.x + threadIdx.x; c < W.ncoll; c += gridDim.x * blockDim.x) {
+            const u32 g = W.coll_off + c, N = P.coll_nmembers[g];
+            const u32 *mn = P.member_node + W.memb_off + P.coll_mstart[g];
+            u32 lo = kUnset, hi = 0;
+            for (u32 i = 0; i < N; i++) {
+                const u64 u = X.nd_off + mn[i];
+                lo = min(lo, P.nd_start[u]);
+                hi = max(hi, P.nd_end[u]);       // kUnset (not ended) is the largest value
+            }
+            P.coll_start[X.coll_res_off + c] = lo;
+            P.coll_end[X.coll_res_off + c] = hi;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- block state
 // The experiment a block holds: its records, and generic pointers to its
 // slice of every dynamic array (shared memory when staged, global if not).
@@ -1748,6 +1773,15 @@ cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_
     k_init_ctl<<<(p.n_exps + 255) / 256, 256, 0, st>>>(p);
     dim3 grid(bx, p.n_exps < 65535 ? p.n_exps : 65535);
     k_init<<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_coll_times(const Params &p, u32 max_colls, cudaStream_t st)
+{
+    u32 bx = (max_colls + 255) / 256;
+    bx = bx ? (bx > 256 ? 256 : bx) : 1;
+    dim3 grid(bx, p.n_exps < 65535 ? p.n_exps : 65535);
+    k_coll_times<<<grid, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -51,7 +51,8 @@ class BatchDesc(C.Structure):
 _RES = [("status", "u4"), ("end_tick", "u4"), ("now", "u4"), ("pkts_injected", "u8"),
         ("pkt_hops", "u8"), ("pkts_delivered", "u8"), ("msgs_delivered", "u8"),
         ("digest", "u8"), ("rec_count", "u4"), ("node_start", "u4"), ("node_end", "u4"),
-        ("rec_sender", "u4"), ("rec_key", "u4"), ("rec_tick", "u4")]
+        ("rec_sender", "u4"), ("rec_key", "u4"), ("rec_tick", "u4"), ("coll_start", "u4"),
+        ("coll_end", "u4")]
 
 
 class ResultsView(C.Structure):
@@ -78,7 +79,7 @@ def library(build: bool = True) -> C.CDLL:
         lib = C.CDLL(path)
         vp, u64p = C.c_void_p, C.POINTER(C.c_uint64)
         lib.mv_workspace_bytes.argtypes = [C.POINTER(BatchDesc), u64p]
-        lib.mv_result_sizes.argtypes = [C.POINTER(BatchDesc), u64p, u64p]
+        lib.mv_result_sizes.argtypes = [C.POINTER(BatchDesc), u64p, u64p, u64p]
         lib.mv_create.argtypes = [C.POINTER(BatchDesc), vp, C.c_uint64, vp, C.POINTER(vp)]
         lib.mv_run.argtypes = [vp, C.c_uint32, u64p]
         lib.mv_run_ex.argtypes = [vp, C.c_uint32, C.POINTER(RunOpts), u64p]
@@ -156,9 +157,9 @@ class Simulator:
         if rc != MV_OK:
             raise MVError(rc, "mv_workspace_bytes")
         self.ws_bytes = int(n.value)
-        nn, nr = C.c_uint64(0), C.c_uint64(0)
-        self.lib.mv_result_sizes(C.byref(self.desc), C.byref(nn), C.byref(nr))
-        self.n_nodes, self.n_recs = int(nn.value), int(nr.value)
+        nn, nr, nco = C.c_uint64(0), C.c_uint64(0), C.c_uint64(0)
+        self.lib.mv_result_sizes(C.byref(self.desc), C.byref(nn), C.byref(nr), C.byref(nco))
+        self.n_nodes, self.n_recs, self.n_colls = int(nn.value), int(nr.value), int(nco.value)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=self.device)
         self.ctx = C.c_void_p()
         with torch.cuda.device(self.device):
@@ -172,6 +173,8 @@ class Simulator:
         self.node_offset = np.concatenate([[0], np.cumsum(nn_per)])
         rc_per = packed["exp_rec_cap"].astype(np.int64)
         self.rec_offset = np.concatenate([[0], np.cumsum(rc_per)])
+        nc_per = packed["work_ncolls"][packed["exp_work"]].astype(np.int64)
+        self.coll_offset = np.concatenate([[0], np.cumsum(nc_per)])
 
     def run(self, max_ticks: int = UNSET - 1, watchdog_ns: int = 0, grid_blocks: int = 0,
             stage: int = STAGE_AUTO, block_warps: int = 0, variant: int = 0) -> int:
@@ -225,6 +228,8 @@ class Simulator:
             r[k] = np.zeros(max(1, self.n_nodes), np.uint32)
         for k in ("rec_sender", "rec_key", "rec_tick"):
             r[k] = np.zeros(max(1, self.n_recs), np.uint32)
+        for k in ("coll_start", "coll_end"):
+            r[k] = np.zeros(max(1, self.n_colls), np.uint32)
         v = ResultsView()
         for n, t in _RES:
             setattr(v, n, r[n].ctypes.data_as(_CT[t]))
@@ -234,6 +239,7 @@ class Simulator:
             raise MVError(rc, "mv_results")
         r["node_offset"] = self.node_offset
         r["rec_offset"] = self.rec_offset
+        r["coll_offset"] = self.coll_offset
         return r
 
     def close(self):

@@ -149,7 +149,16 @@ typedef struct mv_batch_desc {
  * produced; only the first exp_rec_cap are kept).  Per node, concatenated
  * over experiments in batch order (sizes from mv_result_sizes): start and
  * end tick.  Per-message records, concatenated in blocks of exp_rec_cap:
- * sender node, 24-bit connection key, delivery tick, in no particular order.
+ * sender node, 24-bit connection key, delivery tick, in no particular order
+ * (Multiverse section 3.1: the network simulator reports each flow's
+ * completion to the system simulator).  Per collective instance,
+ * concatenated over experiments in batch order (each experiment's block
+ * lists its workload's collectives in order; sizes from mv_result_sizes):
+ * coll_start, the earliest start tick of its member nodes (MV_UNSET if none
+ * started), and coll_end, the latest end tick of its member nodes (MV_UNSET
+ * while some member has not ended); the collective's time is coll_end -
+ * coll_start, and the iteration time is end_tick.  These are computed on
+ * the device from the per-node ticks when either pointer is given.
  */
 typedef struct mv_results_view {
     uint32_t *status, *end_tick, *now;
@@ -157,6 +166,7 @@ typedef struct mv_results_view {
     uint32_t *rec_count;
     uint32_t *node_start, *node_end;
     uint32_t *rec_sender, *rec_key, *rec_tick;
+    uint32_t *coll_start, *coll_end;
 } mv_results_view;
 
 typedef struct mv_ctx mv_ctx;
@@ -196,8 +206,11 @@ typedef struct mv_run_opts {
  * descriptor).  Returns MV_OK, MV_EINVAL or MV_EOVERFLOW. */
 int mv_workspace_bytes(const mv_batch_desc *desc, uint64_t *bytes);
 
-/* Sizes of the concatenated per-node and per-record result arrays. */
-int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_records);
+/* Sizes of the concatenated per-node, per-record and per-collective result
+ * arrays (any pointer may be NULL).  Returns MV_OK or the error of
+ * mv_workspace_bytes for this descriptor. */
+int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_records,
+                    uint64_t *n_colls);
 
 /* Validate the batch, lay it out in the caller's device workspace
  * (`dev_workspace`, `ws_bytes`, 256-byte aligned), upload it on `stream`
@@ -252,14 +265,18 @@ int mv_destroy(mv_ctx *ctx);
  * `max_ticks` and `steps_done` are as for mv_run.  It calls no cudaMalloc,
  * cudaFree or other device-allocating routine.
  *
- * The array belongs to the current device's context: the first call on a
- * device looks up its device address (cudaGetSymbolAddress) and caches it,
- * so make that first call before any stream capture.  Once the library's
- * module is loaded on a device, the 32 MiB stay reserved there until the
- * process exits.  Every call reuses the same array (each call clears and
- * re-uploads what it needs), so calls whose GPU work overlaps -- two host
- * threads, or two streams of the same device -- race and must be serialised
- * by the caller.
+ * The array belongs to the current device: the first call on a device looks
+ * up its device address (cudaGetSymbolAddress, with that device current)
+ * and keeps it, so make that first call before any stream capture begins.
+ * A later call looks the address up again only if the library's device data
+ * was re-initialised since (for example after cudaDeviceReset), which it
+ * detects by a token it keeps beside the array.  Every call waits for its
+ * stream (the results are copied to host memory before it returns).  Once
+ * the library's module is loaded on a device, the 32 MiB stay reserved
+ * there until the process exits.  Every call reuses the same array (each
+ * call clears and re-uploads what it needs), so calls whose GPU work
+ * overlaps -- two host threads, or two streams of the same device -- race
+ * and must be serialised by the caller.
  *
  * Returns MV_OK / MV_INCOMPLETE as mv_run does, MV_ENOMEM when the batch
  * needs more than MV_STATIC_SCRATCH_BYTES of workspace (see

@@ -34,7 +34,7 @@ def test_workspace_bytes_and_result_sizes():
     assert n > 0 and n % 256 == 0
     d, _ = mv.make_desc(p)
     nn, nr = C.c_uint64(), C.c_uint64()
-    assert mv.library().mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)) == mv.MV_OK
+    assert mv.library().mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr), None) == mv.MV_OK
     assert nn.value == 16 * 8 and nr.value == 0
 
 
@@ -190,7 +190,7 @@ for it in range(int(sys.argv[3])):
     n, nn, nr = C.c_uint64(), C.c_uint64(), C.c_uint64()
     c1 = lib.mv_workspace_bytes(C.byref(d), C.byref(n))
     codes.add(c1)
-    codes.add(lib.mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)))
+    codes.add(lib.mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr), None))
     if check_oracle:
         try:
             O.run(p, limit=1)
@@ -248,5 +248,5 @@ def test_size_limits_and_empty_batches():
     assert mv.workspace_bytes(e) > 0
     d, _ = mv.make_desc(e)
     nn, nr = C.c_uint64(), C.c_uint64()
-    assert mv.library().mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)) == mv.MV_OK
+    assert mv.library().mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr), None) == mv.MV_OK
     assert nn.value == 0 and nr.value == 0

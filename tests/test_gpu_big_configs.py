@@ -2,12 +2,16 @@
 
 tests/golden/big_parity.json (written by tests/golden/make_big_parity.py,
 which runs only the seeded generators and the oracle) holds, for sampled
-experiments of the GPT-13B 1F1B batch (config 3), the MoE dispatch/combine
-batch (config 4) and the topology-search batch (config 5), the oracle's
-per-experiment results and SHA-256 digests of its per-node start and end
-ticks, each run to completion or to a stated tick limit.  The samples of one
-batch run here together in one launch, at full size; every result must
-agree bit for bit.
+experiments of the GPT-13B 1F1B batch (config 3: ring and tree, NC 1 and 16,
+chunks of 64 KiB and 1 MiB, and two middle points), the MoE dispatch/combine
+batch (config 4: one per fabric) and the topology-search batch (config 5:
+two fabrics), the oracle's per-experiment results and SHA-256 digests of its
+per-node start and end ticks, its per-collective first start and last end,
+and its per-message completion records sorted by (tick, sender, key), each
+run through its whole iteration (the data-parallel gradient all-reduces
+included; the file records how many of them started and ended).  The samples
+of one batch run here together in one launch, at full size; every result
+must agree bit for bit.
 """
 import collections
 import hashlib
@@ -36,12 +40,17 @@ for e in ENTRIES:
     GROUPS.setdefault((e["batch"], e["limit"]), []).append(e)
 
 
-def group_batch(name, idxs):
+def group_batch(name, ents):
+    idxs = [e["index"] for e in ents]
     if name == "config3":
-        return I.config3().subset(idxs)
-    if name == "config4":
-        return I.config4(n_exp=max(idxs) + 1).subset(idxs)
-    return I.Batch(sum((I.config5(wave=(i, i + 1)).experiments for i in idxs), []))
+        b = I.config3().subset(idxs)
+    elif name == "config4":
+        b = I.config4(n_exp=max(idxs) + 1).subset(idxs)
+    else:
+        b = I.Batch(sum((I.config5(wave=(i, i + 1)).experiments for i in idxs), []))
+    for x, e in zip(b.experiments, ents):
+        x.rec_cap = e["rec_count"]          # every message the oracle delivered
+    return b
 
 
 def sha(a):
@@ -52,7 +61,7 @@ def sha(a):
 def test_full_size_samples_match_oracle(key):
     name, limit = key
     ents = GROUPS[key]
-    p = group_batch(name, [e["index"] for e in ents]).pack()
+    p = group_batch(name, ents).pack()
     got = mv.simulate(p, max_ticks=limit if limit else mv.UNSET - 1)
     for j, e in enumerate(ents):
         for k in G.SCALARS:
@@ -60,3 +69,10 @@ def test_full_size_samples_match_oracle(key):
         a, b = got["node_offset"][j], got["node_offset"][j + 1]
         assert sha(got["node_start"][a:b]) == e["node_start_sha256"], (name, e["index"])
         assert sha(got["node_end"][a:b]) == e["node_end_sha256"], (name, e["index"])
+        a, b = got["coll_offset"][j], got["coll_offset"][j + 1]
+        assert sha(got["coll_start"][a:b]) == e["coll_start_sha256"], (name, e["index"])
+        assert sha(got["coll_end"][a:b]) == e["coll_end_sha256"], (name, e["index"])
+        a, n = got["rec_offset"][j], int(got["rec_count"][j])
+        assert G.records_digest(got["rec_sender"][a:a + n], got["rec_key"][a:a + n],
+                                got["rec_tick"][a:a + n]) == e["records_sha256"], (name, e["index"])
+

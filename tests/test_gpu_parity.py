@@ -1,5 +1,9 @@
 """CUDA path vs the CPU oracle, element by element (all results are integers,
-so the bar is bit-exact).  Every call goes through the C ABI."""
+so the bar is bit-exact): per-experiment counters, per-node start and end
+ticks, per-collective first start and last end, and, where an experiment
+keeps them, its per-message completion records (sender node, connection
+key, delivery tick), compared as sorted lists since the order in which
+records are produced is not a result.  Every call goes through the C ABI."""
 import numpy as np
 import pytest
 
@@ -17,6 +21,13 @@ KEYS = ["status", "end_tick", "now", "pkts_injected", "pkt_hops", "pkts_delivere
         "msgs_delivered", "digest", "rec_count"]
 
 
+def records(res, e, cap):
+    a = res["rec_offset"][e]
+    n = min(int(res["rec_count"][e]), cap)
+    return sorted(zip(res["rec_sender"][a:a + n].tolist(), res["rec_key"][a:a + n].tolist(),
+                      res["rec_tick"][a:a + n].tolist()))
+
+
 def assert_same(got, want, exps=None):
     E = len(want["status"])
     idx = range(E) if exps is None else exps
@@ -31,12 +42,22 @@ def assert_same(got, want, exps=None):
             g, w = got[k][a:b], want[k][a:b]
             bad = np.nonzero(g != w)[0]
             assert bad.size == 0, f"{k} exp {e} node {bad[0]}: {g[bad[0]]} != {w[bad[0]]}"
+        a, b = want["coll_offset"][e], want["coll_offset"][e + 1]
+        assert got["coll_offset"][e] == a and got["coll_offset"][e + 1] == b
+        for k in ("coll_start", "coll_end"):
+            g, w = got[k][a:b], want[k][a:b]
+            bad = np.nonzero(g != w)[0]
+            assert bad.size == 0, f"{k} exp {e} coll {bad[0]}: {g[bad[0]]} != {w[bad[0]]}"
+        cap = int(want["rec_offset"][e + 1] - want["rec_offset"][e])
+        if cap:
+            assert records(got, e, cap) == records(want, e, cap), f"records of exp {e}"
 
 
-def records(res, e, cap):
-    a = res["rec_offset"][e]
-    n = min(int(res["rec_count"][e]), cap)
-    return sorted(zip(res["rec_sender"][a:a + n], res["rec_key"][a:a + n], res["rec_tick"][a:a + n]))
+def every_record(batch, cap):
+    """Keep up to `cap` per-message records in every experiment."""
+    for x in batch.experiments:
+        x.rec_cap = cap
+    return batch
 
 
 def pin_batch():
@@ -55,6 +76,15 @@ def pin_batch():
     w.collective(I.P2P, [0, 2], 3 * 4096)
     w.collective(I.P2P, [1, 2], 3 * 4096)
     ex.append(I.Experiment(t, w, chunk=1 << 20, cap=2, tick_ps=1000, rec_cap=8))
+    # trees with internal members: depth 2 with one and with two channels
+    ex.append(I.Experiment(I.single_switch(4, 1, 0), I.single_collective(4, I.AR, 2 * 4096),
+                           algo=I.TREE, nc=1, chunk=4096, tick_ps=1000, rec_cap=64))
+    for t in (I.single_switch(7, 1, 3), I.leaf_spine(2, 2, 4, 2)):
+        ex.append(I.Experiment(t, I.single_collective(7, I.AR, 4 * 4096), algo=I.TREE, nc=2,
+                               chunk=4096, tick_ps=1000, rec_cap=64))
+    # the largest legal switch and link delay: 64 ports, delta 63
+    ex.append(I.Experiment(I.single_switch(64, 1, 63), I.single_collective(64, I.AR, 64 * 4096),
+                           nc=2, chunk=8192, cap=130, tick_ps=1000))
     # pipelined broadcast
     for A, K, npk in ((1, 3, 2), (3, 5, 3), (7, 16, 1)):
         ex.append(I.Experiment(I.single_switch(A + 1, 1, 0), I.relay_chain(A + 1, K * npk * 4096, K),
@@ -100,22 +130,22 @@ def test_pin_scenarios_bit_exact():
     assert_same(got, want)
     assert (want["status"] != O.ST_RUNNING).all()
     assert O.ST_OOM in want["status"] and O.ST_DEADLOCK in want["status"]
-    for e in range(len(want["status"])):
-        cap = int(p["exp_rec_cap"][e])
-        if cap:
-            assert records(got, e, cap) == records(want, e, cap)
 
 
 def test_config1_bit_exact():
-    p = I.config1().pack()
+    """Config 1 whole, every message's completion record included."""
+    p = every_record(I.config1(), 1 << 14).pack()
     got, want = mv.simulate(p), O.run(p)
+    assert (want["rec_count"] <= 1 << 14).all() and (want["rec_count"] > 0).all()
     assert_same(got, want)
     assert (got["status"] == mv.EXP_DONE).all()
 
 
 def test_config2_bit_exact():
-    p = I.config2().pack()
+    """Config 2 whole, every message's completion record included."""
+    p = every_record(I.config2(), 1 << 11).pack()
     got, want = mv.simulate(p), O.run(p)
+    assert (want["rec_count"] <= 1 << 11).all() and (want["rec_count"] > 0).all()
     assert_same(got, want)
     assert (got["status"] == mv.EXP_DONE).all()
 

@@ -23,7 +23,8 @@ if not torch.cuda.is_available():
 from experiment_network_simulation_gb300 import mv  # noqa: E402
 
 KEYS = ["status", "end_tick", "now", "pkts_injected", "pkt_hops", "pkts_delivered",
-        "msgs_delivered", "digest", "rec_count", "node_start", "node_end"]
+        "msgs_delivered", "digest", "rec_count", "node_start", "node_end", "coll_start",
+        "coll_end"]
 
 
 def simulate_static(packed):
@@ -33,16 +34,21 @@ def simulate_static(packed):
                   C.POINTER(C.c_uint64)]
     f.restype = C.c_int
     d, keep = mv.make_desc(packed)
-    nn, nr = C.c_uint64(), C.c_uint64()
-    assert lib.mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr)) == mv.MV_OK
+    nn, nr, nco = C.c_uint64(), C.c_uint64(), C.c_uint64()
+    assert lib.mv_result_sizes(C.byref(d), C.byref(nn), C.byref(nr), C.byref(nco)) == mv.MV_OK
     E = int(d.n_exps)
     res = {}
     view = mv.ResultsView()
     for name, t in mv._RES:
-        n = E if name in ("status", "end_tick", "now", "pkts_injected", "pkt_hops",
-                          "pkts_delivered", "msgs_delivered", "digest", "rec_count") else \
-            max(1, int(nn.value) if name.startswith("node_") else int(nr.value))
-        res[name] = np.zeros(n, mv._NP[t])
+        if name.startswith("node_"):
+            n = int(nn.value)
+        elif name.startswith("rec_") and name != "rec_count":
+            n = int(nr.value)
+        elif name.startswith("coll_"):
+            n = int(nco.value)
+        else:
+            n = E
+        res[name] = np.zeros(max(1, n), mv._NP[t])
         setattr(view, name, res[name].ctypes.data_as(mv._CT[t]))
     steps = C.c_uint64()
     stream = torch.cuda.current_stream().cuda_stream
@@ -62,6 +68,23 @@ def test_static_matches_regular_two_calls_in_a_row():
             rc, got = simulate_static(packed)
             assert rc == mv.MV_OK
             same(got, want)
+
+
+def test_static_takes_no_device_memory():
+    """Its one promise: after a first call (which loads the library's module
+    and with it the array), further calls leave the device's free memory
+    unchanged."""
+    packed = I.config2(n_exp=32, seed=9).pack()
+    rc, _ = simulate_static(packed)
+    assert rc == mv.MV_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        rc, _ = simulate_static(packed)
+        assert rc == mv.MV_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
 
 
 def test_static_rejects_batches_beyond_its_scratch():
