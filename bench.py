@@ -2,22 +2,37 @@
 """Throughput of the SPME packet simulator on GB300.
 
 Metric: simulated packet-hops per second over a batch of experiments (a
-packet-hop is one packet placed on one link), plus experiments per hour and
-the megakernel's achieved HBM bandwidth against the measured peak.
+packet-hop is one packet placed on one link), plus the megakernel's achieved
+bandwidth (algorithmic bytes over its device time) against the measured HBM
+peak.
 
-One step = the whole path over the batch: mv_reset (back to tick 0,
-routing tables, memory check) + mv_run to completion, inputs resident in HBM.
-Steps are timed with CUDA events on the simulator's stream; L2 is flushed
-(a 512 MiB write) between steps.  ``e2e`` repeats the step through the
-public API from host buffers: mv_create (upload), mv_run, mv_results
-(download), timed by wall clock.
+Default workload: config 3 (the GPT-13B 1F1B iteration on the k=16
+fat-tree, 500 experiments over {ring, tree} x NC x chunk x duration seed), a
+window of its data-parallel gradient all-reduce phase.  Every experiment is
+first run untimed to the window's start tick (once; the simulator's whole
+state is its workspace, so later steps restore that state with one device
+copy).  One step = the whole path over the batch for the window's ticks: one
+megakernel launch that advances all 500 experiments from the start tick to
+start + ticks of their own clocks, inputs resident in HBM.  Steps are timed
+with CUDA events on the simulator's stream; L2 is flushed (a 512 MiB write)
+before each step.
 
---impl reference times the CPU oracle (the plain C simulator, as it stands)
-on the host cores over a bounded sample of the same workload.
+``e2e`` repeats the step from host memory through the public API: the start
+state (the workspace) is copied from pinned host memory to the device, the
+window is run (mv_run) and the per-experiment counters are read back
+(mv_results), timed by wall clock.  Whole-run workloads (configs 1 and 2)
+instead time mv_reset + mv_run to completion, and their e2e creates the
+simulator from the host arrays (mv_create), runs it and reads all results.
+
+--impl reference, and the cpu_baseline leg, time the CPU oracle (the plain C
+simulator, as it stands) on the host cores over a bounded sample of the
+same workload: for a window, each worker runs one experiment to the start
+tick untimed, then times the window from a copy of that state.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import multiprocessing as mp
 import os
@@ -40,9 +55,6 @@ UNIT = "packet-hops/s"
 # downstream queue and reads it back out (32 B); each packet also costs a
 # sender flow-state read-modify-write (16 B) and a receiver update (8 B).
 BYTES_PER_HOP, BYTES_PER_PKT = 32, 24
-# DRAM bytes (read + write) of one megakernel launch of the whole-run
-# workload, from an ncu capture of the current kernel (see profiles/).
-TRAFFIC = {"config2": 6724608}
 
 WORKLOADS = {
     "config1": (lambda seed: I.config1(),
@@ -57,8 +69,30 @@ WORKLOADS = {
                 "1,024 experiments"),
     "config5": (lambda seed: I.config5(n_exp=24),
                 "topology search, GPT-13B at DP128 on 1,024-server 3-tier fabrics (24 of them)"),
+    "gpt_small": (lambda seed: I.gpt_small(seeds=tuple(range(8))),
+                  "the config-3 DAG shape at test size (8 servers x 2 GPUs, k=4 fat-tree), "
+                  "8 experiments"),
 }
-DEFAULT = "config2"
+DEFAULT = "config3"
+# Default window (start tick, ticks) per workload; None = whole runs.  Config
+# 3's window lies in the data-parallel all-reduce phase of its experiments
+# (their iterations end between about 3.4 M and 3.9 M ticks).
+WINDOWS = {"config3": (3_000_000, 4_000), "config5": (300_000, 2_000), "gpt_small": (3_000, 2_000)}
+
+# DRAM bytes (read + write) per megakernel launch from ncu captures of the
+# current kernel, keyed by workload and window; each entry names the kernel
+# source digest it was taken with, and is dropped (traffic: null) once the
+# kernel source differs.
+TRAFFIC: dict = {}
+KERNEL_SOURCES = ["experiment_network_simulation_gb300/csrc/mv_kernel.cu",
+                  "experiment_network_simulation_gb300/csrc/mv_device.cuh"]
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def make_batch(name: str, seed: int = 0, exps: int = 0):
@@ -66,45 +100,113 @@ def make_batch(name: str, seed: int = 0, exps: int = 0):
     return b.subset(range(min(exps, len(b)))) if exps else b
 
 
+def window_of(args):
+    """(start tick, ticks) of the timed window, or None for whole runs."""
+    if args.whole:
+        return None
+    if args.start_tick is not None or args.max_ticks is not None:
+        d = WINDOWS.get(args.workload, (0, 0))
+        s = d[0] if args.start_tick is None else args.start_tick
+        n = d[1] if args.max_ticks is None else args.max_ticks
+        return (s, n) if n > 0 else None
+    return WINDOWS.get(args.workload)
+
+
 # ----------------------------------------------------------------- oracle pool
-_W = {}
-
-
-def _worker_init(name: str, seed: int, exps: int, limit: int):
+def _oracle_worker(conn, name: str, seed: int, exps: int):
+    """One host core: builds the batch, then serves commands.  A window's
+    start state stays in this process, so its windows always run here."""
     sys.path.insert(0, ROOT)
     from oracle import oracle
 
     oracle.build()
-    _W["packed"] = make_batch(name, seed, exps).pack()
-    _W["oracle"] = oracle
-    _W["limit"] = limit
+    packed = make_batch(name, seed, exps).pack()
+    paused = {}
+    conn.send("ready")
+    while True:
+        cmd = conn.recv()
+        if cmd[0] == "quit":
+            break
+        if cmd[0] == "whole":                 # one whole experiment
+            e = cmd[1]
+            t0 = time.perf_counter()
+            r = oracle.run(packed, e, e + 1)
+            conn.send((int(r["pkt_hops"][e]), time.perf_counter() - t0))
+        elif cmd[0] == "prefix":              # untimed: to the window's start tick
+            e, start = cmd[1], cmd[2]
+            p = oracle.Paused(packed, e)
+            p.advance(start)
+            paused[e] = p
+            conn.send(e)
+        elif cmd[0] == "window":              # the window from a copy of the start state
+            e, start, ticks = cmd[1], cmd[2], cmd[3]
+            c = paused[e].clone()
+            h0 = c.counters()["pkt_hops"]
+            t0 = time.perf_counter()
+            c.advance(start + ticks)
+            dt = time.perf_counter() - t0
+            h = c.counters()["pkt_hops"] - h0
+            c.close()
+            conn.send((int(h), dt))
 
 
-def _worker_run(e: int):
-    r = _W["oracle"].run(_W["packed"], e, e + 1, _W["limit"])
-    return int(r["pkt_hops"][e])
+class OraclePool:
+    """The oracle on every host core: a process per core, one experiment per
+    command.  For a window, each process holds the start state of one
+    sampled experiment (computed untimed) and times the window from a copy."""
 
+    def __init__(self, name: str, seed: int, exps: int, window, cores: int):
+        from oracle import oracle
 
-def oracle_sample(name: str, seed: int, budget_s: float, cores: int, exps: int = 0,
-                  limit: int = 0xFFFFFFFE):
-    """Time the oracle over a seeded sample of experiments, all host cores in
-    parallel (one experiment per task, each to completion or to `limit`
-    ticks), until about budget_s of wall clock."""
-    from oracle import oracle
+        oracle.build()
+        self.n_exp = len(make_batch(name, seed, exps))
+        self.order = [int(x) for x in np.random.default_rng(1234).permutation(self.n_exp)]
+        self.window = window
+        ctx = mp.get_context("spawn")
+        self.workers = []
+        for _ in range(min(cores, self.n_exp)):
+            a, b = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(b, name, seed, exps), daemon=True)
+            pr.start()
+            self.workers.append((pr, a))
+        for _, conn in self.workers:
+            assert conn.recv() == "ready"
+        self.sample = []
+        if window:
+            self.sample = self.order[:len(self.workers)]
+            self._all([("prefix", e, window[0]) for e in self.sample])
 
-    oracle.build()
-    n_exp = len(make_batch(name, seed, exps))
-    order = np.random.default_rng(1234).permutation(n_exp)
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(cores, initializer=_worker_init, initargs=(name, seed, exps, limit)) as pool:
-        pool.map(_worker_run, [int(order[0])] * cores)          # warm the workers
+    def _all(self, cmds):
+        for (_, conn), cmd in zip(self.workers, cmds):
+            conn.send(cmd)
+        return [conn.recv() for (_, conn), _ in zip(self.workers, cmds)]
+
+    def window_step(self):
+        """Every sampled experiment's window once, in parallel: (hops, wall seconds)."""
+        t0 = time.perf_counter()
+        res = self._all([("window", e, self.window[0], self.window[1]) for e in self.sample])
+        return sum(h for h, _ in res), time.perf_counter() - t0
+
+    def whole_runs(self, budget_s: float):
+        """Whole experiments in a seeded order, one per process at a time,
+        until about budget_s of wall clock: (hops, wall seconds, done)."""
         hops, done, t0 = 0, 0, time.perf_counter()
-        while done < n_exp and time.perf_counter() - t0 < budget_s:
-            chunk = [int(e) for e in order[done:done + cores]]
-            hops += sum(pool.map(_worker_run, chunk))
+        while done < self.n_exp and time.perf_counter() - t0 < budget_s:
+            chunk = self.order[done:done + len(self.workers)]
+            hops += sum(h for h, _ in self._all([("whole", e) for e in chunk]))
             done += len(chunk)
-        dt = time.perf_counter() - t0
-    return hops, dt, done, n_exp
+        return hops, time.perf_counter() - t0, done
+
+    def close(self):
+        for pr, conn in self.workers:
+            try:
+                conn.send(("quit",))
+            except (BrokenPipeError, OSError):
+                pass
+        for pr, _ in self.workers:
+            pr.join(timeout=5)
+            if pr.is_alive():
+                pr.terminate()
 
 
 # ----------------------------------------------------------------- clocks
@@ -166,34 +268,80 @@ def load_peaks():
         return None
 
 
+def config_of(args, window, n_exp):
+    cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload][1],
+           "experiments": n_exp}
+    if window:
+        cfg["window"] = {"start_tick": window[0], "ticks": window[1],
+                         "note": "each step advances every experiment from start_tick to "
+                                 "start_tick + ticks of its own clock; the run to start_tick "
+                                 "is done once, untimed, and its state restored before each step"}
+    return cfg
+
+
 # ----------------------------------------------------------------- arms
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
     cores = os.cpu_count() or 1
-    name = args.workload
-    per_step = max(1.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
-    lim = args.start_tick + args.max_ticks if (args.start_tick or args.max_ticks) else 0xFFFFFFFE
-    for _ in range(args.warmup):
-        oracle_sample(name, 0, min(per_step, 5.0), cores, args.exps, lim)
-    hops, secs, n_done = 0, 0.0, 0
-    for _ in range(args.steps):
-        h, dt, done, n_exp = oracle_sample(name, 0, per_step, cores, args.exps, lim)
-        hops += h
-        secs += dt
-        n_done += done
+    window = window_of(args)
+    pool = OraclePool(args.workload, 0, args.exps, window, cores)
+    try:
+        if window:
+            for _ in range(args.warmup):
+                pool.window_step()
+            hops, secs = 0, 0.0
+            for _ in range(args.steps):
+                h, dt = pool.window_step()
+                hops += h
+                secs += dt
+            sample = (f"{len(pool.sample)} of {pool.n_exp} experiments (seeded permutation), "
+                      f"ticks [{window[0]}, {window[0] + window[1]}) of each, one experiment per "
+                      f"process, each window from a copy of its start state")
+        else:
+            per_step = max(1.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
+            for _ in range(args.warmup):
+                pool.whole_runs(min(per_step, 5.0))
+            pool.order = pool.order[len(pool.workers):] + pool.order[:len(pool.workers)]
+            hops, secs, n_done = 0, 0.0, 0
+            for _ in range(args.steps):
+                h, dt, done = pool.whole_runs(per_step)
+                hops += h
+                secs += dt
+                n_done += done
+            sample = (f"{n_done // max(1, args.steps)} of {pool.n_exp} experiments per step "
+                      f"(seeded permutation), whole runs, one experiment per process")
+    finally:
+        pool.close()
     value = hops / secs
-    sample = (f"{n_done // max(1, args.steps)} of {n_exp} experiments per step "
-              f"(seeded permutation), one experiment per process")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
-        "data": "synthetic", "config": {"workload": name, "desc": WORKLOADS[name][1]},
+        "data": "synthetic", "config": config_of(args, window, pool.n_exp),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def cpu_leg(args, window):
+    """cpu_baseline of the GPU arm: the oracle on the same workload."""
+    cores = os.cpu_count() or 1
+    pool = OraclePool(args.workload, 0, args.exps, window, cores)
+    try:
+        if window:
+            h, dt = pool.window_step()
+            sample = (f"{len(pool.sample)} of {pool.n_exp} experiments (seeded permutation), "
+                      f"ticks [{window[0]}, {window[0] + window[1]}) of each from its start "
+                      f"state, {dt:.1f} s wall, one experiment per process")
+        else:
+            h, dt, done = pool.whole_runs(args.cpu_budget_s)
+            sample = (f"{done} of {pool.n_exp} experiments (seeded permutation), whole runs, "
+                      f"{dt:.1f} s wall, one experiment per process")
+    finally:
+        pool.close()
+    return {"value": h / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
 
 def run_gpu(args, rank: int, world: int):
@@ -203,30 +351,31 @@ def run_gpu(args, rank: int, world: int):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
+    window = window_of(args)
     batch = make_batch(args.workload, seed=rank, exps=args.exps)   # each rank: its own shard
     packed = batch.pack()
     stream = torch.cuda.Stream(dev)
     sim = mv.Simulator(packed, device=str(dev), stream=stream)
     n_levels = int(packed["sw_level"].max())
-    launches_per_step = n_levels + 4                  # routes per level, up lists, 2 init, megakernel
+    # our kernels a step launches: the megakernel; whole runs also reset
+    # (routes per level, up lists, 2 init)
+    launches_per_step = 1 if window else n_levels + 4
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    window = args.start_tick > 0 or args.max_ticks > 0
-    budget = args.max_ticks if args.max_ticks > 0 else mv.UNSET - 1
+    budget = window[1] if window else mv.UNSET - 1
 
     snap = {}
+    if window:
+        # untimed: every experiment to the window's start tick, once
+        sim.reset()
+        rc = sim.run(max_ticks=window[0])
+        assert rc in (mv.MV_OK, mv.MV_INCOMPLETE), rc
+        c = sim.counters()
+        snap["ws"] = sim.ws.clone()
+        snap["h"] = (int(c["pkt_hops"].sum()), int(c["pkts_injected"].sum()))
+        snap["running"] = int((c["status"] == mv.EXP_RUNNING).sum())
 
     def prefix():
-        """Untimed: back to tick 0 and, for a window, on to its start tick.
-        The simulator's whole state is its workspace, so the window's start
-        state is computed once and then restored by a device copy."""
-        if args.start_tick:
-            if not snap:
-                sim.reset()
-                rc = sim.run(max_ticks=args.start_tick)
-                assert rc in (mv.MV_OK, mv.MV_INCOMPLETE), rc
-                c = sim.counters()
-                snap["ws"] = sim.ws.clone()
-                snap["h"] = (int(c["pkt_hops"].sum()), int(c["pkts_injected"].sum()))
+        if window:
             with torch.cuda.stream(stream):
                 sim.ws.copy_(snap["ws"])
         with torch.cuda.stream(stream):
@@ -234,8 +383,7 @@ def run_gpu(args, rank: int, world: int):
         return snap.get("h", (0, 0))
 
     def timed():
-        """The timed region: reset (unless a window) + one megakernel run."""
-        if not args.start_tick:
+        if not window:
             sim.reset()
         rc = sim.run(max_ticks=budget)
         assert rc in ((mv.MV_OK, mv.MV_INCOMPLETE) if window else (mv.MV_OK,)), rc
@@ -256,8 +404,7 @@ def run_gpu(args, rank: int, world: int):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.steps):
         h0, p0 = prefix()
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
+        ev0.record(stream)
         timed()
         ev1.record(stream)
         ev1.synchronize()
@@ -290,23 +437,38 @@ def run_gpu(args, rank: int, world: int):
         ms_max, hops_all, exps_all = ms_step, float(hops_step), float(len(batch))
     value = hops_all / (ms_max / 1000.0)
 
-    # e2e through the public API from host buffers: create (upload), run,
-    # results (download); whole runs only
+    # e2e through the public API from host memory
     e2e = None
-    if not window and args.e2e_steps > 0:
-        h2d = sum(int(np.asarray(v).nbytes) for k, v in packed.items() if k != "version")
-        e2e_s, d2h = [], 0
-        for _ in range(args.e2e_steps):
-            torch.cuda.synchronize(dev)
-            t0 = time.perf_counter()
-            s2 = mv.Simulator(packed, device=str(dev), stream=stream)
-            s2.run()
-            r2 = s2.results()
-            s2.close()
-            e2e_s.append(time.perf_counter() - t0)
-            d2h = sum(int(v.nbytes) for k, v in r2.items() if isinstance(v, np.ndarray)
-                      and k not in ("node_offset", "rec_offset"))
-            del s2
+    if args.e2e_steps > 0:
+        e2e_s, h2d, d2h = [], 0, 0
+        if window:
+            host = torch.empty(snap["ws"].numel(), dtype=torch.uint8, pin_memory=True)
+            host.copy_(snap["ws"])
+            del snap["ws"]
+            for _ in range(args.e2e_steps):
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                with torch.cuda.stream(stream):
+                    sim.ws.copy_(host, non_blocking=True)     # the start state, host -> device
+                sim.run(max_ticks=budget)
+                c = sim.counters()                            # per-experiment results, device -> host
+                e2e_s.append(time.perf_counter() - t0)
+            h2d = int(host.numel())
+            d2h = sum(int(v.nbytes) for v in c.values())
+            del host
+        else:
+            h2d = sum(int(np.asarray(v).nbytes) for k, v in packed.items() if k != "version")
+            for _ in range(args.e2e_steps):
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                s2 = mv.Simulator(packed, device=str(dev), stream=stream)
+                s2.run()
+                r2 = s2.results()
+                s2.close()
+                e2e_s.append(time.perf_counter() - t0)
+                d2h = sum(int(v.nbytes) for k, v in r2.items() if isinstance(v, np.ndarray)
+                          and not k.endswith("_offset"))
+                del s2
         e2e = {"value": hops_step / statistics.mean(e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -315,32 +477,25 @@ def run_gpu(args, rank: int, world: int):
     alg_bytes = BYTES_PER_HOP * hops_step + BYTES_PER_PKT * pkts_step
     achieved = alg_bytes / (km / 1000.0) / 1e9
     peak = peaks["hbm_gbs"] if peaks else 6800.0
+    key = (args.workload, tuple(window) if window else None, len(batch))
+    tr = TRAFFIC.get(key)
+    traffic = tr["bytes_per_launch"] if tr and tr["kernel_digest"] == kernel_digest() else None
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": TRAFFIC.get(args.workload) if not window else None,
+            "frac": achieved / peak, "traffic": traffic,
             "peak_source": "measured" if peaks else "fallback",
-            "kernel": "k_megakernel", "kernel_ms": km,
-            "alg_bytes_per_launch": alg_bytes}
+            "kernel": "k_megakernel", "kernel_ms": km, "alg_bytes_per_launch": alg_bytes}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cores = os.cpu_count() or 1
-        lim = args.start_tick + args.max_ticks if window else 0xFFFFFFFE
-        h, dt, done, n_exp = oracle_sample(args.workload, 0, args.cpu_budget_s, cores,
-                                           args.exps, lim)
-        what = f"first {lim} ticks of " if window else ""
-        cpu = {"value": h / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{what}{done} of {n_exp} experiments (seeded permutation), "
-                         f"{dt:.1f} s wall, one experiment per process"}
+        cpu = cpu_leg(args, window)
 
     if rank == 0:
-        cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload][1],
-               "experiments": int(exps_all), "packet_hops_per_step": int(hops_all),
-               "l2": "flushed between steps (512 MiB write)",
-               "grid_steps_per_run": int(statistics.mean(steps_grid))}
+        cfg = config_of(args, window, int(exps_all))
+        cfg.update({"packet_hops_per_step": int(hops_all),
+                    "l2": "flushed between steps (512 MiB write)",
+                    "grid_steps_per_run": int(statistics.mean(steps_grid))})
         if window:
-            cfg["window"] = {"start_tick": args.start_tick, "max_ticks": args.max_ticks,
-                             "note": "each step times ticks [start, start + max) of every "
-                                     "experiment's clock; the prefix runs untimed"}
+            cfg["window"]["running_at_start"] = snap["running"]
         out = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -360,7 +515,7 @@ def run_gpu(args, rank: int, world: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
@@ -368,10 +523,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--exps", type=int, default=0, help="first N experiments of the batch")
-    ap.add_argument("--start-tick", type=int, default=0,
-                    help="run every experiment to this tick before the timed region")
-    ap.add_argument("--max-ticks", type=int, default=0,
-                    help="timed run budget in ticks of each experiment's clock (0 = to the end)")
+    ap.add_argument("--start-tick", type=int, default=None,
+                    help="window start (default: the workload's window)")
+    ap.add_argument("--max-ticks", type=int, default=None,
+                    help="window length in ticks of each experiment's clock (0: whole runs)")
+    ap.add_argument("--whole", action="store_true", help="time whole runs, no window")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

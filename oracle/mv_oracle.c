@@ -213,6 +213,9 @@ typedef struct sim {
     uint64_t trace_cap, trace_n;
     uint32_t now;                   /* the tick being simulated */
     int no_skip;                    /* step every tick instead of jumping to the next event */
+    uint32_t t_next;                /* the next tick to simulate (a paused run resumes here) */
+    uint64_t active;                /* ticks simulated so far */
+    int is_clone;                   /* shares the read-only tables of the sim it was copied from */
 } sim;
 
 static void ev(sim *s, uint32_t kind, uint32_t a, uint32_t b)
@@ -899,15 +902,24 @@ static uint32_t next_event(sim *s, uint32_t t)
     return best;
 }
 
-static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *now_out)
+/* Tick 0: the DAG's roots are scheduled to start. */
+static void sim_begin(sim *s)
 {
-    uint32_t t = 0;
-    uint64_t active = 0;
-    if (limit > TICK_LIMIT) limit = TICK_LIMIT;
     s->cur_rank = -1;
     for (uint32_t r = 0; r < s->R; r++)
         for (uint32_t u = s->rank_base[r]; u < s->rank_base[r + 1]; u++)
             if (s->node_npred[u] == 0) pend_add(s, r, u, 0);
+    s->t_next = 0;
+}
+
+/* Step from s->t_next until the experiment stops or its clock reaches
+ * `limit` (exclusive); a later call with a larger limit carries on exactly
+ * as one longer call would. */
+static void sim_advance(sim *s, uint32_t limit)
+{
+    uint32_t t = s->t_next;
+    if (limit > TICK_LIMIT) limit = TICK_LIMIT;
+    s->cur_rank = -1;
     while (s->status == ST_RUNNING) {
         if (s->nodes_left == 0) { s->status = ST_DONE; break; }
         if (t >= limit) break;
@@ -924,7 +936,7 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
             if (!s->nics[r].tick_fail) inject(s, r, t);
         for (uint32_t r = 0; r < s->R; r++)
             if (!s->nics[r].tick_fail) receive(s, r, t);
-        active++;
+        s->active++;
         if (s->status != ST_RUNNING) break;
         if (s->nodes_left == 0) { s->status = ST_DONE; t++; break; }
         if (s->changed) { t++; continue; }
@@ -932,8 +944,7 @@ static void simulate(sim *s, uint32_t limit, uint64_t *ticks_active, uint32_t *n
         if (nx == UNSET) { s->status = ST_DEADLOCK; t++; break; }
         t = s->no_skip ? t + 1 : nx;
     }
-    *ticks_active = active;
-    *now_out = t;
+    s->t_next = t;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -1063,18 +1074,12 @@ static int validate(const orc_batch *b, const offs *o)
     return 0;
 }
 
-static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit,
-                   orc_out *out, uint64_t node_off, uint64_t rec_off, uint64_t coll_off,
-                   orc_event *trace,
-                   uint64_t trace_cap, uint64_t *trace_n, uint32_t flags)
+/* Tables and tick-0 state of experiment e (nothing simulated yet). */
+static void sim_setup(sim *s, const orc_batch *b, const offs *o, uint32_t e)
 {
-    sim S_, *s = &S_;
     memset(s, 0, sizeof *s);
     s->b = b;
     s->e = e;
-    s->trace = trace;
-    s->trace_cap = trace_cap;
-    s->no_skip = (flags & ORC_NO_SKIP) != 0;
     uint32_t ti = b->exp_topo[e], wi = b->exp_work[e];
     s->H = b->topo_nhosts[ti];
     s->S = b->topo_nsw[ti];
@@ -1179,15 +1184,43 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
         s->end[u] = UNSET;
     }
     s->nodes_left = s->NN;
+    s->status = ST_RUNNING;
+    if (!memory_fits(s->mem, s->gpu_mem)) s->status = ST_OOM;
+    else sim_begin(s);
+}
+
+/* Free what a sim owns: its dynamic state, and its tables unless it is a
+ * clone that shares them. */
+static void sim_teardown(sim *s)
+{
+    if (!s->is_clone) {
+        free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
+        free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
+        free(s->col_base); free(s->node_rank); free(s->node_member); free(s->credit_delay);
+    }
+    free(s->head); free(s->tail); free(s->tail0); free(s->slots);
+    free(s->poplog); free(s->last_push);
+    free(s->eg_busy); free(s->eg_rr); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
+    free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
+}
+
+static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit,
+                   orc_out *out, uint64_t node_off, uint64_t rec_off, uint64_t coll_off,
+                   orc_event *trace,
+                   uint64_t trace_cap, uint64_t *trace_n, uint32_t flags)
+{
+    sim S_, *s = &S_;
+    sim_setup(s, b, o, e);
+    uint32_t nco = b->work_ncolls[b->exp_work[e]];
+    s->trace = trace;
+    s->trace_cap = trace_cap;
+    s->no_skip = (flags & ORC_NO_SKIP) != 0;
     s->rec_sender = out->rec_sender + rec_off;
     s->rec_key = out->rec_key + rec_off;
     s->rec_tick = out->rec_tick + rec_off;
-    s->status = ST_RUNNING;
-
-    uint64_t active = 0;
-    uint32_t now = 0;
-    if (!memory_fits(s->mem, s->gpu_mem)) s->status = ST_OOM;
-    else simulate(s, limit, &active, &now);
+    if (s->status == ST_RUNNING) sim_advance(s, limit);
+    uint64_t active = s->active;
+    uint32_t now = s->t_next;
 
     uint32_t endt = 0;
     int any = 0;
@@ -1228,14 +1261,7 @@ static int run_one(const orc_batch *b, const offs *o, uint32_t e, uint32_t limit
         }
     }
     if (trace_n) *trace_n = s->trace_n;
-
-    free(s->sw_base); free(s->port_sw); free(s->route); free(s->up_base); free(s->up_port);
-    free(s->rank_base); free(s->succ_base); free(s->member_base); free(s->row_base);
-    free(s->col_base); free(s->node_rank); free(s->node_member);
-    free(s->head); free(s->tail); free(s->tail0); free(s->slots);
-    free(s->poplog); free(s->credit_delay); free(s->last_push);
-    free(s->eg_busy); free(s->eg_rr); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
-    free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
+    sim_teardown(s);
     return 0;
 }
 
@@ -1286,3 +1312,101 @@ int orc_run(const orc_batch *b, uint32_t e0, uint32_t e1, uint32_t limit, orc_ou
 
 /* exported for the tests that pin the hash against its published values */
 uint64_t orc_mix64(uint64_t z) { return mix64(z); }
+
+/* ------------------------------------------------------------------------ */
+/* A paused run of one experiment, so that a window of ticks can be timed on
+ * its own: create (tick 0), advance to a tick, copy the state, advance the
+ * copy.  This is plumbing around the same simulation steps; it keeps no
+ * per-message records and no trace.  The batch arrays must outlive it. */
+typedef struct orc_handle {
+    sim s;
+} orc_handle;
+
+void *orc_sim_new(const orc_batch *b, uint32_t e)
+{
+    if (e >= b->n_exps) return NULL;
+    offs o;
+    o.host = prefix(b->topo_nhosts, b->n_topos);
+    o.sw = prefix(b->topo_nsw, b->n_topos);
+    o.port = prefix(b->topo_nports, b->n_topos);
+    o.rank = prefix(b->work_nranks, b->n_works);
+    o.node = prefix(b->work_nnodes, b->n_works);
+    o.edge = prefix(b->work_nedges, b->n_works);
+    o.coll = prefix(b->work_ncolls, b->n_works);
+    o.memb = prefix(b->work_nmembers, b->n_works);
+    o.a2a = prefix(b->work_na2a, b->n_works);
+    o.a2a_in = prefix(b->work_na2a_in, b->n_works);
+    orc_handle *h = NULL;
+    if (validate(b, &o) == 0) {
+        h = calloc(1, sizeof *h);
+        sim_setup(&h->s, b, &o, e);
+        h->s.rec_cap = 0;
+    }
+    free(o.host); free(o.sw); free(o.port); free(o.rank); free(o.node); free(o.edge);
+    free(o.coll); free(o.memb); free(o.a2a); free(o.a2a_in);
+    return h;
+}
+
+/* Advance to `limit` (exclusive); returns the experiment's status. */
+int orc_sim_advance(void *hp, uint32_t limit)
+{
+    orc_handle *h = hp;
+    if (h->s.status == ST_RUNNING) sim_advance(&h->s, limit);
+    return h->s.status;
+}
+
+/* status, clock (the next tick the run would simulate), packets injected,
+ * packet-hops, packets delivered, messages delivered */
+void orc_sim_counters(void *hp, uint64_t *out)
+{
+    sim *s = &((orc_handle *)hp)->s;
+    out[0] = (uint64_t)s->status;
+    out[1] = s->t_next;
+    out[2] = s->pkts_injected;
+    out[3] = s->pkt_hops;
+    out[4] = s->pkts_delivered;
+    out[5] = s->msgs_delivered;
+}
+
+static void *dup_bytes(const void *src, size_t n)
+{
+    void *d = malloc(n ? n : 1);
+    if (n) memcpy(d, src, n);
+    return d;
+}
+
+/* A copy of the dynamic state; the read-only tables are shared with the
+ * original, which must outlive the copy. */
+void *orc_sim_clone(void *hp)
+{
+    const sim *a = &((orc_handle *)hp)->s;
+    orc_handle *h = calloc(1, sizeof *h);
+    sim *s = &h->s;
+    *s = *a;
+    s->is_clone = 1;
+    s->head = dup_bytes(a->head, sizeof(uint32_t) * a->nf);
+    s->tail = dup_bytes(a->tail, sizeof(uint32_t) * a->nf);
+    s->tail0 = dup_bytes(a->tail0, sizeof(uint32_t) * a->nf);
+    s->poplog = dup_bytes(a->poplog, sizeof(uint32_t) * (size_t)a->nf * 64);
+    s->slots = dup_bytes(a->slots, sizeof(pkt) * (size_t)a->nf * a->cap);
+    s->last_push = dup_bytes(a->last_push, sizeof(uint32_t) * a->nf);
+    s->eg_busy = dup_bytes(a->eg_busy, sizeof(uint32_t) * (a->Q + 1));
+    s->eg_rr = dup_bytes(a->eg_rr, sizeof(uint32_t) * (a->Q + 1));
+    s->sw_queued = dup_bytes(a->sw_queued, sizeof(uint32_t) * (a->S + 1));
+    s->nics = dup_bytes(a->nics, sizeof(nic) * (a->R + 1));
+    s->npred_left = dup_bytes(a->npred_left, sizeof(uint32_t) * (a->NN + 1));
+    s->cand = dup_bytes(a->cand, sizeof(uint32_t) * (a->NN + 1));
+    s->start = dup_bytes(a->start, sizeof(uint32_t) * (a->NN + 1));
+    s->end = dup_bytes(a->end, sizeof(uint32_t) * (a->NN + 1));
+    s->port_base = dup_bytes(a->port_base, sizeof(uint32_t) * (a->NN + 1));
+    s->done_max = dup_bytes(a->done_max, sizeof(uint32_t) * (a->NN + 1));
+    s->outstanding = dup_bytes(a->outstanding, sizeof(int64_t) * (a->NN + 1));
+    return h;
+}
+
+void orc_sim_free(void *hp)
+{
+    if (!hp) return;
+    sim_teardown(&((orc_handle *)hp)->s);
+    free(hp);
+}

@@ -99,12 +99,80 @@ def _load(path: str | None = None):
             lib.orc_run_ex.restype = C.c_int
             lib.orc_mix64.argtypes = [C.c_uint64]
             lib.orc_mix64.restype = C.c_uint64
+            lib.orc_sim_new.argtypes = [C.POINTER(_Batch), C.c_uint32]
+            lib.orc_sim_new.restype = C.c_void_p
+            lib.orc_sim_advance.argtypes = [C.c_void_p, C.c_uint32]
+            lib.orc_sim_advance.restype = C.c_int
+            lib.orc_sim_counters.argtypes = [C.c_void_p, _P64]
+            lib.orc_sim_clone.argtypes = [C.c_void_p]
+            lib.orc_sim_clone.restype = C.c_void_p
+            lib.orc_sim_free.argtypes = [C.c_void_p]
             _libs[key] = lib
     return _libs[key]
 
 
 def mix64(z: int) -> int:
     return int(_load().orc_mix64(C.c_uint64(z & (2 ** 64 - 1))))
+
+
+def _batch(packed: dict):
+    keep = {}
+    b = _Batch()
+    b.version = packed["version"]
+    b.n_topos = len(packed["topo_nhosts"])
+    b.n_works = len(packed["work_nranks"])
+    b.n_exps = len(packed["exp_topo"])
+    for n, t in _ARR:
+        a = np.ascontiguousarray(packed[n], dtype=_NP[t])
+        if a.size == 0:
+            a = np.zeros(1, _NP[t])
+        keep[n] = a
+        setattr(b, n, a.ctypes.data_as(_CT[t]))
+    return b, keep
+
+
+class Paused:
+    """One experiment of a packed batch, stepped in pieces: ``advance(limit)``
+    simulates up to tick ``limit`` (exclusive) and can be called again with
+    a larger limit; ``clone()`` copies the state, so a window of ticks can be
+    timed from the same start more than once.  No per-message records."""
+
+    def __init__(self, packed: dict, e: int, lib_path: str | None = None, _h=None, _keep=None):
+        self.lib = _load(lib_path)
+        if _h is None:
+            self.b, self.keep = _batch(packed)
+            _h = self.lib.orc_sim_new(C.byref(self.b), e)
+            if not _h:
+                raise RuntimeError("oracle rejected the batch")
+        else:
+            self.b, self.keep = _keep
+        self.h = _h
+
+    def advance(self, limit: int) -> int:
+        return int(self.lib.orc_sim_advance(self.h, limit))
+
+    def counters(self) -> dict:
+        out = np.zeros(6, np.uint64)
+        self.lib.orc_sim_counters(self.h, out.ctypes.data_as(_P64))
+        return dict(zip(("status", "clock", "pkts_injected", "pkt_hops", "pkts_delivered",
+                         "msgs_delivered"), (int(x) for x in out)))
+
+    def clone(self) -> "Paused":
+        c = Paused(None, 0, _h=self.lib.orc_sim_clone(self.h), _keep=(self.b, self.keep))
+        c.lib = self.lib
+        c.parent = self                       # the tables are shared with this one
+        return c
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.orc_sim_free(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,

@@ -18,7 +18,7 @@ def _bench(*args):
 
 
 def test_reference_arm_prints_one_json_line():
-    p = _bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    p = _bench("--impl", "reference", "--workload", "config2", "--steps", "1", "--warmup", "3")
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [l for l in p.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -38,6 +38,27 @@ def test_reference_arm_prints_one_json_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
+def test_reference_arm_times_a_window():
+    """A window workload: every sampled experiment runs to the window's start
+    untimed, then each step times the window's ticks from a copy of that
+    state; the line declares the window."""
+    p = _bench("--impl", "reference", "--workload", "gpt_small", "--steps", "2", "--warmup", "3")
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    assert r["config"]["window"]["start_tick"] == 3000 and r["config"]["window"]["ticks"] == 2000
+    assert r["value"] > 0 and "ticks [3000, 5000)" in r["cpu_baseline"]["sample"]
+
+
+def test_default_workload_is_the_config3_window():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    assert b.DEFAULT == "config3" and b.WINDOWS["config3"][0] > 0
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
 def test_gpu_arm_fails_loudly_without_a_gpu():
     p = _bench("--steps", "1", "--warmup", "3")
@@ -55,7 +76,8 @@ def test_reference_arm_under_torchrun_prints_once():
     p = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
                         "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
                         "--master-port", str(port), os.path.join(ROOT, "bench.py"),
-                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                        "--impl", "reference", "--workload", "config2", "--gpus", "2", "--steps",
+                        "1", "--warmup", "3"],
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
