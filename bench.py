@@ -367,7 +367,7 @@ def run_gpu(args, rank: int, world: int):
     if window:
         # untimed: every experiment to the window's start tick, once
         sim.reset()
-        rc = sim.run(max_ticks=window[0])
+        rc = sim.run(max_ticks=window[0], variant=args.variant, block_warps=args.block_warps)
         assert rc in (mv.MV_OK, mv.MV_INCOMPLETE), rc
         c = sim.counters()
         snap["ws"] = sim.ws.clone()
@@ -385,7 +385,7 @@ def run_gpu(args, rank: int, world: int):
     def timed():
         if not window:
             sim.reset()
-        rc = sim.run(max_ticks=budget)
+        rc = sim.run(max_ticks=budget, variant=args.variant, block_warps=args.block_warps)
         assert rc in ((mv.MV_OK, mv.MV_INCOMPLETE) if window else (mv.MV_OK,)), rc
 
     for _ in range(args.warmup):
@@ -450,7 +450,7 @@ def run_gpu(args, rank: int, world: int):
                 t0 = time.perf_counter()
                 with torch.cuda.stream(stream):
                     sim.ws.copy_(host, non_blocking=True)     # the start state, host -> device
-                sim.run(max_ticks=budget)
+                sim.run(max_ticks=budget, variant=args.variant, block_warps=args.block_warps)
                 c = sim.counters()                            # per-experiment results, device -> host
                 e2e_s.append(time.perf_counter() - t0)
             h2d = int(host.numel())
@@ -462,7 +462,7 @@ def run_gpu(args, rank: int, world: int):
                 torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
                 s2 = mv.Simulator(packed, device=str(dev), stream=stream)
-                s2.run()
+                s2.run(variant=args.variant, block_warps=args.block_warps)
                 r2 = s2.results()
                 s2.close()
                 e2e_s.append(time.perf_counter() - t0)
@@ -491,7 +491,8 @@ def run_gpu(args, rank: int, world: int):
 
     if rank == 0:
         cfg = config_of(args, window, int(exps_all))
-        cfg.update({"packet_hops_per_step": int(hops_all),
+        cfg.update({"kernel_build": args.variant or "automatic",
+                    "packet_hops_per_step": int(hops_all),
                     "l2": "flushed between steps (512 MiB write)",
                     "grid_steps_per_run": int(statistics.mean(steps_grid))})
         if window:
@@ -528,6 +529,8 @@ def main():
     ap.add_argument("--max-ticks", type=int, default=None,
                     help="window length in ticks of each experiment's clock (0: whole runs)")
     ap.add_argument("--whole", action="store_true", help="time whole runs, no window")
+    ap.add_argument("--variant", type=int, default=0, help="kernel build (0: automatic)")
+    ap.add_argument("--block-warps", type=int, default=0, help="warps a block (0: automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

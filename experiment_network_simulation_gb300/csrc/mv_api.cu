@@ -30,6 +30,9 @@ constexpr u64 kStageMax = 112 * 1024;
 constexpr u32 kPartialImage = 88 * 1024;
 // ... and for the build with one 16-warp block an SM
 constexpr u32 kPartialImage3 = 192 * 1024;
+// Largest dynamic shared memory of a block (227 KiB) less the kernel's own
+// static shared memory, for the builds with one block an SM.
+constexpr u32 kBlockSmem = 227 * 1024 - 3 * 1024;
 
 // Byte layout of the workspace: a static part uploaded from the host, then
 // a dynamic part cleared and filled by the set-up kernels.
@@ -786,20 +789,24 @@ int mv_run_ex(mv_ctx *c, uint32_t max_ticks, const mv_run_opts *o, uint64_t *ste
     P.max_ticks = max_ticks;
     u32 warps = c->L.warps, grid = 0, variant = c->L.variant;
     if (o) {
-        if (o->stage > 2 || o->variant > 3) return MV_EINVAL;
+        if (o->stage > 2 || o->variant > 4) return MV_EINVAL;
         P.watchdog_ns = o->watchdog_ns;
         P.stage_mode = o->stage;
         if (o->variant) variant = o->variant;
         if (o->block_warps) warps = o->block_warps;
         grid = o->grid_blocks;
     }
-    if (variant == 3 && !(o && o->block_warps)) warps = kMaxWarps;
-    warps = std::min<u32>(warps, variant == 3 ? kMaxWarps : 8);
+    const u32 max_warps = variant == 4 ? kMaxWarps : variant == 3 ? 16u : 8u;
+    if (variant >= 3 && !(o && o->block_warps)) warps = max_warps;
+    warps = std::min<u32>(warps, max_warps);
     // shared image budget: the batch's own (whole images) for the latency
     // build, else what the build's blocks an SM leave
     u32 image = c->L.image;
     if (variant == 2 && c->L.variant == 2) image = kPartialImage;
     if (variant == 3) image = std::max<u32>(c->L.image, kPartialImage3);
+    if (variant == 4)
+        image = std::max<u32>(c->L.image,
+                              (kBlockSmem - warps * megakernel_scratch_bytes()) & ~15u);
     P.stage_limit = image;
     const u32 smem = megakernel_smem(warps, image);
     int bpsm = 0, nsm = 0;

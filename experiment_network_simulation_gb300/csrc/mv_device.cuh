@@ -23,7 +23,8 @@ constexpr u32 kNAct = 16;     // running collective memberships, per rank
 constexpr u32 kMaxPorts = 64; // ports per switch (one warp, two ports a lane)
 constexpr u32 kTickLimit = 0xFFF00000u;
 constexpr u32 kPopLog = 64;   // credit delay (delta + 1) of a link is at most this
-constexpr u32 kMaxWarps = 16; // warps of the block that steps one experiment (build 3; 8 otherwise)
+constexpr u32 kMaxWarps = 32; // warps of the block that steps one experiment (build 4; 16 for
+                              // build 3; 8 otherwise)
 
 enum : u32 { NODE_COMPUTE = 0, NODE_INTRA = 1, NODE_NET = 2 };
 enum : u32 { COLL_AR = 0, COLL_RS = 1, COLL_AG = 2, COLL_RELAY = 3, COLL_P2P = 4, COLL_A2A = 5 };
@@ -218,10 +219,12 @@ cudaError_t launch_init(const Params &p, u32 max_nodes, u32 max_queues, u32 max_
                         cudaStream_t st);
 cudaError_t launch_coll_times(const Params &p, u32 max_colls, cudaStream_t st);
 // variant 1: latency (one block of <= 8 warps an SM, register view); 2: occupancy (two
-// blocks of 8 warps an SM); 3: one block of 16 warps an SM (more shared memory a block)
+// blocks of 8 warps an SM); 3: one block of 16 warps an SM (more shared memory a block);
+// 4: one block of 32 warps an SM (64 registers a thread)
 cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,
                                int *n_sm);
 u32 megakernel_smem(u32 warps, u32 image_bytes);
+u32 megakernel_scratch_bytes();   // per-warp forwarding scratch
 cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
                               u32 smem_bytes, cudaStream_t st);
 

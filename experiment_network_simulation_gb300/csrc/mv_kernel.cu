@@ -1728,7 +1728,8 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
 // blocks share an SM (more experiments in flight, for experiments whose
 // state stays in global memory and whose ticks wait on memory).
 template <int VAR>
-__global__ void __launch_bounds__(VAR == 3 ? 512 : 256, VAR == 2 ? 2 : 1) k_megakernel(Params P)
+__global__ void __launch_bounds__(VAR == 4 ? 1024 : VAR == 3 ? 512 : 256, VAR == 2 ? 2 : 1)
+k_megakernel(Params P)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
     const u32 nW = blockDim.x >> 5, warp = threadIdx.x >> 5;
@@ -1787,9 +1788,12 @@ cudaError_t launch_coll_times(const Params &p, u32 max_colls, cudaStream_t st)
 
 u32 megakernel_smem(u32 warps, u32 image_bytes) { return warps * (u32)sizeof(SwSmem) + image_bytes; }
 
+u32 megakernel_scratch_bytes() { return (u32)sizeof(SwSmem); }
+
 static const void *megakernel_fn(u32 variant)
 {
-    return variant == 3 ? (const void *)k_megakernel<3>
+    return variant == 4 ? (const void *)k_megakernel<4>
+         : variant == 3 ? (const void *)k_megakernel<3>
          : variant == 2 ? (const void *)k_megakernel<2> : (const void *)k_megakernel<1>;
 }
 
@@ -1811,7 +1815,8 @@ cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *bloc
 cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
                               u32 smem_bytes, cudaStream_t st)
 {
-    if (variant == 3) k_megakernel<3><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    if (variant == 4) k_megakernel<4><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    else if (variant == 3) k_megakernel<3><<<blocks, warps * 32, smem_bytes, st>>>(p);
     else if (variant == 2) k_megakernel<2><<<blocks, warps * 32, smem_bytes, st>>>(p);
     else k_megakernel<1><<<blocks, warps * 32, smem_bytes, st>>>(p);
     return cudaGetLastError();

@@ -187,13 +187,14 @@ typedef struct mv_ctx mv_ctx;
  *   1 = only its wake table is; 2 = nothing is (results are the same in
  *   every mode; the modes exist to test and measure that).
  * block_warps: warps of the block stepping one experiment (0 = automatic;
- *   at most 8, or 16 for variant 3).
+ *   at most 8, 16 for variant 3, 32 for variant 4).
  * variant: the kernel build.  0 = automatic; 1 = one block an SM with the
  *   most registers (for batches whose experiments all fit in shared memory);
  *   2 = two 8-warp blocks an SM (more experiments in flight); 3 = one
  *   16-warp block an SM with twice the shared memory for staging (for
- *   experiments whose hottest arrays do not fit variant 2's share).  Results
- *   are the same in every variant. */
+ *   experiments whose hottest arrays do not fit variant 2's share); 4 = one
+ *   32-warp block an SM at 64 registers a thread (twice the warps stepping
+ *   one experiment).  Results are the same in every variant. */
 typedef struct mv_run_opts {
     uint64_t watchdog_ns;
     uint32_t grid_blocks;

@@ -104,7 +104,7 @@ def random_batch(seed=2024, n=200):
     return I.Batch(ex, "random")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_random_scenarios_bit_exact(variant):
     p = random_batch().pack()
     want = O.run(p)

@@ -213,17 +213,18 @@ def test_watchdog_stops_at_a_tick_boundary_and_resumes():
     assert_same(got, O.run(p))
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 @pytest.mark.parametrize("stage", [mv.STAGE_AUTO, mv.STAGE_WAKE, mv.STAGE_NONE])
 def test_every_build_and_staging_bit_exact(stage, variant):
-    """The same batches through the three kernel builds (one block an SM
+    """The same batches through the four kernel builds (one block an SM
     with a register copy of the view and one switch a pass; two 8-warp blocks
-    an SM, or one 16-warp block, with the shared view and up to four
-    switches a pass), with the state staged in shared memory by priority,
-    only the wake table staged, or nothing staged, and other block shapes."""
+    an SM, one 16-warp block or one 32-warp block, with the shared view and
+    up to four switches a pass), with the state staged in shared memory by
+    priority, only the wake table staged, or nothing staged, and other block
+    shapes."""
     for p in (pin_batch().pack(), I.config1().pack(), I.gpt_small(seeds=(4,)).pack()):
         want = O.run(p)
-        for warps in (0, 1, 3, 16):
+        for warps in (0, 1, 3, 16, 32):
             got = mv.simulate(p, run_opts=dict(stage=stage, block_warps=warps, variant=variant))
             assert_same(got, want)
 
