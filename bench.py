@@ -75,9 +75,11 @@ WORKLOADS = {
 }
 DEFAULT = "config3"
 # Default window (start tick, ticks) per workload; None = whole runs.  Config
-# 3's window lies in the data-parallel all-reduce phase of its experiments
-# (their iterations end between about 3.4 M and 3.9 M ticks).
-WINDOWS = {"config3": (3_000_000, 4_000), "config5": (300_000, 2_000), "gpt_small": (3_000, 2_000)}
+# 3's window lies in the data-parallel all-reduce phase of all 500
+# experiments: by tick 2.6 M every pipeline transfer has ended, the gradient
+# all-reduces started from about 1.7 M on, and the iterations end between
+# about 2.7 M (16 channels) and 4.5 M ticks (trees of 16 channels).
+WINDOWS = {"config3": (2_600_000, 4_000), "config5": (300_000, 2_000), "gpt_small": (3_000, 2_000)}
 
 # DRAM bytes (read + write) per megakernel launch from ncu captures of the
 # current kernel, keyed by workload and window; each entry names the kernel
