@@ -68,7 +68,7 @@ struct Layout {
         r_host_rec;
     u64 static_bytes = 0;
     Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_rdirty, r_pend, r_act,
-        r_lanes, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
+        r_lhot, r_lcold, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
         r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_coll_start, r_coll_end, r_glob,
         r_wake;
     u64 total = 0;
@@ -510,7 +510,8 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_rdirty = L.take(4 * L.rk_total);
     L.r_pend = L.take(8ull * L.pend_total);
     L.r_act = L.take(4ull * L.act_total);
-    L.r_lanes = L.take(sizeof(Lane) * L.lane_total);
+    L.r_lhot = L.take(sizeof(LaneHot) * L.lane_total);
+    L.r_lcold = L.take(sizeof(LaneCold) * L.lane_total);
     L.r_ports = L.take(8ull * L.portc_total);
     L.r_poplog = L.take(4ull * L.plog_total);
     L.r_nd_pred = L.take(4 * L.nd_total);
@@ -598,7 +599,8 @@ Params make_params(void *ws, const Layout &L)
     P.rdirty = at<u32>(ws, L.r_rdirty);
     P.pend = at<uint2>(ws, L.r_pend);
     P.act = at<u32>(ws, L.r_act);
-    P.lanes = at<Lane>(ws, L.r_lanes);
+    P.lhot = at<LaneHot>(ws, L.r_lhot);
+    P.lcold = at<LaneCold>(ws, L.r_lcold);
     P.ports = at<uint2>(ws, L.r_ports);
     P.poplog = at<u32>(ws, L.r_poplog);
     P.nd_pred = at<u32>(ws, L.r_nd_pred);

@@ -63,21 +63,24 @@ struct ExpRec {
     u32 pad;
 };
 
-// One send lane as stored: a stream of messages one rank sends for one
-// channel of one collective membership (a queue pair in RDMA terms), five
-// 16-byte words.  Besides the message counters it caches what every packet
-// or message of the lane needs without another table read: the collective,
-// its member count, kind and first member entry; destination node and rank;
-// the destination's receive slot once its join has been seen; the sender's
-// own receive-counter base.  Field packing (mv_kernel.cu, load_lane):
-//   w0: node, member | chan << 16 | kind << 24, collective, members
-//   w1: message, messages, packets left, destination member
-//   w2: dst_port | dep_base << 8 | dep_mask << 16 | ok_dst << 19 | coll kind << 20,
-//       dep_need, first member entry, connection key
-//   w3: a2a entry, a2a first chunk, destination node, destination rank
-//   w4: destination slot, receive-counter base, 0, 0
-struct Lane {
-    uint4 w[5];
+// One send lane: a stream of messages one rank sends for one channel of one
+// collective membership (a queue pair in RDMA terms), kept as two 32-byte
+// records in two arrays.  The hot record holds everything a packet needs
+// and is the only one read and written per packet (one 32-byte sector); the
+// cold record holds what a new message needs (the collective, its member
+// count, kind and first member entry, the message count and the all-to-all
+// position).  Field packing (mv_kernel.cu, load_lane_hot / load_lane_cold):
+//   hot  a: node, connection key | dep_mask << 24 | ok_dst << 27, packets left,
+//           destination rank | destination slot << 16 | dst_port << 24
+//        b: dep_need, dep_base | receive-counter base << 8 | chan << 16 | kind << 24,
+//           destination node, message
+//   cold a: collective, members | member << 16, first member entry, messages
+//        b: destination member | coll kind << 16, a2a entry, a2a first chunk, 0
+struct LaneHot {
+    uint4 a, b;
+};
+struct LaneCold {
+    uint4 a, b;
 };
 
 // Per-rank control word as stored (48 bytes).
@@ -136,7 +139,8 @@ struct Params {
     u32 *rdirty;             // per rank: a message of one of its running nodes completed
     uint2 *pend;             // per rank: pend_cap (node, start tick)
     u32 *act;                // per rank: act_cap running nodes, ascending
-    Lane *lanes;             // per rank: lane_cap
+    LaneHot *lhot;           // per rank: lane_cap hot lane records
+    LaneCold *lcold;         // per rank: lane_cap cold lane records
     uint2 *ports;            // per rank: port_cap (messages received, owner node)
     u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
     i32 *nd_out;
@@ -169,8 +173,8 @@ __host__ __device__ inline u32 pk_slot(uint4 p) { return p.w >> 25; }
 // (IM_WAKE .. IM_SLOTS) is copied in and back out; the topology records and
 // routing tables after it are only copied in.
 enum : int { IM_WAKE, IM_QPUSH, IM_QPOP, IM_EG, IM_RK, IM_RDIRTY, IM_PRED, IM_CAND, IM_START, IM_END,
-             IM_PBASE, IM_DONE, IM_OUT, IM_ACT, IM_PEND, IM_PORTS, IM_POPLOG, IM_LANES,
-             IM_SLOTS, IM_NDYN, IM_SWREC = IM_NDYN, IM_PORTREC, IM_HOSTREC, IM_ROUTE, IM_UPN,
+             IM_PBASE, IM_DONE, IM_OUT, IM_ACT, IM_PEND, IM_PORTS, IM_POPLOG, IM_LHOT,
+             IM_LCOLD, IM_SLOTS, IM_NDYN, IM_SWREC = IM_NDYN, IM_PORTREC, IM_HOSTREC, IM_ROUTE, IM_UPN,
              IM_UPLIST, IM_N };
 
 __host__ __device__ inline u64 im_round(u64 b) { return (b + 15) & ~15ull; }
@@ -189,7 +193,8 @@ __host__ __device__ inline void image_bytes(const ExpRec &X, const TopoRec &T, u
     sz[IM_PEND] = 8ull * X.nr * X.pend_cap;
     sz[IM_PORTS] = 8ull * X.nr * X.port_cap;
     sz[IM_POPLOG] = 4ull * X.nq * plog;
-    sz[IM_LANES] = sizeof(Lane) * (u64)X.nr * X.lane_cap;
+    sz[IM_LHOT] = sizeof(LaneHot) * (u64)X.nr * X.lane_cap;
+    sz[IM_LCOLD] = sizeof(LaneCold) * (u64)X.nr * X.lane_cap;
     sz[IM_SLOTS] = 16ull * X.nq * X.cap;
     sz[IM_SWREC] = 8ull * T.nsw;
     sz[IM_PORTREC] = 16ull * T.nq;

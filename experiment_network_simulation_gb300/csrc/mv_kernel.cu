@@ -252,7 +252,8 @@ struct XV {
     u32 *rdirty;
     uint2 *pend;
     u32 *act;
-    Lane *lanes;
+    LaneHot *lhot;
+    LaneCold *lcold;
     uint2 *ports;
     u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
     i32 *nd_out;
@@ -282,7 +283,8 @@ struct HV {
     u32 *rdirty;
     uint2 *pend;
     u32 *act;
-    Lane *lanes;
+    LaneHot *lhot;
+    LaneCold *lcold;
     uint2 *ports;
     u32 *nd_pred, *nd_cand, *nd_start, *nd_end, *nd_pbase, *nd_done;
     i32 *nd_out;
@@ -305,7 +307,8 @@ __device__ __forceinline__ HV make_hv(const XV &S)
     V.W.memb_off = S.W.memb_off; V.W.a2a_off = S.W.a2a_off; V.W.a2a_in_off = S.W.a2a_in_off;
     V.plog = S.plog;
     V.q_push = S.q_push; V.q_pop = S.q_pop; V.poplog = S.poplog; V.slots = S.slots; V.eg = S.eg;
-    V.rk = S.rk; V.rdirty = S.rdirty; V.pend = S.pend; V.act = S.act; V.lanes = S.lanes; V.ports = S.ports;
+    V.rk = S.rk; V.rdirty = S.rdirty; V.pend = S.pend; V.act = S.act; V.lhot = S.lhot; V.lcold = S.lcold;
+    V.ports = S.ports;
     V.nd_pred = S.nd_pred; V.nd_cand = S.nd_cand; V.nd_start = S.nd_start; V.nd_end = S.nd_end;
     V.nd_pbase = S.nd_pbase; V.nd_done = S.nd_done; V.nd_out = S.nd_out; V.wake = S.wake;
     V.sw_rec = S.sw_rec; V.port_rec = S.port_rec; V.host_rec = S.host_rec; V.route = S.route;
@@ -695,33 +698,45 @@ struct LaneReg {
     u32 key, a2a_e, a2a_start, dnode;
     u32 drank, dslot, ok_dst, pbase;
 };
-static_assert(sizeof(Lane) == 80, "Lane is five 16-byte words");
+static_assert(sizeof(LaneHot) == 32 && sizeof(LaneCold) == 32, "lane records are 32 bytes");
 static_assert(kNPort <= 256 && kNLane <= 256, "ports and channels fit the packed lane fields");
 // Word by word: the local LaneReg never has its address taken, so it stays
-// in registers.
-__device__ __forceinline__ LaneReg load_lane(const Lane *p)
+// in registers.  A lane's member count, member index and destination member
+// fit 16 bits (collectives have at most 65,535 members), its destination
+// rank 16 bits (hosts), its receive slot, destination port, dependency base
+// and counter base 8 bits (at most 128 receive counters a rank), its
+// channel 8 bits (at most 64 lanes a rank).
+__device__ __forceinline__ LaneReg load_lane_hot(const LaneHot *p)
 {
-    const uint4 a = p->w[0], b = p->w[1], c = p->w[2], d = p->w[3], e = p->w[4];
+    const uint4 a = p->a, b = p->b;
     LaneReg L;
-    L.node = a.x; L.member = a.y & 0xFFFFu; L.chan = (a.y >> 16) & 0xFFu; L.kind = a.y >> 24;
-    L.coll = a.z; L.nmemb = a.w;
-    L.m = b.x; L.nmsg = b.y; L.pkts_left = b.z; L.dst_member = b.w;
-    L.dst_port = c.x & 0xFFu; L.dep_base = (c.x >> 8) & 0xFFu; L.dep_mask = (c.x >> 16) & 7u;
-    L.ok_dst = (c.x >> 19) & 1u; L.ckind = c.x >> 20;
-    L.dep_need = c.y; L.mbase = c.z; L.key = c.w;
-    L.a2a_e = d.x; L.a2a_start = d.y; L.dnode = d.z; L.drank = d.w;
-    L.dslot = e.x; L.pbase = e.y;
+    L.node = a.x;
+    L.key = a.y & 0xFFFFFFu; L.dep_mask = (a.y >> 24) & 7u; L.ok_dst = (a.y >> 27) & 1u;
+    L.pkts_left = a.z;
+    L.drank = a.w & 0xFFFFu; L.dslot = (a.w >> 16) & 0xFFu; L.dst_port = a.w >> 24;
+    L.dep_need = b.x;
+    L.dep_base = b.y & 0xFFu; L.pbase = (b.y >> 8) & 0xFFu; L.chan = (b.y >> 16) & 0xFFu;
+    L.kind = b.y >> 24;
+    L.dnode = b.z; L.m = b.w;
     return L;
 }
-__device__ __forceinline__ void store_lane(Lane *p, const LaneReg &L)
+__device__ __forceinline__ void load_lane_cold(const LaneCold *p, LaneReg &L)
 {
-    p->w[0] = make_uint4(L.node, L.member | (L.chan << 16) | (L.kind << 24), L.coll, L.nmemb);
-    p->w[1] = make_uint4(L.m, L.nmsg, L.pkts_left, L.dst_member);
-    p->w[2] = make_uint4(L.dst_port | (L.dep_base << 8) | (L.dep_mask << 16) | (L.ok_dst << 19) |
-                             (L.ckind << 20),
-                         L.dep_need, L.mbase, L.key);
-    p->w[3] = make_uint4(L.a2a_e, L.a2a_start, L.dnode, L.drank);
-    p->w[4] = make_uint4(L.dslot, L.pbase, 0u, 0u);
+    const uint4 a = p->a, b = p->b;
+    L.coll = a.x; L.nmemb = a.y & 0xFFFFu; L.member = a.y >> 16; L.mbase = a.z; L.nmsg = a.w;
+    L.dst_member = b.x & 0xFFFFu; L.ckind = b.x >> 16; L.a2a_e = b.y; L.a2a_start = b.z;
+}
+__device__ __forceinline__ void store_lane_hot(LaneHot *p, const LaneReg &L)
+{
+    p->a = make_uint4(L.node, L.key | (L.dep_mask << 24) | (L.ok_dst << 27), L.pkts_left,
+                      L.drank | (L.dslot << 16) | (L.dst_port << 24));
+    p->b = make_uint4(L.dep_need, L.dep_base | (L.pbase << 8) | (L.chan << 16) | (L.kind << 24),
+                      L.dnode, L.m);
+}
+__device__ __forceinline__ void store_lane_cold(LaneCold *p, const LaneReg &L)
+{
+    p->a = make_uint4(L.coll, L.nmemb | (L.member << 16), L.mbase, L.nmsg);
+    p->b = make_uint4(L.dst_member | (L.ckind << 16), L.a2a_e, L.a2a_start, 0u);
 }
 
 // Receive-counter occupancy bits, by value (no indexed array, so the rank's
@@ -1082,7 +1097,8 @@ __device__ __forceinline__ bool net_join(RV &v, u32 u)
     }
     u32 nch = nchan(v, c), lpc = tree_of(v, c) ? 3u : 1u;
     const u64 lane_ok = X.lane_cap >= 64 ? ~0ull : ((1ull << X.lane_cap) - 1);
-    Lane *lanes = V.lanes + (u64)v.r * X.lane_cap;
+    LaneHot *lhot = V.lhot + (u64)v.r * X.lane_cap;
+    LaneCold *lcold = V.lcold + (u64)v.r * X.lane_cap;
     for (u32 ch = 0; ch < nch; ch++) {
         for (u32 kd = 0; kd < lpc; kd++) {
             u32 nm = lane_count(v, c, i, ch, kd);
@@ -1098,7 +1114,8 @@ __device__ __forceinline__ bool net_join(RV &v, u32 u)
             L.dnode = kUnset;
             L.pbase = (u32)base;
             L.pkts_left = lane_setup(v, L);
-            store_lane(&lanes[slot], L);
+            store_lane_hot(&lhot[slot], L);
+            store_lane_cold(&lcold[slot], L);
             v.C.lane_mask |= 1ull << slot;
             v.C.blocked = 0;
             out += (i32)nm;
@@ -1235,7 +1252,8 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
     u64 M = v.C.lane_mask;
     u64 hi = v.C.rr < 64 ? (M & (~0ull << v.C.rr)) : 0ull;
     u64 lo = M & ~hi;
-    Lane *lanes = V.lanes + (u64)v.r * X.lane_cap;
+    LaneHot *lhot = V.lhot + (u64)v.r * X.lane_cap;
+    LaneCold *lcold = V.lcold + (u64)v.r * X.lane_cap;
     const uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     bool timed = false;                 // some lane waits for a destination's join
     for (int pass = 0; pass < 2; pass++) {
@@ -1243,7 +1261,7 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
         while (m) {
             u32 l = (u32)__ffsll((long long)m) - 1;
             m &= m - 1;
-            LaneReg L = load_lane(&lanes[l]);
+            LaneReg L = load_lane_hot(&lhot[l]);    // all a packet needs
             bool ok = true;
             for (u32 b = 0; b < 3 && ok; b++)
                 if ((L.dep_mask >> b) & 1u)
@@ -1279,11 +1297,16 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
             v.n_inj++;
             v.changed = true;
             rank_poke(v, hr.w, pk.x);
-            if (--L.pkts_left == 0) {
-                if (++L.m == L.nmsg) v.C.lane_mask &= ~(1ull << l);
-                else L.pkts_left = lane_setup(v, L);
+            if (--L.pkts_left == 0) {           // the message is out: the next one
+                load_lane_cold(&lcold[l], L);
+                if (++L.m == L.nmsg) {
+                    v.C.lane_mask &= ~(1ull << l);
+                } else {
+                    L.pkts_left = lane_setup(v, L);
+                    store_lane_cold(&lcold[l], L);
+                }
             }
-            store_lane(&lanes[l], L);
+            store_lane_hot(&lhot[l], L);
             if (v.C.lane_mask) v.nxt = min(v.nxt, v.C.busy > t + 1 ? v.C.busy : t + 1);
             return;
         }
@@ -1442,7 +1465,8 @@ __device__ const void *global_slice(const Params &P, const ExpRec &X, const Topo
     case IM_PEND: return P.pend + X.pend_off;
     case IM_PORTS: return P.ports + X.portc_off;
     case IM_POPLOG: return P.poplog + X.plog_off;
-    case IM_LANES: return P.lanes + X.lane_off;
+    case IM_LHOT: return P.lhot + X.lane_off;
+    case IM_LCOLD: return P.lcold + X.lane_off;
     case IM_SLOTS: return P.slots + X.slot_off;
     case IM_SWREC: return P.sw_rec + T.sw_off;
     case IM_PORTREC: return P.port_rec + T.port_off;
@@ -1474,7 +1498,8 @@ __device__ void set_slice(XV &V, int k, const void *c)
     case IM_PEND: V.pend = (uint2 *)p; break;
     case IM_PORTS: V.ports = (uint2 *)p; break;
     case IM_POPLOG: V.poplog = (u32 *)p; break;
-    case IM_LANES: V.lanes = (Lane *)p; break;
+    case IM_LHOT: V.lhot = (LaneHot *)p; break;
+    case IM_LCOLD: V.lcold = (LaneCold *)p; break;
     case IM_SLOTS: V.slots = (uint4 *)p; break;
     case IM_SWREC: V.sw_rec = (const uint2 *)p; break;
     case IM_PORTREC: V.port_rec = (const uint4 *)p; break;
