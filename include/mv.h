@@ -204,7 +204,10 @@ typedef struct mv_run_opts {
 } mv_run_opts;
 
 /* Workspace bytes mv_create needs for this batch (validates the
- * descriptor).  Returns MV_OK, MV_EINVAL or MV_EOVERFLOW. */
+ * descriptor).  Multiverse section 3.3: the simulator manages the storage
+ * of every experiment's entities centrally, one column table per component
+ * with an experiment id; here that is one caller-owned device buffer laid
+ * out per experiment.  Returns MV_OK, MV_EINVAL or MV_EOVERFLOW. */
 int mv_workspace_bytes(const mv_batch_desc *desc, uint64_t *bytes);
 
 /* Sizes of the concatenated per-node, per-record and per-collective result
@@ -213,7 +216,11 @@ int mv_workspace_bytes(const mv_batch_desc *desc, uint64_t *bytes);
 int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_records,
                     uint64_t *n_colls);
 
-/* Validate the batch, lay it out in the caller's device workspace
+/* Multiverse section 3.1: the user sets the workload, the collective
+ * library's parameters and the topology and lists the experiments; the GPU
+ * memory simulator checks each experiment before the run (an experiment
+ * that does not fit ends with MV_EXP_OOM).
+ * Validate the batch, lay it out in the caller's device workspace
  * (`dev_workspace`, `ws_bytes`, 256-byte aligned), upload it on `stream`
  * (a cudaStream_t, NULL = legacy default stream), build the routing tables,
  * run the memory check and put every experiment at tick 0.  On success
@@ -222,8 +229,12 @@ int mv_result_sizes(const mv_batch_desc *desc, uint64_t *n_nodes, uint64_t *n_re
 int mv_create(const mv_batch_desc *desc, void *dev_workspace, uint64_t ws_bytes,
               void *stream, mv_ctx **out);
 
-/* Advance every unfinished experiment by at most max_ticks ticks of its own
- * clock, in ONE launch of the persistent megakernel, and wait for it.  Each
+/* Multiverse section 4.3: one megakernel launch runs the whole execution
+ * graph (section 3.2's eight systems in order, every step) for the batch.
+ * Advance every unfinished experiment by at most max_ticks ticks of its own
+ * clock, in ONE launch of the persistent megakernel, and wait for it.
+ * (Ticks are 32-bit: a clock stops at 0xFFF00000, so a larger budget would
+ * mean nothing.)  Each
  * experiment is stepped by one thread block (its entities spread over the
  * block's warps, one block barrier per tick); blocks take experiments
  * largest first.  State stays on the device, so run(a) then run(b) equals
@@ -236,18 +247,25 @@ int mv_run_ex(mv_ctx *ctx, uint32_t max_ticks, const mv_run_opts *opts,
               uint64_t *steps_done);
 
 /* Put every experiment back to tick 0 (clear the dynamic state, rebuild the
- * routing tables, rerun the memory check) without re-uploading the batch.
- * Enqueued on the context's stream; does not wait. */
+ * routing tables, rerun the memory check of Multiverse section 3.1) without
+ * re-uploading the batch.  Enqueued on the context's stream; does not wait.
+ * Returns MV_OK, MV_EINVAL for a NULL context or MV_ECUDA. */
 int mv_reset(mv_ctx *ctx);
 
 /* Device time, in ms, of the megakernel launch of the last mv_run, taken
- * with CUDA events recorded on the context's stream around that launch. */
+ * with CUDA events recorded on the context's stream around that launch.
+ * MV_EINVAL when no run was timed since create or reset. */
 int mv_last_run_ms(mv_ctx *ctx, float *ms);
 
-/* Copy the results to the caller's host buffers (blocking on the stream). */
+/* Multiverse section 3.1: the network simulator tells the system simulator
+ * when each flow completes.  Copy the results (per experiment, per node,
+ * per message record, per collective: see mv_results_view) to the caller's
+ * host buffers, blocking on the stream.  Returns MV_OK, MV_EINVAL for a
+ * NULL context or view, MV_ECUDA if a copy fails. */
 int mv_results(mv_ctx *ctx, const mv_results_view *out);
 
-/* Free the host context.  The workspace is not touched. */
+/* Free the host context (and its two CUDA events).  The workspace is not
+ * touched and stays the caller's.  MV_EINVAL for NULL. */
 int mv_destroy(mv_ctx *ctx);
 
 /*
