@@ -43,7 +43,7 @@ struct Layout {
         nmemb = 0, na2a = 0, na2a_in = 0;
     u64 route_bytes = 0, q_total = 0, slot_total = 0, plog_total = 0, eg_total = 0,
         rk_total = 0, pend_total = 0, act_total = 0, lane_total = 0, portc_total = 0,
-        nd_total = 0, rec_total = 0, coll_total = 0, items = 0;
+        nd_total = 0, rec_total = 0, coll_total = 0, taken_total = 0, items = 0;
     u32 warps = 1, image = 16;      // megakernel block size and shared image budget
     u32 variant = 1;                // 1: every experiment staged whole; 2: some are not
     u32 max_level = 0, max_nodes = 0, max_queues = 0, max_ranks = 0, max_colls = 0;
@@ -67,7 +67,7 @@ struct Layout {
         r_a2a_bytes, r_a2a_in_bytes, r_mem, r_order, r_node_rank, r_sw_rec, r_port_rec,
         r_host_rec;
     u64 static_bytes = 0;
-    Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_slots, r_eg, r_rk, r_rdirty, r_pend, r_act,
+    Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_q_taken, r_slots, r_eg, r_rk, r_rdirty, r_pend, r_act,
         r_lhot, r_lcold, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
         r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_coll_start, r_coll_end, r_glob,
         r_wake;
@@ -354,12 +354,16 @@ int plan(const mv_batch_desc *d, Layout &L)
         X.cap = d->exp_cap[e];
         X.tick_ps = d->exp_tick_ps[e];
         X.rec_cap = d->exp_rec_cap[e];
+        X.voq = d->exp_voq[e];
         X.dur_seed = d->exp_dur_seed[e];
         X.ecmp_seed = d->exp_ecmp_seed[e];
         X.gpu_mem = d->exp_gpu_mem[e];
         if (W.nr > T.nh || X.algo > ALGO_TREE || X.nc == 0 || X.nc > 1024 || X.pkt == 0 ||
-            X.cap < 2 || X.cap > 1024 || X.tick_ps == 0)
+            X.cap < 2 || X.cap > 1024 || X.tick_ps == 0 || X.voq > 1 || (X.voq && X.cap > 64))
             return MV_EINVAL;
+        // with VOQs several packets can leave an ingress's buffer in one tick, so
+        // its pop log keeps the last 64 pops (a whole buffer)
+        X.plog = X.voq ? 64u : T.plog;
         // chunk size matters for every kind but the relay
         if (X.chunk == 0) {
             for (u32 c = 0; c < W.ncoll; c++)
@@ -387,9 +391,11 @@ int plan(const mv_batch_desc *d, Layout &L)
         X.nd_off = L.nd_total;
         X.rec_off = L.rec_total;
         X.coll_res_off = L.coll_total;
+        X.taken_off = L.taken_total;
         L.q_total += X.nq;
         L.slot_total += (u64)X.nq * X.cap;
-        L.plog_total += (u64)X.nq * T.plog;
+        L.plog_total += (u64)X.nq * X.plog;
+        L.taken_total += X.voq ? T.nq : 0;
         L.eg_total += T.nq;
         L.rk_total += W.nr;
         L.pend_total += (u64)W.nr * X.pend_cap;
@@ -504,6 +510,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_up_list = L.take(L.nports);
     L.r_q_push = L.take(8 * L.q_total);
     L.r_q_pop = L.take(8 * L.q_total);
+    L.r_q_taken = L.take(8 * L.taken_total);
     L.r_slots = L.take(16 * L.slot_total);
     L.r_eg = L.take(8 * L.eg_total);
     L.r_rk = L.take(sizeof(RankCtl) * L.rk_total);
@@ -593,6 +600,7 @@ Params make_params(void *ws, const Layout &L)
     P.mem = at<u64>(ws, L.r_mem);
     P.q_push = at<u64>(ws, L.r_q_push);
     P.q_pop = at<u64>(ws, L.r_q_pop);
+    P.q_taken = at<u64>(ws, L.r_q_taken);
     P.slots = at<uint4>(ws, L.r_slots);
     P.eg = at<uint2>(ws, L.r_eg);
     P.rk = at<RankCtl>(ws, L.r_rk);

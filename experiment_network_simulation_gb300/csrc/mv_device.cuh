@@ -55,11 +55,13 @@ struct ExpRec {
     u32 topo, work, algo, nc, pkt, cap, tick_ps, rec_cap;
     u64 chunk, dur_seed, ecmp_seed, gpu_mem;
     u64 q_off, slot_off, plog_off, eg_off, rk_off, pend_off, act_off, lane_off, portc_off,
-        nd_off, rec_off, coll_res_off;
+        nd_off, rec_off, coll_res_off, taken_off;
     u32 nq, nsw, nr, nn;            // queues (switch ingress, then NIC receive), switches, ranks, nodes
     u32 item_off, n_items;          // work items: switches, then groups of 32 ranks
     u32 lane_cap, port_cap, pend_cap, act_cap;
     u32 stage_bytes;                // bytes of the whole dynamic state as one shared-memory image
+    u32 voq;                        // 1: switches keep virtual output queues
+    u32 plog;                       // pop-log entries per queue: the fabric's, or 64 with VOQs
     u32 pad;
 };
 
@@ -132,11 +134,12 @@ struct Params {
     const u32 *order;        // experiments in the order blocks take them (largest first)
     // dynamic state
     u64 *q_push, *q_pop;     // per queue: (tick << 32) | counter of the last push / pop
+    u64 *q_taken;            // with VOQs, per switch ingress queue: slots already forwarded
     u32 *poplog;             // per queue: tick of each of the last plog pops (by head % plog)
     uint4 *slots;            // packet descriptors
     uint2 *eg;               // per switch port: (busy_until, round-robin pointer)
     RankCtl *rk;
-    u32 *rdirty;             // per rank: a message of one of its running nodes completed
+    u32 *rdirty;             // per rank: one of its running memberships has no message left
     uint2 *pend;             // per rank: pend_cap (node, start tick)
     u32 *act;                // per rank: act_cap running nodes, ascending
     LaneHot *lhot;           // per rank: lane_cap hot lane records
@@ -174,14 +177,14 @@ __host__ __device__ inline u32 pk_slot(uint4 p) { return p.w >> 25; }
 // routing tables after it are only copied in.
 enum : int { IM_WAKE, IM_QPUSH, IM_QPOP, IM_EG, IM_RK, IM_RDIRTY, IM_PRED, IM_CAND, IM_START, IM_END,
              IM_PBASE, IM_DONE, IM_OUT, IM_ACT, IM_PEND, IM_PORTS, IM_POPLOG, IM_LHOT,
-             IM_LCOLD, IM_SLOTS, IM_NDYN, IM_SWREC = IM_NDYN, IM_PORTREC, IM_HOSTREC, IM_ROUTE, IM_UPN,
+             IM_LCOLD, IM_TAKEN, IM_SLOTS, IM_NDYN, IM_SWREC = IM_NDYN, IM_PORTREC, IM_HOSTREC, IM_ROUTE, IM_UPN,
              IM_UPLIST, IM_N };
 
 __host__ __device__ inline u64 im_round(u64 b) { return (b + 15) & ~15ull; }
 
 __host__ __device__ inline void image_bytes(const ExpRec &X, const TopoRec &T, u64 *sz)
 {
-    const u32 plog = T.plog, n_eg = T.nq;
+    const u32 plog = X.plog, n_eg = T.nq;
     sz[IM_WAKE] = 12ull * X.n_items;          // own wake + two poke words per item
     sz[IM_QPUSH] = 8ull * X.nq;
     sz[IM_QPOP] = 8ull * X.nq;
@@ -195,6 +198,7 @@ __host__ __device__ inline void image_bytes(const ExpRec &X, const TopoRec &T, u
     sz[IM_POPLOG] = 4ull * X.nq * plog;
     sz[IM_LHOT] = sizeof(LaneHot) * (u64)X.nr * X.lane_cap;
     sz[IM_LCOLD] = sizeof(LaneCold) * (u64)X.nr * X.lane_cap;
+    sz[IM_TAKEN] = X.voq ? 8ull * T.nq : 0;
     sz[IM_SLOTS] = 16ull * X.nq * X.cap;
     sz[IM_SWREC] = 8ull * T.nsw;
     sz[IM_PORTREC] = 16ull * T.nq;

@@ -244,7 +244,7 @@ struct XV {
     TopoRec T;
     WorkRec W;
     u32 e, staged, plog, pad;
-    u64 *q_push, *q_pop;
+    u64 *q_push, *q_pop, *q_taken;
     u32 *poplog;
     uint4 *slots;
     uint2 *eg;
@@ -269,13 +269,13 @@ struct XV {
 // compiler loads each field once.
 struct HV {
     struct {
-        u32 algo, nc, pkt, cap, tick_ps, rec_cap, nr, nsw, lane_cap, port_cap, pend_cap, act_cap;
+        u32 algo, nc, pkt, cap, tick_ps, rec_cap, nr, nsw, lane_cap, port_cap, pend_cap, act_cap, voq;
         u64 chunk, dur_seed, ecmp_seed, rec_off;
     } X;
     struct { u32 nh, nq, rdv; } T;
     struct { u32 node_off, edge_off, coll_off, memb_off, a2a_off, a2a_in_off; } W;
     u32 plog;
-    u64 *q_push, *q_pop;
+    u64 *q_push, *q_pop, *q_taken;
     u32 *poplog;
     uint4 *slots;
     uint2 *eg;
@@ -300,13 +300,13 @@ __device__ __forceinline__ HV make_hv(const XV &S)
     V.X.algo = S.X.algo; V.X.nc = S.X.nc; V.X.pkt = S.X.pkt; V.X.cap = S.X.cap;
     V.X.tick_ps = S.X.tick_ps; V.X.rec_cap = S.X.rec_cap; V.X.nr = S.X.nr; V.X.nsw = S.X.nsw;
     V.X.lane_cap = S.X.lane_cap; V.X.port_cap = S.X.port_cap; V.X.pend_cap = S.X.pend_cap;
-    V.X.act_cap = S.X.act_cap; V.X.chunk = S.X.chunk; V.X.dur_seed = S.X.dur_seed;
+    V.X.act_cap = S.X.act_cap; V.X.voq = S.X.voq; V.X.chunk = S.X.chunk; V.X.dur_seed = S.X.dur_seed;
     V.X.ecmp_seed = S.X.ecmp_seed; V.X.rec_off = S.X.rec_off;
     V.T.nh = S.T.nh; V.T.nq = S.T.nq; V.T.rdv = S.T.rdv;
     V.W.node_off = S.W.node_off; V.W.edge_off = S.W.edge_off; V.W.coll_off = S.W.coll_off;
     V.W.memb_off = S.W.memb_off; V.W.a2a_off = S.W.a2a_off; V.W.a2a_in_off = S.W.a2a_in_off;
     V.plog = S.plog;
-    V.q_push = S.q_push; V.q_pop = S.q_pop; V.poplog = S.poplog; V.slots = S.slots; V.eg = S.eg;
+    V.q_push = S.q_push; V.q_pop = S.q_pop; V.q_taken = S.q_taken; V.poplog = S.poplog; V.slots = S.slots; V.eg = S.eg;
     V.rk = S.rk; V.rdirty = S.rdirty; V.pend = S.pend; V.act = S.act; V.lhot = S.lhot; V.lcold = S.lcold;
     V.ports = S.ports;
     V.nd_pred = S.nd_pred; V.nd_cand = S.nd_cand; V.nd_start = S.nd_start; V.nd_end = S.nd_end;
@@ -383,6 +383,25 @@ __device__ __forceinline__ bool credit_ok(const VW &V, u32 qi, u32 tail, u32 H, 
         back++;
     }
     return tail - (H - back) < cap;
+}
+
+// Credit of a switch ingress queue with virtual output queues: several of
+// its packets may leave in one tick, so the sender reads the queue's current
+// head (H pops so far, this tick's included) and walks back over its pop log
+// (the last 64 pops: a whole buffer) until a pop whose credit has arrived.
+// The consumer writes a pop's log entry before the head that announces it.
+template <class VW>
+__device__ __forceinline__ bool credit_ok_voq(const VW &V, u32 qi, u32 tail, u32 D, u32 t)
+{
+    const u32 H = (u32)ld_vol64(&V.q_pop[qi]);
+    __threadfence_block();
+    const u32 *log = V.poplog + (u64)qi * 64;
+    u32 back = 0;
+    while (back < H && back < 64) {
+        if (ld_vol32(&log[(H - 1 - back) & 63u]) + D <= t) break;
+        back++;
+    }
+    return tail - (H - back) < V.X.cap;
 }
 
 // ---------------------------------------------------------------- switches
@@ -648,6 +667,134 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
     pk_min = __reduce_min_sync(kFull, pk_min);
     if (__any_sync(kFull, bad)) *fail = min(*fail, kFailSwitch);
     u32 w = min(nxt, old > t ? old : kUnset);
+    if (lane == 0) V.wake[s] = w;
+    __syncwarp();
+    return min(w, pk_min);
+}
+
+// Forwarding for one tick at switch s with virtual output queues (the VOQ
+// variant of Multiverse section 4.2): an ingress buffer holds one FIFO per
+// egress.  Plan: each lane scans its ingress buffers in arrival order (up to
+// the first packet not yet ready: a buffer's packets are ready in arrival
+// order) and marks, per egress, the ingresses holding a ready packet for it.
+// Pull: the egresses in index order (one lane at a time); a free egress with
+// credit downstream takes, from the first marked ingress at or after its
+// round-robin pointer that no lower egress served in this tick, its oldest
+// packet for it.  A packet leaving from the middle of a buffer frees its slot
+// once the buffer's head passes it (q_taken marks the slots already gone).
+template <class VT>
+__device__ __forceinline__ u32 switch_voq(const XV &Vs, Acc &acc, u32 s, u32 t, u32 old,
+                                          u32 *poke, SwSmem *sm, u32 *fail)
+{
+    VT V = ViewOf<VT>::get(Vs);
+    const u32 lane = threadIdx.x & 31;
+    const uint2 sr = V.sw_rec[s];
+    const u32 p0 = sr.x, np = sr.y, cap = V.X.cap, pm = V.plog - 1;
+    u32 nxt = kUnset, pk_min = kUnset;
+    bool ready_any = false, bad = false;
+    sm->mask[lane] = 0;
+    sm->mask[lane + 32] = 0;
+    __syncwarp();
+#pragma unroll
+    for (u32 j = 0; j < 2; j++) {
+        const u32 p = lane + 32 * j;
+        if (p >= np) continue;
+        const u32 qi = p0 + p;
+        const u64 pw = ld_vol64(&V.q_push[qi]);
+        const u32 tail0 = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
+        const u64 tk = V.q_taken[qi];
+        u64 seen = 0;                   // egresses this ingress already offers a packet
+        u32 x = (u32)V.q_pop[qi];
+        for (u32 n = 0; x != tail0 && n < cap; n++, x++) {  // a buffer holds at most cap
+            const u32 sl = slot_ix(x, cap);
+            if ((tk >> sl) & 1ull) continue;
+            const uint4 pk = V.slots[(u64)qi * cap + sl];
+            if (pk.x > t) { nxt = min(nxt, pk.x); break; }
+            ready_any = true;
+            const u32 e = route_port(V, s, p0, pk);
+            if (e >= np) { bad = true; continue; }
+            if (!((seen >> e) & 1ull)) {
+                seen |= 1ull << e;
+                atomicOr(&sm->mask[e], 1ull << p);
+            }
+        }
+    }
+    __syncwarp();
+    u64 used = 0;                       // ingresses that sent a packet this tick
+    u32 hops = 0;
+    for (u32 e = 0; e < np; e++) {
+        const unsigned long long M = sm->mask[e] & ~used;
+        u32 took = kUnset;
+        if (M && lane == (e & 31)) {
+            const u32 qe = p0 + e;
+            const uint2 st = V.eg[qe];
+            if (st.x <= t) {
+                const uint4 pr = V.port_rec[qe];    // downstream queue, sigma, delta, its owner
+                const u32 dq = pr.x, sg = pr.y, dl = pr.z;
+                const u32 dtail = (u32)V.q_push[dq];
+                bool ok;
+                if (dq < V.T.nq) {
+                    ok = credit_ok_voq(V, dq, dtail, dl + 1, t);
+                } else {                            // a NIC's receive queue: one pop a tick
+                    const u64 dpop = ld_vol64(&V.q_pop[dq]);
+                    ok = credit_ok(V, dq, dtail, (u32)dpop - ((u32)(dpop >> 32) == t ? 1u : 0u),
+                                   dl + 1, t);
+                }
+                const unsigned long long hi = M & (~0ull << st.y);      // round robin from rr
+                const u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
+                const u32 qin = p0 + i;
+                u64 tk = V.q_taken[qin];
+                const u32 h0 = (u32)V.q_pop[qin];
+                // its oldest packet for e (the plan saw a ready one among the
+                // buffer's cap slots)
+                u32 x = h0, n = 0;
+                uint4 pk = make_uint4(0, 0, 0, 0);
+                if (ok) {
+                    for (; n < cap; n++, x++) {
+                        const u32 sl = slot_ix(x, cap);
+                        if ((tk >> sl) & 1ull) continue;
+                        pk = V.slots[(u64)qin * cap + sl];
+                        if (route_port(V, s, p0, pk) == e) break;
+                    }
+                    if (n == cap) { bad = true; ok = false; }
+                }
+                if (ok) {
+                    pk.x = t + sg + dl;
+                    pk.y += (dl + 1) << 16;
+                    V.slots[(u64)dq * cap + slot_ix(dtail, cap)] = pk;
+                    st_vol64(&V.q_push[dq], ((u64)t << 32) | (u32)(dtail + 1));
+                    V.eg[qe] = make_uint2(t + sg, i + 1 == np ? 0u : i + 1);
+                    // the slot is gone; the head moves past the gone slots
+                    tk |= 1ull << slot_ix(x, cap);
+                    const u32 tl = (u32)V.q_push[qin];
+                    u32 h = h0;
+                    while (h != tl && ((tk >> slot_ix(h, cap)) & 1ull)) {
+                        tk &= ~(1ull << slot_ix(h, cap));
+                        st_vol32(&V.poplog[(u64)qin * V.plog + (h & pm)], t);
+                        h++;
+                    }
+                    V.q_taken[qin] = tk;
+                    if (h != h0) {
+                        __threadfence_block();      // log entries before the head that counts them
+                        st_vol64(&V.q_pop[qin], ((u64)t << 32) | h);
+                    }
+                    if (!(pr.w & 0x80000000u)) atomicMin(&poke[pr.w], pk.x);
+                    else if ((pr.w & 0x7FFFFFFFu) < V.X.nr)
+                        atomicMin(&poke[V.X.nsw + (pr.w & 0x7FFFFFFFu) / 32], pk.x);
+                    pk_min = min(pk_min, pk.x);
+                    hops++;
+                    took = i;
+                }
+            }
+        }
+        took = __shfl_sync(kFull, took, e & 31);
+        if (took != kUnset) used |= 1ull << took;
+    }
+    acc.hops += hops;
+    nxt = __reduce_min_sync(kFull, ready_any ? t + 1 : nxt);   // ready packets: next tick
+    pk_min = __reduce_min_sync(kFull, pk_min);
+    if (__any_sync(kFull, bad)) *fail = min(*fail, kFailSwitch);
+    const u32 w = min(nxt, old > t ? old : kUnset);
     if (lane == 0) V.wake[s] = w;
     __syncwarp();
     return min(w, pk_min);
@@ -1156,7 +1303,8 @@ __device__ __forceinline__ void dag_step(RV &v)
     }
     // Running memberships: an intra-server one can finish whenever its last
     // member has started, so those are checked every tick; a network one
-    // only when a message of this rank's completed (receive sets rdirty).
+    // only once a membership of this rank has no message left (the receive
+    // that takes its count to zero sets rdirty).
     u32 *a = V.act + (u64)v.r * V.X.act_cap;
     u32 w = 0;
     const bool dirty = ld_vol32(&V.rdirty[v.r]) != 0;
@@ -1245,7 +1393,7 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
     const u32 qp = hr.x, hs = hr.y, hd = hr.z;
     u32 head = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
-    if (!credit_ok(V, qp, tail, head, hd + 1, t)) {
+    if (!(X.voq ? credit_ok_voq(V, qp, tail, hd + 1, t) : credit_ok(V, qp, tail, head, hd + 1, t))) {
         v.nxt = min(v.nxt, t + 1);
         return;
     }
@@ -1337,7 +1485,6 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     if (!pk_last(pk)) return;
     v.nxt = min(v.nxt, t + 1);                         // DAG looks at its counts next tick
-    rank_poke(v, rank_item(V, P.node_rank[W_(v).node_off + pk.z]), t + 1);   // the ACK (see below)
     uint2 *ports = V.ports + (u64)v.r * X.port_cap;
     u32 ps = pk_slot(pk);
     uint2 port = ports[ps];
@@ -1348,13 +1495,19 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     const u32 srank = P.node_rank[W_(v).node_off + snd];
     atomicMax(&V.nd_done[own], t);
     __threadfence_block();
-    atomicSub(&V.nd_out[own], 1);
+    const i32 left_own = atomicSub(&V.nd_out[own], 1) - 1;
     atomicMax(&V.nd_done[snd], t + pk_hops(pk));
     __threadfence_block();
-    atomicSub(&V.nd_out[snd], 1);
+    const i32 left_snd = atomicSub(&V.nd_out[snd], 1) - 1;
     __threadfence_block();                 // counts before the flags that announce them
-    atomicOr(&V.rdirty[v.r], 1u);
-    atomicOr(&V.rdirty[srank], 1u);
+    // A membership can only finish when its count reaches zero, so only the
+    // message that takes it there flags its rank for a look at its running
+    // memberships (and, for the sender, wakes its rank group: the ACK).
+    if (left_own == 0) atomicOr(&V.rdirty[v.r], 1u);
+    if (left_snd == 0) {
+        atomicOr(&V.rdirty[srank], 1u);
+        rank_poke(v, rank_item(V, srank), t + 1);
+    }
     v.n_msg++;
     v.dig += mix64(mix64((u64)pk.z | ((u64)pk_key(pk) << 32)) ^ (u64)t);
     u32 idx = atomicAdd(&v.TC->rec_count, 1u);
@@ -1467,6 +1620,7 @@ __device__ const void *global_slice(const Params &P, const ExpRec &X, const Topo
     case IM_POPLOG: return P.poplog + X.plog_off;
     case IM_LHOT: return P.lhot + X.lane_off;
     case IM_LCOLD: return P.lcold + X.lane_off;
+    case IM_TAKEN: return P.q_taken + X.taken_off;
     case IM_SLOTS: return P.slots + X.slot_off;
     case IM_SWREC: return P.sw_rec + T.sw_off;
     case IM_PORTREC: return P.port_rec + T.port_off;
@@ -1500,6 +1654,7 @@ __device__ void set_slice(XV &V, int k, const void *c)
     case IM_POPLOG: V.poplog = (u32 *)p; break;
     case IM_LHOT: V.lhot = (LaneHot *)p; break;
     case IM_LCOLD: V.lcold = (LaneCold *)p; break;
+    case IM_TAKEN: V.q_taken = (u64 *)p; break;
     case IM_SLOTS: V.slots = (uint4 *)p; break;
     case IM_SWREC: V.sw_rec = (const uint2 *)p; break;
     case IM_PORTREC: V.port_rec = (const uint4 *)p; break;
@@ -1537,7 +1692,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
         V.T = P.topo[V.X.topo];
         V.W = P.work[V.X.work];
         V.e = e;
-        V.plog = V.T.plog;
+        V.plog = V.X.plog;
         const ExpCtl c = P.ctl[e];
         TC.end_max1 = c.end_max1;
         TC.rec_count = c.rec_count;
@@ -1591,6 +1746,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
     // queue words in shared memory: a pass reads every free egress's
     // downstream queue words up front instead of after the plan
     const bool qstaged = ((smask >> IM_QPUSH) & (smask >> IM_QPOP) & 1u) != 0;
+    const bool voq = V.X.voq != 0;      // switches keep virtual output queues
     // items are dealt to warps round-robin (item warp + j * nW), so switches
     // and rank groups spread over all warps
     const u32 cnt = warp < nI ? (nI - warp + nW - 1) / nW : 0;
@@ -1631,19 +1787,20 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
             // due switches: the latency build steps them one a pass; the
             // occupancy build packs up to kPack switches and 64 ports a pass
             const bool dsw = due && it < nsw;
-            if (kOnePerPass<VT>::value) {
+            if (kOnePerPass<VT>::value || voq) {
                 u32 Ms1 = __ballot_sync(kFull, dsw);
                 while (Ms1) {
                     const u32 j = (u32)__ffs(Ms1) - 1;
                     Ms1 &= Ms1 - 1;
                     const u32 item = warp + (base + j) * nW;
                     const u32 old = __shfl_sync(kFull, w, j);
-                    rep = min(rep, switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, qstaged));
+                    rep = min(rep, voq ? switch_voq<VT>(V, acc, item, t, old, poke, sm, &fail)
+                                       : switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, qstaged));
                 }
             }
             uint2 sr = make_uint2(0, 0);
-            if (dsw && !kOnePerPass<VT>::value) sr = V.sw_rec[it];
-            u32 Ms = kOnePerPass<VT>::value ? 0u : __ballot_sync(kFull, dsw);
+            if (dsw && !kOnePerPass<VT>::value && !voq) sr = V.sw_rec[it];
+            u32 Ms = (kOnePerPass<VT>::value || voq) ? 0u : __ballot_sync(kFull, dsw);
             u32 n = 0, used = 0;
             while (Ms) {
                 const u32 j = (u32)__ffs(Ms) - 1;

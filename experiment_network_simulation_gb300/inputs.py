@@ -375,6 +375,7 @@ class Experiment:
     ecmp_seed: int = 0
     gpu_mem: int = 80 * 1024 ** 3
     rec_cap: int = 0
+    voq: int = 0                 # 1: switches keep virtual output queues (no head-of-line blocking)
     label: dict = field(default_factory=dict)
 
 
@@ -390,7 +391,7 @@ EXP_FIELDS = [("exp_topo", np.uint32), ("exp_work", np.uint32), ("exp_algo", np.
               ("exp_nc", np.uint32), ("exp_chunk", np.uint64), ("exp_pkt", np.uint32),
               ("exp_cap", np.uint32), ("exp_tick_ps", np.uint32), ("exp_dur_seed", np.uint64),
               ("exp_ecmp_seed", np.uint64), ("exp_gpu_mem", np.uint64),
-              ("exp_rec_cap", np.uint32)]
+              ("exp_rec_cap", np.uint32), ("exp_voq", np.uint32)]
 
 
 class Batch:
@@ -441,7 +442,7 @@ class Batch:
             wi = next(j for j, w in enumerate(self.works) if w is e.work)
             assert e.work.n_ranks <= e.topo.n_hosts
             vals = [ti, wi, e.algo, e.nc, e.chunk, e.pkt, e.cap, e.tick_ps, e.dur_seed,
-                    e.ecmp_seed, e.gpu_mem, e.rec_cap]
+                    e.ecmp_seed, e.gpu_mem, e.rec_cap, e.voq]
             for (f, _), v in zip(EXP_FIELDS, vals):
                 out[f][i] = v
         return out

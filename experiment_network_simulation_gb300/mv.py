@@ -38,7 +38,7 @@ _ARRAYS = [
     ("exp_topo", "u4"), ("exp_work", "u4"), ("exp_algo", "u4"), ("exp_nc", "u4"),
     ("exp_chunk", "u8"), ("exp_pkt", "u4"), ("exp_cap", "u4"), ("exp_tick_ps", "u4"),
     ("exp_dur_seed", "u8"), ("exp_ecmp_seed", "u8"), ("exp_gpu_mem", "u8"),
-    ("exp_rec_cap", "u4")]
+    ("exp_rec_cap", "u4"), ("exp_voq", "u4")]
 _CT = {"u4": _P32, "u8": _P64, "i4": _PI32}
 _NP = {"u4": np.uint32, "u8": np.uint64, "i4": np.int32}
 

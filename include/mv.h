@@ -108,7 +108,9 @@ extern "C" {
  * Experiment e: exp_topo, exp_work, exp_algo, exp_nc (channels, 1..1024),
  * exp_chunk (bytes), exp_pkt (packet bytes), exp_cap (queue slots, 2..1024),
  * exp_tick_ps, exp_dur_seed, exp_ecmp_seed, exp_gpu_mem (bytes per GPU),
- * exp_rec_cap (per-message completion records kept, 0 = none).
+ * exp_rec_cap (per-message completion records kept, 0 = none), exp_voq (the
+ * switches' ingress buffers: 0 = one FIFO per ingress port, head-of-line
+ * blocking kept; 1 = virtual output queues, needs exp_cap <= 64).
  */
 typedef struct mv_batch_desc {
     uint32_t version;                 /* 1 */
@@ -134,6 +136,7 @@ typedef struct mv_batch_desc {
     const uint32_t *exp_pkt, *exp_cap, *exp_tick_ps;
     const uint64_t *exp_dur_seed, *exp_ecmp_seed, *exp_gpu_mem;
     const uint32_t *exp_rec_cap;
+    const uint32_t *exp_voq;
 } mv_batch_desc;
 
 /*

@@ -85,6 +85,7 @@ typedef struct orc_batch {
     const uint32_t *exp_pkt, *exp_cap, *exp_tick_ps;
     const uint64_t *exp_dur_seed, *exp_ecmp_seed, *exp_gpu_mem;
     const uint32_t *exp_rec_cap;
+    const uint32_t *exp_voq;
 } orc_batch;
 
 typedef struct orc_out {
@@ -192,6 +193,8 @@ typedef struct sim {
     uint32_t rdv_delay;             /* 1 + smallest link delta of the topology */
     pkt *slots;                     /* nf * cap */
     uint32_t *eg_busy, *eg_rr;      /* Q */
+    int voq;                        /* switches keep virtual output queues */
+    uint64_t *taken;                /* Q: with VOQs, ring slots already forwarded (by slot) */
     uint32_t *sw_queued;            /* S: packets in the switch's ingress queues */
     nic *nics;                      /* R */
     uint32_t *npred_left, *cand, *start, *end, *port_base, *done_max;
@@ -713,6 +716,82 @@ static void push(sim *s, uint32_t f, const pkt *p, uint32_t t, uint32_t sigma)
     if (f < s->Q) s->sw_queued[s->port_sw[f]]++;
 }
 
+/* Egress qe (egress i of P at its switch) sends packet p, taken from
+ * ingress queue qin at tick t, to its downstream queue d: ready after the
+ * link's serialisation and delay, one (delta + 1) more on the path's
+ * acknowledgement delay; the egress is busy for sigma and its round-robin
+ * pointer moves past the ingress it served. */
+static void send_on(sim *s, uint32_t qe, uint32_t d, pkt p, uint32_t qin, uint32_t i, uint32_t P,
+                    uint32_t t)
+{
+    p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
+    p.hopsum += s->port_delta[qe] + 1;
+    push(s, d, &p, t, s->port_sigma[qe]);
+    ev(s, EV_HOP, qe, qin);
+    s->eg_busy[qe] = t + s->port_sigma[qe];
+    s->eg_rr[qe] = (i + 1) % P;
+    s->pkt_hops++;
+    s->changed = 1;
+}
+
+/* Switch forwarding with virtual output queues (the VOQ variant of the
+ * pull-based forwarding, Multiverse section 4.2): an ingress buffer of cap
+ * slots holds one FIFO per egress.  Plan: for each ingress, the oldest ready
+ * packet for each egress (a buffer's packets are ready in arrival order, so
+ * the scan stops at the first packet that is not).  Pull: the egresses in
+ * index order; a free egress with credit downstream scans the ingress ports
+ * round-robin from its pointer and takes the first one holding a ready
+ * packet for it that no lower egress took a packet from in this tick (an
+ * ingress sends at most one packet a tick).  A packet that leaves from the
+ * middle of the buffer frees its slot when the buffer's head passes it, so
+ * credit counts the span from the head to the tail as in the FIFO switch. */
+static void voq_take(sim *s, uint32_t f, uint32_t x, uint32_t t)
+{
+    s->taken[f] |= 1ull << (x % s->cap);
+    while (s->head[f] != s->tail[f] && ((s->taken[f] >> (s->head[f] % s->cap)) & 1ull)) {
+        s->taken[f] &= ~(1ull << (s->head[f] % s->cap));
+        pop(s, f, t);
+    }
+}
+
+static void forward_voq(sim *s, uint32_t w, uint32_t t)
+{
+    uint32_t P = s->sw_nports[w], base = s->sw_base[w];
+    uint32_t first[64][64];               /* [ingress][egress]: counter of its oldest ready packet */
+    uint32_t wanted[64];
+    memset(wanted, 0, sizeof(uint32_t) * P);
+    for (uint32_t p = 0; p < P; p++) {
+        uint32_t f = base + p;
+        for (uint32_t e = 0; e < P; e++) first[p][e] = UNSET;
+        for (uint32_t x = s->head[f]; x != s->tail0[f]; x++) {
+            if ((s->taken[f] >> (x % s->cap)) & 1ull) continue;
+            pkt *h = slot(s, f, x);
+            if (h->ready > t) break;
+            int32_t e = route_port(s, w, h);
+            if (e < 0) { fail(s, ST_ERROR); continue; }     /* that packet stays */
+            if (first[p][e] == UNSET) { first[p][e] = x; wanted[e]++; }
+        }
+    }
+    uint64_t used = 0;                    /* ingresses a packet left this tick */
+    for (uint32_t e = 0; e != P; e++) {   /* egresses in index order */
+        uint32_t qe = base + e;
+        if (!wanted[e] || t < s->eg_busy[qe]) continue;       /* nothing for it, or busy */
+        uint32_t d = downstream(s, qe);
+        if (!has_credit(s, d, t)) continue;
+        for (uint32_t k = 0; k < P; k++) {
+            uint32_t i = s->eg_rr[qe] + k;         /* round robin from the pointer */
+            if (i >= P) i -= P;
+            if (((used >> i) & 1ull) || first[i][e] == UNSET) continue;
+            pkt p = *slot(s, base + i, first[i][e]);
+            voq_take(s, base + i, first[i][e], t);
+            s->sw_queued[w]--;
+            send_on(s, qe, d, p, base + i, i, P, t);
+            used |= 1ull << i;
+            break;
+        }
+    }
+}
+
 /* Switch forwarding (Multiverse section 4.2, pull-based): plan = for each
  * ingress port, the egress its ready head packet needs; pull = each free
  * egress with credit downstream scans the ingress ports round-robin from its
@@ -720,6 +799,7 @@ static void push(sim *s, uint32_t f, const pkt *p, uint32_t t, uint32_t sigma)
 static void forward(sim *s, uint32_t w, uint32_t t)
 {
     if (s->sw_queued[w] == 0) return;     /* nothing queued: nothing to plan */
+    if (s->voq) { forward_voq(s, w, t); return; }
     uint32_t P = s->sw_nports[w], base = s->sw_base[w];
     int32_t tgt[256];
     uint32_t wanted[256];                 /* how many heads want each egress */
@@ -744,14 +824,7 @@ static void forward(sim *s, uint32_t w, uint32_t t)
             pkt p = *slot(s, base + i, s->head[base + i]);
             pop(s, base + i, t);
             s->sw_queued[w]--;
-            p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
-            p.hopsum += s->port_delta[qe] + 1;
-            push(s, d, &p, t, s->port_sigma[qe]);
-            ev(s, EV_HOP, qe, base + i);
-            s->eg_busy[qe] = t + s->port_sigma[qe];
-            s->eg_rr[qe] = (i + 1) % P;
-            s->pkt_hops++;
-            s->changed = 1;
+            send_on(s, qe, d, p, base + i, i, P, t);
             break;
         }
     }
@@ -968,8 +1041,9 @@ typedef struct offs {
  * 1..65535 members and fewer than 2^40 bytes; every DAG edge joins nodes of
  * one rank and the predecessor counts match the edges; every membership
  * names a node of its own kind and rank; an experiment has 1..1024
- * channels, 2..1024 queue slots and a chunk size whenever a network
- * collective other than the relay needs one. */
+ * channels, 2..1024 queue slots (at most 64 with virtual output queues) and
+ * a chunk size whenever a network collective other than the relay needs
+ * one. */
 static int validate(const orc_batch *b, const offs *o)
 {
     if (b->version != 1 || b->n_topos == 0 || b->n_works == 0) return -2;
@@ -1065,7 +1139,8 @@ static int validate(const orc_batch *b, const offs *o)
         if (ti >= b->n_topos || wi >= b->n_works) return -2;
         if (b->work_nranks[wi] > b->topo_nhosts[ti] || b->exp_algo[e] > A_TREE ||
             b->exp_nc[e] == 0 || b->exp_nc[e] > 1024 || b->exp_pkt[e] == 0 ||
-            b->exp_cap[e] < 2 || b->exp_cap[e] > 1024 || b->exp_tick_ps[e] == 0)
+            b->exp_cap[e] < 2 || b->exp_cap[e] > 1024 || b->exp_tick_ps[e] == 0 ||
+            b->exp_voq[e] > 1 || (b->exp_voq[e] && b->exp_cap[e] > 64))
             return -2;
         if (b->exp_chunk[e] == 0)
             for (uint32_t c = o->coll[wi]; c < o->coll[wi + 1]; c++)
@@ -1169,6 +1244,8 @@ static void sim_setup(sim *s, const orc_batch *b, const offs *o, uint32_t e)
     for (uint32_t f = 0; f < s->nf; f++) s->last_push[f] = UNSET;
     s->eg_busy = calloc(s->Q + 1, sizeof(uint32_t));
     s->eg_rr = calloc(s->Q + 1, sizeof(uint32_t));
+    s->voq = b->exp_voq[e] != 0;
+    s->taken = calloc(s->Q + 1, sizeof(uint64_t));
     s->sw_queued = calloc(s->S + 1, sizeof(uint32_t));
     s->nics = calloc(s->R + 1, sizeof(nic));
     s->npred_left = malloc(sizeof(uint32_t) * (s->NN + 1));
@@ -1200,7 +1277,7 @@ static void sim_teardown(sim *s)
     }
     free(s->head); free(s->tail); free(s->tail0); free(s->slots);
     free(s->poplog); free(s->last_push);
-    free(s->eg_busy); free(s->eg_rr); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
+    free(s->eg_busy); free(s->eg_rr); free(s->taken); free(s->sw_queued); free(s->nics); free(s->npred_left); free(s->cand);
     free(s->start); free(s->end); free(s->port_base); free(s->done_max); free(s->outstanding);
 }
 
@@ -1392,6 +1469,7 @@ void *orc_sim_clone(void *hp)
     s->last_push = dup_bytes(a->last_push, sizeof(uint32_t) * a->nf);
     s->eg_busy = dup_bytes(a->eg_busy, sizeof(uint32_t) * (a->Q + 1));
     s->eg_rr = dup_bytes(a->eg_rr, sizeof(uint32_t) * (a->Q + 1));
+    s->taken = dup_bytes(a->taken, sizeof(uint64_t) * (a->Q + 1));
     s->sw_queued = dup_bytes(a->sw_queued, sizeof(uint32_t) * (a->S + 1));
     s->nics = dup_bytes(a->nics, sizeof(nic) * (a->R + 1));
     s->npred_left = dup_bytes(a->npred_left, sizeof(uint32_t) * (a->NN + 1));

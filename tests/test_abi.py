@@ -101,8 +101,9 @@ def test_library_and_oracle_refuse_the_same_batches():
     """The CUDA library and the CPU oracle take the same inputs: both refuse a
     switch of 65 ports, a link delay of 64 ticks (delay + 1 beyond the
     64-entry pop log), a serialisation time of 65,536 ticks, 1,025 queue
-    slots or channels, and the other malformed descriptors below; both
-    accept the largest legal values (64 ports, delay 63)."""
+    slots or channels, virtual output queues over more than 64 slots, and
+    the other malformed descriptors below; both accept the largest legal
+    values (64 ports, delay 63, 64 slots with virtual output queues)."""
     def one(topo, **kw):
         w = I.lone_message(2, 0, 1, 4096)
         kw.setdefault("chunk", 1 << 20)
@@ -116,6 +117,9 @@ def test_library_and_oracle_refuse_the_same_batches():
     assert _both(one(I.single_switch(4, 1, 0), cap=1025)) == (False, False)
     assert _both(one(I.single_switch(4, 1, 0), nc=1025)) == (False, False)
     assert _both(one(I.single_switch(4, 1, 0), chunk=0)) == (False, False)
+    assert _both(one(I.single_switch(4, 1, 0), cap=64, voq=1)) == (True, True)
+    assert _both(one(I.single_switch(4, 1, 0), cap=65, voq=1)) == (False, False)
+    assert _both(one(I.single_switch(4, 1, 0), voq=2)) == (False, False)
     p = I.config1().pack()
 
     def changed(**changes):
