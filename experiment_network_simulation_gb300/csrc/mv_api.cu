@@ -43,7 +43,8 @@ struct Layout {
         nmemb = 0, na2a = 0, na2a_in = 0;
     u64 route_bytes = 0, q_total = 0, slot_total = 0, plog_total = 0, eg_total = 0,
         rk_total = 0, pend_total = 0, act_total = 0, lane_total = 0, portc_total = 0,
-        nd_total = 0, rec_total = 0, coll_total = 0, taken_total = 0, items = 0;
+        nd_total = 0, rec_total = 0, coll_total = 0, taken_total = 0, items = 0,
+        lcc_total = 0, rcc_total = 0;
     u32 warps = 1, image = 16;      // megakernel block size and shared image budget
     u32 variant = 1;                // 1: every experiment staged whole; 2: some are not
     u32 max_level = 0, max_nodes = 0, max_queues = 0, max_ranks = 0, max_colls = 0;
@@ -56,6 +57,7 @@ struct Layout {
         memb_row, memb_col, node_rank, order;
     std::vector<uint2> sw_rec;
     std::vector<uint4> port_rec, host_rec;
+    std::vector<CcRec> ccrec;
     // regions
     Region r_topo, r_work, r_exp, r_sw_nports, r_sw_level, r_sw_pstart, r_port_sw, r_port_peer,
         r_port_sigma, r_port_delta, r_host_port, r_host_sigma, r_host_delta, r_rank_first,
@@ -65,12 +67,12 @@ struct Layout {
         r_coll_beta_den, r_coll_mstart, r_coll_bytes, r_member_rank, r_member_node,
         r_member_a2a_n, r_memb_row, r_a2a_dst, r_member_a2a_in_n, r_memb_col, r_a2a_in_src,
         r_a2a_bytes, r_a2a_in_bytes, r_mem, r_order, r_node_rank, r_sw_rec, r_port_rec,
-        r_host_rec;
+        r_host_rec, r_ccrec;
     u64 static_bytes = 0;
     Region r_route, r_up_n, r_up_list, r_q_push, r_q_pop, r_q_taken, r_slots, r_eg, r_rk, r_rdirty, r_pend, r_act,
         r_lhot, r_lcold, r_ports, r_poplog, r_nd_pred, r_nd_cand, r_nd_start, r_nd_end, r_nd_pbase, r_nd_done,
         r_nd_out, r_ctl, r_rec_sender, r_rec_key, r_rec_tick, r_coll_start, r_coll_end, r_glob,
-        r_wake;
+        r_wake, r_lcc, r_rcc;
     u64 total = 0;
 
     u64 cur = 0;
@@ -180,6 +182,8 @@ int plan(const mv_batch_desc *d, Layout &L)
         R.nn = d->work_nnodes[w];
         R.ncoll = d->work_ncolls[w];
         R.nmemb = d->work_nmembers[w];
+        // a packet carries its sender's node in 25 bits, kCnpNode reserved
+        if (R.nn >= kCnpNode) return MV_EINVAL;
         R.rank_off = (u32)L.nranks;
         R.node_off = (u32)L.nnodes;
         R.edge_off = (u32)L.nedges;
@@ -364,6 +368,24 @@ int plan(const mv_batch_desc *d, Layout &L)
         // with VOQs several packets can leave an ingress's buffer in one tick, so
         // its pop log keeps the last 64 pops (a whole buffer)
         X.plog = X.voq ? 64u : T.plog;
+        // DCQCN parameters (n_exps records of MV_CC_FIELDS words; NULL: none)
+        if (d->exp_cc) {
+            const u32 *c = d->exp_cc + (u64)MV_CC_FIELDS * e;
+            if (c[0] > 1) return MV_EINVAL;
+            if (c[0]) {
+                CcRec R;
+                std::memset(&R, 0, sizeof R);
+                R.kmin = c[1]; R.kmax = c[2]; R.pmax = c[3]; R.gshift = c[4]; R.n = c[5];
+                R.k = c[6]; R.t = c[7]; R.b = c[8]; R.f = c[9]; R.rai = c[10]; R.rhai = c[11];
+                R.rmin = c[12];
+                if (X.voq || R.kmin > R.kmax || R.pmax > 65536 || R.gshift == 0 || R.gshift > 16 ||
+                    R.n == 0 || R.k == 0 || R.t == 0 || R.b == 0 || R.f > 65535 || R.rai > kLine ||
+                    R.rhai > kLine || R.rmin == 0 || R.rmin > kLine)
+                    return MV_EINVAL;
+                L.ccrec.push_back(R);
+                X.cc = (u32)L.ccrec.size();
+            }
+        }
         // chunk size matters for every kind but the relay
         if (X.chunk == 0) {
             for (u32 c = 0; c < W.ncoll; c++)
@@ -392,10 +414,14 @@ int plan(const mv_batch_desc *d, Layout &L)
         X.rec_off = L.rec_total;
         X.coll_res_off = L.coll_total;
         X.taken_off = L.taken_total;
+        X.lcc_off = L.lcc_total;
+        X.rcc_off = L.rcc_total;
         L.q_total += X.nq;
         L.slot_total += (u64)X.nq * X.cap;
         L.plog_total += (u64)X.nq * X.plog;
         L.taken_total += X.voq ? T.nq : 0;
+        L.lcc_total += X.cc ? (u64)W.nr * X.lane_cap : 0;
+        L.rcc_total += X.cc ? W.nr : 0;
         L.eg_total += T.nq;
         L.rk_total += W.nr;
         L.pend_total += (u64)W.nr * X.pend_cap;
@@ -504,6 +530,7 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_port_rec = L.take(16 * L.nports);
     L.r_host_rec = L.take(16 * L.nhosts);
     L.r_node_rank = L.take(4 * L.nnodes);
+    L.r_ccrec = L.take(sizeof(CcRec) * L.ccrec.size());
     L.static_bytes = L.cur;
     L.r_route = L.take(L.route_bytes);
     L.r_up_n = L.take(L.nsw);
@@ -536,6 +563,8 @@ int plan(const mv_batch_desc *d, Layout &L)
     L.r_coll_end = L.take(4 * L.coll_total);
     L.r_glob = L.take(sizeof(Glob));
     L.r_wake = L.take(12 * L.items);
+    L.r_lcc = L.take(sizeof(LaneCC) * L.lcc_total);
+    L.r_rcc = L.take(sizeof(RankCC) * L.rcc_total);
     L.total = L.cur;
     return MV_OK;
 }
@@ -601,6 +630,9 @@ Params make_params(void *ws, const Layout &L)
     P.q_push = at<u64>(ws, L.r_q_push);
     P.q_pop = at<u64>(ws, L.r_q_pop);
     P.q_taken = at<u64>(ws, L.r_q_taken);
+    P.ccrec = at<CcRec>(ws, L.r_ccrec);
+    P.lcc = at<LaneCC>(ws, L.r_lcc);
+    P.rcc = at<RankCC>(ws, L.r_rcc);
     P.slots = at<uint4>(ws, L.r_slots);
     P.eg = at<uint2>(ws, L.r_eg);
     P.rk = at<RankCtl>(ws, L.r_rk);
@@ -770,6 +802,7 @@ int mv_create(const mv_batch_desc *d, void *ws, uint64_t ws_bytes, void *stream,
     put(img, L.r_a2a_in_bytes, d->a2a_in_bytes, 8 * L.na2a_in);
     put(img, L.r_mem, d->mem, 80 * L.W);
     put(img, L.r_order, L.order.data(), 4ull * L.E);
+    put(img, L.r_ccrec, L.ccrec.data(), sizeof(CcRec) * L.ccrec.size());
     put(img, L.r_sw_rec, L.sw_rec.data(), 8 * L.nsw);
     put(img, L.r_port_rec, L.port_rec.data(), 16 * L.nports);
     put(img, L.r_host_rec, L.host_rec.data(), 16 * L.nhosts);

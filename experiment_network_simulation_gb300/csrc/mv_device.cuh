@@ -62,7 +62,36 @@ struct ExpRec {
     u32 stage_bytes;                // bytes of the whole dynamic state as one shared-memory image
     u32 voq;                        // 1: switches keep virtual output queues
     u32 plog;                       // pop-log entries per queue: the fabric's, or 64 with VOQs
-    u32 pad;
+    u32 cc;                         // DCQCN: 0 = none, else 1 + its parameter record's index
+    u64 lcc_off, rcc_off;           // with DCQCN: its lanes' rate records, its ranks' records
+};
+
+// DCQCN (congestion control) of an experiment, in the simulator's units:
+// marking thresholds (packets) and top probability (2^-16), gain shift,
+// notification gap N, alpha timer K and rate timer T (ticks), byte counter
+// B (packets), fast-recovery count F, additive / hyper / minimum rate
+// (2^-20 of the line rate).
+struct CcRec {
+    u32 kmin, kmax, pmax, gshift, n, k, t, b, f, rai, rhai, rmin, pad[4];
+};
+constexpr u32 kLine = 1u << 20;      // the line rate (and alpha = 1) in DCQCN units
+
+// A send lane's DCQCN reaction-point state (32 bytes, beside its hot and
+// cold records): a = current rate, target rate, alpha, earliest tick of its
+// next packet; b = alpha timer's and rate timer's last expiry, rate-timer
+// events | byte-counter events << 16, packets since the last byte event.
+struct LaneCC {
+    uint4 a, b;
+};
+
+// A rank's DCQCN notification-point state: the last notification per flow
+// (direct-mapped by key mod 64: key | 1 << 31, tick) and the ring of
+// notifications waiting to be sent (sender rank | its lane << 16, key).
+constexpr u32 kNpTab = 64, kCnpRing = 16;
+struct RankCC {
+    uint2 np[kNpTab];
+    uint2 cq[kCnpRing];
+    u32 head, tail, pad0, pad1;
 };
 
 // One send lane: a stream of messages one rank sends for one channel of one
@@ -150,6 +179,9 @@ struct Params {
     ExpCtl *ctl;
     u32 *rec_sender, *rec_key, *rec_tick;
     u32 *coll_start, *coll_end;  // per experiment and collective: first member start, last end
+    const CcRec *ccrec;      // DCQCN parameter records (ExpRec::cc - 1)
+    LaneCC *lcc;             // per lane of a DCQCN experiment: its reaction point
+    RankCC *rcc;             // per rank of a DCQCN experiment: its notification point
     u32 *wake;               // per experiment: own wake tick of each item, then two poke words each
     u32 n_exps, n_topos;
     Glob *glob;
@@ -163,8 +195,14 @@ struct Params {
 
 // Packet descriptor (16 bytes):
 //   x ready tick | y dst host (16 b) + accumulated (delta+1) over hops (16 b)
-//   z sender node | w connection key (24 b) + last flag (1 b) + receive slot (7 b)
+//   z sender node (25 b) + sender lane (6 b) + congestion mark (1 b)
+//   w connection key (24 b) + last flag (1 b) + receive slot (7 b)
+// A DCQCN notification carries node kCnpNode and the lane it is for.
+constexpr u32 kCnpNode = 0x1FFFFFFu;
 __host__ __device__ inline u32 pk_dst(uint4 p) { return p.y & 0xFFFFu; }
+__host__ __device__ inline u32 pk_node(uint4 p) { return p.z & 0x1FFFFFFu; }
+__host__ __device__ inline u32 pk_lane(uint4 p) { return (p.z >> 25) & 63u; }
+__host__ __device__ inline u32 pk_ecn(uint4 p) { return p.z >> 31; }
 __host__ __device__ inline u32 pk_hops(uint4 p) { return p.y >> 16; }
 __host__ __device__ inline u32 pk_key(uint4 p) { return p.w & 0xFFFFFFu; }
 __host__ __device__ inline u32 pk_last(uint4 p) { return (p.w >> 24) & 1u; }

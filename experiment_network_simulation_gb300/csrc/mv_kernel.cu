@@ -269,8 +269,8 @@ struct XV {
 // compiler loads each field once.
 struct HV {
     struct {
-        u32 algo, nc, pkt, cap, tick_ps, rec_cap, nr, nsw, lane_cap, port_cap, pend_cap, act_cap, voq;
-        u64 chunk, dur_seed, ecmp_seed, rec_off;
+        u32 algo, nc, pkt, cap, tick_ps, rec_cap, nr, nsw, lane_cap, port_cap, pend_cap, act_cap, voq, cc;
+        u64 chunk, dur_seed, ecmp_seed, rec_off, lcc_off, rcc_off;
     } X;
     struct { u32 nh, nq, rdv; } T;
     struct { u32 node_off, edge_off, coll_off, memb_off, a2a_off, a2a_in_off; } W;
@@ -302,6 +302,7 @@ __device__ __forceinline__ HV make_hv(const XV &S)
     V.X.lane_cap = S.X.lane_cap; V.X.port_cap = S.X.port_cap; V.X.pend_cap = S.X.pend_cap;
     V.X.act_cap = S.X.act_cap; V.X.voq = S.X.voq; V.X.chunk = S.X.chunk; V.X.dur_seed = S.X.dur_seed;
     V.X.ecmp_seed = S.X.ecmp_seed; V.X.rec_off = S.X.rec_off;
+    V.X.cc = S.X.cc; V.X.lcc_off = S.X.lcc_off; V.X.rcc_off = S.X.rcc_off;
     V.T.nh = S.T.nh; V.T.nq = S.T.nq; V.T.rdv = S.T.rdv;
     V.W.node_off = S.W.node_off; V.W.edge_off = S.W.edge_off; V.W.coll_off = S.W.coll_off;
     V.W.memb_off = S.W.memb_off; V.W.a2a_off = S.W.a2a_off; V.W.a2a_in_off = S.W.a2a_in_off;
@@ -414,6 +415,123 @@ __device__ __forceinline__ u32 route_port(const VW &V, u32 s, u32 p0, uint4 pk)
     if (nup == 0) return 0xFFu;
     u64 h = mix64((u64)pk_key(pk) ^ ((u64)s << 40) ^ V.X.ecmp_seed);
     return V.up_list[p0 + mod_small(h, nup)];
+}
+
+// ---------------------------------------------------------------- DCQCN
+// Reaction point of a send lane (DCQCN, Zhu et al., SIGCOMM 2015; rates and
+// alpha in units of 2^-20).  The state changes at notifications, at packets
+// sent and at timer expiries; expiries are applied in time order whenever
+// the lane's rate is about to be used, which is exact because nothing else
+// reads it in between.
+struct CcState {
+    u32 rc, rt, alpha, next_tx, abase, rbase, tc, bc, sent;
+};
+__device__ __forceinline__ CcState cc_load(const LaneCC *p)
+{
+    const uint4 a = p->a, b = p->b;
+    return CcState{a.x, a.y, a.z, a.w, b.x, b.y, b.z & 0xFFFFu, b.z >> 16, b.w};
+}
+__device__ __forceinline__ void cc_store(LaneCC *p, const CcState &S)
+{
+    p->a = make_uint4(S.rc, S.rt, S.alpha, S.next_tx);
+    p->b = make_uint4(S.abase, S.rbase, S.tc | (S.bc << 16), S.sent);
+}
+
+// A rate increase event: fast recovery while both event counts are below F,
+// hyper increase once both exceed it, additive increase otherwise; the
+// current rate moves halfway to the target, rounded up.
+__device__ __forceinline__ void cc_increase(const CcRec &C, CcState &S)
+{
+    const u32 mx = max(S.tc, S.bc), mn = min(S.tc, S.bc);
+    u64 rt = S.rt;
+    if (mx < C.f) {
+    } else if (mn > C.f) {
+        rt += (u64)(mn - C.f) * C.rhai;
+    } else {
+        rt += C.rai;
+    }
+    S.rt = rt > kLine ? kLine : (u32)rt;
+    S.rc = (S.rt + S.rc + 1) / 2;
+}
+
+// Timer expiries up to tick t (alpha first on a tie): alpha decays every K
+// ticks, the rate timer fires every T ticks.  Once neither can change
+// anything but the timers' phase, the rest are counted in one step.  The
+// loop runs at most (t - last expiry) / min(K, T) times.
+__device__ __noinline__ void cc_catch_up(const CcRec &C, CcState &S, u32 t)
+{
+    for (;;) {
+        if ((S.alpha >> C.gshift) == 0 && S.rc == kLine && S.rt == kLine) {
+            if (t >= S.abase) S.abase += (t - S.abase) / C.k * C.k;
+            if (t >= S.rbase) {
+                const u32 n = (t - S.rbase) / C.t;
+                S.rbase += n * C.t;
+                S.tc = S.tc + n > 0xFFFFu ? 0xFFFFu : S.tc + n;
+            }
+            return;
+        }
+        const u64 ta = (u64)S.abase + C.k, tr = (u64)S.rbase + C.t;
+        if (ta > t && tr > t) return;
+        if (ta <= tr) {
+            S.alpha -= S.alpha >> C.gshift;
+            S.abase = (u32)ta;
+        } else {
+            S.rbase = (u32)tr;
+            if (S.tc < 0xFFFFu) S.tc++;
+            cc_increase(C, S);
+        }
+    }
+}
+
+// A notification taken at tick t: target = current rate, the current rate
+// drops by alpha / 2 (not below Rmin), alpha moves toward 1 by g, the timers
+// and the byte counter restart.
+__device__ __noinline__ void cc_cut(const CcRec &C, CcState &S, u32 t)
+{
+    cc_catch_up(C, S, t);
+    S.rt = S.rc;
+    const u32 dec = (u32)(((u64)S.rc * S.alpha) >> 21);
+    S.rc = S.rc - dec < C.rmin ? C.rmin : S.rc - dec;
+    S.alpha = S.alpha - (S.alpha >> C.gshift) + (kLine >> C.gshift);
+    if (S.alpha > kLine) S.alpha = kLine;
+    S.abase = S.rbase = t;
+    S.tc = S.bc = S.sent = 0;
+}
+
+// The lane sent a packet at tick t over an uplink of serialisation sigma.
+__device__ __noinline__ void cc_sent(const CcRec &C, CcState &S, u32 sigma, u32 t)
+{
+    cc_catch_up(C, S, t);
+    if (++S.sent >= C.b) {
+        S.sent = 0;
+        if (S.bc < 0xFFFFu) S.bc++;
+        cc_increase(C, S);
+    }
+    S.next_tx = t + (u32)((((u64)sigma << 20) + S.rc - 1) / S.rc);
+}
+
+// Congestion point: a switch forwarding packet pk from ingress queue qin
+// (of cap slots, counters h0..tl at the start of the tick) marks it by the
+// number q of that queue's packets that had arrived by tick t (the packet
+// included; those still on the wire do not count): never at q <= kmin,
+// always above kmax, in between with probability pmax (q - kmin) / (kmax -
+// kmin) drawn from a counter-based hash.  A queue's packets arrive in the
+// order they were pushed, so q is found by bisection.
+__device__ __noinline__ bool ecn_mark(const uint4 *slots, u32 cap, u64 seed, const CcRec &C,
+                                      u32 qin, u32 h0, u32 tl, uint4 pk, u32 t)
+{
+    u32 lo = 0, hi = tl - h0;
+    while (lo < hi) {
+        const u32 mid = (lo + hi) / 2;
+        if (slots[(u64)qin * cap + slot_ix(h0 + mid, cap)].x > t) hi = mid;
+        else lo = mid + 1;
+    }
+    const u32 q = lo;
+    if (q <= C.kmin) return false;
+    if (q > C.kmax) return true;
+    const u64 prob = (u64)C.pmax * (q - C.kmin) / (C.kmax - C.kmin);
+    const u64 u = mix64(mix64(((u64)t << 32) | pk_key(pk)) ^ ((u64)qin << 40) ^ seed) & 0xFFFFu;
+    return u < prob;
 }
 
 // Forwarding for one tick (Multiverse section 4.2) at the n switches of a
@@ -564,7 +682,8 @@ __device__ __forceinline__ u32 switch_pack(const XV &Vs, Acc &acc, u32 n, u32 t,
 // `qstaged`: the queue words are in shared memory.
 template <class VT>
 __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t, u32 old,
-                                           u32 *poke, SwSmem *sm, u32 *fail, bool qstaged)
+                                           u32 *poke, SwSmem *sm, u32 *fail, bool qstaged,
+                                           const CcRec *ccr)
 {
     // the view (see ViewOf): as a register copy, stores through the state
     // pointers cannot alias it, so its fields are loaded once per tick
@@ -647,6 +766,13 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
         uint4 pk = sm->pkt[i];
+        if (ccr && !pk_ecn(pk) && pk_node(pk) != kCnpNode) {
+            // DCQCN marking by the ingress queue the packet leaves
+            const u64 iw = ld_vol64(&V.q_push[p0 + i]);
+            const u32 itl = (u32)iw - ((u32)(iw >> 32) == t ? 1u : 0u);
+            if (ecn_mark(V.slots, cap, V.X.ecmp_seed, *ccr, p0 + i, sm->head[i], itl, pk, t))
+                pk.z |= 1u << 31;
+        }
         pk.x = t + sg + dl;
         pk.y += (dl + 1) << 16;
         V.slots[(u64)dq * cap + slot_ix(dtail, cap)] = pk;
@@ -912,6 +1038,7 @@ struct RankViewT {
     u32 nxt;            // this rank's own next wake
     u32 pk_min;         // earliest wake poked into other items
     u32 n_inj, n_del, n_msg, n_done, end_max1;
+    u32 n_cnp;          // DCQCN notifications sent (packet-hops, not packets injected)
     u64 dig;
     __device__ __forceinline__ RankViewT(const Params *p, VT vv) : P(p), V(vv) {}
 };
@@ -1263,6 +1390,9 @@ __device__ __forceinline__ bool net_join(RV &v, u32 u)
             L.pkts_left = lane_setup(v, L);
             store_lane_hot(&lhot[slot], L);
             store_lane_cold(&lcold[slot], L);
+            if (X.cc)                   // line rate, alpha = 1, timers from the join
+                cc_store(P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + slot,
+                         CcState{kLine, kLine, kLine, 0, v.t, v.t, 0, 0, 0});
             v.C.lane_mask |= 1ull << slot;
             v.C.blocked = 0;
             out += (i32)nm;
@@ -1386,15 +1516,37 @@ __device__ __forceinline__ void dag_step(RV &v)
 template <class RV>
 __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
 {
+    const Params &P = *v.P;
     const auto &V = v.V;
     const auto &X = V.X;
     const u32 t = v.t;
-    if (!v.C.lane_mask || v.C.blocked) return;
+    RankCC *rcc = X.cc ? P.rcc + X.rcc_off + v.r : nullptr;
+    const bool cnp = rcc && rcc->head != rcc->tail;     // DCQCN notifications waiting
+    if ((!v.C.lane_mask || v.C.blocked) && !cnp) return;
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
     const u32 qp = hr.x, hs = hr.y, hd = hr.z;
     u32 head = (u32)pw - ((u32)(pw >> 32) == t ? 1u : 0u);
     if (!(X.voq ? credit_ok_voq(V, qp, tail, hd + 1, t) : credit_ok(V, qp, tail, head, hd + 1, t))) {
         v.nxt = min(v.nxt, t + 1);
+        return;
+    }
+    if (cnp) {
+        // a waiting notification goes first: one packet time, the lane
+        // round-robin pointer stays
+        const uint2 c = rcc->cq[rcc->head % kCnpRing];
+        rcc->head++;
+        uint4 pk;
+        pk.x = t + hs + hd;
+        pk.y = (c.x & 0xFFFFu) | ((hd + 1) << 16);
+        pk.z = kCnpNode | (((c.x >> 16) & 63u) << 25);
+        pk.w = c.y;
+        V.slots[(u64)qp * X.cap + slot_ix(tail, X.cap)] = pk;
+        st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
+        v.C.busy = t + hs;
+        v.n_cnp++;
+        v.changed = true;
+        rank_poke(v, hr.w, pk.x);
+        if (v.C.lane_mask || rcc->head != rcc->tail) v.nxt = min(v.nxt, v.C.busy > t + 1 ? v.C.busy : t + 1);
         return;
     }
     u64 M = v.C.lane_mask;
@@ -1433,16 +1585,31 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
                 L.dslot = ld_vol32(&V.nd_pbase[L.dnode]) + L.dst_port;
                 L.ok_dst = 1;
             }
+            LaneCC *lcc = nullptr;
+            CcState S;
+            if (X.cc) {                 // paced by its DCQCN rate
+                lcc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + l;
+                S = cc_load(lcc);
+                if (S.next_tx > t) {
+                    v.nxt = min(v.nxt, S.next_tx);
+                    timed = true;
+                    continue;
+                }
+            }
             uint4 pk;
             pk.x = t + hs + hd;
             pk.y = L.drank | ((hd + 1) << 16);
-            pk.z = L.node;
+            pk.z = L.node | (l << 25);
             pk.w = L.key | ((L.pkts_left == 1 ? 1u : 0u) << 24) | (L.dslot << 25);
             V.slots[(u64)qp * X.cap + slot_ix(tail, X.cap)] = pk;
             st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
             v.C.busy = t + hs;
             v.C.rr = (l + 1) % kNLane;
             v.n_inj++;
+            if (lcc) {
+                cc_sent(P.ccrec[X.cc - 1], S, hs, t);
+                cc_store(lcc, S);
+            }
             v.changed = true;
             rank_poke(v, hr.w, pk.x);
             if (--L.pkts_left == 0) {           // the message is out: the next one
@@ -1480,9 +1647,42 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     if (pk.x > t) { v.nxt = min(v.nxt, pk.x); return; }
     st_vol32(&V.poplog[(u64)ql * V.plog + (head & (V.plog - 1))], t);
     st_vol64(&V.q_pop[ql], ((u64)t << 32) | (u32)(head + 1));
-    v.n_del++;
     v.changed = true;
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
+    const u32 snd = pk_node(pk);
+    if (snd == kCnpNode) {
+        // DCQCN reaction point: the notification reaches the lane it names
+        // if that lane still carries the flow
+        const u32 l = pk_lane(pk);
+        if ((v.C.lane_mask >> l) & 1ull) {
+            const LaneReg L = load_lane_hot(V.lhot + (u64)v.r * X.lane_cap + l);
+            if (L.key == pk_key(pk)) {
+                LaneCC *lcc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + l;
+                CcState S = cc_load(lcc);
+                cc_cut(P.ccrec[X.cc - 1], S, t);
+                cc_store(lcc, S);
+            }
+        }
+        return;
+    }
+    v.n_del++;
+    if (pk_ecn(pk)) {
+        // DCQCN notification point: at most one notification a flow per N
+        // ticks (the last one per flow, direct-mapped by key); it waits in
+        // this rank's ring (a full ring drops it) for the uplink
+        RankCC *rcc = P.rcc + X.rcc_off + v.r;
+        const u32 key = pk_key(pk), j = key % kNpTab;
+        const uint2 e = rcc->np[j];
+        const bool again = e.x == (key | 0x80000000u) &&
+                           (u64)t < (u64)e.y + P.ccrec[X.cc - 1].n;
+        if (!again && rcc->tail - rcc->head < kCnpRing) {
+            rcc->np[j] = make_uint2(key | 0x80000000u, t);
+            rcc->cq[rcc->tail % kCnpRing] =
+                make_uint2(P.node_rank[W_(v).node_off + snd] | (pk_lane(pk) << 16), key);
+            rcc->tail++;
+            v.nxt = min(v.nxt, t + 1);
+        }
+    }
     if (!pk_last(pk)) return;
     v.nxt = min(v.nxt, t + 1);                         // DAG looks at its counts next tick
     uint2 *ports = V.ports + (u64)v.r * X.port_cap;
@@ -1491,7 +1691,7 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     port.x++;
     ports[ps] = port;
     v.C.blocked = 0;
-    u32 own = port.y, snd = pk.z;
+    u32 own = port.y;
     const u32 srank = P.node_rank[W_(v).node_off + snd];
     atomicMax(&V.nd_done[own], t);
     __threadfence_block();
@@ -1509,10 +1709,10 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
         rank_poke(v, rank_item(V, srank), t + 1);
     }
     v.n_msg++;
-    v.dig += mix64(mix64((u64)pk.z | ((u64)pk_key(pk) << 32)) ^ (u64)t);
+    v.dig += mix64(mix64((u64)snd | ((u64)pk_key(pk) << 32)) ^ (u64)t);
     u32 idx = atomicAdd(&v.TC->rec_count, 1u);
     if (idx < X.rec_cap) {
-        P.rec_sender[X.rec_off + idx] = pk.z;
+        P.rec_sender[X.rec_off + idx] = snd;
         P.rec_key[X.rec_off + idx] = pk_key(pk);
         P.rec_tick[X.rec_off + idx] = t;
     }
@@ -1536,7 +1736,7 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
     v.changed = v.fail_over = v.fail_err = false;
     v.nxt = kUnset;
     v.pk_min = kUnset;
-    v.n_inj = v.n_del = v.n_msg = v.n_done = v.end_max1 = 0;
+    v.n_inj = v.n_del = v.n_msg = v.n_done = v.end_max1 = v.n_cnp = 0;
     v.dig = 0;
     if (v.r < V.X.nr) {
         // issue the independent loads together: control word, uplink record,
@@ -1572,7 +1772,7 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
     if (lane == 0) V.wake[it] = w;
     // counters per lane; summed over the warp once per experiment
     acc.inj += v.n_inj;
-    acc.hops += v.n_inj;
+    acc.hops += v.n_inj + v.n_cnp;
     acc.del += v.n_del;
     acc.msg += v.n_msg;
     acc.dig += v.dig;
@@ -1747,6 +1947,9 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
     // downstream queue words up front instead of after the plan
     const bool qstaged = ((smask >> IM_QPUSH) & (smask >> IM_QPOP) & 1u) != 0;
     const bool voq = V.X.voq != 0;      // switches keep virtual output queues
+    // with DCQCN a warp forwards one switch a pass (marking reads the queue)
+    const CcRec *ccr = V.X.cc ? P.ccrec + (V.X.cc - 1) : nullptr;
+    const bool onepass = voq || ccr != nullptr;
     // items are dealt to warps round-robin (item warp + j * nW), so switches
     // and rank groups spread over all warps
     const u32 cnt = warp < nI ? (nI - warp + nW - 1) / nW : 0;
@@ -1787,7 +1990,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
             // due switches: the latency build steps them one a pass; the
             // occupancy build packs up to kPack switches and 64 ports a pass
             const bool dsw = due && it < nsw;
-            if (kOnePerPass<VT>::value || voq) {
+            if (kOnePerPass<VT>::value || onepass) {
                 u32 Ms1 = __ballot_sync(kFull, dsw);
                 while (Ms1) {
                     const u32 j = (u32)__ffs(Ms1) - 1;
@@ -1795,12 +1998,13 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                     const u32 item = warp + (base + j) * nW;
                     const u32 old = __shfl_sync(kFull, w, j);
                     rep = min(rep, voq ? switch_voq<VT>(V, acc, item, t, old, poke, sm, &fail)
-                                       : switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, qstaged));
+                                       : switch_tick<VT>(V, acc, item, t, old, poke, sm, &fail, qstaged,
+                                                         ccr));
                 }
             }
             uint2 sr = make_uint2(0, 0);
-            if (dsw && !kOnePerPass<VT>::value && !voq) sr = V.sw_rec[it];
-            u32 Ms = (kOnePerPass<VT>::value || voq) ? 0u : __ballot_sync(kFull, dsw);
+            if (dsw && !kOnePerPass<VT>::value && !onepass) sr = V.sw_rec[it];
+            u32 Ms = (kOnePerPass<VT>::value || onepass) ? 0u : __ballot_sync(kFull, dsw);
             u32 n = 0, used = 0;
             while (Ms) {
                 const u32 j = (u32)__ffs(Ms) - 1;

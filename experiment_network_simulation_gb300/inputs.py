@@ -376,7 +376,59 @@ class Experiment:
     gpu_mem: int = 80 * 1024 ** 3
     rec_cap: int = 0
     voq: int = 0                 # 1: switches keep virtual output queues (no head-of-line blocking)
+    cc: "DCQCN | None" = None    # congestion control (None: lossless credit only)
     label: dict = field(default_factory=dict)
+
+
+CC_FIELDS = 16
+CC_LINE = 1 << 20                # the line rate in DCQCN rate units
+
+
+@dataclass
+class DCQCN:
+    """DCQCN parameters in the simulator's units (an experiment's `cc`).
+
+    DCQCN (Zhu et al., SIGCOMM 2015; the Multiverse page names it in its
+    implementation section without parameters): switches mark packets by
+    RED on queue occupancy (kmin, kmax in packets, pmax in units of 2^-16),
+    receivers send congestion notifications (at most one a flow per n
+    ticks), senders cut and recover their rate (gain 2^-gshift; alpha timer
+    k and rate timer t in ticks, byte counter b in packets, fast recovery
+    count f, additive / hyper / minimum rates in units of 2^-20 of the line
+    rate)."""
+    kmin: int = 1
+    kmax: int = 49
+    pmax: int = 655                  # 1 %
+    gshift: int = 8                  # g = 1/256
+    n: int = 611
+    k: int = 672
+    t: int = 672
+    b: int = 2560
+    f: int = 5
+    rai: int = 105
+    rhai: int = 1049
+    rmin: int = 1049
+
+    def words(self) -> list[int]:
+        w = [1, self.kmin, self.kmax, self.pmax, self.gshift, self.n, self.k, self.t, self.b,
+             self.f, self.rai, self.rhai, self.rmin]
+        return w + [0] * (CC_FIELDS - len(w))
+
+
+def dcqcn(tick_ps: int, pkt: int = 4096, line_gbps: float = 400.0, **over) -> DCQCN:
+    """Synthetic DCQCN settings converted to ticks, packets and rate units:
+    marking from 5 KB to 200 KB of queue with 1 % at the top, g = 1/256, a
+    notification gap of 50 us, alpha and rate timers of 55 us, a byte
+    counter of 10 MB, five fast-recovery steps, additive increase 40 Mb/s,
+    hyper increase 400 Mb/s and a floor of 0.1 % of the line rate."""
+    us = lambda x: -(-int(x * 1_000_000) // tick_ps)       # ceil(x us / tick)
+    rate = lambda mbps: max(1, round(CC_LINE * mbps / (line_gbps * 1000)))
+    c = DCQCN(kmin=max(0, 5 * 1000 // pkt), kmax=max(1, 200 * 1000 // pkt), pmax=655, gshift=8,
+              n=us(50), k=us(55), t=us(55), b=max(1, 10 * 1024 * 1024 // pkt), f=5,
+              rai=rate(40), rhai=rate(400), rmin=max(1, CC_LINE // 1000))
+    for key, v in over.items():
+        setattr(c, key, v)
+    return c
 
 
 TOPO_FIELDS = ["sw_nports", "sw_level", "port_peer", "port_sigma", "port_delta",
@@ -437,6 +489,7 @@ class Batch:
             out[f] = np.concatenate([a[f] for a in wa]).astype(wa[0][f].dtype)
         for f, dt in EXP_FIELDS:
             out[f] = np.zeros(len(self.experiments), dt)
+        out["exp_cc"] = np.zeros(len(self.experiments) * CC_FIELDS, np.uint32)
         for i, e in enumerate(self.experiments):
             ti = next(j for j, t in enumerate(self.topos) if t is e.topo)
             wi = next(j for j, w in enumerate(self.works) if w is e.work)
@@ -445,6 +498,8 @@ class Batch:
                     e.ecmp_seed, e.gpu_mem, e.rec_cap, e.voq]
             for (f, _), v in zip(EXP_FIELDS, vals):
                 out[f][i] = v
+            if e.cc is not None:
+                out["exp_cc"][i * CC_FIELDS:(i + 1) * CC_FIELDS] = e.cc.words()
         return out
 
     def node_counts(self) -> np.ndarray:

@@ -38,7 +38,8 @@ _ARRAYS = [
     ("exp_topo", "u4"), ("exp_work", "u4"), ("exp_algo", "u4"), ("exp_nc", "u4"),
     ("exp_chunk", "u8"), ("exp_pkt", "u4"), ("exp_cap", "u4"), ("exp_tick_ps", "u4"),
     ("exp_dur_seed", "u8"), ("exp_ecmp_seed", "u8"), ("exp_gpu_mem", "u8"),
-    ("exp_rec_cap", "u4"), ("exp_voq", "u4")]
+    ("exp_rec_cap", "u4"), ("exp_voq", "u4"), ("exp_cc", "u4")]
+CC_FIELDS = 16                     # words of an experiment's DCQCN record (MV_CC_FIELDS)
 _CT = {"u4": _P32, "u8": _P64, "i4": _PI32}
 _NP = {"u4": np.uint32, "u8": np.uint64, "i4": np.int32}
 
@@ -116,7 +117,11 @@ def make_desc(packed: dict):
     d.n_works = len(packed["work_nranks"])
     d.n_exps = len(packed["exp_topo"])
     for n, t in _ARRAYS:
+        if n == "exp_cc" and packed.get(n) is None:
+            continue                              # NULL: no congestion control
         a = np.ascontiguousarray(packed[n], dtype=_NP[t])
+        if n == "exp_cc" and a.size != d.n_exps * CC_FIELDS:
+            raise ValueError(f"exp_cc holds {a.size} words, not {d.n_exps} x {CC_FIELDS}")
         if a.size == 0:
             a = np.zeros(1, _NP[t])
         keep[n] = a

@@ -111,7 +111,22 @@ extern "C" {
  * exp_rec_cap (per-message completion records kept, 0 = none), exp_voq (the
  * switches' ingress buffers: 0 = one FIFO per ingress port, head-of-line
  * blocking kept; 1 = virtual output queues, needs exp_cap <= 64).
+ *
+ * exp_cc (may be NULL: no congestion control anywhere): MV_CC_FIELDS words
+ * per experiment, DCQCN (Zhu et al., SIGCOMM 2015; the Multiverse page,
+ * section 5, names it among the congestion-control algorithms): [0] on (0
+ * or 1), [1] kmin and [2] kmax (switch marking thresholds, arrived packets
+ * in the ingress queue a packet leaves), [3] pmax (marking probability at
+ * kmax, units of 2^-16, <= 65536), [4] gain shift (g = 2^-shift, 1..16),
+ * [5] N (ticks between a flow's notifications, >= 1), [6] K (alpha timer,
+ * ticks, >= 1), [7] T (rate timer, ticks, >= 1), [8] B (byte counter,
+ * packets, >= 1), [9] F (fast-recovery events, <= 65535), [10] R_AI, [11]
+ * R_HAI, [12] R_min (units of 2^-20 of the line rate, <= 2^20; R_min >= 1),
+ * [13..15] zero.  A notification is a packet from the receiver's NIC to
+ * the sender's.  Congestion control with exp_voq = 1 is refused (MV_EINVAL).
+ * A workload holds fewer than 2^25 - 1 nodes.
  */
+#define MV_CC_FIELDS 16
 typedef struct mv_batch_desc {
     uint32_t version;                 /* 1 */
     uint32_t n_topos, n_works, n_exps;
@@ -137,6 +152,7 @@ typedef struct mv_batch_desc {
     const uint64_t *exp_dur_seed, *exp_ecmp_seed, *exp_gpu_mem;
     const uint32_t *exp_rec_cap;
     const uint32_t *exp_voq;
+    const uint32_t *exp_cc;           /* n_exps x MV_CC_FIELDS, or NULL */
 } mv_batch_desc;
 
 /*

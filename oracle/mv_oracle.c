@@ -51,6 +51,8 @@
 #define UNSET 0xFFFFFFFFu
 #define NLANE 64      /* send lanes per NIC (active messages streams)   */
 #define NPORT 128     /* receive counters per rank                      */
+#define NPTAB 64      /* notification-point flow table entries per NIC  */
+#define NCNPQ 16      /* congestion notifications waiting at a NIC      */
 #define NPEND 64      /* scheduled-but-not-started nodes per rank       */
 #define NACT 16       /* running collective memberships per rank        */
 #define TICK_LIMIT 0xFFF00000u   /* largest tick value a run reaches        */
@@ -86,6 +88,7 @@ typedef struct orc_batch {
     const uint64_t *exp_dur_seed, *exp_ecmp_seed, *exp_gpu_mem;
     const uint32_t *exp_rec_cap;
     const uint32_t *exp_voq;
+    const uint32_t *exp_cc;       /* n_exps x CC_FIELDS; NULL: no congestion control */
 } orc_batch;
 
 typedef struct orc_out {
@@ -112,7 +115,18 @@ typedef struct orc_out {
 typedef struct orc_event {
     uint32_t tick, kind, a, b;
 } orc_event;
-enum { EV_START = 1, EV_END = 2, EV_INJECT = 3, EV_HOP = 4, EV_DELIVER = 5, EV_MESSAGE = 6 };
+enum { EV_START = 1, EV_END = 2, EV_INJECT = 3, EV_HOP = 4, EV_DELIVER = 5, EV_MESSAGE = 6,
+       EV_CNP = 7, EV_CUT = 8 };
+
+/* DCQCN parameters of an experiment (CC_FIELDS words each): switch marking
+ * thresholds in packets and the marking probability at kmax (units of
+ * 2^-16); the gain g = 2^-gshift; the notification gap N, the alpha timer
+ * K and the rate timer T in ticks; the byte counter B in packets; the fast
+ * recovery count F; the additive, hyper and minimum rates in units of
+ * 2^-20 of the line rate. */
+enum { CC_ON, CC_KMIN, CC_KMAX, CC_PMAX, CC_GSHIFT, CC_N, CC_K, CC_T, CC_B, CC_F, CC_RAI,
+       CC_RHAI, CC_RMIN, CC_FIELDS = 16 };
+#define CC_LINE (1u << 20)        /* the line rate in rate units */
 #define ORC_NO_SKIP 1u
 
 /* ------------------------------------------------------------------------ */
@@ -132,6 +146,8 @@ static uint32_t umax32(uint32_t a, uint32_t b) { return a > b ? a : b; }
 /* ------------------------------------------------------------------------ */
 typedef struct pkt {
     uint32_t ready, dst, hopsum, sender, pslot, last, key;
+    uint32_t lane, ecn;           /* the sender's lane slot; congestion experienced */
+    uint32_t cnp;                 /* a congestion notification (for lane `lane` of host dst) */
 } pkt;
 
 typedef struct lane {
@@ -140,6 +156,11 @@ typedef struct lane {
     uint32_t m, nmsg, pkts_left;
     uint32_t dst_member, dst_port, dep_base, dep_mask, dep_need, key;
     uint32_t a2a_e, a2a_start;
+    /* DCQCN reaction point: current and target rate, alpha, the earliest
+     * tick of the next packet, the alpha and rate timers' last expiry, the
+     * rate timer and byte counter event counts, and packets since the last
+     * byte-counter event */
+    uint32_t rc, rt, alpha, next_tx, abase, rbase, tc, bc, sent;
 } lane;
 
 typedef struct nic {
@@ -155,6 +176,11 @@ typedef struct nic {
     uint32_t act[NACT];
     int n_act;
     int tick_fail;        /* one of its tables overflowed during this tick  */
+    /* DCQCN notification point: the last notification generated per flow,
+     * in a direct-mapped table (flow key mod NPTAB), and the notifications
+     * waiting to be sent (a ring of NCNPQ) */
+    uint32_t np_key[NPTAB], np_at[NPTAB];
+    uint32_t cq_dst[NCNPQ], cq_lane[NCNPQ], cq_key[NCNPQ], cq_head, cq_tail;
 } nic;
 
 typedef struct sim {
@@ -194,6 +220,7 @@ typedef struct sim {
     pkt *slots;                     /* nf * cap */
     uint32_t *eg_busy, *eg_rr;      /* Q */
     int voq;                        /* switches keep virtual output queues */
+    uint32_t cc[CC_FIELDS];         /* DCQCN parameters (cc[CC_ON] = 0: none) */
     uint64_t *taken;                /* Q: with VOQs, ring slots already forwarded (by slot) */
     uint32_t *sw_queued;            /* S: packets in the switch's ingress queues */
     nic *nics;                      /* R */
@@ -561,6 +588,8 @@ static void net_join(sim *s, uint32_t r, uint32_t u, uint32_t t)
             L->used = 1;
             L->node = u; L->member = i; L->chan = ch; L->kind = k;
             L->m = 0; L->nmsg = nm;
+            L->rc = L->rt = L->alpha = CC_LINE;
+            L->abase = L->rbase = t;
             L->pkts_left = lane_setup(s, L);
             n->n_lanes++;
             n->used_mask |= 1ULL << slot;
@@ -569,7 +598,6 @@ static void net_join(sim *s, uint32_t r, uint32_t u, uint32_t t)
     }
     s->outstanding[u] = out;
     s->done_max[u] = t;
-    (void)t;
 }
 
 static void free_ports(sim *s, uint32_t r, uint32_t u)
@@ -716,6 +744,122 @@ static void push(sim *s, uint32_t f, const pkt *p, uint32_t t, uint32_t sigma)
     if (f < s->Q) s->sw_queued[s->port_sw[f]]++;
 }
 
+/* ------------------------------------------------------------------------ */
+/* DCQCN (Zhu et al., SIGCOMM 2015, an outside source: the Multiverse page
+ * only names the algorithm).  Congestion point: the switch is input-queued,
+ * so the packets waiting for a congested egress sit in the ingress queues
+ * that feed it; a switch marks a packet it forwards when the ingress queue
+ * it leaves held more than kmin arrived (ready) packets at the start of the
+ * tick, counting the packet itself: with probability
+ * pmax (q - kmin) / (kmax - kmin) up to kmax and always above it.  The draw
+ * is a counter-based hash of the tick, the flow key, the queue and the
+ * experiment's seed. */
+static uint32_t head_at_tick_start(sim *s, uint32_t f, uint32_t t)
+{
+    uint32_t h = s->head[f];
+    return (h > 0 && s->poplog[(size_t)f * 64 + (h - 1) % 64] == t) ? h - 1 : h;
+}
+
+static uint32_t ecn_mark(sim *s, uint32_t qin, const pkt *p, uint32_t t)
+{
+    uint32_t q = 0;
+    for (uint32_t x = head_at_tick_start(s, qin, t); x != s->tail0[qin]; x++) {
+        if (slot(s, qin, x)->ready > t) break;        /* still on the wire */
+        q++;
+    }
+    if (q <= s->cc[CC_KMIN]) return 0;
+    if (q > s->cc[CC_KMAX]) return 1;
+    uint64_t prob = (uint64_t)s->cc[CC_PMAX] * (q - s->cc[CC_KMIN]) /
+                    (s->cc[CC_KMAX] - s->cc[CC_KMIN]);
+    uint64_t u = mix64(mix64(((uint64_t)t << 32) | p->key) ^ ((uint64_t)qin << 40) ^ s->ecmp_seed) &
+                 0xFFFFu;
+    return u < prob;
+}
+
+/* Reaction point.  A rate increase event (the rate timer expired or B more
+ * packets went out): fast recovery while both event counts are below F,
+ * hyper increase once both exceed it, additive increase otherwise; the
+ * current rate then moves halfway to the target, rounded up so that it
+ * reaches the target. */
+static void cc_increase(sim *s, lane *L)
+{
+    uint32_t mx = L->tc > L->bc ? L->tc : L->bc, mn = L->tc < L->bc ? L->tc : L->bc;
+    uint32_t F = s->cc[CC_F];
+    uint64_t rt = L->rt;
+    if (mx < F) {
+        /* fast recovery: the target stays */
+    } else if (mn > F) {
+        rt += (uint64_t)(mn - F) * s->cc[CC_RHAI];
+    } else {
+        rt += s->cc[CC_RAI];
+    }
+    L->rt = rt > CC_LINE ? CC_LINE : (uint32_t)rt;
+    L->rc = (L->rt + L->rc + 1) / 2;
+}
+
+/* The timer events up to tick t, in time order (alpha first on a tie):
+ * every K ticks without a notification alpha decays by the factor 1 - g;
+ * every T ticks the rate timer fires a rate increase event.  Once alpha no
+ * longer moves and both rates are at line rate, later events change
+ * nothing but the timers' phase, so they are counted in one step. */
+static void cc_catch_up(sim *s, lane *L, uint32_t t)
+{
+    const uint32_t K = s->cc[CC_K], T = s->cc[CC_T], gs = s->cc[CC_GSHIFT];
+    for (;;) {
+        if ((L->alpha >> gs) == 0 && L->rc == CC_LINE && L->rt == CC_LINE) {
+            if (t >= L->abase) L->abase += (t - L->abase) / K * K;
+            if (t >= L->rbase) {
+                uint32_t n = (t - L->rbase) / T;
+                L->rbase += n * T;
+                L->tc = L->tc + n > 0xFFFFu ? 0xFFFFu : L->tc + n;
+            }
+            return;
+        }
+        uint64_t ta = (uint64_t)L->abase + K, tr = (uint64_t)L->rbase + T;
+        if (ta > t && tr > t) return;
+        if (ta <= tr) {
+            L->alpha -= L->alpha >> gs;
+            L->abase = (uint32_t)ta;
+        } else {
+            L->rbase = (uint32_t)tr;
+            if (L->tc < 0xFFFFu) L->tc++;
+            cc_increase(s, L);
+        }
+    }
+}
+
+/* A congestion notification reaching the lane at tick t: the target rate
+ * becomes the current rate, the current rate drops by the factor
+ * 1 - alpha/2 (not below the minimum rate), alpha moves to
+ * (1 - g) alpha + g, and both timers and the byte counter restart. */
+static void cc_cut(sim *s, lane *L, uint32_t r, uint32_t t)
+{
+    cc_catch_up(s, L, t);
+    const uint32_t gs = s->cc[CC_GSHIFT];
+    L->rt = L->rc;
+    uint32_t dec = (uint32_t)(((uint64_t)L->rc * L->alpha) >> 21);
+    L->rc = L->rc - dec < s->cc[CC_RMIN] ? s->cc[CC_RMIN] : L->rc - dec;
+    L->alpha = L->alpha - (L->alpha >> gs) + (CC_LINE >> gs);
+    if (L->alpha > CC_LINE) L->alpha = CC_LINE;
+    L->abase = L->rbase = t;
+    L->tc = L->bc = L->sent = 0;
+    ev(s, EV_CUT, r, L->rc);
+}
+
+/* The lane sent a packet at tick t over an uplink of serialisation sigma:
+ * the byte counter may fire a rate increase; the next packet may leave
+ * once a packet's time at the current rate has passed. */
+static void cc_sent(sim *s, lane *L, uint32_t sigma, uint32_t t)
+{
+    cc_catch_up(s, L, t);
+    if (++L->sent >= s->cc[CC_B]) {
+        L->sent = 0;
+        if (L->bc < 0xFFFFu) L->bc++;
+        cc_increase(s, L);
+    }
+    L->next_tx = t + (uint32_t)((((uint64_t)sigma << 20) + L->rc - 1) / L->rc);
+}
+
 /* Egress qe (egress i of P at its switch) sends packet p, taken from
  * ingress queue qin at tick t, to its downstream queue d: ready after the
  * link's serialisation and delay, one (delta + 1) more on the path's
@@ -724,6 +868,7 @@ static void push(sim *s, uint32_t f, const pkt *p, uint32_t t, uint32_t sigma)
 static void send_on(sim *s, uint32_t qe, uint32_t d, pkt p, uint32_t qin, uint32_t i, uint32_t P,
                     uint32_t t)
 {
+    if (s->cc[CC_ON] && !p.ecn && !p.cnp) p.ecn = ecn_mark(s, qin, &p, t);
     p.ready = t + s->port_sigma[qe] + s->port_delta[qe];
     p.hopsum += s->port_delta[qe] + 1;
     push(s, d, &p, t, s->port_sigma[qe]);
@@ -837,9 +982,29 @@ static void forward(sim *s, uint32_t w, uint32_t t)
 static void inject(sim *s, uint32_t r, uint32_t t)
 {
     nic *n = &s->nics[r];
-    if (n->n_lanes == 0 || n->busy > t) return;
+    int cnps = n->cq_head != n->cq_tail;
+    if ((n->n_lanes == 0 && !cnps) || n->busy > t) return;
     uint32_t f = s->host_port[r];
     if (!has_credit(s, f, t)) return;
+    if (cnps) {
+        /* a waiting congestion notification goes first; it takes one
+         * packet time and leaves the round-robin pointer where it is */
+        uint32_t k = n->cq_head++ % NCNPQ;
+        const uint32_t sg = s->host_sigma[r], dl = s->host_delta[r];
+        pkt p;
+        memset(&p, 0, sizeof p);
+        p.ready = t + sg + dl;
+        p.dst = n->cq_dst[k];
+        p.hopsum = dl + 1;
+        p.key = n->cq_key[k];
+        p.lane = n->cq_lane[k];
+        p.cnp = 1;
+        push(s, f, &p, t, sg);
+        n->busy = t + sg;
+        s->pkt_hops++;
+        s->changed = 1;
+        return;
+    }
     /* occupied slots in round-robin order from the pointer: those at or
      * after it, then those before it */
     for (int pass = 0; pass < 2; pass++) {
@@ -858,6 +1023,7 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             /* rendezvous: the destination's join reaches this rank one
              * link latency (1 + smallest delta) after it happened */
             if (s->start[dnode] == UNSET || s->start[dnode] + s->rdv_delay > t) continue;
+            if (s->cc[CC_ON] && L->next_tx > t) continue;       /* paced by its rate */
             pkt p;
             p.ready = t + s->host_sigma[r] + s->host_delta[r];
             p.dst = mrank(s, c, L->dst_member);
@@ -866,7 +1032,10 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             p.pslot = s->port_base[dnode] + L->dst_port;
             p.last = L->pkts_left == 1;
             p.key = L->key;
+            p.lane = q;
+            p.ecn = p.cnp = 0;
             push(s, f, &p, t, s->host_sigma[r]);
+            if (s->cc[CC_ON]) cc_sent(s, L, s->host_sigma[r], t);
             ev(s, EV_INJECT, r, p.key);
             n->busy = t + s->host_sigma[r];
             n->rr = (q + 1) % NLANE;
@@ -895,12 +1064,36 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     pkt p = *h;
     if (p.dst != r) s->violations++;
     pop(s, f, t);
-    s->pkts_delivered++;
     s->changed = 1;
+    nic *n = &s->nics[r];
+    if (p.cnp) {
+        /* reaction point: the notification reaches the lane it names; one
+         * meant for an earlier flow of that slot is dropped */
+        lane *L = &n->lanes[p.lane];
+        if (L->used && L->key == p.key) cc_cut(s, L, r, t);
+        return;
+    }
+    s->pkts_delivered++;
     ev(s, EV_DELIVER, r, p.sender);
+    if (p.ecn) {
+        /* notification point: at most one notification a flow per N ticks
+         * (the flow's table entry remembers the last one); it waits in the
+         * NIC's notification ring, which drops it when full */
+        uint32_t j = p.key % NPTAB;
+        if (!(n->np_key[j] == p.key && n->np_at[j] != UNSET &&
+              (uint64_t)t < (uint64_t)n->np_at[j] + s->cc[CC_N]) &&
+            n->cq_tail - n->cq_head < NCNPQ) {
+            n->np_key[j] = p.key;
+            n->np_at[j] = t;
+            uint32_t k = n->cq_tail++ % NCNPQ;
+            n->cq_dst[k] = s->node_rank[p.sender];
+            n->cq_lane[k] = p.lane;
+            n->cq_key[k] = p.key;
+            ev(s, EV_CNP, r, p.key);
+        }
+    }
     if (!p.last) return;
     ev(s, EV_MESSAGE, r, p.sender);
-    nic *n = &s->nics[r];
     n->port_count[p.pslot]++;
     uint32_t own = n->port_node[p.pslot];
     s->outstanding[own]--;
@@ -961,6 +1154,13 @@ static uint32_t next_event(sim *s, uint32_t t)
             if (at < best) best = at;
         }
     }
+    /* a paced lane's next packet */
+    if (s->cc[CC_ON])
+        for (uint32_t r = 0; r < s->R; r++)
+            for (int q = 0; q < NLANE; q++) {
+                lane *L = &s->nics[r].lanes[q];
+                if (L->used && L->next_tx > t && L->next_tx < best) best = L->next_tx;
+            }
     /* a destination's join still on its way to a sending rank */
     for (uint32_t r = 0; r < s->R; r++) {
         nic *n = &s->nics[r];
@@ -1077,6 +1277,7 @@ static int validate(const orc_batch *b, const offs *o)
     }
     for (uint32_t w = 0; w < b->n_works; w++) {
         uint32_t nr = b->work_nranks[w], nn = b->work_nnodes[w], nco = b->work_ncolls[w];
+        if (nn >= (1u << 25) - 1) return -2;  /* a packet names its sender's node in 25 bits */
         const uint32_t *cnt = b->rank_nnodes + o->rank[w];
         const uint32_t *kind = b->node_kind + o->node[w], *arg = b->node_arg + o->node[w];
         const uint32_t *nsucc = b->node_nsucc + o->node[w], *succ = b->succ + o->edge[w];
@@ -1142,6 +1343,16 @@ static int validate(const orc_batch *b, const offs *o)
             b->exp_cap[e] < 2 || b->exp_cap[e] > 1024 || b->exp_tick_ps[e] == 0 ||
             b->exp_voq[e] > 1 || (b->exp_voq[e] && b->exp_cap[e] > 64))
             return -2;
+        if (b->exp_cc) {
+            const uint32_t *c = b->exp_cc + (size_t)CC_FIELDS * e;
+            if (c[CC_ON] > 1) return -2;
+            if (c[CC_ON] && (b->exp_voq[e] || c[CC_KMIN] > c[CC_KMAX] || c[CC_PMAX] > 65536 ||
+                             c[CC_GSHIFT] == 0 || c[CC_GSHIFT] > 16 || c[CC_N] == 0 ||
+                             c[CC_K] == 0 || c[CC_T] == 0 || c[CC_B] == 0 ||
+                             c[CC_F] > 65535 || c[CC_RAI] > CC_LINE || c[CC_RHAI] > CC_LINE ||
+                             c[CC_RMIN] == 0 || c[CC_RMIN] > CC_LINE))
+                return -2;
+        }
         if (b->exp_chunk[e] == 0)
             for (uint32_t c = o->coll[wi]; c < o->coll[wi + 1]; c++)
                 if (!b->coll_intra[c] && b->coll_kind[c] != C_RELAY) return -2;
@@ -1245,9 +1456,12 @@ static void sim_setup(sim *s, const orc_batch *b, const offs *o, uint32_t e)
     s->eg_busy = calloc(s->Q + 1, sizeof(uint32_t));
     s->eg_rr = calloc(s->Q + 1, sizeof(uint32_t));
     s->voq = b->exp_voq[e] != 0;
+    if (b->exp_cc) memcpy(s->cc, b->exp_cc + (size_t)CC_FIELDS * e, sizeof s->cc);
     s->taken = calloc(s->Q + 1, sizeof(uint64_t));
     s->sw_queued = calloc(s->S + 1, sizeof(uint32_t));
     s->nics = calloc(s->R + 1, sizeof(nic));
+    for (uint32_t r = 0; r <= s->R; r++)
+        for (int j = 0; j < NPTAB; j++) s->nics[r].np_at[j] = UNSET;
     s->npred_left = malloc(sizeof(uint32_t) * (s->NN + 1));
     s->cand = calloc(s->NN + 1, sizeof(uint32_t));
     s->start = malloc(sizeof(uint32_t) * (s->NN + 1));

@@ -44,10 +44,11 @@ _ARR = [("topo_nhosts", "u4"), ("topo_nsw", "u4"), ("topo_nports", "u4"),
         ("exp_topo", "u4"), ("exp_work", "u4"), ("exp_algo", "u4"), ("exp_nc", "u4"),
         ("exp_chunk", "u8"), ("exp_pkt", "u4"), ("exp_cap", "u4"), ("exp_tick_ps", "u4"),
         ("exp_dur_seed", "u8"), ("exp_ecmp_seed", "u8"), ("exp_gpu_mem", "u8"),
-        ("exp_rec_cap", "u4"), ("exp_voq", "u4")]
+        ("exp_rec_cap", "u4"), ("exp_voq", "u4"), ("exp_cc", "u4")]
 _CT = {"u4": _P32, "u8": _P64, "i4": _PI32}
 # event trace records (struct orc_event): kinds and their (a, b) fields
-EV_START, EV_END, EV_INJECT, EV_HOP, EV_DELIVER, EV_MESSAGE = range(1, 7)
+EV_START, EV_END, EV_INJECT, EV_HOP, EV_DELIVER, EV_MESSAGE, EV_CNP, EV_CUT = range(1, 9)
+CC_FIELDS = 16                 # words of an experiment's DCQCN record (exp_cc)
 EVENT = np.dtype([("tick", np.uint32), ("kind", np.uint32), ("a", np.uint32), ("b", np.uint32)])
 _NP = {"u4": np.uint32, "u8": np.uint64, "i4": np.int32}
 
@@ -123,7 +124,11 @@ def _batch(packed: dict):
     b.n_works = len(packed["work_nranks"])
     b.n_exps = len(packed["exp_topo"])
     for n, t in _ARR:
+        if n == "exp_cc" and packed.get(n) is None:
+            continue                              # NULL: no congestion control
         a = np.ascontiguousarray(packed[n], dtype=_NP[t])
+        if n == "exp_cc" and a.size != b.n_exps * CC_FIELDS:
+            raise ValueError(f"exp_cc holds {a.size} words, not {b.n_exps} x {CC_FIELDS}")
         if a.size == 0:
             a = np.zeros(1, _NP[t])
         keep[n] = a
@@ -188,18 +193,7 @@ def run(packed: dict, e0: int = 0, e1: int = 0, limit: int = UNSET - 1,
     no_skip steps every tick instead of jumping over idle ones (same results
     but `ticks_active`, by the skipping rule; a brute-force check of it)."""
     lib = _load(lib_path)
-    keep = {}
-    b = _Batch()
-    b.version = packed["version"]
-    b.n_topos = len(packed["topo_nhosts"])
-    b.n_works = len(packed["work_nranks"])
-    b.n_exps = len(packed["exp_topo"])
-    for n, t in _ARR:
-        a = np.ascontiguousarray(packed[n], dtype=_NP[t])
-        if a.size == 0:
-            a = np.zeros(1, _NP[t])
-        keep[n] = a
-        setattr(b, n, a.ctypes.data_as(_CT[t]))
+    b, keep = _batch(packed)
     E = b.n_exps
     # result sizes; an out-of-range workload index is refused by the oracle
     # itself before it writes anything, so clip it here only to size arrays

@@ -1,0 +1,61 @@
+"""DCQCN congestion control on the CUDA path, bit-exact against the oracle:
+the oracle's DCQCN pin scenarios, seeded random collectives with aggressive
+settings in every kernel build, the GPT DAG at test size and config 1 with
+the generator's DCQCN settings."""
+import numpy as np
+import pytest
+
+from experiment_network_simulation_gb300 import inputs as I
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from experiment_network_simulation_gb300 import mv  # noqa: E402
+from test_gpu_parity import assert_same  # noqa: E402
+from test_oracle_dcqcn import _random_batch, cc  # noqa: E402
+
+
+def pin_batch():
+    ex = []
+    t = I.single_switch(3, 1, 0)
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], 120 * 4096)
+    w.collective(I.P2P, [1, 2], 120 * 4096)
+    ex.append(I.Experiment(t, w, cap=4, cc=cc(kmin=1, kmax=1), chunk=1 << 30, tick_ps=1000,
+                           rec_cap=512))
+    for delta in (0, 1, 12):
+        ex.append(I.Experiment(I.single_switch(2, 1, delta), I.lone_message(2, 0, 1, 40 * 4096),
+                               cc=cc(kmin=1, kmax=1, n=5, k=7, t=9, f=2, rai=100, rhai=100,
+                                     rmin=100), chunk=1 << 30, tick_ps=1000, rec_cap=64))
+    ex.append(I.Experiment(I.single_switch(2, 64, 0), I.lone_message(2, 0, 1, 400 * 4096),
+                           cc=cc(kmin=0, kmax=0, t=300, f=100), chunk=1 << 30, tick_ps=1000,
+                           rec_cap=512))
+    ex.append(I.Experiment(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 300 * 4096),
+                           cc=cc(kmin=0, kmax=0, n=50, k=30), chunk=1 << 30, tick_ps=1000,
+                           rec_cap=512))
+    return I.Batch(ex, "dcqcn-pins")
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+def test_dcqcn_pins_and_random_traffic_bit_exact(variant):
+    for b in (pin_batch(), _random_batch(11, 80, cc(kmin=1, kmax=4, pmax=30000, n=5, k=7, t=11,
+                                                    b=6, f=2, rai=3000, rhai=20000, rmin=5000))):
+        p = b.pack()
+        want = O.run(p)
+        assert (want["status"] == O.ST_DONE).all()
+        assert_same(mv.simulate(p, run_opts=dict(variant=variant)), want)
+
+
+def test_dcqcn_gpt_small_and_config1_bit_exact():
+    b = I.gpt_small(seeds=(0, 1))
+    c = I.config1()
+    for x in b.experiments + c.experiments:
+        x.cc = I.dcqcn(x.tick_ps, x.pkt)
+    for batch in (b, c):
+        p = batch.pack()
+        want = O.run(p)
+        assert (want["status"] == O.ST_DONE).all()
+        assert_same(mv.simulate(p), want)
