@@ -853,13 +853,14 @@ int mv_run_ex(mv_ctx *c, uint32_t max_ticks, const mv_run_opts *o, uint64_t *ste
     P.stage_limit = image;
     const u32 smem = megakernel_smem(warps, image);
     int bpsm = 0, nsm = 0;
-    cudaError_t e = megakernel_prepare(variant, warps, smem, &bpsm, &nsm);
+    const bool cc = !c->L.ccrec.empty();     // the build with the DCQCN code
+    cudaError_t e = megakernel_prepare(variant, cc, warps, smem, &bpsm, &nsm);
     if (e != cudaSuccess || bpsm == 0) return MV_ECUDA;
     u32 blocks = std::min<u32>(c->L.E, (u32)(bpsm * nsm));
     if (grid) blocks = std::min(blocks, grid);
     e = cudaMemsetAsync(P.glob, 0, sizeof(Glob), c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev0, c->stream);
-    if (e == cudaSuccess) e = launch_megakernel(variant, P, blocks, warps, smem, c->stream);
+    if (e == cudaSuccess) e = launch_megakernel(variant, cc, P, blocks, warps, smem, c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev1, c->stream);
     c->timed = e == cudaSuccess;
     Glob g;

@@ -268,11 +268,12 @@ cudaError_t launch_coll_times(const Params &p, u32 max_colls, cudaStream_t st);
 // variant 1: latency (one block of <= 8 warps an SM, register view); 2: occupancy (two
 // blocks of 8 warps an SM); 3: one block of 16 warps an SM (more shared memory a block);
 // 4: one block of 32 warps an SM (64 registers a thread)
-cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,
-                               int *n_sm);
+// cc: the build with the DCQCN code (needed when an experiment has DCQCN)
+cudaError_t megakernel_prepare(u32 variant, bool cc, u32 warps, u32 smem_bytes,
+                               int *blocks_per_sm, int *n_sm);
 u32 megakernel_smem(u32 warps, u32 image_bytes);
 u32 megakernel_scratch_bytes();   // per-warp forwarding scratch
-cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
+cudaError_t launch_megakernel(u32 variant, bool cc, const Params &p, u32 blocks, u32 warps,
                               u32 smem_bytes, cudaStream_t st);
 
 }  // namespace mv

@@ -1025,9 +1025,11 @@ __device__ __forceinline__ void port_set(RankReg &C, u32 p, bool on)
     else C.port_hi = on ? (C.port_hi | bit) : (C.port_hi & ~bit);
 }
 
-// Per-rank view used while processing one tick.
-template <class VT>
+// Per-rank view used while processing one tick.  CC: the kernel build
+// handles DCQCN experiments (without it the DCQCN code is compiled out).
+template <class VT, bool CC>
 struct RankViewT {
+    static constexpr bool kCC = CC;
     const Params *P;
     VT V;            // the view: a register copy (HV) or the block's shared view (const XV &)
     Team *TC;
@@ -1390,7 +1392,7 @@ __device__ __forceinline__ bool net_join(RV &v, u32 u)
             L.pkts_left = lane_setup(v, L);
             store_lane_hot(&lhot[slot], L);
             store_lane_cold(&lcold[slot], L);
-            if (X.cc)                   // line rate, alpha = 1, timers from the join
+            if (RV::kCC && X.cc)        // line rate, alpha = 1, timers from the join
                 cc_store(P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + slot,
                          CcState{kLine, kLine, kLine, 0, v.t, v.t, 0, 0, 0});
             v.C.lane_mask |= 1ull << slot;
@@ -1520,7 +1522,7 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
     const auto &V = v.V;
     const auto &X = V.X;
     const u32 t = v.t;
-    RankCC *rcc = X.cc ? P.rcc + X.rcc_off + v.r : nullptr;
+    RankCC *rcc = (RV::kCC && X.cc) ? P.rcc + X.rcc_off + v.r : nullptr;
     const bool cnp = rcc && rcc->head != rcc->tail;     // DCQCN notifications waiting
     if ((!v.C.lane_mask || v.C.blocked) && !cnp) return;
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
@@ -1587,7 +1589,7 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
             }
             LaneCC *lcc = nullptr;
             CcState S;
-            if (X.cc) {                 // paced by its DCQCN rate
+            if (RV::kCC && X.cc) {      // paced by its DCQCN rate
                 lcc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + l;
                 S = cc_load(lcc);
                 if (S.next_tx > t) {
@@ -1650,7 +1652,7 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     v.changed = true;
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     const u32 snd = pk_node(pk);
-    if (snd == kCnpNode) {
+    if (RV::kCC && snd == kCnpNode) {
         // DCQCN reaction point: the notification reaches the lane it names
         // if that lane still carries the flow
         const u32 l = pk_lane(pk);
@@ -1666,7 +1668,7 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
         return;
     }
     v.n_del++;
-    if (pk_ecn(pk)) {
+    if (RV::kCC && pk_ecn(pk)) {
         // DCQCN notification point: at most one notification a flow per N
         // ticks (the last one per flow, direct-mapped by key); it waits in
         // this rank's ring (a full ring drops it) for the uplink
@@ -1722,12 +1724,12 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
 // pending wake; pokes for other items go to `poke`.  Returns the warp's
 // earliest known next event; *done / *fail receive nodes completed and the
 // failure key.
-template <class VT>
+template <class VT, bool CC>
 __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC, Acc &acc, u32 g,
                                          u32 t, u32 old, u32 *poke, u32 *done_out, u32 *fail)
 {
     const u32 lane = threadIdx.x & 31;
-    RankViewT<VT> v(&P, ViewOf<VT>::get(Vs));     // the view (see ViewOf)
+    RankViewT<VT, CC> v(&P, ViewOf<VT>::get(Vs));     // the view (see ViewOf)
     v.TC = &TC;
     v.poke = poke;
     const auto &V = v.V;
@@ -1880,7 +1882,7 @@ __shared__ u32 s_slot;
 
 // Step experiment e from its clock until it finishes, stops, or reaches the
 // run's tick budget; `img` is this block's shared-memory image space.
-template <class VT>
+template <class VT, bool CC>
 __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSmem *sm,
                                u64 t_start)
 {
@@ -1948,7 +1950,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
     const bool qstaged = ((smask >> IM_QPUSH) & (smask >> IM_QPOP) & 1u) != 0;
     const bool voq = V.X.voq != 0;      // switches keep virtual output queues
     // with DCQCN a warp forwards one switch a pass (marking reads the queue)
-    const CcRec *ccr = V.X.cc ? P.ccrec + (V.X.cc - 1) : nullptr;
+    const CcRec *ccr = (CC && V.X.cc) ? P.ccrec + (V.X.cc - 1) : nullptr;
     const bool onepass = voq || ccr != nullptr;
     // items are dealt to warps round-robin (item warp + j * nW), so switches
     // and rank groups spread over all warps
@@ -2035,7 +2037,7 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
                 Mr &= Mr - 1;
                 const u32 item = warp + (base + j) * nW;
                 const u32 old = __shfl_sync(kFull, w, j);
-                rep = min(rep, rank_tick<VT>(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail));
+                rep = min(rep, rank_tick<VT, CC>(P, V, TC, acc, item - nsw, t, old, poke, &done, &fail));
             }
         }
         rep = __reduce_min_sync(kFull, rep);
@@ -2112,8 +2114,9 @@ __device__ void run_experiment(const Params &P, u32 e, unsigned char *img, SwSme
 // use up to 255 registers a thread (lowest latency per tick, for
 // experiments stepped from shared memory); MINB = 2 caps registers so two
 // blocks share an SM (more experiments in flight, for experiments whose
-// state stays in global memory and whose ticks wait on memory).
-template <int VAR>
+// state stays in global memory and whose ticks wait on memory).  CC: with
+// the DCQCN code (batches holding a DCQCN experiment).
+template <int VAR, bool CC>
 __global__ void __launch_bounds__(VAR == 4 ? 1024 : VAR == 3 ? 512 : 256, VAR == 2 ? 2 : 1)
 k_megakernel(Params P)
 {
@@ -2128,7 +2131,7 @@ k_megakernel(Params P)
         const u32 slot = s_slot;
         __syncthreads();
         if (slot >= P.n_exps) break;
-        run_experiment<typename ViewFor<VAR>::T>(P, P.order[slot], img, sw + warp, t_start);
+        run_experiment<typename ViewFor<VAR>::T, CC>(P, P.order[slot], img, sw + warp, t_start);
     }
 }
 
@@ -2176,35 +2179,49 @@ u32 megakernel_smem(u32 warps, u32 image_bytes) { return warps * (u32)sizeof(SwS
 
 u32 megakernel_scratch_bytes() { return (u32)sizeof(SwSmem); }
 
-static const void *megakernel_fn(u32 variant)
+template <int VAR>
+static const void *megakernel_fn_of(bool cc)
 {
-    return variant == 4 ? (const void *)k_megakernel<4>
-         : variant == 3 ? (const void *)k_megakernel<3>
-         : variant == 2 ? (const void *)k_megakernel<2> : (const void *)k_megakernel<1>;
+    return cc ? (const void *)k_megakernel<VAR, true> : (const void *)k_megakernel<VAR, false>;
 }
 
-cudaError_t megakernel_prepare(u32 variant, u32 warps, u32 smem_bytes, int *blocks_per_sm,
-                               int *n_sm)
+static const void *megakernel_fn(u32 variant, bool cc)
+{
+    return variant == 4 ? megakernel_fn_of<4>(cc)
+         : variant == 3 ? megakernel_fn_of<3>(cc)
+         : variant == 2 ? megakernel_fn_of<2>(cc) : megakernel_fn_of<1>(cc);
+}
+
+cudaError_t megakernel_prepare(u32 variant, bool cc, u32 warps, u32 smem_bytes,
+                               int *blocks_per_sm, int *n_sm)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const void *fn = megakernel_fn(variant);
+    const void *fn = megakernel_fn(variant, cc);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, (int)(warps * 32),
                                                          smem_bytes);
 }
 
-cudaError_t launch_megakernel(u32 variant, const Params &p, u32 blocks, u32 warps,
+template <int VAR>
+static void launch_variant(bool cc, const Params &p, u32 blocks, u32 warps, u32 smem_bytes,
+                           cudaStream_t st)
+{
+    if (cc) k_megakernel<VAR, true><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    else k_megakernel<VAR, false><<<blocks, warps * 32, smem_bytes, st>>>(p);
+}
+
+cudaError_t launch_megakernel(u32 variant, bool cc, const Params &p, u32 blocks, u32 warps,
                               u32 smem_bytes, cudaStream_t st)
 {
-    if (variant == 4) k_megakernel<4><<<blocks, warps * 32, smem_bytes, st>>>(p);
-    else if (variant == 3) k_megakernel<3><<<blocks, warps * 32, smem_bytes, st>>>(p);
-    else if (variant == 2) k_megakernel<2><<<blocks, warps * 32, smem_bytes, st>>>(p);
-    else k_megakernel<1><<<blocks, warps * 32, smem_bytes, st>>>(p);
+    if (variant == 4) launch_variant<4>(cc, p, blocks, warps, smem_bytes, st);
+    else if (variant == 3) launch_variant<3>(cc, p, blocks, warps, smem_bytes, st);
+    else if (variant == 2) launch_variant<2>(cc, p, blocks, warps, smem_bytes, st);
+    else launch_variant<1>(cc, p, blocks, warps, smem_bytes, st);
     return cudaGetLastError();
 }
 
