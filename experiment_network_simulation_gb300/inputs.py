@@ -376,7 +376,7 @@ class Experiment:
     gpu_mem: int = 80 * 1024 ** 3
     rec_cap: int = 0
     voq: int = 0                 # 1: switches keep virtual output queues (no head-of-line blocking)
-    cc: "DCQCN | None" = None    # congestion control (None: lossless credit only)
+    cc: "DCQCN | DCTCP | None" = None   # congestion control (None: lossless credit only)
     label: dict = field(default_factory=dict)
 
 
@@ -413,6 +413,28 @@ class DCQCN:
         w = [1, self.kmin, self.kmax, self.pmax, self.gshift, self.n, self.k, self.t, self.b,
              self.f, self.rai, self.rhai, self.rmin]
         return w + [0] * (CC_FIELDS - len(w))
+
+
+@dataclass
+class DCTCP:
+    """DCTCP parameters (an experiment's `cc`).
+
+    DCTCP (Alizadeh et al., SIGCOMM 2010; named by the Multiverse page):
+    switches mark packets above kmark queued packets, receivers acknowledge
+    every packet with its mark, senders keep a window (packets) that grows
+    by one packet a window of data and shrinks by alpha / 2 when marks came
+    back, alpha being the gain-weighted (2^-gshift) average marked
+    fraction."""
+    kmark: int = 16
+    gshift: int = 4                  # g = 1/16
+    w0: int = 10
+    wmax: int = 256
+
+    def words(self) -> list[int]:
+        w = [0] * CC_FIELDS
+        w[0], w[1], w[2], w[4], w[13], w[14] = 2, self.kmark, self.kmark, self.gshift, self.w0, \
+            self.wmax
+        return w
 
 
 def dcqcn(tick_ps: int, pkt: int = 4096, line_gbps: float = 400.0, **over) -> DCQCN:

@@ -52,7 +52,7 @@
 #define NLANE 64      /* send lanes per NIC (active messages streams)   */
 #define NPORT 128     /* receive counters per rank                      */
 #define NPTAB 64      /* notification-point flow table entries per NIC  */
-#define NCNPQ 16      /* congestion notifications waiting at a NIC      */
+#define NCNPQ 64      /* control packets waiting at a NIC (DCQCN uses 16) */
 #define NPEND 64      /* scheduled-but-not-started nodes per rank       */
 #define NACT 16       /* running collective memberships per rank        */
 #define TICK_LIMIT 0xFFF00000u   /* largest tick value a run reaches        */
@@ -116,16 +116,19 @@ typedef struct orc_event {
     uint32_t tick, kind, a, b;
 } orc_event;
 enum { EV_START = 1, EV_END = 2, EV_INJECT = 3, EV_HOP = 4, EV_DELIVER = 5, EV_MESSAGE = 6,
-       EV_CNP = 7, EV_CUT = 8 };
+       EV_CNP = 7, EV_CUT = 8, EV_WINDOW = 9, EV_ACK = 10 };
 
-/* DCQCN parameters of an experiment (CC_FIELDS words each): switch marking
- * thresholds in packets and the marking probability at kmax (units of
- * 2^-16); the gain g = 2^-gshift; the notification gap N, the alpha timer
- * K and the rate timer T in ticks; the byte counter B in packets; the fast
- * recovery count F; the additive, hyper and minimum rates in units of
- * 2^-20 of the line rate. */
+/* Congestion control of an experiment (CC_FIELDS words each).  CC_ON: 0
+ * none, 1 DCQCN, 2 DCTCP.  DCQCN: switch marking thresholds in packets and
+ * the marking probability at kmax (units of 2^-16); the gain g = 2^-gshift;
+ * the notification gap N, the alpha timer K and the rate timer T in ticks;
+ * the byte counter B in packets; the fast recovery count F; the additive,
+ * hyper and minimum rates in units of 2^-20 of the line rate.  DCTCP: the
+ * marking threshold (kmin = kmax), the gain shift, and the initial and
+ * largest window in packets (CC_W0, CC_WMAX). */
 enum { CC_ON, CC_KMIN, CC_KMAX, CC_PMAX, CC_GSHIFT, CC_N, CC_K, CC_T, CC_B, CC_F, CC_RAI,
-       CC_RHAI, CC_RMIN, CC_FIELDS = 16 };
+       CC_RHAI, CC_RMIN, CC_W0, CC_WMAX, CC_FIELDS = 16 };
+enum { CC_DCQCN = 1, CC_DCTCP = 2 };
 #define CC_LINE (1u << 20)        /* the line rate in rate units */
 #define ORC_NO_SKIP 1u
 
@@ -147,7 +150,10 @@ static uint32_t umax32(uint32_t a, uint32_t b) { return a > b ? a : b; }
 typedef struct pkt {
     uint32_t ready, dst, hopsum, sender, pslot, last, key;
     uint32_t lane, ecn;           /* the sender's lane slot; congestion experienced */
-    uint32_t cnp;                 /* a congestion notification (for lane `lane` of host dst) */
+    uint32_t cnp;                 /* a control packet for lane `lane` of host dst: a DCQCN
+                                     notification, or a DCTCP acknowledgement of n packets,
+                                     m of them marked */
+    uint32_t n, m;
 } pkt;
 
 typedef struct lane {
@@ -161,6 +167,11 @@ typedef struct lane {
      * rate timer and byte counter event counts, and packets since the last
      * byte-counter event */
     uint32_t rc, rt, alpha, next_tx, abase, rbase, tc, bc, sent;
+    /* DCTCP sender: window (units of 2^-10 packets), packets sent and
+     * acknowledged, the acknowledged count that closes the observation
+     * window, acknowledgements and marks in it; a lane that sent all its
+     * messages keeps its slot (draining) until every packet is acknowledged */
+    uint32_t wnd, sentc, acked, wend, wa, wm, draining;
 } lane;
 
 typedef struct nic {
@@ -180,7 +191,8 @@ typedef struct nic {
      * in a direct-mapped table (flow key mod NPTAB), and the notifications
      * waiting to be sent (a ring of NCNPQ) */
     uint32_t np_key[NPTAB], np_at[NPTAB];
-    uint32_t cq_dst[NCNPQ], cq_lane[NCNPQ], cq_key[NCNPQ], cq_head, cq_tail;
+    uint32_t cq_dst[NCNPQ], cq_lane[NCNPQ], cq_key[NCNPQ], cq_n[NCNPQ], cq_m[NCNPQ], cq_head,
+        cq_tail;
 } nic;
 
 typedef struct sim {
@@ -590,6 +602,8 @@ static void net_join(sim *s, uint32_t r, uint32_t u, uint32_t t)
             L->m = 0; L->nmsg = nm;
             L->rc = L->rt = L->alpha = CC_LINE;
             L->abase = L->rbase = t;
+            L->wnd = s->cc[CC_W0] << 10;
+            L->wend = s->cc[CC_W0];
             L->pkts_left = lane_setup(s, L);
             n->n_lanes++;
             n->used_mask |= 1ULL << slot;
@@ -999,6 +1013,8 @@ static void inject(sim *s, uint32_t r, uint32_t t)
         p.key = n->cq_key[k];
         p.lane = n->cq_lane[k];
         p.cnp = 1;
+        p.n = n->cq_n[k];
+        p.m = n->cq_m[k];
         push(s, f, &p, t, sg);
         n->busy = t + sg;
         s->pkt_hops++;
@@ -1013,6 +1029,7 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             uint32_t q = (uint32_t)__builtin_ctzll(m);
             m &= m - 1;
             lane *L = &n->lanes[q];
+            if (L->draining) continue;                      /* all sent: waits for its acks */
             int ok = 1;
             for (uint32_t b = 0; b < 3; b++)
                 if ((L->dep_mask >> b) & 1u)
@@ -1023,7 +1040,9 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             /* rendezvous: the destination's join reaches this rank one
              * link latency (1 + smallest delta) after it happened */
             if (s->start[dnode] == UNSET || s->start[dnode] + s->rdv_delay > t) continue;
-            if (s->cc[CC_ON] && L->next_tx > t) continue;       /* paced by its rate */
+            if (s->cc[CC_ON] == CC_DCQCN && L->next_tx > t) continue;   /* paced by its rate */
+            if (s->cc[CC_ON] == CC_DCTCP && L->sentc - L->acked >= L->wnd >> 10)
+                continue;                                   /* its window is full */
             pkt p;
             p.ready = t + s->host_sigma[r] + s->host_delta[r];
             p.dst = mrank(s, c, L->dst_member);
@@ -1033,9 +1052,10 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             p.last = L->pkts_left == 1;
             p.key = L->key;
             p.lane = q;
-            p.ecn = p.cnp = 0;
+            p.ecn = p.cnp = p.n = p.m = 0;
             push(s, f, &p, t, s->host_sigma[r]);
-            if (s->cc[CC_ON]) cc_sent(s, L, s->host_sigma[r], t);
+            if (s->cc[CC_ON] == CC_DCQCN) cc_sent(s, L, s->host_sigma[r], t);
+            if (s->cc[CC_ON] == CC_DCTCP) L->sentc++;
             ev(s, EV_INJECT, r, p.key);
             n->busy = t + s->host_sigma[r];
             n->rr = (q + 1) % NLANE;
@@ -1043,12 +1063,57 @@ static void inject(sim *s, uint32_t r, uint32_t t)
             s->pkt_hops++;
             s->changed = 1;
             if (--L->pkts_left == 0) {
-                if (++L->m == L->nmsg) { L->used = 0; n->n_lanes--; n->used_mask &= ~(1ULL << q); }
-                else L->pkts_left = lane_setup(s, L);
+                if (++L->m == L->nmsg) {
+                    if (s->cc[CC_ON] == CC_DCTCP) L->draining = 1;
+                    else { L->used = 0; n->n_lanes--; n->used_mask &= ~(1ULL << q); }
+                } else {
+                    L->pkts_left = lane_setup(s, L);
+                }
             }
             return;
         }
     }
+}
+
+/* DCTCP (Alizadeh et al., SIGCOMM 2010, an outside source: the Multiverse
+ * page only names it).  An acknowledgement of n packets, m of them marked,
+ * reaching lane q of rank r at tick t.  Once the packets sent before the
+ * last window update are all acknowledged the observation window closes:
+ * alpha <- (1 - g) alpha + g F with F the marked fraction of its
+ * acknowledgements, and the window shrinks by the factor 1 - alpha/2 (not
+ * below one packet) if any was marked, else grows by one packet (up to
+ * Wmax).  A draining lane frees its slot once every packet is
+ * acknowledged. */
+static void dctcp_ack(sim *s, uint32_t r, uint32_t q, uint32_t na, uint32_t ma, uint32_t t)
+{
+    nic *n = &s->nics[r];
+    lane *L = &n->lanes[q];
+    if (!L->used) return;
+    const uint32_t gs = s->cc[CC_GSHIFT];
+    ev(s, EV_ACK, r, na | (ma << 8) | (q << 16));
+    L->acked += na;
+    L->wa += na;
+    L->wm += ma;
+    if (L->acked >= L->wend) {
+        uint32_t F = (uint32_t)(((uint64_t)L->wm << 20) / L->wa);
+        L->alpha = L->alpha - (L->alpha >> gs) + (F >> gs);
+        if (L->wm) {
+            uint32_t dec = (uint32_t)(((uint64_t)L->wnd * L->alpha) >> 21);
+            L->wnd = L->wnd - dec < 1024 ? 1024 : L->wnd - dec;
+        } else {
+            L->wnd += 1024;
+            if (L->wnd > s->cc[CC_WMAX] << 10) L->wnd = s->cc[CC_WMAX] << 10;
+        }
+        L->wa = L->wm = 0;
+        L->wend = L->sentc;
+        ev(s, EV_WINDOW, r, L->wnd);
+    }
+    if (L->draining && L->acked == L->sentc) {
+        L->used = 0;
+        n->n_lanes--;
+        n->used_mask &= ~(1ULL << q);
+    }
+    (void)t;
 }
 
 /* NIC receive (NICRcvSys + ACKSys): the ready head of the NIC's downlink
@@ -1066,6 +1131,10 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     pop(s, f, t);
     s->changed = 1;
     nic *n = &s->nics[r];
+    if (p.cnp && s->cc[CC_ON] == CC_DCTCP) {
+        dctcp_ack(s, r, p.lane, p.n, p.m, t);
+        return;
+    }
     if (p.cnp) {
         /* reaction point: the notification reaches the lane it names; one
          * meant for an earlier flow of that slot is dropped */
@@ -1075,20 +1144,44 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     }
     s->pkts_delivered++;
     ev(s, EV_DELIVER, r, p.sender);
-    if (p.ecn) {
+    if (s->cc[CC_ON] == CC_DCTCP) {
+        /* every data packet is acknowledged; an acknowledgement still
+         * waiting for the same lane takes it over (up to 15 packets) */
+        uint32_t sr = s->node_rank[p.sender];
+        if (n->cq_tail != n->cq_head) {
+            uint32_t k = (n->cq_tail - 1) % NCNPQ;
+            if (n->cq_dst[k] == sr && n->cq_lane[k] == p.lane && n->cq_n[k] < 15) {
+                n->cq_n[k]++;
+                n->cq_m[k] += p.ecn;
+                goto acked;
+            }
+        }
+        if (n->cq_tail - n->cq_head >= NCNPQ) {
+            fail(s, ST_OVERFLOW);                     /* the acknowledgement ring is full */
+        } else {
+            uint32_t k = n->cq_tail++ % NCNPQ;
+            n->cq_dst[k] = sr;
+            n->cq_lane[k] = p.lane;
+            n->cq_key[k] = p.key;
+            n->cq_n[k] = 1;
+            n->cq_m[k] = p.ecn;
+        }
+    acked:;
+    } else if (p.ecn) {
         /* notification point: at most one notification a flow per N ticks
          * (the flow's table entry remembers the last one); it waits in the
          * NIC's notification ring, which drops it when full */
         uint32_t j = p.key % NPTAB;
         if (!(n->np_key[j] == p.key && n->np_at[j] != UNSET &&
               (uint64_t)t < (uint64_t)n->np_at[j] + s->cc[CC_N]) &&
-            n->cq_tail - n->cq_head < NCNPQ) {
+            n->cq_tail - n->cq_head < 16) {
             n->np_key[j] = p.key;
             n->np_at[j] = t;
             uint32_t k = n->cq_tail++ % NCNPQ;
             n->cq_dst[k] = s->node_rank[p.sender];
             n->cq_lane[k] = p.lane;
             n->cq_key[k] = p.key;
+            n->cq_n[k] = n->cq_m[k] = 0;
             ev(s, EV_CNP, r, p.key);
         }
     }
@@ -1155,7 +1248,7 @@ static uint32_t next_event(sim *s, uint32_t t)
         }
     }
     /* a paced lane's next packet */
-    if (s->cc[CC_ON])
+    if (s->cc[CC_ON] == CC_DCQCN)
         for (uint32_t r = 0; r < s->R; r++)
             for (int q = 0; q < NLANE; q++) {
                 lane *L = &s->nics[r].lanes[q];
@@ -1345,8 +1438,13 @@ static int validate(const orc_batch *b, const offs *o)
             return -2;
         if (b->exp_cc) {
             const uint32_t *c = b->exp_cc + (size_t)CC_FIELDS * e;
-            if (c[CC_ON] > 1) return -2;
-            if (c[CC_ON] && (b->exp_voq[e] || c[CC_KMIN] > c[CC_KMAX] || c[CC_PMAX] > 65536 ||
+            if (c[CC_ON] > CC_DCTCP) return -2;
+            if (c[CC_ON] == CC_DCTCP &&
+                (b->exp_voq[e] || c[CC_KMIN] != c[CC_KMAX] || c[CC_GSHIFT] == 0 ||
+                 c[CC_GSHIFT] > 16 || c[CC_W0] == 0 || c[CC_WMAX] < c[CC_W0] ||
+                 c[CC_WMAX] > 65535))
+                return -2;
+            if (c[CC_ON] == CC_DCQCN && (b->exp_voq[e] || c[CC_KMIN] > c[CC_KMAX] || c[CC_PMAX] > 65536 ||
                              c[CC_GSHIFT] == 0 || c[CC_GSHIFT] > 16 || c[CC_N] == 0 ||
                              c[CC_K] == 0 || c[CC_T] == 0 || c[CC_B] == 0 ||
                              c[CC_F] > 65535 || c[CC_RAI] > CC_LINE || c[CC_RHAI] > CC_LINE ||

@@ -47,7 +47,8 @@ _ARR = [("topo_nhosts", "u4"), ("topo_nsw", "u4"), ("topo_nports", "u4"),
         ("exp_rec_cap", "u4"), ("exp_voq", "u4"), ("exp_cc", "u4")]
 _CT = {"u4": _P32, "u8": _P64, "i4": _PI32}
 # event trace records (struct orc_event): kinds and their (a, b) fields
-EV_START, EV_END, EV_INJECT, EV_HOP, EV_DELIVER, EV_MESSAGE, EV_CNP, EV_CUT = range(1, 9)
+(EV_START, EV_END, EV_INJECT, EV_HOP, EV_DELIVER, EV_MESSAGE, EV_CNP, EV_CUT, EV_WINDOW,
+ EV_ACK) = range(1, 11)
 CC_FIELDS = 16                 # words of an experiment's DCQCN record (exp_cc)
 EVENT = np.dtype([("tick", np.uint32), ("kind", np.uint32), ("a", np.uint32), ("b", np.uint32)])
 _NP = {"u4": np.uint32, "u8": np.uint64, "i4": np.int32}

@@ -15,7 +15,7 @@ if not torch.cuda.is_available():
 
 from experiment_network_simulation_gb300 import mv  # noqa: E402
 from test_gpu_parity import assert_same  # noqa: E402
-from test_oracle_dcqcn import _random_batch, cc  # noqa: E402
+from test_oracle_cc import _random_batch, cc  # noqa: E402
 
 
 def pin_batch():

@@ -215,3 +215,142 @@ def test_parameter_limits_are_refused():
     e = I.Experiment(t, w, tick_ps=1000, chunk=1 << 20, cc=cc(), voq=1)
     with pytest.raises(Exception):
         O.run(I.Batch([e]).pack())
+
+
+# ================================================================ DCTCP
+# DCTCP is Alizadeh et al., SIGCOMM 2010 (an outside source: the Multiverse
+# page names it without parameters).  Windows are in units of 2^-10 packets.
+W1 = 1 << 10
+
+
+def tcp(**kw):
+    base = dict(kmark=NEVER, gshift=4, w0=10, wmax=256)
+    base.update(kw)
+    return I.DCTCP(**base)
+
+
+@pytest.mark.parametrize("delta,w", [(0, 2), (0, 3), (2, 2), (1, 5)])
+def test_window_limited_lone_flow_closed_form(delta, w):
+    """A lone flow whose window is fixed at w packets (w0 = wmax, nothing
+    marked) sends w packets back to back, then waits for acknowledgements:
+    a packet sent at t is delivered at t + L (1 + delta), its
+    acknowledgement leaves the receiver's NIC the next tick and is taken off
+    the sender's downlink at t + 2 L (1 + delta) + 1, which frees the window
+    for a packet at t + 2 L (1 + delta) + 2.  So packet k leaves at
+    t0 + (2 L (1 + delta) + 2) floor(k / w) + k mod w (while w is below that
+    round trip), and every packet is acknowledged (one acknowledgement
+    packet each, L hops) but those still on their way when the last message
+    completes the run."""
+    n, L = 24, 2
+    t = I.single_switch(2, 1, delta)
+    r, ev = traced(t, I.lone_message(2, 0, 1, n * 4096), cc=tcp(w0=w, wmax=w))
+    inj = of_kind(ev, O.EV_INJECT, 0)["tick"].astype(np.int64)
+    rtt = 2 * L * (1 + delta) + 2
+    assert w < rtt
+    want = inj[0] + rtt * (np.arange(n) // w) + np.arange(n) % w
+    assert (inj == want).all()
+    acks = of_kind(ev, O.EV_ACK, 0)
+    assert (acks["b"] & 0xFF == 1).all() and n - w <= len(acks) < n
+    assert r["pkt_hops"][0] >= n * L + len(acks) * L
+
+
+def test_window_grows_one_packet_a_window_until_wmax():
+    """Nothing marked: each closed observation window adds one packet to the
+    window, up to wmax (1, 2, 3, 4, 4, ... packets)."""
+    t = I.single_switch(2, 1, 0)
+    r, ev = traced(t, I.lone_message(2, 0, 1, 60 * 4096), cc=tcp(w0=1, wmax=4))
+    w = of_kind(ev, O.EV_WINDOW, 0)["b"].tolist()
+    assert w[:4] == [2 * W1, 3 * W1, 4 * W1, 4 * W1]
+    assert max(w) == 4 * W1
+
+
+def test_window_halves_while_everything_is_marked():
+    """Every forwarded packet marked (threshold 0): each window's marked
+    fraction is 1, so alpha stays 1 ((1 - g) + g) and each closed window
+    halves the window, down to one packet: 8 -> 4 -> 2 -> 1 -> 1."""
+    t = I.single_switch(2, 1, 0)
+    r, ev = traced(t, I.lone_message(2, 0, 1, 60 * 4096), cc=tcp(kmark=0, w0=8, wmax=8))
+    w = of_kind(ev, O.EV_WINDOW, 0)["b"].tolist()
+    assert w[:5] == [4 * W1, 2 * W1, 1 * W1, 1 * W1, 1 * W1]
+
+
+def test_window_updates_follow_the_acknowledgement_stream():
+    """A two-sender incast with marking above one queued packet: from the
+    acknowledgements each sender received (packets and marks, in order) and
+    the packets it had sent by then, the published update (close the window
+    once every packet sent before the last update is acknowledged; alpha <-
+    (1 - g) alpha + g F; the window shrinks by alpha / 2 if F > 0, else
+    grows one packet) gives every window the oracle logged."""
+    t = I.single_switch(3, 1, 0)
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], 150 * 4096)
+    w.collective(I.P2P, [1, 2], 150 * 4096)
+    gs, w0, wmax = 4, 10, 64
+    r, ev = traced(t, w, cap=8, cc=tcp(kmark=1, gshift=gs, w0=w0, wmax=wmax))
+    saw_partial = False
+    for sender in (0, 1):
+        mine = ev[ev["a"] == sender]
+        wnd, alpha, acked, wend, wa, wm, sent = w0 * W1, LINE, 0, w0, 0, 0, 0
+        got = []
+        for x in mine:
+            if x["kind"] == O.EV_INJECT:
+                sent += 1
+            elif x["kind"] == O.EV_ACK:
+                n, m = int(x["b"]) & 0xFF, (int(x["b"]) >> 8) & 0xFF
+                acked, wa, wm = acked + n, wa + n, wm + m
+                if acked >= wend:
+                    F = (wm << 20) // wa
+                    saw_partial |= 0 < wm < wa
+                    alpha = alpha - (alpha >> gs) + (F >> gs)
+                    if wm:
+                        wnd = max(W1, wnd - ((wnd * alpha) >> 21))
+                    else:
+                        wnd = min(wmax * W1, wnd + W1)
+                    wa = wm = 0
+                    wend = sent
+                    got.append(wnd)
+        logged = of_kind(ev, O.EV_WINDOW, sender)["b"].tolist()
+        assert got == logged and len(logged) > 5
+    assert saw_partial                                   # some window was partly marked
+
+
+def test_dctcp_random_traffic_keeps_invariants():
+    """Seeded random collectives under DCTCP (threshold two packets, small
+    windows): every run ends, every packet is delivered and acknowledged,
+    no run-time invariant breaks, and stepping tick by tick changes
+    nothing."""
+    p = _random_batch(13, 80, tcp(kmark=2, gshift=3, w0=2, wmax=12)).pack()
+    a, b = O.run(p), O.run(p, no_skip=True)
+    assert (a["status"] == O.ST_DONE).all()
+    assert (a["violations"] == 0).all()
+    assert (a["pkts_injected"] == a["pkts_delivered"]).all()
+    for k in ("end_tick", "pkts_injected", "pkt_hops", "msgs_delivered", "digest", "node_end"):
+        assert (a[k] == b[k]).all(), k
+    off = O.run(_random_batch(13, 80, None).pack())
+    assert (a["end_tick"] >= off["end_tick"]).mean() > 0.5   # windows slow most runs
+
+
+def test_dctcp_parameter_limits_are_refused():
+    """DCTCP needs one marking threshold (kmin = kmax), a gain shift of
+    1..16, an initial window of at least one packet and wmax between w0 and
+    65,535; with VOQs it is refused."""
+    t = I.single_switch(2, 1, 0)
+    wl = I.lone_message(2, 0, 1, 4096)
+    ok = I.Experiment(t, wl, tick_ps=1000, chunk=1 << 20, cc=tcp())
+    assert O.run(I.Batch([ok]).pack())["status"][0] == O.ST_DONE
+    for bad in (dict(gshift=0), dict(gshift=17), dict(w0=0), dict(w0=5, wmax=4),
+                dict(wmax=65536)):
+        e = I.Experiment(t, wl, tick_ps=1000, chunk=1 << 20, cc=tcp(**bad))
+        with pytest.raises(Exception):
+            O.run(I.Batch([e]).pack())
+    c = tcp()
+    wds = c.words()
+    wds[2] -= 1                                          # kmin != kmax
+    e = I.Experiment(t, wl, tick_ps=1000, chunk=1 << 20, cc=c)
+    p = I.Batch([e]).pack()
+    p["exp_cc"][:16] = wds
+    with pytest.raises(Exception):
+        O.run(p)
+    e = I.Experiment(t, wl, tick_ps=1000, chunk=1 << 20, cc=tcp(), voq=1)
+    with pytest.raises(Exception):
+        O.run(I.Batch([e]).pack())
