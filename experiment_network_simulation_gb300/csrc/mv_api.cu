@@ -371,16 +371,22 @@ int plan(const mv_batch_desc *d, Layout &L)
         // DCQCN parameters (n_exps records of MV_CC_FIELDS words; NULL: none)
         if (d->exp_cc) {
             const u32 *c = d->exp_cc + (u64)MV_CC_FIELDS * e;
-            if (c[0] > 1) return MV_EINVAL;
+            if (c[0] > kDctcp) return MV_EINVAL;
             if (c[0]) {
                 CcRec R;
                 std::memset(&R, 0, sizeof R);
+                R.mode = c[0];
                 R.kmin = c[1]; R.kmax = c[2]; R.pmax = c[3]; R.gshift = c[4]; R.n = c[5];
                 R.k = c[6]; R.t = c[7]; R.b = c[8]; R.f = c[9]; R.rai = c[10]; R.rhai = c[11];
-                R.rmin = c[12];
-                if (X.voq || R.kmin > R.kmax || R.pmax > 65536 || R.gshift == 0 || R.gshift > 16 ||
-                    R.n == 0 || R.k == 0 || R.t == 0 || R.b == 0 || R.f > 65535 || R.rai > kLine ||
-                    R.rhai > kLine || R.rmin == 0 || R.rmin > kLine)
+                R.rmin = c[12]; R.w0 = c[13]; R.wmax = c[14];
+                if (R.mode == kDctcp &&
+                    (X.voq || R.kmin != R.kmax || R.gshift == 0 || R.gshift > 16 || R.w0 == 0 ||
+                     R.wmax < R.w0 || R.wmax > 65535))
+                    return MV_EINVAL;
+                if (R.mode == kDcqcn &&
+                    (X.voq || R.kmin > R.kmax || R.pmax > 65536 || R.gshift == 0 || R.gshift > 16 ||
+                     R.n == 0 || R.k == 0 || R.t == 0 || R.b == 0 || R.f > 65535 || R.rai > kLine ||
+                     R.rhai > kLine || R.rmin == 0 || R.rmin > kLine))
                     return MV_EINVAL;
                 L.ccrec.push_back(R);
                 X.cc = (u32)L.ccrec.size();

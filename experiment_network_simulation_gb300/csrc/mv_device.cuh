@@ -66,31 +66,39 @@ struct ExpRec {
     u64 lcc_off, rcc_off;           // with DCQCN: its lanes' rate records, its ranks' records
 };
 
-// DCQCN (congestion control) of an experiment, in the simulator's units:
-// marking thresholds (packets) and top probability (2^-16), gain shift,
-// notification gap N, alpha timer K and rate timer T (ticks), byte counter
-// B (packets), fast-recovery count F, additive / hyper / minimum rate
-// (2^-20 of the line rate).
+// Congestion control of an experiment, in the simulator's units.  mode 1,
+// DCQCN: marking thresholds (packets) and top probability (2^-16), gain
+// shift, notification gap N, alpha timer K and rate timer T (ticks), byte
+// counter B (packets), fast-recovery count F, additive / hyper / minimum
+// rate (2^-20 of the line rate).  mode 2, DCTCP: the marking threshold
+// (kmin = kmax), gain shift, initial and largest window (packets).
+constexpr u32 kDcqcn = 1, kDctcp = 2;
 struct CcRec {
-    u32 kmin, kmax, pmax, gshift, n, k, t, b, f, rai, rhai, rmin, pad[4];
+    u32 kmin, kmax, pmax, gshift, n, k, t, b, f, rai, rhai, rmin, w0, wmax, mode, pad;
 };
 constexpr u32 kLine = 1u << 20;      // the line rate (and alpha = 1) in DCQCN units
 
-// A send lane's DCQCN reaction-point state (32 bytes, beside its hot and
-// cold records): a = current rate, target rate, alpha, earliest tick of its
-// next packet; b = alpha timer's and rate timer's last expiry, rate-timer
-// events | byte-counter events << 16, packets since the last byte event.
+// A send lane's congestion-control state (32 bytes, beside its hot and cold
+// records).  DCQCN reaction point: a = current rate, target rate, alpha,
+// earliest tick of its next packet; b = alpha timer's and rate timer's last
+// expiry, rate-timer events | byte-counter events << 16, packets since the
+// last byte event.  DCTCP sender: a = window (2^-10 packets), alpha,
+// packets sent, packets acknowledged; b = acknowledged count that closes
+// the observation window, its acknowledgements, its marks, draining (all
+// sent, waiting for acknowledgements).
 struct LaneCC {
     uint4 a, b;
 };
 
-// A rank's DCQCN notification-point state: the last notification per flow
-// (direct-mapped by key mod 64: key | 1 << 31, tick) and the ring of
-// notifications waiting to be sent (sender rank | its lane << 16, key).
-constexpr u32 kNpTab = 64, kCnpRing = 16;
+// A rank's congestion-control state at the receiving side: DCQCN's last
+// notification per flow (direct-mapped by key mod 64: key | 1 << 31, tick),
+// and the ring of control packets waiting to be sent (sender rank | its
+// lane << 16 | packets acknowledged << 22 | of them marked << 26, key):
+// DCQCN notifications (at most kCnpRing of them) or DCTCP acknowledgements.
+constexpr u32 kNpTab = 64, kCnpRing = 16, kCtlRing = 64;
 struct RankCC {
     uint2 np[kNpTab];
-    uint2 cq[kCnpRing];
+    uint2 cq[kCtlRing];
     u32 head, tail, pad0, pad1;
 };
 

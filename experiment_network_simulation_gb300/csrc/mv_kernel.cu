@@ -352,6 +352,7 @@ struct Acc {
 // order, as the serial phase order visits them) come before switch errors.
 __device__ __forceinline__ u32 fail_key_rank(u32 r, u32 code) { return (r << 3) | code; }
 constexpr u32 kFailSwitch = 0xF0000000u | EXP_ERROR;
+constexpr u32 kFailReceive = 0xF1000000u;     // receive-phase failures order after the switches
 
 // Per-warp scratch of one forwarding pass.  A pass handles a pack of up to
 // kPack switches laid side by side over the 64 port positions (a lane has
@@ -1037,6 +1038,7 @@ struct RankViewT {
     u32 r, t;
     RankReg C;
     bool changed, fail_over, fail_err;
+    bool fail_rx;       // a table overflowed in the receive phase (after the switches)
     u32 nxt;            // this rank's own next wake
     u32 pk_min;         // earliest wake poked into other items
     u32 n_inj, n_del, n_msg, n_done, end_max1;
@@ -1392,9 +1394,16 @@ __device__ __forceinline__ bool net_join(RV &v, u32 u)
             L.pkts_left = lane_setup(v, L);
             store_lane_hot(&lhot[slot], L);
             store_lane_cold(&lcold[slot], L);
-            if (RV::kCC && X.cc)        // line rate, alpha = 1, timers from the join
-                cc_store(P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + slot,
-                         CcState{kLine, kLine, kLine, 0, v.t, v.t, 0, 0, 0});
+            if (RV::kCC && X.cc) {
+                LaneCC *lc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + slot;
+                const CcRec &C = P.ccrec[X.cc - 1];
+                if (C.mode == kDctcp) {         // window w0, alpha = 1, first window: w0 packets
+                    lc->a = make_uint4(C.w0 << 10, kLine, 0, 0);
+                    lc->b = make_uint4(C.w0, 0, 0, 0);
+                } else {                        // line rate, alpha = 1, timers from the join
+                    cc_store(lc, CcState{kLine, kLine, kLine, 0, v.t, v.t, 0, 0, 0});
+                }
+            }
             v.C.lane_mask |= 1ull << slot;
             v.C.blocked = 0;
             out += (i32)nm;
@@ -1523,7 +1532,8 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
     const auto &X = V.X;
     const u32 t = v.t;
     RankCC *rcc = (RV::kCC && X.cc) ? P.rcc + X.rcc_off + v.r : nullptr;
-    const bool cnp = rcc && rcc->head != rcc->tail;     // DCQCN notifications waiting
+    const bool cnp = rcc && rcc->head != rcc->tail;     // control packets waiting
+    const u32 ccmode = rcc ? P.ccrec[X.cc - 1].mode : 0u;
     if ((!v.C.lane_mask || v.C.blocked) && !cnp) return;
     if (v.C.busy > t) { v.nxt = min(v.nxt, v.C.busy); return; }
     const u32 qp = hr.x, hs = hr.y, hd = hr.z;
@@ -1535,13 +1545,13 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
     if (cnp) {
         // a waiting notification goes first: one packet time, the lane
         // round-robin pointer stays
-        const uint2 c = rcc->cq[rcc->head % kCnpRing];
+        const uint2 c = rcc->cq[rcc->head % kCtlRing];
         rcc->head++;
         uint4 pk;
         pk.x = t + hs + hd;
         pk.y = (c.x & 0xFFFFu) | ((hd + 1) << 16);
         pk.z = kCnpNode | (((c.x >> 16) & 63u) << 25);
-        pk.w = c.y;
+        pk.w = c.y | (((c.x >> 22) & 15u) << 24) | (((c.x >> 26) & 15u) << 28);
         V.slots[(u64)qp * X.cap + slot_ix(tail, X.cap)] = pk;
         st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
         v.C.busy = t + hs;
@@ -1564,6 +1574,9 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
             u32 l = (u32)__ffsll((long long)m) - 1;
             m &= m - 1;
             LaneReg L = load_lane_hot(&lhot[l]);    // all a packet needs
+            LaneCC *lcc = nullptr;
+            if (RV::kCC && ccmode) lcc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + l;
+            if (RV::kCC && ccmode == kDctcp && lcc->b.w) continue;   // all sent: waits for acks
             bool ok = true;
             for (u32 b = 0; b < 3 && ok; b++)
                 if ((L.dep_mask >> b) & 1u)
@@ -1587,16 +1600,19 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
                 L.dslot = ld_vol32(&V.nd_pbase[L.dnode]) + L.dst_port;
                 L.ok_dst = 1;
             }
-            LaneCC *lcc = nullptr;
             CcState S;
-            if (RV::kCC && X.cc) {      // paced by its DCQCN rate
-                lcc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + l;
+            if (RV::kCC && ccmode == kDcqcn) {      // paced by its DCQCN rate
                 S = cc_load(lcc);
                 if (S.next_tx > t) {
                     v.nxt = min(v.nxt, S.next_tx);
                     timed = true;
                     continue;
                 }
+            }
+            uint4 ca = make_uint4(0, 0, 0, 0);
+            if (RV::kCC && ccmode == kDctcp) {      // its DCTCP window is full: waits for acks
+                ca = lcc->a;
+                if (ca.z - ca.w >= (ca.x >> 10)) continue;
             }
             uint4 pk;
             pk.x = t + hs + hd;
@@ -1608,16 +1624,19 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
             v.C.busy = t + hs;
             v.C.rr = (l + 1) % kNLane;
             v.n_inj++;
-            if (lcc) {
+            if (RV::kCC && ccmode == kDcqcn) {
                 cc_sent(P.ccrec[X.cc - 1], S, hs, t);
                 cc_store(lcc, S);
             }
+            if (RV::kCC && ccmode == kDctcp) lcc->a.z = ca.z + 1;   // packets sent
             v.changed = true;
             rank_poke(v, hr.w, pk.x);
             if (--L.pkts_left == 0) {           // the message is out: the next one
                 load_lane_cold(&lcold[l], L);
                 if (++L.m == L.nmsg) {
-                    v.C.lane_mask &= ~(1ull << l);
+                    // a DCTCP lane keeps its slot until every packet is acknowledged
+                    if (RV::kCC && ccmode == kDctcp) lcc->b.w = 1;
+                    else v.C.lane_mask &= ~(1ull << l);
                 } else {
                     L.pkts_left = lane_setup(v, L);
                     store_lane_cold(&lcold[l], L);
@@ -1631,6 +1650,42 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
     // every lane waits for receive counts: nothing changes that but a
     // message completing at this rank (receive) or a new lane (join)
     if (!timed) v.C.blocked = 1;
+}
+
+// DCTCP sender (Alizadeh et al., SIGCOMM 2010): an acknowledgement of n
+// packets, m of them marked, for lane l.  Once the packets sent before the
+// last update are all acknowledged the observation window closes: alpha <-
+// (1 - g) alpha + g F (F the marked fraction), and the window shrinks by
+// alpha / 2 (not below one packet) if any was marked, else grows by one
+// packet (up to wmax).  A draining lane frees its slot once every packet is
+// acknowledged.
+template <class RV>
+__device__ __forceinline__ void dctcp_ack(RV &v, u32 l, u32 n, u32 m)
+{
+    const Params &P = *v.P;
+    const auto &X = v.V.X;
+    if (!((v.C.lane_mask >> l) & 1ull)) return;
+    const CcRec &C = P.ccrec[X.cc - 1];
+    LaneCC *lc = P.lcc + X.lcc_off + (u64)v.r * X.lane_cap + l;
+    uint4 a = lc->a, b = lc->b;        // a: window, alpha, sent, acked; b: wend, wa, wm, draining
+    a.w += n;
+    b.y += n;
+    b.z += m;
+    if (a.w >= b.x) {
+        const u32 F = (u32)(((u64)b.z << 20) / b.y);
+        a.y = a.y - (a.y >> C.gshift) + (F >> C.gshift);
+        if (b.z) {
+            const u32 dec = (u32)(((u64)a.x * a.y) >> 21);
+            a.x = a.x - dec < 1024u ? 1024u : a.x - dec;
+        } else {
+            a.x = min(a.x + 1024u, C.wmax << 10);
+        }
+        b.y = b.z = 0;
+        b.x = a.z;
+    }
+    lc->a = a;
+    lc->b = b;
+    if (b.w && a.w == a.z) v.C.lane_mask &= ~(1ull << l);
 }
 
 // NICRcvSys + ACKSys: take the ready head of the downlink queue; the last
@@ -1653,9 +1708,14 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     const u32 snd = pk_node(pk);
     if (RV::kCC && snd == kCnpNode) {
+        const u32 l = pk_lane(pk);
+        if (P.ccrec[X.cc - 1].mode == kDctcp) {
+            dctcp_ack(v, l, (pk.w >> 24) & 15u, pk.w >> 28);
+            v.C.blocked = 0;                   // its window may have room again
+            return;
+        }
         // DCQCN reaction point: the notification reaches the lane it names
         // if that lane still carries the flow
-        const u32 l = pk_lane(pk);
         if ((v.C.lane_mask >> l) & 1ull) {
             const LaneReg L = load_lane_hot(V.lhot + (u64)v.r * X.lane_cap + l);
             if (L.key == pk_key(pk)) {
@@ -1668,7 +1728,31 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
         return;
     }
     v.n_del++;
-    if (RV::kCC && pk_ecn(pk)) {
+    if (RV::kCC && X.cc && P.ccrec[X.cc - 1].mode == kDctcp) {
+        // DCTCP: every data packet is acknowledged with its mark; an
+        // acknowledgement still waiting for the same lane takes it over (up
+        // to 15); a full ring is a table overflow
+        RankCC *rcc = P.rcc + X.rcc_off + v.r;
+        const u32 id = P.node_rank[W_(v).node_off + snd] | (pk_lane(pk) << 16);
+        const u32 mk = pk_ecn(pk);
+        bool merged = false;
+        if (rcc->tail != rcc->head) {
+            uint2 &q = rcc->cq[(rcc->tail - 1) % kCtlRing];
+            if ((q.x & 0x3FFFFFu) == id && ((q.x >> 22) & 15u) < 15u) {
+                q.x += (1u << 22) + (mk << 26);
+                merged = true;
+            }
+        }
+        if (!merged) {
+            if (rcc->tail - rcc->head >= kCtlRing) {
+                v.fail_rx = true;
+            } else {
+                rcc->cq[rcc->tail % kCtlRing] = make_uint2(id | (1u << 22) | (mk << 26), pk_key(pk));
+                rcc->tail++;
+            }
+        }
+        v.nxt = min(v.nxt, t + 1);
+    } else if (RV::kCC && pk_ecn(pk)) {
         // DCQCN notification point: at most one notification a flow per N
         // ticks (the last one per flow, direct-mapped by key); it waits in
         // this rank's ring (a full ring drops it) for the uplink
@@ -1679,7 +1763,7 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
                            (u64)t < (u64)e.y + P.ccrec[X.cc - 1].n;
         if (!again && rcc->tail - rcc->head < kCnpRing) {
             rcc->np[j] = make_uint2(key | 0x80000000u, t);
-            rcc->cq[rcc->tail % kCnpRing] =
+            rcc->cq[rcc->tail % kCtlRing] =
                 make_uint2(P.node_rank[W_(v).node_off + snd] | (pk_lane(pk) << 16), key);
             rcc->tail++;
             v.nxt = min(v.nxt, t + 1);
@@ -1735,7 +1819,7 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
     const auto &V = v.V;
     const u32 it = V.X.nsw + g;
     v.r = g * 32 + lane; v.t = t;
-    v.changed = v.fail_over = v.fail_err = false;
+    v.changed = v.fail_over = v.fail_err = v.fail_rx = false;
     v.nxt = kUnset;
     v.pk_min = kUnset;
     v.n_inj = v.n_del = v.n_msg = v.n_done = v.end_max1 = v.n_cnp = 0;
@@ -1765,9 +1849,11 @@ __device__ __forceinline__ u32 rank_tick(const Params &P, const XV &Vs, Team &TC
     const u32 pkm = __reduce_min_sync(kFull, v.pk_min);
     u32 done = 0;
     if (__any_sync(kFull, v.n_done != 0)) done = __reduce_add_sync(kFull, v.n_done);
-    if (__any_sync(kFull, v.fail_over || v.fail_err)) {
+    if (__any_sync(kFull, v.fail_over || v.fail_err || v.fail_rx)) {
+        // failures in phase order: DAG step (by rank), switches, receive (by rank)
         u32 fk = v.fail_over ? fail_key_rank(v.r, EXP_OVERFLOW)
-               : v.fail_err ? fail_key_rank(v.r, EXP_ERROR) : kUnset;
+               : v.fail_err ? fail_key_rank(v.r, EXP_ERROR)
+               : v.fail_rx ? kFailReceive | fail_key_rank(v.r, EXP_OVERFLOW) : kUnset;
         *fail = min(*fail, __reduce_min_sync(kFull, fk));
     }
     u32 w = min(nxt, old > t ? old : kUnset);

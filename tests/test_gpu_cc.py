@@ -1,7 +1,7 @@
-"""DCQCN congestion control on the CUDA path, bit-exact against the oracle:
-the oracle's DCQCN pin scenarios, seeded random collectives with aggressive
-settings in every kernel build, the GPT DAG at test size and config 1 with
-the generator's DCQCN settings."""
+"""Congestion control (DCQCN and DCTCP) on the CUDA path, bit-exact against
+the oracle: the oracle's pin scenarios, seeded random collectives with
+aggressive settings in every kernel build, the GPT DAG at test size and
+config 1 with the generators' settings."""
 import numpy as np
 import pytest
 
@@ -15,7 +15,7 @@ if not torch.cuda.is_available():
 
 from experiment_network_simulation_gb300 import mv  # noqa: E402
 from test_gpu_parity import assert_same  # noqa: E402
-from test_oracle_cc import _random_batch, cc  # noqa: E402
+from test_oracle_cc import _random_batch, cc, tcp  # noqa: E402
 
 
 def pin_batch():
@@ -54,6 +54,45 @@ def test_dcqcn_gpt_small_and_config1_bit_exact():
     c = I.config1()
     for x in b.experiments + c.experiments:
         x.cc = I.dcqcn(x.tick_ps, x.pkt)
+    for batch in (b, c):
+        p = batch.pack()
+        want = O.run(p)
+        assert (want["status"] == O.ST_DONE).all()
+        assert_same(mv.simulate(p), want)
+
+
+def tcp_pin_batch():
+    ex = []
+    for delta, w in ((0, 2), (0, 3), (2, 2), (1, 5)):
+        ex.append(I.Experiment(I.single_switch(2, 1, delta), I.lone_message(2, 0, 1, 24 * 4096),
+                               cc=tcp(w0=w, wmax=w), chunk=1 << 30, tick_ps=1000, rec_cap=64))
+    ex.append(I.Experiment(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 60 * 4096),
+                           cc=tcp(w0=1, wmax=4), chunk=1 << 30, tick_ps=1000, rec_cap=64))
+    ex.append(I.Experiment(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 60 * 4096),
+                           cc=tcp(kmark=0, w0=8, wmax=8), chunk=1 << 30, tick_ps=1000, rec_cap=64))
+    t = I.single_switch(3, 1, 0)
+    w = I.Workload(3)
+    w.collective(I.P2P, [0, 2], 150 * 4096)
+    w.collective(I.P2P, [1, 2], 150 * 4096)
+    ex.append(I.Experiment(t, w, cap=8, cc=tcp(kmark=1, gshift=4, w0=10, wmax=64),
+                           chunk=1 << 30, tick_ps=1000, rec_cap=512))
+    return I.Batch(ex, "dctcp-pins")
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+def test_dctcp_pins_and_random_traffic_bit_exact(variant):
+    for b in (tcp_pin_batch(), _random_batch(13, 80, tcp(kmark=2, gshift=3, w0=2, wmax=12))):
+        p = b.pack()
+        want = O.run(p)
+        assert (want["status"] == O.ST_DONE).all()
+        assert_same(mv.simulate(p, run_opts=dict(variant=variant)), want)
+
+
+def test_dctcp_gpt_small_and_config1_bit_exact():
+    b = I.gpt_small(seeds=(0, 1))
+    c = I.config1()
+    for x in b.experiments + c.experiments:
+        x.cc = I.DCTCP()
     for batch in (b, c):
         p = batch.pack()
         want = O.run(p)
