@@ -1711,7 +1711,8 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
         const u32 l = pk_lane(pk);
         if (P.ccrec[X.cc - 1].mode == kDctcp) {
             dctcp_ack(v, l, (pk.w >> 24) & 15u, pk.w >> 28);
-            v.C.blocked = 0;                   // its window may have room again
+            v.C.blocked = 0;                   // its window may have room again:
+            v.nxt = min(v.nxt, t + 1);         // the lanes look next tick
             return;
         }
         // DCQCN reaction point: the notification reaches the lane it names
