@@ -113,9 +113,14 @@ extern "C" {
  * blocking kept; 1 = virtual output queues, needs exp_cap <= 64).
  *
  * exp_cc (may be NULL: no congestion control anywhere): MV_CC_FIELDS words
- * per experiment, DCQCN (Zhu et al., SIGCOMM 2015; the Multiverse page,
- * section 5, names it among the congestion-control algorithms): [0] on (0
- * or 1), [1] kmin and [2] kmax (switch marking thresholds, arrived packets
+ * per experiment.  [0] selects none (0), DCQCN (1) or DCTCP (2); the
+ * Multiverse page, section 5, names both among its congestion-control
+ * algorithms.  DCTCP (Alizadeh et al., SIGCOMM 2010): [1] = [2] the marking
+ * threshold (arrived packets in the ingress queue a packet leaves), [4] gain
+ * shift (1..16), [13] initial window w0 (packets, >= 1), [14] largest window
+ * (w0..65535); receivers acknowledge every packet, an overflowing
+ * acknowledgement ring is MV_EXP_OVERFLOW.  DCQCN (Zhu et al., SIGCOMM
+ * 2015): [1] kmin and [2] kmax (switch marking thresholds, arrived packets
  * in the ingress queue a packet leaves), [3] pmax (marking probability at
  * kmax, units of 2^-16, <= 65536), [4] gain shift (g = 2^-shift, 1..16),
  * [5] N (ticks between a flow's notifications, >= 1), [6] K (alpha timer,
