@@ -182,8 +182,9 @@ int plan(const mv_batch_desc *d, Layout &L)
         R.nn = d->work_nnodes[w];
         R.ncoll = d->work_ncolls[w];
         R.nmemb = d->work_nmembers[w];
-        // a packet carries its sender's node in 25 bits, kCnpNode reserved
-        if (R.nn >= kCnpNode) return MV_EINVAL;
+        // a packet carries its sender's node in 25 bits, the top 256 values
+        // reserved for control packets
+        if (R.nn >= kCtlNode) return MV_EINVAL;
         R.rank_off = (u32)L.nranks;
         R.node_off = (u32)L.nnodes;
         R.edge_off = (u32)L.nedges;

@@ -93,7 +93,7 @@ struct LaneCC {
 // A rank's congestion-control state at the receiving side: DCQCN's last
 // notification per flow (direct-mapped by key mod 64: key | 1 << 31, tick),
 // and the ring of control packets waiting to be sent (sender rank | its
-// lane << 16 | packets acknowledged << 22 | of them marked << 26, key):
+// lane << 16 | packets acknowledged << 22, key | of them marked << 24):
 // DCQCN notifications (at most kCnpRing of them) or DCTCP acknowledgements.
 constexpr u32 kNpTab = 64, kCnpRing = 16, kCtlRing = 64;
 struct RankCC {
@@ -205,8 +205,11 @@ struct Params {
 //   x ready tick | y dst host (16 b) + accumulated (delta+1) over hops (16 b)
 //   z sender node (25 b) + sender lane (6 b) + congestion mark (1 b)
 //   w connection key (24 b) + last flag (1 b) + receive slot (7 b)
-// A DCQCN notification carries node kCnpNode and the lane it is for.
-constexpr u32 kCnpNode = 0x1FFFFFFu;
+// A control packet (a DCQCN notification, a DCTCP acknowledgement) carries
+// node kCtlNode + the packets it acknowledges (0 for a notification), the
+// lane it is for, and in w the flow key and the marked packets it
+// acknowledges (bits 24..31).
+constexpr u32 kCtlNode = 0x1FFFF00u;
 __host__ __device__ inline u32 pk_dst(uint4 p) { return p.y & 0xFFFFu; }
 __host__ __device__ inline u32 pk_node(uint4 p) { return p.z & 0x1FFFFFFu; }
 __host__ __device__ inline u32 pk_lane(uint4 p) { return (p.z >> 25) & 63u; }

@@ -767,7 +767,7 @@ __device__ __forceinline__ u32 switch_tick(const XV &Vs, Acc &acc, u32 s, u32 t,
         unsigned long long hi = st.y < 64 ? (M & (~0ull << st.y)) : 0ull;
         u32 i = (u32)__ffsll((long long)(hi ? hi : M)) - 1;
         uint4 pk = sm->pkt[i];
-        if (ccr && !pk_ecn(pk) && pk_node(pk) != kCnpNode) {
+        if (ccr && !pk_ecn(pk) && pk_node(pk) < kCtlNode) {
             // DCQCN marking by the ingress queue the packet leaves
             const u64 iw = ld_vol64(&V.q_push[p0 + i]);
             const u32 itl = (u32)iw - ((u32)(iw >> 32) == t ? 1u : 0u);
@@ -1550,8 +1550,8 @@ __device__ __forceinline__ void inject(RV &v, uint4 hr, u64 pw, u32 tail)
         uint4 pk;
         pk.x = t + hs + hd;
         pk.y = (c.x & 0xFFFFu) | ((hd + 1) << 16);
-        pk.z = kCnpNode | (((c.x >> 16) & 63u) << 25);
-        pk.w = c.y | (((c.x >> 22) & 15u) << 24) | (((c.x >> 26) & 15u) << 28);
+        pk.z = (kCtlNode + (c.x >> 22)) | (((c.x >> 16) & 63u) << 25);
+        pk.w = c.y;
         V.slots[(u64)qp * X.cap + slot_ix(tail, X.cap)] = pk;
         st_vol64(&V.q_push[qp], ((u64)t << 32) | (u32)(tail + 1));
         v.C.busy = t + hs;
@@ -1707,10 +1707,10 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     v.changed = true;
     if (head + 1 != tail) v.nxt = min(v.nxt, t + 1);
     const u32 snd = pk_node(pk);
-    if (RV::kCC && snd == kCnpNode) {
+    if (RV::kCC && snd >= kCtlNode) {
         const u32 l = pk_lane(pk);
         if (P.ccrec[X.cc - 1].mode == kDctcp) {
-            dctcp_ack(v, l, (pk.w >> 24) & 15u, pk.w >> 28);
+            dctcp_ack(v, l, snd - kCtlNode, pk.w >> 24);
             v.C.blocked = 0;                   // its window may have room again:
             v.nxt = min(v.nxt, t + 1);         // the lanes look next tick
             return;
@@ -1730,25 +1730,29 @@ __device__ __forceinline__ void receive(RV &v, u32 ql, u32 head, u32 tail, uint4
     }
     v.n_del++;
     if (RV::kCC && X.cc && P.ccrec[X.cc - 1].mode == kDctcp) {
-        // DCTCP: every data packet is acknowledged with its mark; an
-        // acknowledgement still waiting for the same lane takes it over (up
-        // to 15); a full ring is a table overflow
+        // DCTCP: every data packet is acknowledged with its mark; the
+        // newest acknowledgement still waiting for the same sender lane takes
+        // it over (up to 255), else a new one joins the ring; a full ring is
+        // a table overflow
         RankCC *rcc = P.rcc + X.rcc_off + v.r;
         const u32 id = P.node_rank[W_(v).node_off + snd] | (pk_lane(pk) << 16);
         const u32 mk = pk_ecn(pk);
         bool merged = false;
-        if (rcc->tail != rcc->head) {
-            uint2 &q = rcc->cq[(rcc->tail - 1) % kCtlRing];
-            if ((q.x & 0x3FFFFFu) == id && ((q.x >> 22) & 15u) < 15u) {
-                q.x += (1u << 22) + (mk << 26);
+        for (u32 i = rcc->tail; i != rcc->head;) {      // at most kCtlRing entries
+            uint2 &q = rcc->cq[--i % kCtlRing];
+            if ((q.x & 0x3FFFFFu) != id) continue;
+            if ((q.x >> 22) < 255u) {
+                q.x += 1u << 22;
+                q.y += mk << 24;
                 merged = true;
             }
+            break;
         }
         if (!merged) {
             if (rcc->tail - rcc->head >= kCtlRing) {
                 v.fail_rx = true;
             } else {
-                rcc->cq[rcc->tail % kCtlRing] = make_uint2(id | (1u << 22) | (mk << 26), pk_key(pk));
+                rcc->cq[rcc->tail % kCtlRing] = make_uint2(id | (1u << 22), pk_key(pk) | (mk << 24));
                 rcc->tail++;
             }
         }

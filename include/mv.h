@@ -129,7 +129,7 @@ extern "C" {
  * R_HAI, [12] R_min (units of 2^-20 of the line rate, <= 2^20; R_min >= 1),
  * [13..15] zero.  A notification is a packet from the receiver's NIC to
  * the sender's.  Congestion control with exp_voq = 1 is refused (MV_EINVAL).
- * A workload holds fewer than 2^25 - 1 nodes.
+ * A workload holds fewer than 2^25 - 256 nodes.
  */
 #define MV_CC_FIELDS 16
 typedef struct mv_batch_desc {

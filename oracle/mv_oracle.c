@@ -1145,16 +1145,19 @@ static void receive(sim *s, uint32_t r, uint32_t t)
     s->pkts_delivered++;
     ev(s, EV_DELIVER, r, p.sender);
     if (s->cc[CC_ON] == CC_DCTCP) {
-        /* every data packet is acknowledged; an acknowledgement still
-         * waiting for the same lane takes it over (up to 15 packets) */
+        /* every data packet is acknowledged: the newest acknowledgement
+         * still waiting for the same sender lane takes it over (up to 255
+         * packets), else a new one joins the ring */
         uint32_t sr = s->node_rank[p.sender];
-        if (n->cq_tail != n->cq_head) {
-            uint32_t k = (n->cq_tail - 1) % NCNPQ;
-            if (n->cq_dst[k] == sr && n->cq_lane[k] == p.lane && n->cq_n[k] < 15) {
+        for (uint32_t i = n->cq_tail; i != n->cq_head;) {
+            uint32_t k = --i % NCNPQ;
+            if (n->cq_dst[k] != sr || n->cq_lane[k] != p.lane) continue;
+            if (n->cq_n[k] < 255) {
                 n->cq_n[k]++;
                 n->cq_m[k] += p.ecn;
                 goto acked;
             }
+            break;
         }
         if (n->cq_tail - n->cq_head >= NCNPQ) {
             fail(s, ST_OVERFLOW);                     /* the acknowledgement ring is full */
@@ -1370,7 +1373,7 @@ static int validate(const orc_batch *b, const offs *o)
     }
     for (uint32_t w = 0; w < b->n_works; w++) {
         uint32_t nr = b->work_nranks[w], nn = b->work_nnodes[w], nco = b->work_ncolls[w];
-        if (nn >= (1u << 25) - 1) return -2;  /* a packet names its sender's node in 25 bits */
+        if (nn >= (1u << 25) - 256) return -2;  /* a packet names its sender's node in 25 bits */
         const uint32_t *cnt = b->rank_nnodes + o->rank[w];
         const uint32_t *kind = b->node_kind + o->node[w], *arg = b->node_arg + o->node[w];
         const uint32_t *nsucc = b->node_nsucc + o->node[w], *succ = b->succ + o->edge[w];

@@ -39,8 +39,11 @@ UNSET = 0xFFFFFFFF
 # samples cover both algorithms x NC {1, 16} x chunk {64K, 1M}, plus two
 # middle points, each through its whole iteration (data-parallel phase
 # included).  Config 5: two whole iterations on two different fabrics.
+# "config3-dcqcn" / "config3-dctcp": config-3 experiments with the
+# generators' DCQCN or DCTCP settings.
 # (batch, experiment index, tick limit or None), longest first.
 ENTRIES = [
+    ("config3-dctcp", 254, None), ("config3-dcqcn", 0, None),
     ("config5", 0, None), ("config5", 13, None),
     ("config3", 0, None), ("config3", 42, None), ("config3", 203, None), ("config3", 241, None),
     ("config3", 254, None), ("config3", 295, None), ("config3", 456, None),
@@ -50,13 +53,25 @@ ENTRIES = [
 SCALARS = ["status", "end_tick", "now", "pkts_injected", "pkt_hops", "pkts_delivered",
            "msgs_delivered", "digest", "rec_count"]
 # message records kept per experiment (more than any sampled experiment delivers)
-REC_CAP = {"config3": 1 << 26, "config4": 1 << 20, "config5": 1 << 27}
+REC_CAP = {"config3": 1 << 26, "config4": 1 << 20, "config5": 1 << 27,
+           "config3-dcqcn": 1 << 26, "config3-dctcp": 1 << 26}
+
+
+def with_cc(name: str, b):
+    """The batch's experiments with the congestion control its name asks for."""
+    from experiment_network_simulation_gb300 import inputs as I
+    for e in b.experiments:
+        if name.endswith("-dcqcn"):
+            e.cc = I.dcqcn(e.tick_ps, e.pkt)
+        elif name.endswith("-dctcp"):
+            e.cc = I.DCTCP()
+    return b
 
 
 def one_batch(name: str, idx: int, rec_cap: int = 0):
     from experiment_network_simulation_gb300 import inputs as I
-    if name == "config3":
-        b = I.config3().subset([idx])
+    if name.startswith("config3"):
+        b = with_cc(name, I.config3().subset([idx]))
     elif name == "config4":
         b = I.config4(n_exp=idx + 1).subset([idx])
     elif name == "config5":

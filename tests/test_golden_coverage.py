@@ -32,3 +32,20 @@ def test_every_sample_kept_all_its_records():
     for e in ENTRIES:
         assert e["rec_count"] == e["msgs_delivered"] and "records_sha256" in e
         assert e["violations"] == 0
+
+
+def test_congestion_controlled_samples_run_whole_iterations():
+    """A config-3 experiment under DCQCN and one under DCTCP (the generators'
+    settings) are stored through their whole iterations, data-parallel
+    all-reduces included, and differ from the same experiments without
+    congestion control where those are stored."""
+    cc = [e for e in ENTRIES if e["batch"] in ("config3-dcqcn", "config3-dctcp")]
+    assert {e["batch"] for e in cc} == {"config3-dcqcn", "config3-dctcp"}
+    plain = {e["index"]: e for e in ENTRIES if e["batch"] == "config3"}
+    for e in cc:
+        assert e["limit"] is None and e["status"] == 0, (e["batch"], e["index"])
+        assert e["net_allreduce_started"] == e["net_allreduce_members"] > 0
+        assert e["net_allreduce_ended"] == e["net_allreduce_members"]
+        if e["index"] in plain:
+            assert e["digest"] != plain[e["index"]]["digest"] or \
+                e["pkt_hops"] != plain[e["index"]]["pkt_hops"]

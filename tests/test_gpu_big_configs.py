@@ -4,8 +4,8 @@ tests/golden/big_parity.json (written by tests/golden/make_big_parity.py,
 which runs only the seeded generators and the oracle) holds, for sampled
 experiments of the GPT-13B 1F1B batch (config 3: ring and tree, NC 1 and 16,
 chunks of 64 KiB and 1 MiB, and two middle points), the MoE dispatch/combine
-batch (config 4: one per fabric) and the topology-search batch (config 5:
-two fabrics), the oracle's per-experiment results and SHA-256 digests of its
+batch (config 4: one per fabric), the topology-search batch (config 5:
+two fabrics) and config-3 experiments under DCQCN and under DCTCP, the oracle's per-experiment results and SHA-256 digests of its
 per-node start and end ticks, its per-collective first start and last end,
 and its per-message completion records sorted by (tick, sender, key), each
 run through its whole iteration (the data-parallel gradient all-reduces
@@ -42,8 +42,8 @@ for e in ENTRIES:
 
 def group_batch(name, ents):
     idxs = [e["index"] for e in ents]
-    if name == "config3":
-        b = I.config3().subset(idxs)
+    if name.startswith("config3"):
+        b = G.with_cc(name, I.config3().subset(idxs))
     elif name == "config4":
         b = I.config4(n_exp=max(idxs) + 1).subset(idxs)
     else:
