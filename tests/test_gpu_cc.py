@@ -98,3 +98,29 @@ def test_dctcp_gpt_small_and_config1_bit_exact():
         want = O.run(p)
         assert (want["status"] == O.ST_DONE).all()
         assert_same(mv.simulate(p), want)
+
+
+@pytest.mark.parametrize("which", ["dcqcn", "dctcp"])
+def test_congestion_control_resumes_and_repeats(which):
+    """The congestion-control state (rates, windows, notification rings)
+    lives in the workspace: a run in pieces of 50 ticks, stopped at tick
+    boundaries, equals one run, which equals the oracle; a second run
+    repeats it bit for bit."""
+    if which == "dcqcn":
+        b = _random_batch(21, 40, cc(kmin=1, kmax=4, pmax=30000, n=5, k=7, t=11, b=6, f=2,
+                                     rai=3000, rhai=20000, rmin=5000))
+    else:
+        b = _random_batch(21, 40, tcp(kmark=2, gshift=3, w0=2, wmax=12))
+    p = b.pack()
+    once = mv.simulate(p)
+    assert_same(once, O.run(p))
+    sim = mv.Simulator(p)
+    calls = 0
+    while sim.run(max_ticks=50) == mv.MV_INCOMPLETE:
+        calls += 1
+        assert calls < 100_000
+    got = sim.results()
+    sim.close()
+    assert calls > 3
+    assert_same(got, once)
+    assert_same(mv.simulate(p), once)
