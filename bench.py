@@ -85,7 +85,17 @@ WINDOWS = {"config3": (2_600_000, 4_000), "config5": (300_000, 2_000), "gpt_smal
 # current kernel, keyed by workload and window; each entry names the kernel
 # source digest it was taken with, and is dropped (traffic: null) once the
 # kernel source differs.
-TRAFFIC: dict = {}
+TRAFFIC: dict = {
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one window launch of
+    # config 3's first 152 experiments (72,359,266,048 + 41,792,947,712 B for
+    # 802,918,438 packet-hops); the 500-experiment step is too large to
+    # capture, so its entry is that figure scaled by packet-hops
+    # (2,344,660,048 a step): traffic grows with the hops.
+    ("config3", (2_600_000, 4_000), 152): {"bytes_per_launch": 114_152_213_760,
+                                           "kernel_digest": "2408b8ec10073668"},
+    ("config3", (2_600_000, 4_000), 500): {"bytes_per_launch": 333_344_113_582,
+                                           "kernel_digest": "2408b8ec10073668"},
+}
 KERNEL_SOURCES = ["experiment_network_simulation_gb300/csrc/mv_kernel.cu",
                   "experiment_network_simulation_gb300/csrc/mv_device.cuh"]
 
