@@ -36,6 +36,10 @@ def pin_batch():
     ex.append(I.Experiment(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 300 * 4096),
                            cc=cc(kmin=0, kmax=0, n=50, k=30), chunk=1 << 30, tick_ps=1000,
                            rec_cap=512))
+    ex.append(I.Experiment(I.single_switch(2, 1, 0), I.lone_message(2, 0, 1, 300 * 4096),
+                           cc=cc(kmin=0, kmax=0, n=25, k=400, t=7, b=3, f=2, rai=1 << 9,
+                                 rhai=1 << 10, rmin=1 << 12, gshift=4),
+                           chunk=1 << 30, tick_ps=1000, rec_cap=512))
     return I.Batch(ex, "dcqcn-pins")
 
 

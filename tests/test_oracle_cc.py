@@ -178,6 +178,81 @@ def test_alpha_decay_between_two_cuts():
     assert g2 == dl[dl >= g1 + 50][0]
 
 
+# ---------------------------------------------------------------- every rule at once
+def test_reaction_point_replays_the_published_rules():
+    """A lone flow, every forwarded packet marked, notifications at most one
+    per 25 ticks (so the rate never recovers fully and the target stays below
+    the line rate), a short rate timer (T = 7), a byte counter of 3 packets,
+    F = 2, gain 1/16 and small increase steps, so that fast recovery,
+    additive and hyper increase (with unequal event counts) and the byte
+    counter all occur; alpha decays over K = 400 ticks.  Replaying the
+    published rules (timer events in time order, alpha first on a tie; each
+    packet sent, then any notification taken in that tick; RC <- ceil((RT +
+    RC) / 2) after each increase) from the lane's join over the ticks the
+    oracle logged predicts every cut value and every gap between packets."""
+    sig, gs, N, K, T, B, F = 1, 4, 25, 400, 7, 3, 2
+    rai, rhai, rmin = 1 << 9, 1 << 10, 1 << 12
+    t = I.single_switch(2, sig, 0)
+    r, ev = traced(t, I.lone_message(2, 0, 1, 300 * 4096),
+                   cc=cc(kmin=0, kmax=0, n=N, k=K, t=T, b=B, f=F, rai=rai, rhai=rhai, rmin=rmin,
+                         gshift=gs))
+    t0 = int(ev[(ev["kind"] == O.EV_START) & (ev["b"] == 0)]["tick"][0])
+    cuts = {int(x["tick"]): int(x["b"]) for x in of_kind(ev, O.EV_CUT, 0)}
+    sends = [int(x) for x in of_kind(ev, O.EV_INJECT, 0)["tick"]]
+    assert len(cuts) >= 5
+    st = dict(rc=LINE, rt=LINE, alpha=LINE, abase=t0, rbase=t0, tc=0, bc=0, sent=0)
+    modes, hyper_below_line = set(), []
+
+    def increase():
+        mx, mn = max(st["tc"], st["bc"]), min(st["tc"], st["bc"])
+        if mx < F:
+            modes.add("fast recovery")
+        elif mn > F:
+            modes.add("hyper")
+            if st["rt"] < LINE and st["tc"] != st["bc"]:
+                hyper_below_line.append(1)
+            st["rt"] = min(LINE, st["rt"] + (mn - F) * rhai)
+        else:
+            modes.add("additive")
+            st["rt"] = min(LINE, st["rt"] + rai)
+        st["rc"] = (st["rt"] + st["rc"] + 1) // 2
+
+    def timers(now):
+        while True:
+            ta, tr = st["abase"] + K, st["rbase"] + T
+            if ta > now and tr > now:
+                return
+            if ta <= tr:
+                st["alpha"] -= st["alpha"] >> gs
+                st["abase"] = ta
+            else:
+                st["rbase"] = tr
+                st["tc"] += 1
+                increase()
+
+    gaps = {}
+    for now in sorted(set(sends) | set(cuts)):
+        timers(now)
+        if now in sends:
+            st["sent"] += 1
+            if st["sent"] >= B:
+                st["sent"] = 0
+                st["bc"] += 1
+                increase()
+            gaps[now] = -(-sig * LINE // st["rc"])
+        if now in cuts:
+            st["rt"] = st["rc"]
+            st["rc"] = max(rmin, st["rc"] - ((st["rc"] * st["alpha"]) >> 21))
+            st["alpha"] = min(LINE, st["alpha"] - (st["alpha"] >> gs) + (LINE >> gs))
+            st["abase"] = st["rbase"] = now
+            st["tc"] = st["bc"] = st["sent"] = 0
+            assert cuts[now] == st["rc"], now
+    for a, b in zip(sends[:-1], sends[1:]):
+        assert b - a == gaps[a], (a, b - a, gaps[a])
+    assert modes == {"fast recovery", "additive", "hyper"}
+    assert hyper_below_line                              # a hyper step that moved the target
+
+
 # ---------------------------------------------------------------- random traffic
 def test_random_congestion_controlled_traffic_keeps_invariants():
     """Seeded random collectives with aggressive settings (marking from two
