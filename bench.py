@@ -167,7 +167,7 @@ class OraclePool:
     command.  For a window, each process holds the start state of one
     sampled experiment (computed untimed) and times the window from a copy."""
 
-    def __init__(self, name: str, seed: int, exps: int, window, cores: int):
+    def __init__(self, name: str, seed: int, exps: int, window, cores: int, wait: bool = True):
         from oracle import oracle
 
         oracle.build()
@@ -184,9 +184,23 @@ class OraclePool:
         for _, conn in self.workers:
             assert conn.recv() == "ready"
         self.sample = []
+        self.pending = False
         if window:
+            # each worker runs its experiment to the window's start; with
+            # wait=False the caller does other work meanwhile (settle())
             self.sample = self.order[:len(self.workers)]
-            self._all([("prefix", e, window[0]) for e in self.sample])
+            for (_, conn), e in zip(self.workers, self.sample):
+                conn.send(("prefix", e, window[0]))
+            self.pending = True
+            if wait:
+                self.settle()
+
+    def settle(self):
+        """Wait for the start states of the sampled experiments."""
+        if self.pending:
+            for _, conn in self.workers[:len(self.sample)]:
+                conn.recv()
+            self.pending = False
 
     def _all(self, cmds):
         for (_, conn), cmd in zip(self.workers, cmds):
@@ -337,11 +351,14 @@ def run_reference(args, rank: int, world: int):
     }), flush=True)
 
 
-def cpu_leg(args, window):
-    """cpu_baseline of the GPU arm: the oracle on the same workload."""
+def cpu_leg(args, window, pool=None):
+    """cpu_baseline of the GPU arm: the oracle on the same workload (`pool`:
+    one started earlier, whose start states may still be on their way)."""
     cores = os.cpu_count() or 1
-    pool = OraclePool(args.workload, 0, args.exps, window, cores)
+    if pool is None:
+        pool = OraclePool(args.workload, 0, args.exps, window, cores)
     try:
+        pool.settle()
         if window:
             h, dt = pool.window_step()
             sample = (f"{len(pool.sample)} of {pool.n_exp} experiments (seeded permutation), "
@@ -357,9 +374,19 @@ def cpu_leg(args, window):
 
 
 def run_gpu(args, rank: int, world: int):
+    # the CPU baseline's processes start first (spawned, before any GPU
+    # call) and run their experiments to the window's start while the GPU
+    # does the same; the timed GPU steps wait until they are done
     import torch
 
     from experiment_network_simulation_gb300 import mv
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py: the GPU arm needs a CUDA device")
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = OraclePool(args.workload, 0, args.exps, window_of(args), os.cpu_count() or 1,
+                          wait=False)
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -400,6 +427,8 @@ def run_gpu(args, rank: int, world: int):
         rc = sim.run(max_ticks=budget, variant=args.variant, block_warps=args.block_warps)
         assert rc in ((mv.MV_OK, mv.MV_INCOMPLETE) if window else (mv.MV_OK,)), rc
 
+    if pool is not None:
+        pool.settle()                                 # the host cores are quiet from here on
     for _ in range(args.warmup):
         prefix()
         timed()
@@ -499,7 +528,7 @@ def run_gpu(args, rank: int, world: int):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_leg(args, window)
+        cpu = cpu_leg(args, window, pool)
 
     if rank == 0:
         cfg = config_of(args, window, int(exps_all))
