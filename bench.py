@@ -108,8 +108,28 @@ def kernel_digest() -> str:
 
 
 def make_batch(name: str, seed: int = 0, exps: int = 0):
-    b = WORKLOADS[name][0](seed)
-    return b.subset(range(min(exps, len(b)))) if exps else b
+    """The named workload; "+voq", "+dcqcn", "+dctcp" suffixes give every
+    experiment virtual output queues or that congestion control (the
+    generators' settings)."""
+    base, *mods = name.split("+")
+    b = WORKLOADS[base][0](seed)
+    b = b.subset(range(min(exps, len(b)))) if exps else b
+    for e in b.experiments:
+        for m in mods:
+            if m == "voq":
+                e.voq = 1
+            elif m == "dcqcn":
+                e.cc = I.dcqcn(e.tick_ps, e.pkt)
+            elif m == "dctcp":
+                e.cc = I.DCTCP()
+            else:
+                raise ValueError(f"unknown workload variant {m!r}")
+    return b
+
+
+def batch_name(args) -> str:
+    return args.workload + ("+voq" if args.voq else "") + \
+        ("" if args.cc == "none" else "+" + args.cc)
 
 
 def window_of(args):
@@ -297,6 +317,10 @@ def load_peaks():
 def config_of(args, window, n_exp):
     cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload][1],
            "experiments": n_exp}
+    if args.voq:
+        cfg["switch"] = "virtual output queues"
+    if args.cc != "none":
+        cfg["congestion_control"] = args.cc
     if window:
         cfg["window"] = {"start_tick": window[0], "ticks": window[1],
                          "note": "each step advances every experiment from start_tick to "
@@ -311,7 +335,7 @@ def run_reference(args, rank: int, world: int):
         return
     cores = os.cpu_count() or 1
     window = window_of(args)
-    pool = OraclePool(args.workload, 0, args.exps, window, cores)
+    pool = OraclePool(batch_name(args), 0, args.exps, window, cores)
     try:
         if window:
             for _ in range(args.warmup):
@@ -356,7 +380,7 @@ def cpu_leg(args, window, pool=None):
     one started earlier, whose start states may still be on their way)."""
     cores = os.cpu_count() or 1
     if pool is None:
-        pool = OraclePool(args.workload, 0, args.exps, window, cores)
+        pool = OraclePool(batch_name(args), 0, args.exps, window, cores)
     try:
         pool.settle()
         if window:
@@ -385,13 +409,13 @@ def run_gpu(args, rank: int, world: int):
         raise RuntimeError("bench.py: the GPU arm needs a CUDA device")
     pool = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        pool = OraclePool(args.workload, 0, args.exps, window_of(args), os.cpu_count() or 1,
+        pool = OraclePool(batch_name(args), 0, args.exps, window_of(args), os.cpu_count() or 1,
                           wait=False)
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     window = window_of(args)
-    batch = make_batch(args.workload, seed=rank, exps=args.exps)   # each rank: its own shard
+    batch = make_batch(batch_name(args), seed=rank, exps=args.exps)   # each rank: its own shard
     packed = batch.pack()
     stream = torch.cuda.Stream(dev)
     sim = mv.Simulator(packed, device=str(dev), stream=stream)
@@ -518,7 +542,7 @@ def run_gpu(args, rank: int, world: int):
     alg_bytes = BYTES_PER_HOP * hops_step + BYTES_PER_PKT * pkts_step
     achieved = alg_bytes / (km / 1000.0) / 1e9
     peak = peaks["hbm_gbs"] if peaks else 6800.0
-    key = (args.workload, tuple(window) if window else None, len(batch))
+    key = (batch_name(args), tuple(window) if window else None, len(batch))
     tr = TRAFFIC.get(key)
     traffic = tr["bytes_per_launch"] if tr and tr["kernel_digest"] == kernel_digest() else None
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -571,6 +595,9 @@ def main():
                     help="window length in ticks of each experiment's clock (0: whole runs)")
     ap.add_argument("--whole", action="store_true", help="time whole runs, no window")
     ap.add_argument("--variant", type=int, default=0, help="kernel build (0: automatic)")
+    ap.add_argument("--voq", action="store_true", help="switches with virtual output queues")
+    ap.add_argument("--cc", default="none", choices=["none", "dcqcn", "dctcp"],
+                    help="congestion control of every experiment")
     ap.add_argument("--block-warps", type=int, default=0, help="warps a block (0: automatic)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -84,3 +84,17 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     r = json.loads(lines[0])
     assert r["impl"] == "reference" and r["n_gpus"] == 2 and r["value"] > 0
+
+
+def test_reference_arm_with_switch_and_congestion_control_variants():
+    """--voq and --cc name their variant in the line's config and change the
+    workload (DCTCP's windows slow config 1's ring)."""
+    lines = {}
+    for extra in ([], ["--voq"], ["--cc", "dctcp"]):
+        p = _bench("--impl", "reference", "--workload", "config1", "--steps", "1", "--warmup", "3",
+                   *extra)
+        assert p.returncode == 0, p.stderr[-2000:]
+        lines[tuple(extra)] = json.loads([l for l in p.stdout.splitlines() if l.strip()][-1])
+    assert lines[("--voq",)]["config"]["switch"] == "virtual output queues"
+    assert lines[("--cc", "dctcp")]["config"]["congestion_control"] == "dctcp"
+    assert "switch" not in lines[()]["config"] and "congestion_control" not in lines[()]["config"]
